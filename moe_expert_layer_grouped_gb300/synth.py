@@ -1,0 +1,141 @@
+"""Seeded synthetic inputs for the MoE layer forward.
+
+This module is shared by the CUDA path's tests and benchmark and by the CPU
+oracle's tests. It holds none of the layer's arithmetic: it only draws
+tensors with torch's seeded generators and converts the expert weights to the
+FP8 e4m3 storage format the layer consumes (per-output-channel scale =
+row amax / 448, codes from torch's own e4m3fn cast), which is input
+preparation, not a step of the forward.
+
+Workloads (the shapes, value distributions and routing structure of a
+DeepSeek-V3-style and a Mixtral-style MoE layer):
+  tiny               T=8     H=128  I=64    E=8   G=1 TG=1 K=2 softmax rsf 1.0
+  dsv3_decode_t128   T=128   H=7168 I=2048  E=256 G=8 TG=4 K=8 sigmoid rsf 2.5
+                     bias ~N(0, 0.1)
+  dsv3_prefill_t8192 T=8192  same layer, bias 0
+  mixtral_t4096      T=4096  H=4096 I=14336 E=8   G=1 TG=1 K=2 softmax rsf 1.0
+  dsv3_skewed_t16384 T=16384 same layer as decode; bias +3.0 on the 26
+                     experts with e % 10 == 0, -10 on the 32 with e % 8 == 7,
+                     the rest ~N(0, 0.1)
+Hidden states and router logits ~N(0, 1); weights ~N(0, 0.02).
+"""
+from dataclasses import dataclass, replace
+from typing import Optional
+
+import torch
+
+SIGMOID = 0
+SOFTMAX = 1
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    T: int
+    H: int
+    I: int
+    E: int
+    num_groups: int
+    topk_group: int
+    top_k: int
+    scoring: int
+    renormalize: bool
+    rsf: float
+    bias: str  # "none" | "normal" | "zero" | "skewed"
+
+    @property
+    def M(self):
+        return self.T * self.top_k
+
+    def with_tokens(self, T):
+        return replace(self, T=T, name=f"{self.name}@T{T}")
+
+
+WORKLOADS = {
+    "tiny": Workload("tiny", 8, 128, 64, 8, 1, 1, 2, SOFTMAX, True, 1.0, "none"),
+    "dsv3_decode_t128": Workload("dsv3_decode_t128", 128, 7168, 2048, 256, 8, 4, 8,
+                                 SIGMOID, True, 2.5, "normal"),
+    "dsv3_prefill_t8192": Workload("dsv3_prefill_t8192", 8192, 7168, 2048, 256, 8, 4, 8,
+                                   SIGMOID, True, 2.5, "zero"),
+    "mixtral_t4096": Workload("mixtral_t4096", 4096, 4096, 14336, 8, 1, 1, 2, SOFTMAX,
+                              True, 1.0, "none"),
+    "dsv3_skewed_t16384": Workload("dsv3_skewed_t16384", 16384, 7168, 2048, 256, 8, 4, 8,
+                                   SIGMOID, True, 2.5, "skewed"),
+}
+
+# tensor ids: each tensor draws from its own generator stream
+_TID = {"x": 0, "logits": 1, "bias": 2, "w13": 3, "w2": 4}
+
+
+def _gen(seed: int, tensor: str, device) -> torch.Generator:
+    g = torch.Generator(device=device)
+    g.manual_seed((int(seed) * 1_000_003 + _TID[tensor] * 7919 + 17) & 0x7FFF_FFFF_FFFF_FFFF)
+    return g
+
+
+def normal(shape, std, seed, tensor, device="cpu", dtype=torch.float32):
+    g = _gen(seed, tensor, device)
+    return torch.randn(shape, generator=g, device=device, dtype=torch.float32).mul_(std).to(dtype)
+
+
+def quantize_weight_rows(w: torch.Tensor):
+    """fp32 weights [..., rows, cols] -> (e4m3 codes as uint8, fp32 scale per row)."""
+    amax = w.abs().amax(dim=-1)
+    scale = torch.clamp(amax, min=1e-12) / 448.0
+    q = (w / scale.unsqueeze(-1)).clamp_(-448.0, 448.0).to(torch.float8_e4m3fn)
+    return q.view(torch.uint8), scale.to(torch.float32)
+
+
+def expert_weights(E, rows, cols, seed, tensor, device="cpu", std=0.02):
+    """[E, rows, cols] FP8 codes + [E, rows] scales, drawn expert by expert."""
+    q = torch.empty((E, rows, cols), dtype=torch.uint8, device=device)
+    s = torch.empty((E, rows), dtype=torch.float32, device=device)
+    g = _gen(seed, tensor, device)
+    for e in range(E):
+        w = torch.randn((rows, cols), generator=g, device=device, dtype=torch.float32).mul_(std)
+        q[e], s[e] = quantize_weight_rows(w)
+    return q, s
+
+
+def router_bias(wl: Workload, seed, device="cpu") -> Optional[torch.Tensor]:
+    if wl.bias == "none":
+        return None
+    if wl.bias == "zero":
+        return torch.zeros(wl.E, dtype=torch.float32, device=device)
+    b = normal((wl.E,), 0.1, seed, "bias", device)
+    if wl.bias == "skewed":
+        e = torch.arange(wl.E, device=device)
+        b = torch.where(e % 10 == 0, torch.full_like(b, 3.0), b)
+        b = torch.where(e % 8 == 7, torch.full_like(b, -10.0), b)
+    return b
+
+
+def make_inputs(wl: Workload, seed=0, device="cpu", weights=True):
+    """All inputs of one forward, on `device`.
+
+    x: bf16 [T,H]; logits: f32 [T,E]; bias: f32 [E] or None;
+    w13: u8 [E,2I,H] (rows 0..I-1 gate, I..2I-1 up) with s13 f32 [E,2I];
+    w2: u8 [E,H,I] with s2 f32 [E,H].
+    """
+    d = dict(
+        x=normal((wl.T, wl.H), 1.0, seed, "x", device, torch.bfloat16),
+        logits=normal((wl.T, wl.E), 1.0, seed, "logits", device),
+        bias=router_bias(wl, seed, device),
+    )
+    if weights:
+        d["w13"], d["s13"] = expert_weights(wl.E, 2 * wl.I, wl.H, seed, "w13", device)
+        d["w2"], d["s2"] = expert_weights(wl.E, wl.H, wl.I, seed, "w2", device)
+    return d
+
+
+def to_numpy_inputs(d):
+    """torch inputs -> numpy arrays in the oracle's formats (bf16 as uint16)."""
+    out = {}
+    for k, v in d.items():
+        if v is None:
+            out[k] = None
+        elif v.dtype == torch.bfloat16:
+            out[k] = v.detach().cpu().view(torch.int16).numpy().view("uint16")
+        else:
+            out[k] = v.detach().cpu().numpy()
+    return out

@@ -1,0 +1,251 @@
+"""numpy front end of the CPU oracle (oracle.c).
+
+TEST INFRASTRUCTURE: only the tests, ``__graft_entry__.smoke()`` and the CPU
+baseline leg of ``bench.py`` import this module. The product library never
+does.
+
+Every function takes and returns numpy arrays; bf16 tensors travel as their
+uint16 bit patterns and FP8 e4m3 tensors as uint8 codes.
+"""
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+SIGMOID = 0
+SOFTMAX = 1
+
+_lib = None
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        L = ctypes.CDLL(path)
+        P = ctypes.c_void_p
+        i32, i64, f32 = ctypes.c_int, ctypes.c_int64, ctypes.c_float
+        sig = {
+            "oracle_set_threads": (None, [i32]),
+            "oracle_get_threads": (i32, []),
+            "oracle_exp32": (f32, [f32]),
+            "oracle_exp32_n": (None, [P, P, i64]),
+            "oracle_sigmoid32": (f32, [f32]),
+            "oracle_sigmoid32_n": (None, [P, P, i64]),
+            "oracle_e4m3_encode": (ctypes.c_uint8, [f32]),
+            "oracle_e4m3_encode_n": (None, [P, P, i64]),
+            "oracle_e4m3_decode": (ctypes.c_double, [ctypes.c_uint8]),
+            "oracle_bf16_round_n": (None, [P, P, i64]),
+            "oracle_gate": (i32, [P, P, i32, i32, i32, i32, i32, i32, i32, f32, P, P]),
+            "oracle_route": (None, [P, i32, i32, i32, P, P]),
+            "oracle_row_quant": (None, [P, i64, i32, P, P]),
+            "oracle_permute_quant": (None, [P, P, i32, i32, i32, i32, P, P, P, P]),
+            "oracle_grouped_gemm": (None, [P, P, P, P, P, i32, i32, i32, i32, P]),
+            "oracle_silu_mul": (None, [P, i64, i32, P]),
+            "oracle_unpermute_sum": (None, [P, P, P, i32, i32, i32, P]),
+            "oracle_forward_tokens": (i32, [P, P, P, P, P, P, P, i32, i32, i32, i32, i32,
+                                            i32, i32, i32, i32, f32, P, i32, P, P, P]),
+        }
+        for name, (res, args) in sig.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _p(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def set_threads(n):
+    lib().oracle_set_threads(int(n))
+
+
+def get_threads():
+    return lib().oracle_get_threads()
+
+
+def exp32(x):
+    x = _c(x, np.float32)
+    y = np.empty_like(x)
+    lib().oracle_exp32_n(_p(x), _p(y), x.size)
+    return y
+
+
+def sigmoid32(x):
+    x = _c(x, np.float32)
+    y = np.empty_like(x)
+    lib().oracle_sigmoid32_n(_p(x), _p(y), x.size)
+    return y
+
+
+def e4m3_encode(x):
+    x = _c(x, np.float32)
+    q = np.empty(x.shape, np.uint8)
+    lib().oracle_e4m3_encode_n(_p(x), _p(q), x.size)
+    return q
+
+
+def e4m3_decode_table():
+    L = lib()
+    return np.array([L.oracle_e4m3_decode(i) for i in range(256)], np.float64)
+
+
+def e4m3_decode(q):
+    return e4m3_decode_table()[np.asarray(q, np.uint8)]
+
+
+def bf16_round(v):
+    """fp64 values -> bf16 bit patterns (uint16), round to nearest even."""
+    v = _c(v, np.float64)
+    out = np.empty(v.shape, np.uint16)
+    lib().oracle_bf16_round_n(_p(v), _p(out), v.size)
+    return out
+
+
+def bf16_to_f64(bits):
+    b = np.asarray(bits, np.uint16).astype(np.uint32) << 16
+    return b.view(np.float32).astype(np.float64)
+
+
+def gate(logits, bias, num_groups, topk_group, top_k, scoring=SIGMOID,
+         renormalize=True, routed_scaling_factor=1.0):
+    logits = _c(logits, np.float32)
+    T, E = logits.shape
+    b = None if bias is None else _c(bias, np.float32)
+    ids = np.empty((T, top_k), np.int32)
+    w = np.empty((T, top_k), np.float32)
+    rc = lib().oracle_gate(_p(logits), _p(b), T, E, num_groups, topk_group, top_k,
+                           scoring, int(bool(renormalize)), float(routed_scaling_factor),
+                           _p(ids), _p(w))
+    if rc != 0:
+        raise ValueError(f"oracle_gate: status {rc}")
+    return ids, w
+
+
+def route(topk_ids, E):
+    ids = _c(topk_ids, np.int32)
+    T, K = ids.shape
+    offsets = np.empty(E + 1, np.int32)
+    src2dst = np.empty(T * K, np.int32)
+    lib().oracle_route(_p(ids), T, E, K, _p(offsets), _p(src2dst))
+    return offsets, src2dst
+
+
+def row_quant(x_bits):
+    x = _c(x_bits, np.uint16)
+    R, C = x.shape
+    q = np.empty((R, C), np.uint8)
+    s = np.empty(R, np.float32)
+    lib().oracle_row_quant(_p(x), R, C, _p(q), _p(s))
+    return q, s
+
+
+def permute_quant(x_bits, topk_ids, E):
+    x = _c(x_bits, np.uint16)
+    ids = _c(topk_ids, np.int32)
+    T, H = x.shape
+    K = ids.shape[1]
+    M = T * K
+    a_q = np.empty((M, H), np.uint8)
+    sa = np.empty(M, np.float32)
+    src2dst = np.empty(M, np.int32)
+    offsets = np.empty(E + 1, np.int32)
+    lib().oracle_permute_quant(_p(x), _p(ids), T, H, E, K, _p(a_q), _p(sa), _p(src2dst),
+                               _p(offsets))
+    return a_q, sa, src2dst, offsets
+
+
+def grouped_gemm(A, scale_a, B, scale_b, offsets):
+    A = _c(A, np.uint8)
+    B = _c(B, np.uint8)
+    sa = _c(scale_a, np.float32)
+    sb = _c(scale_b, np.float32)
+    off = _c(offsets, np.int32)
+    M, Kd = A.shape
+    E, N, Kd2 = B.shape
+    assert Kd == Kd2 and off.size == E + 1
+    C = np.empty((M, N), np.float64)
+    lib().oracle_grouped_gemm(_p(A), _p(sa), _p(B), _p(sb), _p(off), M, N, Kd, E, _p(C))
+    return C
+
+
+def silu_mul(C):
+    C = _c(C, np.float64)
+    M, N2 = C.shape
+    I = N2 // 2
+    h = np.empty((M, I), np.float64)
+    lib().oracle_silu_mul(_p(C), M, I, _p(h))
+    return h
+
+
+def act_quant(h_bits):
+    """Per-row requantisation of bf16 h (bit patterns) -> (codes, scales)."""
+    return row_quant(h_bits)
+
+
+def unpermute_sum(down, src2dst, topk_w):
+    down = _c(down, np.float64)
+    s2d = _c(src2dst, np.int32)
+    w = _c(topk_w, np.float32)
+    T, K = w.shape
+    H = down.shape[1]
+    out = np.empty((T, H), np.float64)
+    lib().oracle_unpermute_sum(_p(down), _p(s2d), _p(w), T, K, H, _p(out))
+    return out
+
+
+def forward_tokens(x_bits, logits, bias, w13, s13, w2, s2, num_groups, topk_group,
+                   top_k, scoring, renormalize, routed_scaling_factor, tokens=None):
+    """Whole layer for the listed tokens (all tokens when None).
+
+    Returns (out [n,H] fp64, ids [n,K], w [n,K])."""
+    x = _c(x_bits, np.uint16)
+    logits = _c(logits, np.float32)
+    T, H = x.shape
+    E = logits.shape[1]
+    I = w2.shape[2]
+    assert w13.shape == (E, 2 * I, H) and w2.shape == (E, H, I)
+    b = None if bias is None else _c(bias, np.float32)
+    tok = np.arange(T, dtype=np.int64) if tokens is None else _c(tokens, np.int64)
+    n = tok.size
+    out = np.empty((n, H), np.float64)
+    ids = np.empty((n, top_k), np.int32)
+    w = np.empty((n, top_k), np.float32)
+    w13 = _c(w13, np.uint8)
+    w2 = _c(w2, np.uint8)
+    s13 = _c(s13, np.float32)
+    s2 = _c(s2, np.float32)
+    rc = lib().oracle_forward_tokens(_p(x), _p(logits), _p(b), _p(w13), _p(s13), _p(w2),
+                                     _p(s2), T, H, I, E, num_groups, topk_group, top_k,
+                                     scoring, int(bool(renormalize)),
+                                     float(routed_scaling_factor), _p(tok), n, _p(out),
+                                     _p(ids), _p(w))
+    if rc != 0:
+        raise ValueError(f"oracle_forward_tokens: status {rc}")
+    return out, ids, w
+
+
+def forward_steps(x_bits, logits, bias, w13, s13, w2, s2, num_groups, topk_group, top_k,
+                  scoring, renormalize, routed_scaling_factor):
+    """The layer step by step over all tokens, returning every intermediate
+    (small configurations only: materialises [M, 2I] in fp64)."""
+    E = logits.shape[1]
+    ids, w = gate(logits, bias, num_groups, topk_group, top_k, scoring, renormalize,
+                  routed_scaling_factor)
+    a_q, sa, src2dst, offsets = permute_quant(x_bits, ids, E)
+    C13 = grouped_gemm(a_q, sa, w13, s13, offsets)
+    h = silu_mul(C13)
+    h_bits = bf16_round(h)
+    q2, sa2 = act_quant(h_bits)
+    down = grouped_gemm(q2, sa2, w2, s2, offsets)
+    out = unpermute_sum(down, src2dst, w)
+    return dict(ids=ids, w=w, a_q=a_q, scale_a=sa, src2dst=src2dst, offsets=offsets,
+                c13=C13, h=h, h_bits=h_bits, q2=q2, scale_a2=sa2, down=down, out=out)

@@ -1,0 +1,115 @@
+/*
+ * Oracle for the grouped-expert MoE layer forward: plain, slow, CPU-only C.
+ *
+ * TEST INFRASTRUCTURE. Only the test suite, the smoke check and the CPU
+ * baseline leg of the benchmark may load this library. The product path (the
+ * CUDA library) never links, loads or calls it, and shares no code with it.
+ *
+ * What it computes follows three sglang pull-request pages:
+ *   - "Fix one bug in the grouped-gemm triton kernel" (sglang #6772),
+ *     Highlights: scale_a is indexed by row (m_range_start + offs_am), not by
+ *     the expert id, when block quantisation is off.
+ *   - "Support token-level quantization for EP MoE" (sglang #6782), Summary of
+ *     Changes / Changelog: per-token dynamic FP8 activation scales, loaded per
+ *     token in the pre-reorder kernel and in the grouped GEMM, reordered via
+ *     src2dst, and the activation output requantised per token.
+ *   - "[1/2] sgl-kernel: Fuse routed scaling factor into select_experts"
+ *     (sglang #8364), Motivation / Highlights: routed_scaling_factor is
+ *     multiplied into the renormalised top-k weights inside the gate.
+ * Steps the pages leave open are fixed by the readings listed in each
+ * function's comment.
+ *
+ * Precision: fp64 everywhere the method does not fix a precision, except
+ * where floating point decides an integer (top-k ids, FP8 codes): those
+ * decisions are taken in fp32, the precision of the kernel, with IEEE
+ * single-precision operations written out one by one (this file must be
+ * compiled with -ffp-contract=off).
+ *
+ * Layouts (all row-major, element sizes in brackets):
+ *   logits [T,E] f32, bias [E] f32 (may be NULL), topk_ids [T,K] i32,
+ *   topk_w [T,K] f32, x [T,H] bf16 bits (u16), a_q [M,H] e4m3 (u8),
+ *   scale_a [M] f32, src2dst [T*K] i32, offsets [E+1] i32,
+ *   w13 [E,2I,H] e4m3 with rows 0..I-1 the gate projection and I..2I-1 the
+ *   up projection, s13 [E,2I] f32, w2 [E,H,I] e4m3, s2 [E,H] f32.
+ */
+#ifndef MOE_ORACLE_H
+#define MOE_ORACLE_H
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Scoring functions of the gate. */
+enum { ORACLE_SIGMOID = 0, ORACLE_SOFTMAX = 1 };
+
+void oracle_set_threads(int n);
+int oracle_get_threads(void);
+
+/* fp32 exponential: Cody-Waite reduction + degree-7 Taylor polynomial. */
+float oracle_exp32(float x);
+void oracle_exp32_n(const float* x, float* y, int64_t n);
+/* fp32 logistic function 1 / (1 + exp(-x)). */
+float oracle_sigmoid32(float x);
+void oracle_sigmoid32_n(const float* x, float* y, int64_t n);
+
+/* OCP FP8 e4m3 (fn): round to nearest even, saturate to +-448. */
+uint8_t oracle_e4m3_encode(float x);
+void oracle_e4m3_encode_n(const float* x, uint8_t* q, int64_t n);
+double oracle_e4m3_decode(uint8_t q);
+
+/* fp64 -> bf16 bits, round to nearest even (single rounding). */
+uint16_t oracle_bf16_round(double v);
+void oracle_bf16_round_n(const double* v, uint16_t* out, int64_t n);
+
+/* Gate. Returns 0, or -1 for invalid arguments, -2 for unsupported ones. */
+int oracle_gate(const float* logits, const float* bias, int T, int E,
+                int num_groups, int topk_group, int top_k, int scoring,
+                int renormalize, float routed_scaling_factor,
+                int32_t* topk_ids, float* topk_w);
+
+/* Stable counting sort of the flattened (token, slot) pairs by expert. */
+void oracle_route(const int32_t* topk_ids, int T, int E, int K,
+                  int32_t* offsets, int32_t* src2dst);
+
+/* Per-row dynamic FP8 quantisation of a bf16 matrix [R,C]. */
+void oracle_row_quant(const uint16_t* x, int64_t R, int C, uint8_t* q,
+                      float* scale);
+
+/* Route + quantise each token once + scatter its codes and scale to the K
+ * destinations (pre-reorder). */
+void oracle_permute_quant(const uint16_t* x, const int32_t* topk_ids, int T,
+                          int H, int E, int K, uint8_t* a_q, float* scale_a,
+                          int32_t* src2dst, int32_t* offsets);
+
+/* Grouped GEMM: C[r,n] = (sum_k A[r,k] B[e,n,k]) * scale_a[r] * scale_b[e,n]
+ * for r in expert e's segment, in fp64. */
+void oracle_grouped_gemm(const uint8_t* A, const float* scale_a,
+                         const uint8_t* B, const float* scale_b,
+                         const int32_t* offsets, int M, int N, int Kd, int E,
+                         double* C);
+
+/* h[r,j] = silu(C[r,j]) * C[r,I+j] in fp64. */
+void oracle_silu_mul(const double* C, int64_t M, int I, double* h);
+
+/* out[t,:] = sum_k w[t,k] * down[src2dst[t*K+k], :] in fp64. */
+void oracle_unpermute_sum(const double* down, const int32_t* src2dst,
+                          const float* topk_w, int T, int K, int H,
+                          double* out);
+
+/* Whole layer for the tokens listed in `tokens` (n_tok of them; each token's
+ * output depends on that token alone). out [n_tok,H] fp64. Also returns the
+ * gate result of those tokens when ids_out / w_out are non-NULL. */
+int oracle_forward_tokens(const uint16_t* x, const float* logits,
+                          const float* bias, const uint8_t* w13,
+                          const float* s13, const uint8_t* w2, const float* s2,
+                          int T, int H, int I, int E, int num_groups,
+                          int topk_group, int top_k, int scoring,
+                          int renormalize, float routed_scaling_factor,
+                          const int64_t* tokens, int n_tok, double* out,
+                          int32_t* ids_out, float* w_out);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

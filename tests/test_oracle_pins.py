@@ -1,0 +1,457 @@
+"""Pins of the CPU oracle against values fixed by the pages and by mathematics.
+
+Each test checks an oracle function against something other than itself:
+hand-worked cases (tests/golden), closed forms, brute-force enumeration,
+invariants, exhaustive nearest-value search, or a library routine the step
+reduces to in a special case. CPU only.
+"""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ---------------------------------------------------------------------------
+# FP8 e4m3
+# ---------------------------------------------------------------------------
+def e4m3_value_from_format(code: int) -> float:
+    """OCP e4m3 ("fn"): 1 sign, 4 exponent (bias 7), 3 mantissa bits; exponent
+    field 0 is subnormal (m/8 * 2^-6); S.1111.111 is NaN; no infinities."""
+    s = -1.0 if code & 0x80 else 1.0
+    e = (code >> 3) & 0xF
+    m = code & 0x7
+    if e == 0xF and m == 0x7:
+        return math.nan
+    if e == 0:
+        return s * (m / 8.0) * 2.0 ** -6
+    return s * (1.0 + m / 8.0) * 2.0 ** (e - 7)
+
+
+def test_e4m3_decode_matches_format_and_torch():
+    table = oracle.e4m3_decode_table()
+    ref = np.array([e4m3_value_from_format(c) for c in range(256)])
+    assert np.array_equal(np.isnan(table), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(table[ok], ref[ok])
+    # library cross-check: torch's float8_e4m3fn decoding of every code
+    tq = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(np.isnan(tq), np.isnan(ref))
+    assert np.array_equal(tq[ok], ref[ok])
+    assert table[0x7E] == 448.0 and table[0x01] == 2.0 ** -9 and table[0x08] == 2.0 ** -6
+
+
+def _nearest_even_reference(x: np.ndarray) -> np.ndarray:
+    """Nearest e4m3 code by search over the sorted positive code values,
+    ties to the even code, saturation at 448, sign carried separately."""
+    pos_codes = np.arange(0, 0x7F)  # 0x00..0x7E: finite, increasing values
+    pos_vals = np.array([e4m3_value_from_format(int(c)) for c in pos_codes])
+    a = np.abs(x.astype(np.float64))
+    sign = np.signbit(x).astype(np.uint8) << 7
+    hi = np.searchsorted(pos_vals, a, side="left")  # first value >= a
+    hi = np.clip(hi, 0, len(pos_vals) - 1)
+    lo = np.clip(hi - 1, 0, None)
+    d_hi = pos_vals[hi] - a
+    d_lo = a - pos_vals[lo]
+    pick_lo = (d_lo < d_hi) | ((d_lo == d_hi) & (pos_codes[lo] % 2 == 0))
+    exact = pos_vals[hi] == a
+    code = np.where(exact, pos_codes[hi], np.where(pick_lo, pos_codes[lo], pos_codes[hi]))
+    code = np.where(a >= 448.0, 0x7E, code)
+    return (code.astype(np.uint8) | sign).astype(np.uint8)
+
+
+def test_e4m3_encode_exhaustive_nearest_even():
+    # every fp32 bit pattern with magnitude in [2^-12, 2^9] (everything below
+    # rounds to zero, everything above saturates), both signs, in chunks
+    lo_bits = np.float32(2.0 ** -12).view(np.uint32)
+    hi_bits = np.float32(2.0 ** 9).view(np.uint32)
+    step = 1 << 22
+    for start in range(int(lo_bits), int(hi_bits) + 1, step):
+        bits = np.arange(start, min(start + step, int(hi_bits) + 1), dtype=np.uint32)
+        x = bits.view(np.float32)
+        for xs in (x, -x):
+            got = oracle.e4m3_encode(xs)
+            ref = _nearest_even_reference(xs)
+            bad = np.nonzero(got != ref)[0]
+            assert bad.size == 0, (xs[bad[:5]], got[bad[:5]], ref[bad[:5]])
+
+
+def test_e4m3_encode_specials_and_torch():
+    x = np.array([0.0, -0.0, 1e-30, -1e-30, 448.0, 449.0, 463.99, 464.0, 1e6, -1e6,
+                  2.0 ** -10, 2.0 ** -10 * 1.0000001, 3 * 2.0 ** -10], np.float32)
+    q = oracle.e4m3_encode(x)
+    assert list(q) == [0x00, 0x80, 0x00, 0x80, 0x7E, 0x7E, 0x7E, 0x7E, 0x7E, 0xFE,
+                       0x00, 0x01, 0x02]
+    # torch's e4m3fn cast is round-to-nearest-even without saturation: agree
+    # on every finite value inside the range
+    rng = np.random.default_rng(0)
+    v = (rng.standard_normal(200_000) * rng.choice([1e-3, 1e-1, 1, 30, 300], 200_000)).astype(np.float32)
+    v = np.clip(v, -448, 448)
+    tq = torch.from_numpy(v).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(oracle.e4m3_encode(v), tq)
+
+
+# ---------------------------------------------------------------------------
+# fp32 exp / sigmoid
+# ---------------------------------------------------------------------------
+def _ulp32(x):
+    x = np.abs(x.astype(np.float32))
+    return (np.nextafter(x, np.float32(np.inf)) - x).astype(np.float64)
+
+
+def test_exp32_within_two_ulp():
+    x = np.concatenate([np.linspace(-87.0, 88.5, 2_000_003, dtype=np.float32),
+                        np.linspace(-1, 1, 1_000_001, dtype=np.float32)])
+    y = oracle.exp32(x).astype(np.float64)
+    ref = np.exp(x.astype(np.float64))
+    err = np.abs(y - ref) / _ulp32(ref.astype(np.float32))
+    assert err.max() <= 2.0, err.max()
+    assert oracle.exp32(np.array([0.0], np.float32))[0] == 1.0
+    assert np.isinf(oracle.exp32(np.array([89.0], np.float32))[0])
+    assert oracle.exp32(np.array([-110.0], np.float32))[0] == 0.0
+
+
+def test_sigmoid32_within_three_ulp():
+    x = np.linspace(-30, 30, 1_000_001, dtype=np.float32)
+    y = oracle.sigmoid32(x).astype(np.float64)
+    xd = x.astype(np.float64)
+    ref = 1.0 / (1.0 + np.exp(-xd))
+    err = np.abs(y - ref) / _ulp32(ref.astype(np.float32))
+    assert err.max() <= 3.0, err.max()
+    assert oracle.sigmoid32(np.array([0.0], np.float32))[0] == 0.5
+
+
+# ---------------------------------------------------------------------------
+# Gate
+# ---------------------------------------------------------------------------
+def _load_gate_cases():
+    with open(os.path.join(GOLDEN, "gate_cases.json")) as f:
+        return json.load(f)["cases"]
+
+
+@pytest.mark.parametrize("case", _load_gate_cases(), ids=lambda c: c["name"])
+def test_gate_handworked(case):
+    scoring = oracle.SIGMOID if case["scoring"] == "sigmoid" else oracle.SOFTMAX
+    logits = np.array(case["logits"], np.float32)
+    bias = None if case["bias"] is None else np.array(case["bias"], np.float32)
+    ids, w = oracle.gate(logits, bias, case["num_groups"], case["topk_group"], case["top_k"],
+                         scoring, case["renormalize"], case["rsf"])
+    assert ids.tolist() == case["ids"]
+    tol = case.get("w_tol_rel", 0.0)
+    np.testing.assert_allclose(w, np.array(case["w"]), rtol=tol, atol=0)
+
+
+def _gate_problem(rng, T, E, G, scale_bias=0.3):
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    bias = (rng.standard_normal(E) * scale_bias).astype(np.float32)
+    # plant exact ties: copy some logits within rows
+    logits[:, 1] = logits[:, 0]
+    return logits, bias
+
+
+def _check_selection(keys, gsz, TG, K, ids):
+    """Brute force: the kept groups are a best TG-subset of all C(G, TG) subsets
+    under (score desc, index asc); the picks are the K best keys of the kept
+    groups under (key desc, index asc), in that order."""
+    E = keys.size
+    G = E // gsz
+    gscore = []
+    for g in range(G):
+        v = np.sort(keys[g * gsz:(g + 1) * gsz])[::-1]
+        gscore.append(np.float32(v[0] + v[1]) if gsz >= 2 else v[0])
+    rank = sorted(range(G), key=lambda g: (-float(gscore[g]), g))
+    best = None
+    for sub in itertools.combinations(range(G), TG):
+        key = sorted((rank.index(g) for g in sub))
+        if best is None or key < best[0]:
+            best = (key, set(sub))
+    kept = best[1]
+    allowed = [e for e in range(E) if e // gsz in kept]
+    want = sorted(allowed, key=lambda e: (-float(keys[e]), e))[:K]
+    assert list(ids) == want
+
+
+@pytest.mark.parametrize("E,G,TG,K", [(8, 4, 2, 2), (16, 4, 2, 3), (12, 3, 2, 4), (16, 8, 3, 5),
+                                      (16, 16, 4, 4), (16, 2, 1, 8), (6, 1, 1, 3)])
+def test_gate_bruteforce_enumeration(E, G, TG, K):
+    rng = np.random.default_rng(E * 100 + G * 10 + K)
+    T = 200
+    logits, bias = _gate_problem(rng, T, E, G)
+    ids, w = oracle.gate(logits, bias, G, TG, K, oracle.SIGMOID, True, 2.5)
+    s = oracle.sigmoid32(logits)
+    keys = (s + bias[None, :]).astype(np.float32)  # fp32 add, as the gate does
+    for t in range(T):
+        _check_selection(keys[t], E // G, TG, K, ids[t])
+
+
+def test_gate_weight_sum_is_rsf_and_linear():
+    rng = np.random.default_rng(7)
+    logits, bias = _gate_problem(rng, 500, 64, 8)
+    for rsf in (1.0, 2.5):
+        ids, w = oracle.gate(logits, bias, 8, 4, 8, oracle.SIGMOID, True, rsf)
+        ulp = float(np.spacing(np.float32(rsf)))
+        assert np.abs(w.astype(np.float64).sum(1) - rsf).max() <= 8 * ulp
+        # all ids distinct within a token
+        assert all(len(set(r)) == 8 for r in ids.tolist())
+    ids1, w1 = oracle.gate(logits, bias, 8, 4, 8, oracle.SIGMOID, True, 1.0)
+    ids2, w2 = oracle.gate(logits, bias, 8, 4, 8, oracle.SIGMOID, True, 2.0)
+    assert np.array_equal(ids1, ids2)
+    assert np.array_equal(w2, w1 * 2)  # scaling by 2 is exact
+    # softmax: closed form for K=2 (renormalised pair)
+    lg = rng.standard_normal((300, 8)).astype(np.float32)
+    ids, w = oracle.gate(lg, None, 1, 1, 2, oracle.SOFTMAX, True, 1.0)
+    top = np.argsort(-lg, axis=1, kind="stable")[:, :2]
+    assert np.array_equal(ids, top)
+    l0 = np.take_along_axis(lg, top[:, :1], 1)[:, 0].astype(np.float64)
+    l1 = np.take_along_axis(lg, top[:, 1:2], 1)[:, 0].astype(np.float64)
+    np.testing.assert_allclose(w[:, 0], 1.0 / (1.0 + np.exp(l1 - l0)), rtol=1e-6)
+    np.testing.assert_allclose(w.sum(1), 1.0, rtol=1e-6)
+
+
+def test_gate_no_renormalise():
+    rng = np.random.default_rng(3)
+    lg = rng.standard_normal((50, 16)).astype(np.float32)
+    ids, w = oracle.gate(lg, None, 1, 1, 4, oracle.SIGMOID, False, 2.5)
+    s = 1.0 / (1.0 + np.exp(-np.take_along_axis(lg, ids, 1).astype(np.float64)))
+    np.testing.assert_allclose(w, s * 2.5, rtol=1e-6)
+    ids, w = oracle.gate(lg, None, 1, 1, 4, oracle.SOFTMAX, False, 1.0)
+    p = np.exp(lg - lg.max(1, keepdims=True))
+    p = p / p.sum(1, keepdims=True)
+    np.testing.assert_allclose(w, np.take_along_axis(p, ids, 1), rtol=1e-6)
+
+
+def test_gate_rejects_bad_arguments():
+    lg = np.zeros((2, 8), np.float32)
+    for args in [(3, 1, 2), (4, 5, 2), (4, 2, 5), (4, 0, 1)]:
+        with pytest.raises(ValueError):
+            oracle.gate(lg, None, *args, oracle.SIGMOID, True, 1.0)
+    with pytest.raises(ValueError):  # softmax takes no correction bias
+        oracle.gate(lg, np.zeros(8, np.float32), 1, 1, 2, oracle.SOFTMAX, True, 1.0)
+
+
+# ---------------------------------------------------------------------------
+# Routing / pre-reorder
+# ---------------------------------------------------------------------------
+def _ids(rng, T, E, K, skew=False):
+    if skew:
+        p = np.zeros(E)
+        p[: max(K, E // 4)] = 1.0
+        p /= p.sum()
+        return np.stack([rng.choice(E, K, replace=False, p=p) for _ in range(T)]).astype(np.int32)
+    return np.stack([rng.choice(E, K, replace=False) for _ in range(T)]).astype(np.int32)
+
+
+@pytest.mark.parametrize("T,E,K,skew", [(37, 8, 2, False), (300, 64, 8, True), (1, 4, 4, False),
+                                        (0, 8, 2, False)])
+def test_route_invariants(T, E, K, skew):
+    rng = np.random.default_rng(T + E)
+    ids = _ids(rng, T, E, K, skew) if T else np.zeros((0, K), np.int32)
+    off, s2d = oracle.route(ids, E)
+    hist = np.bincount(ids.ravel(), minlength=E)
+    assert off[0] == 0 and np.array_equal(np.diff(off), hist)
+    assert np.array_equal(np.sort(s2d), np.arange(T * K))  # bijection onto [0, M)
+    flat = ids.ravel()
+    for e in range(E):
+        seg = np.nonzero(flat == e)[0]  # flattened (t,k) indices, ascending
+        dst = s2d[seg]
+        assert np.array_equal(dst, np.arange(off[e], off[e + 1]))  # in segment, ascending t
+
+
+def test_permute_then_unpermute_is_identity():
+    rng = np.random.default_rng(11)
+    T, H, E, K = 50, 64, 16, 4
+    ids = _ids(rng, T, E, K)
+    x = rng.standard_normal((T, H))
+    off, s2d = oracle.route(ids, E)
+    perm = np.zeros((T * K, H))
+    perm[s2d] = np.repeat(x, K, axis=0)
+    w = np.zeros((T, K), np.float32)
+    w[:, 0] = 1.0
+    out = oracle.unpermute_sum(perm, s2d, w)
+    assert np.array_equal(out, x)
+    # and with weights: sum of K equal rows times weights
+    w = rng.random((T, K)).astype(np.float32)
+    out = oracle.unpermute_sum(perm, s2d, w)
+    np.testing.assert_allclose(out, x * w.astype(np.float64).sum(1, keepdims=True), rtol=1e-12)
+
+
+def _bf16_bits(a):
+    return torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def test_row_quant_closed_form():
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal((40, 96)) * (10.0 ** rng.uniform(-3, 3, (40, 1)))
+    x[3] = 0.0  # an all-zero row
+    xb = _bf16_bits(x)
+    xv = oracle.bf16_to_f64(xb)
+    q, s = oracle.row_quant(xb)
+    amax = np.abs(xv).max(1).astype(np.float32)
+    exp_s = (np.maximum(amax, np.float32(1e-10)) / np.float32(448.0)).astype(np.float32)
+    assert np.array_equal(s, exp_s)
+    dec = oracle.e4m3_decode(q)
+    # each code is the nearest-even e4m3 of x / scale (pinned above), so
+    # |dec - x/s| <= half an e4m3 step: relative 2^-4 for normal values
+    r = xv / s[:, None].astype(np.float64)
+    assert np.all(np.abs(dec - r) <= np.maximum(np.abs(r) * 2.0 ** -4, 2.0 ** -10) + 1e-12)
+    # the row maximum lands on +-448 (code 0x7E / 0xFE)
+    nz = amax > 0
+    am = np.argmax(np.abs(xv), 1)
+    assert np.all(np.abs(dec[np.arange(40), am])[nz] == 448.0)
+    assert np.all(q[3] == 0)
+
+
+def test_permute_quant_scatter():
+    rng = np.random.default_rng(9)
+    T, H, E, K = 33, 64, 8, 2
+    ids = _ids(rng, T, E, K)
+    xb = _bf16_bits(rng.standard_normal((T, H)))
+    a_q, sa, s2d, off = oracle.permute_quant(xb, ids, E)
+    q, s = oracle.row_quant(xb)
+    off2, s2d2 = oracle.route(ids, E)
+    assert np.array_equal(off, off2) and np.array_equal(s2d, s2d2)
+    for t in range(T):
+        for k in range(K):
+            d = s2d[t * K + k]
+            assert np.array_equal(a_q[d], q[t]) and sa[d] == s[t]
+
+
+# ---------------------------------------------------------------------------
+# Grouped GEMM
+# ---------------------------------------------------------------------------
+def _codes_of(vals):
+    """e4m3 codes of exactly representable values."""
+    return oracle.e4m3_encode(np.asarray(vals, np.float32))
+
+
+def test_grouped_gemm_exact_integers():
+    rng = np.random.default_rng(1)
+    E, N, Kd = 3, 24, 64
+    counts = [5, 0, 9]
+    off = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    M = int(off[-1])
+    Av = rng.integers(-4, 5, (M, Kd)).astype(np.float32)
+    Bv = rng.integers(-3, 4, (E, N, Kd)).astype(np.float32)
+    A, B = _codes_of(Av), _codes_of(Bv)
+    C = oracle.grouped_gemm(A, np.ones(M, np.float32), B, np.ones((E, N), np.float32), off)
+    for e in range(E):
+        r0, r1 = off[e], off[e + 1]
+        ref = Av[r0:r1].astype(np.int64) @ Bv[e].astype(np.int64).T
+        assert np.array_equal(C[r0:r1], ref.astype(np.float64))
+
+
+def test_grouped_gemm_scales_per_row_and_channel():
+    """scale_a applies per ROW of the permuted activations, not per expert
+    (the bug fixed in sglang #6772 indexed it by expert id)."""
+    rng = np.random.default_rng(2)
+    E, N, Kd = 2, 16, 32
+    off = np.array([0, 4, 10], np.int32)
+    M = 10
+    A = rng.integers(0, 256, (M, Kd)).astype(np.uint8)
+    A[(A & 0x7F) == 0x7F] = 0  # no NaN codes
+    B = rng.integers(0, 256, (E, N, Kd)).astype(np.uint8)
+    B[(B & 0x7F) == 0x7F] = 0
+    sa = (10.0 ** rng.uniform(-3, 3, M)).astype(np.float32)
+    sb = rng.uniform(0.5, 2, (E, N)).astype(np.float32)
+    C = oracle.grouped_gemm(A, sa, B, sb, off)
+    Ad = oracle.e4m3_decode(A)
+    Bd = oracle.e4m3_decode(B)
+    for e in range(E):
+        r0, r1 = off[e], off[e + 1]
+        ref = (Ad[r0:r1] @ Bd[e].T) * sa[r0:r1, None].astype(np.float64) * sb[e][None, :].astype(np.float64)
+        np.testing.assert_allclose(C[r0:r1], ref, rtol=1e-13, atol=1e-300)
+    # a per-expert scale (first row's scale for the whole segment) differs
+    wrong = (Ad[4:10] @ Bd[1].T) * np.float64(sa[4]) * sb[1][None, :].astype(np.float64)
+    assert not np.allclose(C[4:10], wrong, rtol=1e-3)
+
+
+def test_silu_mul_closed_forms():
+    from scipy.special import expit
+    g = np.array([0.0, 30.0, -30.0, 1.0, -2.5, 100.0])
+    u = np.array([1.0, 2.0, 3.0, -1.0, 0.5, 1.0])
+    C = np.concatenate([g, u])[None, :]
+    h = oracle.silu_mul(C)[0]
+    assert h[0] == 0.0
+    np.testing.assert_allclose(h[1], 60.0, rtol=1e-12)
+    np.testing.assert_allclose(h[5], 100.0, rtol=1e-15)
+    np.testing.assert_allclose(h, g * expit(g) * u, rtol=1e-14)
+
+
+def test_bf16_round_single_rounding():
+    v = np.array([1.0, 1.0 + 2 ** -8, 1.0 + 2 ** -8 + 2 ** -40, 1.0 + 3 * 2 ** -8, -1.5,
+                  1.0 + 2 ** -8 - 2 ** -40, 3.0e38, 0.0])
+    got = oracle.bf16_round(v)
+    # torch rounds fp32 -> bf16 correctly; build the expected values from
+    # the cases where fp64 -> fp32 is exact, and the tie-breaking ones by hand
+    assert got[0] == 0x3F80
+    assert got[1] == 0x3F80          # exact tie -> even
+    assert got[2] == 0x3F81          # above the tie -> up (double rounding would give even)
+    assert got[3] == 0x3F82          # tie -> even (up)
+    assert got[4] == 0xBFC0
+    assert got[5] == 0x3F80          # below the tie -> down
+    assert got[7] == 0x0000
+    rng = np.random.default_rng(0)
+    x = rng.standard_normal(100_000).astype(np.float32)
+    tb = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(oracle.bf16_round(x.astype(np.float64)), tb)
+
+
+# ---------------------------------------------------------------------------
+# Whole layer
+# ---------------------------------------------------------------------------
+def _random_layer(rng, T, H, I, E):
+    from moe_expert_layer_grouped_gb300 import synth
+    x = _bf16_bits(rng.standard_normal((T, H)))
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    w13, s13 = synth.quantize_weight_rows(torch.from_numpy(rng.standard_normal((E, 2 * I, H)) * 0.02).float())
+    w2, s2 = synth.quantize_weight_rows(torch.from_numpy(rng.standard_normal((E, H, I)) * 0.02).float())
+    return x, logits, w13.numpy(), s13.numpy(), w2.numpy(), s2.numpy()
+
+
+def test_layer_single_expert_is_dense_fp8_mlp():
+    """E=1, K=1, rsf=1: routing is the identity and the layer is a dense FP8
+    MLP, computed here with numpy matmuls."""
+    rng = np.random.default_rng(4)
+    T, H, I = 6, 64, 32
+    x, logits, w13, s13, w2, s2 = _random_layer(rng, T, H, I, 1)
+    out, ids, w = oracle.forward_tokens(x, logits, None, w13, s13, w2, s2, 1, 1, 1,
+                                        oracle.SOFTMAX, True, 1.0)
+    assert np.all(ids == 0) and np.all(w == 1.0)
+    q, sa = oracle.row_quant(x)
+    C = (oracle.e4m3_decode(q) @ oracle.e4m3_decode(w13[0]).T) * sa[:, None].astype(np.float64) \
+        * s13[0][None, :].astype(np.float64)
+    g, u = C[:, :I], C[:, I:]
+    h = g / (1 + np.exp(-g)) * u
+    hb = oracle.bf16_round(h)
+    q2, sa2 = oracle.row_quant(hb)
+    ref = (oracle.e4m3_decode(q2) @ oracle.e4m3_decode(w2[0]).T) * sa2[:, None].astype(np.float64) \
+        * s2[0][None, :].astype(np.float64)
+    np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max())
+
+
+def test_layer_token_path_equals_step_path_and_is_linear_in_rsf():
+    rng = np.random.default_rng(6)
+    T, H, I, E = 24, 64, 32, 8
+    x, logits, w13, s13, w2, s2 = _random_layer(rng, T, H, I, E)
+    bias = (rng.standard_normal(E) * 0.1).astype(np.float32)
+    steps = oracle.forward_steps(x, logits, bias, w13, s13, w2, s2, 4, 2, 3, oracle.SIGMOID,
+                                 True, 2.5)
+    out, ids, w = oracle.forward_tokens(x, logits, bias, w13, s13, w2, s2, 4, 2, 3,
+                                        oracle.SIGMOID, True, 2.5)
+    assert np.array_equal(ids, steps["ids"]) and np.array_equal(w, steps["w"])
+    np.testing.assert_allclose(out, steps["out"], rtol=1e-12, atol=1e-12 * np.abs(out).max())
+    out1, _, _ = oracle.forward_tokens(x, logits, bias, w13, s13, w2, s2, 4, 2, 3,
+                                       oracle.SIGMOID, True, 1.25)
+    np.testing.assert_allclose(out, 2 * out1, rtol=1e-6, atol=1e-9)
+    # a subset of tokens gives the same rows
+    sub = np.array([5, 0, 23], np.int64)
+    outs, _, _ = oracle.forward_tokens(x, logits, bias, w13, s13, w2, s2, 4, 2, 3,
+                                       oracle.SIGMOID, True, 2.5, tokens=sub)
+    assert np.array_equal(outs, out[sub])
