@@ -1,0 +1,520 @@
+"""Benchmark of the MoE layer forward on GB300.
+
+One step = one moe_forward over one batch of synthetic tokens (gate,
+pre-reorder + FP8 quant, w13 GEMM + SiLU*mul, requant, w2 GEMM, weighted
+post-reorder). Prints ONE JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME] [--no-secondary] [--no-cpu-baseline]
+
+Default workload: DeepSeek-V3-shaped decode, T=128 tokens, H=7168, I=2048,
+E=256 experts (8 groups, 4 kept, top-8), sigmoid + correction bias, rsf 2.5;
+FP8 e4m3 per-channel weights resident in HBM. A second object in the same
+line ("secondary") reports the T=8192 prefill shape of the same layer.
+Multi-GPU (torchrun): every rank runs an independent replica on its own
+batch (weak scaling; the data path has no collective); the barrier and the
+max-over-ranks time use NCCL only for timing.
+"""
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+DEFAULT_WORKLOAD = "dsv3_decode_t128"
+SECONDARY_WORKLOAD = "dsv3_prefill_t8192"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+FP8_PER_BF16 = 2.0  # nominal dense FP8 : bf16 tensor throughput
+LAUNCHES_PER_FORWARD = 8  # gate, 3x pre-reorder, w13 GEMM, requant, w2 GEMM, post-reorder
+N_BATCHES = 4  # distinct token batches cycled through the timed steps
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--seed", type=int, default=0)
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return dict(hbm=float(p["hbm_gbs"]), bf16=float(p["bf16_tflops"]),
+                    bf16_sustained=float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                    sm_max=float(p.get("sm_max_mhz", 0)), source="measured")
+    except Exception:
+        return dict(hbm=FALLBACK_HBM_GBS, bf16=FALLBACK_BF16_TFLOPS,
+                    bf16_sustained=FALLBACK_BF16_TFLOPS, sm_max=2070.0, source="fallback")
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+
+    def summary(self, t0, t1):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        rows = [l for (t, l) in self.lines if t0 <= t <= t1] or [l for (_, l) in self.lines[-3:]]
+        for l in rows:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for name, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        sm.sort()
+        return {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# algorithmic work of one step
+# ---------------------------------------------------------------------------
+def step_work(wl, offsets_list):
+    """Algorithmic bytes / flops per forward, averaged over the batches.
+    Weights count once per expert that received at least one token."""
+    T, H, I, E, K = wl.T, wl.H, wl.I, wl.E, wl.top_k
+    M = T * K
+    res = []
+    for off in offsets_list:
+        cnt = off[1:] - off[:-1]
+        active = int((cnt > 0).sum())
+        w13 = active * (2 * I * H + 2 * I * 4)
+        w2 = active * (H * I + H * 4)
+        gemm13_bytes = w13 + M * H + M * 4 + M * I * 2 + (E + 1) * 4
+        gemm2_bytes = w2 + M * I + M * 4 + M * H * 2 + (E + 1) * 4
+        flops13 = 2.0 * M * 2 * I * H
+        flops2 = 2.0 * M * H * I
+        layer_bytes = w13 + w2 + T * H * 2 + T * E * 4 + T * H * 2
+        res.append(dict(active=active, gemm13_bytes=gemm13_bytes, gemm2_bytes=gemm2_bytes,
+                        flops13=flops13, flops2=flops2, layer_bytes=layer_bytes,
+                        layer_flops=flops13 + flops2))
+    avg = {k: sum(r[k] for r in res) / len(res) for k in res[0]}
+    return avg
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in ("gemm.cu", "ptx.cuh", "common.cuh"):
+        with open(os.path.join(ROOT, "moe_expert_layer_grouped_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload):
+    """dram bytes per launch of the w13 GEMM from the committed ncu summary,
+    if it was taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", f"grouped_gemm_w13_{workload}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    vals = {}
+    for line in text.splitlines():
+        if ":" in line and line.strip().startswith("- "):
+            k, v = line.strip()[2:].split(":", 1)
+            vals[k.strip()] = v.strip().strip("`")
+    if vals.get("kernel_source_sha256_16") != kernel_source_hash():
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+def make_batches(wl, seed, dev, synth):
+    batches = []
+    for b in range(N_BATCHES):
+        d = synth.make_inputs(wl, seed=seed * 100 + b, device=dev, weights=False)
+        batches.append((d["x"], d["logits"]))
+    return batches
+
+
+def time_forward(layer, batches, steps, warmup, torch, out):
+    for i in range(warmup):
+        x, l = batches[i % len(batches)]
+        layer(x, l, out=out)
+    torch.cuda.synchronize()
+    st = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for i in range(steps):
+        x, l = batches[i % len(batches)]
+        layer(x, l, out=out)
+    e1.record(st)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1)
+
+
+def time_breakdown(moe, layer, wl, batches, steps, torch):
+    """The same launches as moe_forward, issued step by step through the C ABI
+    with events between them, to time each kernel inside a running step."""
+    dev = batches[0][0].device
+    T, H, I, E, K = wl.T, wl.H, wl.I, wl.E, wl.top_k
+    M = T * K
+    ids = torch.empty((T, K), dtype=torch.int32, device=dev)
+    w = torch.empty((T, K), dtype=torch.float32, device=dev)
+    a_q = torch.empty((M, H), dtype=torch.uint8, device=dev)
+    sa = torch.empty(M, dtype=torch.float32, device=dev)
+    s2d = torch.empty(M, dtype=torch.int32, device=dev)
+    off = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    pws = torch.empty(max(moe.moe_permute_workspace_size(T, E, K), 256), dtype=torch.uint8,
+                      device=dev)
+    h = torch.empty((M, I), dtype=torch.bfloat16, device=dev)
+    q2 = torch.empty((M, I), dtype=torch.uint8, device=dev)
+    sa2 = torch.empty(M, dtype=torch.float32, device=dev)
+    down = torch.empty((M, H), dtype=torch.bfloat16, device=dev)
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    names = ["gate", "permute_quant", "grouped_gemm_w13", "act_quant", "grouped_gemm_w2",
+             "unpermute_sum"]
+    st = torch.cuda.current_stream()
+
+    def one(i, ev):
+        x, l = batches[i % len(batches)]
+        if ev: ev[0].record(st)
+        moe.moe_gate(l, layer.bias, wl.num_groups, wl.topk_group, K, wl.scoring, wl.renormalize,
+                     wl.rsf, topk_ids=ids, topk_w=w)
+        if ev: ev[1].record(st)
+        moe.moe_permute_quant(x, ids, E, a_q=a_q, scale_a=sa, src2dst=s2d, offsets=off,
+                              workspace=pws)
+        if ev: ev[2].record(st)
+        moe.moe_grouped_gemm(a_q, sa, layer.w13, layer.s13, off, moe.EPI_SILU_MUL, C=h)
+        if ev: ev[3].record(st)
+        moe.moe_act_quant(h, q=q2, scale=sa2)
+        if ev: ev[4].record(st)
+        moe.moe_grouped_gemm(q2, sa2, layer.w2, layer.s2, off, moe.EPI_BF16, C=down)
+        if ev: ev[5].record(st)
+        moe.moe_unpermute_sum(down, s2d, w, out=out)
+        if ev: ev[6].record(st)
+
+    for i in range(3):
+        one(i, None)
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(steps)]
+    for i in range(steps):
+        one(i, evs[i])
+    torch.cuda.synchronize()
+    tot = {n: 0.0 for n in names}
+    for ev in evs:
+        for j, n in enumerate(names):
+            tot[n] += ev[j].elapsed_time(ev[j + 1])
+    offs = []
+    for b in range(len(batches)):
+        one(b, None)
+        torch.cuda.synchronize()
+        offs.append(off.cpu().numpy().copy())
+    return {n: tot[n] / steps for n in names}, offs
+
+
+def time_e2e(layer, batches, steps, warmup, torch):
+    xs = [b[0].cpu().pin_memory() for b in batches]
+    ls = [b[1].cpu().pin_memory() for b in batches]
+    T, H = batches[0][0].shape
+    outs = [torch.empty((T, H), dtype=torch.bfloat16).pin_memory() for _ in batches]
+    for i in range(warmup):
+        j = i % len(batches)
+        layer.forward_host(xs[j], ls[j], outs[j])
+    torch.cuda.synchronize()
+    st = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for i in range(steps):
+        j = i % len(batches)
+        layer.forward_host(xs[j], ls[j], outs[j])
+    e1.record(st)
+    torch.cuda.synchronize()
+    h2d = xs[0].numel() * 2 + ls[0].numel() * 4
+    d2h = outs[0].numel() * 2
+    return e0.elapsed_time(e1) / steps, h2d, d2h
+
+
+def run_workload(moe, synth, torch, wl, seed, steps, warmup, dev, pk, want_clocks):
+    d = synth.make_inputs(wl, seed=seed, device=dev, weights=True)
+    layer = moe.MoELayer(d["w13"], d["s13"], d["w2"], d["s2"], d["bias"], wl.num_groups,
+                         wl.topk_group, wl.top_k, wl.scoring, wl.renormalize, wl.rsf, wl.T)
+    batches = make_batches(wl, seed, dev, synth)
+    out = torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device=dev)
+    clocks = ClockSampler(dev.index) if want_clocks else None
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    t0 = time.time()
+    ms_total = time_forward(layer, batches, steps, warmup, torch, out)
+    t1 = time.time()
+    if clocks:
+        clocks.stop()
+    if moe.moe_device_status() != 0:
+        raise RuntimeError("device error during the timed region")
+    ms = ms_total / steps
+    kern, offs = time_breakdown(moe, layer, wl, batches, max(10, min(steps, 200)), torch)
+    work = step_work(wl, offs)
+    return dict(layer=layer, batches=batches, ms=ms, ms_total=ms_total, kern=kern, work=work,
+                clocks=clocks.summary(t0, t1) if clocks else None, t0=t0, t1=t1)
+
+
+def roofline_decode(r, pk, workload):
+    k = r["kern"]["grouped_gemm_w13"]
+    bytes_ = r["work"]["gemm13_bytes"]
+    achieved = bytes_ / (k * 1e-3) / 1e9
+    tr = recorded_traffic(workload)
+    return {"kernel": "grouped_gemm_w13", "bound": "hbm", "achieved": round(achieved, 1),
+            "peak": pk["hbm"], "unit": "GB/s", "frac": round(achieved / pk["hbm"], 4),
+            "traffic": tr, "algorithmic_bytes_per_launch": int(bytes_),
+            "launch_ms": round(k, 4), "peak_source": f"{pk['source']} hbm_gbs"}
+
+
+def roofline_prefill(r, pk):
+    k = r["kern"]["grouped_gemm_w13"]
+    fl = r["work"]["flops13"]
+    achieved = fl / (k * 1e-3) / 1e12
+    peak = pk["bf16_sustained"] * FP8_PER_BF16
+    return {"kernel": "grouped_gemm_w13", "bound": "tensor", "achieved": round(achieved, 1),
+            "peak": round(peak, 1), "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+            "traffic": None, "algorithmic_flops_per_launch": fl, "launch_ms": round(k, 4),
+            "peak_source": f"{pk['source']} bf16_tflops_sustained x {FP8_PER_BF16} (fp8/bf16)"}
+
+
+def cpu_baseline(synth, torch, wl, seed, r, budget_s=15.0):
+    """The oracle, as it stands, on a bounded sample of tokens of the first
+    timed batch; weights copied from the device."""
+    import numpy as np
+    import oracle
+    n = synth.to_numpy_inputs({"w13": r["layer"].w13, "s13": r["layer"].s13,
+                               "w2": r["layer"].w2, "s2": r["layer"].s2,
+                               "bias": r["layer"].bias, "x": r["batches"][0][0],
+                               "logits": r["batches"][0][1]})
+    args = (n["x"], n["logits"], n["bias"], n["w13"], n["s13"], n["w2"], n["s2"],
+            wl.num_groups, wl.topk_group, wl.top_k, wl.scoring, wl.renormalize, wl.rsf)
+    threads = oracle.get_threads()
+    t = time.time()
+    oracle.forward_tokens(*args, tokens=np.arange(min(threads, wl.T), dtype=np.int64))
+    per_tok = (time.time() - t) / min(threads, wl.T)
+    ntok = int(max(1, min(wl.T, budget_s / max(per_tok, 1e-6))))
+    t = time.time()
+    oracle.forward_tokens(*args, tokens=np.arange(ntok, dtype=np.int64))
+    dt = time.time() - t
+    return {"value": round(ntok / dt, 3), "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"{ntok} of the {wl.T} tokens of one {wl.name} batch, whole layer "
+                      f"(gate..post-reorder), {dt:.1f} s"}
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import moe_expert_layer_grouped_gb300 as moe
+    from moe_expert_layer_grouped_gb300 import synth
+    import __graft_entry__
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if rank == 0:
+        __graft_entry__.build()
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        dist.barrier()
+        if rank != 0:
+            __graft_entry__.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    pk = peaks()
+    wl = synth.WORKLOADS[args.workload]
+    steps = args.steps if args.steps is not None else max(20, int(4000 * 128 / wl.T))
+    warmup = max(3, args.warmup)
+    seed = args.seed + rank
+
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    r = run_workload(moe, synth, torch, wl, seed, steps, warmup, dev, pk, want_clocks=True)
+    ms_total = r["ms_total"]
+    if world > 1:
+        t = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms = ms_total / steps
+    value = world * wl.T / (ms * 1e-3)
+
+    e2e_ms, h2d, d2h = time_e2e(r["layer"], r["batches"], steps, warmup, torch)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    line = {
+        "metric": "MoE-layer tokens/s + % of FP8/HBM roofline, DeepSeek-V3 shape T=128/8192",
+        "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": steps,
+        "warmup": warmup, "ms_per_step": round(ms, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "fp8_e4m3 x fp8_e4m3 -> fp32 (bf16 io)",
+        "data": "synthetic (seeded; weights ~N(0,0.02) quantised to e4m3 per channel)",
+        "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E,
+                   "num_groups": wl.num_groups, "topk_group": wl.topk_group, "top_k": wl.top_k,
+                   "scoring": "sigmoid" if wl.scoring == 0 else "softmax", "rsf": wl.rsf,
+                   "batches_cycled": N_BATCHES,
+                   "l2": "no flush: each step streams the active experts' weights "
+                         f"(~{r['work']['layer_bytes'] / 1e9:.2f} GB) through the 129 MB L2",
+                   "parallelism": f"replicas x{world} (no collective on the data path)"},
+        "tflops": round(r["work"]["layer_flops"] / (r["ms"] * 1e-3) / 1e12, 2),
+        "layer_hbm_gbs": round(r["work"]["layer_bytes"] / (r["ms"] * 1e-3) / 1e9, 1),
+        "active_experts": r["work"]["active"],
+        "kernels_ms": {k: round(v, 4) for k, v in r["kern"].items()},
+        "roofline": roofline_decode(r, pk, wl.name) if wl.T <= 512 else roofline_prefill(r, pk),
+        "e2e": {"value": round(world * wl.T / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": steps * LAUNCHES_PER_FORWARD,
+        "clocks": r["clocks"],
+    }
+    if not args.no_secondary and rank == 0 and world == 1:
+        wl2 = synth.WORKLOADS[SECONDARY_WORKLOAD]
+        del r
+        torch.cuda.empty_cache()
+        s_steps = max(20, steps // 20)
+        r2 = run_workload(moe, synth, torch, wl2, seed, s_steps, warmup, dev, pk,
+                          want_clocks=True)
+        line["secondary"] = {
+            "workload": wl2.name, "T": wl2.T, "value": round(wl2.T / (r2["ms"] * 1e-3), 1),
+            "unit": "tokens/s", "ms_per_step": round(r2["ms"], 4), "steps": s_steps,
+            "tflops": round(r2["work"]["layer_flops"] / (r2["ms"] * 1e-3) / 1e12, 2),
+            "layer_fp8_tensor_frac": round(
+                r2["work"]["layer_flops"] / (r2["ms"] * 1e-3) / 1e12
+                / (pk["bf16_sustained"] * FP8_PER_BF16), 4),
+            "kernels_ms": {k: round(v, 4) for k, v in r2["kern"].items()},
+            "roofline": roofline_prefill(r2, pk), "clocks": r2["clocks"]}
+        r = None
+        del r2
+        torch.cuda.empty_cache()
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        d = synth.make_inputs(wl, seed=seed, device=dev, weights=True)
+        layer = moe.MoELayer(d["w13"], d["s13"], d["w2"], d["s2"], d["bias"], wl.num_groups,
+                             wl.topk_group, wl.top_k, wl.scoring, wl.renormalize, wl.rsf, wl.T)
+        line["cpu_baseline"] = cpu_baseline(synth, torch, wl, seed,
+                                            {"layer": layer, "batches": make_batches(
+                                                wl, seed, dev, synth)})
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_reference(args):
+    """The reference arm: the CPU oracle as it stands, timed on the host cores
+    on a bounded sample of the same workload (rank 0 only)."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import numpy as np
+    import torch
+
+    import oracle
+    from moe_expert_layer_grouped_gb300 import synth
+    from oracle import build as oracle_build
+    oracle_build.build()
+    wl = synth.WORKLOADS[args.workload]
+    steps = args.steps if args.steps is not None else 3
+    warmup = max(0, min(args.warmup, 1))
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    d = synth.make_inputs(wl, seed=args.seed, device=dev, weights=True)
+    n = synth.to_numpy_inputs(d)
+    del d
+    fargs = (n["x"], n["logits"], n["bias"], n["w13"], n["s13"], n["w2"], n["s2"],
+             wl.num_groups, wl.topk_group, wl.top_k, wl.scoring, wl.renormalize, wl.rsf)
+    threads = oracle.get_threads()
+    t = time.time()
+    oracle.forward_tokens(*fargs, tokens=np.arange(min(threads, wl.T), dtype=np.int64))
+    per_tok = (time.time() - t) / min(threads, wl.T)
+    budget = max(5.0, 60.0 / max(1, steps + warmup))
+    ntok = int(max(1, min(wl.T, budget / max(per_tok, 1e-6))))
+    toks = np.arange(ntok, dtype=np.int64)
+    for _ in range(warmup):
+        oracle.forward_tokens(*fargs, tokens=toks)
+    t = time.time()
+    for _ in range(steps):
+        oracle.forward_tokens(*fargs, tokens=toks)
+    dt = (time.time() - t) / steps
+    value = ntok / dt
+    sample = (f"{ntok} of the {wl.T} tokens of one {wl.name} batch per step, whole layer "
+              f"(gate..post-reorder) in fp64")
+    line = {
+        "impl": "reference",
+        "metric": "MoE-layer tokens/s + % of FP8/HBM roofline, DeepSeek-V3 shape T=128/8192",
+        "value": round(value, 3), "unit": "tokens/s", "n_gpus": args.gpus, "steps": steps,
+        "warmup": warmup, "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64 (FP8 codes decoded exactly)",
+        "data": "synthetic (seeded)",
+        "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E,
+                   "top_k": wl.top_k},
+        "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": threads,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,232 @@
+/*
+ * moe_gb300: forward pass of a grouped-expert Mixture-of-Experts layer with
+ * all experts on one GB300 (sm_103a), as a C ABI.
+ *
+ * The layer follows three sglang pull-request pages:
+ *   [P1] "Fix one bug in the grouped-gemm triton kernel" (sglang #6772)
+ *   [P2] "Support token-level quantization for EP MoE" (sglang #6782)
+ *   [P3] "[1/2] sgl-kernel: Fuse routed scaling factor into select_experts"
+ *        (sglang #8364)
+ * Steps, in order: grouped top-k gate with routed_scaling_factor fused in
+ * (moe_gate), pre-reorder with per-token FP8 quantisation
+ * (moe_permute_quant), w13 grouped GEMM with per-row scale_a and
+ * per-channel scale_b plus SiLU*mul (moe_grouped_gemm), per-token
+ * requantisation (moe_act_quant), w2 grouped GEMM (moe_grouped_gemm) and
+ * the weighted post-reorder (moe_unpermute_sum); moe_forward runs them all.
+ *
+ * Conventions for every entry point:
+ *  - Pointers are DEVICE pointers unless the name ends in _host. The caller
+ *    owns every buffer; no entry point allocates device memory per call.
+ *    (The library keeps, per device, a 4-byte error word it allocates at
+ *    load time as a static device variable.)
+ *  - bf16 tensors are passed as void* to 16-bit bfloat16 values, FP8 tensors
+ *    as void* to 8-bit OCP e4m3 ("e4m3fn": bias 7, max 448, no inf) codes.
+ *  - All tensors are dense, row-major, with the last dimension contiguous.
+ *    Every tensor pointer must be 16-byte aligned.
+ *  - `stream` is a cudaStream_t (NULL: the legacy default stream). Every call
+ *    is asynchronous on that stream and never synchronises the host.
+ *  - Errors are returned as moe_status codes and never thrown. Arguments are
+ *    validated on the host before anything is launched; an invalid call
+ *    launches nothing. MOE_ERR_CUDA means a launch failed (the CUDA error is
+ *    left for cudaGetLastError). Faults detected inside a kernel (an expert
+ *    id out of range, a pipeline wait that timed out) set the device error
+ *    word; read and clear it with moe_device_status().
+ *  - Inputs containing NaN or Inf are outside the contract.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = -1, /* a size, pointer or alignment is invalid */
+  MOE_ERR_UNSUPPORTED = -2, /* valid but outside what the kernels handle */
+  MOE_ERR_WORKSPACE = -3,   /* workspace missing or too small */
+  MOE_ERR_CUDA = -4,        /* a CUDA runtime/driver call failed */
+  MOE_ERR_DEVICE = -5       /* moe_device_status: a kernel flagged a fault */
+} moe_status;
+
+typedef enum { MOE_SCORE_SIGMOID = 0, MOE_SCORE_SOFTMAX = 1 } moe_scoring;
+
+typedef enum {
+  MOE_EPI_BF16 = 0,    /* C[r,n] = bf16(acc * scale_a[r] * scale_b[e,n]) */
+  MOE_EPI_SILU_MUL = 1 /* h[r,j] = bf16(silu(C[r,j]) * C[r,I+j]), I = N/2 */
+} moe_epilogue;
+
+/* Device-side fault codes reported by moe_device_status(). */
+enum {
+  MOE_DEV_OK = 0,
+  MOE_DEV_BAD_EXPERT_ID = 1,  /* moe_permute_quant: topk_ids out of [0,E) */
+  MOE_DEV_PIPE_TIMEOUT = 2,   /* moe_grouped_gemm: a pipeline wait gave up */
+  MOE_DEV_BAD_OFFSETS = 3     /* moe_grouped_gemm: offsets not monotone or > M */
+};
+
+/* Human-readable name of a status code (static string). */
+MOE_API const char* moe_status_string(moe_status s);
+
+/* Version of this ABI: (major << 16) | minor. */
+MOE_API int moe_abi_version(void);
+
+/*
+ * moe_gate — grouped, bias-corrected top-k expert selection.
+ * [P3] Motivation/Highlights: the selected experts' weights are normalised
+ * and multiplied by routed_scaling_factor inside the gate; [P3] names the
+ * biased grouped top-k op. Semantics (readings where the pages are silent):
+ *   scoring SIGMOID: s = 1/(1+exp(-l)) (fp32, exp by Cody-Waite reduction and
+ *     a degree-7 Taylor polynomial); key b = s + bias[e] (bias NULL: 0).
+ *     Group g (experts [g*E/G, (g+1)*E/G)) scores the sum of its two largest
+ *     keys (its only key for one-expert groups); the topk_group best groups
+ *     are kept; the top_k largest keys among the kept groups are selected.
+ *     Ties go to the lower index. Slot k holds the k-th selection.
+ *     Weights: w_k = s_k / S * rsf with S the fp32 slot-order sum of the
+ *     selected s (renormalize != 0), or w_k = s_k * rsf.
+ *   scoring SOFTMAX (requires bias == NULL and num_groups == 1): experts are
+ *     selected by logit; w_k = exp(l_k - l_slot0) / S * rsf (renormalize), or
+ *     exp(l_k - l_max) / Z * rsf with Z summed over all experts in order.
+ * logits [T,E] f32; bias [E] f32 or NULL; topk_ids [T,top_k] i32 (out);
+ * topk_w [T,top_k] f32 (out). Bit-exact across runs.
+ * Limits: 1 <= E <= 1024, E % num_groups == 0, num_groups <= 64,
+ * 1 <= topk_group <= num_groups, 1 <= top_k <= min(32, topk_group*E/G).
+ */
+MOE_API moe_status moe_gate(const float* logits, const float* bias, int T, int E,
+                    int num_groups, int topk_group, int top_k, int scoring,
+                    int renormalize, float routed_scaling_factor,
+                    int32_t* topk_ids, float* topk_w, void* stream);
+
+/* Workspace bytes moe_permute_quant needs for T tokens, E experts. */
+MOE_API size_t moe_permute_workspace_size(int T, int E, int K);
+
+/*
+ * moe_permute_quant — pre-reorder with dynamic per-token FP8 quantisation.
+ * [P2] Summary/Changelog: per-token activation scales from per-token maxima,
+ * loaded per token in the pre-reorder; the scales are written in permuted
+ * order through src2dst ([P2] Code Review). [P1] Highlights: each expert
+ * owns a contiguous row range starting at m_range_start.
+ *   Routing: the flattened pairs i = t*K + k are counting-sorted by expert,
+ *   stable in i (so ascending t within an expert): offsets[0] = 0,
+ *   offsets[e+1] = offsets[e] + count[e]; src2dst[i] = destination row.
+ *   Quantisation of token t: amax = max|x[t,:]|, scale = max(amax,1e-10)/448
+ *   (fp32), code = e4m3_rne_satfinite(x / scale) (IEEE division);
+ *   a_q[src2dst[t*K+k], :] = codes and scale_a[src2dst[t*K+k]] = scale for
+ *   every slot k.
+ * x [T,H] bf16; topk_ids [T,K] i32 (values in [0,E), distinct per token);
+ * a_q [T*K,H] e4m3 (out); scale_a [T*K] f32 (out); src2dst [T*K] i32 (out);
+ * offsets [E+1] i32 (out); ws: moe_permute_workspace_size(T,E,K) bytes,
+ * 256-byte aligned (contents on entry ignored). Bit-exact.
+ * Limits: H % 32 == 0, 1 <= E <= 1024, 1 <= K <= 32, T*K < 2^31.
+ */
+MOE_API moe_status moe_permute_quant(const void* x, const int32_t* topk_ids, int T,
+                             int H, int E, int K, void* a_q, float* scale_a,
+                             int32_t* src2dst, int32_t* offsets, void* ws,
+                             size_t ws_bytes, void* stream);
+
+/*
+ * moe_grouped_gemm — FP8 grouped GEMM over expert row segments, tcgen05.
+ * [P1] Highlights and [P2] Changelog: within expert e's rows
+ * [offsets[e], offsets[e+1]) the fp32 accumulator is dequantised by the
+ * ROW's per-token scale_a times the weight scale; no block quantisation.
+ *   acc[r,n] = sum_k A[r,k] * B[e,n,k]   (fp32 accumulate on tensor cores)
+ *   epilogue MOE_EPI_BF16:     C [M,N] bf16 = acc * scale_a[r] * scale_b[e,n]
+ *   epilogue MOE_EPI_SILU_MUL: with I = N/2, g = that value for n = j and
+ *     u for n = I + j: C [M,I] bf16 = silu(g) * u; if row_amax != NULL it
+ *     must hold zeros on entry and receives max_j |C[r,j]| (after bf16
+ *     rounding) for every row.
+ * A [M,Kd] e4m3 (rows grouped by expert); scale_a [M] f32;
+ * B [E,N,Kd] e4m3 (K-major weights; for SILU_MUL rows 0..I-1 are the gate
+ * projection and I..2I-1 the up projection); scale_b [E,N] f32;
+ * offsets [E+1] i32 on the device (monotone, offsets[E] <= M). Rows beyond
+ * offsets[E] are not written. No workspace.
+ * Limits: Kd % 32 == 0, N % 32 == 0 (SILU_MUL: N % 64 == 0), E <= 1024.
+ */
+MOE_API moe_status moe_grouped_gemm(const void* A, const float* scale_a,
+                            const void* B, const float* scale_b,
+                            const int32_t* offsets, int M, int N, int Kd,
+                            int E, int epilogue, void* C, float* row_amax,
+                            void* stream);
+
+/*
+ * moe_act_quant — per-token requantisation of the activation output.
+ * [P2] Changelog/Code Review: down_input is quantised per token to FP8 with
+ * the per-token quantiser, giving w2_input_scale.
+ *   amax = row_amax[r] if row_amax != NULL, else max_j |h[r,j]|;
+ *   scale[r] = max(amax,1e-10)/448 (fp32); q[r,j] = e4m3_rne_satfinite(
+ *   h[r,j] / scale[r]).
+ * h [M,I] bf16; row_amax [M] f32 or NULL; q [M,I] e4m3 (out);
+ * scale [M] f32 (out). Bit-exact. Limits: I % 32 == 0.
+ */
+MOE_API moe_status moe_act_quant(const void* h, const float* row_amax, int M, int I,
+                         void* q, float* scale, void* stream);
+
+/*
+ * moe_unpermute_sum — weighted post-reorder back to token order.
+ * [P3] Motivation names moe_sum_reduce, the weighted top-k sum.
+ *   out[t,:] = bf16( sum_{k=0..K-1} topk_w[t,k] * down[src2dst[t*K+k], :] )
+ * accumulated in fp32 in slot order.
+ * down [M,H] bf16; src2dst [T*K] i32; topk_w [T,K] f32; out [T,H] bf16.
+ * Limits: H % 8 == 0, 1 <= K <= 32.
+ */
+MOE_API moe_status moe_unpermute_sum(const void* down, const int32_t* src2dst,
+                             const float* topk_w, int T, int K, int H,
+                             void* out, void* stream);
+
+/* Workspace bytes moe_forward / moe_forward_host need. */
+MOE_API size_t moe_workspace_size(int T, int H, int I, int E, int K);
+
+/*
+ * moe_forward — the whole layer: gate, pre-reorder + quant, w13 GEMM with
+ * SiLU*mul, requant, w2 GEMM, weighted post-reorder, on one stream.
+ * x [T,H] bf16; logits [T,E] f32; bias [E] f32 or NULL;
+ * w13 [E,2I,H] e4m3 (rows: gate then up); s13 [E,2I] f32;
+ * w2 [E,H,I] e4m3; s2 [E,H] f32; out [T,H] bf16.
+ * ws: moe_workspace_size(T,H,I,E,top_k) bytes, 256-byte aligned; it holds
+ * every intermediate (ids, weights, permuted codes, h, ...).
+ * Limits: those of the steps; H % 32 == 0 and I % 32 == 0.
+ */
+MOE_API moe_status moe_forward(const void* x, const float* logits, const float* bias,
+                       const void* w13, const float* s13, const void* w2,
+                       const float* s2, int T, int H, int I, int E,
+                       int num_groups, int topk_group, int top_k, int scoring,
+                       int renormalize, float routed_scaling_factor, void* out,
+                       void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * moe_forward_host — moe_forward with the per-step tensors in HOST memory:
+ * copies x_host [T,H] bf16 and logits_host [T,E] f32 to the device (into
+ * the workspace), runs the layer and copies the result to out_host [T,H]
+ * bf16, all asynchronously on `stream` (use pinned host memory for true
+ * asynchrony; the host buffers must stay valid until the stream reaches
+ * the end of this call). Weights, scales and bias stay device pointers.
+ */
+MOE_API moe_status moe_forward_host(const void* x_host, const float* logits_host,
+                            const float* bias, const void* w13,
+                            const float* s13, const void* w2, const float* s2,
+                            int T, int H, int I, int E, int num_groups,
+                            int topk_group, int top_k, int scoring,
+                            int renormalize, float routed_scaling_factor,
+                            void* out_host, void* ws, size_t ws_bytes,
+                            void* stream);
+
+/*
+ * moe_device_status — synchronises the current device, copies its device
+ * error word into *code (one of MOE_DEV_*), clears it, and returns MOE_OK
+ * when it was zero, MOE_ERR_DEVICE otherwise (MOE_ERR_CUDA if the copy
+ * failed).
+ */
+MOE_API moe_status moe_device_status(int* code);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -1,0 +1,284 @@
+"""Python binding of libmoe_gb300.so, the C ABI of the grouped-expert MoE
+layer forward on GB300 (sm_103a).
+
+The functions carry the C entry points' names and only marshal arguments:
+they allocate output tensors with torch when none are given, pass raw device
+pointers, sizes and the current CUDA stream, and raise MoEError on a
+non-zero status. Every step of the layer runs in the library's CUDA kernels;
+there is no fallback: if the library is not built, every call raises.
+
+Tensor formats: bf16 tensors are torch.bfloat16; FP8 e4m3 tensors are
+torch.uint8 (codes) or torch.float8_e4m3fn; everything is contiguous and on
+the same CUDA device.
+"""
+import ctypes
+import os
+
+__all__ = [
+    "MoEError", "SIGMOID", "SOFTMAX", "EPI_BF16", "EPI_SILU_MUL", "library_path", "load",
+    "moe_gate", "moe_permute_quant", "moe_permute_workspace_size", "moe_grouped_gemm",
+    "moe_act_quant", "moe_unpermute_sum", "moe_workspace_size", "moe_forward",
+    "moe_forward_host", "moe_device_status", "MoELayer",
+]
+
+SIGMOID = 0
+SOFTMAX = 1
+EPI_BF16 = 0
+EPI_SILU_MUL = 1
+
+_STATUS = {0: "MOE_OK", -1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_UNSUPPORTED",
+           -3: "MOE_ERR_WORKSPACE", -4: "MOE_ERR_CUDA", -5: "MOE_ERR_DEVICE"}
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+def library_path():
+    return os.path.join(_HERE, "_lib", "libmoe_gb300.so")
+
+
+class MoEError(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        super().__init__(f"{fn}: {_STATUS.get(status, status)}")
+
+
+_lib = None
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_F = ctypes.c_float
+_SZ = ctypes.c_size_t
+_SIGNATURES = {
+    "moe_status_string": (ctypes.c_char_p, [_I]),
+    "moe_abi_version": (_I, []),
+    "moe_gate": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P]),
+    "moe_permute_workspace_size": (_SZ, [_I, _I, _I]),
+    "moe_permute_quant": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_grouped_gemm": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P]),
+    "moe_act_quant": (_I, [_P, _P, _I, _I, _P, _P, _P]),
+    "moe_unpermute_sum": (_I, [_P, _P, _P, _I, _I, _I, _P, _P]),
+    "moe_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
+    "moe_forward": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _F,
+                         _P, _P, _SZ, _P]),
+    "moe_forward_host": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I,
+                              _F, _P, _P, _SZ, _P]),
+    "moe_device_status": (_I, [ctypes.POINTER(_I)]),
+}
+
+
+def load():
+    """Load libmoe_gb300.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"{path} is missing: build it with `python -c 'import __graft_entry__ as g; "
+                f"g.build()'` (needs nvcc); the MoE layer has no non-CUDA path")
+        lib = ctypes.CDLL(path)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def _check(fn, status):
+    if status != 0:
+        raise MoEError(fn, status)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is not None:
+            if not t.is_cuda:
+                raise ValueError("moe_gb300: tensors must be CUDA tensors")
+            if not t.is_contiguous():
+                raise ValueError("moe_gb300: tensors must be contiguous")
+
+
+def _u8(t):
+    import torch
+    return t.view(torch.uint8) if t.dtype != torch.uint8 else t
+
+
+def moe_gate(logits, bias, num_groups, topk_group, top_k, scoring=SIGMOID, renormalize=True,
+             routed_scaling_factor=1.0, topk_ids=None, topk_w=None, stream=None):
+    import torch
+    _need_cuda(logits, bias)
+    T, E = logits.shape
+    if topk_ids is None:
+        topk_ids = torch.empty((T, top_k), dtype=torch.int32, device=logits.device)
+    if topk_w is None:
+        topk_w = torch.empty((T, top_k), dtype=torch.float32, device=logits.device)
+    _check("moe_gate", load().moe_gate(
+        _ptr(logits), _ptr(bias), T, E, num_groups, topk_group, top_k, scoring,
+        int(bool(renormalize)), float(routed_scaling_factor), _ptr(topk_ids), _ptr(topk_w),
+        _stream(stream)))
+    return topk_ids, topk_w
+
+
+def moe_permute_workspace_size(T, E, K):
+    return load().moe_permute_workspace_size(T, E, K)
+
+
+def moe_permute_quant(x, topk_ids, E, a_q=None, scale_a=None, src2dst=None, offsets=None,
+                      workspace=None, stream=None):
+    import torch
+    _need_cuda(x, topk_ids)
+    T, H = x.shape
+    K = topk_ids.shape[1]
+    dev = x.device
+    M = T * K
+    a_q = torch.empty((M, H), dtype=torch.uint8, device=dev) if a_q is None else a_q
+    scale_a = torch.empty(M, dtype=torch.float32, device=dev) if scale_a is None else scale_a
+    src2dst = torch.empty(M, dtype=torch.int32, device=dev) if src2dst is None else src2dst
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev) if offsets is None else offsets
+    nws = moe_permute_workspace_size(T, E, K)
+    if workspace is None:
+        workspace = torch.empty(max(nws, 256), dtype=torch.uint8, device=dev)
+    _check("moe_permute_quant", load().moe_permute_quant(
+        _ptr(x), _ptr(topk_ids), T, H, E, K, _ptr(_u8(a_q)), _ptr(scale_a), _ptr(src2dst),
+        _ptr(offsets), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream)))
+    return a_q, scale_a, src2dst, offsets
+
+
+def moe_grouped_gemm(A, scale_a, B, scale_b, offsets, epilogue=EPI_BF16, C=None, row_amax=None,
+                     stream=None):
+    import torch
+    _need_cuda(A, scale_a, B, scale_b, offsets, C, row_amax)
+    M, Kd = A.shape
+    E, N, Kd2 = B.shape
+    if Kd2 != Kd:
+        raise ValueError("moe_grouped_gemm: K mismatch")
+    if C is None:
+        cols = N // 2 if epilogue == EPI_SILU_MUL else N
+        C = torch.empty((M, cols), dtype=torch.bfloat16, device=A.device)
+    _check("moe_grouped_gemm", load().moe_grouped_gemm(
+        _ptr(_u8(A)), _ptr(scale_a), _ptr(_u8(B)), _ptr(scale_b), _ptr(offsets), M, N, Kd, E,
+        epilogue, _ptr(C), _ptr(row_amax), _stream(stream)))
+    return C
+
+
+def moe_act_quant(h, row_amax=None, q=None, scale=None, stream=None):
+    import torch
+    _need_cuda(h, row_amax)
+    M, I = h.shape
+    q = torch.empty((M, I), dtype=torch.uint8, device=h.device) if q is None else q
+    scale = torch.empty(M, dtype=torch.float32, device=h.device) if scale is None else scale
+    _check("moe_act_quant", load().moe_act_quant(
+        _ptr(h), _ptr(row_amax), M, I, _ptr(_u8(q)), _ptr(scale), _stream(stream)))
+    return q, scale
+
+
+def moe_unpermute_sum(down, src2dst, topk_w, out=None, stream=None):
+    import torch
+    _need_cuda(down, src2dst, topk_w)
+    T, K = topk_w.shape
+    H = down.shape[1]
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=down.device) if out is None else out
+    _check("moe_unpermute_sum", load().moe_unpermute_sum(
+        _ptr(down), _ptr(src2dst), _ptr(topk_w), T, K, H, _ptr(out), _stream(stream)))
+    return out
+
+
+def moe_workspace_size(T, H, I, E, K):
+    return load().moe_workspace_size(T, H, I, E, K)
+
+
+def _dims(x, logits, w13, w2):
+    T, H = x.shape
+    E = logits.shape[1]
+    I = w2.shape[2]
+    if tuple(w13.shape) != (E, 2 * I, H) or tuple(w2.shape) != (E, H, I):
+        raise ValueError("moe_forward: weight shapes do not match [E,2I,H] / [E,H,I]")
+    return T, H, I, E
+
+
+def moe_forward(x, logits, bias, w13, s13, w2, s2, num_groups, topk_group, top_k,
+                scoring=SIGMOID, renormalize=True, routed_scaling_factor=1.0, out=None,
+                workspace=None, stream=None):
+    import torch
+    _need_cuda(x, logits, bias, w13, s13, w2, s2, out, workspace)
+    T, H, I, E = _dims(x, logits, w13, w2)
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=x.device) if out is None else out
+    nws = moe_workspace_size(T, H, I, E, top_k)
+    if workspace is None:
+        workspace = torch.empty(nws, dtype=torch.uint8, device=x.device)
+    _check("moe_forward", load().moe_forward(
+        _ptr(x), _ptr(logits), _ptr(bias), _ptr(_u8(w13)), _ptr(s13), _ptr(_u8(w2)), _ptr(s2),
+        T, H, I, E, num_groups, topk_group, top_k, scoring, int(bool(renormalize)),
+        float(routed_scaling_factor), _ptr(out), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out
+
+
+def moe_forward_host(x_host, logits_host, bias, w13, s13, w2, s2, num_groups, topk_group, top_k,
+                     scoring, renormalize, routed_scaling_factor, out_host, workspace,
+                     stream=None):
+    """x_host, logits_host and out_host are CPU tensors (pinned for asynchrony);
+    the copies run on `stream` inside the call."""
+    _need_cuda(bias, w13, s13, w2, s2, workspace)
+    for t in (x_host, logits_host, out_host):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError("moe_forward_host: x, logits and out must be contiguous host tensors")
+    T, H, I, E = _dims(x_host, logits_host, w13, w2)
+    _check("moe_forward_host", load().moe_forward_host(
+        _ptr(x_host), _ptr(logits_host), _ptr(bias), _ptr(_u8(w13)), _ptr(s13), _ptr(_u8(w2)),
+        _ptr(s2), T, H, I, E, num_groups, topk_group, top_k, scoring, int(bool(renormalize)),
+        float(routed_scaling_factor), _ptr(out_host), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out_host
+
+
+def moe_device_status():
+    """Synchronise the device and return (and clear) its device error code."""
+    code = ctypes.c_int(0)
+    st = load().moe_device_status(ctypes.byref(code))
+    if st not in (0, -5):
+        raise MoEError("moe_device_status", st)
+    return code.value
+
+
+class MoELayer:
+    """A layer's resident weights plus a reusable workspace; calls moe_forward."""
+
+    def __init__(self, w13, s13, w2, s2, bias, num_groups, topk_group, top_k, scoring,
+                 renormalize, routed_scaling_factor, max_tokens):
+        import torch
+        self.w13, self.s13, self.w2, self.s2, self.bias = w13, s13, w2, s2, bias
+        self.E, I2, self.H = w13.shape
+        self.I = I2 // 2
+        self.num_groups, self.topk_group, self.top_k = num_groups, topk_group, top_k
+        self.scoring, self.renormalize, self.rsf = scoring, renormalize, routed_scaling_factor
+        self.max_tokens = max_tokens
+        self.workspace = torch.empty(
+            moe_workspace_size(max_tokens, self.H, self.I, self.E, top_k), dtype=torch.uint8,
+            device=w13.device)
+
+    def __call__(self, x, logits, out=None, stream=None):
+        if x.shape[0] > self.max_tokens:
+            raise ValueError("MoELayer: more tokens than the workspace was sized for")
+        return moe_forward(x, logits, self.bias, self.w13, self.s13, self.w2, self.s2,
+                           self.num_groups, self.topk_group, self.top_k, self.scoring,
+                           self.renormalize, self.rsf, out=out, workspace=self.workspace,
+                           stream=stream)
+
+    def forward_host(self, x_host, logits_host, out_host, stream=None):
+        return moe_forward_host(x_host, logits_host, self.bias, self.w13, self.s13, self.w2,
+                                self.s2, self.num_groups, self.topk_group, self.top_k,
+                                self.scoring, self.renormalize, self.rsf, out_host,
+                                self.workspace, stream=stream)

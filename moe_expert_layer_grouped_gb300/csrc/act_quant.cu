@@ -1,0 +1,59 @@
+// moe_act_quant: per-token FP8 requantisation of the SiLU*mul output
+// ("Support token-level quantization for EP MoE", sglang #6782, Changelog
+// and Code Review: down_input is requantised per token, giving
+// w2_input_scale). One warp per row, 128-bit loads: pass 1 reduces the row's
+// amax (skipped when the GEMM epilogue supplied it), pass 2 re-reads the row
+// (an L1 hit) and writes the codes.
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int kWarps = 8;
+
+__global__ void __launch_bounds__(kWarps * 32)
+    act_quant_kernel(const __nv_bfloat16* __restrict__ h, const float* __restrict__ row_amax,
+                     int M, int I, uint8_t* __restrict__ q, float* __restrict__ scale) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t row = (int64_t)blockIdx.x * kWarps + warp;
+  if (row >= M) return;
+  const int nvec = I >> 3;
+  const uint4* hr = reinterpret_cast<const uint4*>(h + row * I);
+  float amax;
+  if (row_amax != nullptr) {
+    amax = __ldg(row_amax + row);
+  } else {
+    amax = 0.0f;
+#pragma unroll 4
+    for (int i = lane; i < nvec; i += 32) {
+      float f[8];
+      bf16x8_to_f32(__ldg(hr + i), f);
+      amax = absmax8(f, amax);
+    }
+    amax = warp_max(amax);
+  }
+  const float sc = token_scale(amax);
+  if (lane == 0) scale[row] = sc;
+  uint2* qr = reinterpret_cast<uint2*>(q + row * I);
+#pragma unroll 4
+  for (int i = lane; i < nvec; i += 32) {
+    float f[8];
+    bf16x8_to_f32(__ldg(hr + i), f);
+    qr[i] = quant8(f, sc);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_act_quant(const void* h, const float* row_amax, int M, int I, void* q,
+                             float* scale, cudaStream_t st) {
+  if (M == 0) return cudaSuccess;
+  const int blocks = (M + kWarps - 1) / kWarps;
+  act_quant_kernel<<<blocks, kWarps * 32, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(h),
+                                                   row_amax, M, I,
+                                                   reinterpret_cast<uint8_t*>(q), scale);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

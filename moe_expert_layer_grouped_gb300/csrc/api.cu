@@ -1,0 +1,344 @@
+// C ABI of the MoE layer forward: argument validation, workspace layout and
+// the one-stream orchestration of moe_forward. Declarations and the meaning
+// of every argument are in include/moe_gb300.h.
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+// The device error word: written by kernels that detect a fault, read and
+// cleared by moe_device_status().
+static __device__ int g_device_error;
+
+int* device_error_word() {
+  static std::mutex mu;
+  static int* addr[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lk(mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+    addr[dev] = static_cast<int*>(p);
+  }
+  return addr[dev];
+}
+
+int sm_count() {
+  static std::mutex mu;
+  static int count[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+  std::lock_guard<std::mutex> lk(mu);
+  if (count[dev] == 0) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    count[dev] = n > 0 ? n : 1;
+  }
+  return count[dev];
+}
+
+namespace {
+
+constexpr int kMaxE = 1024;
+constexpr int kMaxK = 32;
+constexpr int kMaxH = 16384;  // permute_quant keeps a row in registers
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool ok_ptr(const void* p) { return p != nullptr && aligned16(p); }
+
+moe_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return MOE_OK;
+  if (e == cudaErrorNotSupported) return MOE_ERR_UNSUPPORTED;
+  return MOE_ERR_CUDA;
+}
+
+moe_status check_gate(const float* logits, const float* bias, int T, int E, int G, int TG,
+                      int K, int scoring, const int32_t* ids, const float* w) {
+  if (T < 0 || E < 1 || G < 1 || TG < 1 || K < 1) return MOE_ERR_INVALID_ARG;
+  if (E % G != 0 || TG > G || K > TG * (E / G)) return MOE_ERR_INVALID_ARG;
+  if (scoring != MOE_SCORE_SIGMOID && scoring != MOE_SCORE_SOFTMAX) return MOE_ERR_INVALID_ARG;
+  if (E > kMaxE || K > kMaxK || G > 64) return MOE_ERR_UNSUPPORTED;
+  if (scoring == MOE_SCORE_SOFTMAX && (bias != nullptr || G != 1)) return MOE_ERR_UNSUPPORTED;
+  if (T > 0 && (!ok_ptr(logits) || !ok_ptr(ids) || !ok_ptr(w))) return MOE_ERR_INVALID_ARG;
+  if (bias != nullptr && !aligned16(bias)) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+moe_status check_permute(const void* x, const int32_t* ids, int T, int H, int E, int K,
+                         const void* a_q, const float* sa, const int32_t* s2d,
+                         const int32_t* offsets, const void* ws, size_t ws_bytes) {
+  if (T < 0 || H < 1 || E < 1 || K < 1) return MOE_ERR_INVALID_ARG;
+  if (H % 32 != 0) return MOE_ERR_INVALID_ARG;
+  if (E > kMaxE || K > kMaxK || H > kMaxH) return MOE_ERR_UNSUPPORTED;
+  if ((int64_t)T * K >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
+  if (!ok_ptr(offsets)) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!ok_ptr(x) || !ok_ptr(ids) || !ok_ptr(a_q) || !ok_ptr(sa) || !ok_ptr(s2d)))
+    return MOE_ERR_INVALID_ARG;
+  const size_t need = permute_ws_bytes(T, E);
+  if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0 || ws_bytes < need)
+    return MOE_ERR_WORKSPACE;
+  return MOE_OK;
+}
+
+moe_status check_gemm(const void* A, const float* sa, const void* B, const float* sb,
+                      const int32_t* offsets, int M, int N, int Kd, int E, int epi,
+                      const void* C, const float* row_amax) {
+  if (M < 0 || N < 1 || Kd < 1 || E < 1) return MOE_ERR_INVALID_ARG;
+  if (epi != MOE_EPI_BF16 && epi != MOE_EPI_SILU_MUL) return MOE_ERR_INVALID_ARG;
+  if (Kd % 32 != 0 || N % 32 != 0) return MOE_ERR_INVALID_ARG;
+  if (epi == MOE_EPI_SILU_MUL && N % 64 != 0) return MOE_ERR_INVALID_ARG;
+  if (E > kMaxE) return MOE_ERR_UNSUPPORTED;
+  if ((int64_t)E * N >= ((int64_t)1 << 31) || (int64_t)M >= ((int64_t)1 << 31))
+    return MOE_ERR_UNSUPPORTED;
+  if (!ok_ptr(offsets) || !ok_ptr(B) || !ok_ptr(sb)) return MOE_ERR_INVALID_ARG;
+  if (M > 0 && (!ok_ptr(A) || !ok_ptr(sa) || !ok_ptr(C))) return MOE_ERR_INVALID_ARG;
+  if (row_amax != nullptr && !aligned16(row_amax)) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+// moe_forward's workspace: every intermediate, 256-byte aligned pieces.
+struct FwdLayout {
+  size_t ids, w, perm, offsets, s2d, sa, sa2, a_q, h, q2, down, x_in, logits_in, out, total;
+};
+
+FwdLayout fwd_layout(int T, int H, int I, int E, int K) {
+  FwdLayout L;
+  const size_t M = (size_t)T * K;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o += align_up(bytes > 0 ? bytes : 1);
+    return at;
+  };
+  L.ids = take(M * 4);
+  L.w = take(M * 4);
+  L.perm = take(permute_ws_bytes(T, E));
+  L.offsets = take((size_t)(E + 1) * 4);
+  L.s2d = take(M * 4);
+  L.sa = take(M * 4);
+  L.sa2 = take(M * 4);
+  L.a_q = take(M * (size_t)H);
+  L.h = take(M * (size_t)I * 2);
+  L.q2 = take(M * (size_t)I);
+  L.down = take(M * (size_t)H * 2);
+  L.x_in = take((size_t)T * H * 2);
+  L.logits_in = take((size_t)T * E * 4);
+  L.out = take((size_t)T * H * 2);
+  L.total = o;
+  return L;
+}
+
+template <typename Tp>
+Tp* at(void* ws, size_t off) {
+  return reinterpret_cast<Tp*>(static_cast<char*>(ws) + off);
+}
+
+moe_status check_forward(const void* x, const float* logits, const float* bias, const void* w13,
+                         const float* s13, const void* w2, const float* s2, int T, int H, int I,
+                         int E, int G, int TG, int K, int scoring, const void* out,
+                         const void* ws, size_t ws_bytes) {
+  if (H < 1 || I < 1 || H % 32 != 0 || I % 32 != 0) return MOE_ERR_INVALID_ARG;
+  if (H > kMaxH) return MOE_ERR_UNSUPPORTED;
+  // the gate check without its output pointers (they live in the workspace)
+  if (T < 0 || E < 1 || G < 1 || TG < 1 || K < 1) return MOE_ERR_INVALID_ARG;
+  if (E % G != 0 || TG > G || K > TG * (E / G)) return MOE_ERR_INVALID_ARG;
+  if (scoring != MOE_SCORE_SIGMOID && scoring != MOE_SCORE_SOFTMAX) return MOE_ERR_INVALID_ARG;
+  if (E > kMaxE || K > kMaxK || G > 64) return MOE_ERR_UNSUPPORTED;
+  if (scoring == MOE_SCORE_SOFTMAX && (bias != nullptr || G != 1)) return MOE_ERR_UNSUPPORTED;
+  if ((int64_t)E * 2 * I >= ((int64_t)1 << 31) || (int64_t)E * H >= ((int64_t)1 << 31) ||
+      (int64_t)T * K >= ((int64_t)1 << 31))
+    return MOE_ERR_UNSUPPORTED;
+  if (!ok_ptr(w13) || !ok_ptr(s13) || !ok_ptr(w2) || !ok_ptr(s2)) return MOE_ERR_INVALID_ARG;
+  if (bias != nullptr && !aligned16(bias)) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!ok_ptr(x) || !ok_ptr(logits) || !ok_ptr(out))) return MOE_ERR_INVALID_ARG;
+  if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0 ||
+      ws_bytes < fwd_layout(T, H, I, E, K).total)
+    return MOE_ERR_WORKSPACE;
+  return MOE_OK;
+}
+
+moe_status run_forward(const void* x, const float* logits, const float* bias, const void* w13,
+                       const float* s13, const void* w2, const float* s2, int T, int H, int I,
+                       int E, int G, int TG, int K, int scoring, int renorm, float rsf,
+                       void* out, void* ws, cudaStream_t st) {
+  const FwdLayout L = fwd_layout(T, H, I, E, K);
+  int* err = device_error_word();
+  if (err == nullptr) return MOE_ERR_CUDA;
+  const int M = T * K;
+  int32_t* ids = at<int32_t>(ws, L.ids);
+  float* w = at<float>(ws, L.w);
+  int32_t* offsets = at<int32_t>(ws, L.offsets);
+  int32_t* s2d = at<int32_t>(ws, L.s2d);
+  float* sa = at<float>(ws, L.sa);
+  float* sa2 = at<float>(ws, L.sa2);
+  void* a_q = at<void>(ws, L.a_q);
+  void* h = at<void>(ws, L.h);
+  void* q2 = at<void>(ws, L.q2);
+  void* down = at<void>(ws, L.down);
+  cudaError_t e;
+  if ((e = launch_gate(logits, bias, T, E, G, TG, K, scoring, renorm, rsf, ids, w, st)))
+    return cuda_status(e);
+  if ((e = launch_permute_quant(x, ids, T, H, E, K, a_q, sa, s2d, offsets, at<void>(ws, L.perm),
+                                err, st)))
+    return cuda_status(e);
+  if ((e = launch_grouped_gemm(a_q, sa, w13, s13, offsets, M, 2 * I, H, E, MOE_EPI_SILU_MUL, h,
+                               nullptr, err, st)))
+    return cuda_status(e);
+  if ((e = launch_act_quant(h, nullptr, M, I, q2, sa2, st))) return cuda_status(e);
+  if ((e = launch_grouped_gemm(q2, sa2, w2, s2, offsets, M, H, I, E, MOE_EPI_BF16, down, nullptr,
+                               err, st)))
+    return cuda_status(e);
+  if ((e = launch_unpermute_sum(down, s2d, w, T, K, H, out, err, st))) return cuda_status(e);
+  return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+const char* moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
+    case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+    case MOE_ERR_DEVICE: return "MOE_ERR_DEVICE";
+  }
+  return "unknown moe_status";
+}
+
+int moe_abi_version(void) { return (1 << 16) | 0; }
+
+moe_status moe_gate(const float* logits, const float* bias, int T, int E, int num_groups,
+                    int topk_group, int top_k, int scoring, int renormalize,
+                    float routed_scaling_factor, int32_t* topk_ids, float* topk_w,
+                    void* stream) {
+  moe_status s = check_gate(logits, bias, T, E, num_groups, topk_group, top_k, scoring, topk_ids,
+                            topk_w);
+  if (s != MOE_OK) return s;
+  return cuda_status(launch_gate(logits, bias, T, E, num_groups, topk_group, top_k, scoring,
+                                 renormalize, routed_scaling_factor, topk_ids, topk_w,
+                                 static_cast<cudaStream_t>(stream)));
+}
+
+size_t moe_permute_workspace_size(int T, int E, int K) {
+  (void)K;
+  if (T < 0 || E < 1) return 0;
+  return permute_ws_bytes(T, E);
+}
+
+moe_status moe_permute_quant(const void* x, const int32_t* topk_ids, int T, int H, int E, int K,
+                             void* a_q, float* scale_a, int32_t* src2dst, int32_t* offsets,
+                             void* ws, size_t ws_bytes, void* stream) {
+  moe_status s = check_permute(x, topk_ids, T, H, E, K, a_q, scale_a, src2dst, offsets, ws,
+                               ws_bytes);
+  if (s != MOE_OK) return s;
+  int* err = device_error_word();
+  if (err == nullptr) return MOE_ERR_CUDA;
+  return cuda_status(launch_permute_quant(x, topk_ids, T, H, E, K, a_q, scale_a, src2dst,
+                                          offsets, ws, err, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_grouped_gemm(const void* A, const float* scale_a, const void* B,
+                            const float* scale_b, const int32_t* offsets, int M, int N, int Kd,
+                            int E, int epilogue, void* C, float* row_amax, void* stream) {
+  moe_status s = check_gemm(A, scale_a, B, scale_b, offsets, M, N, Kd, E, epilogue, C, row_amax);
+  if (s != MOE_OK) return s;
+  int* err = device_error_word();
+  if (err == nullptr) return MOE_ERR_CUDA;
+  return cuda_status(launch_grouped_gemm(A, scale_a, B, scale_b, offsets, M, N, Kd, E, epilogue,
+                                         C, row_amax, err, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_act_quant(const void* h, const float* row_amax, int M, int I, void* q,
+                         float* scale, void* stream) {
+  if (M < 0 || I < 1 || I % 32 != 0) return MOE_ERR_INVALID_ARG;
+  if (M > 0 && (!ok_ptr(h) || !ok_ptr(q) || !ok_ptr(scale))) return MOE_ERR_INVALID_ARG;
+  if (row_amax != nullptr && !aligned16(row_amax)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_act_quant(h, row_amax, M, I, q, scale,
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_unpermute_sum(const void* down, const int32_t* src2dst, const float* topk_w,
+                             int T, int K, int H, void* out, void* stream) {
+  if (T < 0 || K < 1 || H < 1 || H % 8 != 0) return MOE_ERR_INVALID_ARG;
+  if (K > kMaxK) return MOE_ERR_UNSUPPORTED;
+  if ((int64_t)T * K >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
+  if (T > 0 && (!ok_ptr(down) || !ok_ptr(src2dst) || !ok_ptr(topk_w) || !ok_ptr(out)))
+    return MOE_ERR_INVALID_ARG;
+  int* err = device_error_word();
+  if (err == nullptr) return MOE_ERR_CUDA;
+  return cuda_status(launch_unpermute_sum(down, src2dst, topk_w, T, K, H, out, err,
+                                          static_cast<cudaStream_t>(stream)));
+}
+
+size_t moe_workspace_size(int T, int H, int I, int E, int K) {
+  if (T < 0 || H < 1 || I < 1 || E < 1 || K < 1) return 0;
+  return fwd_layout(T, H, I, E, K).total;
+}
+
+moe_status moe_forward(const void* x, const float* logits, const float* bias, const void* w13,
+                       const float* s13, const void* w2, const float* s2, int T, int H, int I,
+                       int E, int num_groups, int topk_group, int top_k, int scoring,
+                       int renormalize, float routed_scaling_factor, void* out, void* ws,
+                       size_t ws_bytes, void* stream) {
+  moe_status s = check_forward(x, logits, bias, w13, s13, w2, s2, T, H, I, E, num_groups,
+                               topk_group, top_k, scoring, out, ws, ws_bytes);
+  if (s != MOE_OK) return s;
+  if (T == 0) return MOE_OK;
+  return run_forward(x, logits, bias, w13, s13, w2, s2, T, H, I, E, num_groups, topk_group,
+                     top_k, scoring, renormalize, routed_scaling_factor, out, ws,
+                     static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_forward_host(const void* x_host, const float* logits_host, const float* bias,
+                            const void* w13, const float* s13, const void* w2, const float* s2,
+                            int T, int H, int I, int E, int num_groups, int topk_group,
+                            int top_k, int scoring, int renormalize,
+                            float routed_scaling_factor, void* out_host, void* ws,
+                            size_t ws_bytes, void* stream) {
+  if (T > 0 && (x_host == nullptr || logits_host == nullptr || out_host == nullptr))
+    return MOE_ERR_INVALID_ARG;
+  if (ws == nullptr) return MOE_ERR_WORKSPACE;
+  const FwdLayout L = fwd_layout(T < 0 ? 0 : T, H < 1 ? 1 : H, I < 1 ? 1 : I, E < 1 ? 1 : E,
+                                 top_k < 1 ? 1 : top_k);
+  void* x_d = at<void>(ws, L.x_in);
+  float* l_d = at<float>(ws, L.logits_in);
+  void* o_d = at<void>(ws, L.out);
+  moe_status s = check_forward(x_d, l_d, bias, w13, s13, w2, s2, T, H, I, E, num_groups,
+                               topk_group, top_k, scoring, o_d, ws, ws_bytes);
+  if (s != MOE_OK) return s;
+  if (T == 0) return MOE_OK;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t xb = (size_t)T * H * 2, lb = (size_t)T * E * 4;
+  if (cudaMemcpyAsync(x_d, x_host, xb, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+      cudaMemcpyAsync(l_d, logits_host, lb, cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  s = run_forward(x_d, l_d, bias, w13, s13, w2, s2, T, H, I, E, num_groups, topk_group, top_k,
+                  scoring, renormalize, routed_scaling_factor, o_d, ws, st);
+  if (s != MOE_OK) return s;
+  if (cudaMemcpyAsync(out_host, o_d, xb, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+moe_status moe_device_status(int* code) {
+  if (code == nullptr) return MOE_ERR_INVALID_ARG;
+  *code = 0;
+  if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof(int)) != cudaSuccess) return MOE_ERR_CUDA;
+  const int zero = 0;
+  if (cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int)) != cudaSuccess) return MOE_ERR_CUDA;
+  *code = v;
+  return v == 0 ? MOE_OK : MOE_ERR_DEVICE;
+}
+
+}  // extern "C"

@@ -1,0 +1,44 @@
+// Host-side launchers of the kernels, called by the C ABI (api.cu) after it
+// has validated every argument. Each returns the CUDA error of its launch.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace moe {
+
+// Per-device state (device error word, SM count), set up on first use.
+int* device_error_word();
+int sm_count();
+
+constexpr size_t kAlign = 256;
+inline size_t align_up(size_t v, size_t a = kAlign) { return (v + a - 1) / a * a; }
+
+// gate.cu
+cudaError_t launch_gate(const float* logits, const float* bias, int T, int E, int G, int TG,
+                        int K, int scoring, int renorm, float rsf, int32_t* ids, float* w,
+                        cudaStream_t st);
+
+// permute.cu
+size_t permute_ws_bytes(int T, int E);
+cudaError_t launch_permute_quant(const void* x, const int32_t* ids, int T, int H, int E, int K,
+                                 void* a_q, float* scale_a, int32_t* src2dst, int32_t* offsets,
+                                 void* ws, int* err, cudaStream_t st);
+
+// gemm.cu
+// Returns cudaErrorNotSupported when the TMA descriptors cannot be encoded.
+cudaError_t launch_grouped_gemm(const void* A, const float* scale_a, const void* B,
+                                const float* scale_b, const int32_t* offsets, int M, int N,
+                                int Kd, int E, int epilogue, void* C, float* row_amax, int* err,
+                                cudaStream_t st);
+
+// act_quant.cu
+cudaError_t launch_act_quant(const void* h, const float* row_amax, int M, int I, void* q,
+                             float* scale, cudaStream_t st);
+
+// unpermute.cu
+cudaError_t launch_unpermute_sum(const void* down, const int32_t* src2dst, const float* w,
+                                 int T, int K, int H, void* out, int* err, cudaStream_t st);
+
+}  // namespace moe

@@ -1,0 +1,137 @@
+"""The C-ABI library: it loads without a GPU, exports every entry point the
+header declares (and nothing internal), and rejects invalid arguments with
+the documented status codes before touching the device. CPU only."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import moe_expert_layer_grouped_gb300 as moe
+from moe_expert_layer_grouped_gb300 import build as cuda_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe_gb300.h")
+
+OK, INVALID, UNSUPPORTED, WORKSPACE, CUDA = 0, -1, -2, -3, -4
+
+
+@pytest.fixture(scope="module")
+def lib():
+    cuda_build.build()
+    return moe.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for want in ["moe_gate", "moe_permute_quant", "moe_grouped_gemm", "moe_act_quant",
+                 "moe_unpermute_sum", "moe_forward", "moe_forward_host", "moe_workspace_size",
+                 "moe_permute_workspace_size", "moe_device_status", "moe_status_string",
+                 "moe_abi_version"]:
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", moe.library_path()],
+                         capture_output=True, text=True, check=True).stdout
+    exported = {l.split()[-1] for l in out.splitlines() if " T " in l}
+    assert set(declared_functions()) <= exported
+    # internal launchers stay hidden
+    assert not any("launch_" in s for s in exported)
+
+
+def test_status_strings_and_version(lib):
+    assert lib.moe_status_string(0) == b"MOE_OK"
+    assert lib.moe_status_string(-3) == b"MOE_ERR_WORKSPACE"
+    assert lib.moe_abi_version() >> 16 == 1
+
+
+P = ctypes.c_void_p
+GOOD = P(0x10000)      # aligned placeholders: never dereferenced, the calls
+ODD = P(0x10008)       # below fail validation before any device work
+
+
+def test_gate_argument_validation(lib):
+    g = lib.moe_gate
+    # E % G != 0, TG > G, K > TG*E/G, K > 32, E > 1024, bad scoring
+    assert g(GOOD, None, 4, 10, 3, 1, 2, 0, 1, 1.0, GOOD, GOOD, None) == INVALID
+    assert g(GOOD, None, 4, 8, 4, 5, 2, 0, 1, 1.0, GOOD, GOOD, None) == INVALID
+    assert g(GOOD, None, 4, 8, 4, 1, 3, 0, 1, 1.0, GOOD, GOOD, None) == INVALID
+    assert g(GOOD, None, 4, 64, 1, 1, 33, 0, 1, 1.0, GOOD, GOOD, None) == UNSUPPORTED
+    assert g(GOOD, None, 4, 2048, 1, 1, 2, 0, 1, 1.0, GOOD, GOOD, None) == UNSUPPORTED
+    assert g(GOOD, None, 4, 8, 1, 1, 2, 7, 1, 1.0, GOOD, GOOD, None) == INVALID
+    # softmax takes no bias and no groups
+    assert g(GOOD, GOOD, 4, 8, 1, 1, 2, 1, 1, 1.0, GOOD, GOOD, None) == UNSUPPORTED
+    assert g(GOOD, None, 4, 8, 2, 1, 2, 1, 1, 1.0, GOOD, GOOD, None) == UNSUPPORTED
+    # null / misaligned pointers
+    assert g(None, None, 4, 8, 1, 1, 2, 0, 1, 1.0, GOOD, GOOD, None) == INVALID
+    assert g(ODD, None, 4, 8, 1, 1, 2, 0, 1, 1.0, GOOD, GOOD, None) == INVALID
+    assert g(GOOD, ODD, 4, 8, 1, 1, 2, 0, 1, 1.0, GOOD, GOOD, None) == INVALID
+
+
+def test_permute_argument_validation(lib):
+    f = lib.moe_permute_quant
+    need = lib.moe_permute_workspace_size(100, 8, 2)
+    assert need > 0
+    args = lambda **kw: [kw.get("x", GOOD), GOOD, kw.get("T", 100), kw.get("H", 64), 8,
+                         kw.get("K", 2), GOOD, GOOD, GOOD, GOOD, kw.get("ws", P(0x100000)),
+                         kw.get("wsb", need), None]
+    assert f(*args(H=48)) == INVALID                       # H % 32
+    assert f(*args(K=33)) == UNSUPPORTED
+    assert f(*args(H=32768)) == UNSUPPORTED
+    assert f(*args(x=None)) == INVALID
+    assert f(*args(wsb=need - 1)) == WORKSPACE
+    assert f(*args(ws=None)) == WORKSPACE
+    assert f(*args(ws=P(0x100010))) == WORKSPACE           # not 256-byte aligned
+
+
+def test_gemm_act_unpermute_validation(lib):
+    g = lib.moe_grouped_gemm
+    assert g(GOOD, GOOD, GOOD, GOOD, GOOD, 64, 48, 64, 4, 0, GOOD, None, None) == INVALID
+    assert g(GOOD, GOOD, GOOD, GOOD, GOOD, 64, 64, 48, 4, 0, GOOD, None, None) == INVALID
+    assert g(GOOD, GOOD, GOOD, GOOD, GOOD, 64, 96, 64, 4, 1, GOOD, None, None) == INVALID
+    assert g(GOOD, GOOD, GOOD, GOOD, GOOD, 64, 64, 64, 4, 2, GOOD, None, None) == INVALID
+    assert g(GOOD, GOOD, GOOD, GOOD, GOOD, 64, 64, 64, 2048, 0, GOOD, None, None) == UNSUPPORTED
+    assert g(ODD, GOOD, GOOD, GOOD, GOOD, 64, 64, 64, 4, 0, GOOD, None, None) == INVALID
+    a = lib.moe_act_quant
+    assert a(GOOD, None, 10, 48, GOOD, GOOD, None) == INVALID
+    assert a(None, None, 10, 64, GOOD, GOOD, None) == INVALID
+    u = lib.moe_unpermute_sum
+    assert u(GOOD, GOOD, GOOD, 10, 2, 12, GOOD, None) == INVALID
+    assert u(GOOD, GOOD, GOOD, 10, 40, 64, GOOD, None) == UNSUPPORTED
+
+
+def test_forward_validation_and_workspace(lib):
+    f = lib.moe_forward
+    T, H, I, E, K = 16, 128, 64, 8, 2
+    need = lib.moe_workspace_size(T, H, I, E, K)
+    assert need >= T * K * (H + 2 * I + I + 2 * H)
+    assert lib.moe_workspace_size(2 * T, H, I, E, K) > need
+    base = [GOOD, GOOD, None, GOOD, GOOD, GOOD, GOOD, T, H, I, E, 1, 1, K, 1, 1, 1.0, GOOD]
+    assert f(*base, P(0x100000), need - 1, None) == WORKSPACE
+    assert f(*base, None, need, None) == WORKSPACE
+    bad_i = list(base)
+    bad_i[9] = 48
+    assert f(*bad_i, P(0x100000), need, None) == INVALID
+    bad_w = list(base)
+    bad_w[3] = None
+    assert f(*bad_w, P(0x100000), need, None) == INVALID
+    # T == 0 is a valid no-op
+    assert f(None, None, None, GOOD, GOOD, GOOD, GOOD, 0, H, I, E, 1, 1, K, 1, 1, 1.0, None,
+             P(0x100000), lib.moe_workspace_size(0, H, I, E, K), None) == OK
+
+
+def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
+    monkeypatch.setattr(moe, "_lib", None)
+    monkeypatch.setattr(moe, "library_path", lambda: str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="missing"):
+        moe.load()

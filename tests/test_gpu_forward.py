@@ -1,0 +1,192 @@
+"""Whole-layer parity of moe_forward (C ABI, CUDA kernels) against the CPU
+oracle on the five workloads: every token on the small ones, a fixed sample of
+tokens on the large ones (a token's output depends on that token alone), run
+through the same MoELayer call the benchmark times. Plus edge cases: the
+per-row scale regression, guard bands around every output, empty and one-token
+batches, the host-buffer entry point."""
+import numpy as np
+import pytest
+import torch
+
+import moe_expert_layer_grouped_gb300 as moe
+import oracle
+from moe_expert_layer_grouped_gb300 import synth
+
+from gpu_util import assert_parity, bf16_bits, bf16_np
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import __graft_entry__
+    __graft_entry__.build()
+    yield
+    assert moe.moe_device_status() == 0
+
+
+def _layer(wl, d):
+    return moe.MoELayer(d["w13"], d["s13"], d["w2"], d["s2"], d["bias"], wl.num_groups,
+                        wl.topk_group, wl.top_k, wl.scoring, wl.renormalize, wl.rsf, wl.T)
+
+
+def _oracle_tokens(wl, d, tokens):
+    n = {k: (None if v is None else v) for k, v in synth.to_numpy_inputs(d).items()}
+    return oracle.forward_tokens(n["x"], n["logits"], n["bias"], n["w13"], n["s13"], n["w2"],
+                                 n["s2"], wl.num_groups, wl.topk_group, wl.top_k, wl.scoring,
+                                 wl.renormalize, wl.rsf, tokens=tokens)
+
+
+def _check_workload(wl, seed, device_gen, n_sample=None):
+    d = synth.make_inputs(wl, seed=seed, device=DEV if device_gen else "cpu")
+    d = {k: (None if v is None else v.to(DEV)) for k, v in d.items()}
+    layer = _layer(wl, d)
+    out = layer(d["x"], d["logits"])
+    ids, w = moe.moe_gate(d["logits"], d["bias"], wl.num_groups, wl.topk_group, wl.top_k,
+                          wl.scoring, wl.renormalize, wl.rsf)
+    torch.cuda.synchronize()
+    assert moe.moe_device_status() == 0
+    if n_sample is None:
+        tokens = np.arange(wl.T, dtype=np.int64)
+    else:
+        rng = np.random.default_rng(seed)
+        tokens = np.unique(np.concatenate([[0, wl.T - 1],
+                                           rng.choice(wl.T, n_sample, replace=False)]))
+    ref, rids, rw = _oracle_tokens(wl, d, tokens)
+    sel = torch.from_numpy(tokens).to(DEV)
+    assert np.array_equal(ids[sel].cpu().numpy(), rids)
+    assert np.array_equal(w[sel].cpu().numpy(), rw)
+    got = bf16_np(out[sel])
+    return assert_parity(got, ref, wl.name)
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_forward_tiny(seed):
+    _check_workload(synth.WORKLOADS["tiny"], seed, device_gen=False)
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_forward_dsv3_decode_t128(seed):
+    _check_workload(synth.WORKLOADS["dsv3_decode_t128"], seed, device_gen=True,
+                    n_sample=None if seed == 0 else 32)
+
+
+@pytest.mark.parametrize("name", ["dsv3_prefill_t8192", "mixtral_t4096", "dsv3_skewed_t16384"])
+def test_forward_large_sampled(name):
+    _check_workload(synth.WORKLOADS[name], 0, device_gen=True, n_sample=40)
+
+
+@pytest.mark.parametrize("T,H,I,E,G,TG,K,scoring,rsf", [
+    (1, 256, 128, 16, 4, 2, 4, synth.SIGMOID, 2.5),      # one token
+    (5, 128, 64, 1, 1, 1, 1, synth.SOFTMAX, 1.0),        # dense: E=1, K=1
+    (300, 384, 192, 24, 4, 2, 6, synth.SIGMOID, 2.5),    # ragged tiles
+    (129, 512, 256, 3, 1, 1, 3, synth.SIGMOID, 1.0),     # every expert takes every token
+])
+def test_forward_shapes(T, H, I, E, G, TG, K, scoring, rsf):
+    bias = "none" if scoring == synth.SOFTMAX else "normal"
+    wl = synth.Workload("shape", T, H, I, E, G, TG, K, scoring, True, rsf, bias)
+    _check_workload(wl, 3, device_gen=False)
+
+
+def test_forward_rsf_linear_and_empty_batch():
+    wl = synth.Workload("lin", 64, 256, 128, 16, 4, 2, 4, synth.SIGMOID, True, 1.0, "normal")
+    d = {k: (None if v is None else v.to(DEV)) for k, v in synth.make_inputs(wl, 4).items()}
+    args = (d["w13"], d["s13"], d["w2"], d["s2"], 4, 2, 4, synth.SIGMOID, True)
+    o1 = moe.moe_forward(d["x"], d["logits"], d["bias"], *args[:4], *args[4:], 1.0)
+    o2 = moe.moe_forward(d["x"], d["logits"], d["bias"], *args[:4], *args[4:], 2.0)
+    # rsf scales the weights exactly by 2; only the final bf16 rounding differs
+    assert torch.equal(o2, (o1.float() * 2).to(torch.bfloat16))
+    empty = moe.moe_forward(d["x"][:0], d["logits"][:0], d["bias"], *args[:4], *args[4:], 1.0)
+    assert empty.shape == (0, 256)
+
+
+def test_row_scale_regression():
+    """Tokens routed to the same experts with magnitudes 1e-3..1e3: each
+    token's output must be right relative to its own size, which only a
+    per-row scale_a gives (sglang #6772: scale_a indexed by expert id made
+    EPMoE wrong without block quantisation)."""
+    wl = synth.Workload("rows", 64, 256, 128, 4, 1, 1, 2, synth.SIGMOID, True, 1.0, "none")
+    d = synth.make_inputs(wl, 5)
+    d["x"] = (d["x"].float() * (10.0 ** torch.linspace(-3, 3, 64)).unsqueeze(1)).to(torch.bfloat16)
+    d["logits"][:, :2] += 10.0  # everyone picks experts 0 and 1
+    dd = {k: (None if v is None else v.to(DEV)) for k, v in d.items()}
+    out = _layer(wl, dd)(dd["x"], dd["logits"])
+    ref, _, _ = _oracle_tokens(wl, d, np.arange(64))
+    got = bf16_np(out)
+    per_token = np.abs(got - ref).max(1) / np.abs(ref).max(1)
+    assert per_token.max() <= 2e-2, per_token.max()
+
+
+def test_guard_bands_around_every_output():
+    """Outputs written into the middle of larger buffers filled with a
+    sentinel: nothing outside the documented extents changes."""
+    T, H, I, E, K = 70, 256, 128, 8, 2
+    wl = synth.Workload("guard", T, H, I, E, 1, 1, K, synth.SOFTMAX, True, 1.0, "none")
+    d = {k: (None if v is None else v.to(DEV)) for k, v in synth.make_inputs(wl, 6).items()}
+    G = 4096  # guard bytes on each side
+
+    def guarded(nbytes):
+        buf = torch.full((nbytes + 2 * G,), 0xA5, dtype=torch.uint8, device=DEV)
+        return buf, buf[G:G + nbytes]
+
+    def intact(buf, nbytes):
+        return bool((buf[:G] == 0xA5).all() and (buf[G + nbytes:] == 0xA5).all())
+
+    M = T * K
+    b_ids, ids = guarded(M * 4)
+    b_w, w = guarded(M * 4)
+    moe.moe_gate(d["logits"], None, 1, 1, K, synth.SOFTMAX, True, 1.0,
+                 topk_ids=ids.view(torch.int32).view(T, K), topk_w=w.view(torch.float32).view(T, K))
+    ids_t, w_t = ids.view(torch.int32).view(T, K), w.view(torch.float32).view(T, K)
+    b_aq, aq = guarded(M * H)
+    b_sa, sa = guarded(M * 4)
+    b_sd, sd = guarded(M * 4)
+    b_off, off = guarded((E + 1) * 4)
+    moe.moe_permute_quant(d["x"], ids_t, E, a_q=aq.view(M, H), scale_a=sa.view(torch.float32),
+                          src2dst=sd.view(torch.int32), offsets=off.view(torch.int32))
+    b_h, h = guarded(M * I * 2)
+    moe.moe_grouped_gemm(aq.view(M, H), sa.view(torch.float32), d["w13"], d["s13"],
+                         off.view(torch.int32), moe.EPI_SILU_MUL,
+                         C=h.view(torch.bfloat16).view(M, I))
+    b_q2, q2 = guarded(M * I)
+    b_s2, s2 = guarded(M * 4)
+    moe.moe_act_quant(h.view(torch.bfloat16).view(M, I), q=q2.view(M, I),
+                      scale=s2.view(torch.float32))
+    b_dn, dn = guarded(M * H * 2)
+    moe.moe_grouped_gemm(q2.view(M, I), s2.view(torch.float32), d["w2"], d["s2"],
+                         off.view(torch.int32), moe.EPI_BF16, C=dn.view(torch.bfloat16).view(M, H))
+    b_out, out = guarded(T * H * 2)
+    moe.moe_unpermute_sum(dn.view(torch.bfloat16).view(M, H), sd.view(torch.int32), w_t,
+                          out=out.view(torch.bfloat16).view(T, H))
+    torch.cuda.synchronize()
+    for buf, n in [(b_ids, M * 4), (b_w, M * 4), (b_aq, M * H), (b_sa, M * 4), (b_sd, M * 4),
+                   (b_off, (E + 1) * 4), (b_h, M * I * 2), (b_q2, M * I), (b_s2, M * 4),
+                   (b_dn, M * H * 2), (b_out, T * H * 2)]:
+        assert intact(buf, n)
+    # and the step-by-step chain equals moe_forward
+    full = moe.moe_forward(d["x"], d["logits"], None, d["w13"], d["s13"], d["w2"], d["s2"], 1, 1,
+                           K, synth.SOFTMAX, True, 1.0)
+    assert torch.equal(full, out.view(torch.bfloat16).view(T, H))
+
+
+def test_forward_host_buffers_match_device_call():
+    wl = synth.Workload("host", 32, 1024, 512, 32, 4, 2, 4, synth.SIGMOID, True, 2.5, "normal")
+    d = {k: (None if v is None else v.to(DEV)) for k, v in synth.make_inputs(wl, 7, DEV).items()}
+    layer = _layer(wl, d)
+    ref = layer(d["x"], d["logits"]).cpu()
+    xh = d["x"].cpu().pin_memory()
+    lh = d["logits"].cpu().pin_memory()
+    oh = torch.empty((wl.T, wl.H), dtype=torch.bfloat16).pin_memory()
+    layer.forward_host(xh, lh, oh)
+    torch.cuda.current_stream().synchronize()
+    assert torch.equal(oh, ref)
+
+
+def test_repeated_calls_are_deterministic():
+    wl = synth.WORKLOADS["dsv3_decode_t128"]
+    d = {k: (None if v is None else v.to(DEV)) for k, v in synth.make_inputs(wl, 0, DEV).items()}
+    layer = _layer(wl, d)
+    a = layer(d["x"], d["logits"]).clone()
+    for _ in range(3):
+        assert torch.equal(layer(d["x"], d["logits"]), a)
