@@ -132,6 +132,39 @@ MOE_API moe_status moe_permute_quant(const void* x, const int32_t* topk_ids, int
                              int32_t* src2dst, int32_t* offsets, void* ws,
                              size_t ws_bytes, void* stream);
 
+/* Size of the fixed device scratch behind moe_permute_quant_noalloc. */
+#define MOE_PERMUTE_NOALLOC_SCRATCH_BYTES ((size_t)4 << 20)
+
+/*
+ * moe_permute_quant_noalloc — moe_permute_quant without a workspace argument.
+ * The pages have no counterpart: this entry point exists for callers that
+ * cannot allocate device memory and have no workspace to hand over, such as
+ * code running as a plug-in inside another runtime that owns all device
+ * memory and passes it only its input and output buffers, or code on a
+ * latency-critical path where an allocation (which can synchronise the
+ * device) is not acceptable. It computes exactly what moe_permute_quant
+ * computes, with the same arguments minus ws / ws_bytes.
+ *   Scratch: a fixed array of MOE_PERMUTE_NOALLOC_SCRATCH_BYTES (4 MiB) in
+ *   the library's device memory, reserved on every GPU that loads the
+ *   library until the process exits. The call needs
+ *   moe_permute_workspace_size(T,E,K) <= MOE_PERMUTE_NOALLOC_SCRATCH_BYTES
+ *   (e.g. T <= 65536 tokens at E = 256); larger sizes return
+ *   MOE_ERR_WORKSPACE and launch nothing.
+ *   Set-up: the first call on each device looks up the array's device
+ *   address with that device current; make that first call before any
+ *   stream capture.
+ *   Sharing: every call uses the same array and leaves its contents behind.
+ *   Nothing in it has to start at zero (a call writes every scratch entry it
+ *   later reads). Calls that overlap on the GPU (different streams, or
+ *   unordered calls from several threads) race on the array and produce
+ *   wrong results: order them.
+ *   It calls no cudaMalloc, cudaFree or other allocating routine.
+ */
+MOE_API moe_status moe_permute_quant_noalloc(const void* x, const int32_t* topk_ids, int T,
+                                             int H, int E, int K, void* a_q, float* scale_a,
+                                             int32_t* src2dst, int32_t* offsets,
+                                             void* stream);
+
 /*
  * moe_grouped_gemm — FP8 grouped GEMM over expert row segments, tcgen05.
  * [P1] Highlights and [P2] Changelog: within expert e's rows

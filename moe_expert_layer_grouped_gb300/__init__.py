@@ -17,7 +17,7 @@ import os
 __all__ = [
     "MoEError", "SIGMOID", "SOFTMAX", "EPI_BF16", "EPI_SILU_MUL", "library_path", "load",
     "moe_gate", "moe_permute_quant", "moe_permute_workspace_size", "moe_grouped_gemm",
-    "moe_act_quant", "moe_unpermute_sum", "moe_workspace_size", "moe_forward",
+    "moe_permute_quant_noalloc", "moe_act_quant", "moe_unpermute_sum", "moe_workspace_size", "moe_forward",
     "moe_forward_host", "moe_device_status", "MoELayer",
 ]
 
@@ -54,6 +54,7 @@ _SIGNATURES = {
     "moe_gate": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P]),
     "moe_permute_workspace_size": (_SZ, [_I, _I, _I]),
     "moe_permute_quant": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_permute_quant_noalloc": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
     "moe_grouped_gemm": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P]),
     "moe_act_quant": (_I, [_P, _P, _I, _I, _P, _P, _P]),
     "moe_unpermute_sum": (_I, [_P, _P, _P, _I, _I, _I, _P, _P]),
@@ -153,6 +154,20 @@ def moe_permute_quant(x, topk_ids, E, a_q=None, scale_a=None, src2dst=None, offs
         _ptr(x), _ptr(topk_ids), T, H, E, K, _ptr(_u8(a_q)), _ptr(scale_a), _ptr(src2dst),
         _ptr(offsets), _ptr(workspace), workspace.numel() * workspace.element_size(),
         _stream(stream)))
+    return a_q, scale_a, src2dst, offsets
+
+
+def moe_permute_quant_noalloc(x, topk_ids, E, a_q, scale_a, src2dst, offsets, stream=None):
+    """moe_permute_quant for callers that cannot allocate: the caller passes
+    every output buffer and the library uses its fixed device scratch instead
+    of a workspace (see include/moe_gb300.h for the size limit and the rule
+    that overlapping calls race). Allocates nothing."""
+    _need_cuda(x, topk_ids, a_q, scale_a, src2dst, offsets)
+    T, H = x.shape
+    K = topk_ids.shape[1]
+    _check("moe_permute_quant_noalloc", load().moe_permute_quant_noalloc(
+        _ptr(x), _ptr(topk_ids), T, H, E, K, _ptr(_u8(a_q)), _ptr(scale_a), _ptr(src2dst),
+        _ptr(offsets), _stream(stream)))
     return a_q, scale_a, src2dst, offsets
 
 

@@ -246,6 +246,26 @@ moe_status moe_permute_quant(const void* x, const int32_t* topk_ids, int T, int 
                                           offsets, ws, err, static_cast<cudaStream_t>(stream)));
 }
 
+moe_status moe_permute_quant_noalloc(const void* x, const int32_t* topk_ids, int T, int H,
+                                     int E, int K, void* a_q, float* scale_a, int32_t* src2dst,
+                                     int32_t* offsets, void* stream) {
+  // the same checks as moe_permute_quant, with the fixed scratch as workspace;
+  // all of them come before any CUDA call
+  if (T < 0 || H < 1 || E < 1 || K < 1 || H % 32 != 0) return MOE_ERR_INVALID_ARG;
+  if (E > kMaxE || K > kMaxK || H > kMaxH) return MOE_ERR_UNSUPPORTED;
+  if ((int64_t)T * K >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
+  if (!ok_ptr(offsets)) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!ok_ptr(x) || !ok_ptr(topk_ids) || !ok_ptr(a_q) || !ok_ptr(scale_a) ||
+                !ok_ptr(src2dst)))
+    return MOE_ERR_INVALID_ARG;
+  if (permute_ws_bytes(T, E) > MOE_PERMUTE_NOALLOC_SCRATCH_BYTES) return MOE_ERR_WORKSPACE;
+  void* ws = permute_static_scratch();
+  int* err = device_error_word();
+  if (ws == nullptr || err == nullptr) return MOE_ERR_CUDA;
+  return cuda_status(launch_permute_quant(x, topk_ids, T, H, E, K, a_q, scale_a, src2dst,
+                                          offsets, ws, err, static_cast<cudaStream_t>(stream)));
+}
+
 moe_status moe_grouped_gemm(const void* A, const float* scale_a, const void* B,
                             const float* scale_b, const int32_t* offsets, int M, int N, int Kd,
                             int E, int epilogue, void* C, float* row_amax, void* stream) {

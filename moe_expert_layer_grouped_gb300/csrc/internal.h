@@ -26,6 +26,10 @@ cudaError_t launch_permute_quant(const void* x, const int32_t* ids, int T, int H
                                  void* a_q, float* scale_a, int32_t* src2dst, int32_t* offsets,
                                  void* ws, int* err, cudaStream_t st);
 
+// permute.cu: device address of the fixed scratch used by
+// moe_permute_quant_noalloc on the current device (nullptr on failure).
+void* permute_static_scratch();
+
 // gemm.cu
 // Returns cudaErrorNotSupported when the TMA descriptors cannot be encoded.
 cudaError_t launch_grouped_gemm(const void* A, const float* scale_a, const void* B,

@@ -13,6 +13,8 @@
 //     counting sort by expert in ascending token order -- and its row is
 //     loaded once (128-bit vectors, kept in registers), reduced to amax,
 //     quantised and stored to all K destinations with its scale.
+#include <mutex>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -184,6 +186,27 @@ void launch_quant(const void* x, const int32_t* ids, const uint32_t* bits, const
 }
 
 }  // namespace
+
+// Scratch of moe_permute_quant_noalloc, for callers that cannot allocate:
+// a fixed array in the library's device memory (held on every device that
+// loads the library until exit) standing in for the caller's workspace.
+// In host code the name is only a host-side handle, never a device address:
+// permute_static_scratch() looks the device address up once per device.
+static __device__ __align__(256) unsigned char g_permute_scratch[MOE_PERMUTE_NOALLOC_SCRATCH_BYTES];
+
+void* permute_static_scratch() {
+  static std::mutex mu;
+  static void* addr[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lk(mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_permute_scratch) != cudaSuccess) return nullptr;
+    addr[dev] = p;
+  }
+  return addr[dev];
+}
 
 size_t permute_ws_bytes(int T, int E) {
   const size_t C = (size_t)(T + 31) / 32;
