@@ -17,6 +17,8 @@ DeepSeek-V3-style and a Mixtral-style MoE layer):
   dsv3_skewed_t16384 T=16384 same layer as decode; bias +3.0 on the 26
                      experts with e % 10 == 0, -10 on the 32 with e % 8 == 7,
                      the rest ~N(0, 0.1)
+  dsv3_decode_t128_e32 / dsv3_prefill_t2048_e32: the DeepSeek-V3 layer with
+                     32 experts, small cases for profiling
 Hidden states and router logits ~N(0, 1); weights ~N(0, 0.02).
 """
 from dataclasses import dataclass, replace
@@ -61,6 +63,12 @@ WORKLOADS = {
                               True, 1.0, "none"),
     "dsv3_skewed_t16384": Workload("dsv3_skewed_t16384", 16384, 7168, 2048, 256, 8, 4, 8,
                                    SIGMOID, True, 2.5, "skewed"),
+    # the same layer with 32 experts (1.4 GB of weights): small cases for
+    # profiling the decode (weight-streaming) and prefill (tensor) GEMMs
+    "dsv3_decode_t128_e32": Workload("dsv3_decode_t128_e32", 128, 7168, 2048, 32, 8, 4, 8,
+                                     SIGMOID, True, 2.5, "normal"),
+    "dsv3_prefill_t2048_e32": Workload("dsv3_prefill_t2048_e32", 2048, 7168, 2048, 32, 8, 4, 8,
+                                       SIGMOID, True, 2.5, "zero"),
 }
 
 # tensor ids: each tensor draws from its own generator stream
