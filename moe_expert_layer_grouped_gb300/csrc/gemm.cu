@@ -5,31 +5,43 @@
 // offs_am; "Support token-level quantization for EP MoE", sglang #6782,
 // Changelog: per-token scale_a in the grouped GEMM).
 //
+// Orientation: the weights are the MMA's M side and the tokens its N side
+// (D^T = W * A^T). A tile is 128 weight rows x N tokens of one expert, with
+// N the expert's remaining tokens rounded up to 16 (at most BNMAX), so an
+// expert's token count is padded to a multiple of 16 rather than of 128.
+//
 // Design (one persistent CTA per SM, 192 threads, warp-specialised):
-//   warp 0      TMA producer: A tile [128 rows x 128 B] + B tile
-//               [256 rows x 128 B] per stage into a 4-stage ring, 128-byte
-//               swizzled; weights streamed with an evict-first L2 policy,
-//               activations kept with evict-last.
+//   warp 0      TMA producer: per stage the 128 weight rows (one 128-row box,
+//               or for SiLU two 64-row boxes, 128 B of K each) and the tile's
+//               tokens (rounded up to 16, covered exactly by boxes of
+//               256/128/64/32/16 rows) into a STAGES-deep ring, 128-byte
+//               swizzled; weights streamed evict-first when each weight
+//               block is read once, tokens kept with evict-last.
 //   warp 1      MMA issuer: tcgen05.mma.cta_group::1.kind::f8f6f4,
-//               M=128 x N=256 x K=32 per instruction, fp32 accumulator in
-//               tensor memory; two accumulators (2 x 256 columns) so the
-//               epilogue of tile i overlaps the main loop of tile i+1.
-//   warps 2..5  epilogue: tcgen05.ld of the accumulator (one token row per
-//               thread), dequantise by scale_a[row] * scale_b[e,n], then
-//               either bf16 out or SiLU(gate) * up -> bf16 (+ row amax).
-// Tiles are (expert, n-block, m-block) with the m-block fastest, so the
-// m-blocks of one expert stream the same weight block at the same time and
-// share it through L2. The tile table is derived on the device from the
-// expert offsets (no host synchronisation); rows of a tile past the
-// expert's segment are computed but never stored.
-// For SiLU*mul, the n-block takes gate rows [nb*128, nb*128+128) and the
-// matching up rows [I+nb*128, ...) as the two halves of the 256-row B tile,
-// so gate and up land in the same thread's accumulator columns.
+//               M=128 x N x K=32, fp32 accumulator in tensor memory; two
+//               accumulators (2 x 256 columns) so the epilogue of tile i
+//               overlaps the main loop of tile i+1.
+//   warps 2..5  epilogue: tcgen05.ld (one weight row per thread, 32 tokens
+//               per load), dequantise by scale_a[token] * scale_b[e, row],
+//               then bf16 out, or SiLU(gate) * up; the bf16 block is
+//               transposed through shared memory so each token row is stored
+//               with 16-byte vectors.
+// SiLU*mul: a w13 tile holds gate rows [j0, j0+64) in TMEM lanes 0..63 and
+// the matching up rows [I+j0, I+j0+64) in lanes 64..127. The warp holding
+// gate lanes and the warp holding the same j's up lanes trade alternate
+// 32-token chunks through shared memory, so each computes silu(g)*u for half
+// of the tokens.
+// Tiles are (expert, weight block, token chunk) with the token chunk fastest,
+// so the chunks of one expert stream the same weight block at the same time
+// and share it through L2. The tile table is derived on the device from the
+// expert offsets (no host synchronisation); tokens past the expert's segment
+// are never stored.
 // Every pipeline wait is bounded (2 s); on timeout the CTA sets the device
 // error word, lets its in-flight copies and MMAs land, frees its tensor
 // memory and exits.
 #include <cuda.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "common.cuh"
@@ -39,22 +51,22 @@
 namespace moe {
 namespace {
 
-constexpr int BM = 128;   // token rows per tile (MMA M)
-constexpr int BN = 256;   // weight rows per tile (MMA N)
+constexpr int BM = 128;   // weight rows per tile (MMA M)
 constexpr int BK = 128;   // K bytes (= e4m3 elements) per pipeline stage
-constexpr int STAGES = 4;
-constexpr int A_BYTES = BM * BK;
-constexpr int B_BYTES = BN * BK;
-constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int W_BYTES = BM * BK;
 constexpr int THREADS = 192;
-constexpr uint32_t TMEM_COLS = 2 * BN;
+constexpr uint32_t ACC_COLS = 256;  // TMEM columns per accumulator
+constexpr uint32_t TMEM_COLS = 2 * ACC_COLS;
 constexpr int MAX_E = 1024;
 constexpr uint64_t WAIT_NS = 2000000000ull;
 constexpr uint64_t DRAIN_NS = 200000000ull;
 
+template <int XROWS, int STAGES, bool SILU>
 struct Smem {
-  uint8_t a[STAGES][A_BYTES];  // each stage 1024-byte aligned (swizzle atom)
-  uint8_t b[STAGES][B_BYTES];
+  uint8_t w[STAGES][W_BYTES];         // weights: 1024-byte aligned stages
+  uint8_t x[STAGES][XROWS * BK];      // this CTA's token rows
+  float xchg[SILU ? 2 : 1][2][32 * 32];  // SiLU pairs: 2 slots of 32 tokens x 32 lanes
+  uint16_t stage_out[4][32 * 32];        // per epilogue warp: bf16 [token][32 columns]
   uint64_t full[STAGES];
   uint64_t empty[STAGES];
   uint64_t tfull[2];
@@ -69,6 +81,15 @@ struct Smem {
   int offs[MAX_E + 1];
 };
 
+// Token boxes of 64/32/16 rows: a tile's tokens (rounded up to 16) are
+// covered exactly by 64-row boxes plus at most one 32- and one 16-row box
+// (64-row boxes measured fastest; weights also move in 64-row boxes).
+constexpr int NXBOX = 3;
+struct Maps {
+  CUtensorMap w;           // weights: 64-row boxes
+  CUtensorMap x[NXBOX];    // tokens: box rows 64 >> i
+};
+
 struct Params {
   const float* scale_a;
   const float* scale_b;
@@ -76,77 +97,89 @@ struct Params {
   void* C;
   float* row_amax;
   int* err;
-  int M, N, Kd, E, epilogue, I, NB, KB;
+  int M, N, Kd, E, I, NB, KB;
+  int stream_weights;  // 1: each weight block is read by one tile (evict-first)
 };
 
-// tile -> (expert, n-block, m-block)
-__device__ __forceinline__ void decode_tile(const Smem& sm, int E, int NB, int tile, int& e,
-                                            int& nb, int& mb) {
+template <int BNMAX>
+struct TileInfo {
+  int e, nb, tok0, ntok;
+};
+
+// tile -> (expert, weight block, token chunk)
+template <int BNMAX, class S>
+__device__ __forceinline__ TileInfo<BNMAX> decode_tile(const S& sm, int E, int NB, int tile) {
   int lo = 0, hi = E - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
     if (sm.tile_start[mid] <= tile) lo = mid;
     else hi = mid - 1;
   }
-  e = lo;
-  const int local = tile - sm.tile_start[e];
-  const int mbc = (sm.tile_start[e + 1] - sm.tile_start[e]) / NB;
-  nb = local / mbc;
-  mb = local - nb * mbc;
+  TileInfo<BNMAX> t;
+  t.e = lo;
+  const int local = tile - sm.tile_start[lo];
+  const int nch = (sm.tile_start[lo + 1] - sm.tile_start[lo]) / NB;
+  t.nb = local / nch;
+  const int tc = local - t.nb * nch;
+  // equal chunks (multiples of 16 tokens) so the tiles that share a weight
+  // block run at the same speed and meet it in L2
+  const int cnt = sm.offs[lo + 1] - sm.offs[lo];
+  const int csz = ((cnt + nch - 1) / nch + 15) & ~15;
+  t.tok0 = sm.offs[lo] + tc * csz;
+  t.ntok = min(csz, cnt - tc * csz);
+  return t;
 }
 
-__device__ __forceinline__ void load_scales32(const float* p, int valid_cols, float (&s)[32]) {
-  if (valid_cols >= 32) {
-#pragma unroll
-    for (int i = 0; i < 32; i += 4) {
-      const float4 v = __ldg(reinterpret_cast<const float4*>(p + i));
-      s[i] = v.x;
-      s[i + 1] = v.y;
-      s[i + 2] = v.z;
-      s[i + 3] = v.w;
-    }
-  } else {
-#pragma unroll
-    for (int i = 0; i < 32; ++i) s[i] = (i < valid_cols) ? __ldg(p + i) : 0.0f;
-  }
+__device__ __forceinline__ void bar_sync_named(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
-__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const uint32_t (&pk)[16],
-                                              int valid_cols) {
-  if (valid_cols >= 32) {
-    uint4* d = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-      d[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-  } else {
-    uint16_t* d = reinterpret_cast<uint16_t*>(dst);
-#pragma unroll
-    for (int i = 0; i < 32; ++i)
-      if (i < valid_cols) d[i] = (uint16_t)((i & 1) ? (pk[i >> 1] >> 16) : (pk[i >> 1] & 0xffffu));
-  }
+// Named barrier that also returns whether any participating thread passed a
+// non-zero `pred`.
+__device__ __forceinline__ int bar_red_or(int id, int count, int pred) {
+  int r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.s32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, %3, p;\n\t"
+      "selp.s32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(pred), "r"(id), "r"(count)
+      : "memory");
+  return r;
 }
 
+// CS = 1: one CTA per tile of 128 weight rows x N tokens.
+// CS = 2: a CTA pair (cluster of 2) computes 256 weight rows x N tokens with
+// the 2-SM MMA (tcgen05.mma.cta_group::2, issued by the even CTA): each CTA
+// holds its own 128 weight rows (its own weight block) and half of the N
+// token rows, and receives its 128 x N slice of the accumulator in its own
+// tensor memory, so a CTA moves and stores two thirds of the bytes a single
+// CTA would for the same MMA work. Epilogues are per CTA as in CS = 1.
+template <int BNMAX, int STAGES, bool SILU, int CS>
 __global__ void __launch_bounds__(THREADS, 1)
-    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
-                        const __grid_constant__ CUtensorMap tmB, const Params p) {
+    grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
+  static_assert(CS == 1 || CS == 2, "single CTA or CTA pair");
+  constexpr bool PAIR = (CS == 2);
+  using S = Smem<BNMAX / CS, STAGES, SILU>;
   extern __shared__ uint8_t smem_raw[];
-  Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                      ~static_cast<uintptr_t>(1023));
+  S& sm = *reinterpret_cast<S*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                ~static_cast<uintptr_t>(1023));
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
   const int E = p.E;
 
   if (warp == 0 && lane == 0) {
-    ptx::prefetch_tensormap(&tmA);
-    ptx::prefetch_tensormap(&tmB);
+    ptx::prefetch_tensormap(&maps.w);
+    for (int i = 0; i < NXBOX; ++i) ptx::prefetch_tensormap(&maps.x[i]);
     for (int s = 0; s < STAGES; ++s) {
-      ptx::mbar_init(&sm.full[s], 1);
-      ptx::mbar_init(&sm.empty[s], 1);
+      ptx::mbar_init(&sm.full[s], 1);   // pair: only the even CTA's is used
+      ptx::mbar_init(&sm.empty[s], 1);  // one (multicast) MMA commit
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(&sm.tfull[b], 1);
-      ptx::mbar_init(&sm.tempty[b], 128);
+      ptx::mbar_init(&sm.tempty[b], 128 * CS);  // pair: both CTAs' epilogues
     }
     ptx::mbar_init(&sm.drain, 1);
     sm.abort = 0;
@@ -154,9 +187,20 @@ __global__ void __launch_bounds__(THREADS, 1)
     ptx::fence_mbar_init();
   }
   if (warp == 1) {
-    ptx::tmem_alloc(&sm.tmem_base, TMEM_COLS);
-    ptx::tmem_relinquish();
+    if (PAIR) {
+      ptx::tmem_alloc_pair(&sm.tmem_base, TMEM_COLS);
+      ptx::tmem_relinquish_pair();
+    } else {
+      ptx::tmem_alloc(&sm.tmem_base, TMEM_COLS);
+      ptx::tmem_relinquish();
+    }
   }
+  const int rank = PAIR ? (int)ptx::cluster_ctarank() : 0;
+  const int cluster = blockIdx.x / CS;
+  const int nclusters = gridDim.x / CS;
+  const int NBG = p.NB / CS;  // weight-block groups per expert
+  constexpr uint16_t kPair = 0x3;
+  if (PAIR) ptx::cluster_sync();  // the peer's barriers exist before any signal
 
   // ---- tile table from the expert offsets --------------------------------
   for (int i = tid; i <= E; i += THREADS) sm.offs[i] = __ldg(p.offsets + i);
@@ -168,7 +212,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   for (int e = e0; e < e1; ++e) {
     const int lo = sm.offs[e], hi = sm.offs[e + 1];
     if (lo < 0 || hi < lo || hi > p.M) bad = 1;
-    else local += (hi - lo + BM - 1) / BM;
+    else local += (hi - lo + BNMAX - 1) / BNMAX;
   }
   sm.thr_sum[tid] = local;
   bad = __syncthreads_or(bad);
@@ -179,17 +223,17 @@ __global__ void __launch_bounds__(THREADS, 1)
       sm.thr_sum[i] = run;
       run += v;
     }
-    sm.total_tiles = bad ? 0 : run * p.NB;
-    sm.tile_start[E] = run * p.NB;
+    sm.total_tiles = bad ? 0 : run * NBG;
+    sm.tile_start[E] = run * NBG;
     if (bad) flag_error(p.err, MOE_DEV_BAD_OFFSETS);
   }
   __syncthreads();
   {
     int run = sm.thr_sum[tid];
     for (int e = e0; e < e1; ++e) {
-      sm.tile_start[e] = run * p.NB;
+      sm.tile_start[e] = run * NBG;
       const int lo = sm.offs[e], hi = sm.offs[e + 1];
-      if (!bad) run += (hi - lo + BM - 1) / BM;
+      if (!bad) run += (hi - lo + BNMAX - 1) / BNMAX;
     }
   }
   ptx::tc_fence_before();
@@ -201,33 +245,66 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (warp == 0) {
     // ======================= TMA producer ===================================
     if (lane == 0) {
-      const uint64_t pol_a = ptx::policy_evict_last();
-      const uint64_t pol_b = ptx::policy_evict_first();
+      const uint64_t pol_w = p.stream_weights ? ptx::policy_evict_first() : ptx::policy_evict_normal();
+      const uint64_t pol_x = ptx::policy_evict_last();
       uint32_t s = 0, ph = 0, armed = 0, armed_par = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-        int e, nb, mb;
-        decode_tile(sm, E, p.NB, tile, e, nb, mb);
-        const int m0 = sm.offs[e] + mb * BM;
-        int y0, y1;
-        if (p.epilogue == MOE_EPI_SILU_MUL) {
-          y0 = e * p.N + nb * 128;
+      for (int g = cluster; ok && g < total; g += nclusters) {
+        const TileInfo<BNMAX> t = decode_tile<BNMAX>(sm, E, NBG, g);
+        const int nb = t.nb * CS + rank;
+        // token rows of the MMA (N): a multiple of 16, of 32 for a pair so
+        // each CTA holds N/2 rows; this CTA loads rows [rank*half, +half)
+        const int rows = PAIR ? (t.ntok + 31) & ~31 : (t.ntok + 15) & ~15;
+        const int half = rows / CS;
+        const uint32_t bytes = CS * W_BYTES + (uint32_t)rows * BK;  // all CTAs' loads
+        int y0, y1;  // first rows of the two 64-row weight boxes
+        if (SILU) {  // gate rows [j0, j0+64) and up rows [I+j0, I+j0+64)
+          y0 = t.e * p.N + nb * 64;
           y1 = y0 + p.I;
         } else {
-          y0 = e * p.N + nb * BN;
-          y1 = y0 + 128;
+          y0 = t.e * p.N + nb * BM;
+          y1 = y0 + 64;
         }
         for (int kb = 0; kb < p.KB; ++kb) {
           if (!ptx::mbar_wait(&sm.empty[s], ph ^ 1u, &sm.abort, WAIT_NS)) {
             ok = false;
             break;
           }
-          ptx::mbar_arrive_expect_tx(&sm.full[s], STAGE_BYTES);
-          armed |= 1u << s;
-          armed_par = (armed_par & ~(1u << s)) | (ph << s);
-          ptx::tma_load_2d(sm.a[s], &tmA, &sm.full[s], kb * BK, m0, pol_a);
-          ptx::tma_load_2d(sm.b[s], &tmB, &sm.full[s], kb * BK, y0, pol_b);
-          ptx::tma_load_2d(sm.b[s] + 128 * BK, &tmB, &sm.full[s], kb * BK, y1, pol_b);
+          if (rank == 0) {
+            ptx::mbar_arrive_expect_tx(&sm.full[s], bytes);
+            armed |= 1u << s;
+            armed_par = (armed_par & ~(1u << s)) | (ph << s);
+          }
+          const int kx = kb * BK;
+          if (PAIR) {
+            // completions count on the even CTA's barrier
+            const uint32_t fb = ptx::map_to_rank(ptx::smem_u32(&sm.full[s]), 0);
+            ptx::tma_load_2d_pair(sm.w[s], &maps.w, fb, kx, y0, pol_w);
+            ptx::tma_load_2d_pair(sm.w[s] + 64 * BK, &maps.w, fb, kx, y1, pol_w);
+            int r = 0;
+#pragma unroll
+            for (int i = 0; i < NXBOX; ++i) {
+              const int box = 64 >> i;
+              while (half - r >= box) {
+                ptx::tma_load_2d_pair(sm.x[s] + r * BK, &maps.x[i], fb, kx,
+                                      t.tok0 + rank * half + r, pol_x);
+                r += box;
+              }
+            }
+          } else {
+            ptx::tma_load_2d(sm.w[s], &maps.w, &sm.full[s], kx, y0, pol_w);
+            ptx::tma_load_2d(sm.w[s] + 64 * BK, &maps.w, &sm.full[s], kx, y1, pol_w);
+            int r = 0;
+#pragma unroll
+            for (int i = 0; i < NXBOX; ++i) {
+              const int box = 64 >> i;
+              while (rows - r >= box) {
+                ptx::tma_load_2d(sm.x[s] + r * BK, &maps.x[i], &sm.full[s], kx, t.tok0 + r,
+                                 pol_x);
+                r += box;
+              }
+            }
+          }
           if (++s == STAGES) {
             s = 0;
             ph ^= 1u;
@@ -244,12 +321,14 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   } else if (warp == 1) {
     // ======================= MMA issuer =====================================
-    if (lane == 0) {
-      constexpr uint32_t idesc = ptx::idesc_e4m3_f32(BM, BN);
+    if (lane == 0 && rank == 0) {  // pair: the even CTA issues for both
       uint32_t s = 0, ph = 0;
       bool ok = true, issued = false;
       int iter = 0;
-      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x, ++iter) {
+      for (int g = cluster; ok && g < total; g += nclusters, ++iter) {
+        const TileInfo<BNMAX> t = decode_tile<BNMAX>(sm, E, NBG, g);
+        const int n_mma = PAIR ? (t.ntok + 31) & ~31 : (t.ntok + 15) & ~15;
+        const uint32_t idesc = ptx::idesc_e4m3_f32(BM * CS, n_mma);
         const int b = iter & 1;
         const uint32_t tph = (iter >> 1) & 1;
         if (!ptx::mbar_wait(&sm.tempty[b], tph ^ 1u, &sm.abort, WAIT_NS)) {
@@ -257,35 +336,48 @@ __global__ void __launch_bounds__(THREADS, 1)
           break;
         }
         ptx::tc_fence_after();
-        const uint32_t d = tmem + (uint32_t)(b * BN);
+        const uint32_t d = tmem + (uint32_t)b * ACC_COLS;
         for (int kb = 0; kb < p.KB; ++kb) {
           if (!ptx::mbar_wait(&sm.full[s], ph, &sm.abort, WAIT_NS)) {
             ok = false;
             break;
           }
           ptx::tc_fence_after();
-          const uint32_t a0 = ptx::smem_u32(sm.a[s]);
-          const uint32_t b0 = ptx::smem_u32(sm.b[s]);
+          const uint32_t a0 = ptx::smem_u32(sm.w[s]);
+          const uint32_t b0 = ptx::smem_u32(sm.x[s]);
 #pragma unroll
           for (int kk = 0; kk < BK / 32; ++kk) {
-            ptx::mma_e4m3(d, ptx::sdesc_sw128(a0 + kk * 32), ptx::sdesc_sw128(b0 + kk * 32),
-                          idesc, (kb | kk) != 0 ? 1u : 0u);
+            if (PAIR)
+              ptx::mma_e4m3_pair(d, ptx::sdesc_sw128(a0 + kk * 32),
+                                 ptx::sdesc_sw128(b0 + kk * 32), idesc, (kb | kk) != 0 ? 1u : 0u);
+            else
+              ptx::mma_e4m3(d, ptx::sdesc_sw128(a0 + kk * 32), ptx::sdesc_sw128(b0 + kk * 32),
+                            idesc, (kb | kk) != 0 ? 1u : 0u);
           }
           issued = true;
-          ptx::mma_commit(&sm.empty[s]);
+          if (PAIR)
+            ptx::mma_commit_pair_mcast(&sm.empty[s], kPair);  // frees the stage in both CTAs
+          else
+            ptx::mma_commit(&sm.empty[s]);
           if (++s == STAGES) {
             s = 0;
             ph ^= 1u;
           }
         }
         if (!ok) break;
-        ptx::mma_commit(&sm.tfull[b]);
+        if (PAIR)
+          ptx::mma_commit_pair_mcast(&sm.tfull[b], kPair);  // both CTAs' epilogues
+        else
+          ptx::mma_commit(&sm.tfull[b]);
       }
       if (!ok) {
         sm.abort = 1;
         flag_error(p.err, MOE_DEV_PIPE_TIMEOUT);
         if (issued) {
-          ptx::mma_commit(&sm.drain);
+          if (PAIR)
+            ptx::mma_commit_pair_mcast(&sm.drain, 0x1);
+          else
+            ptx::mma_commit(&sm.drain);
           ptx::mbar_wait(&sm.drain, 0, &sm.never, DRAIN_NS);
         }
       }
@@ -294,93 +386,153 @@ __global__ void __launch_bounds__(THREADS, 1)
     // ======================= epilogue (warps 2..5) ==========================
     const int q = warp & 3;  // TMEM lane quadrant this warp may access
     int iter = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++iter) {
+    for (int g = cluster; g < total; g += nclusters, ++iter) {
+      TileInfo<BNMAX> t = decode_tile<BNMAX>(sm, E, NBG, g);
+      t.nb = t.nb * CS + rank;
       const int b = iter & 1;
       const uint32_t tph = (iter >> 1) & 1;
-      int e, nb, mb;
-      decode_tile(sm, E, p.NB, tile, e, nb, mb);
-      const int row = sm.offs[e] + mb * BM + q * 32 + lane;
-      const bool valid = row < sm.offs[e + 1];
       bool ok = ptx::mbar_wait(&sm.tfull[b], tph, &sm.abort, WAIT_NS);
       ok = __all_sync(kFull, ok);
+      // the two warps of a SiLU exchange pair leave together or not at all
+      if (SILU) ok = !bar_red_or(1 + (q & 1), 64, !ok);
       if (!ok) {
         sm.abort = 1;
         flag_error(p.err, MOE_DEV_PIPE_TIMEOUT);
         break;
       }
       ptx::tc_fence_after();
-      const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * BN);
-      const float sa = valid ? __ldg(p.scale_a + row) : 0.0f;
-      if (p.epilogue == MOE_EPI_SILU_MUL) {
+      const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)b * ACC_COLS;
+      const int nchunk = (t.ntok + 31) >> 5;
+      const int64_t e = t.e;
+      if (SILU) {
         const int I = p.I;
-        __nv_bfloat16* hrow = reinterpret_cast<__nv_bfloat16*>(p.C) + (int64_t)row * I;
-        float amax = 0.0f;
+        const int pair = q & 1;           // which 32 of the tile's 64 j
+        const bool holds_gate = q < 2;    // lanes 0..63 gate, 64..127 up
+        const int j = t.nb * 64 + pair * 32 + lane;
+        const bool jv = j < I;
+        const float sg = jv ? __ldg(p.scale_b + e * p.N + j) : 0.0f;
+        const float su = jv ? __ldg(p.scale_b + e * p.N + I + j) : 0.0f;
+        __nv_bfloat16* hbase = reinterpret_cast<__nv_bfloat16*>(p.C);
+        // of every 32-token chunk the gate holder computes tokens 0..15 and
+        // the up holder tokens 16..31; each hands the other its half
+        const int mine0 = holds_gate ? 0 : 16;
+        uint16_t* ost = sm.stage_out[q];
+        const int jrow = t.nb * 64 + pair * 32;  // first j of this warp's 32
 #pragma unroll 1
-        for (int c = 0; c < 128; c += 32) {
-          uint32_t g[32], u[32];
-          ptx::tmem_ld_32x32b_x32(tbase + c, g);
-          ptx::tmem_ld_32x32b_x32(tbase + 128 + c, u);
+        for (int c = 0; c < nchunk; ++c) {
+          uint32_t v[32];
+          ptx::tmem_ld_32x32b_x32(tbase + c * 32, v);
           ptx::tmem_ld_wait();
-          ptx::reg_fence(g);
-          ptx::reg_fence(u);
-          const int j0 = nb * 128 + c;
-          const int vc = min(32, I - j0);
-          if (!valid || vc <= 0) continue;
-          float sg[32], su[32];
-          const float* sb = p.scale_b + (int64_t)e * p.N + j0;
-          load_scales32(sb, vc, sg);
-          load_scales32(sb + I, vc, su);
-          uint32_t pk[16];
+          ptx::reg_fence(v);
+          float* give = sm.xchg[pair][c & 1] + (holds_gate ? 16 * 32 : 0);
+          const float* take = sm.xchg[pair][c & 1] + (holds_gate ? 0 : 16 * 32);
+          float own_v[16];  // this warp's half of the chunk, the other half goes out
 #pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            float hv[2];
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const float gv = __uint_as_float(g[i + h]) * sa * sg[i + h];
-              const float uv = __uint_as_float(u[i + h]) * sa * su[i + h];
-              hv[h] = gv / (1.0f + __expf(-gv)) * uv;
-            }
-            pk[i >> 1] = pack_bf16x2(hv[0], hv[1]);
-            const float r0 = fabsf(__uint_as_float(pk[i >> 1] << 16));
-            const float r1 = fabsf(__uint_as_float(pk[i >> 1] & 0xffff0000u));
-            if (i < vc) amax = fmaxf(amax, r0);
-            if (i + 1 < vc) amax = fmaxf(amax, r1);
+          for (int i = 0; i < 16; ++i) {
+            const float lo = __uint_as_float(v[i]), hi = __uint_as_float(v[16 + i]);
+            own_v[i] = holds_gate ? lo : hi;
+            give[i * 32 + lane] = holds_gate ? hi : lo;
           }
-          store_bf16x32(hrow + j0, pk, vc);
+          bar_sync_named(1 + pair, 64);
+          const int tk0 = c * 32 + mine0;
+          const float sa_l =
+              (lane < 16 && tk0 + lane < t.ntok) ? __ldg(p.scale_a + t.tok0 + tk0 + lane) : 0.0f;
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float other = take[i * 32 + lane];
+            const float own = own_v[i];
+            const float sa = __shfl_sync(kFull, sa_l, i);
+            const float g = (holds_gate ? own : other) * sa * sg;
+            const float u = (holds_gate ? other : own) * sa * su;
+            const float h = g / (1.0f + __expf(-g)) * u;
+            const __nv_bfloat16 hb = __float2bfloat16_rn(h);
+            ost[i * 32 + lane] = __bfloat16_as_ushort(hb);
+            if (p.row_amax != nullptr) {
+              const float m = warp_max(jv ? fabsf(__bfloat162float(hb)) : 0.0f);
+              if (lane == 0 && tk0 + i < t.ntok)
+                atomicMax(reinterpret_cast<int*>(p.row_amax + t.tok0 + tk0 + i),
+                          __float_as_int(m));
+            }
+          }
+          __syncwarp();
+          // 16 tokens x 32 j: four lanes per token row, 16 bytes each
+          if (jrow < I) {
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+              const int r = k * 8 + (lane >> 2);
+              if (tk0 + r < t.ntok)
+                *reinterpret_cast<uint4*>(hbase + (int64_t)(t.tok0 + tk0 + r) * I + jrow +
+                                          (lane & 3) * 8) =
+                    *reinterpret_cast<const uint4*>(ost + r * 32 + (lane & 3) * 8);
+            }
+          }
+          __syncwarp();
         }
-        if (p.row_amax != nullptr && valid)
-          atomicMax(reinterpret_cast<int*>(p.row_amax + row), __float_as_int(amax));
+        // the partner must be done reading this tile's slots before the next
+        // tile overwrites them
+        bar_sync_named(1 + pair, 64);
       } else {
         const int N = p.N;
-        __nv_bfloat16* crow = reinterpret_cast<__nv_bfloat16*>(p.C) + (int64_t)row * N;
+        const int ncol0 = t.nb * BM + q * 32;  // first column of this warp's 32
+        const int n = ncol0 + lane;
+        const bool nv = n < N;
+        const float sb = nv ? __ldg(p.scale_b + e * N + n) : 0.0f;
+        uint16_t* ost = sm.stage_out[q];
+        __nv_bfloat16* cbase = reinterpret_cast<__nv_bfloat16*>(p.C);
+        // the next chunk's TMEM load is in flight while this one is stored
+        uint32_t v[32];
+        ptx::tmem_ld_32x32b_x32(tbase, v);
 #pragma unroll 1
-        for (int c = 0; c < BN; c += 32) {
-          uint32_t acc[32];
-          ptx::tmem_ld_32x32b_x32(tbase + c, acc);
+        for (int c = 0; c < nchunk; ++c) {
           ptx::tmem_ld_wait();
-          ptx::reg_fence(acc);
-          const int n0 = nb * BN + c;
-          const int vc = min(32, N - n0);
-          if (!valid || vc <= 0) continue;
-          float sb[32];
-          load_scales32(p.scale_b + (int64_t)e * N + n0, vc, sb);
-          uint32_t pk[16];
+          ptx::reg_fence(v);
+          float f[32];
 #pragma unroll
-          for (int i = 0; i < 32; i += 2)
-            pk[i >> 1] = pack_bf16x2(__uint_as_float(acc[i]) * sa * sb[i],
-                                     __uint_as_float(acc[i + 1]) * sa * sb[i + 1]);
-          store_bf16x32(crow + n0, pk, vc);
+          for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]);
+          if (c + 1 < nchunk) ptx::tmem_ld_32x32b_x32(tbase + (c + 1) * 32, v);
+          const int tk0 = c * 32;
+          const float sa_l = (tk0 + lane < t.ntok) ? __ldg(p.scale_a + t.tok0 + tk0 + lane) : 0.0f;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float sa = __shfl_sync(kFull, sa_l, i);
+            ost[i * 32 + lane] = __bfloat16_as_ushort(__float2bfloat16_rn(f[i] * sa * sb));
+          }
+          __syncwarp();
+          // 32 tokens x 32 columns: four lanes per token row, 16 bytes each
+          if (ncol0 < N) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const int r = k * 8 + (lane >> 2);
+              if (tk0 + r < t.ntok)
+                *reinterpret_cast<uint4*>(cbase + (int64_t)(t.tok0 + tk0 + r) * N + ncol0 +
+                                          (lane & 3) * 8) =
+                    *reinterpret_cast<const uint4*>(ost + r * 32 + (lane & 3) * 8);
+            }
+          }
+          __syncwarp();
         }
       }
       ptx::tc_fence_before();
-      ptx::mbar_arrive(&sm.tempty[b]);
+      if (PAIR && rank != 0)
+        ptx::mbar_arrive_cluster(ptx::map_to_rank(ptx::smem_u32(&sm.tempty[b]), 0));
+      else
+        ptx::mbar_arrive(&sm.tempty[b]);
     }
   }
 
   // ---- teardown -------------------------------------------------------------
   ptx::tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (PAIR) {
+    // both CTAs are done with the shared accumulator before it is freed, and
+    // neither leaves while the other may still signal its barriers
+    ptx::cluster_sync();
+    if (warp == 1) {
+      ptx::tc_fence_after();
+      ptx::tmem_dealloc_pair(tmem, TMEM_COLS);
+    }
+    ptx::cluster_sync();
+  } else if (warp == 1) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, TMEM_COLS);
   }
@@ -396,33 +548,101 @@ EncodeTiledFn encode_fn() {
   static EncodeTiledFn fn = nullptr;
   static std::once_flag once;
   std::call_once(once, [] {
-    void* p = nullptr;
+    void* ptr = nullptr;
     cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
   });
   return fn;
 }
 
-// 2-D u8 tensor [rows, cols] (cols contiguous), box 128 x 128, 128-byte
-// swizzle, zero fill outside the tensor.
-bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols) {
+// 2-D u8 tensor [rows, cols] (cols contiguous), box 128 B x box_rows,
+// 128-byte swizzle, zero fill outside the tensor. Encoded maps are cached by
+// (address, shape, box) so repeated calls on the same buffers skip the
+// driver-side encoding.
+bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
+              uint32_t box_rows) {
+  struct Entry {
+    const void* base;
+    uint64_t rows, cols;
+    uint32_t box;
+    int dev;
+    CUtensorMap map;
+  };
+  static std::mutex mu;
+  static Entry cache[64];
+  static int next = 0;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    for (const Entry& c : cache)
+      if (c.base == base && c.rows == rows && c.cols == cols && c.box == box_rows &&
+          c.dev == dev) {
+        *m = c.map;
+        return true;
+      }
+  }
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return false;
   const cuuint64_t dims[2] = {cols, rows};
   const cuuint64_t strides[1] = {cols};
-  const cuuint32_t box[2] = {BK, 128};
+  const cuuint32_t box[2] = {BK, box_rows};
   const cuuint32_t es[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
-         CUDA_SUCCESS;
+  if (fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  std::lock_guard<std::mutex> lk(mu);
+  cache[next] = Entry{base, rows, cols, box_rows, dev, *m};
+  next = (next + 1) % 64;
+  return true;
 }
 
-constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
-static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+template <int BNMAX, int STAGES, bool SILU, int CS>
+cudaError_t launch_cfg(const Maps& maps, const Params& p, int M, int E, cudaStream_t st) {
+  constexpr size_t smem = sizeof(Smem<BNMAX / CS, STAGES, SILU>) + 1024;
+  static_assert(smem <= 227 * 1024, "shared memory budget");
+  auto kern = grouped_gemm_kernel<BNMAX, STAGES, SILU, CS>;
+  static std::mutex mu;
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    if (dev >= 64 || !attr_set[dev]) {
+      cudaError_t e =
+          cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+      if (dev < 64) attr_set[dev] = true;
+    }
+  }
+  const long long upper = ((long long)(M + BNMAX - 1) / BNMAX + E) * (p.NB / CS) * CS;
+  int grid = (int)std::min<long long>(sm_count(), upper);
+  grid = std::max(CS, grid / CS * CS);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CS;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (CS > 1) {
+    // a persistent grid of pairs must be co-resident: no more clusters than
+    // the GPU can hold at once
+    int nclusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&nclusters, kern, &cfg) == cudaSuccess && nclusters > 0)
+      cfg.gridDim = dim3(std::min(grid, nclusters * CS));
+  }
+  return cudaLaunchKernelEx(&cfg, kern, maps, p);
+}
 
 }  // namespace
 
@@ -431,10 +651,14 @@ cudaError_t launch_grouped_gemm(const void* A, const float* scale_a, const void*
                                 int Kd, int E, int epilogue, void* C, float* row_amax, int* err,
                                 cudaStream_t st) {
   if (M == 0) return cudaSuccess;
-  CUtensorMap mA, mB;
-  if (!make_map(&mA, A, (uint64_t)M, (uint64_t)Kd) ||
-      !make_map(&mB, B, (uint64_t)E * (uint64_t)N, (uint64_t)Kd))
+  const bool silu = (epilogue == MOE_EPI_SILU_MUL);
+  const bool small = (int64_t)M <= (int64_t)32 * E;  // few rows per expert (decode)
+  Maps maps;
+  if (!make_map(&maps.w, B, (uint64_t)E * (uint64_t)N, (uint64_t)Kd, 64))
     return cudaErrorNotSupported;
+  for (int i = 0; i < NXBOX; ++i)
+    if (!make_map(&maps.x[i], A, (uint64_t)M, (uint64_t)Kd, 64u >> i))
+      return cudaErrorNotSupported;
   Params p;
   p.scale_a = scale_a;
   p.scale_b = scale_b;
@@ -446,29 +670,23 @@ cudaError_t launch_grouped_gemm(const void* A, const float* scale_a, const void*
   p.N = N;
   p.Kd = Kd;
   p.E = E;
-  p.epilogue = epilogue;
   p.I = N / 2;
-  p.NB = (epilogue == MOE_EPI_SILU_MUL) ? (p.I + 127) / 128 : (N + BN - 1) / BN;
+  p.NB = silu ? (p.I + 63) / 64 : (N + BM - 1) / BM;
   p.KB = (Kd + BK - 1) / BK;
-  const long long upper = ((long long)(M + BM - 1) / BM + E) * p.NB;
-  const int grid = (int)std::min<long long>(sm_count(), upper);
-
-  static std::mutex mu;
-  static bool attr_set[64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  {
-    std::lock_guard<std::mutex> lk(mu);
-    if (dev >= 64 || !attr_set[dev]) {
-      cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           (int)kSmemBytes);
-      if (e != cudaSuccess) return e;
-      if (dev < 64) attr_set[dev] = true;
-    }
-  }
-  grouped_gemm_kernel<<<grid, THREADS, kSmemBytes, st>>>(mA, mB, p);
-  return cudaGetLastError();
+  p.stream_weights = 0;
+  // few rows per expert (decode): small token tiles and a deep weight ring,
+  // weights streamed once; many (prefill): tiles of up to 256 tokens
+  p.stream_weights = small ? 1 : 0;
+  if (small)
+    return silu ? launch_cfg<64, 8, true, 1>(maps, p, M, E, st)
+                : launch_cfg<64, 8, false, 1>(maps, p, M, E, st);
+  // many tokens per expert: CTA pairs on pairs of weight blocks (2-SM MMA),
+  // 6 stages of 16 KB weights + 16 KB tokens per CTA
+  if (p.NB % 2 == 0)
+    return silu ? launch_cfg<256, 6, true, 2>(maps, p, M, E, st)
+                : launch_cfg<256, 6, false, 2>(maps, p, M, E, st);
+  return silu ? launch_cfg<256, 4, true, 1>(maps, p, M, E, st)
+              : launch_cfg<256, 4, false, 1>(maps, p, M, E, st);
 }
 
 }  // namespace moe

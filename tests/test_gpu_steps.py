@@ -196,6 +196,9 @@ GEMM_SHAPES = [
     ([300], 768, 384),
     ([17, 64, 200, 3], 320, 96),
     ([129, 127], 256, 7168),
+    # few rows per expert overall (small token tiles) but one expert with
+    # several token chunks
+    ([150, 0, 3, 40, 0, 0, 7, 0, 0, 0, 0, 0, 0, 0, 0, 1], 256, 512),
 ]
 
 
