@@ -60,11 +60,15 @@ constexpr uint32_t TMEM_COLS = 2 * ACC_COLS;
 constexpr int MAX_E = 1024;
 constexpr uint64_t WAIT_NS = 2000000000ull;
 constexpr uint64_t DRAIN_NS = 200000000ull;
+#ifndef PAIR_KC
+#define PAIR_KC 2
+#define PAIR_STAGES 3
+#endif
 
-template <int XROWS, int STAGES, bool SILU>
+template <int XROWS, int STAGES, bool SILU, int KC>
 struct Smem {
-  uint8_t w[STAGES][W_BYTES];         // weights: 1024-byte aligned stages
-  uint8_t x[STAGES][XROWS * BK];      // this CTA's token rows
+  uint8_t w[STAGES][KC][W_BYTES];     // weights: KC K-chunks of 128 B per stage
+  uint8_t x[STAGES][KC][XROWS * BK];  // this CTA's token rows
   float xchg[SILU ? 2 : 1][2][32 * 32];  // SiLU pairs: 2 slots of 32 tokens x 32 lanes
   uint16_t stage_out[4][32 * 32];        // per epilogue warp: bf16 [token][32 columns]
   uint64_t full[STAGES];
@@ -156,12 +160,13 @@ __device__ __forceinline__ int bar_red_or(int id, int count, int pred) {
 // token rows, and receives its 128 x N slice of the accumulator in its own
 // tensor memory, so a CTA moves and stores two thirds of the bytes a single
 // CTA would for the same MMA work. Epilogues are per CTA as in CS = 1.
-template <int BNMAX, int STAGES, bool SILU, int CS>
+template <int BNMAX, int STAGES, bool SILU, int CS, int KC>
 __global__ void __launch_bounds__(THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
   static_assert(CS == 1 || CS == 2, "single CTA or CTA pair");
   constexpr bool PAIR = (CS == 2);
-  using S = Smem<BNMAX / CS, STAGES, SILU>;
+  using S = Smem<BNMAX / CS, STAGES, SILU, KC>;
+  const int KS = (p.KB + KC - 1) / KC;  // pipeline stages per tile
   extern __shared__ uint8_t smem_raw[];
   S& sm = *reinterpret_cast<S*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                 ~static_cast<uintptr_t>(1023));
@@ -256,7 +261,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         // each CTA holds N/2 rows; this CTA loads rows [rank*half, +half)
         const int rows = PAIR ? (t.ntok + 31) & ~31 : (t.ntok + 15) & ~15;
         const int half = rows / CS;
-        const uint32_t bytes = CS * W_BYTES + (uint32_t)rows * BK;  // all CTAs' loads
+        const uint32_t bytes = KC * (CS * W_BYTES + (uint32_t)rows * BK);  // all CTAs' loads
         int y0, y1;  // first rows of the two 64-row weight boxes
         if (SILU) {  // gate rows [j0, j0+64) and up rows [I+j0, I+j0+64)
           y0 = t.e * p.N + nb * 64;
@@ -265,7 +270,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           y0 = t.e * p.N + nb * BM;
           y1 = y0 + 64;
         }
-        for (int kb = 0; kb < p.KB; ++kb) {
+        for (int ks = 0; ks < KS; ++ks) {
           if (!ptx::mbar_wait(&sm.empty[s], ph ^ 1u, &sm.abort, WAIT_NS)) {
             ok = false;
             break;
@@ -275,33 +280,37 @@ __global__ void __launch_bounds__(THREADS, 1)
             armed |= 1u << s;
             armed_par = (armed_par & ~(1u << s)) | (ph << s);
           }
-          const int kx = kb * BK;
-          if (PAIR) {
-            // completions count on the even CTA's barrier
-            const uint32_t fb = ptx::map_to_rank(ptx::smem_u32(&sm.full[s]), 0);
-            ptx::tma_load_2d_pair(sm.w[s], &maps.w, fb, kx, y0, pol_w);
-            ptx::tma_load_2d_pair(sm.w[s] + 64 * BK, &maps.w, fb, kx, y1, pol_w);
-            int r = 0;
+          // pair: completions count on the even CTA's barrier
+          const uint32_t fb = PAIR ? ptx::map_to_rank(ptx::smem_u32(&sm.full[s]), 0) : 0u;
 #pragma unroll
-            for (int i = 0; i < NXBOX; ++i) {
-              const int box = 64 >> i;
-              while (half - r >= box) {
-                ptx::tma_load_2d_pair(sm.x[s] + r * BK, &maps.x[i], fb, kx,
-                                      t.tok0 + rank * half + r, pol_x);
-                r += box;
+          for (int kc = 0; kc < KC; ++kc) {
+            const int kx = (ks * KC + kc) * BK;  // past Kd: zero-filled, adds nothing
+            uint8_t* wdst = sm.w[s][kc];
+            uint8_t* xdst = sm.x[s][kc];
+            if (PAIR) {
+              ptx::tma_load_2d_pair(wdst, &maps.w, fb, kx, y0, pol_w);
+              ptx::tma_load_2d_pair(wdst + 64 * BK, &maps.w, fb, kx, y1, pol_w);
+              int r = 0;
+#pragma unroll
+              for (int i = 0; i < NXBOX; ++i) {
+                const int box = 64 >> i;
+                while (half - r >= box) {
+                  ptx::tma_load_2d_pair(xdst + r * BK, &maps.x[i], fb, kx,
+                                        t.tok0 + rank * half + r, pol_x);
+                  r += box;
+                }
               }
-            }
-          } else {
-            ptx::tma_load_2d(sm.w[s], &maps.w, &sm.full[s], kx, y0, pol_w);
-            ptx::tma_load_2d(sm.w[s] + 64 * BK, &maps.w, &sm.full[s], kx, y1, pol_w);
-            int r = 0;
+            } else {
+              ptx::tma_load_2d(wdst, &maps.w, &sm.full[s], kx, y0, pol_w);
+              ptx::tma_load_2d(wdst + 64 * BK, &maps.w, &sm.full[s], kx, y1, pol_w);
+              int r = 0;
 #pragma unroll
-            for (int i = 0; i < NXBOX; ++i) {
-              const int box = 64 >> i;
-              while (rows - r >= box) {
-                ptx::tma_load_2d(sm.x[s] + r * BK, &maps.x[i], &sm.full[s], kx, t.tok0 + r,
-                                 pol_x);
-                r += box;
+              for (int i = 0; i < NXBOX; ++i) {
+                const int box = 64 >> i;
+                while (rows - r >= box) {
+                  ptx::tma_load_2d(xdst + r * BK, &maps.x[i], &sm.full[s], kx, t.tok0 + r, pol_x);
+                  r += box;
+                }
               }
             }
           }
@@ -337,22 +346,26 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         ptx::tc_fence_after();
         const uint32_t d = tmem + (uint32_t)b * ACC_COLS;
-        for (int kb = 0; kb < p.KB; ++kb) {
+        for (int ks = 0; ks < KS; ++ks) {
           if (!ptx::mbar_wait(&sm.full[s], ph, &sm.abort, WAIT_NS)) {
             ok = false;
             break;
           }
           ptx::tc_fence_after();
-          const uint32_t a0 = ptx::smem_u32(sm.w[s]);
-          const uint32_t b0 = ptx::smem_u32(sm.x[s]);
 #pragma unroll
-          for (int kk = 0; kk < BK / 32; ++kk) {
-            if (PAIR)
-              ptx::mma_e4m3_pair(d, ptx::sdesc_sw128(a0 + kk * 32),
-                                 ptx::sdesc_sw128(b0 + kk * 32), idesc, (kb | kk) != 0 ? 1u : 0u);
-            else
-              ptx::mma_e4m3(d, ptx::sdesc_sw128(a0 + kk * 32), ptx::sdesc_sw128(b0 + kk * 32),
-                            idesc, (kb | kk) != 0 ? 1u : 0u);
+          for (int kc = 0; kc < KC; ++kc) {
+            const uint32_t a0 = ptx::smem_u32(sm.w[s][kc]);
+            const uint32_t b0 = ptx::smem_u32(sm.x[s][kc]);
+#pragma unroll
+            for (int kk = 0; kk < BK / 32; ++kk) {
+              const uint32_t acc = (ks | kc | kk) != 0 ? 1u : 0u;
+              if (PAIR)
+                ptx::mma_e4m3_pair(d, ptx::sdesc_sw128(a0 + kk * 32),
+                                   ptx::sdesc_sw128(b0 + kk * 32), idesc, acc);
+              else
+                ptx::mma_e4m3(d, ptx::sdesc_sw128(a0 + kk * 32), ptx::sdesc_sw128(b0 + kk * 32),
+                              idesc, acc);
+            }
           }
           issued = true;
           if (PAIR)
@@ -418,10 +431,12 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int mine0 = holds_gate ? 0 : 16;
         uint16_t* ost = sm.stage_out[q];
         const int jrow = t.nb * 64 + pair * 32;  // first j of this warp's 32
+        const bool amax = p.row_amax != nullptr;
+        // the next chunk's TMEM load is in flight while this one is processed
+        uint32_t v[32];
+        ptx::tmem_ld_32x32b_x32(tbase, v);
 #pragma unroll 1
         for (int c = 0; c < nchunk; ++c) {
-          uint32_t v[32];
-          ptx::tmem_ld_32x32b_x32(tbase + c * 32, v);
           ptx::tmem_ld_wait();
           ptx::reg_fence(v);
           float* give = sm.xchg[pair][c & 1] + (holds_gate ? 16 * 32 : 0);
@@ -433,6 +448,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             own_v[i] = holds_gate ? lo : hi;
             give[i * 32 + lane] = holds_gate ? hi : lo;
           }
+          if (c + 1 < nchunk) ptx::tmem_ld_32x32b_x32(tbase + (c + 1) * 32, v);
           bar_sync_named(1 + pair, 64);
           const int tk0 = c * 32 + mine0;
           const float sa_l =
@@ -440,14 +456,14 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const float other = take[i * 32 + lane];
-            const float own = own_v[i];
             const float sa = __shfl_sync(kFull, sa_l, i);
-            const float g = (holds_gate ? own : other) * sa * sg;
-            const float u = (holds_gate ? other : own) * sa * su;
-            const float h = g / (1.0f + __expf(-g)) * u;
-            const __nv_bfloat16 hb = __float2bfloat16_rn(h);
+            const float g = (holds_gate ? own_v[i] : other) * sa * sg;
+            const float u = (holds_gate ? other : own_v[i]) * sa * su;
+            // silu(g) * u; the result is rounded to bf16, so a fast divide
+            // (2 ulp) is well inside its precision
+            const __nv_bfloat16 hb = __float2bfloat16_rn(__fdividef(g, 1.0f + __expf(-g)) * u);
             ost[i * 32 + lane] = __bfloat16_as_ushort(hb);
-            if (p.row_amax != nullptr) {
+            if (amax) {
               const float m = warp_max(jv ? fabsf(__bfloat162float(hb)) : 0.0f);
               if (lane == 0 && tk0 + i < t.ntok)
                 atomicMax(reinterpret_cast<int*>(p.row_amax + t.tok0 + tk0 + i),
@@ -601,11 +617,11 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
   return true;
 }
 
-template <int BNMAX, int STAGES, bool SILU, int CS>
+template <int BNMAX, int STAGES, bool SILU, int CS, int KC>
 cudaError_t launch_cfg(const Maps& maps, const Params& p, int M, int E, cudaStream_t st) {
-  constexpr size_t smem = sizeof(Smem<BNMAX / CS, STAGES, SILU>) + 1024;
+  constexpr size_t smem = sizeof(Smem<BNMAX / CS, STAGES, SILU, KC>) + 1024;
   static_assert(smem <= 227 * 1024, "shared memory budget");
-  auto kern = grouped_gemm_kernel<BNMAX, STAGES, SILU, CS>;
+  auto kern = grouped_gemm_kernel<BNMAX, STAGES, SILU, CS, KC>;
   static std::mutex mu;
   static bool attr_set[64] = {};
   int dev = 0;
@@ -678,15 +694,15 @@ cudaError_t launch_grouped_gemm(const void* A, const float* scale_a, const void*
   // weights streamed once; many (prefill): tiles of up to 256 tokens
   p.stream_weights = small ? 1 : 0;
   if (small)
-    return silu ? launch_cfg<64, 8, true, 1>(maps, p, M, E, st)
-                : launch_cfg<64, 8, false, 1>(maps, p, M, E, st);
+    return silu ? launch_cfg<64, 8, true, 1, 1>(maps, p, M, E, st)
+                : launch_cfg<64, 8, false, 1, 1>(maps, p, M, E, st);
   // many tokens per expert: CTA pairs on pairs of weight blocks (2-SM MMA),
-  // 6 stages of 16 KB weights + 16 KB tokens per CTA
+  // 3 stages of 2 x (16 KB weights + 16 KB tokens) per CTA
   if (p.NB % 2 == 0)
-    return silu ? launch_cfg<256, 6, true, 2>(maps, p, M, E, st)
-                : launch_cfg<256, 6, false, 2>(maps, p, M, E, st);
-  return silu ? launch_cfg<256, 4, true, 1>(maps, p, M, E, st)
-              : launch_cfg<256, 4, false, 1>(maps, p, M, E, st);
+    return silu ? launch_cfg<256, PAIR_STAGES, true, 2, PAIR_KC>(maps, p, M, E, st)
+                : launch_cfg<256, PAIR_STAGES, false, 2, PAIR_KC>(maps, p, M, E, st);
+  return silu ? launch_cfg<256, 4, true, 1, 1>(maps, p, M, E, st)
+              : launch_cfg<256, 4, false, 1, 1>(maps, p, M, E, st);
 }
 
 }  // namespace moe

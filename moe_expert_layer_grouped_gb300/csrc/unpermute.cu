@@ -2,7 +2,9 @@
 // down[src2dst[t*K+k]] accumulated in fp32 in slot order (the role of
 // moe_sum_reduce in "[1/2] sgl-kernel: Fuse routed scaling factor into
 // select_experts", sglang #8364, Motivation; routed_scaling_factor is
-// already inside w). One CTA per token, 128-bit gathers of the K rows.
+// already inside w). CTAs of 128 threads take one token and a slice of 2048
+// columns (so small batches still spread over the SMs); 128-bit gathers of
+// the K rows.
 #include "common.cuh"
 #include "internal.h"
 
@@ -10,6 +12,7 @@ namespace moe {
 namespace {
 
 constexpr int kThreads = 128;
+constexpr int kVecPerBlock = 256;  // 16-byte vectors (2048 bf16) per CTA
 
 __global__ void __launch_bounds__(kThreads)
     unpermute_kernel(const __nv_bfloat16* __restrict__ down, const int32_t* __restrict__ src2dst,
@@ -19,6 +22,7 @@ __global__ void __launch_bounds__(kThreads)
   __shared__ float w[32];
   const int t = blockIdx.x;
   const int64_t M = (int64_t)gridDim.x * K;
+  const int v0 = blockIdx.y * kVecPerBlock;
   if (threadIdx.x < K) {
     const int d = __ldg(src2dst + (int64_t)t * K + threadIdx.x);
     float wk = __ldg(topk_w + (int64_t)t * K + threadIdx.x);
@@ -32,9 +36,9 @@ __global__ void __launch_bounds__(kThreads)
     w[threadIdx.x] = wk;
   }
   __syncthreads();
-  const int nvec = H >> 3;
+  const int nvec = min(H >> 3, v0 + kVecPerBlock);
   uint4* o = reinterpret_cast<uint4*>(out + (int64_t)t * H);
-  for (int i = threadIdx.x; i < nvec; i += kThreads) {
+  for (int i = v0 + threadIdx.x; i < nvec; i += kThreads) {
     float acc[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
@@ -59,7 +63,8 @@ __global__ void __launch_bounds__(kThreads)
 cudaError_t launch_unpermute_sum(const void* down, const int32_t* src2dst, const float* w,
                                  int T, int K, int H, void* out, int* err, cudaStream_t st) {
   if (T == 0) return cudaSuccess;
-  unpermute_kernel<<<T, kThreads, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(down),
+  const dim3 grid(T, (H / 8 + kVecPerBlock - 1) / kVecPerBlock);
+  unpermute_kernel<<<grid, kThreads, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(down),
                                            src2dst, w, K, H,
                                            reinterpret_cast<__nv_bfloat16*>(out), err);
   return cudaGetLastError();
