@@ -4,11 +4,13 @@
 // sglang #8364, Motivation and Highlights).
 //
 // Lane l holds experts [l*EPL, (l+1)*EPL) in registers. Group scores (sum of
-// the two largest biased scores per group) are computed from a per-warp
-// shared-memory copy of the keys; the topk_group groups and then the top_k
-// experts are picked by repeated warp arg-max reductions (key descending,
-// index ascending), so the result does not depend on scheduling and matches
-// a sort with ties broken by the lower index.
+// the two largest biased scores per group) come from a butterfly merge of the
+// lanes' top-2 pairs when a group is a power-of-two number of whole lanes
+// (DeepSeek-V3: 4 lanes x 8 experts), else from a per-warp shared-memory copy
+// of the keys. The topk_group groups and then the top_k experts are picked
+// by repeated warp maxima over (order-preserving key, index) packed in 64
+// bits (key descending, index ascending), so the result does not depend on
+// scheduling and matches a sort with ties broken by the lower index.
 //
 // Every floating-point step that decides an id or a weight uses explicit
 // round-to-nearest intrinsics (no contraction), so the fp32 scores are
@@ -70,6 +72,29 @@ __device__ __forceinline__ void warp_argmax(float& v, int& i, float& carry) {
   }
 }
 
+// Total order on fp32 keys as unsigned integers (larger float -> larger
+// integer; -0 and +0 equal, as in IEEE comparison), packed with the index so
+// that one unsigned max picks the larger key and, among equal keys, the lower
+// index. 0 is below every packed key.
+__device__ __forceinline__ uint64_t pack_key(float f, int idx) {
+  uint32_t u = __float_as_uint(f == 0.0f ? 0.0f : f);
+  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return ((uint64_t)u << 32) | (uint32_t)(0xFFFFFFFFu - (uint32_t)idx);
+}
+
+__device__ __forceinline__ int packed_index(uint64_t k) {
+  return (int)(0xFFFFFFFFu - (uint32_t)(k & 0xFFFFFFFFull));
+}
+
+__device__ __forceinline__ uint64_t warp_max_u64(uint64_t v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const uint64_t ov = __shfl_xor_sync(kFull, v, o);
+    v = ov > v ? ov : v;
+  }
+  return v;
+}
+
 constexpr int kWarpsPerBlock = 4;
 
 template <int EPL>
@@ -107,7 +132,38 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
   // ---- group-limited selection -------------------------------------------
   const int gsz = E / G;
   uint64_t kept = ~0ull;
-  if (TG < G) {
+  // groups made of whole lanes (a power-of-two number of them): the group's
+  // two largest keys by a butterfly merge of per-lane top-2 pairs
+  const int lpg = gsz / EPL;
+  const bool lane_groups = TG < G && gsz % EPL == 0 && (lpg & (lpg - 1)) == 0;
+  if (lane_groups) {
+    float b1 = -CUDART_INF_F, b2 = -CUDART_INF_F;
+#pragma unroll
+    for (int j = 0; j < EPL; ++j) {
+      const float v = key[j];
+      if (v > b1) {
+        b2 = b1;
+        b1 = v;
+      } else if (v > b2) {
+        b2 = v;
+      }
+    }
+    for (int o = 1; o < lpg; o <<= 1) {
+      const float ob1 = __shfl_xor_sync(kFull, b1, o);
+      const float ob2 = __shfl_xor_sync(kFull, b2, o);
+      const float n2 = fmaxf(fminf(b1, ob1), fmaxf(b2, ob2));
+      b1 = fmaxf(b1, ob1);
+      b2 = n2;
+    }
+    const float gscore = (gsz >= 2) ? __fadd_rn(b1, b2) : b1;
+    const int gid = (lane * EPL) / gsz;
+    const bool has = lane * EPL < E;
+    kept = 0ull;
+    for (int it = 0; it < TG; ++it) {
+      const uint64_t c = (has && !((kept >> gid) & 1ull)) ? pack_key(gscore, gid) : 0ull;
+      kept |= 1ull << packed_index(warp_max_u64(c));
+    }
+  } else if (TG < G) {
     // padded index e + e/32 keeps the group scans free of bank conflicts
     float* ks = keys_smem + warp * (E + (E >> 5) + 1);
 #pragma unroll
@@ -156,24 +212,28 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
   }
 
   // ---- top-k over the kept groups ----------------------------------------
-  uint32_t taken = 0;
+  uint32_t open = 0;  // this lane's experts still eligible
+#pragma unroll
+  for (int j = 0; j < EPL; ++j) {
+    const int e = lane * EPL + j;
+    if (e < E && ((kept >> (e / gsz)) & 1ull)) open |= 1u << j;
+  }
   float my_s = 0.0f, S = 0.0f, m0 = 0.0f;
   int my_id = 0;
   for (int k = 0; k < K; ++k) {
-    float bv = -CUDART_INF_F, bs = 0.0f;
-    int bi = 0x7fffffff;
+    uint64_t c = 0ull;
 #pragma unroll
     for (int j = 0; j < EPL; ++j) {
-      const int e = lane * EPL + j;
-      const bool ok = e < E && !((taken >> j) & 1u) && ((kept >> (e / gsz)) & 1ull);
-      if (ok && (key[j] > bv || bi == 0x7fffffff)) {
-        bv = key[j];
-        bi = e;
-        bs = sv[j];
-      }
+      const uint64_t cj = ((open >> j) & 1u) ? pack_key(key[j], lane * EPL + j) : 0ull;
+      c = cj > c ? cj : c;
     }
-    warp_argmax(bv, bi, bs);
-    if (bi / EPL == lane) taken |= 1u << (bi % EPL);
+    const int bi = packed_index(warp_max_u64(c));
+    const int slot = bi & (EPL - 1);
+    if (bi / EPL == lane) open &= ~(1u << slot);
+    float sel = sv[0];
+#pragma unroll
+    for (int j = 1; j < EPL; ++j) sel = (slot == j) ? sv[j] : sel;
+    const float bs = __shfl_sync(kFull, sel, bi / EPL);
     float term = bs;
     if (!sigmoid) {
       if (k == 0) m0 = bs;
