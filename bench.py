@@ -146,6 +146,26 @@ def step_work(wl, offsets_list):
     return avg
 
 
+def max_over_ranks(value, dist, device):
+    """The slowest rank's value (timing is taken as the max over ranks)."""
+    import torch
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(tokens_per_rank, world, ms_per_step):
+    """Whole-job throughput: every rank processes its own batch each step."""
+    return world * tokens_per_rank / (ms_per_step * 1e-3)
+
+
+def rank_seed(seed, rank):
+    """Each replica draws its own token batches (weights are per-rank copies)."""
+    return seed + rank
+
+
 def kernel_source_hash():
     h = hashlib.sha256()
     for f in ("gemm.cu", "ptx.cuh", "common.cuh"):
@@ -380,25 +400,18 @@ def run_ours(args):
     wl = synth.WORKLOADS[args.workload]
     steps = args.steps if args.steps is not None else max(20, int(4000 * 128 / wl.T))
     warmup = max(3, args.warmup)
-    seed = args.seed + rank
+    seed = rank_seed(args.seed, rank)
 
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     r = run_workload(moe, synth, torch, wl, seed, steps, warmup, dev, pk, want_clocks=True)
-    ms_total = r["ms_total"]
-    if world > 1:
-        t = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(r["ms_total"], dist if world > 1 else None, dev)
     ms = ms_total / steps
-    value = world * wl.T / (ms * 1e-3)
+    value = job_tokens_per_s(wl.T, world, ms)
 
     e2e_ms, h2d, d2h = time_e2e(r["layer"], r["batches"], steps, warmup, torch)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, dist if world > 1 else None, dev)
 
     line = {
         "metric": "MoE-layer tokens/s + % of FP8/HBM roofline, DeepSeek-V3 shape T=128/8192",
@@ -418,7 +431,7 @@ def run_ours(args):
         "active_experts": r["work"]["active"],
         "kernels_ms": {k: round(v, 4) for k, v in r["kern"].items()},
         "roofline": roofline_decode(r, pk, wl.name) if wl.T <= 512 else roofline_prefill(r, pk),
-        "e2e": {"value": round(world * wl.T / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
+        "e2e": {"value": round(job_tokens_per_s(wl.T, world, e2e_ms), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": steps * LAUNCHES_PER_FORWARD,
         "clocks": r["clocks"],
