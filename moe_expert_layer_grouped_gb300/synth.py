@@ -19,6 +19,10 @@ DeepSeek-V3-style and a Mixtral-style MoE layer):
                      the rest ~N(0, 0.1)
   dsv3_decode_t128_e32 / dsv3_prefill_t2048_e32: the DeepSeek-V3 layer with
                      32 experts, small cases for profiling
+  *_shared           the same layers plus n_shared shared experts (DeepSeek-V3
+                     has one, of the routed experts' size), stored after the
+                     routed experts in w13/w2 and drawn after them from the
+                     same streams, so the routed weights are unchanged
 Hidden states and router logits ~N(0, 1); weights ~N(0, 0.02).
 """
 from dataclasses import dataclass, replace
@@ -44,6 +48,7 @@ class Workload:
     renormalize: bool
     rsf: float
     bias: str  # "none" | "normal" | "zero" | "skewed"
+    n_shared: int = 0  # shared experts, stored as experts E .. E+n_shared-1
 
     @property
     def M(self):
@@ -70,6 +75,9 @@ WORKLOADS = {
     "dsv3_prefill_t2048_e32": Workload("dsv3_prefill_t2048_e32", 2048, 7168, 2048, 32, 8, 4, 8,
                                        SIGMOID, True, 2.5, "zero"),
 }
+for _name, _S in [("tiny", 1), ("dsv3_decode_t128", 1), ("dsv3_prefill_t8192", 1)]:
+    WORKLOADS[f"{_name}_shared"] = replace(WORKLOADS[_name], name=f"{_name}_shared",
+                                           n_shared=_S)
 
 # tensor ids: each tensor draws from its own generator stream
 _TID = {"x": 0, "logits": 1, "bias": 2, "w13": 3, "w2": 4}
@@ -123,7 +131,8 @@ def make_inputs(wl: Workload, seed=0, device="cpu", weights=True):
 
     x: bf16 [T,H]; logits: f32 [T,E]; bias: f32 [E] or None;
     w13: u8 [E,2I,H] (rows 0..I-1 gate, I..2I-1 up) with s13 f32 [E,2I];
-    w2: u8 [E,H,I] with s2 f32 [E,H].
+    w2: u8 [E,H,I] with s2 f32 [E,H]; with n_shared shared experts the
+    leading dimension is E + n_shared.
     """
     d = dict(
         x=normal((wl.T, wl.H), 1.0, seed, "x", device, torch.bfloat16),
@@ -131,8 +140,9 @@ def make_inputs(wl: Workload, seed=0, device="cpu", weights=True):
         bias=router_bias(wl, seed, device),
     )
     if weights:
-        d["w13"], d["s13"] = expert_weights(wl.E, 2 * wl.I, wl.H, seed, "w13", device)
-        d["w2"], d["s2"] = expert_weights(wl.E, wl.H, wl.I, seed, "w2", device)
+        n = wl.E + wl.n_shared
+        d["w13"], d["s13"] = expert_weights(n, 2 * wl.I, wl.H, seed, "w13", device)
+        d["w2"], d["s2"] = expert_weights(n, wl.H, wl.I, seed, "w2", device)
     return d
 
 

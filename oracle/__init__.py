@@ -47,6 +47,9 @@ def lib():
             "oracle_unpermute_sum": (None, [P, P, P, i32, i32, i32, P]),
             "oracle_forward_tokens": (i32, [P, P, P, P, P, P, P, i32, i32, i32, i32, i32,
                                             i32, i32, i32, i32, f32, P, i32, P, P, P]),
+            "oracle_forward_tokens_shared": (i32, [P, P, P, P, P, P, P, i32, i32, i32, i32,
+                                                   i32, i32, i32, i32, i32, i32, f32, P, i32,
+                                                   P, P, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -203,16 +206,19 @@ def unpermute_sum(down, src2dst, topk_w):
 
 
 def forward_tokens(x_bits, logits, bias, w13, s13, w2, s2, num_groups, topk_group,
-                   top_k, scoring, renormalize, routed_scaling_factor, tokens=None):
+                   top_k, scoring, renormalize, routed_scaling_factor, tokens=None,
+                   n_shared=0):
     """Whole layer for the listed tokens (all tokens when None).
 
-    Returns (out [n,H] fp64, ids [n,K], w [n,K])."""
+    With n_shared > 0, w13/w2 (and their scales) hold E + n_shared experts, the
+    last n_shared being shared experts that every token adds with weight 1.
+    Returns (out [n,H] fp64, ids [n,K], w [n,K]) (routed slots only)."""
     x = _c(x_bits, np.uint16)
     logits = _c(logits, np.float32)
     T, H = x.shape
     E = logits.shape[1]
     I = w2.shape[2]
-    assert w13.shape == (E, 2 * I, H) and w2.shape == (E, H, I)
+    assert w13.shape == (E + n_shared, 2 * I, H) and w2.shape == (E + n_shared, H, I)
     b = None if bias is None else _c(bias, np.float32)
     tok = np.arange(T, dtype=np.int64) if tokens is None else _c(tokens, np.int64)
     n = tok.size
@@ -223,23 +229,31 @@ def forward_tokens(x_bits, logits, bias, w13, s13, w2, s2, num_groups, topk_grou
     w2 = _c(w2, np.uint8)
     s13 = _c(s13, np.float32)
     s2 = _c(s2, np.float32)
-    rc = lib().oracle_forward_tokens(_p(x), _p(logits), _p(b), _p(w13), _p(s13), _p(w2),
-                                     _p(s2), T, H, I, E, num_groups, topk_group, top_k,
-                                     scoring, int(bool(renormalize)),
-                                     float(routed_scaling_factor), _p(tok), n, _p(out),
-                                     _p(ids), _p(w))
+    rc = lib().oracle_forward_tokens_shared(_p(x), _p(logits), _p(b), _p(w13), _p(s13),
+                                            _p(w2), _p(s2), T, H, I, E, int(n_shared),
+                                            num_groups, topk_group, top_k, scoring,
+                                            int(bool(renormalize)),
+                                            float(routed_scaling_factor), _p(tok), n, _p(out),
+                                            _p(ids), _p(w))
     if rc != 0:
         raise ValueError(f"oracle_forward_tokens: status {rc}")
     return out, ids, w
 
 
 def forward_steps(x_bits, logits, bias, w13, s13, w2, s2, num_groups, topk_group, top_k,
-                  scoring, renormalize, routed_scaling_factor):
+                  scoring, renormalize, routed_scaling_factor, n_shared=0):
     """The layer step by step over all tokens, returning every intermediate
-    (small configurations only: materialises [M, 2I] in fp64)."""
+    (small configurations only: materialises [M, 2I] in fp64). Shared experts
+    (n_shared > 0) take slots K .. K+n_shared-1 of every token, ids E.., weight 1."""
     E = logits.shape[1]
     ids, w = gate(logits, bias, num_groups, topk_group, top_k, scoring, renormalize,
                   routed_scaling_factor)
+    if n_shared:
+        T = ids.shape[0]
+        ids = np.concatenate([ids, np.broadcast_to(
+            np.arange(E, E + n_shared, dtype=np.int32), (T, n_shared))], axis=1)
+        w = np.concatenate([w, np.ones((T, n_shared), np.float32)], axis=1)
+        E += n_shared
     a_q, sa, src2dst, offsets = permute_quant(x_bits, ids, E)
     C13 = grouped_gemm(a_q, sa, w13, s13, offsets)
     h = silu_mul(C13)

@@ -499,8 +499,29 @@ int oracle_forward_tokens(const uint16_t* x, const float* logits,
                           int renormalize, float routed_scaling_factor,
                           const int64_t* tokens, int n_tok, double* out,
                           int32_t* ids_out, float* w_out) {
+  return oracle_forward_tokens_shared(x, logits, bias, w13, s13, w2, s2, T, H, I, E, 0,
+                                      num_groups, topk_group, top_k, scoring, renormalize,
+                                      routed_scaling_factor, tokens, n_tok, out, ids_out,
+                                      w_out);
+}
+
+/* The layer with n_shared shared experts ("[1/2] sgl-kernel: Fuse routed
+ * scaling factor into select_experts", sglang #8364, Highlights: shared expert
+ * fusion alongside the fused scaling factor). Reading: every token also runs
+ * experts E .. E+n_shared-1 of w13/w2, each added with weight 1 after the K
+ * routed slots (routed_scaling_factor is already inside the routed weights),
+ * i.e. the DeepSeek-V3 layer output shared(x) + sum_k w_k expert_k(x). */
+int oracle_forward_tokens_shared(const uint16_t* x, const float* logits,
+                                 const float* bias, const uint8_t* w13,
+                                 const float* s13, const uint8_t* w2, const float* s2,
+                                 int T, int H, int I, int E, int n_shared,
+                                 int num_groups, int topk_group, int top_k, int scoring,
+                                 int renormalize, float routed_scaling_factor,
+                                 const int64_t* tokens, int n_tok, double* out,
+                                 int32_t* ids_out, float* w_out) {
   int rc = gate_check(T, E, num_groups, topk_group, top_k, scoring, bias);
   if (rc) return rc;
+  if (n_shared < 0) return -1;
   for (int i = 0; i < n_tok; ++i)
     if (tokens[i] < 0 || tokens[i] >= T) return -1;
   init_lut();
@@ -543,8 +564,9 @@ int oracle_forward_tokens(const uint16_t* x, const float* logits,
       for (int hh = 0; hh < H; ++hh)
         a[hh] = g_e4m3_lut[oracle_e4m3_encode(bf16_to_f32(xr[hh]) / sa)];
       for (int cc = 0; cc < H; ++cc) o[cc] = 0.0;
-      for (int k = 0; k < K; ++k) {
-        int e = ids[k];
+      for (int k = 0; k < K + n_shared; ++k) {
+        /* routed slots, then the shared experts with weight 1 */
+        const int e = k < K ? ids[k] : E + (k - K);
         const uint8_t* We = w13 + (int64_t)e * N13 * H;
         for (int n = 0; n < N13; ++n) {
           const uint8_t* b = We + (int64_t)n * H;
@@ -563,7 +585,7 @@ int oracle_forward_tokens(const uint16_t* x, const float* logits,
         for (int j = 0; j < I; ++j)
           h2[j] = g_e4m3_lut[oracle_e4m3_encode(bf16_to_f32(hb[j]) / sa2)];
         const uint8_t* W2e = w2 + (int64_t)e * H * I;
-        double wk = (double)w[k];
+        double wk = k < K ? (double)w[k] : 1.0;
         for (int cc = 0; cc < H; ++cc) {
           const uint8_t* b = W2e + (int64_t)cc * I;
           double acc = 0.0;

@@ -109,6 +109,19 @@ int oracle_forward_tokens(const uint16_t* x, const float* logits,
                           const int64_t* tokens, int n_tok, double* out,
                           int32_t* ids_out, float* w_out);
 
+/* The same with n_shared shared experts stored as experts E .. E+n_shared-1
+ * of w13 [E+n_shared,2I,H] / w2 [E+n_shared,H,I] (scales likewise): each
+ * token adds every shared expert's output with weight 1 after its K routed
+ * experts. The gate sees only the E routed experts. */
+int oracle_forward_tokens_shared(const uint16_t* x, const float* logits,
+                                 const float* bias, const uint8_t* w13,
+                                 const float* s13, const uint8_t* w2, const float* s2,
+                                 int T, int H, int I, int E, int n_shared,
+                                 int num_groups, int topk_group, int top_k, int scoring,
+                                 int renormalize, float routed_scaling_factor,
+                                 const int64_t* tokens, int n_tok, double* out,
+                                 int32_t* ids_out, float* w_out);
+
 #ifdef __cplusplus
 }
 #endif

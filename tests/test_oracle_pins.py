@@ -415,6 +415,22 @@ def _random_layer(rng, T, H, I, E):
     return x, logits, w13.numpy(), s13.numpy(), w2.numpy(), s2.numpy()
 
 
+def _dense_fp8_mlp(x, w13e, s13e, w2e, s2e):
+    """One expert applied to every token, with numpy matmuls: per-token FP8
+    input, w13 with both scales, silu(gate)*up rounded to bf16, per-token
+    requantisation, w2 with both scales."""
+    I = w2e.shape[1]
+    q, sa = oracle.row_quant(x)
+    C = (oracle.e4m3_decode(q) @ oracle.e4m3_decode(w13e).T) * sa[:, None].astype(np.float64) \
+        * s13e[None, :].astype(np.float64)
+    g, u = C[:, :I], C[:, I:]
+    h = g / (1 + np.exp(-g)) * u
+    hb = oracle.bf16_round(h)
+    q2, sa2 = oracle.row_quant(hb)
+    return (oracle.e4m3_decode(q2) @ oracle.e4m3_decode(w2e).T) * sa2[:, None].astype(np.float64) \
+        * s2e[None, :].astype(np.float64)
+
+
 def test_layer_single_expert_is_dense_fp8_mlp():
     """E=1, K=1, rsf=1: routing is the identity and the layer is a dense FP8
     MLP, computed here with numpy matmuls."""
@@ -424,16 +440,34 @@ def test_layer_single_expert_is_dense_fp8_mlp():
     out, ids, w = oracle.forward_tokens(x, logits, None, w13, s13, w2, s2, 1, 1, 1,
                                         oracle.SOFTMAX, True, 1.0)
     assert np.all(ids == 0) and np.all(w == 1.0)
-    q, sa = oracle.row_quant(x)
-    C = (oracle.e4m3_decode(q) @ oracle.e4m3_decode(w13[0]).T) * sa[:, None].astype(np.float64) \
-        * s13[0][None, :].astype(np.float64)
-    g, u = C[:, :I], C[:, I:]
-    h = g / (1 + np.exp(-g)) * u
-    hb = oracle.bf16_round(h)
-    q2, sa2 = oracle.row_quant(hb)
-    ref = (oracle.e4m3_decode(q2) @ oracle.e4m3_decode(w2[0]).T) * sa2[:, None].astype(np.float64) \
-        * s2[0][None, :].astype(np.float64)
+    ref = _dense_fp8_mlp(x, w13[0], s13[0], w2[0], s2[0])
     np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max())
+
+
+@pytest.mark.parametrize("n_shared", [1, 2])
+def test_layer_shared_experts_add_dense_mlps(n_shared):
+    """Shared experts (stored after the E routed ones) add each one's dense
+    FP8 MLP with weight 1, whatever routed_scaling_factor is: the layer with
+    them minus the layer without them is the sum of those MLPs (numpy)."""
+    rng = np.random.default_rng(40 + n_shared)
+    T, H, I, E = 12, 64, 32, 8
+    x, logits, w13, s13, w2, s2 = _random_layer(rng, T, H, I, E + n_shared)
+    bias = (rng.standard_normal(E) * 0.1).astype(np.float32)
+    args = (4, 2, 3, oracle.SIGMOID, True, 2.5)
+    base, ids0, w0 = oracle.forward_tokens(x, logits[:, :E], bias, w13[:E], s13[:E], w2[:E],
+                                           s2[:E], *args)
+    out, ids, w = oracle.forward_tokens(x, logits[:, :E], bias, w13, s13, w2, s2, *args,
+                                        n_shared=n_shared)
+    assert np.array_equal(ids, ids0) and np.array_equal(w, w0)  # the gate sees E experts
+    ref = sum(_dense_fp8_mlp(x, w13[E + j], s13[E + j], w2[E + j], s2[E + j])
+              for j in range(n_shared))
+    np.testing.assert_allclose(out - base, ref, rtol=1e-9, atol=1e-12 * np.abs(out).max())
+    # the step-by-step path (shared experts as extra slots of every token) agrees
+    steps = oracle.forward_steps(x, logits[:, :E], bias, w13, s13, w2, s2, *args,
+                                 n_shared=n_shared)
+    assert np.array_equal(steps["ids"][:, 3:], np.tile(np.arange(E, E + n_shared), (T, 1)))
+    assert np.all(steps["w"][:, 3:] == 1.0)
+    np.testing.assert_allclose(out, steps["out"], rtol=1e-12, atol=1e-12 * np.abs(out).max())
 
 
 def test_layer_token_path_equals_step_path_and_is_linear_in_rsf():
