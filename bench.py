@@ -125,8 +125,10 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 def step_work(wl, offsets_list):
     """Algorithmic bytes / flops per forward, averaged over the batches.
-    Weights count once per expert that received at least one token."""
-    T, H, I, E, K = wl.T, wl.H, wl.I, wl.E, wl.top_k
+    Weights count once per expert that received at least one token. Shared
+    experts count as experts every token visits (E + n_shared experts,
+    top_k + n_shared slots); the logits cover the E routed experts."""
+    T, H, I, E, K = wl.T, wl.H, wl.I, wl.E + wl.n_shared, wl.top_k + wl.n_shared
     M = T * K
     res = []
     for off in offsets_list:
@@ -138,7 +140,7 @@ def step_work(wl, offsets_list):
         gemm2_bytes = w2 + M * I + M * 4 + M * H * 2 + (E + 1) * 4
         flops13 = 2.0 * M * 2 * I * H
         flops2 = 2.0 * M * H * I
-        layer_bytes = w13 + w2 + T * H * 2 + T * E * 4 + T * H * 2
+        layer_bytes = w13 + w2 + T * H * 2 + T * wl.E * 4 + T * H * 2
         res.append(dict(active=active, gemm13_bytes=gemm13_bytes, gemm2_bytes=gemm2_bytes,
                         flops13=flops13, flops2=flops2, layer_bytes=layer_bytes,
                         layer_flops=flops13 + flops2))
@@ -224,12 +226,21 @@ def time_forward(layer, batches, steps, warmup, torch, out):
 
 def time_breakdown(moe, layer, wl, batches, steps, torch):
     """The same launches as moe_forward, issued step by step through the C ABI
-    with events between them, to time each kernel inside a running step."""
+    with events between them, to time each kernel inside a running step.
+    With shared experts the gate's K routed slots are widened to K + n_shared
+    by a torch copy between the gate's and the permute's events (moe_forward
+    does this inside its gate kernel), so it is not part of any kernel time."""
     dev = batches[0][0].device
-    T, H, I, E, K = wl.T, wl.H, wl.I, wl.E, wl.top_k
+    S = wl.n_shared
+    T, H, I, E, K = wl.T, wl.H, wl.I, wl.E + S, wl.top_k + S
     M = T * K
+    ids_r = torch.empty((T, wl.top_k), dtype=torch.int32, device=dev)
+    w_r = torch.empty((T, wl.top_k), dtype=torch.float32, device=dev)
     ids = torch.empty((T, K), dtype=torch.int32, device=dev)
     w = torch.empty((T, K), dtype=torch.float32, device=dev)
+    if S:
+        ids[:, wl.top_k:] = torch.arange(wl.E, E, dtype=torch.int32, device=dev)
+        w[:, wl.top_k:] = 1.0
     a_q = torch.empty((M, H), dtype=torch.uint8, device=dev)
     sa = torch.empty(M, dtype=torch.float32, device=dev)
     s2d = torch.empty(M, dtype=torch.int32, device=dev)
@@ -248,9 +259,14 @@ def time_breakdown(moe, layer, wl, batches, steps, torch):
     def one(i, ev):
         x, l = batches[i % len(batches)]
         if ev: ev[0].record(st)
-        moe.moe_gate(l, layer.bias, wl.num_groups, wl.topk_group, K, wl.scoring, wl.renormalize,
-                     wl.rsf, topk_ids=ids, topk_w=w)
+        moe.moe_gate(l, layer.bias, wl.num_groups, wl.topk_group, wl.top_k, wl.scoring,
+                     wl.renormalize, wl.rsf, topk_ids=ids if not S else ids_r,
+                     topk_w=w if not S else w_r)
         if ev: ev[1].record(st)
+        if S:
+            ids[:, :wl.top_k] = ids_r
+            w[:, :wl.top_k] = w_r
+        if ev: ev[7].record(st)
         moe.moe_permute_quant(x, ids, E, a_q=a_q, scale_a=sa, src2dst=s2d, offsets=off,
                               workspace=pws)
         if ev: ev[2].record(st)
@@ -266,14 +282,14 @@ def time_breakdown(moe, layer, wl, batches, steps, torch):
     for i in range(3):
         one(i, None)
     torch.cuda.synchronize()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(steps)]
     for i in range(steps):
         one(i, evs[i])
     torch.cuda.synchronize()
     tot = {n: 0.0 for n in names}
     for ev in evs:
         for j, n in enumerate(names):
-            tot[n] += ev[j].elapsed_time(ev[j + 1])
+            tot[n] += (ev[7] if j == 1 else ev[j]).elapsed_time(ev[j + 1])
     offs = []
     for b in range(len(batches)):
         one(b, None)
@@ -307,7 +323,8 @@ def time_e2e(layer, batches, steps, warmup, torch):
 def run_workload(moe, synth, torch, wl, seed, steps, warmup, dev, pk, want_clocks):
     d = synth.make_inputs(wl, seed=seed, device=dev, weights=True)
     layer = moe.MoELayer(d["w13"], d["s13"], d["w2"], d["s2"], d["bias"], wl.num_groups,
-                         wl.topk_group, wl.top_k, wl.scoring, wl.renormalize, wl.rsf, wl.T)
+                         wl.topk_group, wl.top_k, wl.scoring, wl.renormalize, wl.rsf, wl.T,
+                         n_shared=wl.n_shared)
     batches = make_batches(wl, seed, dev, synth)
     out = torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device=dev)
     clocks = ClockSampler(dev.index) if want_clocks else None
@@ -363,13 +380,14 @@ def cpu_baseline(synth, torch, wl, seed, r, budget_s=15.0):
             wl.num_groups, wl.topk_group, wl.top_k, wl.scoring, wl.renormalize, wl.rsf)
     threads = oracle.get_threads()
     t = time.time()
-    oracle.forward_tokens(*args, tokens=np.arange(min(threads, wl.T), dtype=np.int64))
+    oracle.forward_tokens(*args, tokens=np.arange(min(threads, wl.T), dtype=np.int64),
+                          n_shared=wl.n_shared)
     per_tok = (time.time() - t) / min(threads, wl.T)
     ntok = int(max(1, min(wl.T, budget_s / max(per_tok, 1e-6))))
     reps = max(1, int(budget_s / max(per_tok * ntok, 1e-6)))
     toks = np.tile(np.arange(ntok, dtype=np.int64), reps)
     t = time.time()
-    oracle.forward_tokens(*args, tokens=toks)
+    oracle.forward_tokens(*args, tokens=toks, n_shared=wl.n_shared)
     dt = time.time() - t
     return {"value": round(toks.size / dt, 3), "unit": "tokens/s", "cores": threads,
             "kind": "oracle",
@@ -422,7 +440,7 @@ def run_ours(args):
         "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E,
                    "num_groups": wl.num_groups, "topk_group": wl.topk_group, "top_k": wl.top_k,
                    "scoring": "sigmoid" if wl.scoring == 0 else "softmax", "rsf": wl.rsf,
-                   "batches_cycled": N_BATCHES,
+                   "n_shared": wl.n_shared, "batches_cycled": N_BATCHES,
                    "l2": "no flush: each step streams the active experts' weights "
                          f"(~{r['work']['layer_bytes'] / 1e9:.2f} GB) through the 129 MB L2",
                    "parallelism": f"replicas x{world} (no collective on the data path)"},
@@ -458,7 +476,8 @@ def run_ours(args):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         d = synth.make_inputs(wl, seed=seed, device=dev, weights=True)
         layer = moe.MoELayer(d["w13"], d["s13"], d["w2"], d["s2"], d["bias"], wl.num_groups,
-                             wl.topk_group, wl.top_k, wl.scoring, wl.renormalize, wl.rsf, wl.T)
+                             wl.topk_group, wl.top_k, wl.scoring, wl.renormalize, wl.rsf, wl.T,
+                             n_shared=wl.n_shared)
         line["cpu_baseline"] = cpu_baseline(synth, torch, wl, seed,
                                             {"layer": layer, "batches": make_batches(
                                                 wl, seed, dev, synth)})
@@ -493,16 +512,18 @@ def run_reference(args):
              wl.num_groups, wl.topk_group, wl.top_k, wl.scoring, wl.renormalize, wl.rsf)
     threads = oracle.get_threads()
     t = time.time()
-    oracle.forward_tokens(*fargs, tokens=np.arange(min(threads, wl.T), dtype=np.int64))
+    S = wl.n_shared
+    oracle.forward_tokens(*fargs, tokens=np.arange(min(threads, wl.T), dtype=np.int64),
+                          n_shared=S)
     per_tok = (time.time() - t) / min(threads, wl.T)
     budget = max(5.0, 60.0 / max(1, steps + warmup))
     ntok = int(max(1, min(wl.T, budget / max(per_tok, 1e-6))))
     toks = np.arange(ntok, dtype=np.int64)
     for _ in range(warmup):
-        oracle.forward_tokens(*fargs, tokens=toks)
+        oracle.forward_tokens(*fargs, tokens=toks, n_shared=S)
     t = time.time()
     for _ in range(steps):
-        oracle.forward_tokens(*fargs, tokens=toks)
+        oracle.forward_tokens(*fargs, tokens=toks, n_shared=S)
     dt = (time.time() - t) / steps
     value = ntok / dt
     sample = (f"{ntok} of the {wl.T} tokens of one {wl.name} batch per step, whole layer "
@@ -515,7 +536,7 @@ def run_reference(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "f64 (FP8 codes decoded exactly)",
         "data": "synthetic (seeded)",
         "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E,
-                   "top_k": wl.top_k},
+                   "top_k": wl.top_k, "n_shared": wl.n_shared},
         "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": threads,
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,

@@ -252,6 +252,43 @@ MOE_API moe_status moe_forward_host(const void* x_host, const float* logits_host
                             void* stream);
 
 /*
+ * moe_forward_shared — moe_forward plus n_shared shared experts, which every
+ * token runs besides its top_k routed experts. [P3] Highlights (sglang
+ * #8364) notes that shared-expert fusion works together with the scaling
+ * factor fused into the gate; the pages give no formula, so this takes the
+ * DeepSeek-V3 layer: out = sum_k w_k expert_k(x) + sum_j shared_j(x), the
+ * shared experts with weight 1 (routed_scaling_factor is already in w_k).
+ * Layout: the shared experts are experts E .. E+n_shared-1 of the weight
+ * tensors, of the routed experts' size: w13 [E+n_shared,2I,H],
+ * s13 [E+n_shared,2I], w2 [E+n_shared,H,I], s2 [E+n_shared,H]. logits and
+ * bias cover the E routed experts only. The gate appends the shared slots
+ * to each token's row and the rest of the layer runs as a routed layer of
+ * E+n_shared experts and top_k+n_shared slots, summed in slot order.
+ * ws: moe_workspace_size(T,H,I,E+n_shared,top_k+n_shared) bytes.
+ * n_shared == 0 is moe_forward. Limits: E+n_shared <= 1024,
+ * top_k+n_shared <= 32; otherwise those of moe_forward.
+ */
+MOE_API moe_status moe_forward_shared(const void* x, const float* logits,
+                              const float* bias, const void* w13,
+                              const float* s13, const void* w2, const float* s2,
+                              int T, int H, int I, int E, int n_shared,
+                              int num_groups, int topk_group, int top_k,
+                              int scoring, int renormalize,
+                              float routed_scaling_factor, void* out, void* ws,
+                              size_t ws_bytes, void* stream);
+
+/* moe_forward_shared with the per-step tensors in host memory, as
+ * moe_forward_host. */
+MOE_API moe_status moe_forward_shared_host(const void* x_host,
+                              const float* logits_host, const float* bias,
+                              const void* w13, const float* s13, const void* w2,
+                              const float* s2, int T, int H, int I, int E,
+                              int n_shared, int num_groups, int topk_group,
+                              int top_k, int scoring, int renormalize,
+                              float routed_scaling_factor, void* out_host,
+                              void* ws, size_t ws_bytes, void* stream);
+
+/*
  * moe_device_status — synchronises the current device, copies its device
  * error word into *code (one of MOE_DEV_*), clears it, and returns MOE_OK
  * when it was zero, MOE_ERR_DEVICE otherwise (MOE_ERR_CUDA if the copy

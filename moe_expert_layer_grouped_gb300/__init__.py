@@ -17,6 +17,7 @@ import os
 __all__ = [
     "MoEError", "SIGMOID", "SOFTMAX", "EPI_BF16", "EPI_SILU_MUL", "library_path", "load",
     "moe_gate", "moe_permute_quant", "moe_permute_workspace_size", "moe_grouped_gemm",
+    "moe_forward_shared", "moe_forward_shared_host",
     "moe_permute_quant_noalloc", "moe_act_quant", "moe_unpermute_sum", "moe_workspace_size", "moe_forward",
     "moe_forward_host", "moe_device_status", "MoELayer",
 ]
@@ -63,6 +64,10 @@ _SIGNATURES = {
                          _P, _P, _SZ, _P]),
     "moe_forward_host": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I,
                               _F, _P, _P, _SZ, _P]),
+    "moe_forward_shared": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I,
+                                _I, _F, _P, _P, _SZ, _P]),
+    "moe_forward_shared_host": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I,
+                                     _I, _I, _F, _P, _P, _SZ, _P]),
     "moe_device_status": (_I, [ctypes.POINTER(_I)]),
 }
 
@@ -214,12 +219,14 @@ def moe_workspace_size(T, H, I, E, K):
     return load().moe_workspace_size(T, H, I, E, K)
 
 
-def _dims(x, logits, w13, w2):
+def _dims(x, logits, w13, w2, n_shared=0):
     T, H = x.shape
     E = logits.shape[1]
     I = w2.shape[2]
-    if tuple(w13.shape) != (E, 2 * I, H) or tuple(w2.shape) != (E, H, I):
-        raise ValueError("moe_forward: weight shapes do not match [E,2I,H] / [E,H,I]")
+    n = E + n_shared
+    if tuple(w13.shape) != (n, 2 * I, H) or tuple(w2.shape) != (n, H, I):
+        raise ValueError("moe_forward: weight shapes do not match [E+n_shared,2I,H] / "
+                         "[E+n_shared,H,I]")
     return T, H, I, E
 
 
@@ -259,6 +266,43 @@ def moe_forward_host(x_host, logits_host, bias, w13, s13, w2, s2, num_groups, to
     return out_host
 
 
+def moe_forward_shared(x, logits, bias, w13, s13, w2, s2, n_shared, num_groups, topk_group,
+                       top_k, scoring=SIGMOID, renormalize=True, routed_scaling_factor=1.0,
+                       out=None, workspace=None, stream=None):
+    """moe_forward plus n_shared shared experts stored as experts E.. of w13/w2."""
+    import torch
+    _need_cuda(x, logits, bias, w13, s13, w2, s2, out, workspace)
+    T, H, I, E = _dims(x, logits, w13, w2, n_shared)
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=x.device) if out is None else out
+    if workspace is None:
+        nws = moe_workspace_size(T, H, I, E + n_shared, top_k + n_shared)
+        workspace = torch.empty(nws, dtype=torch.uint8, device=x.device)
+    _check("moe_forward_shared", load().moe_forward_shared(
+        _ptr(x), _ptr(logits), _ptr(bias), _ptr(_u8(w13)), _ptr(s13), _ptr(_u8(w2)), _ptr(s2),
+        T, H, I, E, int(n_shared), num_groups, topk_group, top_k, scoring,
+        int(bool(renormalize)), float(routed_scaling_factor), _ptr(out), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out
+
+
+def moe_forward_shared_host(x_host, logits_host, bias, w13, s13, w2, s2, n_shared, num_groups,
+                            topk_group, top_k, scoring, renormalize, routed_scaling_factor,
+                            out_host, workspace, stream=None):
+    """moe_forward_shared with x, logits and out in host memory (as moe_forward_host)."""
+    _need_cuda(bias, w13, s13, w2, s2, workspace)
+    for t in (x_host, logits_host, out_host):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError("moe_forward_shared_host: x, logits and out must be contiguous "
+                             "host tensors")
+    T, H, I, E = _dims(x_host, logits_host, w13, w2, n_shared)
+    _check("moe_forward_shared_host", load().moe_forward_shared_host(
+        _ptr(x_host), _ptr(logits_host), _ptr(bias), _ptr(_u8(w13)), _ptr(s13), _ptr(_u8(w2)),
+        _ptr(s2), T, H, I, E, int(n_shared), num_groups, topk_group, top_k, scoring,
+        int(bool(renormalize)), float(routed_scaling_factor), _ptr(out_host), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out_host
+
+
 def moe_device_status():
     """Synchronise the device and return (and clear) its device error code."""
     code = ctypes.c_int(0)
@@ -269,30 +313,45 @@ def moe_device_status():
 
 
 class MoELayer:
-    """A layer's resident weights plus a reusable workspace; calls moe_forward."""
+    """A layer's resident weights plus a reusable workspace; calls moe_forward
+    (moe_forward_shared when the layer has shared experts, stored as the last
+    n_shared experts of w13/w2)."""
 
     def __init__(self, w13, s13, w2, s2, bias, num_groups, topk_group, top_k, scoring,
-                 renormalize, routed_scaling_factor, max_tokens):
+                 renormalize, routed_scaling_factor, max_tokens, n_shared=0):
         import torch
         self.w13, self.s13, self.w2, self.s2, self.bias = w13, s13, w2, s2, bias
-        self.E, I2, self.H = w13.shape
+        EA, I2, self.H = w13.shape
+        self.n_shared = n_shared
+        self.E = EA - n_shared  # routed experts
         self.I = I2 // 2
         self.num_groups, self.topk_group, self.top_k = num_groups, topk_group, top_k
         self.scoring, self.renormalize, self.rsf = scoring, renormalize, routed_scaling_factor
         self.max_tokens = max_tokens
         self.workspace = torch.empty(
-            moe_workspace_size(max_tokens, self.H, self.I, self.E, top_k), dtype=torch.uint8,
-            device=w13.device)
+            moe_workspace_size(max_tokens, self.H, self.I, EA, top_k + n_shared),
+            dtype=torch.uint8, device=w13.device)
 
     def __call__(self, x, logits, out=None, stream=None):
         if x.shape[0] > self.max_tokens:
             raise ValueError("MoELayer: more tokens than the workspace was sized for")
+        if self.n_shared:
+            return moe_forward_shared(x, logits, self.bias, self.w13, self.s13, self.w2,
+                                      self.s2, self.n_shared, self.num_groups, self.topk_group,
+                                      self.top_k, self.scoring, self.renormalize, self.rsf,
+                                      out=out, workspace=self.workspace, stream=stream)
         return moe_forward(x, logits, self.bias, self.w13, self.s13, self.w2, self.s2,
                            self.num_groups, self.topk_group, self.top_k, self.scoring,
                            self.renormalize, self.rsf, out=out, workspace=self.workspace,
                            stream=stream)
 
     def forward_host(self, x_host, logits_host, out_host, stream=None):
+        if self.n_shared:
+            return moe_forward_shared_host(x_host, logits_host, self.bias, self.w13, self.s13,
+                                           self.w2, self.s2, self.n_shared, self.num_groups,
+                                           self.topk_group, self.top_k, self.scoring,
+                                           self.renormalize, self.rsf, out_host,
+                                           self.workspace, stream=stream)
         return moe_forward_host(x_host, logits_host, self.bias, self.w13, self.s13, self.w2,
                                 self.s2, self.num_groups, self.topk_group, self.top_k,
                                 self.scoring, self.renormalize, self.rsf, out_host,

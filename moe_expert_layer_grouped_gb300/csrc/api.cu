@@ -136,38 +136,44 @@ Tp* at(void* ws, size_t off) {
   return reinterpret_cast<Tp*>(static_cast<char*>(ws) + off);
 }
 
+// S: shared experts, stored after the E routed ones (0 for moe_forward).
 moe_status check_forward(const void* x, const float* logits, const float* bias, const void* w13,
                          const float* s13, const void* w2, const float* s2, int T, int H, int I,
-                         int E, int G, int TG, int K, int scoring, const void* out,
+                         int E, int S, int G, int TG, int K, int scoring, const void* out,
                          const void* ws, size_t ws_bytes) {
+  if (S < 0) return MOE_ERR_INVALID_ARG;
   if (H < 1 || I < 1 || H % 32 != 0 || I % 32 != 0) return MOE_ERR_INVALID_ARG;
   if (H > kMaxH) return MOE_ERR_UNSUPPORTED;
   // the gate check without its output pointers (they live in the workspace)
   if (T < 0 || E < 1 || G < 1 || TG < 1 || K < 1) return MOE_ERR_INVALID_ARG;
   if (E % G != 0 || TG > G || K > TG * (E / G)) return MOE_ERR_INVALID_ARG;
   if (scoring != MOE_SCORE_SIGMOID && scoring != MOE_SCORE_SOFTMAX) return MOE_ERR_INVALID_ARG;
-  if (E > kMaxE || K > kMaxK || G > 64) return MOE_ERR_UNSUPPORTED;
+  if (E + S > kMaxE || K + S > kMaxK || G > 64) return MOE_ERR_UNSUPPORTED;
   if (scoring == MOE_SCORE_SOFTMAX && (bias != nullptr || G != 1)) return MOE_ERR_UNSUPPORTED;
-  if ((int64_t)E * 2 * I >= ((int64_t)1 << 31) || (int64_t)E * H >= ((int64_t)1 << 31) ||
-      (int64_t)T * K >= ((int64_t)1 << 31))
+  if ((int64_t)(E + S) * 2 * I >= ((int64_t)1 << 31) ||
+      (int64_t)(E + S) * H >= ((int64_t)1 << 31) || (int64_t)T * (K + S) >= ((int64_t)1 << 31))
     return MOE_ERR_UNSUPPORTED;
   if (!ok_ptr(w13) || !ok_ptr(s13) || !ok_ptr(w2) || !ok_ptr(s2)) return MOE_ERR_INVALID_ARG;
   if (bias != nullptr && !aligned16(bias)) return MOE_ERR_INVALID_ARG;
   if (T > 0 && (!ok_ptr(x) || !ok_ptr(logits) || !ok_ptr(out))) return MOE_ERR_INVALID_ARG;
   if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0 ||
-      ws_bytes < fwd_layout(T, H, I, E, K).total)
+      ws_bytes < fwd_layout(T, H, I, E + S, K + S).total)
     return MOE_ERR_WORKSPACE;
   return MOE_OK;
 }
 
+// The gate picks K of the E routed experts and appends the S shared ones
+// (weight 1) to every token's row; from the permute on, the layer is a
+// routed layer of E + S experts and K + S slots.
 moe_status run_forward(const void* x, const float* logits, const float* bias, const void* w13,
                        const float* s13, const void* w2, const float* s2, int T, int H, int I,
-                       int E, int G, int TG, int K, int scoring, int renorm, float rsf,
+                       int E, int S, int G, int TG, int K, int scoring, int renorm, float rsf,
                        void* out, void* ws, cudaStream_t st) {
-  const FwdLayout L = fwd_layout(T, H, I, E, K);
+  const int EA = E + S, KA = K + S;  // experts and slots after the gate
+  const FwdLayout L = fwd_layout(T, H, I, EA, KA);
   int* err = device_error_word();
   if (err == nullptr) return MOE_ERR_CUDA;
-  const int M = T * K;
+  const int M = T * KA;
   int32_t* ids = at<int32_t>(ws, L.ids);
   float* w = at<float>(ws, L.w);
   int32_t* offsets = at<int32_t>(ws, L.offsets);
@@ -179,19 +185,19 @@ moe_status run_forward(const void* x, const float* logits, const float* bias, co
   void* q2 = at<void>(ws, L.q2);
   void* down = at<void>(ws, L.down);
   cudaError_t e;
-  if ((e = launch_gate(logits, bias, T, E, G, TG, K, scoring, renorm, rsf, ids, w, st)))
+  if ((e = launch_gate(logits, bias, T, E, G, TG, K, scoring, renorm, rsf, ids, w, S, st)))
     return cuda_status(e);
-  if ((e = launch_permute_quant(x, ids, T, H, E, K, a_q, sa, s2d, offsets, at<void>(ws, L.perm),
-                                err, st)))
+  if ((e = launch_permute_quant(x, ids, T, H, EA, KA, a_q, sa, s2d, offsets,
+                                at<void>(ws, L.perm), err, st)))
     return cuda_status(e);
-  if ((e = launch_grouped_gemm(a_q, sa, w13, s13, offsets, M, 2 * I, H, E, MOE_EPI_SILU_MUL, h,
+  if ((e = launch_grouped_gemm(a_q, sa, w13, s13, offsets, M, 2 * I, H, EA, MOE_EPI_SILU_MUL, h,
                                nullptr, err, st)))
     return cuda_status(e);
   if ((e = launch_act_quant(h, nullptr, M, I, q2, sa2, st))) return cuda_status(e);
-  if ((e = launch_grouped_gemm(q2, sa2, w2, s2, offsets, M, H, I, E, MOE_EPI_BF16, down, nullptr,
-                               err, st)))
+  if ((e = launch_grouped_gemm(q2, sa2, w2, s2, offsets, M, H, I, EA, MOE_EPI_BF16, down,
+                               nullptr, err, st)))
     return cuda_status(e);
-  if ((e = launch_unpermute_sum(down, s2d, w, T, K, H, out, err, st))) return cuda_status(e);
+  if ((e = launch_unpermute_sum(down, s2d, w, T, KA, H, out, err, st))) return cuda_status(e);
   return MOE_OK;
 }
 
@@ -224,7 +230,7 @@ moe_status moe_gate(const float* logits, const float* bias, int T, int E, int nu
                             topk_w);
   if (s != MOE_OK) return s;
   return cuda_status(launch_gate(logits, bias, T, E, num_groups, topk_group, top_k, scoring,
-                                 renormalize, routed_scaling_factor, topk_ids, topk_w,
+                                 renormalize, routed_scaling_factor, topk_ids, topk_w, 0,
                                  static_cast<cudaStream_t>(stream)));
 }
 
@@ -304,18 +310,61 @@ size_t moe_workspace_size(int T, int H, int I, int E, int K) {
   return fwd_layout(T, H, I, E, K).total;
 }
 
+moe_status moe_forward_shared(const void* x, const float* logits, const float* bias,
+                              const void* w13, const float* s13, const void* w2, const float* s2,
+                              int T, int H, int I, int E, int n_shared, int num_groups,
+                              int topk_group, int top_k, int scoring, int renormalize,
+                              float routed_scaling_factor, void* out, void* ws, size_t ws_bytes,
+                              void* stream) {
+  moe_status s = check_forward(x, logits, bias, w13, s13, w2, s2, T, H, I, E, n_shared,
+                               num_groups, topk_group, top_k, scoring, out, ws, ws_bytes);
+  if (s != MOE_OK) return s;
+  if (T == 0) return MOE_OK;
+  return run_forward(x, logits, bias, w13, s13, w2, s2, T, H, I, E, n_shared, num_groups,
+                     topk_group, top_k, scoring, renormalize, routed_scaling_factor, out, ws,
+                     static_cast<cudaStream_t>(stream));
+}
+
 moe_status moe_forward(const void* x, const float* logits, const float* bias, const void* w13,
                        const float* s13, const void* w2, const float* s2, int T, int H, int I,
                        int E, int num_groups, int topk_group, int top_k, int scoring,
                        int renormalize, float routed_scaling_factor, void* out, void* ws,
                        size_t ws_bytes, void* stream) {
-  moe_status s = check_forward(x, logits, bias, w13, s13, w2, s2, T, H, I, E, num_groups,
-                               topk_group, top_k, scoring, out, ws, ws_bytes);
+  return moe_forward_shared(x, logits, bias, w13, s13, w2, s2, T, H, I, E, 0, num_groups,
+                            topk_group, top_k, scoring, renormalize, routed_scaling_factor, out,
+                            ws, ws_bytes, stream);
+}
+
+moe_status moe_forward_shared_host(const void* x_host, const float* logits_host,
+                                   const float* bias, const void* w13, const float* s13,
+                                   const void* w2, const float* s2, int T, int H, int I, int E,
+                                   int n_shared, int num_groups, int topk_group, int top_k,
+                                   int scoring, int renormalize, float routed_scaling_factor,
+                                   void* out_host, void* ws, size_t ws_bytes, void* stream) {
+  if (T > 0 && (x_host == nullptr || logits_host == nullptr || out_host == nullptr))
+    return MOE_ERR_INVALID_ARG;
+  if (ws == nullptr) return MOE_ERR_WORKSPACE;
+  const int S = n_shared < 0 ? 0 : n_shared;
+  const FwdLayout L = fwd_layout(T < 0 ? 0 : T, H < 1 ? 1 : H, I < 1 ? 1 : I,
+                                 (E < 1 ? 1 : E) + S, (top_k < 1 ? 1 : top_k) + S);
+  void* x_d = at<void>(ws, L.x_in);
+  float* l_d = at<float>(ws, L.logits_in);
+  void* o_d = at<void>(ws, L.out);
+  moe_status s = check_forward(x_d, l_d, bias, w13, s13, w2, s2, T, H, I, E, n_shared,
+                               num_groups, topk_group, top_k, scoring, o_d, ws, ws_bytes);
   if (s != MOE_OK) return s;
   if (T == 0) return MOE_OK;
-  return run_forward(x, logits, bias, w13, s13, w2, s2, T, H, I, E, num_groups, topk_group,
-                     top_k, scoring, renormalize, routed_scaling_factor, out, ws,
-                     static_cast<cudaStream_t>(stream));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t xb = (size_t)T * H * 2, lb = (size_t)T * E * 4;
+  if (cudaMemcpyAsync(x_d, x_host, xb, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+      cudaMemcpyAsync(l_d, logits_host, lb, cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  s = run_forward(x_d, l_d, bias, w13, s13, w2, s2, T, H, I, E, n_shared, num_groups,
+                  topk_group, top_k, scoring, renormalize, routed_scaling_factor, o_d, ws, st);
+  if (s != MOE_OK) return s;
+  if (cudaMemcpyAsync(out_host, o_d, xb, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
 }
 
 moe_status moe_forward_host(const void* x_host, const float* logits_host, const float* bias,
@@ -324,29 +373,9 @@ moe_status moe_forward_host(const void* x_host, const float* logits_host, const 
                             int top_k, int scoring, int renormalize,
                             float routed_scaling_factor, void* out_host, void* ws,
                             size_t ws_bytes, void* stream) {
-  if (T > 0 && (x_host == nullptr || logits_host == nullptr || out_host == nullptr))
-    return MOE_ERR_INVALID_ARG;
-  if (ws == nullptr) return MOE_ERR_WORKSPACE;
-  const FwdLayout L = fwd_layout(T < 0 ? 0 : T, H < 1 ? 1 : H, I < 1 ? 1 : I, E < 1 ? 1 : E,
-                                 top_k < 1 ? 1 : top_k);
-  void* x_d = at<void>(ws, L.x_in);
-  float* l_d = at<float>(ws, L.logits_in);
-  void* o_d = at<void>(ws, L.out);
-  moe_status s = check_forward(x_d, l_d, bias, w13, s13, w2, s2, T, H, I, E, num_groups,
-                               topk_group, top_k, scoring, o_d, ws, ws_bytes);
-  if (s != MOE_OK) return s;
-  if (T == 0) return MOE_OK;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const size_t xb = (size_t)T * H * 2, lb = (size_t)T * E * 4;
-  if (cudaMemcpyAsync(x_d, x_host, xb, cudaMemcpyHostToDevice, st) != cudaSuccess ||
-      cudaMemcpyAsync(l_d, logits_host, lb, cudaMemcpyHostToDevice, st) != cudaSuccess)
-    return MOE_ERR_CUDA;
-  s = run_forward(x_d, l_d, bias, w13, s13, w2, s2, T, H, I, E, num_groups, topk_group, top_k,
-                  scoring, renormalize, routed_scaling_factor, o_d, ws, st);
-  if (s != MOE_OK) return s;
-  if (cudaMemcpyAsync(out_host, o_d, xb, cudaMemcpyDeviceToHost, st) != cudaSuccess)
-    return MOE_ERR_CUDA;
-  return MOE_OK;
+  return moe_forward_shared_host(x_host, logits_host, bias, w13, s13, w2, s2, T, H, I, E, 0,
+                                 num_groups, topk_group, top_k, scoring, renormalize,
+                                 routed_scaling_factor, out_host, ws, ws_bytes, stream);
 }
 
 moe_status moe_device_status(int* code) {

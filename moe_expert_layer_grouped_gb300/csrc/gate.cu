@@ -101,7 +101,7 @@ template <int EPL>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     gate_kernel(const float* __restrict__ logits, const float* __restrict__ bias, int T, int E,
                 int G, int TG, int K, int scoring, int renorm, float rsf,
-                int32_t* __restrict__ ids_out, float* __restrict__ w_out) {
+                int32_t* __restrict__ ids_out, float* __restrict__ w_out, int n_shared) {
   extern __shared__ float keys_smem[];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -269,20 +269,26 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     if (lane < K) lk = __ldg(l + my_id);
     wk = __fmul_rn(__fdiv_rn(exp32(__fsub_rn(lk, mx)), Z), rsf);
   }
+  // rows of K + n_shared slots: the routed picks, then the shared experts
+  // (ids E .. E+n_shared-1, weight 1)
+  const int64_t row = (int64_t)t * (K + n_shared);
   if (lane < K) {
-    ids_out[(int64_t)t * K + lane] = my_id;
-    w_out[(int64_t)t * K + lane] = wk;
+    ids_out[row + lane] = my_id;
+    w_out[row + lane] = wk;
+  } else if (lane < K + n_shared) {
+    ids_out[row + lane] = E + (lane - K);
+    w_out[row + lane] = 1.0f;
   }
 }
 
 template <int EPL>
 cudaError_t launch_epl(const float* logits, const float* bias, int T, int E, int G, int TG,
                        int K, int scoring, int renorm, float rsf, int32_t* ids, float* w,
-                       cudaStream_t st) {
+                       int S, cudaStream_t st) {
   const int blocks = (T + kWarpsPerBlock - 1) / kWarpsPerBlock;
   const size_t smem = (TG < G) ? sizeof(float) * kWarpsPerBlock * (E + (E >> 5) + 1) : 0;
   gate_kernel<EPL><<<blocks, kWarpsPerBlock * 32, smem, st>>>(logits, bias, T, E, G, TG, K,
-                                                              scoring, renorm, rsf, ids, w);
+                                                              scoring, renorm, rsf, ids, w, S);
   return cudaGetLastError();
 }
 
@@ -290,15 +296,16 @@ cudaError_t launch_epl(const float* logits, const float* bias, int T, int E, int
 
 cudaError_t launch_gate(const float* logits, const float* bias, int T, int E, int G, int TG,
                         int K, int scoring, int renorm, float rsf, int32_t* ids, float* w,
-                        cudaStream_t st) {
+                        int n_shared, cudaStream_t st) {
   if (T == 0) return cudaSuccess;
+  const int S = n_shared;
   const int per_lane = (E + 31) / 32;
-  if (per_lane <= 1) return launch_epl<1>(logits, bias, T, E, G, TG, K, scoring, renorm, rsf, ids, w, st);
-  if (per_lane <= 2) return launch_epl<2>(logits, bias, T, E, G, TG, K, scoring, renorm, rsf, ids, w, st);
-  if (per_lane <= 4) return launch_epl<4>(logits, bias, T, E, G, TG, K, scoring, renorm, rsf, ids, w, st);
-  if (per_lane <= 8) return launch_epl<8>(logits, bias, T, E, G, TG, K, scoring, renorm, rsf, ids, w, st);
-  if (per_lane <= 16) return launch_epl<16>(logits, bias, T, E, G, TG, K, scoring, renorm, rsf, ids, w, st);
-  return launch_epl<32>(logits, bias, T, E, G, TG, K, scoring, renorm, rsf, ids, w, st);
+  if (per_lane <= 1) return launch_epl<1>(logits, bias, T, E, G, TG, K, scoring, renorm, rsf, ids, w, S, st);
+  if (per_lane <= 2) return launch_epl<2>(logits, bias, T, E, G, TG, K, scoring, renorm, rsf, ids, w, S, st);
+  if (per_lane <= 4) return launch_epl<4>(logits, bias, T, E, G, TG, K, scoring, renorm, rsf, ids, w, S, st);
+  if (per_lane <= 8) return launch_epl<8>(logits, bias, T, E, G, TG, K, scoring, renorm, rsf, ids, w, S, st);
+  if (per_lane <= 16) return launch_epl<16>(logits, bias, T, E, G, TG, K, scoring, renorm, rsf, ids, w, S, st);
+  return launch_epl<32>(logits, bias, T, E, G, TG, K, scoring, renorm, rsf, ids, w, S, st);
 }
 
 }  // namespace moe

@@ -15,10 +15,11 @@ int sm_count();
 constexpr size_t kAlign = 256;
 inline size_t align_up(size_t v, size_t a = kAlign) { return (v + a - 1) / a * a; }
 
-// gate.cu
+// gate.cu: ids/w rows hold K + n_shared slots, the last n_shared being the
+// shared experts E .. E+n_shared-1 with weight 1 (K + n_shared <= 32).
 cudaError_t launch_gate(const float* logits, const float* bias, int T, int E, int G, int TG,
                         int K, int scoring, int renorm, float rsf, int32_t* ids, float* w,
-                        cudaStream_t st);
+                        int n_shared, cudaStream_t st);
 
 // permute.cu
 size_t permute_ws_bytes(int T, int E);

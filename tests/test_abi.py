@@ -34,7 +34,7 @@ def test_header_declares_the_entry_points():
     for want in ["moe_gate", "moe_permute_quant", "moe_grouped_gemm", "moe_act_quant",
                  "moe_unpermute_sum", "moe_forward", "moe_forward_host", "moe_workspace_size",
                  "moe_permute_workspace_size", "moe_device_status", "moe_status_string",
-                 "moe_abi_version"]:
+                 "moe_abi_version", "moe_forward_shared", "moe_forward_shared_host"]:
         assert want in names
 
 
@@ -128,6 +128,27 @@ def test_forward_validation_and_workspace(lib):
     # T == 0 is a valid no-op
     assert f(None, None, None, GOOD, GOOD, GOOD, GOOD, 0, H, I, E, 1, 1, K, 1, 1, 1.0, None,
              P(0x100000), lib.moe_workspace_size(0, H, I, E, K), None) == OK
+
+
+def test_forward_shared_validation(lib):
+    """Shared experts: the workspace must cover E + n_shared experts and
+    top_k + n_shared slots; n_shared < 0 and top_k + n_shared > 32 are refused
+    before any device work."""
+    f, fh = lib.moe_forward_shared, lib.moe_forward_shared_host
+    T, H, I, E, K = 16, 128, 64, 8, 2
+    need = lib.moe_workspace_size(T, H, I, E + 1, K + 1)
+    assert need > lib.moe_workspace_size(T, H, I, E, K)
+
+    def base(S):
+        return [GOOD, GOOD, None, GOOD, GOOD, GOOD, GOOD, T, H, I, E, S, 1, 1, K, 1, 1, 1.0,
+                GOOD]
+    ws = P(0x100000)
+    assert f(*base(1), ws, lib.moe_workspace_size(T, H, I, E, K), None) == WORKSPACE
+    assert f(*base(1), ws, need - 1, None) == WORKSPACE
+    assert f(*base(-1), ws, need, None) == INVALID
+    assert f(*base(31), ws, 1 << 40, None) == UNSUPPORTED      # top_k + n_shared > 32
+    assert fh(*base(1), None, need, None) == WORKSPACE
+    assert fh(*base(-1), ws, need, None) == INVALID
 
 
 def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):

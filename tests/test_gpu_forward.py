@@ -3,7 +3,8 @@ oracle on the five workloads: every token on the small ones, a fixed sample of
 tokens on the large ones (a token's output depends on that token alone), run
 through the same MoELayer call the benchmark times. Plus edge cases: the
 per-row scale regression, guard bands around every output, empty and one-token
-batches, the host-buffer entry point."""
+batches, the host-buffer entry point. Shared experts (moe_forward_shared)
+are checked the same way on layers that add one or two of them."""
 import numpy as np
 import pytest
 import torch
@@ -28,14 +29,15 @@ def built():
 
 def _layer(wl, d):
     return moe.MoELayer(d["w13"], d["s13"], d["w2"], d["s2"], d["bias"], wl.num_groups,
-                        wl.topk_group, wl.top_k, wl.scoring, wl.renormalize, wl.rsf, wl.T)
+                        wl.topk_group, wl.top_k, wl.scoring, wl.renormalize, wl.rsf, wl.T,
+                        n_shared=wl.n_shared)
 
 
 def _oracle_tokens(wl, d, tokens):
     n = {k: (None if v is None else v) for k, v in synth.to_numpy_inputs(d).items()}
     return oracle.forward_tokens(n["x"], n["logits"], n["bias"], n["w13"], n["s13"], n["w2"],
                                  n["s2"], wl.num_groups, wl.topk_group, wl.top_k, wl.scoring,
-                                 wl.renormalize, wl.rsf, tokens=tokens)
+                                 wl.renormalize, wl.rsf, tokens=tokens, n_shared=wl.n_shared)
 
 
 def _check_workload(wl, seed, device_gen, n_sample=None):
@@ -87,6 +89,43 @@ def test_forward_shapes(T, H, I, E, G, TG, K, scoring, rsf):
     bias = "none" if scoring == synth.SOFTMAX else "normal"
     wl = synth.Workload("shape", T, H, I, E, G, TG, K, scoring, True, rsf, bias)
     _check_workload(wl, 3, device_gen=False)
+
+
+@pytest.mark.parametrize("name,seed,n_sample", [
+    ("tiny_shared", 0, None), ("tiny_shared", 1, None), ("tiny_shared", 2, None),
+    ("dsv3_decode_t128_shared", 0, None), ("dsv3_prefill_t8192_shared", 0, 40),
+])
+def test_forward_shared_expert(name, seed, n_sample):
+    wl = synth.WORKLOADS[name]
+    _check_workload(wl, seed, device_gen=wl.T > 8, n_sample=n_sample)
+
+
+def test_forward_two_shared_experts_ragged():
+    wl = synth.Workload("two_shared", 100, 256, 128, 16, 4, 2, 4, synth.SIGMOID, True, 2.5,
+                        "normal", n_shared=2)
+    _check_workload(wl, 7, device_gen=False)
+
+
+def test_forward_shared_zero_and_host_buffers():
+    """n_shared = 0 is moe_forward bit for bit; the host-buffer entry point
+    gives the device one's output bit for bit."""
+    wl = synth.WORKLOADS["tiny_shared"].with_tokens(40)
+    d = {k: (None if v is None else v.to(DEV)) for k, v in synth.make_inputs(wl, 9).items()}
+    E = wl.E
+    cfg = (wl.num_groups, wl.topk_group, wl.top_k, wl.scoring, wl.renormalize, wl.rsf)
+    routed = (d["w13"][:E], d["s13"][:E], d["w2"][:E], d["s2"][:E])
+    a = moe.moe_forward(d["x"], d["logits"], d["bias"], *routed, *cfg)
+    b = moe.moe_forward_shared(d["x"], d["logits"], d["bias"], *routed, 0, *cfg)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    layer = _layer(wl, d)
+    dev_out = layer(d["x"], d["logits"])
+    xh, lh = d["x"].cpu().pin_memory(), d["logits"].cpu().pin_memory()
+    oh = torch.empty_like(xh).pin_memory()
+    layer.forward_host(xh, lh, oh)
+    torch.cuda.synchronize()
+    assert torch.equal(oh.view(torch.int16), dev_out.cpu().view(torch.int16))
+    # the shared expert contributes: the layer differs from the routed-only one
+    assert not torch.equal(dev_out, a)
 
 
 def test_forward_rsf_linear_and_empty_batch():
