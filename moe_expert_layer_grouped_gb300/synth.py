@@ -23,6 +23,10 @@ DeepSeek-V3-style and a Mixtral-style MoE layer):
                      has one, of the routed experts' size), stored after the
                      routed experts in w13/w2 and drawn after them from the
                      same streams, so the routed weights are unchanged
+  *_block            the same layers with block-quantised FP8 weights
+                     (DeepSeek-V3's checkpoint format: one scale per 128 x 128
+                     block, s13 [E, 2I/128, H/128], s2 [E, H/128, I/128]) drawn
+                     from the same fp32 values; tiny_block has I = 128
 Hidden states and router logits ~N(0, 1); weights ~N(0, 0.02).
 """
 from dataclasses import dataclass, replace
@@ -49,6 +53,7 @@ class Workload:
     rsf: float
     bias: str  # "none" | "normal" | "zero" | "skewed"
     n_shared: int = 0  # shared experts, stored as experts E .. E+n_shared-1
+    quant: str = "token"  # "token": per-channel weight scales; "block": 128 x 128 blocks
 
     @property
     def M(self):
@@ -78,6 +83,10 @@ WORKLOADS = {
 for _name, _S in [("tiny", 1), ("dsv3_decode_t128", 1), ("dsv3_prefill_t8192", 1)]:
     WORKLOADS[f"{_name}_shared"] = replace(WORKLOADS[_name], name=f"{_name}_shared",
                                            n_shared=_S)
+WORKLOADS["tiny_block"] = replace(WORKLOADS["tiny"], name="tiny_block", I=128, quant="block")
+for _name in ["dsv3_decode_t128", "dsv3_prefill_t8192", "mixtral_t4096"]:
+    WORKLOADS[f"{_name}_block"] = replace(WORKLOADS[_name], name=f"{_name}_block",
+                                          quant="block")
 
 # tensor ids: each tensor draws from its own generator stream
 _TID = {"x": 0, "logits": 1, "bias": 2, "w13": 3, "w2": 4}
@@ -102,14 +111,29 @@ def quantize_weight_rows(w: torch.Tensor):
     return q.view(torch.uint8), scale.to(torch.float32)
 
 
-def expert_weights(E, rows, cols, seed, tensor, device="cpu", std=0.02):
-    """[E, rows, cols] FP8 codes + [E, rows] scales, drawn expert by expert."""
+def quantize_weight_blocks(w: torch.Tensor, blk: int = 128):
+    """fp32 weights [..., rows, cols] -> (e4m3 codes as uint8, fp32 scale per
+    blk x blk block [..., rows/blk, cols/blk])."""
+    *lead, R, C = w.shape
+    wb = w.reshape(*lead, R // blk, blk, C // blk, blk)
+    amax = wb.abs().amax(dim=(-3, -1))
+    scale = torch.clamp(amax, min=1e-12) / 448.0
+    q = (wb / scale[..., :, None, :, None]).clamp_(-448.0, 448.0).to(torch.float8_e4m3fn)
+    return q.reshape(*lead, R, C).view(torch.uint8), scale.to(torch.float32)
+
+
+def expert_weights(E, rows, cols, seed, tensor, device="cpu", std=0.02, quant="token"):
+    """[E, rows, cols] FP8 codes + scales ([E, rows] per channel, or
+    [E, rows/128, cols/128] per block), drawn expert by expert."""
     q = torch.empty((E, rows, cols), dtype=torch.uint8, device=device)
-    s = torch.empty((E, rows), dtype=torch.float32, device=device)
+    if quant == "block":
+        s = torch.empty((E, rows // 128, cols // 128), dtype=torch.float32, device=device)
+    else:
+        s = torch.empty((E, rows), dtype=torch.float32, device=device)
     g = _gen(seed, tensor, device)
     for e in range(E):
         w = torch.randn((rows, cols), generator=g, device=device, dtype=torch.float32).mul_(std)
-        q[e], s[e] = quantize_weight_rows(w)
+        q[e], s[e] = quantize_weight_blocks(w) if quant == "block" else quantize_weight_rows(w)
     return q, s
 
 
@@ -132,7 +156,8 @@ def make_inputs(wl: Workload, seed=0, device="cpu", weights=True):
     x: bf16 [T,H]; logits: f32 [T,E]; bias: f32 [E] or None;
     w13: u8 [E,2I,H] (rows 0..I-1 gate, I..2I-1 up) with s13 f32 [E,2I];
     w2: u8 [E,H,I] with s2 f32 [E,H]; with n_shared shared experts the
-    leading dimension is E + n_shared.
+    leading dimension is E + n_shared. Block workloads: s13 [E, 2I/128, H/128],
+    s2 [E, H/128, I/128].
     """
     d = dict(
         x=normal((wl.T, wl.H), 1.0, seed, "x", device, torch.bfloat16),
@@ -141,8 +166,9 @@ def make_inputs(wl: Workload, seed=0, device="cpu", weights=True):
     )
     if weights:
         n = wl.E + wl.n_shared
-        d["w13"], d["s13"] = expert_weights(n, 2 * wl.I, wl.H, seed, "w13", device)
-        d["w2"], d["s2"] = expert_weights(n, wl.H, wl.I, seed, "w2", device)
+        d["w13"], d["s13"] = expert_weights(n, 2 * wl.I, wl.H, seed, "w13", device,
+                                            quant=wl.quant)
+        d["w2"], d["s2"] = expert_weights(n, wl.H, wl.I, seed, "w2", device, quant=wl.quant)
     return d
 
 

@@ -50,6 +50,12 @@ def lib():
             "oracle_forward_tokens_shared": (i32, [P, P, P, P, P, P, P, i32, i32, i32, i32,
                                                    i32, i32, i32, i32, i32, i32, f32, P, i32,
                                                    P, P, P]),
+            "oracle_block_quant": (None, [P, i64, i32, P, P]),
+            "oracle_permute_quant_block": (None, [P, P, i32, i32, i32, i32, P, P, P, P]),
+            "oracle_grouped_gemm_block": (None, [P, P, P, P, P, i32, i32, i32, i32, P]),
+            "oracle_forward_tokens_block": (i32, [P, P, P, P, P, P, P, i32, i32, i32, i32,
+                                                  i32, i32, i32, i32, i32, i32, f32, P, i32,
+                                                  P, P, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -260,6 +266,107 @@ def forward_steps(x_bits, logits, bias, w13, s13, w2, s2, num_groups, topk_group
     h_bits = bf16_round(h)
     q2, sa2 = act_quant(h_bits)
     down = grouped_gemm(q2, sa2, w2, s2, offsets)
+    out = unpermute_sum(down, src2dst, w)
+    return dict(ids=ids, w=w, a_q=a_q, scale_a=sa, src2dst=src2dst, offsets=offsets,
+                c13=C13, h=h, h_bits=h_bits, q2=q2, scale_a2=sa2, down=down, out=out)
+
+
+# ---------------------------------------------------------------------------
+# block-quantised FP8: 128-channel activation blocks, 128 x 128 weight blocks
+# ---------------------------------------------------------------------------
+QB = 128
+
+
+def block_quant(x_bits):
+    """bf16 [R,C] (bit patterns) -> (e4m3 codes [R,C], scales [R, C/128])."""
+    x = _c(x_bits, np.uint16)
+    R, C = x.shape
+    assert C % QB == 0
+    q = np.empty((R, C), np.uint8)
+    s = np.empty((R, C // QB), np.float32)
+    lib().oracle_block_quant(_p(x), R, C, _p(q), _p(s))
+    return q, s
+
+
+def permute_quant_block(x_bits, topk_ids, E):
+    x = _c(x_bits, np.uint16)
+    ids = _c(topk_ids, np.int32)
+    T, H = x.shape
+    K = ids.shape[1]
+    M = T * K
+    a_q = np.empty((M, H), np.uint8)
+    sa = np.empty((M, H // QB), np.float32)
+    src2dst = np.empty(M, np.int32)
+    offsets = np.empty(E + 1, np.int32)
+    lib().oracle_permute_quant_block(_p(x), _p(ids), T, H, E, K, _p(a_q), _p(sa), _p(src2dst),
+                                     _p(offsets))
+    return a_q, sa, src2dst, offsets
+
+
+def grouped_gemm_block(A, scale_a, B, scale_b, offsets):
+    """scale_a [M, Kd/128]; scale_b [E, N/128, Kd/128]; fp64 result [M, N]."""
+    A = _c(A, np.uint8)
+    B = _c(B, np.uint8)
+    sa = _c(scale_a, np.float32)
+    sb = _c(scale_b, np.float32)
+    off = _c(offsets, np.int32)
+    M, Kd = A.shape
+    E, N, Kd2 = B.shape
+    assert Kd == Kd2 and off.size == E + 1 and Kd % QB == 0 and N % QB == 0
+    assert sa.shape == (M, Kd // QB) and sb.shape == (E, N // QB, Kd // QB)
+    C = np.empty((M, N), np.float64)
+    lib().oracle_grouped_gemm_block(_p(A), _p(sa), _p(B), _p(sb), _p(off), M, N, Kd, E, _p(C))
+    return C
+
+
+def forward_tokens_block(x_bits, logits, bias, w13, s13, w2, s2, num_groups, topk_group, top_k,
+                         scoring, renormalize, routed_scaling_factor, tokens=None, n_shared=0):
+    """Whole layer in block FP8 for the listed tokens: s13 [E+S, 2I/128, H/128],
+    s2 [E+S, H/128, I/128]. Returns (out [n,H] fp64, ids [n,K], w [n,K])."""
+    x = _c(x_bits, np.uint16)
+    logits = _c(logits, np.float32)
+    T, H = x.shape
+    E = logits.shape[1]
+    I = w2.shape[2]
+    n = E + n_shared
+    assert w13.shape == (n, 2 * I, H) and w2.shape == (n, H, I)
+    assert s13.shape == (n, 2 * I // QB, H // QB) and s2.shape == (n, H // QB, I // QB)
+    b = None if bias is None else _c(bias, np.float32)
+    tok = np.arange(T, dtype=np.int64) if tokens is None else _c(tokens, np.int64)
+    nt = tok.size
+    out = np.empty((nt, H), np.float64)
+    ids = np.empty((nt, top_k), np.int32)
+    w = np.empty((nt, top_k), np.float32)
+    w13, w2 = _c(w13, np.uint8), _c(w2, np.uint8)
+    s13, s2 = _c(s13, np.float32), _c(s2, np.float32)
+    rc = lib().oracle_forward_tokens_block(_p(x), _p(logits), _p(b), _p(w13), _p(s13), _p(w2),
+                                           _p(s2), T, H, I, E, int(n_shared), num_groups,
+                                           topk_group, top_k, scoring, int(bool(renormalize)),
+                                           float(routed_scaling_factor), _p(tok), nt, _p(out),
+                                           _p(ids), _p(w))
+    if rc != 0:
+        raise ValueError(f"oracle_forward_tokens_block: status {rc}")
+    return out, ids, w
+
+
+def forward_steps_block(x_bits, logits, bias, w13, s13, w2, s2, num_groups, topk_group, top_k,
+                        scoring, renormalize, routed_scaling_factor, n_shared=0):
+    """The block-FP8 layer step by step over all tokens (small configurations)."""
+    E = logits.shape[1]
+    ids, w = gate(logits, bias, num_groups, topk_group, top_k, scoring, renormalize,
+                  routed_scaling_factor)
+    if n_shared:
+        T = ids.shape[0]
+        ids = np.concatenate([ids, np.broadcast_to(
+            np.arange(E, E + n_shared, dtype=np.int32), (T, n_shared))], axis=1)
+        w = np.concatenate([w, np.ones((T, n_shared), np.float32)], axis=1)
+        E += n_shared
+    a_q, sa, src2dst, offsets = permute_quant_block(x_bits, ids, E)
+    C13 = grouped_gemm_block(a_q, sa, w13, s13, offsets)
+    h = silu_mul(C13)
+    h_bits = bf16_round(h)
+    q2, sa2 = block_quant(h_bits)
+    down = grouped_gemm_block(q2, sa2, w2, s2, offsets)
     out = unpermute_sum(down, src2dst, w)
     return dict(ids=ids, w=w, a_q=a_q, scale_a=sa, src2dst=src2dst, offsets=offsets,
                 c13=C13, h=h, h_bits=h_bits, q2=q2, scale_a2=sa2, down=down, out=out)

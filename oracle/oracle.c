@@ -604,3 +604,211 @@ int oracle_forward_tokens_shared(const uint16_t* x, const float* logits,
   }
   return status;
 }
+
+/* ------------------------------------------------------------------------
+ * Block-quantised FP8 (DeepSeek-V3's checkpoint format; the group_k/group_n
+ * path that "Fix one bug in the grouped-gemm triton kernel", sglang #6772,
+ * Highlights, contrasts with the per-token path). Activations carry one fp32
+ * scale per token per 128 consecutive channels, weights one per 128 x 128
+ * block (output-channel block x input-channel block). Each 128-channel
+ * partial sum is dequantised by its own pair of scales:
+ *   C[r,n] = sum_kb ( sum_{k in kb} q[r,k] W[n,k] ) * sa[r,kb] * sb[n/128,kb]
+ * Block quantisation uses the per-token rule on each 128-block:
+ *   s = max(amax_block, 1e-10) / 448, q = e4m3(x / s).
+ * ---------------------------------------------------------------------- */
+#define QB 128
+
+void oracle_block_quant(const uint16_t* x, int64_t R, int C, uint8_t* q, float* scale) {
+  const int nb = C / QB;
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < R; ++r) {
+    for (int b = 0; b < nb; ++b) {
+      const uint16_t* blk = x + r * C + (int64_t)b * QB;
+      float amax = 0.0f;
+      for (int c = 0; c < QB; ++c) {
+        float v = fabsf(bf16_to_f32(blk[c]));
+        if (v > amax) amax = v;
+      }
+      float sc = fmaxf(amax, 1e-10f) / 448.0f;
+      scale[r * nb + b] = sc;
+      for (int c = 0; c < QB; ++c)
+        q[r * C + (int64_t)b * QB + c] = oracle_e4m3_encode(bf16_to_f32(blk[c]) / sc);
+    }
+  }
+}
+
+void oracle_permute_quant_block(const uint16_t* x, const int32_t* topk_ids, int T, int H,
+                                int E, int K, uint8_t* a_q, float* scale_a, int32_t* src2dst,
+                                int32_t* offsets) {
+  const int nb = H / QB;
+  oracle_route(topk_ids, T, E, K, offsets, src2dst);
+  uint8_t* q = (uint8_t*)malloc((size_t)T * H + 1);
+  float* sc = (float*)malloc(sizeof(float) * ((size_t)T * nb + 1));
+  oracle_block_quant(x, T, H, q, sc);
+  for (int t = 0; t < T; ++t) {
+    for (int k = 0; k < K; ++k) {
+      int64_t d = src2dst[(int64_t)t * K + k];
+      memcpy(a_q + d * H, q + (int64_t)t * H, (size_t)H);
+      memcpy(scale_a + d * nb, sc + (int64_t)t * nb, sizeof(float) * (size_t)nb);
+    }
+  }
+  free(q);
+  free(sc);
+}
+
+void oracle_grouped_gemm_block(const uint8_t* A, const float* scale_a, const uint8_t* B,
+                               const float* scale_b, const int32_t* offsets, int M, int N,
+                               int Kd, int E, double* C) {
+  init_lut();
+  const int KB = Kd / QB, NBk = N / QB;
+  int32_t* row_e = (int32_t*)malloc(sizeof(int32_t) * (size_t)(M > 0 ? M : 1));
+  for (int r = 0; r < M; ++r) row_e[r] = -1;
+  for (int e = 0; e < E; ++e)
+    for (int r = offsets[e]; r < offsets[e + 1] && r < M; ++r) row_e[r] = e;
+#pragma omp parallel
+  {
+    double* a = (double*)malloc(sizeof(double) * (size_t)Kd);
+#pragma omp for schedule(dynamic, 1)
+    for (int r = 0; r < M; ++r) {
+      int e = row_e[r];
+      double* c = C + (int64_t)r * N;
+      if (e < 0) {
+        for (int n = 0; n < N; ++n) c[n] = 0.0;
+        continue;
+      }
+      for (int k = 0; k < Kd; ++k) a[k] = g_e4m3_lut[A[(int64_t)r * Kd + k]];
+      const uint8_t* Be = B + (int64_t)e * N * Kd;
+      const float* sbe = scale_b + (int64_t)e * NBk * KB;
+      for (int n = 0; n < N; ++n) {
+        const uint8_t* b = Be + (int64_t)n * Kd;
+        double acc = 0.0;
+        for (int kb = 0; kb < KB; ++kb) {
+          double part = 0.0;
+          for (int k = kb * QB; k < (kb + 1) * QB; ++k) part += a[k] * g_e4m3_lut[b[k]];
+          acc += part * (double)scale_a[(int64_t)r * KB + kb] *
+                 (double)sbe[(int64_t)(n / QB) * KB + kb];
+        }
+        c[n] = acc;
+      }
+    }
+    free(a);
+  }
+  free(row_e);
+}
+
+/* Whole layer with block-quantised FP8 for the listed tokens, with n_shared
+ * shared experts as in oracle_forward_tokens_shared. s13 [E+S, 2I/128, H/128],
+ * s2 [E+S, H/128, I/128]. */
+int oracle_forward_tokens_block(const uint16_t* x, const float* logits, const float* bias,
+                                const uint8_t* w13, const float* s13, const uint8_t* w2,
+                                const float* s2, int T, int H, int I, int E, int n_shared,
+                                int num_groups, int topk_group, int top_k, int scoring,
+                                int renormalize, float routed_scaling_factor,
+                                const int64_t* tokens, int n_tok, double* out,
+                                int32_t* ids_out, float* w_out) {
+  int rc = gate_check(T, E, num_groups, topk_group, top_k, scoring, bias);
+  if (rc) return rc;
+  if (n_shared < 0 || H % QB != 0 || I % QB != 0) return -1;
+  for (int i = 0; i < n_tok; ++i)
+    if (tokens[i] < 0 || tokens[i] >= T) return -1;
+  init_lut();
+  const int K = top_k;
+  const int N13 = 2 * I;
+  const int KBH = H / QB, KBI = I / QB;
+  int status = 0;
+#pragma omp parallel
+  {
+    kv_t* kv = (kv_t*)malloc(sizeof(kv_t) * (size_t)E);
+    kv_t* gkv = (kv_t*)malloc(sizeof(kv_t) * (size_t)(E + num_groups));
+    float* s = (float*)malloc(sizeof(float) * (size_t)E);
+    double* a = (double*)malloc(sizeof(double) * (size_t)H);
+    float* sa = (float*)malloc(sizeof(float) * (size_t)KBH);
+    double* c = (double*)malloc(sizeof(double) * (size_t)N13);
+    uint16_t* hb = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)I);
+    double* h2 = (double*)malloc(sizeof(double) * (size_t)I);
+    float* sa2 = (float*)malloc(sizeof(float) * (size_t)KBI);
+    int32_t ids[64];
+    float w[64];
+#pragma omp for schedule(dynamic, 1)
+    for (int i = 0; i < n_tok; ++i) {
+      int64_t t = tokens[i];
+      double* o = out + (int64_t)i * H;
+      if (K > 64) {
+        status = -2;
+        continue;
+      }
+      gate_token(logits + t * E, bias, E, num_groups, topk_group, K, scoring, renormalize,
+                 routed_scaling_factor, ids, w, kv, gkv, s);
+      if (ids_out)
+        for (int k = 0; k < K; ++k) ids_out[(int64_t)i * K + k] = ids[k];
+      if (w_out)
+        for (int k = 0; k < K; ++k) w_out[(int64_t)i * K + k] = w[k];
+      /* block quantisation of the hidden state: one scale per 128 channels */
+      const uint16_t* xr = x + t * H;
+      for (int b = 0; b < KBH; ++b) {
+        float amax = 0.0f;
+        for (int hh = b * QB; hh < (b + 1) * QB; ++hh) {
+          float v = fabsf(bf16_to_f32(xr[hh]));
+          if (v > amax) amax = v;
+        }
+        sa[b] = fmaxf(amax, 1e-10f) / 448.0f;
+        for (int hh = b * QB; hh < (b + 1) * QB; ++hh)
+          a[hh] = g_e4m3_lut[oracle_e4m3_encode(bf16_to_f32(xr[hh]) / sa[b])];
+      }
+      for (int cc = 0; cc < H; ++cc) o[cc] = 0.0;
+      for (int k = 0; k < K + n_shared; ++k) {
+        const int e = k < K ? ids[k] : E + (k - K);
+        const uint8_t* We = w13 + (int64_t)e * N13 * H;
+        const float* sbe = s13 + (int64_t)e * (N13 / QB) * KBH;
+        for (int n = 0; n < N13; ++n) {
+          const uint8_t* b = We + (int64_t)n * H;
+          double acc = 0.0;
+          for (int kb = 0; kb < KBH; ++kb) {
+            double part = 0.0;
+            for (int hh = kb * QB; hh < (kb + 1) * QB; ++hh) part += a[hh] * g_e4m3_lut[b[hh]];
+            acc += part * (double)sa[kb] * (double)sbe[(int64_t)(n / QB) * KBH + kb];
+          }
+          c[n] = acc;
+        }
+        for (int j = 0; j < I; ++j) {
+          double g = c[j], u = c[I + j];
+          hb[j] = oracle_bf16_round(g / (1.0 + exp(-g)) * u);
+        }
+        /* block requantisation of h */
+        for (int b = 0; b < KBI; ++b) {
+          float amax2 = 0.0f;
+          for (int j = b * QB; j < (b + 1) * QB; ++j) {
+            float v = fabsf(bf16_to_f32(hb[j]));
+            if (v > amax2) amax2 = v;
+          }
+          sa2[b] = fmaxf(amax2, 1e-10f) / 448.0f;
+          for (int j = b * QB; j < (b + 1) * QB; ++j)
+            h2[j] = g_e4m3_lut[oracle_e4m3_encode(bf16_to_f32(hb[j]) / sa2[b])];
+        }
+        const uint8_t* W2e = w2 + (int64_t)e * H * I;
+        const float* sb2 = s2 + (int64_t)e * (H / QB) * KBI;
+        double wk = k < K ? (double)w[k] : 1.0;
+        for (int cc = 0; cc < H; ++cc) {
+          const uint8_t* b = W2e + (int64_t)cc * I;
+          double acc = 0.0;
+          for (int kb = 0; kb < KBI; ++kb) {
+            double part = 0.0;
+            for (int j = kb * QB; j < (kb + 1) * QB; ++j) part += h2[j] * g_e4m3_lut[b[j]];
+            acc += part * (double)sa2[kb] * (double)sb2[(int64_t)(cc / QB) * KBI + kb];
+          }
+          o[cc] += wk * acc;
+        }
+      }
+    }
+    free(kv);
+    free(gkv);
+    free(s);
+    free(a);
+    free(sa);
+    free(c);
+    free(hb);
+    free(h2);
+    free(sa2);
+  }
+  return status;
+}

@@ -122,6 +122,34 @@ int oracle_forward_tokens_shared(const uint16_t* x, const float* logits,
                                  const int64_t* tokens, int n_tok, double* out,
                                  int32_t* ids_out, float* w_out);
 
+/* ---- block-quantised FP8 (128-channel activation blocks, 128 x 128 weight
+ * blocks; every dimension that is blocked must be a multiple of 128) ---- */
+
+/* x bf16 [R,C] -> q e4m3 [R,C], scale f32 [R, C/128]: per 128-block of a row,
+ * scale = max(amax, 1e-10)/448, q = e4m3(x / scale). */
+void oracle_block_quant(const uint16_t* x, int64_t R, int C, uint8_t* q, float* scale);
+
+/* oracle_permute_quant with block scales: scale_a [T*K, H/128]. */
+void oracle_permute_quant_block(const uint16_t* x, const int32_t* topk_ids, int T, int H,
+                                int E, int K, uint8_t* a_q, float* scale_a, int32_t* src2dst,
+                                int32_t* offsets);
+
+/* C[r,n] = sum_kb (sum_{k in kb} A[r,k] B[e,n,k]) * scale_a[r,kb] *
+ * scale_b[e, n/128, kb] in fp64. scale_a [M, Kd/128]; scale_b [E, N/128, Kd/128]. */
+void oracle_grouped_gemm_block(const uint8_t* A, const float* scale_a, const uint8_t* B,
+                               const float* scale_b, const int32_t* offsets, int M, int N,
+                               int Kd, int E, double* C);
+
+/* The whole layer in block FP8 (with n_shared shared experts as in
+ * oracle_forward_tokens_shared). s13 [E+S, 2I/128, H/128]; s2 [E+S, H/128, I/128]. */
+int oracle_forward_tokens_block(const uint16_t* x, const float* logits, const float* bias,
+                                const uint8_t* w13, const float* s13, const uint8_t* w2,
+                                const float* s2, int T, int H, int I, int E, int n_shared,
+                                int num_groups, int topk_group, int top_k, int scoring,
+                                int renormalize, float routed_scaling_factor,
+                                const int64_t* tokens, int n_tok, double* out,
+                                int32_t* ids_out, float* w_out);
+
 #ifdef __cplusplus
 }
 #endif

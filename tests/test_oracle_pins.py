@@ -489,3 +489,130 @@ def test_layer_token_path_equals_step_path_and_is_linear_in_rsf():
     outs, _, _ = oracle.forward_tokens(x, logits, bias, w13, s13, w2, s2, 4, 2, 3,
                                        oracle.SIGMOID, True, 2.5, tokens=sub)
     assert np.array_equal(outs, out[sub])
+
+
+# ---------------------------------------------------------------------------
+# Block-quantised FP8 (128-channel activation blocks, 128 x 128 weight blocks)
+# ---------------------------------------------------------------------------
+def test_block_quant_is_row_quant_per_block():
+    """Each 128-block of a row is quantised exactly as a row of its own by
+    the (exhaustively pinned) per-token rule; a block's scale depends only on
+    that block (scaling one block by 4 scales only its scale)."""
+    rng = np.random.default_rng(50)
+    R, nb = 9, 5
+    x = rng.standard_normal((R, nb * 128)) * (10.0 ** rng.uniform(-3, 3, (R, nb)))[:, :, None].repeat(128, 2).reshape(R, -1)
+    xb = _bf16_bits(x)
+    q, s = oracle.block_quant(xb)
+    q1, s1 = oracle.row_quant(xb.reshape(R * nb, 128))
+    assert np.array_equal(q.reshape(R * nb, 128), q1)
+    assert np.array_equal(s.reshape(-1).view(np.uint32), s1.view(np.uint32))
+    x2 = x.copy()
+    x2[:, 128:256] *= 4.0
+    q2, s2 = oracle.block_quant(_bf16_bits(x2))
+    assert np.array_equal(q2, q)
+    assert np.array_equal(s2[:, 1], s[:, 1] * 4) and np.array_equal(s2[:, [0, 2, 3, 4]], s[:, [0, 2, 3, 4]])
+
+
+def test_grouped_gemm_block_exact_with_power_of_two_scales():
+    """Small integer codes and power-of-two block scales: every term is exact,
+    so the result equals sum over K blocks of 2^(u+v) x (integer block dot
+    product), computed here with numpy integer matmuls per block. A swapped
+    or transposed scale index changes the powers and fails."""
+    rng = np.random.default_rng(51)
+    counts, N, Kd = [70, 0, 33], 384, 512
+    E, KB, NB = len(counts), Kd // 128, N // 128
+    off = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    M = int(off[-1])
+    Ai = rng.integers(-3, 4, (M, Kd))
+    Bi = rng.integers(-2, 3, (E, N, Kd))
+    A = _codes_of(Ai.astype(np.float32))
+    B = _codes_of(Bi.astype(np.float32))
+    u = rng.integers(-6, 7, (M, KB))
+    v = rng.integers(-6, 7, (E, NB, KB))
+    C = oracle.grouped_gemm_block(A, (2.0 ** u).astype(np.float32), B,
+                                  (2.0 ** v).astype(np.float32), off)
+    ref = np.zeros((M, N))
+    for e in range(E):
+        rows = slice(off[e], off[e + 1])
+        for kb in range(KB):
+            ks = slice(kb * 128, (kb + 1) * 128)
+            part = Ai[rows, ks] @ Bi[e, :, ks].T                       # exact integers
+            ref[rows] += part * 2.0 ** (u[rows, kb][:, None] + np.repeat(v[e, :, kb], 128)[None, :])
+    assert np.array_equal(C, ref)
+
+
+def test_grouped_gemm_block_with_uniform_scales_is_per_token_gemm():
+    """Scales constant along K (one per row, one per 128-row weight block)
+    reduce block FP8 to the per-row x per-channel GEMM."""
+    rng = np.random.default_rng(52)
+    counts, N, Kd = [40, 17], 256, 384
+    E = len(counts)
+    off = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    M = int(off[-1])
+    A = _codes_of(rng.standard_normal((M, Kd)).astype(np.float32))
+    B = _codes_of(rng.standard_normal((E, N, Kd)).astype(np.float32))
+    ra = (10.0 ** rng.uniform(-2, 1, M)).astype(np.float32)
+    rb = (10.0 ** rng.uniform(-3, -1, (E, N // 128))).astype(np.float32)
+    C = oracle.grouped_gemm_block(A, np.repeat(ra[:, None], Kd // 128, 1), B,
+                                  np.repeat(rb[:, :, None], Kd // 128, 2), off)
+    ref = oracle.grouped_gemm(A, ra, B, np.repeat(rb, 128, 1), off)
+    np.testing.assert_allclose(C, ref, rtol=1e-12, atol=0)
+
+
+def _random_block_layer(rng, T, H, I, E):
+    from moe_expert_layer_grouped_gb300 import synth
+    x = _bf16_bits(rng.standard_normal((T, H)))
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    w13, s13 = synth.quantize_weight_blocks(
+        torch.from_numpy(rng.standard_normal((E, 2 * I, H)) * 0.02).float())
+    w2, s2 = synth.quantize_weight_blocks(
+        torch.from_numpy(rng.standard_normal((E, H, I)) * 0.02).float())
+    return x, logits, w13.numpy(), s13.numpy(), w2.numpy(), s2.numpy()
+
+
+def _dense_block_mlp(x, w13e, s13e, w2e, s2e):
+    """One expert on every token in block FP8 with numpy: dequantise the
+    codes block by block, multiply in fp64."""
+    I = w2e.shape[1]
+
+    def deq_act(bits):
+        q, s = oracle.block_quant(bits)
+        return oracle.e4m3_decode(q) * np.repeat(s.astype(np.float64), 128, 1)
+
+    def deq_w(q, s):
+        return oracle.e4m3_decode(q) * np.repeat(np.repeat(s.astype(np.float64), 128, 0), 128, 1)
+
+    C = deq_act(x) @ deq_w(w13e, s13e).T
+    g, u = C[:, :I], C[:, I:]
+    hb = oracle.bf16_round(g / (1 + np.exp(-g)) * u)
+    return deq_act(hb) @ deq_w(w2e, s2e).T
+
+
+def test_layer_block_single_expert_is_dense_block_mlp():
+    rng = np.random.default_rng(53)
+    T, H, I = 6, 256, 128
+    x, logits, w13, s13, w2, s2 = _random_block_layer(rng, T, H, I, 1)
+    out, ids, w = oracle.forward_tokens_block(x, logits, None, w13, s13, w2, s2, 1, 1, 1,
+                                              oracle.SOFTMAX, True, 1.0)
+    assert np.all(ids == 0) and np.all(w == 1.0)
+    ref = _dense_block_mlp(x, w13[0], s13[0], w2[0], s2[0])
+    np.testing.assert_allclose(out, ref, rtol=1e-9, atol=1e-12 * np.abs(ref).max())
+
+
+def test_layer_block_token_path_equals_step_path_with_shared_expert():
+    rng = np.random.default_rng(54)
+    T, H, I, E, S = 20, 256, 128, 8, 1
+    x, logits, w13, s13, w2, s2 = _random_block_layer(rng, T, H, I, E + S)
+    bias = (rng.standard_normal(E) * 0.1).astype(np.float32)
+    args = (4, 2, 3, oracle.SIGMOID, True, 2.5)
+    steps = oracle.forward_steps_block(x, logits[:, :E], bias, w13, s13, w2, s2, *args,
+                                       n_shared=S)
+    out, ids, w = oracle.forward_tokens_block(x, logits[:, :E], bias, w13, s13, w2, s2, *args,
+                                              n_shared=S)
+    assert np.array_equal(ids, steps["ids"][:, :3]) and np.array_equal(w, steps["w"][:, :3])
+    np.testing.assert_allclose(out, steps["out"], rtol=1e-12, atol=1e-12 * np.abs(out).max())
+    # the shared expert adds its dense block MLP with weight 1
+    base, _, _ = oracle.forward_tokens_block(x, logits[:, :E], bias, w13[:E], s13[:E], w2[:E],
+                                             s2[:E], *args)
+    ref = _dense_block_mlp(x, w13[E], s13[E], w2[E], s2[E])
+    np.testing.assert_allclose(out - base, ref, rtol=1e-9, atol=1e-12 * np.abs(out).max())
