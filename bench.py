@@ -134,10 +134,16 @@ def step_work(wl, offsets_list):
     for off in offsets_list:
         cnt = off[1:] - off[:-1]
         active = int((cnt > 0).sum())
-        w13 = active * (2 * I * H + 2 * I * 4)
-        w2 = active * (H * I + H * 4)
-        gemm13_bytes = w13 + M * H + M * 4 + M * I * 2 + (E + 1) * 4
-        gemm2_bytes = w2 + M * I + M * 4 + M * H * 2 + (E + 1) * 4
+        if wl.quant == "block":  # scales per 128 x 128 weight block / 128 channels
+            w13 = active * (2 * I * H + (2 * I // 128) * (H // 128) * 4)
+            w2 = active * (H * I + (H // 128) * (I // 128) * 4)
+            sa, sa2 = M * (H // 128) * 4, M * (I // 128) * 4
+        else:
+            w13 = active * (2 * I * H + 2 * I * 4)
+            w2 = active * (H * I + H * 4)
+            sa, sa2 = M * 4, M * 4
+        gemm13_bytes = w13 + M * H + sa + M * I * 2 + (E + 1) * 4
+        gemm2_bytes = w2 + M * I + sa2 + M * H * 2 + (E + 1) * 4
         flops13 = 2.0 * M * 2 * I * H
         flops2 = 2.0 * M * H * I
         layer_bytes = w13 + w2 + T * H * 2 + T * wl.E * 4 + T * H * 2
@@ -241,15 +247,16 @@ def time_breakdown(moe, layer, wl, batches, steps, torch):
     if S:
         ids[:, wl.top_k:] = torch.arange(wl.E, E, dtype=torch.int32, device=dev)
         w[:, wl.top_k:] = 1.0
+    block = wl.quant == "block"
     a_q = torch.empty((M, H), dtype=torch.uint8, device=dev)
-    sa = torch.empty(M, dtype=torch.float32, device=dev)
+    sa = torch.empty((M, H // 128) if block else M, dtype=torch.float32, device=dev)
     s2d = torch.empty(M, dtype=torch.int32, device=dev)
     off = torch.empty(E + 1, dtype=torch.int32, device=dev)
     pws = torch.empty(max(moe.moe_permute_workspace_size(T, E, K), 256), dtype=torch.uint8,
                       device=dev)
     h = torch.empty((M, I), dtype=torch.bfloat16, device=dev)
     q2 = torch.empty((M, I), dtype=torch.uint8, device=dev)
-    sa2 = torch.empty(M, dtype=torch.float32, device=dev)
+    sa2 = torch.empty((M, I // 128) if block else M, dtype=torch.float32, device=dev)
     down = torch.empty((M, H), dtype=torch.bfloat16, device=dev)
     out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
     names = ["gate", "permute_quant", "grouped_gemm_w13", "act_quant", "grouped_gemm_w2",
@@ -267,14 +274,27 @@ def time_breakdown(moe, layer, wl, batches, steps, torch):
             ids[:, :wl.top_k] = ids_r
             w[:, :wl.top_k] = w_r
         if ev: ev[7].record(st)
-        moe.moe_permute_quant(x, ids, E, a_q=a_q, scale_a=sa, src2dst=s2d, offsets=off,
-                              workspace=pws)
+        if block:
+            moe.moe_permute_quant_block(x, ids, E, a_q=a_q, scale_a=sa, src2dst=s2d,
+                                        offsets=off, workspace=pws)
+        else:
+            moe.moe_permute_quant(x, ids, E, a_q=a_q, scale_a=sa, src2dst=s2d, offsets=off,
+                                  workspace=pws)
         if ev: ev[2].record(st)
-        moe.moe_grouped_gemm(a_q, sa, layer.w13, layer.s13, off, moe.EPI_SILU_MUL, C=h)
+        if block:
+            moe.moe_grouped_gemm_block(a_q, sa, layer.w13, layer.s13, off, moe.EPI_SILU_MUL, C=h)
+        else:
+            moe.moe_grouped_gemm(a_q, sa, layer.w13, layer.s13, off, moe.EPI_SILU_MUL, C=h)
         if ev: ev[3].record(st)
-        moe.moe_act_quant(h, q=q2, scale=sa2)
+        if block:
+            moe.moe_act_quant_block(h, q=q2, scale=sa2)
+        else:
+            moe.moe_act_quant(h, q=q2, scale=sa2)
         if ev: ev[4].record(st)
-        moe.moe_grouped_gemm(q2, sa2, layer.w2, layer.s2, off, moe.EPI_BF16, C=down)
+        if block:
+            moe.moe_grouped_gemm_block(q2, sa2, layer.w2, layer.s2, off, moe.EPI_BF16, C=down)
+        else:
+            moe.moe_grouped_gemm(q2, sa2, layer.w2, layer.s2, off, moe.EPI_BF16, C=down)
         if ev: ev[5].record(st)
         moe.moe_unpermute_sum(down, s2d, w, out=out)
         if ev: ev[6].record(st)
@@ -324,7 +344,7 @@ def run_workload(moe, synth, torch, wl, seed, steps, warmup, dev, pk, want_clock
     d = synth.make_inputs(wl, seed=seed, device=dev, weights=True)
     layer = moe.MoELayer(d["w13"], d["s13"], d["w2"], d["s2"], d["bias"], wl.num_groups,
                          wl.topk_group, wl.top_k, wl.scoring, wl.renormalize, wl.rsf, wl.T,
-                         n_shared=wl.n_shared)
+                         n_shared=wl.n_shared, quant=wl.quant)
     batches = make_batches(wl, seed, dev, synth)
     out = torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device=dev)
     clocks = ClockSampler(dev.index) if want_clocks else None
@@ -379,15 +399,15 @@ def cpu_baseline(synth, torch, wl, seed, r, budget_s=15.0):
     args = (n["x"], n["logits"], n["bias"], n["w13"], n["s13"], n["w2"], n["s2"],
             wl.num_groups, wl.topk_group, wl.top_k, wl.scoring, wl.renormalize, wl.rsf)
     threads = oracle.get_threads()
+    fwd = oracle.forward_tokens_block if wl.quant == "block" else oracle.forward_tokens
     t = time.time()
-    oracle.forward_tokens(*args, tokens=np.arange(min(threads, wl.T), dtype=np.int64),
-                          n_shared=wl.n_shared)
+    fwd(*args, tokens=np.arange(min(threads, wl.T), dtype=np.int64), n_shared=wl.n_shared)
     per_tok = (time.time() - t) / min(threads, wl.T)
     ntok = int(max(1, min(wl.T, budget_s / max(per_tok, 1e-6))))
     reps = max(1, int(budget_s / max(per_tok * ntok, 1e-6)))
     toks = np.tile(np.arange(ntok, dtype=np.int64), reps)
     t = time.time()
-    oracle.forward_tokens(*args, tokens=toks, n_shared=wl.n_shared)
+    fwd(*args, tokens=toks, n_shared=wl.n_shared)
     dt = time.time() - t
     return {"value": round(toks.size / dt, 3), "unit": "tokens/s", "cores": threads,
             "kind": "oracle",
@@ -440,7 +460,7 @@ def run_ours(args):
         "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E,
                    "num_groups": wl.num_groups, "topk_group": wl.topk_group, "top_k": wl.top_k,
                    "scoring": "sigmoid" if wl.scoring == 0 else "softmax", "rsf": wl.rsf,
-                   "n_shared": wl.n_shared, "batches_cycled": N_BATCHES,
+                   "n_shared": wl.n_shared, "quant": wl.quant, "batches_cycled": N_BATCHES,
                    "l2": "no flush: each step streams the active experts' weights "
                          f"(~{r['work']['layer_bytes'] / 1e9:.2f} GB) through the 129 MB L2",
                    "parallelism": f"replicas x{world} (no collective on the data path)"},
@@ -477,7 +497,7 @@ def run_ours(args):
         d = synth.make_inputs(wl, seed=seed, device=dev, weights=True)
         layer = moe.MoELayer(d["w13"], d["s13"], d["w2"], d["s2"], d["bias"], wl.num_groups,
                              wl.topk_group, wl.top_k, wl.scoring, wl.renormalize, wl.rsf, wl.T,
-                             n_shared=wl.n_shared)
+                             n_shared=wl.n_shared, quant=wl.quant)
         line["cpu_baseline"] = cpu_baseline(synth, torch, wl, seed,
                                             {"layer": layer, "batches": make_batches(
                                                 wl, seed, dev, synth)})
@@ -513,17 +533,17 @@ def run_reference(args):
     threads = oracle.get_threads()
     t = time.time()
     S = wl.n_shared
-    oracle.forward_tokens(*fargs, tokens=np.arange(min(threads, wl.T), dtype=np.int64),
-                          n_shared=S)
+    fwd = oracle.forward_tokens_block if wl.quant == "block" else oracle.forward_tokens
+    fwd(*fargs, tokens=np.arange(min(threads, wl.T), dtype=np.int64), n_shared=S)
     per_tok = (time.time() - t) / min(threads, wl.T)
     budget = max(5.0, 60.0 / max(1, steps + warmup))
     ntok = int(max(1, min(wl.T, budget / max(per_tok, 1e-6))))
     toks = np.arange(ntok, dtype=np.int64)
     for _ in range(warmup):
-        oracle.forward_tokens(*fargs, tokens=toks, n_shared=S)
+        fwd(*fargs, tokens=toks, n_shared=S)
     t = time.time()
     for _ in range(steps):
-        oracle.forward_tokens(*fargs, tokens=toks, n_shared=S)
+        fwd(*fargs, tokens=toks, n_shared=S)
     dt = (time.time() - t) / steps
     value = ntok / dt
     sample = (f"{ntok} of the {wl.T} tokens of one {wl.name} batch per step, whole layer "
@@ -536,7 +556,7 @@ def run_reference(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "f64 (FP8 codes decoded exactly)",
         "data": "synthetic (seeded)",
         "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E,
-                   "top_k": wl.top_k, "n_shared": wl.n_shared},
+                   "top_k": wl.top_k, "n_shared": wl.n_shared, "quant": wl.quant},
         "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": threads,
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,

@@ -288,6 +288,68 @@ MOE_API moe_status moe_forward_shared_host(const void* x_host,
                               float routed_scaling_factor, void* out_host,
                               void* ws, size_t ws_bytes, void* stream);
 
+/* ==========================================================================
+ * Block-quantised FP8: one fp32 scale per 128 x 128 weight block (output
+ * block x input block) and one per token per 128 input channels, the format
+ * DeepSeek-V3 checkpoints ship in. [P1] Highlights contrasts the per-token
+ * path with this block (group_k / group_n) path; it does not write the
+ * formula, taken here as: every 128-channel partial sum is dequantised by
+ * its own activation and weight block scales,
+ *   C[r,n] = sum_kb ( sum_{k in kb} A[r,k] B[e,n,k] ) * sa[r,kb] * sb[e,n/128,kb]
+ * and activations are quantised per block with the per-token rule
+ * (scale = max(amax_block, 1e-10)/448, code = e4m3(x / scale)).
+ * ======================================================================== */
+
+/* moe_permute_quant with block scales: scale_a [T*K, H/128] f32, row d
+ * holding the scales of the token copied to row d. H % 128 == 0. Same
+ * workspace as moe_permute_quant. Codes and scales bit-exact. */
+MOE_API moe_status moe_permute_quant_block(const void* x, const int32_t* topk_ids,
+                              int T, int H, int E, int K, void* a_q,
+                              float* scale_a, int32_t* src2dst, int32_t* offsets,
+                              void* ws, size_t ws_bytes, void* stream);
+
+/* moe_grouped_gemm with block scales: scale_a [M, Kd/128] f32, scale_b
+ * [E, N/128, Kd/128] f32; epilogues as moe_grouped_gemm (no row amax).
+ * Kd % 128 == 0; N % 128 == 0 (SILU_MUL: N % 256 == 0, i.e. I % 128 == 0). */
+MOE_API moe_status moe_grouped_gemm_block(const void* A, const float* scale_a,
+                              const void* B, const float* scale_b,
+                              const int32_t* offsets, int M, int N, int Kd, int E,
+                              int epilogue, void* C, void* stream);
+
+/* moe_act_quant with block scales: scale [M, I/128] f32. I % 128 == 0.
+ * Bit-exact. */
+MOE_API moe_status moe_act_quant_block(const void* h, int M, int I, void* q,
+                              float* scale, void* stream);
+
+/* Workspace bytes of moe_forward_block / moe_forward_block_host; with shared
+ * experts pass E + n_shared and top_k + n_shared. 0 if H or I is not a
+ * multiple of 128. */
+MOE_API size_t moe_block_workspace_size(int T, int H, int I, int E, int K);
+
+/* The whole layer in block FP8 (with n_shared shared experts as in
+ * moe_forward_shared; 0 for none): s13 [E+n_shared, 2I/128, H/128],
+ * s2 [E+n_shared, H/128, I/128]; otherwise as moe_forward_shared.
+ * H % 128 == 0 and I % 128 == 0. */
+MOE_API moe_status moe_forward_block(const void* x, const float* logits,
+                              const float* bias, const void* w13,
+                              const float* s13, const void* w2, const float* s2,
+                              int T, int H, int I, int E, int n_shared,
+                              int num_groups, int topk_group, int top_k,
+                              int scoring, int renormalize,
+                              float routed_scaling_factor, void* out, void* ws,
+                              size_t ws_bytes, void* stream);
+
+/* moe_forward_block with x, logits and out in host memory, as
+ * moe_forward_host. */
+MOE_API moe_status moe_forward_block_host(const void* x_host,
+                              const float* logits_host, const float* bias,
+                              const void* w13, const float* s13, const void* w2,
+                              const float* s2, int T, int H, int I, int E,
+                              int n_shared, int num_groups, int topk_group,
+                              int top_k, int scoring, int renormalize,
+                              float routed_scaling_factor, void* out_host,
+                              void* ws, size_t ws_bytes, void* stream);
+
 /*
  * moe_device_status — synchronises the current device, copies its device
  * error word into *code (one of MOE_DEV_*), clears it, and returns MOE_OK

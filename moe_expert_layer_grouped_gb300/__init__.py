@@ -17,7 +17,9 @@ import os
 __all__ = [
     "MoEError", "SIGMOID", "SOFTMAX", "EPI_BF16", "EPI_SILU_MUL", "library_path", "load",
     "moe_gate", "moe_permute_quant", "moe_permute_workspace_size", "moe_grouped_gemm",
-    "moe_forward_shared", "moe_forward_shared_host",
+    "moe_forward_shared", "moe_forward_shared_host", "moe_permute_quant_block",
+    "moe_grouped_gemm_block", "moe_act_quant_block", "moe_block_workspace_size",
+    "moe_forward_block", "moe_forward_block_host",
     "moe_permute_quant_noalloc", "moe_act_quant", "moe_unpermute_sum", "moe_workspace_size", "moe_forward",
     "moe_forward_host", "moe_device_status", "MoELayer",
 ]
@@ -68,6 +70,14 @@ _SIGNATURES = {
                                 _I, _F, _P, _P, _SZ, _P]),
     "moe_forward_shared_host": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I,
                                      _I, _I, _F, _P, _P, _SZ, _P]),
+    "moe_permute_quant_block": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_grouped_gemm_block": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P]),
+    "moe_act_quant_block": (_I, [_P, _I, _I, _P, _P, _P]),
+    "moe_block_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
+    "moe_forward_block": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I,
+                               _I, _F, _P, _P, _SZ, _P]),
+    "moe_forward_block_host": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I,
+                                    _I, _I, _F, _P, _P, _SZ, _P]),
     "moe_device_status": (_I, [ctypes.POINTER(_I)]),
 }
 
@@ -303,6 +313,103 @@ def moe_forward_shared_host(x_host, logits_host, bias, w13, s13, w2, s2, n_share
     return out_host
 
 
+# ---- block-quantised FP8 (128-channel activation scales, 128 x 128 weight scales)
+def moe_permute_quant_block(x, topk_ids, E, a_q=None, scale_a=None, src2dst=None, offsets=None,
+                            workspace=None, stream=None):
+    """moe_permute_quant with one scale per token per 128 channels: scale_a [T*K, H/128]."""
+    import torch
+    _need_cuda(x, topk_ids)
+    T, H = x.shape
+    K = topk_ids.shape[1]
+    dev = x.device
+    M = T * K
+    a_q = torch.empty((M, H), dtype=torch.uint8, device=dev) if a_q is None else a_q
+    if scale_a is None:
+        scale_a = torch.empty((M, H // 128), dtype=torch.float32, device=dev)
+    src2dst = torch.empty(M, dtype=torch.int32, device=dev) if src2dst is None else src2dst
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev) if offsets is None else offsets
+    if workspace is None:
+        workspace = torch.empty(max(moe_permute_workspace_size(T, E, K), 256), dtype=torch.uint8,
+                                device=dev)
+    _check("moe_permute_quant_block", load().moe_permute_quant_block(
+        _ptr(x), _ptr(topk_ids), T, H, E, K, _ptr(_u8(a_q)), _ptr(scale_a), _ptr(src2dst),
+        _ptr(offsets), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream)))
+    return a_q, scale_a, src2dst, offsets
+
+
+def moe_grouped_gemm_block(A, scale_a, B, scale_b, offsets, epilogue=EPI_BF16, C=None,
+                           stream=None):
+    """scale_a [M, Kd/128]; scale_b [E, N/128, Kd/128]."""
+    import torch
+    _need_cuda(A, scale_a, B, scale_b, offsets, C)
+    M, Kd = A.shape
+    E, N, Kd2 = B.shape
+    if Kd2 != Kd:
+        raise ValueError("moe_grouped_gemm_block: K mismatch")
+    if C is None:
+        cols = N // 2 if epilogue == EPI_SILU_MUL else N
+        C = torch.empty((M, cols), dtype=torch.bfloat16, device=A.device)
+    _check("moe_grouped_gemm_block", load().moe_grouped_gemm_block(
+        _ptr(_u8(A)), _ptr(scale_a), _ptr(_u8(B)), _ptr(scale_b), _ptr(offsets), M, N, Kd, E,
+        epilogue, _ptr(C), _stream(stream)))
+    return C
+
+
+def moe_act_quant_block(h, q=None, scale=None, stream=None):
+    """Requantisation with one scale per row per 128 channels: scale [M, I/128]."""
+    import torch
+    _need_cuda(h)
+    M, I = h.shape
+    q = torch.empty((M, I), dtype=torch.uint8, device=h.device) if q is None else q
+    if scale is None:
+        scale = torch.empty((M, I // 128), dtype=torch.float32, device=h.device)
+    _check("moe_act_quant_block", load().moe_act_quant_block(
+        _ptr(h), M, I, _ptr(_u8(q)), _ptr(scale), _stream(stream)))
+    return q, scale
+
+
+def moe_block_workspace_size(T, H, I, E, K):
+    return load().moe_block_workspace_size(T, H, I, E, K)
+
+
+def moe_forward_block(x, logits, bias, w13, s13, w2, s2, n_shared, num_groups, topk_group, top_k,
+                      scoring=SIGMOID, renormalize=True, routed_scaling_factor=1.0, out=None,
+                      workspace=None, stream=None):
+    """The layer in block FP8: s13 [E+n_shared, 2I/128, H/128], s2 [E+n_shared, H/128, I/128]."""
+    import torch
+    _need_cuda(x, logits, bias, w13, s13, w2, s2, out, workspace)
+    T, H, I, E = _dims(x, logits, w13, w2, n_shared)
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=x.device) if out is None else out
+    if workspace is None:
+        nws = moe_block_workspace_size(T, H, I, E + n_shared, top_k + n_shared)
+        workspace = torch.empty(nws, dtype=torch.uint8, device=x.device)
+    _check("moe_forward_block", load().moe_forward_block(
+        _ptr(x), _ptr(logits), _ptr(bias), _ptr(_u8(w13)), _ptr(s13), _ptr(_u8(w2)), _ptr(s2),
+        T, H, I, E, int(n_shared), num_groups, topk_group, top_k, scoring,
+        int(bool(renormalize)), float(routed_scaling_factor), _ptr(out), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out
+
+
+def moe_forward_block_host(x_host, logits_host, bias, w13, s13, w2, s2, n_shared, num_groups,
+                           topk_group, top_k, scoring, renormalize, routed_scaling_factor,
+                           out_host, workspace, stream=None):
+    """moe_forward_block with x, logits and out in host memory."""
+    _need_cuda(bias, w13, s13, w2, s2, workspace)
+    for t in (x_host, logits_host, out_host):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError("moe_forward_block_host: x, logits and out must be contiguous "
+                             "host tensors")
+    T, H, I, E = _dims(x_host, logits_host, w13, w2, n_shared)
+    _check("moe_forward_block_host", load().moe_forward_block_host(
+        _ptr(x_host), _ptr(logits_host), _ptr(bias), _ptr(_u8(w13)), _ptr(s13), _ptr(_u8(w2)),
+        _ptr(s2), T, H, I, E, int(n_shared), num_groups, topk_group, top_k, scoring,
+        int(bool(renormalize)), float(routed_scaling_factor), _ptr(out_host), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out_host
+
+
 def moe_device_status():
     """Synchronise the device and return (and clear) its device error code."""
     code = ctypes.c_int(0)
@@ -315,11 +422,15 @@ def moe_device_status():
 class MoELayer:
     """A layer's resident weights plus a reusable workspace; calls moe_forward
     (moe_forward_shared when the layer has shared experts, stored as the last
-    n_shared experts of w13/w2)."""
+    n_shared experts of w13/w2; moe_forward_block for block-quantised weights,
+    quant="block")."""
 
     def __init__(self, w13, s13, w2, s2, bias, num_groups, topk_group, top_k, scoring,
-                 renormalize, routed_scaling_factor, max_tokens, n_shared=0):
+                 renormalize, routed_scaling_factor, max_tokens, n_shared=0, quant="token"):
         import torch
+        if quant not in ("token", "block"):
+            raise ValueError("MoELayer: quant is 'token' or 'block'")
+        self.quant = quant
         self.w13, self.s13, self.w2, self.s2, self.bias = w13, s13, w2, s2, bias
         EA, I2, self.H = w13.shape
         self.n_shared = n_shared
@@ -328,13 +439,18 @@ class MoELayer:
         self.num_groups, self.topk_group, self.top_k = num_groups, topk_group, top_k
         self.scoring, self.renormalize, self.rsf = scoring, renormalize, routed_scaling_factor
         self.max_tokens = max_tokens
-        self.workspace = torch.empty(
-            moe_workspace_size(max_tokens, self.H, self.I, EA, top_k + n_shared),
-            dtype=torch.uint8, device=w13.device)
+        size = moe_block_workspace_size if quant == "block" else moe_workspace_size
+        self.workspace = torch.empty(size(max_tokens, self.H, self.I, EA, top_k + n_shared),
+                                     dtype=torch.uint8, device=w13.device)
 
     def __call__(self, x, logits, out=None, stream=None):
         if x.shape[0] > self.max_tokens:
             raise ValueError("MoELayer: more tokens than the workspace was sized for")
+        if self.quant == "block":
+            return moe_forward_block(x, logits, self.bias, self.w13, self.s13, self.w2, self.s2,
+                                     self.n_shared, self.num_groups, self.topk_group,
+                                     self.top_k, self.scoring, self.renormalize, self.rsf,
+                                     out=out, workspace=self.workspace, stream=stream)
         if self.n_shared:
             return moe_forward_shared(x, logits, self.bias, self.w13, self.s13, self.w2,
                                       self.s2, self.n_shared, self.num_groups, self.topk_group,
@@ -346,6 +462,12 @@ class MoELayer:
                            stream=stream)
 
     def forward_host(self, x_host, logits_host, out_host, stream=None):
+        if self.quant == "block":
+            return moe_forward_block_host(x_host, logits_host, self.bias, self.w13, self.s13,
+                                          self.w2, self.s2, self.n_shared, self.num_groups,
+                                          self.topk_group, self.top_k, self.scoring,
+                                          self.renormalize, self.rsf, out_host,
+                                          self.workspace, stream=stream)
         if self.n_shared:
             return moe_forward_shared_host(x_host, logits_host, self.bias, self.w13, self.s13,
                                            self.w2, self.s2, self.n_shared, self.num_groups,

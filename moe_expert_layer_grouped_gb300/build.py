@@ -17,7 +17,8 @@ OBJ = os.path.join(HERE, "_build")
 LIB_DIR = os.path.join(HERE, "_lib")
 LIB = os.path.join(LIB_DIR, "libmoe_gb300.so")
 
-SOURCES = ["api.cu", "gate.cu", "permute.cu", "gemm.cu", "act_quant.cu", "unpermute.cu"]
+SOURCES = ["api.cu", "gate.cu", "permute.cu", "gemm.cu", "gemm_block.cu", "act_quant.cu",
+           "unpermute.cu"]
 HEADERS = ["common.cuh", "ptx.cuh", "internal.h"]
 
 NVCC_FLAGS = [

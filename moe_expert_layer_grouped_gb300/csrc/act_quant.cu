@@ -3,7 +3,8 @@
 // and Code Review: down_input is requantised per token, giving
 // w2_input_scale). One warp per row, 128-bit loads: pass 1 reduces the row's
 // amax (skipped when the GEMM epilogue supplied it), pass 2 re-reads the row
-// (an L1 hit) and writes the codes.
+// (an L1 hit) and writes the codes. The block variant (one scale per 128
+// channels, the block-quantised FP8 path) quantises each block in one pass.
 #include "common.cuh"
 #include "internal.h"
 
@@ -44,7 +45,48 @@ __global__ void __launch_bounds__(kWarps * 32)
   }
 }
 
+// Block requantisation: one scale per 128 channels of a row (scale
+// [M, I/128]). A warp takes a row two blocks at a time, a half-warp per
+// block (16 lanes x 8 values), the block amax by a 16-lane shuffle.
+__global__ void __launch_bounds__(kWarps * 32)
+    act_quant_block_kernel(const __nv_bfloat16* __restrict__ h, int M, int I,
+                           uint8_t* __restrict__ q, float* __restrict__ scale) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t row = (int64_t)blockIdx.x * kWarps + warp;
+  if (row >= M) return;  // warp-uniform
+  const int nb = I >> 7;
+  const uint4* hr = reinterpret_cast<const uint4*>(h + row * I);
+  uint2* qr = reinterpret_cast<uint2*>(q + row * I);
+  for (int b0 = 0; b0 < nb; b0 += 2) {
+    const int b = b0 + (lane >> 4);
+    const bool in = b < nb;
+    const int vi = b * 16 + (lane & 15);
+    float f[8];
+    float m = 0.0f;
+    if (in) {
+      bf16x8_to_f32(__ldg(hr + vi), f);
+      m = absmax8(f, 0.0f);
+    }
+#pragma unroll
+    for (int o = 1; o < 16; o <<= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
+    if (in) {
+      const float sc = token_scale(m);
+      qr[vi] = quant8(f, sc);
+      if ((lane & 15) == 0) scale[row * nb + b] = sc;
+    }
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_act_quant_block(const void* h, int M, int I, void* q, float* scale,
+                                   cudaStream_t st) {
+  if (M == 0) return cudaSuccess;
+  const int blocks = (M + kWarps - 1) / kWarps;
+  act_quant_block_kernel<<<blocks, kWarps * 32, 0, st>>>(
+      reinterpret_cast<const __nv_bfloat16*>(h), M, I, reinterpret_cast<uint8_t*>(q), scale);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_act_quant(const void* h, const float* row_amax, int M, int I, void* q,
                              float* scale, cudaStream_t st) {

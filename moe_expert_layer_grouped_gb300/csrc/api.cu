@@ -104,7 +104,8 @@ struct FwdLayout {
   size_t ids, w, perm, offsets, s2d, sa, sa2, a_q, h, q2, down, x_in, logits_in, out, total;
 };
 
-FwdLayout fwd_layout(int T, int H, int I, int E, int K) {
+// block: 128-channel block scales (scale_a [M, H/128], scale_a2 [M, I/128]).
+FwdLayout fwd_layout(int T, int H, int I, int E, int K, bool block = false) {
   FwdLayout L;
   const size_t M = (size_t)T * K;
   size_t o = 0;
@@ -118,8 +119,8 @@ FwdLayout fwd_layout(int T, int H, int I, int E, int K) {
   L.perm = take(permute_ws_bytes(T, E));
   L.offsets = take((size_t)(E + 1) * 4);
   L.s2d = take(M * 4);
-  L.sa = take(M * 4);
-  L.sa2 = take(M * 4);
+  L.sa = take(M * 4 * (size_t)(block ? H / 128 : 1));
+  L.sa2 = take(M * 4 * (size_t)(block ? I / 128 : 1));
   L.a_q = take(M * (size_t)H);
   L.h = take(M * (size_t)I * 2);
   L.q2 = take(M * (size_t)I);
@@ -140,9 +141,10 @@ Tp* at(void* ws, size_t off) {
 moe_status check_forward(const void* x, const float* logits, const float* bias, const void* w13,
                          const float* s13, const void* w2, const float* s2, int T, int H, int I,
                          int E, int S, int G, int TG, int K, int scoring, const void* out,
-                         const void* ws, size_t ws_bytes) {
+                         const void* ws, size_t ws_bytes, bool block) {
   if (S < 0) return MOE_ERR_INVALID_ARG;
   if (H < 1 || I < 1 || H % 32 != 0 || I % 32 != 0) return MOE_ERR_INVALID_ARG;
+  if (block && (H % 128 != 0 || I % 128 != 0)) return MOE_ERR_INVALID_ARG;
   if (H > kMaxH) return MOE_ERR_UNSUPPORTED;
   // the gate check without its output pointers (they live in the workspace)
   if (T < 0 || E < 1 || G < 1 || TG < 1 || K < 1) return MOE_ERR_INVALID_ARG;
@@ -157,7 +159,7 @@ moe_status check_forward(const void* x, const float* logits, const float* bias, 
   if (bias != nullptr && !aligned16(bias)) return MOE_ERR_INVALID_ARG;
   if (T > 0 && (!ok_ptr(x) || !ok_ptr(logits) || !ok_ptr(out))) return MOE_ERR_INVALID_ARG;
   if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0 ||
-      ws_bytes < fwd_layout(T, H, I, E + S, K + S).total)
+      ws_bytes < fwd_layout(T, H, I, E + S, K + S, block).total)
     return MOE_ERR_WORKSPACE;
   return MOE_OK;
 }
@@ -165,12 +167,14 @@ moe_status check_forward(const void* x, const float* logits, const float* bias, 
 // The gate picks K of the E routed experts and appends the S shared ones
 // (weight 1) to every token's row; from the permute on, the layer is a
 // routed layer of E + S experts and K + S slots.
+// block: the block-scaled FP8 steps (128-channel activation scales, 128 x 128
+// weight scales) in place of the per-token ones.
 moe_status run_forward(const void* x, const float* logits, const float* bias, const void* w13,
                        const float* s13, const void* w2, const float* s2, int T, int H, int I,
                        int E, int S, int G, int TG, int K, int scoring, int renorm, float rsf,
-                       void* out, void* ws, cudaStream_t st) {
+                       void* out, void* ws, cudaStream_t st, bool block) {
   const int EA = E + S, KA = K + S;  // experts and slots after the gate
-  const FwdLayout L = fwd_layout(T, H, I, EA, KA);
+  const FwdLayout L = fwd_layout(T, H, I, EA, KA, block);
   int* err = device_error_word();
   if (err == nullptr) return MOE_ERR_CUDA;
   const int M = T * KA;
@@ -187,16 +191,29 @@ moe_status run_forward(const void* x, const float* logits, const float* bias, co
   cudaError_t e;
   if ((e = launch_gate(logits, bias, T, E, G, TG, K, scoring, renorm, rsf, ids, w, S, st)))
     return cuda_status(e);
-  if ((e = launch_permute_quant(x, ids, T, H, EA, KA, a_q, sa, s2d, offsets,
-                                at<void>(ws, L.perm), err, st)))
-    return cuda_status(e);
-  if ((e = launch_grouped_gemm(a_q, sa, w13, s13, offsets, M, 2 * I, H, EA, MOE_EPI_SILU_MUL, h,
-                               nullptr, err, st)))
-    return cuda_status(e);
-  if ((e = launch_act_quant(h, nullptr, M, I, q2, sa2, st))) return cuda_status(e);
-  if ((e = launch_grouped_gemm(q2, sa2, w2, s2, offsets, M, H, I, EA, MOE_EPI_BF16, down,
-                               nullptr, err, st)))
-    return cuda_status(e);
+  if (block) {
+    if ((e = launch_permute_quant_block(x, ids, T, H, EA, KA, a_q, sa, s2d, offsets,
+                                        at<void>(ws, L.perm), err, st)))
+      return cuda_status(e);
+    if ((e = launch_grouped_gemm_block(a_q, sa, w13, s13, offsets, M, 2 * I, H, EA,
+                                       MOE_EPI_SILU_MUL, h, err, st)))
+      return cuda_status(e);
+    if ((e = launch_act_quant_block(h, M, I, q2, sa2, st))) return cuda_status(e);
+    if ((e = launch_grouped_gemm_block(q2, sa2, w2, s2, offsets, M, H, I, EA, MOE_EPI_BF16,
+                                       down, err, st)))
+      return cuda_status(e);
+  } else {
+    if ((e = launch_permute_quant(x, ids, T, H, EA, KA, a_q, sa, s2d, offsets,
+                                  at<void>(ws, L.perm), err, st)))
+      return cuda_status(e);
+    if ((e = launch_grouped_gemm(a_q, sa, w13, s13, offsets, M, 2 * I, H, EA, MOE_EPI_SILU_MUL,
+                                 h, nullptr, err, st)))
+      return cuda_status(e);
+    if ((e = launch_act_quant(h, nullptr, M, I, q2, sa2, st))) return cuda_status(e);
+    if ((e = launch_grouped_gemm(q2, sa2, w2, s2, offsets, M, H, I, EA, MOE_EPI_BF16, down,
+                                 nullptr, err, st)))
+      return cuda_status(e);
+  }
   if ((e = launch_unpermute_sum(down, s2d, w, T, KA, H, out, err, st))) return cuda_status(e);
   return MOE_OK;
 }
@@ -310,19 +327,69 @@ size_t moe_workspace_size(int T, int H, int I, int E, int K) {
   return fwd_layout(T, H, I, E, K).total;
 }
 
+}  // extern "C"
+
+namespace moe {
+namespace {
+
+moe_status forward_device(const void* x, const float* logits, const float* bias, const void* w13,
+                          const float* s13, const void* w2, const float* s2, int T, int H, int I,
+                          int E, int S, int G, int TG, int K, int scoring, int renorm, float rsf,
+                          void* out, void* ws, size_t ws_bytes, void* stream, bool block) {
+  moe_status s = check_forward(x, logits, bias, w13, s13, w2, s2, T, H, I, E, S, G, TG, K,
+                               scoring, out, ws, ws_bytes, block);
+  if (s != MOE_OK) return s;
+  if (T == 0) return MOE_OK;
+  return run_forward(x, logits, bias, w13, s13, w2, s2, T, H, I, E, S, G, TG, K, scoring, renorm,
+                     rsf, out, ws, static_cast<cudaStream_t>(stream), block);
+}
+
+// x, logits and out in host memory: copied through the workspace on `stream`.
+moe_status forward_host(const void* x_host, const float* logits_host, const float* bias,
+                        const void* w13, const float* s13, const void* w2, const float* s2,
+                        int T, int H, int I, int E, int S, int G, int TG, int K, int scoring,
+                        int renorm, float rsf, void* out_host, void* ws, size_t ws_bytes,
+                        void* stream, bool block) {
+  if (T > 0 && (x_host == nullptr || logits_host == nullptr || out_host == nullptr))
+    return MOE_ERR_INVALID_ARG;
+  if (ws == nullptr) return MOE_ERR_WORKSPACE;
+  if (S < 0 || H < 1 || I < 1 || E < 1 || K < 1) return MOE_ERR_INVALID_ARG;
+  if (block && (H % 128 != 0 || I % 128 != 0)) return MOE_ERR_INVALID_ARG;
+  const FwdLayout L = fwd_layout(T < 0 ? 0 : T, H, I, E + S, K + S, block);
+  void* x_d = at<void>(ws, L.x_in);
+  float* l_d = at<float>(ws, L.logits_in);
+  void* o_d = at<void>(ws, L.out);
+  moe_status s = check_forward(x_d, l_d, bias, w13, s13, w2, s2, T, H, I, E, S, G, TG, K,
+                               scoring, o_d, ws, ws_bytes, block);
+  if (s != MOE_OK) return s;
+  if (T == 0) return MOE_OK;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t xb = (size_t)T * H * 2, lb = (size_t)T * E * 4;
+  if (cudaMemcpyAsync(x_d, x_host, xb, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+      cudaMemcpyAsync(l_d, logits_host, lb, cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  s = run_forward(x_d, l_d, bias, w13, s13, w2, s2, T, H, I, E, S, G, TG, K, scoring, renorm,
+                  rsf, o_d, ws, st, block);
+  if (s != MOE_OK) return s;
+  if (cudaMemcpyAsync(out_host, o_d, xb, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" {
+
 moe_status moe_forward_shared(const void* x, const float* logits, const float* bias,
                               const void* w13, const float* s13, const void* w2, const float* s2,
                               int T, int H, int I, int E, int n_shared, int num_groups,
                               int topk_group, int top_k, int scoring, int renormalize,
                               float routed_scaling_factor, void* out, void* ws, size_t ws_bytes,
                               void* stream) {
-  moe_status s = check_forward(x, logits, bias, w13, s13, w2, s2, T, H, I, E, n_shared,
-                               num_groups, topk_group, top_k, scoring, out, ws, ws_bytes);
-  if (s != MOE_OK) return s;
-  if (T == 0) return MOE_OK;
-  return run_forward(x, logits, bias, w13, s13, w2, s2, T, H, I, E, n_shared, num_groups,
-                     topk_group, top_k, scoring, renormalize, routed_scaling_factor, out, ws,
-                     static_cast<cudaStream_t>(stream));
+  return forward_device(x, logits, bias, w13, s13, w2, s2, T, H, I, E, n_shared, num_groups,
+                        topk_group, top_k, scoring, renormalize, routed_scaling_factor, out, ws,
+                        ws_bytes, stream, false);
 }
 
 moe_status moe_forward(const void* x, const float* logits, const float* bias, const void* w13,
@@ -330,9 +397,9 @@ moe_status moe_forward(const void* x, const float* logits, const float* bias, co
                        int E, int num_groups, int topk_group, int top_k, int scoring,
                        int renormalize, float routed_scaling_factor, void* out, void* ws,
                        size_t ws_bytes, void* stream) {
-  return moe_forward_shared(x, logits, bias, w13, s13, w2, s2, T, H, I, E, 0, num_groups,
-                            topk_group, top_k, scoring, renormalize, routed_scaling_factor, out,
-                            ws, ws_bytes, stream);
+  return forward_device(x, logits, bias, w13, s13, w2, s2, T, H, I, E, 0, num_groups,
+                        topk_group, top_k, scoring, renormalize, routed_scaling_factor, out, ws,
+                        ws_bytes, stream, false);
 }
 
 moe_status moe_forward_shared_host(const void* x_host, const float* logits_host,
@@ -341,30 +408,9 @@ moe_status moe_forward_shared_host(const void* x_host, const float* logits_host,
                                    int n_shared, int num_groups, int topk_group, int top_k,
                                    int scoring, int renormalize, float routed_scaling_factor,
                                    void* out_host, void* ws, size_t ws_bytes, void* stream) {
-  if (T > 0 && (x_host == nullptr || logits_host == nullptr || out_host == nullptr))
-    return MOE_ERR_INVALID_ARG;
-  if (ws == nullptr) return MOE_ERR_WORKSPACE;
-  const int S = n_shared < 0 ? 0 : n_shared;
-  const FwdLayout L = fwd_layout(T < 0 ? 0 : T, H < 1 ? 1 : H, I < 1 ? 1 : I,
-                                 (E < 1 ? 1 : E) + S, (top_k < 1 ? 1 : top_k) + S);
-  void* x_d = at<void>(ws, L.x_in);
-  float* l_d = at<float>(ws, L.logits_in);
-  void* o_d = at<void>(ws, L.out);
-  moe_status s = check_forward(x_d, l_d, bias, w13, s13, w2, s2, T, H, I, E, n_shared,
-                               num_groups, topk_group, top_k, scoring, o_d, ws, ws_bytes);
-  if (s != MOE_OK) return s;
-  if (T == 0) return MOE_OK;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const size_t xb = (size_t)T * H * 2, lb = (size_t)T * E * 4;
-  if (cudaMemcpyAsync(x_d, x_host, xb, cudaMemcpyHostToDevice, st) != cudaSuccess ||
-      cudaMemcpyAsync(l_d, logits_host, lb, cudaMemcpyHostToDevice, st) != cudaSuccess)
-    return MOE_ERR_CUDA;
-  s = run_forward(x_d, l_d, bias, w13, s13, w2, s2, T, H, I, E, n_shared, num_groups,
-                  topk_group, top_k, scoring, renormalize, routed_scaling_factor, o_d, ws, st);
-  if (s != MOE_OK) return s;
-  if (cudaMemcpyAsync(out_host, o_d, xb, cudaMemcpyDeviceToHost, st) != cudaSuccess)
-    return MOE_ERR_CUDA;
-  return MOE_OK;
+  return forward_host(x_host, logits_host, bias, w13, s13, w2, s2, T, H, I, E, n_shared,
+                      num_groups, topk_group, top_k, scoring, renormalize,
+                      routed_scaling_factor, out_host, ws, ws_bytes, stream, false);
 }
 
 moe_status moe_forward_host(const void* x_host, const float* logits_host, const float* bias,
@@ -373,9 +419,72 @@ moe_status moe_forward_host(const void* x_host, const float* logits_host, const 
                             int top_k, int scoring, int renormalize,
                             float routed_scaling_factor, void* out_host, void* ws,
                             size_t ws_bytes, void* stream) {
-  return moe_forward_shared_host(x_host, logits_host, bias, w13, s13, w2, s2, T, H, I, E, 0,
-                                 num_groups, topk_group, top_k, scoring, renormalize,
-                                 routed_scaling_factor, out_host, ws, ws_bytes, stream);
+  return forward_host(x_host, logits_host, bias, w13, s13, w2, s2, T, H, I, E, 0, num_groups,
+                      topk_group, top_k, scoring, renormalize, routed_scaling_factor, out_host,
+                      ws, ws_bytes, stream, false);
+}
+
+// ---- block-quantised FP8 -------------------------------------------------------
+moe_status moe_permute_quant_block(const void* x, const int32_t* topk_ids, int T, int H, int E,
+                                   int K, void* a_q, float* scale_a, int32_t* src2dst,
+                                   int32_t* offsets, void* ws, size_t ws_bytes, void* stream) {
+  moe_status s = check_permute(x, topk_ids, T, H, E, K, a_q, scale_a, src2dst, offsets, ws,
+                               ws_bytes);
+  if (s != MOE_OK) return s;
+  if (H % 128 != 0) return MOE_ERR_INVALID_ARG;
+  int* err = device_error_word();
+  if (err == nullptr) return MOE_ERR_CUDA;
+  return cuda_status(launch_permute_quant_block(x, topk_ids, T, H, E, K, a_q, scale_a, src2dst,
+                                                offsets, ws, err,
+                                                static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_grouped_gemm_block(const void* A, const float* scale_a, const void* B,
+                                  const float* scale_b, const int32_t* offsets, int M, int N,
+                                  int Kd, int E, int epilogue, void* C, void* stream) {
+  moe_status s = check_gemm(A, scale_a, B, scale_b, offsets, M, N, Kd, E, epilogue, C, nullptr);
+  if (s != MOE_OK) return s;
+  if (Kd % 128 != 0 || N % (epilogue == MOE_EPI_SILU_MUL ? 256 : 128) != 0)
+    return MOE_ERR_INVALID_ARG;
+  int* err = device_error_word();
+  if (err == nullptr) return MOE_ERR_CUDA;
+  return cuda_status(launch_grouped_gemm_block(A, scale_a, B, scale_b, offsets, M, N, Kd, E,
+                                               epilogue, C, err,
+                                               static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_act_quant_block(const void* h, int M, int I, void* q, float* scale,
+                               void* stream) {
+  if (M < 0 || I < 1 || I % 128 != 0) return MOE_ERR_INVALID_ARG;
+  if (M > 0 && (!ok_ptr(h) || !ok_ptr(q) || !ok_ptr(scale))) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_act_quant_block(h, M, I, q, scale, static_cast<cudaStream_t>(stream)));
+}
+
+size_t moe_block_workspace_size(int T, int H, int I, int E, int K) {
+  if (T < 0 || H < 128 || I < 128 || E < 1 || K < 1 || H % 128 != 0 || I % 128 != 0) return 0;
+  return fwd_layout(T, H, I, E, K, true).total;
+}
+
+moe_status moe_forward_block(const void* x, const float* logits, const float* bias,
+                             const void* w13, const float* s13, const void* w2, const float* s2,
+                             int T, int H, int I, int E, int n_shared, int num_groups,
+                             int topk_group, int top_k, int scoring, int renormalize,
+                             float routed_scaling_factor, void* out, void* ws, size_t ws_bytes,
+                             void* stream) {
+  return forward_device(x, logits, bias, w13, s13, w2, s2, T, H, I, E, n_shared, num_groups,
+                        topk_group, top_k, scoring, renormalize, routed_scaling_factor, out, ws,
+                        ws_bytes, stream, true);
+}
+
+moe_status moe_forward_block_host(const void* x_host, const float* logits_host,
+                                  const float* bias, const void* w13, const float* s13,
+                                  const void* w2, const float* s2, int T, int H, int I, int E,
+                                  int n_shared, int num_groups, int topk_group, int top_k,
+                                  int scoring, int renormalize, float routed_scaling_factor,
+                                  void* out_host, void* ws, size_t ws_bytes, void* stream) {
+  return forward_host(x_host, logits_host, bias, w13, s13, w2, s2, T, H, I, E, n_shared,
+                      num_groups, topk_group, top_k, scoring, renormalize,
+                      routed_scaling_factor, out_host, ws, ws_bytes, stream, true);
 }
 
 moe_status moe_device_status(int* code) {

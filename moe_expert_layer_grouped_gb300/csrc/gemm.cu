@@ -46,20 +46,17 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "gemm_common.cuh"
 #include "ptx.cuh"
 
 namespace moe {
 namespace {
 
-constexpr int BM = 128;   // weight rows per tile (MMA M)
-constexpr int BK = 128;   // K bytes (= e4m3 elements) per pipeline stage
-constexpr int W_BYTES = BM * BK;
+using namespace gemm_common;
+
 constexpr int THREADS = 192;
 constexpr uint32_t ACC_COLS = 256;  // TMEM columns per accumulator
 constexpr uint32_t TMEM_COLS = 2 * ACC_COLS;
-constexpr int MAX_E = 1024;
-constexpr uint64_t WAIT_NS = 2000000000ull;
-constexpr uint64_t DRAIN_NS = 200000000ull;
 #ifndef PAIR_KC
 #define PAIR_KC 2
 #define PAIR_STAGES 3
@@ -85,14 +82,6 @@ struct Smem {
   int offs[MAX_E + 1];
 };
 
-// Token boxes of 64/32/16 rows: a tile's tokens (rounded up to 16) are
-// covered exactly by 64-row boxes plus at most one 32- and one 16-row box
-// (64-row boxes measured fastest; weights also move in 64-row boxes).
-constexpr int NXBOX = 3;
-struct Maps {
-  CUtensorMap w;           // weights: 64-row boxes
-  CUtensorMap x[NXBOX];    // tokens: box rows 64 >> i
-};
 
 struct Params {
   const float* scale_a;
@@ -104,54 +93,6 @@ struct Params {
   int M, N, Kd, E, I, NB, KB;
   int stream_weights;  // 1: each weight block is read by one tile (evict-first)
 };
-
-template <int BNMAX>
-struct TileInfo {
-  int e, nb, tok0, ntok;
-};
-
-// tile -> (expert, weight block, token chunk)
-template <int BNMAX, class S>
-__device__ __forceinline__ TileInfo<BNMAX> decode_tile(const S& sm, int E, int NB, int tile) {
-  int lo = 0, hi = E - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (sm.tile_start[mid] <= tile) lo = mid;
-    else hi = mid - 1;
-  }
-  TileInfo<BNMAX> t;
-  t.e = lo;
-  const int local = tile - sm.tile_start[lo];
-  const int nch = (sm.tile_start[lo + 1] - sm.tile_start[lo]) / NB;
-  t.nb = local / nch;
-  const int tc = local - t.nb * nch;
-  // equal chunks (multiples of 16 tokens) so the tiles that share a weight
-  // block run at the same speed and meet it in L2
-  const int cnt = sm.offs[lo + 1] - sm.offs[lo];
-  const int csz = ((cnt + nch - 1) / nch + 15) & ~15;
-  t.tok0 = sm.offs[lo] + tc * csz;
-  t.ntok = min(csz, cnt - tc * csz);
-  return t;
-}
-
-__device__ __forceinline__ void bar_sync_named(int id, int count) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-
-// Named barrier that also returns whether any participating thread passed a
-// non-zero `pred`.
-__device__ __forceinline__ int bar_red_or(int id, int count, int pred) {
-  int r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.s32 p, %1, 0;\n\t"
-      "bar.red.or.pred q, %2, %3, p;\n\t"
-      "selp.s32 %0, 1, 0, q;\n\t}"
-      : "=r"(r)
-      : "r"(pred), "r"(id), "r"(count)
-      : "memory");
-  return r;
-}
 
 // CS = 1: one CTA per tile of 128 weight rows x N tokens.
 // CS = 2: a CTA pair (cluster of 2) computes 256 weight rows x N tokens with
@@ -208,44 +149,12 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (PAIR) ptx::cluster_sync();  // the peer's barriers exist before any signal
 
   // ---- tile table from the expert offsets --------------------------------
-  for (int i = tid; i <= E; i += THREADS) sm.offs[i] = __ldg(p.offsets + i);
-  __syncthreads();
-  const int per = (E + THREADS - 1) / THREADS;
-  const int e0 = min(E, tid * per), e1 = min(E, e0 + per);
-  int local = 0;
-  int bad = 0;
-  for (int e = e0; e < e1; ++e) {
-    const int lo = sm.offs[e], hi = sm.offs[e + 1];
-    if (lo < 0 || hi < lo || hi > p.M) bad = 1;
-    else local += (hi - lo + BNMAX - 1) / BNMAX;
-  }
-  sm.thr_sum[tid] = local;
-  bad = __syncthreads_or(bad);
-  if (tid == 0) {
-    int run = 0;
-    for (int i = 0; i < THREADS; ++i) {
-      const int v = sm.thr_sum[i];
-      sm.thr_sum[i] = run;
-      run += v;
-    }
-    sm.total_tiles = bad ? 0 : run * NBG;
-    sm.tile_start[E] = run * NBG;
-    if (bad) flag_error(p.err, MOE_DEV_BAD_OFFSETS);
-  }
-  __syncthreads();
-  {
-    int run = sm.thr_sum[tid];
-    for (int e = e0; e < e1; ++e) {
-      sm.tile_start[e] = run * NBG;
-      const int lo = sm.offs[e], hi = sm.offs[e + 1];
-      if (!bad) run += (hi - lo + BNMAX - 1) / BNMAX;
-    }
-  }
+  build_tile_table<BNMAX, THREADS>(sm, p.offsets, E, p.M, NBG, p.err, tid);
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
-  const int total = sm.total_tiles;
+  const int total = sm.total_tiles;  // after the barrier above
 
   if (warp == 0) {
     // ======================= TMA producer ===================================
@@ -555,68 +464,6 @@ __global__ void __launch_bounds__(THREADS, 1)
 }
 
 // ---- host side ---------------------------------------------------------------
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
-                                         cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(ptr);
-  });
-  return fn;
-}
-
-// 2-D u8 tensor [rows, cols] (cols contiguous), box 128 B x box_rows,
-// 128-byte swizzle, zero fill outside the tensor. Encoded maps are cached by
-// (address, shape, box) so repeated calls on the same buffers skip the
-// driver-side encoding.
-bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
-              uint32_t box_rows) {
-  struct Entry {
-    const void* base;
-    uint64_t rows, cols;
-    uint32_t box;
-    int dev;
-    CUtensorMap map;
-  };
-  static std::mutex mu;
-  static Entry cache[64];
-  static int next = 0;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  {
-    std::lock_guard<std::mutex> lk(mu);
-    for (const Entry& c : cache)
-      if (c.base == base && c.rows == rows && c.cols == cols && c.box == box_rows &&
-          c.dev == dev) {
-        *m = c.map;
-        return true;
-      }
-  }
-  EncodeTiledFn fn = encode_fn();
-  if (fn == nullptr) return false;
-  const cuuint64_t dims[2] = {cols, rows};
-  const cuuint64_t strides[1] = {cols};
-  const cuuint32_t box[2] = {BK, box_rows};
-  const cuuint32_t es[2] = {1, 1};
-  if (fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
-         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-    return false;
-  std::lock_guard<std::mutex> lk(mu);
-  cache[next] = Entry{base, rows, cols, box_rows, dev, *m};
-  next = (next + 1) % 64;
-  return true;
-}
-
 template <int BNMAX, int STAGES, bool SILU, int CS, int KC>
 cudaError_t launch_cfg(const Maps& maps, const Params& p, int M, int E, cudaStream_t st) {
   constexpr size_t smem = sizeof(Smem<BNMAX / CS, STAGES, SILU, KC>) + 1024;
@@ -662,6 +509,73 @@ cudaError_t launch_cfg(const Maps& maps, const Params& p, int M, int E, cudaStre
 
 }  // namespace
 
+namespace gemm_common {
+
+namespace {
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+}  // namespace
+
+// Encoded maps are cached by (address, shape, box) so repeated calls on the
+// same buffers skip the driver-side encoding.
+bool make_tma_map_u8(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
+                     uint32_t box_rows) {
+  struct Entry {
+    const void* base;
+    uint64_t rows, cols;
+    uint32_t box;
+    int dev;
+    CUtensorMap map;
+  };
+  static std::mutex mu;
+  static Entry cache[64];
+  static int next = 0;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    for (const Entry& c : cache)
+      if (c.base == base && c.rows == rows && c.cols == cols && c.box == box_rows &&
+          c.dev == dev) {
+        *m = c.map;
+        return true;
+      }
+  }
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols};
+  const cuuint32_t box[2] = {BK, box_rows};
+  const cuuint32_t es[2] = {1, 1};
+  if (fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  std::lock_guard<std::mutex> lk(mu);
+  cache[next] = Entry{base, rows, cols, box_rows, dev, *m};
+  next = (next + 1) % 64;
+  return true;
+}
+
+}  // namespace gemm_common
+
 cudaError_t launch_grouped_gemm(const void* A, const float* scale_a, const void* B,
                                 const float* scale_b, const int32_t* offsets, int M, int N,
                                 int Kd, int E, int epilogue, void* C, float* row_amax, int* err,
@@ -670,10 +584,10 @@ cudaError_t launch_grouped_gemm(const void* A, const float* scale_a, const void*
   const bool silu = (epilogue == MOE_EPI_SILU_MUL);
   const bool small = (int64_t)M <= (int64_t)32 * E;  // few rows per expert (decode)
   Maps maps;
-  if (!make_map(&maps.w, B, (uint64_t)E * (uint64_t)N, (uint64_t)Kd, 64))
+  if (!make_tma_map_u8(&maps.w, B, (uint64_t)E * (uint64_t)N, (uint64_t)Kd, 64))
     return cudaErrorNotSupported;
   for (int i = 0; i < NXBOX; ++i)
-    if (!make_map(&maps.x[i], A, (uint64_t)M, (uint64_t)Kd, 64u >> i))
+    if (!make_tma_map_u8(&maps.x[i], A, (uint64_t)M, (uint64_t)Kd, 64u >> i))
       return cudaErrorNotSupported;
   Params p;
   p.scale_a = scale_a;

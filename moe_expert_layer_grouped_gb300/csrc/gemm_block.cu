@@ -1,0 +1,446 @@
+// moe_grouped_gemm_block: the grouped FP8 GEMM with block scales — one fp32
+// scale per 128 x 128 weight block and one per token per 128 input channels
+// (the group_k / group_n path that "Fix one bug in the grouped-gemm triton
+// kernel", sglang #6772, Highlights, contrasts with the per-token one):
+//   C[r,n] = sum_kb (sum_{k in kb} A[r,k] W[e,n,k]) * sa[r,kb] * sb[e,n/128,kb]
+//
+// The scales change every 128 channels of K, so the tensor cores cannot keep
+// one accumulator across K. A K block is exactly one pipeline stage: the MMA
+// thread writes each block's partial sum afresh into one of two TMEM buffers,
+// and the epilogue warps fold it into fp32 registers with its factor
+// sa[token,kb] * sb[kb] while the MMA fills the other buffer.
+//
+// Orientation and tiles as in moe_grouped_gemm: weights on the MMA's M side
+// (128 rows per tile, which is one weight scale block), tokens on N (at most
+// BNMAX per tile, 16-token granularity). One persistent CTA per SM, 320
+// threads:
+//   warp 0      TMA producer (one K block of weights and tokens per stage)
+//   warp 1      MMA issuer (tcgen05.mma.cta_group::1.kind::f8f6f4, K=32 x 4)
+//   warps 2..9  epilogue: warp w reads TMEM lane quadrant w % 4 and one half
+//               of the tile's token columns; per K block the 256 epilogue
+//               threads first stage the per-token factors of both weight
+//               scales in shared memory (one token each), then accumulate.
+// SiLU*mul and the bf16 stores work as in moe_grouped_gemm (gate rows in TMEM
+// lanes 0..63, up rows in 64..127, exchanged through shared memory).
+// Every wait is bounded; the epilogue warps take abort decisions together
+// through bar.red so no warp is left at a named barrier.
+#include <cuda.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "common.cuh"
+#include "gemm_common.cuh"
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace moe {
+namespace {
+
+using namespace gemm_common;
+
+constexpr int EPI_WARPS = 8;
+constexpr int BTHREADS = 64 + 32 * EPI_WARPS;
+constexpr int EPI_THREADS = 32 * EPI_WARPS;
+constexpr int BAR_KB = 1;    // named barrier of the 256 epilogue threads
+constexpr int BAR_PAIR = 2;  // 2..5: the SiLU exchange pairs
+
+template <int BNMAX, int STAGES, bool SILU>
+struct BSmem {
+  uint8_t w[STAGES][W_BYTES];          // weights, one K block per stage
+  uint8_t x[STAGES][BNMAX * BK];       // tokens
+  float fs[2][2][BNMAX];               // per partial buffer: sa*sb per token (main/gate, up)
+  float xchg[SILU ? 4 : 1][32 * 32];   // SiLU: one slot per exchange pair
+  uint16_t stage_out[EPI_WARPS][32 * 32];
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
+  uint64_t pfull[2];   // a K block's partial sum is in TMEM buffer b
+  uint64_t pempty[2];  // the epilogue has read buffer b
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+  int total_tiles;
+  int never;
+  int thr_sum[BTHREADS];
+  int tile_start[MAX_E + 1];
+  int offs[MAX_E + 1];
+};
+
+struct BParams {
+  const float* scale_a;  // [M, KB]
+  const float* scale_b;  // [E, N/128, KB]
+  const int32_t* offsets;
+  void* C;
+  int* err;
+  int M, N, Kd, E, I, NB, KB;
+  int stream_weights;
+};
+
+template <int BNMAX, int STAGES, bool SILU>
+__global__ void __launch_bounds__(BTHREADS, 1)
+    grouped_gemm_block_kernel(const __grid_constant__ Maps maps, const BParams p) {
+  using S = BSmem<BNMAX, STAGES, SILU>;
+  constexpr uint32_t TCOLS = 2 * BNMAX;  // two partial buffers
+  constexpr int HC = BNMAX / 2;          // token columns per epilogue warp
+  constexpr int NCH = HC / 32;           // 32-column chunks per epilogue warp
+  static_assert(NCH >= 1 && BNMAX <= EPI_THREADS, "tile shape");
+  extern __shared__ uint8_t smem_raw[];
+  S& sm = *reinterpret_cast<S*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                ~static_cast<uintptr_t>(1023));
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int E = p.E;
+  const int KB = p.KB;
+
+  if (warp == 0 && lane == 0) {
+    ptx::prefetch_tensormap(&maps.w);
+    for (int i = 0; i < NXBOX; ++i) ptx::prefetch_tensormap(&maps.x[i]);
+    for (int s = 0; s < STAGES; ++s) {
+      ptx::mbar_init(&sm.full[s], 1);
+      ptx::mbar_init(&sm.empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(&sm.pfull[b], 1);
+      ptx::mbar_init(&sm.pempty[b], EPI_WARPS);
+    }
+    ptx::mbar_init(&sm.drain, 1);
+    sm.abort = 0;
+    sm.never = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(&sm.tmem_base, TCOLS);
+    ptx::tmem_relinquish();
+  }
+  build_tile_table<BNMAX, BTHREADS>(sm, p.offsets, E, p.M, p.NB, p.err, tid);
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+  const int total = sm.total_tiles;
+  const int ncta = gridDim.x;
+
+  if (warp == 0) {
+    // ======================= TMA producer ===================================
+    if (lane == 0) {
+      const uint64_t pol_w =
+          p.stream_weights ? ptx::policy_evict_first() : ptx::policy_evict_normal();
+      const uint64_t pol_x = ptx::policy_evict_last();
+      uint32_t s = 0, ph = 0, armed = 0, armed_par = 0;
+      bool ok = true;
+      for (int g = blockIdx.x; ok && g < total; g += ncta) {
+        const TileInfo<BNMAX> t = decode_tile<BNMAX>(sm, E, p.NB, g);
+        const int rows = (t.ntok + 15) & ~15;
+        const uint32_t bytes = W_BYTES + (uint32_t)rows * BK;
+        int y0, y1;  // first rows of the two 64-row weight boxes
+        if (SILU) {  // gate rows [j0, j0+64) and up rows [I+j0, I+j0+64)
+          y0 = t.e * p.N + t.nb * 64;
+          y1 = y0 + p.I;
+        } else {
+          y0 = t.e * p.N + t.nb * BM;
+          y1 = y0 + 64;
+        }
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!ptx::mbar_wait(&sm.empty[s], ph ^ 1u, &sm.abort, WAIT_NS)) {
+            ok = false;
+            break;
+          }
+          ptx::mbar_arrive_expect_tx(&sm.full[s], bytes);
+          armed |= 1u << s;
+          armed_par = (armed_par & ~(1u << s)) | (ph << s);
+          const int kx = kb * BK;
+          ptx::tma_load_2d(sm.w[s], &maps.w, &sm.full[s], kx, y0, pol_w);
+          ptx::tma_load_2d(sm.w[s] + 64 * BK, &maps.w, &sm.full[s], kx, y1, pol_w);
+          int r = 0;
+#pragma unroll
+          for (int i = 0; i < NXBOX; ++i) {
+            const int box = 64 >> i;
+            while (rows - r >= box) {
+              ptx::tma_load_2d(sm.x[s] + r * BK, &maps.x[i], &sm.full[s], kx, t.tok0 + r, pol_x);
+              r += box;
+            }
+          }
+          if (++s == STAGES) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        sm.abort = 1;
+        flag_error(p.err, MOE_DEV_PIPE_TIMEOUT);
+        for (int i = 0; i < STAGES; ++i)
+          if ((armed >> i) & 1u)
+            ptx::mbar_wait(&sm.full[i], (armed_par >> i) & 1u, &sm.never, DRAIN_NS);
+      }
+    }
+  } else if (warp == 1) {
+    // ======================= MMA issuer =====================================
+    if (lane == 0) {
+      uint32_t s = 0, ph = 0;
+      uint32_t kbg = 0;  // K blocks issued so far (selects the partial buffer)
+      bool ok = true, issued = false;
+      for (int g = blockIdx.x; ok && g < total; g += ncta) {
+        const TileInfo<BNMAX> t = decode_tile<BNMAX>(sm, E, p.NB, g);
+        const uint32_t idesc = ptx::idesc_e4m3_f32(BM, (t.ntok + 15) & ~15);
+        for (int kb = 0; kb < KB; ++kb, ++kbg) {
+          const uint32_t b = kbg & 1u;
+          if (!ptx::mbar_wait(&sm.pempty[b], ((kbg >> 1) & 1u) ^ 1u, &sm.abort, WAIT_NS) ||
+              !ptx::mbar_wait(&sm.full[s], ph, &sm.abort, WAIT_NS)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t d = tmem + b * BNMAX;
+          const uint32_t a0 = ptx::smem_u32(sm.w[s]);
+          const uint32_t b0 = ptx::smem_u32(sm.x[s]);
+#pragma unroll
+          for (int kk = 0; kk < BK / 32; ++kk)
+            ptx::mma_e4m3(d, ptx::sdesc_sw128(a0 + kk * 32), ptx::sdesc_sw128(b0 + kk * 32),
+                          idesc, kk != 0 ? 1u : 0u);
+          issued = true;
+          ptx::mma_commit(&sm.empty[s]);
+          ptx::mma_commit(&sm.pfull[b]);
+          if (++s == STAGES) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        sm.abort = 1;
+        flag_error(p.err, MOE_DEV_PIPE_TIMEOUT);
+        if (issued) {
+          ptx::mma_commit(&sm.drain);
+          ptx::mbar_wait(&sm.drain, 0, &sm.never, DRAIN_NS);
+        }
+      }
+    }
+  } else {
+    // ======================= epilogue (warps 2..9) ==========================
+    const int q = warp & 3;              // TMEM lane quadrant this warp may access
+    const int hsel = (warp - 2) >> 2;    // which half of the token columns
+    const int et = tid - 64;             // epilogue thread: stages token et's factors
+    const int NBk = p.N / 128;           // weight scale blocks along N
+    const bool up_rows = SILU && q >= 2;
+    uint32_t kbg = 0;
+    int bad = 0;
+    bool stop = false;
+    for (int g = blockIdx.x; !stop && g < total; g += ncta) {
+      const TileInfo<BNMAX> t = decode_tile<BNMAX>(sm, E, p.NB, g);
+      const int n_mma = (t.ntok + 15) & ~15;
+      // the tile's weight scale rows: one 128-row block (bf16 out), or the
+      // gate and the up block (SiLU)
+      const int blk0 = SILU ? (t.nb * 64) / 128 : t.nb;
+      const int blk1 = SILU ? (p.I + t.nb * 64) / 128 : t.nb;
+      const float* sb0 = p.scale_b + ((int64_t)t.e * NBk + blk0) * KB;
+      const float* sb1 = p.scale_b + ((int64_t)t.e * NBk + blk1) * KB;
+      const bool tv = et < t.ntok;
+      const float* sa_row = p.scale_a + (int64_t)(t.tok0 + (tv ? et : 0)) * KB;
+      float sa_n = tv ? __ldg(sa_row) : 0.0f;
+      float acc[HC];
+#pragma unroll
+      for (int i = 0; i < HC; ++i) acc[i] = 0.0f;
+      for (int kb = 0; kb < KB; ++kb, ++kbg) {
+        const uint32_t b = kbg & 1u;
+        if (et < BNMAX) {
+          sm.fs[b][0][et] = sa_n * __ldg(sb0 + kb);
+          if (SILU) sm.fs[b][1][et] = sa_n * __ldg(sb1 + kb);
+        }
+        sa_n = (tv && kb + 1 < KB) ? __ldg(sa_row + kb + 1) : 0.0f;
+        // the factors are staged; a failure anywhere stops every epilogue warp
+        if (bar_red_or(BAR_KB, EPI_THREADS, bad)) {
+          stop = true;
+          break;
+        }
+        bool ok = ptx::mbar_wait(&sm.pfull[b], (kbg >> 1) & 1u, &sm.abort, WAIT_NS);
+        ok = __all_sync(kFull, ok);
+        if (!ok) {
+          bad = 1;
+          continue;
+        }
+        ptx::tc_fence_after();
+        const float* f = sm.fs[b][up_rows ? 1 : 0] + hsel * HC;
+        const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + b * BNMAX + hsel * HC;
+#pragma unroll
+        for (int c = 0; c < NCH; ++c) {
+          if (hsel * HC + c * 32 < n_mma) {  // warp-uniform
+            uint32_t v[32];
+            ptx::tmem_ld_32x32b_x32(tb + c * 32, v);
+            ptx::tmem_ld_wait();
+            ptx::reg_fence(v);
+#pragma unroll
+            for (int i = 0; i < 32; i += 4) {
+              const float4 fv = *reinterpret_cast<const float4*>(f + c * 32 + i);
+              acc[c * 32 + i + 0] = fmaf(__uint_as_float(v[i + 0]), fv.x, acc[c * 32 + i + 0]);
+              acc[c * 32 + i + 1] = fmaf(__uint_as_float(v[i + 1]), fv.y, acc[c * 32 + i + 1]);
+              acc[c * 32 + i + 2] = fmaf(__uint_as_float(v[i + 2]), fv.z, acc[c * 32 + i + 2]);
+              acc[c * 32 + i + 3] = fmaf(__uint_as_float(v[i + 3]), fv.w, acc[c * 32 + i + 3]);
+            }
+          }
+        }
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&sm.pempty[b]);
+      }
+      if (stop || bar_red_or(BAR_KB, EPI_THREADS, bad)) {
+        stop = true;
+        break;
+      }
+      // ---- the tile's output: every K block is in acc ----
+      uint16_t* ost = sm.stage_out[warp - 2];
+      if (SILU) {
+        const int I = p.I;
+        const int pair = (q & 1) + 2 * hsel;
+        const bool holds_gate = q < 2;
+        const int mine0 = holds_gate ? 0 : 16;  // gate: tokens 0..15 of a chunk, up: 16..31
+        float* xs = sm.xchg[pair];
+        const int jrow = t.nb * 64 + (q & 1) * 32;  // first j of this warp's 32
+        __nv_bfloat16* hbase = reinterpret_cast<__nv_bfloat16*>(p.C);
+#pragma unroll
+        for (int c = 0; c < NCH; ++c) {
+          const int col0 = hsel * HC + c * 32;  // first token column of the chunk
+          if (col0 >= t.ntok) break;            // the same for both warps of the pair
+          // hand the partner the half it computes: the gate holder gives
+          // tokens 16..31 (slots 0..15), the up holder tokens 0..15 (16..31)
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            xs[(holds_gate ? i : 16 + i) * 32 + lane] =
+                holds_gate ? acc[c * 32 + 16 + i] : acc[c * 32 + i];
+          bar_sync_named(BAR_PAIR + pair, 64);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float own = holds_gate ? acc[c * 32 + i] : acc[c * 32 + 16 + i];
+            const float other = xs[(holds_gate ? 16 + i : i) * 32 + lane];
+            const float gv = holds_gate ? own : other;
+            const float uv = holds_gate ? other : own;
+            const __nv_bfloat16 hb =
+                __float2bfloat16_rn(__fdividef(gv, 1.0f + __expf(-gv)) * uv);
+            ost[i * 32 + lane] = __bfloat16_as_ushort(hb);
+          }
+          __syncwarp();
+          // 16 tokens x 32 j: four lanes per token row, 16 bytes each
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            const int r = k * 8 + (lane >> 2);
+            const int tk = col0 + mine0 + r;
+            if (tk < t.ntok)
+              *reinterpret_cast<uint4*>(hbase + (int64_t)(t.tok0 + tk) * I + jrow +
+                                        (lane & 3) * 8) =
+                  *reinterpret_cast<const uint4*>(ost + r * 32 + (lane & 3) * 8);
+          }
+          __syncwarp();
+          bar_sync_named(BAR_PAIR + pair, 64);  // the slot is free again
+        }
+      } else {
+        const int N = p.N;
+        const int ncol0 = t.nb * BM + q * 32;  // first output column of this warp's 32
+        __nv_bfloat16* cbase = reinterpret_cast<__nv_bfloat16*>(p.C);
+#pragma unroll
+        for (int c = 0; c < NCH; ++c) {
+          const int col0 = hsel * HC + c * 32;
+          if (col0 >= t.ntok) break;
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            ost[i * 32 + lane] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[c * 32 + i]));
+          __syncwarp();
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int r = k * 8 + (lane >> 2);
+            if (col0 + r < t.ntok)
+              *reinterpret_cast<uint4*>(cbase + (int64_t)(t.tok0 + col0 + r) * N + ncol0 +
+                                        (lane & 3) * 8) =
+                  *reinterpret_cast<const uint4*>(ost + r * 32 + (lane & 3) * 8);
+          }
+          __syncwarp();
+        }
+      }
+    }
+    if (stop) {
+      sm.abort = 1;
+      flag_error(p.err, MOE_DEV_PIPE_TIMEOUT);
+    }
+  }
+
+  // ---- teardown -------------------------------------------------------------
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, TCOLS);
+  }
+}
+
+// The deepest ring that fits next to the rest of the shared memory (at most 8).
+template <int BNMAX, bool SILU>
+constexpr int block_stages() {
+  constexpr size_t fixed = sizeof(BSmem<BNMAX, 1, SILU>) - (W_BYTES + BNMAX * BK) + 1024;
+  constexpr size_t per = W_BYTES + BNMAX * BK + 16;
+  constexpr size_t n = (227 * 1024 - fixed) / per;
+  return n > 8 ? 8 : (int)n;
+}
+
+template <int BNMAX, bool SILU>
+cudaError_t launch_block_cfg(const Maps& maps, const BParams& p, int M, int E, cudaStream_t st) {
+  constexpr int STAGES = block_stages<BNMAX, SILU>();
+  static_assert(STAGES >= 3, "pipeline depth");
+  constexpr size_t smem = sizeof(BSmem<BNMAX, STAGES, SILU>) + 1024;
+  static_assert(smem <= 227 * 1024, "shared memory budget");
+  auto kern = grouped_gemm_block_kernel<BNMAX, STAGES, SILU>;
+  static std::mutex mu;
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    if (dev >= 64 || !attr_set[dev]) {
+      cudaError_t e =
+          cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+      if (dev < 64) attr_set[dev] = true;
+    }
+  }
+  const long long upper = ((long long)(M + BNMAX - 1) / BNMAX + E) * p.NB;
+  const int grid = (int)std::max<long long>(1, std::min<long long>(sm_count(), upper));
+  kern<<<grid, BTHREADS, smem, st>>>(maps, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_grouped_gemm_block(const void* A, const float* scale_a, const void* B,
+                                      const float* scale_b, const int32_t* offsets, int M, int N,
+                                      int Kd, int E, int epilogue, void* C, int* err,
+                                      cudaStream_t st) {
+  if (M == 0) return cudaSuccess;
+  const bool silu = (epilogue == MOE_EPI_SILU_MUL);
+  const bool small = (int64_t)M <= (int64_t)32 * E;  // few rows per expert (decode)
+  Maps maps;
+  if (!make_tma_map_u8(&maps.w, B, (uint64_t)E * (uint64_t)N, (uint64_t)Kd, 64))
+    return cudaErrorNotSupported;
+  for (int i = 0; i < NXBOX; ++i)
+    if (!make_tma_map_u8(&maps.x[i], A, (uint64_t)M, (uint64_t)Kd, 64u >> i))
+      return cudaErrorNotSupported;
+  BParams p;
+  p.scale_a = scale_a;
+  p.scale_b = scale_b;
+  p.offsets = offsets;
+  p.C = C;
+  p.err = err;
+  p.M = M;
+  p.N = N;
+  p.Kd = Kd;
+  p.E = E;
+  p.I = N / 2;
+  p.NB = silu ? p.I / 64 : N / BM;
+  p.KB = Kd / BK;
+  p.stream_weights = small ? 1 : 0;
+  if (small)
+    return silu ? launch_block_cfg<64, true>(maps, p, M, E, st)
+                : launch_block_cfg<64, false>(maps, p, M, E, st);
+  return silu ? launch_block_cfg<128, true>(maps, p, M, E, st)
+              : launch_block_cfg<128, false>(maps, p, M, E, st);
+}
+
+}  // namespace moe

@@ -1,0 +1,134 @@
+// Pieces shared by the grouped GEMM kernels (per-token scales in gemm.cu,
+// 128 x 128 block scales in gemm_block.cu): tile geometry, the tile table
+// built on the device from the expert offsets, named-barrier helpers and the
+// TMA descriptor cache.
+//
+// A tile is (expert, weight block, token chunk): 128 weight rows (the MMA's
+// M side) against up to BNMAX of the expert's tokens (its N side). An
+// expert's tokens are split into equal chunks, multiples of 16, and the tile
+// index runs token chunk fastest so the chunks that read one weight block
+// run side by side and share it through L2.
+#pragma once
+
+#include <cuda.h>
+#include <stdint.h>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace moe {
+namespace gemm_common {
+
+constexpr int BM = 128;   // weight rows per tile (MMA M)
+constexpr int BK = 128;   // K bytes (= e4m3 elements) per K chunk
+constexpr int W_BYTES = BM * BK;
+constexpr int MAX_E = 1024;
+constexpr uint64_t WAIT_NS = 2000000000ull;   // bound of every pipeline wait
+constexpr uint64_t DRAIN_NS = 200000000ull;   // bound of the waits after a timeout
+
+// Token boxes of 64/32/16 rows: a tile's tokens (rounded up to 16) are
+// covered exactly by 64-row boxes plus at most one 32- and one 16-row box
+// (64-row boxes measured fastest; weights also move in 64-row boxes).
+constexpr int NXBOX = 3;
+struct Maps {
+  CUtensorMap w;           // weights: 64-row boxes
+  CUtensorMap x[NXBOX];    // tokens: box rows 64 >> i
+};
+
+template <int BNMAX>
+struct TileInfo {
+  int e, nb, tok0, ntok;
+};
+
+// tile -> (expert, weight block, token chunk)
+template <int BNMAX, class S>
+__device__ __forceinline__ TileInfo<BNMAX> decode_tile(const S& sm, int E, int NB, int tile) {
+  int lo = 0, hi = E - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (sm.tile_start[mid] <= tile) lo = mid;
+    else hi = mid - 1;
+  }
+  TileInfo<BNMAX> t;
+  t.e = lo;
+  const int local = tile - sm.tile_start[lo];
+  const int nch = (sm.tile_start[lo + 1] - sm.tile_start[lo]) / NB;
+  t.nb = local / nch;
+  const int tc = local - t.nb * nch;
+  // equal chunks (multiples of 16 tokens) so the tiles that share a weight
+  // block run at the same speed and meet it in L2
+  const int cnt = sm.offs[lo + 1] - sm.offs[lo];
+  const int csz = ((cnt + nch - 1) / nch + 15) & ~15;
+  t.tok0 = sm.offs[lo] + tc * csz;
+  t.ntok = min(csz, cnt - tc * csz);
+  return t;
+}
+
+__device__ __forceinline__ void bar_sync_named(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// Named barrier that also returns whether any participating thread passed a
+// non-zero `pred`.
+__device__ __forceinline__ int bar_red_or(int id, int count, int pred) {
+  int r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.s32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, %3, p;\n\t"
+      "selp.s32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(pred), "r"(id), "r"(count)
+      : "memory");
+  return r;
+}
+
+
+// Builds sm.offs[0..E], sm.tile_start[0..E] and sm.total_tiles (0 when the
+// offsets are not monotone within [0, M], with MOE_DEV_BAD_OFFSETS raised)
+// for NBG weight-block groups per expert and token chunks of at most BNMAX.
+// Called by all THREADS threads; the caller synchronises before reading.
+template <int BNMAX, int THREADS, class S>
+__device__ __forceinline__ void build_tile_table(S& sm, const int32_t* offsets, int E, int M,
+                                                 int NBG, int* err, int tid) {
+  for (int i = tid; i <= E; i += THREADS) sm.offs[i] = __ldg(offsets + i);
+  __syncthreads();
+  const int per = (E + THREADS - 1) / THREADS;
+  const int e0 = min(E, tid * per), e1 = min(E, e0 + per);
+  int local = 0;
+  int bad = 0;
+  for (int e = e0; e < e1; ++e) {
+    const int lo = sm.offs[e], hi = sm.offs[e + 1];
+    if (lo < 0 || hi < lo || hi > M) bad = 1;
+    else local += (hi - lo + BNMAX - 1) / BNMAX;
+  }
+  sm.thr_sum[tid] = local;
+  bad = __syncthreads_or(bad);
+  if (tid == 0) {
+    int run = 0;
+    for (int i = 0; i < THREADS; ++i) {
+      const int v = sm.thr_sum[i];
+      sm.thr_sum[i] = run;
+      run += v;
+    }
+    sm.total_tiles = bad ? 0 : run * NBG;
+    sm.tile_start[E] = run * NBG;
+    if (bad) flag_error(err, MOE_DEV_BAD_OFFSETS);
+  }
+  __syncthreads();
+  int run = sm.thr_sum[tid];
+  for (int e = e0; e < e1; ++e) {
+    sm.tile_start[e] = run * NBG;
+    const int lo = sm.offs[e], hi = sm.offs[e + 1];
+    if (!bad) run += (hi - lo + BNMAX - 1) / BNMAX;
+  }
+}
+
+// Host: 2-D u8 tensor [rows, cols] (cols contiguous) with a box of 128 B x
+// box_rows, 128-byte swizzle, zero fill outside the tensor. False when the
+// driver cannot encode it.
+bool make_tma_map_u8(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
+                     uint32_t box_rows);
+
+}  // namespace gemm_common
+}  // namespace moe

@@ -27,6 +27,12 @@ cudaError_t launch_permute_quant(const void* x, const int32_t* ids, int T, int H
                                  void* a_q, float* scale_a, int32_t* src2dst, int32_t* offsets,
                                  void* ws, int* err, cudaStream_t st);
 
+// permute.cu: the same with one scale per 128 channels, scale_a [T*K, H/128]
+// (H % 128 == 0).
+cudaError_t launch_permute_quant_block(const void* x, const int32_t* ids, int T, int H, int E,
+                                       int K, void* a_q, float* scale_a, int32_t* src2dst,
+                                       int32_t* offsets, void* ws, int* err, cudaStream_t st);
+
 // permute.cu: device address of the fixed scratch used by
 // moe_permute_quant_noalloc on the current device (nullptr on failure).
 void* permute_static_scratch();
@@ -38,9 +44,20 @@ cudaError_t launch_grouped_gemm(const void* A, const float* scale_a, const void*
                                 int Kd, int E, int epilogue, void* C, float* row_amax, int* err,
                                 cudaStream_t st);
 
+// gemm_block.cu: block scales, scale_a [M, Kd/128], scale_b [E, N/128, Kd/128]
+// (N % 128 == 0, Kd % 128 == 0); no row amax.
+cudaError_t launch_grouped_gemm_block(const void* A, const float* scale_a, const void* B,
+                                      const float* scale_b, const int32_t* offsets, int M, int N,
+                                      int Kd, int E, int epilogue, void* C, int* err,
+                                      cudaStream_t st);
+
 // act_quant.cu
 cudaError_t launch_act_quant(const void* h, const float* row_amax, int M, int I, void* q,
                              float* scale, cudaStream_t st);
+
+// act_quant.cu: one scale per 128 channels, scale [M, I/128] (I % 128 == 0).
+cudaError_t launch_act_quant_block(const void* h, int M, int I, void* q, float* scale,
+                                   cudaStream_t st);
 
 // unpermute.cu
 cudaError_t launch_unpermute_sum(const void* down, const int32_t* src2dst, const float* w,

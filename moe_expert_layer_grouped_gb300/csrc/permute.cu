@@ -118,7 +118,11 @@ __global__ void __launch_bounds__(1024)
 
 constexpr int kQuantThreads = 128;
 
-template <int VPT>  // 16-byte vectors (8 bf16) per thread
+// BLOCK: one scale per 128 channels (scale_a [M, H/128]) instead of one per
+// token. A 128-channel block is 16 vectors, held by the 16 lanes of a
+// half-warp (vector tid + i*128 lies in block tid/16 + 8i), so its amax is a
+// 16-lane shuffle reduction.
+template <int VPT, bool BLOCK>  // VPT: 16-byte vectors (8 bf16) per thread
 __global__ void __launch_bounds__(kQuantThreads)
     permute_quant_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ ids,
                          const uint32_t* __restrict__ bits, const int32_t* __restrict__ base,
@@ -153,6 +157,33 @@ __global__ void __launch_bounds__(kQuantThreads)
       amax = absmax8(f, amax);
     }
   }
+  if (BLOCK) {
+    __syncthreads();  // dst[] is complete
+    const int nb = H >> 7;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+      const int idx = tid + i * kQuantThreads;
+      float f[8];
+      float m = 0.0f;
+      if (idx < nvec) {
+        bf16x8_to_f32(v[i], f);
+        m = absmax8(f, 0.0f);
+      }
+#pragma unroll
+      for (int o = 1; o < 16; o <<= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
+      if (idx < nvec) {
+        const float sc = token_scale(m);
+        const uint2 q = quant8(f, sc);
+        for (int k = 0; k < K; ++k) {
+          const int d = dst[k];
+          if (d < 0) continue;
+          *reinterpret_cast<uint2*>(a_q + (int64_t)d * H + (int64_t)idx * 8) = q;
+          if ((idx & 15) == 0) scale_a[(int64_t)d * nb + (idx >> 4)] = sc;
+        }
+      }
+    }
+    return;
+  }
   amax = warp_max(amax);
   if ((tid & 31) == 0) red[tid >> 5] = amax;
   __syncthreads();
@@ -176,11 +207,11 @@ __global__ void __launch_bounds__(kQuantThreads)
   }
 }
 
-template <int VPT>
+template <int VPT, bool BLOCK>
 void launch_quant(const void* x, const int32_t* ids, const uint32_t* bits, const int32_t* base,
                   int T, int H, int E, int K, void* a_q, float* scale_a, int32_t* src2dst,
                   cudaStream_t st) {
-  permute_quant_kernel<VPT><<<T, kQuantThreads, 0, st>>>(
+  permute_quant_kernel<VPT, BLOCK><<<T, kQuantThreads, 0, st>>>(
       reinterpret_cast<const __nv_bfloat16*>(x), ids, bits, base, H, E, K,
       reinterpret_cast<uint8_t*>(a_q), scale_a, src2dst);
 }
@@ -213,9 +244,12 @@ size_t permute_ws_bytes(int T, int E) {
   return 2 * align_up(C * (size_t)E * 4);
 }
 
-cudaError_t launch_permute_quant(const void* x, const int32_t* ids, int T, int H, int E, int K,
-                                 void* a_q, float* scale_a, int32_t* src2dst, int32_t* offsets,
-                                 void* ws, int* err, cudaStream_t st) {
+namespace {
+
+template <bool BLOCK>
+cudaError_t permute_quant(const void* x, const int32_t* ids, int T, int H, int E, int K,
+                          void* a_q, float* scale_a, int32_t* src2dst, int32_t* offsets,
+                          void* ws, int* err, cudaStream_t st) {
   const int C = (T + 31) / 32;
   uint32_t* bits = reinterpret_cast<uint32_t*>(ws);
   int32_t* base = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(ws) +
@@ -228,13 +262,27 @@ cudaError_t launch_permute_quant(const void* x, const int32_t* ids, int T, int H
   route_scan_kernel<<<1, 1024, 0, st>>>(bits, C, E, base, offsets);
   if (T > 0) {
     const int vpt = (H / 8 + kQuantThreads - 1) / kQuantThreads;
-    if (vpt <= 1) launch_quant<1>(x, ids, bits, base, T, H, E, K, a_q, scale_a, src2dst, st);
-    else if (vpt <= 2) launch_quant<2>(x, ids, bits, base, T, H, E, K, a_q, scale_a, src2dst, st);
-    else if (vpt <= 4) launch_quant<4>(x, ids, bits, base, T, H, E, K, a_q, scale_a, src2dst, st);
-    else if (vpt <= 8) launch_quant<8>(x, ids, bits, base, T, H, E, K, a_q, scale_a, src2dst, st);
-    else launch_quant<16>(x, ids, bits, base, T, H, E, K, a_q, scale_a, src2dst, st);
+    if (vpt <= 1) launch_quant<1, BLOCK>(x, ids, bits, base, T, H, E, K, a_q, scale_a, src2dst, st);
+    else if (vpt <= 2) launch_quant<2, BLOCK>(x, ids, bits, base, T, H, E, K, a_q, scale_a, src2dst, st);
+    else if (vpt <= 4) launch_quant<4, BLOCK>(x, ids, bits, base, T, H, E, K, a_q, scale_a, src2dst, st);
+    else if (vpt <= 8) launch_quant<8, BLOCK>(x, ids, bits, base, T, H, E, K, a_q, scale_a, src2dst, st);
+    else launch_quant<16, BLOCK>(x, ids, bits, base, T, H, E, K, a_q, scale_a, src2dst, st);
   }
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_permute_quant(const void* x, const int32_t* ids, int T, int H, int E, int K,
+                                 void* a_q, float* scale_a, int32_t* src2dst, int32_t* offsets,
+                                 void* ws, int* err, cudaStream_t st) {
+  return permute_quant<false>(x, ids, T, H, E, K, a_q, scale_a, src2dst, offsets, ws, err, st);
+}
+
+cudaError_t launch_permute_quant_block(const void* x, const int32_t* ids, int T, int H, int E,
+                                       int K, void* a_q, float* scale_a, int32_t* src2dst,
+                                       int32_t* offsets, void* ws, int* err, cudaStream_t st) {
+  return permute_quant<true>(x, ids, T, H, E, K, a_q, scale_a, src2dst, offsets, ws, err, st);
 }
 
 }  // namespace moe

@@ -34,7 +34,9 @@ def test_header_declares_the_entry_points():
     for want in ["moe_gate", "moe_permute_quant", "moe_grouped_gemm", "moe_act_quant",
                  "moe_unpermute_sum", "moe_forward", "moe_forward_host", "moe_workspace_size",
                  "moe_permute_workspace_size", "moe_device_status", "moe_status_string",
-                 "moe_abi_version", "moe_forward_shared", "moe_forward_shared_host"]:
+                 "moe_abi_version", "moe_forward_shared", "moe_forward_shared_host",
+                 "moe_permute_quant_block", "moe_grouped_gemm_block", "moe_act_quant_block",
+                 "moe_block_workspace_size", "moe_forward_block", "moe_forward_block_host"]:
         assert want in names
 
 
@@ -149,6 +151,32 @@ def test_forward_shared_validation(lib):
     assert f(*base(31), ws, 1 << 40, None) == UNSUPPORTED      # top_k + n_shared > 32
     assert fh(*base(1), None, need, None) == WORKSPACE
     assert fh(*base(-1), ws, need, None) == INVALID
+
+
+def test_block_validation(lib):
+    """Block FP8 needs the blocked dimensions to be multiples of 128 (I for
+    SiLU*mul, so N = 2I a multiple of 256); refused before any device work."""
+    g = lib.moe_grouped_gemm_block
+    assert g(GOOD, GOOD, GOOD, GOOD, GOOD, 64, 256, 192, 4, 0, GOOD, None) == INVALID   # Kd
+    assert g(GOOD, GOOD, GOOD, GOOD, GOOD, 64, 192, 256, 4, 0, GOOD, None) == INVALID   # N
+    assert g(GOOD, GOOD, GOOD, GOOD, GOOD, 64, 384, 256, 4, 1, GOOD, None) == INVALID   # I=192
+    assert g(GOOD, GOOD, GOOD, GOOD, GOOD, 64, 256, 256, 2048, 0, GOOD, None) == UNSUPPORTED
+    assert lib.moe_act_quant_block(GOOD, 10, 192, GOOD, GOOD, None) == INVALID
+    p = lib.moe_permute_quant_block
+    need = lib.moe_permute_workspace_size(16, 8, 2)
+    assert p(GOOD, GOOD, 16, 160, 8, 2, GOOD, GOOD, GOOD, GOOD, P(0x100000), need,
+             None) == INVALID
+    assert lib.moe_block_workspace_size(16, 160, 128, 8, 2) == 0
+    T, H, I, E, K = 256, 256, 128, 8, 2
+    need = lib.moe_block_workspace_size(T, H, I, E, K)
+    assert need > lib.moe_workspace_size(T, H, I, E, K)   # per-block scales take more room
+    f = lib.moe_forward_block
+    base = [GOOD, GOOD, None, GOOD, GOOD, GOOD, GOOD, T, H, I, E, 0, 1, 1, K, 1, 1, 1.0, GOOD]
+    assert f(*base, P(0x100000), need - 1, None) == WORKSPACE
+    bad = list(base)
+    bad[9] = 192  # I not a multiple of 128
+    assert f(*bad, P(0x100000), 1 << 40, None) == INVALID
+    assert lib.moe_forward_block_host(*bad, P(0x100000), 1 << 40, None) == INVALID
 
 
 def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
