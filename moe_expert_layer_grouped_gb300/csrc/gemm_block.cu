@@ -6,9 +6,10 @@
 //
 // The scales change every 128 channels of K, so the tensor cores cannot keep
 // one accumulator across K. A K block is exactly one pipeline stage: the MMA
-// thread writes each block's partial sum afresh into one of two TMEM buffers,
-// and the epilogue warps fold it into fp32 registers with its factor
-// sa[token,kb] * sb[kb] while the MMA fills the other buffer.
+// thread writes each block's partial sum afresh into one of up to four TMEM
+// buffers, and the epilogue warps fold it into fp32 registers with its
+// factor sa[token,kb] * sb[kb] (loaded a block ahead) while the MMA fills
+// the next buffers.
 //
 // Orientation and tiles as in moe_grouped_gemm: weights on the MMA's M side
 // (128 rows per tile, which is one weight scale block), tokens on N (at most
@@ -17,13 +18,13 @@
 //   warp 0      TMA producer (one K block of weights and tokens per stage)
 //   warp 1      MMA issuer (tcgen05.mma.cta_group::1.kind::f8f6f4, K=32 x 4)
 //   warps 2..9  epilogue: warp w reads TMEM lane quadrant w % 4 and one half
-//               of the tile's token columns; per K block the 256 epilogue
-//               threads first stage the per-token factors of both weight
-//               scales in shared memory (one token each), then accumulate.
+//               of the tile's token columns; per K block it stages its
+//               columns' factors sa*sb in its own shared-memory row (no
+//               barrier across warps), then accumulates.
 // SiLU*mul and the bf16 stores work as in moe_grouped_gemm (gate rows in TMEM
 // lanes 0..63, up rows in 64..127, exchanged through shared memory).
-// Every wait is bounded; the epilogue warps take abort decisions together
-// through bar.red so no warp is left at a named barrier.
+// Every wait is bounded; the two warps of a SiLU exchange pair take the abort
+// decision together through bar.red so neither is left at a named barrier.
 #include <cuda.h>
 
 #include <algorithm>
@@ -42,20 +43,26 @@ using namespace gemm_common;
 constexpr int EPI_WARPS = 8;
 constexpr int BTHREADS = 64 + 32 * EPI_WARPS;
 constexpr int EPI_THREADS = 32 * EPI_WARPS;
-constexpr int BAR_KB = 1;    // named barrier of the 256 epilogue threads
 constexpr int BAR_PAIR = 2;  // 2..5: the SiLU exchange pairs
+
+// TMEM partial buffers: all 512 columns, at most 4 (the MMA runs up to
+// NPB - 1 K blocks ahead of the epilogue).
+template <int BNMAX>
+__host__ __device__ constexpr int npb() {
+  return 512 / BNMAX > 4 ? 4 : 512 / BNMAX;
+}
 
 template <int BNMAX, int STAGES, bool SILU>
 struct BSmem {
   uint8_t w[STAGES][W_BYTES];          // weights, one K block per stage
   uint8_t x[STAGES][BNMAX * BK];       // tokens
-  float fs[2][2][BNMAX];               // per partial buffer: sa*sb per token (main/gate, up)
+  float fw[EPI_WARPS][BNMAX / 2];      // per epilogue warp: sa*sb of its token columns
   float xchg[SILU ? 4 : 1][32 * 32];   // SiLU: one slot per exchange pair
   uint16_t stage_out[EPI_WARPS][32 * 32];
   uint64_t full[STAGES];
   uint64_t empty[STAGES];
-  uint64_t pfull[2];   // a K block's partial sum is in TMEM buffer b
-  uint64_t pempty[2];  // the epilogue has read buffer b
+  uint64_t pfull[npb<BNMAX>()];   // a K block's partial sum is in TMEM buffer b
+  uint64_t pempty[npb<BNMAX>()];  // the epilogue has read buffer b
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
@@ -76,11 +83,25 @@ struct BParams {
   int stream_weights;
 };
 
+// acc0/1 += v0/1 * f0/1, two lanes of fp32 at once (each rounded as fmaf).
+__device__ __forceinline__ void fma2(float& acc0, float& acc1, float v0, float v1, float f0,
+                                     float f1) {
+  asm("{\n\t.reg .b64 a, b, c;\n\t"
+      "mov.b64 a, {%2, %3};\n\t"
+      "mov.b64 b, {%4, %5};\n\t"
+      "mov.b64 c, {%0, %1};\n\t"
+      "fma.rn.f32x2 c, a, b, c;\n\t"
+      "mov.b64 {%0, %1}, c;\n\t}"
+      : "+f"(acc0), "+f"(acc1)
+      : "f"(v0), "f"(v1), "f"(f0), "f"(f1));
+}
+
 template <int BNMAX, int STAGES, bool SILU>
 __global__ void __launch_bounds__(BTHREADS, 1)
     grouped_gemm_block_kernel(const __grid_constant__ Maps maps, const BParams p) {
   using S = BSmem<BNMAX, STAGES, SILU>;
-  constexpr uint32_t TCOLS = 2 * BNMAX;  // two partial buffers
+  constexpr int NPB = npb<BNMAX>();
+  constexpr uint32_t TCOLS = NPB * BNMAX;  // the partial buffers
   constexpr int HC = BNMAX / 2;          // token columns per epilogue warp
   constexpr int NCH = HC / 32;           // 32-column chunks per epilogue warp
   static_assert(NCH >= 1 && BNMAX <= EPI_THREADS, "tile shape");
@@ -100,7 +121,7 @@ __global__ void __launch_bounds__(BTHREADS, 1)
       ptx::mbar_init(&sm.full[s], 1);
       ptx::mbar_init(&sm.empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < NPB; ++b) {
       ptx::mbar_init(&sm.pfull[b], 1);
       ptx::mbar_init(&sm.pempty[b], EPI_WARPS);
     }
@@ -185,8 +206,8 @@ __global__ void __launch_bounds__(BTHREADS, 1)
         const TileInfo<BNMAX> t = decode_tile<BNMAX>(sm, E, p.NB, g);
         const uint32_t idesc = ptx::idesc_e4m3_f32(BM, (t.ntok + 15) & ~15);
         for (int kb = 0; kb < KB; ++kb, ++kbg) {
-          const uint32_t b = kbg & 1u;
-          if (!ptx::mbar_wait(&sm.pempty[b], ((kbg >> 1) & 1u) ^ 1u, &sm.abort, WAIT_NS) ||
+          const uint32_t b = kbg % NPB;
+          if (!ptx::mbar_wait(&sm.pempty[b], ((kbg / NPB) & 1u) ^ 1u, &sm.abort, WAIT_NS) ||
               !ptx::mbar_wait(&sm.full[s], ph, &sm.abort, WAIT_NS)) {
             ok = false;
             break;
@@ -221,73 +242,77 @@ __global__ void __launch_bounds__(BTHREADS, 1)
     // ======================= epilogue (warps 2..9) ==========================
     const int q = warp & 3;              // TMEM lane quadrant this warp may access
     const int hsel = (warp - 2) >> 2;    // which half of the token columns
-    const int et = tid - 64;             // epilogue thread: stages token et's factors
+    const int col0w = hsel * HC;         // first token column of this warp
     const int NBk = p.N / 128;           // weight scale blocks along N
     const bool up_rows = SILU && q >= 2;
+    float* fw = sm.fw[warp - 2];
     uint32_t kbg = 0;
-    int bad = 0;
     bool stop = false;
     for (int g = blockIdx.x; !stop && g < total; g += ncta) {
       const TileInfo<BNMAX> t = decode_tile<BNMAX>(sm, E, p.NB, g);
       const int n_mma = (t.ntok + 15) & ~15;
-      // the tile's weight scale rows: one 128-row block (bf16 out), or the
-      // gate and the up block (SiLU)
-      const int blk0 = SILU ? (t.nb * 64) / 128 : t.nb;
-      const int blk1 = SILU ? (p.I + t.nb * 64) / 128 : t.nb;
-      const float* sb0 = p.scale_b + ((int64_t)t.e * NBk + blk0) * KB;
-      const float* sb1 = p.scale_b + ((int64_t)t.e * NBk + blk1) * KB;
-      const bool tv = et < t.ntok;
-      const float* sa_row = p.scale_a + (int64_t)(t.tok0 + (tv ? et : 0)) * KB;
-      float sa_n = tv ? __ldg(sa_row) : 0.0f;
+      // the weight scale row of this warp's TMEM lanes: the tile's 128-row
+      // block (bf16 out), or its gate or its up block (SiLU)
+      const int blk = SILU ? ((up_rows ? p.I : 0) + t.nb * 64) / 128 : t.nb;
+      const float* sbw = p.scale_b + ((int64_t)t.e * NBk + blk) * KB;
+      // lane l stages the factors of token columns col0w + l + 32c; this K
+      // block's scales are loaded one block ahead
+      const float* sa_p[NCH];
+      bool tv[NCH];
+      float sa_c[NCH];
+#pragma unroll
+      for (int c = 0; c < NCH; ++c) {
+        const int col = col0w + c * 32 + lane;
+        tv[c] = col < t.ntok;
+        sa_p[c] = p.scale_a + (int64_t)(t.tok0 + (tv[c] ? col : 0)) * KB;
+        sa_c[c] = tv[c] ? __ldg(sa_p[c]) : 0.0f;
+      }
+      float sb_c = __ldg(sbw);
       float acc[HC];
 #pragma unroll
       for (int i = 0; i < HC; ++i) acc[i] = 0.0f;
       for (int kb = 0; kb < KB; ++kb, ++kbg) {
-        const uint32_t b = kbg & 1u;
-        if (et < BNMAX) {
-          sm.fs[b][0][et] = sa_n * __ldg(sb0 + kb);
-          if (SILU) sm.fs[b][1][et] = sa_n * __ldg(sb1 + kb);
+        const uint32_t b = kbg % NPB;
+#pragma unroll
+        for (int c = 0; c < NCH; ++c) fw[c * 32 + lane] = sa_c[c] * sb_c;
+        if (kb + 1 < KB) {
+#pragma unroll
+          for (int c = 0; c < NCH; ++c) sa_c[c] = tv[c] ? __ldg(sa_p[c] + kb + 1) : 0.0f;
+          sb_c = __ldg(sbw + kb + 1);
         }
-        sa_n = (tv && kb + 1 < KB) ? __ldg(sa_row + kb + 1) : 0.0f;
-        // the factors are staged; a failure anywhere stops every epilogue warp
-        if (bar_red_or(BAR_KB, EPI_THREADS, bad)) {
+        __syncwarp();
+        bool ok = ptx::mbar_wait(&sm.pfull[b], (kbg / NPB) & 1u, &sm.abort, WAIT_NS);
+        if (!__all_sync(kFull, ok)) {
           stop = true;
           break;
         }
-        bool ok = ptx::mbar_wait(&sm.pfull[b], (kbg >> 1) & 1u, &sm.abort, WAIT_NS);
-        ok = __all_sync(kFull, ok);
-        if (!ok) {
-          bad = 1;
-          continue;
-        }
         ptx::tc_fence_after();
-        const float* f = sm.fs[b][up_rows ? 1 : 0] + hsel * HC;
-        const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + b * BNMAX + hsel * HC;
+        const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + b * BNMAX + col0w;
 #pragma unroll
         for (int c = 0; c < NCH; ++c) {
-          if (hsel * HC + c * 32 < n_mma) {  // warp-uniform
+          if (col0w + c * 32 < n_mma) {  // warp-uniform
             uint32_t v[32];
             ptx::tmem_ld_32x32b_x32(tb + c * 32, v);
             ptx::tmem_ld_wait();
             ptx::reg_fence(v);
 #pragma unroll
             for (int i = 0; i < 32; i += 4) {
-              const float4 fv = *reinterpret_cast<const float4*>(f + c * 32 + i);
-              acc[c * 32 + i + 0] = fmaf(__uint_as_float(v[i + 0]), fv.x, acc[c * 32 + i + 0]);
-              acc[c * 32 + i + 1] = fmaf(__uint_as_float(v[i + 1]), fv.y, acc[c * 32 + i + 1]);
-              acc[c * 32 + i + 2] = fmaf(__uint_as_float(v[i + 2]), fv.z, acc[c * 32 + i + 2]);
-              acc[c * 32 + i + 3] = fmaf(__uint_as_float(v[i + 3]), fv.w, acc[c * 32 + i + 3]);
+              const float4 fv = *reinterpret_cast<const float4*>(fw + c * 32 + i);
+              fma2(acc[c * 32 + i + 0], acc[c * 32 + i + 1], __uint_as_float(v[i + 0]),
+                   __uint_as_float(v[i + 1]), fv.x, fv.y);
+              fma2(acc[c * 32 + i + 2], acc[c * 32 + i + 3], __uint_as_float(v[i + 2]),
+                   __uint_as_float(v[i + 3]), fv.z, fv.w);
             }
           }
         }
         ptx::tc_fence_before();
-        __syncwarp();
+        __syncwarp();  // also: the factors are read before the next block's are written
         if (lane == 0) ptx::mbar_arrive(&sm.pempty[b]);
       }
-      if (stop || bar_red_or(BAR_KB, EPI_THREADS, bad)) {
-        stop = true;
-        break;
-      }
+      // the two warps of a SiLU exchange pair go on to the output together
+      // or not at all (a warp that stopped still meets its partner here)
+      if (SILU && bar_red_or(BAR_PAIR + (q & 1) + 2 * hsel, 64, stop)) stop = true;
+      if (stop) break;
       // ---- the tile's output: every K block is in acc ----
       uint16_t* ost = sm.stage_out[warp - 2];
       if (SILU) {

@@ -84,7 +84,8 @@ for _name, _S in [("tiny", 1), ("dsv3_decode_t128", 1), ("dsv3_prefill_t8192", 1
     WORKLOADS[f"{_name}_shared"] = replace(WORKLOADS[_name], name=f"{_name}_shared",
                                            n_shared=_S)
 WORKLOADS["tiny_block"] = replace(WORKLOADS["tiny"], name="tiny_block", I=128, quant="block")
-for _name in ["dsv3_decode_t128", "dsv3_prefill_t8192", "mixtral_t4096"]:
+for _name in ["dsv3_decode_t128", "dsv3_prefill_t8192", "mixtral_t4096", "dsv3_decode_t128_e32",
+              "dsv3_prefill_t2048_e32"]:
     WORKLOADS[f"{_name}_block"] = replace(WORKLOADS[_name], name=f"{_name}_block",
                                           quant="block")
 
