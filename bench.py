@@ -176,7 +176,7 @@ def rank_seed(seed, rank):
 
 def kernel_source_hash():
     h = hashlib.sha256()
-    for f in ("gemm.cu", "ptx.cuh", "common.cuh"):
+    for f in ("gemm.cu", "gemm_common.cuh", "ptx.cuh", "common.cuh"):
         with open(os.path.join(ROOT, "moe_expert_layer_grouped_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
