@@ -351,6 +351,23 @@ MOE_API moe_status moe_forward_block_host(const void* x_host,
                               void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * moe_test_gemm_timeout — failure-detection test of the GEMM pipeline (the
+ * pages have no counterpart). Runs moe_grouped_gemm, except that CTA 0 arms
+ * its pipeline stage number stall_stage (>= 0, counted over its tiles) but
+ * never issues that stage's loads. Its bounded waits then run out (about 2 s):
+ * the CTA sets the device error word to MOE_DEV_PIPE_TIMEOUT, lets its
+ * issued copies and MMAs land, frees its tensor memory and exits; the other
+ * CTAs finish normally. The call itself returns MOE_OK; moe_device_status
+ * then reports the timeout, and the context stays usable. C is left partly
+ * written. The same argument checks as moe_grouped_gemm.
+ */
+MOE_API moe_status moe_test_gemm_timeout(const void* A, const float* scale_a,
+                              const void* B, const float* scale_b,
+                              const int32_t* offsets, int M, int N, int Kd,
+                              int E, int epilogue, void* C, int stall_stage,
+                              void* stream);
+
+/*
  * moe_device_status — synchronises the current device, copies its device
  * error word into *code (one of MOE_DEV_*), clears it, and returns MOE_OK
  * when it was zero, MOE_ERR_DEVICE otherwise (MOE_ERR_CUDA if the copy

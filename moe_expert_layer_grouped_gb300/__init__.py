@@ -19,7 +19,7 @@ __all__ = [
     "moe_gate", "moe_permute_quant", "moe_permute_workspace_size", "moe_grouped_gemm",
     "moe_forward_shared", "moe_forward_shared_host", "moe_permute_quant_block",
     "moe_grouped_gemm_block", "moe_act_quant_block", "moe_block_workspace_size",
-    "moe_forward_block", "moe_forward_block_host",
+    "moe_forward_block", "moe_forward_block_host", "moe_test_gemm_timeout",
     "moe_permute_quant_noalloc", "moe_act_quant", "moe_unpermute_sum", "moe_workspace_size", "moe_forward",
     "moe_forward_host", "moe_device_status", "MoELayer",
 ]
@@ -28,6 +28,11 @@ SIGMOID = 0
 SOFTMAX = 1
 EPI_BF16 = 0
 EPI_SILU_MUL = 1
+# device error codes read by moe_device_status()
+DEV_OK = 0
+DEV_BAD_EXPERT_ID = 1
+DEV_PIPE_TIMEOUT = 2
+DEV_BAD_OFFSETS = 3
 
 _STATUS = {0: "MOE_OK", -1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_UNSUPPORTED",
            -3: "MOE_ERR_WORKSPACE", -4: "MOE_ERR_CUDA", -5: "MOE_ERR_DEVICE"}
@@ -74,6 +79,7 @@ _SIGNATURES = {
     "moe_grouped_gemm_block": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P]),
     "moe_act_quant_block": (_I, [_P, _I, _I, _P, _P, _P]),
     "moe_block_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
+    "moe_test_gemm_timeout": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _I, _P]),
     "moe_forward_block": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I,
                                _I, _F, _P, _P, _SZ, _P]),
     "moe_forward_block_host": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I,
@@ -408,6 +414,20 @@ def moe_forward_block_host(x_host, logits_host, bias, w13, s13, w2, s2, n_shared
         int(bool(renormalize)), float(routed_scaling_factor), _ptr(out_host), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
     return out_host
+
+
+def moe_test_gemm_timeout(A, scale_a, B, scale_b, offsets, epilogue, C, stall_stage,
+                          stream=None):
+    """Failure-detection test: one pipeline stage of CTA 0 never receives its
+    bytes, so the GEMM's bounded waits run out (~2 s); moe_device_status()
+    then returns DEV_PIPE_TIMEOUT and the context stays usable."""
+    _need_cuda(A, scale_a, B, scale_b, offsets, C)
+    M, Kd = A.shape
+    E, N, _ = B.shape
+    _check("moe_test_gemm_timeout", load().moe_test_gemm_timeout(
+        _ptr(_u8(A)), _ptr(scale_a), _ptr(_u8(B)), _ptr(scale_b), _ptr(offsets), M, N, Kd, E,
+        epilogue, _ptr(C), int(stall_stage), _stream(stream)))
+    return C
 
 
 def moe_device_status():

@@ -300,6 +300,20 @@ moe_status moe_grouped_gemm(const void* A, const float* scale_a, const void* B,
                                          C, row_amax, err, static_cast<cudaStream_t>(stream)));
 }
 
+moe_status moe_test_gemm_timeout(const void* A, const float* scale_a, const void* B,
+                                 const float* scale_b, const int32_t* offsets, int M, int N,
+                                 int Kd, int E, int epilogue, void* C, int stall_stage,
+                                 void* stream) {
+  moe_status s = check_gemm(A, scale_a, B, scale_b, offsets, M, N, Kd, E, epilogue, C, nullptr);
+  if (s != MOE_OK) return s;
+  if (stall_stage < 0) return MOE_ERR_INVALID_ARG;
+  int* err = device_error_word();
+  if (err == nullptr) return MOE_ERR_CUDA;
+  return cuda_status(launch_grouped_gemm(A, scale_a, B, scale_b, offsets, M, N, Kd, E, epilogue,
+                                         C, nullptr, err, static_cast<cudaStream_t>(stream),
+                                         stall_stage));
+}
+
 moe_status moe_act_quant(const void* h, const float* row_amax, int M, int I, void* q,
                          float* scale, void* stream) {
   if (M < 0 || I < 1 || I % 32 != 0) return MOE_ERR_INVALID_ARG;

@@ -92,6 +92,7 @@ struct Params {
   int* err;
   int M, N, Kd, E, I, NB, KB;
   int stream_weights;  // 1: each weight block is read by one tile (evict-first)
+  int stall_stage;     // failure test: CTA 0 never loads its stage with this index (-1: none)
 };
 
 // CS = 1: one CTA per tile of 128 weight rows x N tokens.
@@ -156,12 +157,16 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t tmem = sm.tmem_base;
   const int total = sm.total_tiles;  // after the barrier above
 
+  // stages the producer armed (and the phase of the latest arming), for the
+  // drain after an abort
+  uint32_t armed = 0, armed_par = 0;
   if (warp == 0) {
     // ======================= TMA producer ===================================
     if (lane == 0) {
       const uint64_t pol_w = p.stream_weights ? ptx::policy_evict_first() : ptx::policy_evict_normal();
       const uint64_t pol_x = ptx::policy_evict_last();
-      uint32_t s = 0, ph = 0, armed = 0, armed_par = 0;
+      uint32_t s = 0, ph = 0;
+      int gstage = 0;  // stages issued by this CTA
       bool ok = true;
       for (int g = cluster; ok && g < total; g += nclusters) {
         const TileInfo<BNMAX> t = decode_tile<BNMAX>(sm, E, NBG, g);
@@ -191,8 +196,11 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
           // pair: completions count on the even CTA's barrier
           const uint32_t fb = PAIR ? ptx::map_to_rank(ptx::smem_u32(&sm.full[s]), 0) : 0u;
+          // failure test: the stage is armed but its bytes never come, so the
+          // bounded waits run out
+          const bool stall = blockIdx.x == 0 && gstage++ == p.stall_stage;
 #pragma unroll
-          for (int kc = 0; kc < KC; ++kc) {
+          for (int kc = 0; kc < (stall ? 0 : KC); ++kc) {
             const int kx = (ks * KC + kc) * BK;  // past Kd: zero-filled, adds nothing
             uint8_t* wdst = sm.w[s][kc];
             uint8_t* xdst = sm.x[s][kc];
@@ -232,9 +240,6 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (!ok) {
         sm.abort = 1;
         flag_error(p.err, MOE_DEV_PIPE_TIMEOUT);
-        for (int i = 0; i < STAGES; ++i)
-          if ((armed >> i) & 1u)
-            ptx::mbar_wait(&sm.full[i], (armed_par >> i) & 1u, &sm.never, DRAIN_NS);
       }
     }
   } else if (warp == 1) {
@@ -448,6 +453,13 @@ __global__ void __launch_bounds__(THREADS, 1)
   // ---- teardown -------------------------------------------------------------
   ptx::tc_fence_before();
   __syncthreads();
+  // after an abort (whichever role gave up, possibly after the producer had
+  // finished its loop), every copy the producer issued lands before the CTA
+  // frees its tensor memory and leaves
+  if (warp == 0 && lane == 0 && *reinterpret_cast<volatile int*>(&sm.abort))
+    for (int i = 0; i < STAGES; ++i)
+      if ((armed >> i) & 1u)
+        ptx::mbar_wait(&sm.full[i], (armed_par >> i) & 1u, &sm.never, DRAIN_NS);
   if (PAIR) {
     // both CTAs are done with the shared accumulator before it is freed, and
     // neither leaves while the other may still signal its barriers
@@ -579,7 +591,7 @@ bool make_tma_map_u8(CUtensorMap* m, const void* base, uint64_t rows, uint64_t c
 cudaError_t launch_grouped_gemm(const void* A, const float* scale_a, const void* B,
                                 const float* scale_b, const int32_t* offsets, int M, int N,
                                 int Kd, int E, int epilogue, void* C, float* row_amax, int* err,
-                                cudaStream_t st) {
+                                cudaStream_t st, int stall_stage) {
   if (M == 0) return cudaSuccess;
   const bool silu = (epilogue == MOE_EPI_SILU_MUL);
   const bool small = (int64_t)M <= (int64_t)32 * E;  // few rows per expert (decode)
@@ -607,6 +619,7 @@ cudaError_t launch_grouped_gemm(const void* A, const float* scale_a, const void*
   // few rows per expert (decode): small token tiles and a deep weight ring,
   // weights streamed once; many (prefill): tiles of up to 256 tokens
   p.stream_weights = small ? 1 : 0;
+  p.stall_stage = stall_stage;
   if (small)
     return silu ? launch_cfg<64, 8, true, 1, 1>(maps, p, M, E, st)
                 : launch_cfg<64, 8, false, 1, 1>(maps, p, M, E, st);

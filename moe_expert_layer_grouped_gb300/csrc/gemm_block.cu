@@ -142,13 +142,16 @@ __global__ void __launch_bounds__(BTHREADS, 1)
   const int total = sm.total_tiles;
   const int ncta = gridDim.x;
 
+  // stages the producer armed (and the phase of the latest arming), for the
+  // drain after an abort
+  uint32_t armed = 0, armed_par = 0;
   if (warp == 0) {
     // ======================= TMA producer ===================================
     if (lane == 0) {
       const uint64_t pol_w =
           p.stream_weights ? ptx::policy_evict_first() : ptx::policy_evict_normal();
       const uint64_t pol_x = ptx::policy_evict_last();
-      uint32_t s = 0, ph = 0, armed = 0, armed_par = 0;
+      uint32_t s = 0, ph = 0;
       bool ok = true;
       for (int g = blockIdx.x; ok && g < total; g += ncta) {
         const TileInfo<BNMAX> t = decode_tile<BNMAX>(sm, E, p.NB, g);
@@ -191,9 +194,6 @@ __global__ void __launch_bounds__(BTHREADS, 1)
       if (!ok) {
         sm.abort = 1;
         flag_error(p.err, MOE_DEV_PIPE_TIMEOUT);
-        for (int i = 0; i < STAGES; ++i)
-          if ((armed >> i) & 1u)
-            ptx::mbar_wait(&sm.full[i], (armed_par >> i) & 1u, &sm.never, DRAIN_NS);
       }
     }
   } else if (warp == 1) {
@@ -391,6 +391,13 @@ __global__ void __launch_bounds__(BTHREADS, 1)
   // ---- teardown -------------------------------------------------------------
   ptx::tc_fence_before();
   __syncthreads();
+  // after an abort (whichever role gave up, possibly after the producer had
+  // finished its loop), every copy the producer issued lands before the CTA
+  // frees its tensor memory and leaves
+  if (warp == 0 && lane == 0 && *reinterpret_cast<volatile int*>(&sm.abort))
+    for (int i = 0; i < STAGES; ++i)
+      if ((armed >> i) & 1u)
+        ptx::mbar_wait(&sm.full[i], (armed_par >> i) & 1u, &sm.never, DRAIN_NS);
   if (warp == 1) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, TCOLS);

@@ -42,7 +42,7 @@ void* permute_static_scratch();
 cudaError_t launch_grouped_gemm(const void* A, const float* scale_a, const void* B,
                                 const float* scale_b, const int32_t* offsets, int M, int N,
                                 int Kd, int E, int epilogue, void* C, float* row_amax, int* err,
-                                cudaStream_t st);
+                                cudaStream_t st, int stall_stage = -1);
 
 // gemm_block.cu: block scales, scale_a [M, Kd/128], scale_b [E, N/128, Kd/128]
 // (N % 128 == 0, Kd % 128 == 0); no row amax.

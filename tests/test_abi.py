@@ -36,7 +36,8 @@ def test_header_declares_the_entry_points():
                  "moe_permute_workspace_size", "moe_device_status", "moe_status_string",
                  "moe_abi_version", "moe_forward_shared", "moe_forward_shared_host",
                  "moe_permute_quant_block", "moe_grouped_gemm_block", "moe_act_quant_block",
-                 "moe_block_workspace_size", "moe_forward_block", "moe_forward_block_host"]:
+                 "moe_block_workspace_size", "moe_forward_block", "moe_forward_block_host",
+                 "moe_test_gemm_timeout"]:
         assert want in names
 
 
@@ -104,6 +105,9 @@ def test_gemm_act_unpermute_validation(lib):
     assert g(GOOD, GOOD, GOOD, GOOD, GOOD, 64, 64, 64, 4, 2, GOOD, None, None) == INVALID
     assert g(GOOD, GOOD, GOOD, GOOD, GOOD, 64, 64, 64, 2048, 0, GOOD, None, None) == UNSUPPORTED
     assert g(ODD, GOOD, GOOD, GOOD, GOOD, 64, 64, 64, 4, 0, GOOD, None, None) == INVALID
+    tg = lib.moe_test_gemm_timeout
+    assert tg(GOOD, GOOD, GOOD, GOOD, GOOD, 64, 64, 64, 4, 0, GOOD, -1, None) == INVALID
+    assert tg(GOOD, GOOD, GOOD, GOOD, GOOD, 64, 48, 64, 4, 0, GOOD, 2, None) == INVALID
     a = lib.moe_act_quant
     assert a(GOOD, None, 10, 48, GOOD, GOOD, None) == INVALID
     assert a(None, None, 10, 64, GOOD, GOOD, None) == INVALID

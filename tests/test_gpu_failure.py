@@ -1,0 +1,54 @@
+"""Failure detection on the GPU without a fault: a GEMM pipeline wait that
+can never complete (one stage's bytes are never loaded) must give up after
+its bound, report MOE_DEV_PIPE_TIMEOUT through the device error word and
+leave the context usable for the next call."""
+import numpy as np
+import pytest
+import torch
+
+import moe_expert_layer_grouped_gb300 as moe
+import oracle
+
+from gpu_util import assert_parity, bf16_np, ragged_offsets, random_e4m3
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import __graft_entry__
+    __graft_entry__.build()
+    assert moe.moe_device_status() == moe.DEV_OK
+    yield
+
+
+def _problem(epi):
+    rng = np.random.default_rng(77 + epi)
+    counts, N, Kd = [20, 3, 0, 17, 9, 30, 1, 12], 256, 512   # few rows per expert: one CTA per tile
+    off = ragged_offsets(counts)
+    M = int(off[-1])
+    A = random_e4m3(rng, (M, Kd))
+    B = random_e4m3(rng, (len(counts), N, Kd))
+    sa = (10.0 ** rng.uniform(-3, 1, M)).astype(np.float32)
+    sb = (10.0 ** rng.uniform(-4, -2, (len(counts), N))).astype(np.float32)
+    return A, sa, B, sb, off
+
+
+@pytest.mark.parametrize("epi", [moe.EPI_BF16, moe.EPI_SILU_MUL])
+def test_gemm_wait_timeout_is_reported_and_context_survives(epi):
+    A, sa, B, sb, off = _problem(epi)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+    N = B.shape[1]
+    cols = N // 2 if epi == moe.EPI_SILU_MUL else N
+    C = torch.zeros((A.shape[0], cols), dtype=torch.bfloat16, device=DEV)
+    moe.moe_test_gemm_timeout(t(A), t(sa), t(B), t(sb), t(off), epi, C, stall_stage=2)
+    assert moe.moe_device_status() == moe.DEV_PIPE_TIMEOUT
+    assert moe.moe_device_status() == moe.DEV_OK        # reading clears it
+    # the same GEMM right after, on the same context, is correct
+    C2 = moe.moe_grouped_gemm(t(A), t(sa), t(B), t(sb), t(off), epi)
+    assert moe.moe_device_status() == moe.DEV_OK
+    ref = oracle.grouped_gemm(A, sa, B, sb, off)
+    if epi == moe.EPI_SILU_MUL:
+        ref = oracle.silu_mul(ref)
+    assert_parity(bf16_np(C2), ref, "gemm after a timeout")
