@@ -1,0 +1,132 @@
+"""The oracle's pins must catch plausible mistakes in the oracle.
+
+Each case plants one mistake in a copy of oracle/oracle.c (a dropped
+factor, a flipped tie-break, a wrong rounding, a transposed or shifted
+index, a swapped operand), builds that copy with the oracle's own flags,
+points the oracle module at it, and runs the pins that guard that part: at
+least one of them must fail. The real oracle source is never modified; the
+planted copy lives in pytest's temporary directory (CPU only).
+"""
+import os
+import shutil
+import subprocess
+
+import pytest
+
+import oracle
+import test_oracle_pins as pins
+from oracle import build as oracle_build
+
+GATE_CASES = pins._load_gate_cases()
+
+
+def _gate_handworked():
+    for case in GATE_CASES:
+        pins.test_gate_handworked(case)
+
+
+def _gate_bruteforce():
+    for args in [(8, 4, 2, 2), (16, 4, 2, 3), (12, 3, 2, 4), (16, 8, 3, 5)]:
+        pins.test_gate_bruteforce_enumeration(*args)
+
+
+# (name, text in oracle.c, planted replacement, pins expected to catch it)
+MUTATIONS = [
+    ("renormalised weights lose routed_scaling_factor",
+     "      for (int k = 0; k < K; ++k) w[k] = (s[ids[k]] / S) * rsf;",
+     "      for (int k = 0; k < K; ++k) w[k] = (s[ids[k]] / S);",
+     [_gate_handworked, pins.test_gate_weight_sum_is_rsf_and_linear]),
+    ("ties go to the higher index",
+     "  return (a->idx < b->idx) ? -1 : (a->idx > b->idx ? 1 : 0);",
+     "  return (a->idx > b->idx) ? -1 : (a->idx < b->idx ? 1 : 0);",
+     [_gate_handworked, _gate_bruteforce]),
+    ("group score from the best expert only",
+     "      gkv[g].key = (gsz >= 2) ? (b1 + b2) : b1;",
+     "      gkv[g].key = b1;",
+     [_gate_handworked, _gate_bruteforce]),
+    ("weights from the bias-corrected score",
+     "      s[e] = oracle_sigmoid32(l[e]);",
+     "      s[e] = oracle_sigmoid32(l[e]) + (bias ? bias[e] : 0.0f);",
+     [_gate_handworked, _gate_bruteforce]),
+    ("exp with a wrong 1/6! coefficient",
+     "  p = fmaf(p, r, 0x1.6c16c2p-10f);  /* 1/6! */",
+     "  p = fmaf(p, r, 0x1.6c16c2p-9f);  /* 1/6! */",
+     [pins.test_exp32_within_two_ulp, pins.test_sigmoid32_within_three_ulp]),
+    ("FP8 ties rounded away from zero",
+     "  float u = ldexpf(a, 3 - E);\n  int m = (int)rintf(u);",
+     "  float u = ldexpf(a, 3 - E);\n  int m = (int)roundf(u);",
+     [pins.test_e4m3_encode_specials_and_torch, pins.test_e4m3_encode_exhaustive_nearest_even]),
+    ("FP8 overflow to NaN instead of saturation",
+     "  if (a >= 448.0f) return (uint8_t)(sign | 0x7E);",
+     "  if (a >= 448.0f) return (uint8_t)(sign | 0x7F);",
+     [pins.test_e4m3_encode_specials_and_torch]),
+    ("bf16 by truncation",
+     "  b += 0x7FFFu + lsb;",
+     "  b += 0u * lsb;",
+     [pins.test_bf16_round_single_rounding]),
+    ("unstable order within an expert",
+     "    src2dst[i] = offsets[e] + fill[e];",
+     "    src2dst[i] = offsets[e + 1] - 1 - fill[e];",
+     [lambda: pins.test_route_invariants(37, 8, 2, False), pins.test_permute_quant_scatter]),
+    ("weight scale read with the row index",
+     "        c[n] = acc * (double)scale_a[r] * (double)scale_b[(int64_t)e * N + n];",
+     "        c[n] = acc * (double)scale_a[r] * (double)scale_b[(int64_t)e * N + (r % N)];",
+     [pins.test_grouped_gemm_scales_per_row_and_channel]),
+    ("gate and up halves swapped",
+     "      double g = C[r * 2 * I + j];\n      double u = C[r * 2 * I + I + j];",
+     "      double u = C[r * 2 * I + j];\n      double g = C[r * 2 * I + I + j];",
+     [pins.test_silu_mul_closed_forms]),
+    ("post-reorder uses slot 0's weight for every slot",
+     "      double w = (double)topk_w[(int64_t)t * K + k];",
+     "      double w = (double)topk_w[(int64_t)t * K];",
+     [pins.test_permute_then_unpermute_is_identity]),
+    ("shared experts weighted by routed_scaling_factor",
+     "        const uint8_t* W2e = w2 + (int64_t)e * H * I;\n        double wk = k < K ? (double)w[k] : 1.0;",
+     "        const uint8_t* W2e = w2 + (int64_t)e * H * I;\n"
+     "        double wk = k < K ? (double)w[k] : (double)routed_scaling_factor;",
+     [lambda: pins.test_layer_shared_experts_add_dense_mlps(1)]),
+    ("block amax carried across blocks",
+     "    for (int b = 0; b < nb; ++b) {\n      const uint16_t* blk = x + r * C + (int64_t)b * QB;\n"
+     "      float amax = 0.0f;",
+     "    float amax = 0.0f;\n    for (int b = 0; b < nb; ++b) {\n"
+     "      const uint16_t* blk = x + r * C + (int64_t)b * QB;",
+     [pins.test_block_quant_is_row_quant_per_block]),
+    ("block weight scale index transposed",
+     "          acc += part * (double)scale_a[(int64_t)r * KB + kb] *\n"
+     "                 (double)sbe[(int64_t)(n / QB) * KB + kb];",
+     "          acc += part * (double)scale_a[(int64_t)r * KB + kb] *\n"
+     "                 (double)sbe[(int64_t)kb * NBk + (n / QB)];",
+     [pins.test_grouped_gemm_block_exact_with_power_of_two_scales,
+      pins.test_grouped_gemm_block_with_uniform_scales_is_per_token_gemm]),
+]
+
+
+@pytest.fixture
+def planted(tmp_path, monkeypatch):
+    """Builds a copy of the oracle with one text replacement and makes the
+    oracle module load it (restored when the test ends)."""
+
+    def plant(old, new):
+        src = open(os.path.join(oracle_build.HERE, "oracle.c")).read()
+        assert src.count(old) == 1, "the planted site must exist exactly once"
+        (tmp_path / "oracle.c").write_text(src.replace(old, new))
+        shutil.copy(os.path.join(oracle_build.HERE, "oracle.h"), tmp_path / "oracle.h")
+        so = tmp_path / "liboracle_planted.so"
+        subprocess.run(["gcc", *oracle_build.CFLAGS, str(tmp_path / "oracle.c"), "-o", str(so),
+                        "-lm"], check=True)
+        monkeypatch.setattr(oracle_build, "build", lambda force=False: str(so))
+        monkeypatch.setattr(oracle, "_lib", None)
+
+    return plant
+
+
+@pytest.mark.parametrize("name,old,new,guards", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_planted_mistake_is_caught(planted, name, old, new, guards):
+    planted(old, new)
+    caught = []
+    for guard in guards:
+        try:
+            guard()
+        except AssertionError:
+            caught.append(getattr(guard, "__name__", "pin"))
+    assert caught, f"no pin caught: {name}"
