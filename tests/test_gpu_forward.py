@@ -128,6 +128,26 @@ def test_forward_shared_zero_and_host_buffers():
     assert not torch.equal(dev_out, a)
 
 
+@pytest.mark.parametrize("T,quant", [(48, "token"), (48, "block"), (1, "token")])
+def test_forward_maximum_sizes(T, quant):
+    """The largest arguments the library takes: E = 1024 experts, top-32 of
+    them (4 of 8 groups kept), hidden size 16384; every token against the oracle."""
+    wl = synth.Workload(f"max_{quant}", T, 16384, 128, 1024, 8, 4, 32, synth.SIGMOID, True, 2.5,
+                        "normal", quant=quant)
+    d = synth.make_inputs(wl, seed=11, device=DEV)
+    layer = moe.MoELayer(d["w13"], d["s13"], d["w2"], d["s2"], d["bias"], wl.num_groups,
+                         wl.topk_group, wl.top_k, wl.scoring, wl.renormalize, wl.rsf, wl.T,
+                         quant=quant)
+    out = layer(d["x"], d["logits"])
+    torch.cuda.synchronize()
+    assert moe.moe_device_status() == 0
+    n = synth.to_numpy_inputs(d)
+    fwd = oracle.forward_tokens_block if quant == "block" else oracle.forward_tokens
+    ref, _, _ = fwd(n["x"], n["logits"], n["bias"], n["w13"], n["s13"], n["w2"], n["s2"],
+                    wl.num_groups, wl.topk_group, wl.top_k, wl.scoring, wl.renormalize, wl.rsf)
+    assert_parity(bf16_np(out), ref, wl.name)
+
+
 def test_forward_rsf_linear_and_empty_batch():
     wl = synth.Workload("lin", 64, 256, 128, 16, 4, 2, 4, synth.SIGMOID, True, 1.0, "normal")
     d = {k: (None if v is None else v.to(DEV)) for k, v in synth.make_inputs(wl, 4).items()}
