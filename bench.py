@@ -318,6 +318,31 @@ def time_breakdown(moe, layer, wl, batches, steps, torch):
     return {n: tot[n] / steps for n in names}, offs
 
 
+def time_graph(layer, batches, steps, warmup, torch):
+    """Per-step time of graph replays of the forward (device time of the
+    replays only; each batch is copied into the graph's buffers first)."""
+    x = batches[0][0].clone()
+    lg = batches[0][1].clone()
+    out = torch.empty_like(x)
+    g = layer.capture(x, lg, out)
+    st = torch.cuda.current_stream()
+    for i in range(warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    total = 0.0
+    for i in range(steps):
+        xb, lb = batches[i % len(batches)]
+        x.copy_(xb)
+        lg.copy_(lb)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        g.replay()
+        e1.record(st)
+        e1.synchronize()
+        total += e0.elapsed_time(e1)
+    return total / steps
+
+
 def time_e2e(layer, batches, steps, warmup, torch):
     xs = [b[0].cpu().pin_memory() for b in batches]
     ls = [b[1].cpu().pin_memory() for b in batches]
@@ -449,6 +474,7 @@ def run_ours(args):
     value = job_tokens_per_s(wl.T, world, ms)
 
     e2e_ms, h2d, d2h = time_e2e(r["layer"], r["batches"], steps, warmup, torch)
+    graph_ms = time_graph(r["layer"], r["batches"], steps, warmup, torch)
     e2e_ms = max_over_ranks(e2e_ms, dist if world > 1 else None, dev)
 
     line = {
@@ -471,6 +497,9 @@ def run_ours(args):
         "roofline": roofline_decode(r, pk, wl.name) if wl.T <= 512 else roofline_prefill(r, pk),
         "e2e": {"value": round(job_tokens_per_s(wl.T, world, e2e_ms), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "graph": {"ms_per_step": round(graph_ms, 5),
+                  "note": "the same forward replayed from a CUDA graph (MoELayer.capture), "
+                          "inputs copied into its fixed buffers between steps, copies untimed"},
         "gpu_launches": steps * LAUNCHES_PER_FORWARD,
         "clocks": r["clocks"],
     }

@@ -481,6 +481,25 @@ class MoELayer:
                            self.renormalize, self.rsf, out=out, workspace=self.workspace,
                            stream=stream)
 
+    def capture(self, x, logits, out):
+        """Records one forward on the fixed device buffers x, logits and out
+        into a CUDA graph and returns it (torch.cuda.CUDAGraph); g.replay()
+        reruns the layer on whatever those buffers hold, launching the same
+        kernels without per-call host work. One eager call first, outside the
+        capture, does the per-device set-up (kernel attributes, TMA
+        descriptors, the device error word)."""
+        import torch
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            self(x, logits, out=out)
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self(x, logits, out=out)
+        return g
+
     def forward_host(self, x_host, logits_host, out_host, stream=None):
         if self.quant == "block":
             return moe_forward_block_host(x_host, logits_host, self.bias, self.w13, self.s13,

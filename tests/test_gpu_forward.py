@@ -148,6 +148,30 @@ def test_forward_maximum_sizes(T, quant):
     assert_parity(bf16_np(out), ref, wl.name)
 
 
+@pytest.mark.parametrize("name", ["dsv3_decode_t128", "dsv3_decode_t128_block",
+                                  "dsv3_decode_t128_shared"])
+def test_forward_cuda_graph_replay(name):
+    """A forward recorded into a CUDA graph, replayed on new inputs written
+    into the same buffers, gives the eager forward's output bit for bit."""
+    wl = synth.WORKLOADS[name]
+    d = synth.make_inputs(wl, seed=0, device=DEV)
+    layer = moe.MoELayer(d["w13"], d["s13"], d["w2"], d["s2"], d["bias"], wl.num_groups,
+                         wl.topk_group, wl.top_k, wl.scoring, wl.renormalize, wl.rsf, wl.T,
+                         n_shared=wl.n_shared, quant=wl.quant)
+    x, logits = d["x"].clone(), d["logits"].clone()
+    out = torch.empty_like(x)
+    g = layer.capture(x, logits, out)
+    for seed in (1, 2):
+        b = synth.make_inputs(wl, seed=seed, device=DEV, weights=False)
+        x.copy_(b["x"])
+        logits.copy_(b["logits"])
+        g.replay()
+        eager = layer(b["x"], b["logits"])
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int16), eager.view(torch.int16))
+    assert moe.moe_device_status() == 0
+
+
 def test_forward_rsf_linear_and_empty_batch():
     wl = synth.Workload("lin", 64, 256, 128, 16, 4, 2, 4, synth.SIGMOID, True, 1.0, "normal")
     d = {k: (None if v is None else v.to(DEV)) for k, v in synth.make_inputs(wl, 4).items()}
