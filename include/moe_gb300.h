@@ -236,11 +236,15 @@ MOE_API moe_status moe_forward(const void* x, const float* logits, const float* 
 
 /*
  * moe_forward_host — moe_forward with the per-step tensors in HOST memory:
- * copies x_host [T,H] bf16 and logits_host [T,E] f32 to the device (into
- * the workspace), runs the layer and copies the result to out_host [T,H]
- * bf16, all asynchronously on `stream` (use pinned host memory for true
- * asynchrony; the host buffers must stay valid until the stream reaches
- * the end of this call). Weights, scales and bias stay device pointers.
+ * x_host [T,H] bf16 and logits_host [T,E] f32 in, out_host [T,H] bf16 out,
+ * all asynchronously on `stream` (the host buffers must stay valid until the
+ * stream reaches the end of this call). When all three buffers are pinned
+ * and mapped into the device's address space (cudaHostAlloc, or torch's
+ * pin_memory, with unified addressing), the kernels read x and logits and
+ * write out in host memory directly over the host link; otherwise x and
+ * logits are copied into the workspace first and out is copied back (use
+ * pinned memory for asynchrony). Same results either way. Weights, scales
+ * and bias stay device pointers.
  */
 MOE_API moe_status moe_forward_host(const void* x_host, const float* logits_host,
                             const float* bias, const void* w13,

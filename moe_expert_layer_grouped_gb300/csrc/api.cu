@@ -358,7 +358,22 @@ moe_status forward_device(const void* x, const float* logits, const float* bias,
                      rsf, out, ws, static_cast<cudaStream_t>(stream), block);
 }
 
-// x, logits and out in host memory: copied through the workspace on `stream`.
+// The device address of a host buffer the GPU can read and write in place
+// (pinned and mapped into the device's address space), else nullptr.
+void* mapped_host_view(const void* host) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, host) != cudaSuccess) {
+    cudaGetLastError();  // not a CUDA-known pointer: clear the error
+    return nullptr;
+  }
+  if (a.type == cudaMemoryTypeHost && a.devicePointer != nullptr) return a.devicePointer;
+  return nullptr;
+}
+
+// x, logits and out in host memory. When all three are pinned and mapped,
+// the kernels read the inputs and write the output in host memory directly
+// (the bytes still cross the host link inside the call); otherwise they are
+// copied through the workspace on `stream`.
 moe_status forward_host(const void* x_host, const float* logits_host, const float* bias,
                         const void* w13, const float* s13, const void* w2, const float* s2,
                         int T, int H, int I, int E, int S, int G, int TG, int K, int scoring,
@@ -369,6 +384,15 @@ moe_status forward_host(const void* x_host, const float* logits_host, const floa
   if (ws == nullptr) return MOE_ERR_WORKSPACE;
   if (S < 0 || H < 1 || I < 1 || E < 1 || K < 1) return MOE_ERR_INVALID_ARG;
   if (block && (H % 128 != 0 || I % 128 != 0)) return MOE_ERR_INVALID_ARG;
+  if (T > 0) {
+    void* xv = mapped_host_view(x_host);
+    void* lv = mapped_host_view(logits_host);
+    void* ov = mapped_host_view(out_host);
+    if (xv != nullptr && lv != nullptr && ov != nullptr)
+      return forward_device(xv, static_cast<const float*>(lv), bias, w13, s13, w2, s2, T, H, I,
+                            E, S, G, TG, K, scoring, renorm, rsf, ov, ws, ws_bytes, stream,
+                            block);
+  }
   const FwdLayout L = fwd_layout(T < 0 ? 0 : T, H, I, E + S, K + S, block);
   void* x_d = at<void>(ws, L.x_in);
   float* l_d = at<float>(ws, L.logits_in);

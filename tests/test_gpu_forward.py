@@ -264,6 +264,18 @@ def test_forward_host_buffers_match_device_call():
     layer.forward_host(xh, lh, oh)
     torch.cuda.current_stream().synchronize()
     assert torch.equal(oh, ref)
+    # pinned buffers are read and written in place by the kernels; pageable
+    # ones (and a mix) go through staging copies: the same result every way
+    for pinned in [(False, False, False), (True, False, True), (False, True, True)]:
+        xs = d["x"].cpu().pin_memory() if pinned[0] else d["x"].cpu().clone()
+        ls = d["logits"].cpu().pin_memory() if pinned[1] else d["logits"].cpu().clone()
+        os_ = torch.zeros((wl.T, wl.H), dtype=torch.bfloat16)
+        if pinned[2]:
+            os_ = os_.pin_memory()
+        layer.forward_host(xs, ls, os_)
+        torch.cuda.current_stream().synchronize()
+        assert torch.equal(os_, ref), pinned
+    assert moe.moe_device_status() == 0
 
 
 def test_repeated_calls_are_deterministic():
