@@ -32,7 +32,12 @@ SECONDARY_WORKLOAD = "dsv3_prefill_t8192"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 FP8_PER_BF16 = 2.0  # nominal dense FP8 : bf16 tensor throughput
-LAUNCHES_PER_FORWARD = 8  # gate, 3x pre-reorder, w13 GEMM, requant, w2 GEMM, post-reorder
+def launches_per_forward(wl):
+    """Kernels one forward launches: gate, pre-reorder (one launch for T <= 512
+    and T*K <= 4096 slots, else three), w13 GEMM, requant, w2 GEMM, post-reorder."""
+    k = wl.top_k + wl.n_shared
+    pre = 1 if (wl.T <= 512 and wl.T * k <= 4096) else 3
+    return 5 + pre
 N_BATCHES = 4  # distinct token batches cycled through the timed steps
 
 
@@ -500,7 +505,7 @@ def run_ours(args):
         "graph": {"ms_per_step": round(graph_ms, 5),
                   "note": "the same forward replayed from a CUDA graph (MoELayer.capture), "
                           "inputs copied into its fixed buffers between steps, copies untimed"},
-        "gpu_launches": steps * LAUNCHES_PER_FORWARD,
+        "gpu_launches": steps * launches_per_forward(wl),
         "clocks": r["clocks"],
     }
     if not args.no_secondary and rank == 0 and world == 1:

@@ -3,7 +3,9 @@
 // Changes / Changelog / Code Review; expert row ranges from "Fix one bug in
 // the grouped-gemm triton kernel", sglang #6772, Highlights).
 //
-// Three launches, all deterministic (no atomics whose order matters):
+// Batches with T <= 512 and T*K <= 4096 take one launch
+// (permute_quant_small_kernel, below),
+// larger ones three, all deterministic (no atomics whose order matters):
 //  1. route_bits: for every block of 32 tokens c and expert e, a 32-bit mask
 //     of the tokens in the block that chose e (bits[c][e]).
 //  2. route_scan (one CTA): per expert, the running token count before each
@@ -118,31 +120,16 @@ __global__ void __launch_bounds__(1024)
 
 constexpr int kQuantThreads = 128;
 
-// BLOCK: one scale per 128 channels (scale_a [M, H/128]) instead of one per
-// token. A 128-channel block is 16 vectors, held by the 16 lanes of a
-// half-warp (vector tid + i*128 lies in block tid/16 + 8i), so its amax is a
-// 16-lane shuffle reduction.
-template <int VPT, bool BLOCK>  // VPT: 16-byte vectors (8 bf16) per thread
-__global__ void __launch_bounds__(kQuantThreads)
-    permute_quant_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ ids,
-                         const uint32_t* __restrict__ bits, const int32_t* __restrict__ base,
-                         int H, int E, int K, uint8_t* __restrict__ a_q,
-                         float* __restrict__ scale_a, int32_t* __restrict__ src2dst) {
-  __shared__ int dst[32];
-  __shared__ float red[kQuantThreads / 32];
-  const int t = blockIdx.x;
+// Loads token t's row once (128-bit vectors, kept in registers), reduces its
+// amax (per row, or per 128 channels when BLOCK), quantises it and stores the
+// codes and scale to every destination row dst[0..K) >= 0. dst[] is written
+// by threads 0..K-1 before the call; it is read only after a block barrier.
+template <int VPT, bool BLOCK>
+__device__ __forceinline__ void quant_scatter(const __nv_bfloat16* __restrict__ x, int t, int H,
+                                              int K, const int* dst, float* red,
+                                              uint8_t* __restrict__ a_q,
+                                              float* __restrict__ scale_a) {
   const int tid = threadIdx.x;
-  if (tid < K) {
-    const int e = __ldg(ids + (int64_t)t * K + tid);
-    int d = -1;
-    if ((unsigned)e < (unsigned)E) {
-      const int64_t i = (int64_t)(t >> 5) * E + e;
-      const uint32_t below = __ldg(bits + i) & ((1u << (t & 31)) - 1u);
-      d = __ldg(base + i) + __popc(below);
-    }
-    dst[tid] = d;
-    src2dst[(int64_t)t * K + tid] = d;
-  }
   const int nvec = H >> 3;
   const uint4* xr = reinterpret_cast<const uint4*>(x + (int64_t)t * H);
   uint4 v[VPT];
@@ -207,6 +194,151 @@ __global__ void __launch_bounds__(kQuantThreads)
   }
 }
 
+// BLOCK: one scale per 128 channels (scale_a [M, H/128]) instead of one per
+// token. A 128-channel block is 16 vectors, held by the 16 lanes of a
+// half-warp (vector tid + i*128 lies in block tid/16 + 8i), so its amax is a
+// 16-lane shuffle reduction.
+template <int VPT, bool BLOCK>  // VPT: 16-byte vectors (8 bf16) per thread
+__global__ void __launch_bounds__(kQuantThreads)
+    permute_quant_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ ids,
+                         const uint32_t* __restrict__ bits, const int32_t* __restrict__ base,
+                         int H, int E, int K, uint8_t* __restrict__ a_q,
+                         float* __restrict__ scale_a, int32_t* __restrict__ src2dst) {
+  __shared__ int dst[32];
+  __shared__ float red[kQuantThreads / 32];
+  const int t = blockIdx.x;
+  const int tid = threadIdx.x;
+  if (tid < K) {
+    const int e = __ldg(ids + (int64_t)t * K + tid);
+    int d = -1;
+    if ((unsigned)e < (unsigned)E) {
+      const int64_t i = (int64_t)(t >> 5) * E + e;
+      const uint32_t below = __ldg(bits + i) & ((1u << (t & 31)) - 1u);
+      d = __ldg(base + i) + __popc(below);
+    }
+    dst[tid] = d;
+    src2dst[(int64_t)t * K + tid] = d;
+  }
+  quant_scatter<VPT, BLOCK>(x, t, H, K, dst, red, a_q, scale_a);
+}
+
+// Small batches (T <= 512, T*K <= 4096): one launch does the routing and the
+// quantisation. Every CTA (one per token) loads the whole batch's ids into
+// shared memory, histograms them per expert and scans the histogram (the
+// same offsets in every CTA; CTA 0 stores them), then ranks its own K slots
+// among the earlier tokens' -- the stable counting sort of the three-launch
+// path, with the same handling of bad ids: an id out of range gets
+// destination -1, an id repeated within a token counts once and its repeats
+// share the first one's row, and either raises MOE_DEV_BAD_EXPERT_ID.
+constexpr int kSmallRoute = 4096;
+constexpr int kSmallTokens = 512;  // every CTA re-reads all T*K ids: keep T small
+
+template <int VPT, bool BLOCK>
+__global__ void __launch_bounds__(kQuantThreads)
+    permute_quant_small_kernel(const __nv_bfloat16* __restrict__ x,
+                               const int32_t* __restrict__ ids, int T, int H, int E, int K,
+                               uint8_t* __restrict__ a_q, float* __restrict__ scale_a,
+                               int32_t* __restrict__ src2dst, int32_t* __restrict__ offsets,
+                               int* err) {
+  extern __shared__ int route_smem[];
+  __shared__ int dst[32];
+  __shared__ float red[kQuantThreads / 32];
+  __shared__ int wpart[kQuantThreads / 32];
+  const int n = T * K;
+  int* raw = route_smem;    // [n] the ids as given
+  int* s_ids = raw + n;     // [n] per slot: e (counts), E + e (a repeat of e), -1 (out of range)
+  int* cnt = s_ids + n;     // [E]
+  int* off = cnt + E;       // [E + 1]
+  const int t = blockIdx.x;
+  const int tid = threadIdx.x;
+  const int lane = tid & 31, warp = tid >> 5;
+  for (int i = tid; i < n; i += kQuantThreads) raw[i] = __ldg(ids + i);
+  for (int e = tid; e < E; e += kQuantThreads) cnt[e] = 0;
+  __syncthreads();
+  int bad = 0;
+  for (int i = tid; i < n; i += kQuantThreads) {
+    const int e = raw[i];
+    int v = -1;
+    if ((unsigned)e < (unsigned)E) {
+      v = e;
+      for (int j = i - i % K; j < i; ++j)
+        if (raw[j] == e) v = E + e;
+    }
+    bad |= (v < 0 || v >= E);
+    s_ids[i] = v;
+  }
+  bad = __syncthreads_or(bad);
+  if (bad && t == 0 && tid == 0) flag_error(err, MOE_DEV_BAD_EXPERT_ID);
+  for (int i = tid; i < n; i += kQuantThreads) {
+    const int v = s_ids[i];
+    if ((unsigned)v < (unsigned)E) atomicAdd(&cnt[v], 1);  // counts: order-free
+  }
+  __syncthreads();
+  // exclusive scan of cnt over the block: ceil(E/128) consecutive experts per thread
+  const int per = (E + kQuantThreads - 1) / kQuantThreads;
+  const int e0 = min(E, tid * per), e1 = min(E, e0 + per);
+  int local = 0;
+  for (int e = e0; e < e1; ++e) local += cnt[e];
+  int incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(kFull, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) wpart[warp] = incl;
+  __syncthreads();
+  int run = incl - local;
+  for (int w = 0; w < warp; ++w) run += wpart[w];
+  for (int e = e0; e < e1; ++e) {
+    off[e] = run;
+    run += cnt[e];
+  }
+  if (tid == kQuantThreads - 1) off[E] = run;
+  __syncthreads();
+  if (t == 0)
+    for (int e = tid; e <= E; e += kQuantThreads) offsets[e] = off[e];
+  // this token's slots: the rank of each of its experts among the earlier
+  // tokens, by one pass over their slots with the token's experts marked in
+  // a per-expert table (cnt[] is free again)
+  const int prev = t * K;
+  int* slot_of = cnt;
+  __shared__ int rank[32];
+  for (int e = tid; e < E; e += kQuantThreads) slot_of[e] = -1;
+  if (tid < 32) rank[tid] = 0;
+  __syncthreads();
+  if (tid < K) {
+    const int v = s_ids[prev + tid];
+    if ((unsigned)v < (unsigned)E) slot_of[v] = tid;  // first occurrences are distinct
+  }
+  __syncthreads();
+  for (int i = tid; i < prev; i += kQuantThreads) {
+    const int v = s_ids[i];
+    if ((unsigned)v < (unsigned)E) {
+      const int k = slot_of[v];
+      if (k >= 0) atomicAdd(&rank[k], 1);  // counts: order-free
+    }
+  }
+  __syncthreads();
+  if (tid < K) {
+    const int v = s_ids[prev + tid];
+    const int e = v >= E ? v - E : v;  // a repeat shares its expert's row
+    const int d = v >= 0 ? off[e] + rank[slot_of[e]] : -1;
+    dst[tid] = d;
+    src2dst[(int64_t)t * K + tid] = d;
+  }
+  quant_scatter<VPT, BLOCK>(x, t, H, K, dst, red, a_q, scale_a);
+}
+
+template <int VPT, bool BLOCK>
+void launch_small(const void* x, const int32_t* ids, int T, int H, int E, int K, void* a_q,
+                  float* scale_a, int32_t* src2dst, int32_t* offsets, int* err,
+                  cudaStream_t st) {
+  const size_t smem = sizeof(int) * (2 * (size_t)T * K + 2 * (size_t)E + 1);
+  permute_quant_small_kernel<VPT, BLOCK><<<T, kQuantThreads, smem, st>>>(
+      reinterpret_cast<const __nv_bfloat16*>(x), ids, T, H, E, K,
+      reinterpret_cast<uint8_t*>(a_q), scale_a, src2dst, offsets, err);
+}
+
 template <int VPT, bool BLOCK>
 void launch_quant(const void* x, const int32_t* ids, const uint32_t* bits, const int32_t* base,
                   int T, int H, int E, int K, void* a_q, float* scale_a, int32_t* src2dst,
@@ -250,6 +382,15 @@ template <bool BLOCK>
 cudaError_t permute_quant(const void* x, const int32_t* ids, int T, int H, int E, int K,
                           void* a_q, float* scale_a, int32_t* src2dst, int32_t* offsets,
                           void* ws, int* err, cudaStream_t st) {
+  if (T > 0 && T <= kSmallTokens && T * K <= kSmallRoute) {
+    const int vpt = (H / 8 + kQuantThreads - 1) / kQuantThreads;
+    if (vpt <= 1) launch_small<1, BLOCK>(x, ids, T, H, E, K, a_q, scale_a, src2dst, offsets, err, st);
+    else if (vpt <= 2) launch_small<2, BLOCK>(x, ids, T, H, E, K, a_q, scale_a, src2dst, offsets, err, st);
+    else if (vpt <= 4) launch_small<4, BLOCK>(x, ids, T, H, E, K, a_q, scale_a, src2dst, offsets, err, st);
+    else if (vpt <= 8) launch_small<8, BLOCK>(x, ids, T, H, E, K, a_q, scale_a, src2dst, offsets, err, st);
+    else launch_small<16, BLOCK>(x, ids, T, H, E, K, a_q, scale_a, src2dst, offsets, err, st);
+    return cudaGetLastError();
+  }
   const int C = (T + 31) / 32;
   uint32_t* bits = reinterpret_cast<uint32_t*>(ws);
   int32_t* base = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(ws) +

@@ -92,7 +92,10 @@ def _ids(rng, T, E, K, hot=None):
 
 @pytest.mark.parametrize("T,H,E,K,hot", [(1, 32, 4, 1, None), (37, 128, 8, 2, None),
                                          (300, 7168, 256, 8, None), (1000, 4096, 8, 2, None),
-                                         (2049, 256, 64, 6, 10), (70, 16384, 3, 3, None)])
+                                         (2049, 256, 64, 6, 10), (70, 16384, 3, 3, None),
+                                         # the one-launch path ends at T*K = 4096
+                                         (512, 512, 1024, 8, 40), (513, 512, 1024, 8, 40),
+                                         (128, 7168, 256, 8, 60), (4096, 256, 16, 1, None)])
 def test_permute_quant_bit_exact(T, H, E, K, hot):
     rng = np.random.default_rng(T + H)
     ids = _ids(rng, T, E, K, hot)
@@ -120,6 +123,44 @@ def test_permute_empty_and_bad_ids():
     moe.moe_permute_quant(x, bad, E)
     assert moe.moe_device_status() == 1
     assert moe.moe_device_status() == 0  # cleared
+
+
+@pytest.mark.parametrize("T", [64, 1200])   # the one-launch and the three-launch routing
+def test_permute_bad_ids_same_on_both_paths(T):
+    """Out-of-range ids get destination -1, an id repeated within a token
+    counts once and shares its first occurrence's row, both raise the device
+    error; the rest is the stable counting sort (checked against a plain
+    numpy restatement of that rule)."""
+    rng = np.random.default_rng(T)
+    E, K, H = 16, 4, 128
+    ids = _ids(rng, T, E, K)
+    ids[3, 2] = 99            # out of range
+    ids[5, 3] = ids[5, 1]     # repeat within the token
+    ids[T - 1, 0] = -7
+    x = torch.randn((T, H), dtype=torch.bfloat16, device=DEV)
+    a_q, sa, s2d, off = moe.moe_permute_quant(x, torch.from_numpy(ids).to(DEV), E)
+    assert moe.moe_device_status() == 1
+    cnt = np.zeros(E, np.int64)
+    first = np.full((T, K), -1)
+    for t in range(T):
+        for k in range(K):
+            e = ids[t, k]
+            if 0 <= e < E and e not in ids[t, :k]:
+                first[t, k] = e
+    for e in first[first >= 0]:
+        cnt[e] += 1
+    ref_off = np.concatenate([[0], np.cumsum(cnt)])
+    assert np.array_equal(off.cpu().numpy(), ref_off)
+    seen = np.zeros(E, np.int64)
+    ref = np.full((T, K), -1)
+    for t in range(T):
+        for k in range(K):
+            e = ids[t, k]
+            if 0 <= e < E:
+                ref[t, k] = ref_off[e] + seen[e]
+        for e in set(first[t][first[t] >= 0]):
+            seen[e] += 1
+    assert np.array_equal(s2d.cpu().numpy().reshape(T, K), ref)
 
 
 def test_fp8_encoder_matches_oracle_on_every_bf16():
