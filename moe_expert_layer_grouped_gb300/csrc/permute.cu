@@ -124,7 +124,7 @@ constexpr int kQuantThreads = 128;
 // amax (per row, or per 128 channels when BLOCK), quantises it and stores the
 // codes and scale to every destination row dst[0..K) >= 0. dst[] is written
 // by threads 0..K-1 before the call; it is read only after a block barrier.
-template <int VPT, bool BLOCK>
+template <int VPT, bool BLOCK, int NT = kQuantThreads>
 __device__ __forceinline__ void quant_scatter(const __nv_bfloat16* __restrict__ x, int t, int H,
                                               int K, const int* dst, float* red,
                                               uint8_t* __restrict__ a_q,
@@ -136,7 +136,7 @@ __device__ __forceinline__ void quant_scatter(const __nv_bfloat16* __restrict__ 
   float amax = 0.0f;
 #pragma unroll
   for (int i = 0; i < VPT; ++i) {
-    const int idx = tid + i * kQuantThreads;
+    const int idx = tid + i * NT;
     if (idx < nvec) {
       v[i] = __ldg(xr + idx);
       float f[8];
@@ -149,7 +149,7 @@ __device__ __forceinline__ void quant_scatter(const __nv_bfloat16* __restrict__ 
     const int nb = H >> 7;
 #pragma unroll
     for (int i = 0; i < VPT; ++i) {
-      const int idx = tid + i * kQuantThreads;
+      const int idx = tid + i * NT;
       float f[8];
       float m = 0.0f;
       if (idx < nvec) {
@@ -176,12 +176,12 @@ __device__ __forceinline__ void quant_scatter(const __nv_bfloat16* __restrict__ 
   __syncthreads();
   amax = red[0];
 #pragma unroll
-  for (int w = 1; w < kQuantThreads / 32; ++w) amax = fmaxf(amax, red[w]);
+  for (int w = 1; w < NT / 32; ++w) amax = fmaxf(amax, red[w]);
   const float sc = token_scale(amax);
   if (tid < K && dst[tid] >= 0) scale_a[dst[tid]] = sc;
 #pragma unroll
   for (int i = 0; i < VPT; ++i) {
-    const int idx = tid + i * kQuantThreads;
+    const int idx = tid + i * NT;
     if (idx < nvec) {
       float f[8];
       bf16x8_to_f32(v[i], f);
@@ -232,9 +232,13 @@ __global__ void __launch_bounds__(kQuantThreads)
 // share the first one's row, and either raises MOE_DEV_BAD_EXPERT_ID.
 constexpr int kSmallRoute = 4096;
 constexpr int kSmallTokens = 512;  // every CTA re-reads all T*K ids: keep T small
+#ifndef SMALL_THREADS
+#define SMALL_THREADS 512
+#endif
+constexpr int kSmallThreads = SMALL_THREADS;  // more warps per token than the large path
 
 template <int VPT, bool BLOCK>
-__global__ void __launch_bounds__(kQuantThreads)
+__global__ void __launch_bounds__(kSmallThreads)
     permute_quant_small_kernel(const __nv_bfloat16* __restrict__ x,
                                const int32_t* __restrict__ ids, int T, int H, int E, int K,
                                uint8_t* __restrict__ a_q, float* __restrict__ scale_a,
@@ -242,8 +246,8 @@ __global__ void __launch_bounds__(kQuantThreads)
                                int* err) {
   extern __shared__ int route_smem[];
   __shared__ int dst[32];
-  __shared__ float red[kQuantThreads / 32];
-  __shared__ int wpart[kQuantThreads / 32];
+  __shared__ float red[kSmallThreads / 32];
+  __shared__ int wpart[kSmallThreads / 32];
   const int n = T * K;
   int* raw = route_smem;    // [n] the ids as given
   int* s_ids = raw + n;     // [n] per slot: e (counts), E + e (a repeat of e), -1 (out of range)
@@ -252,11 +256,11 @@ __global__ void __launch_bounds__(kQuantThreads)
   const int t = blockIdx.x;
   const int tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
-  for (int i = tid; i < n; i += kQuantThreads) raw[i] = __ldg(ids + i);
-  for (int e = tid; e < E; e += kQuantThreads) cnt[e] = 0;
+  for (int i = tid; i < n; i += kSmallThreads) raw[i] = __ldg(ids + i);
+  for (int e = tid; e < E; e += kSmallThreads) cnt[e] = 0;
   __syncthreads();
   int bad = 0;
-  for (int i = tid; i < n; i += kQuantThreads) {
+  for (int i = tid; i < n; i += kSmallThreads) {
     const int e = raw[i];
     int v = -1;
     if ((unsigned)e < (unsigned)E) {
@@ -269,13 +273,13 @@ __global__ void __launch_bounds__(kQuantThreads)
   }
   bad = __syncthreads_or(bad);
   if (bad && t == 0 && tid == 0) flag_error(err, MOE_DEV_BAD_EXPERT_ID);
-  for (int i = tid; i < n; i += kQuantThreads) {
+  for (int i = tid; i < n; i += kSmallThreads) {
     const int v = s_ids[i];
     if ((unsigned)v < (unsigned)E) atomicAdd(&cnt[v], 1);  // counts: order-free
   }
   __syncthreads();
   // exclusive scan of cnt over the block: ceil(E/128) consecutive experts per thread
-  const int per = (E + kQuantThreads - 1) / kQuantThreads;
+  const int per = (E + kSmallThreads - 1) / kSmallThreads;
   const int e0 = min(E, tid * per), e1 = min(E, e0 + per);
   int local = 0;
   for (int e = e0; e < e1; ++e) local += cnt[e];
@@ -293,17 +297,17 @@ __global__ void __launch_bounds__(kQuantThreads)
     off[e] = run;
     run += cnt[e];
   }
-  if (tid == kQuantThreads - 1) off[E] = run;
+  if (tid == kSmallThreads - 1) off[E] = run;
   __syncthreads();
   if (t == 0)
-    for (int e = tid; e <= E; e += kQuantThreads) offsets[e] = off[e];
+    for (int e = tid; e <= E; e += kSmallThreads) offsets[e] = off[e];
   // this token's slots: the rank of each of its experts among the earlier
   // tokens, by one pass over their slots with the token's experts marked in
   // a per-expert table (cnt[] is free again)
   const int prev = t * K;
   int* slot_of = cnt;
   __shared__ int rank[32];
-  for (int e = tid; e < E; e += kQuantThreads) slot_of[e] = -1;
+  for (int e = tid; e < E; e += kSmallThreads) slot_of[e] = -1;
   if (tid < 32) rank[tid] = 0;
   __syncthreads();
   if (tid < K) {
@@ -311,7 +315,7 @@ __global__ void __launch_bounds__(kQuantThreads)
     if ((unsigned)v < (unsigned)E) slot_of[v] = tid;  // first occurrences are distinct
   }
   __syncthreads();
-  for (int i = tid; i < prev; i += kQuantThreads) {
+  for (int i = tid; i < prev; i += kSmallThreads) {
     const int v = s_ids[i];
     if ((unsigned)v < (unsigned)E) {
       const int k = slot_of[v];
@@ -326,7 +330,7 @@ __global__ void __launch_bounds__(kQuantThreads)
     dst[tid] = d;
     src2dst[(int64_t)t * K + tid] = d;
   }
-  quant_scatter<VPT, BLOCK>(x, t, H, K, dst, red, a_q, scale_a);
+  quant_scatter<VPT, BLOCK, kSmallThreads>(x, t, H, K, dst, red, a_q, scale_a);
 }
 
 template <int VPT, bool BLOCK>
@@ -334,7 +338,7 @@ void launch_small(const void* x, const int32_t* ids, int T, int H, int E, int K,
                   float* scale_a, int32_t* src2dst, int32_t* offsets, int* err,
                   cudaStream_t st) {
   const size_t smem = sizeof(int) * (2 * (size_t)T * K + 2 * (size_t)E + 1);
-  permute_quant_small_kernel<VPT, BLOCK><<<T, kQuantThreads, smem, st>>>(
+  permute_quant_small_kernel<VPT, BLOCK><<<T, kSmallThreads, smem, st>>>(
       reinterpret_cast<const __nv_bfloat16*>(x), ids, T, H, E, K,
       reinterpret_cast<uint8_t*>(a_q), scale_a, src2dst, offsets, err);
 }
@@ -383,7 +387,7 @@ cudaError_t permute_quant(const void* x, const int32_t* ids, int T, int H, int E
                           void* a_q, float* scale_a, int32_t* src2dst, int32_t* offsets,
                           void* ws, int* err, cudaStream_t st) {
   if (T > 0 && T <= kSmallTokens && T * K <= kSmallRoute) {
-    const int vpt = (H / 8 + kQuantThreads - 1) / kQuantThreads;
+    const int vpt = (H / 8 + kSmallThreads - 1) / kSmallThreads;
     if (vpt <= 1) launch_small<1, BLOCK>(x, ids, T, H, E, K, a_q, scale_a, src2dst, offsets, err, st);
     else if (vpt <= 2) launch_small<2, BLOCK>(x, ids, T, H, E, K, a_q, scale_a, src2dst, offsets, err, st);
     else if (vpt <= 4) launch_small<4, BLOCK>(x, ids, T, H, E, K, a_q, scale_a, src2dst, offsets, err, st);

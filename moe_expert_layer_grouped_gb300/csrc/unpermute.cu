@@ -2,9 +2,9 @@
 // down[src2dst[t*K+k]] accumulated in fp32 in slot order (the role of
 // moe_sum_reduce in "[1/2] sgl-kernel: Fuse routed scaling factor into
 // select_experts", sglang #8364, Motivation; routed_scaling_factor is
-// already inside w). CTAs of 128 threads take one token and a slice of 2048
-// columns (so small batches still spread over the SMs); 128-bit gathers of
-// the K rows.
+// already inside w). CTAs of 128 threads take one token and a slice of 1024
+// columns, one 16-byte vector per thread (so small batches still spread over
+// the SMs); 128-bit gathers of the K rows.
 #include "common.cuh"
 #include "internal.h"
 
@@ -12,7 +12,7 @@ namespace moe {
 namespace {
 
 constexpr int kThreads = 128;
-constexpr int kVecPerBlock = 256;  // 16-byte vectors (2048 bf16) per CTA
+constexpr int kVecPerBlock = 128;  // 16-byte vectors (1024 bf16) per CTA: one per thread
 
 __global__ void __launch_bounds__(kThreads)
     unpermute_kernel(const __nv_bfloat16* __restrict__ down, const int32_t* __restrict__ src2dst,
