@@ -163,7 +163,12 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (warp == 0) {
     // ======================= TMA producer ===================================
     if (lane == 0) {
+      // weights: evict-first when a block is read once (every block when
+      // streaming; otherwise the blocks of experts whose tokens fit one
+      // chunk), so they do not push the token tiles, read once per weight
+      // block group, out of L2
       const uint64_t pol_w = p.stream_weights ? ptx::policy_evict_first() : ptx::policy_evict_normal();
+      const uint64_t pol_w1 = ptx::policy_evict_first();
       const uint64_t pol_x = ptx::policy_evict_last();
       uint32_t s = 0, ph = 0;
       int gstage = 0;  // stages issued by this CTA
@@ -205,8 +210,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             uint8_t* wdst = sm.w[s][kc];
             uint8_t* xdst = sm.x[s][kc];
             if (PAIR) {
-              ptx::tma_load_2d_pair(wdst, &maps.w, fb, kx, y0, pol_w);
-              ptx::tma_load_2d_pair(wdst + 64 * BK, &maps.w, fb, kx, y1, pol_w);
+              const uint64_t pw = t.nch == 1 ? pol_w1 : pol_w;
+              ptx::tma_load_2d_pair(wdst, &maps.w, fb, kx, y0, pw);
+              ptx::tma_load_2d_pair(wdst + 64 * BK, &maps.w, fb, kx, y1, pw);
               int r = 0;
 #pragma unroll
               for (int i = 0; i < NXBOX; ++i) {
@@ -218,8 +224,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
               }
             } else {
-              ptx::tma_load_2d(wdst, &maps.w, &sm.full[s], kx, y0, pol_w);
-              ptx::tma_load_2d(wdst + 64 * BK, &maps.w, &sm.full[s], kx, y1, pol_w);
+              const uint64_t pw = t.nch == 1 ? pol_w1 : pol_w;
+              ptx::tma_load_2d(wdst, &maps.w, &sm.full[s], kx, y0, pw);
+              ptx::tma_load_2d(wdst + 64 * BK, &maps.w, &sm.full[s], kx, y1, pw);
               int r = 0;
 #pragma unroll
               for (int i = 0; i < NXBOX; ++i) {

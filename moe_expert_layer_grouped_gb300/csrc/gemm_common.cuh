@@ -38,6 +38,7 @@ struct Maps {
 template <int BNMAX>
 struct TileInfo {
   int e, nb, tok0, ntok;
+  int nch;  // token chunks of the expert (1: the weight block is read by this tile only)
 };
 
 // tile -> (expert, weight block, token chunk)
@@ -54,6 +55,7 @@ __device__ __forceinline__ TileInfo<BNMAX> decode_tile(const S& sm, int E, int N
   const int local = tile - sm.tile_start[lo];
   const int nch = (sm.tile_start[lo + 1] - sm.tile_start[lo]) / NB;
   t.nb = local / nch;
+  t.nch = nch;
   const int tc = local - t.nb * nch;
   // equal chunks (multiples of 16 tokens) so the tiles that share a weight
   // block run at the same speed and meet it in L2
