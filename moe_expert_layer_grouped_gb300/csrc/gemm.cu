@@ -623,13 +623,14 @@ cudaError_t launch_grouped_gemm(const void* A, const float* scale_a, const void*
   p.NB = silu ? (p.I + 63) / 64 : (N + BM - 1) / BM;
   p.KB = (Kd + BK - 1) / BK;
   p.stream_weights = 0;
-  // few rows per expert (decode): small token tiles and a deep weight ring,
-  // weights streamed once; many (prefill): tiles of up to 256 tokens
+  // few rows per expert (decode): small token tiles, weights streamed once
+  // through 4 stages of two 128-byte K chunks (256 contiguous bytes of each
+  // weight row per stage); many (prefill): tiles of up to 256 tokens
   p.stream_weights = small ? 1 : 0;
   p.stall_stage = stall_stage;
   if (small)
-    return silu ? launch_cfg<64, 8, true, 1, 1>(maps, p, M, E, st)
-                : launch_cfg<64, 8, false, 1, 1>(maps, p, M, E, st);
+    return silu ? launch_cfg<64, 4, true, 1, 2>(maps, p, M, E, st)
+                : launch_cfg<64, 4, false, 1, 2>(maps, p, M, E, st);
   // many tokens per expert: CTA pairs on pairs of weight blocks (2-SM MMA),
   // 3 stages of 2 x (16 KB weights + 16 KB tokens) per CTA
   if (p.NB % 2 == 0)

@@ -25,7 +25,9 @@ def built():
 
 def _problem(epi):
     rng = np.random.default_rng(77 + epi)
-    counts, N, Kd = [20, 3, 0, 17, 9, 30, 1, 12], 256, 512   # few rows per expert: one CTA per tile
+    # few rows per expert: one CTA per tile; K = 1024 gives every tile several
+    # pipeline stages whatever their depth in K
+    counts, N, Kd = [20, 3, 0, 17, 9, 30, 1, 12], 256, 1024
     off = ragged_offsets(counts)
     M = int(off[-1])
     A = random_e4m3(rng, (M, Kd))
@@ -42,7 +44,7 @@ def test_gemm_wait_timeout_is_reported_and_context_survives(epi):
     N = B.shape[1]
     cols = N // 2 if epi == moe.EPI_SILU_MUL else N
     C = torch.zeros((A.shape[0], cols), dtype=torch.bfloat16, device=DEV)
-    moe.moe_test_gemm_timeout(t(A), t(sa), t(B), t(sb), t(off), epi, C, stall_stage=2)
+    moe.moe_test_gemm_timeout(t(A), t(sa), t(B), t(sb), t(off), epi, C, stall_stage=1)
     assert moe.moe_device_status() == moe.DEV_PIPE_TIMEOUT
     assert moe.moe_device_status() == moe.DEV_OK        # reading clears it
     # the same GEMM right after, on the same context, is correct
