@@ -11,12 +11,12 @@
 // expert's token count is padded to a multiple of 16 rather than of 128.
 //
 // Design (one persistent CTA per SM, 192 threads, warp-specialised):
-//   warp 0      TMA producer: per stage the 128 weight rows (one 128-row box,
-//               or for SiLU two 64-row boxes, 128 B of K each) and the tile's
-//               tokens (rounded up to 16, covered exactly by boxes of
-//               256/128/64/32/16 rows) into a STAGES-deep ring, 128-byte
-//               swizzled; weights streamed evict-first when each weight
-//               block is read once, tokens kept with evict-last.
+//   warp 0      TMA producer: per stage KC chunks of 128 B of K, each the
+//               128 weight rows (two 64-row boxes: for SiLU the gate and the
+//               up rows) and the tile's tokens (rounded up to 16, covered
+//               exactly by boxes of 64/32/16 rows), into a STAGES-deep ring,
+//               128-byte swizzled; weight blocks read by one tile only are
+//               loaded evict-first, tokens evict-last.
 //   warp 1      MMA issuer: tcgen05.mma.cta_group::1.kind::f8f6f4,
 //               M=128 x N x K=32, fp32 accumulator in tensor memory; two
 //               accumulators (2 x 256 columns) so the epilogue of tile i
@@ -36,6 +36,10 @@
 // and share it through L2. The tile table is derived on the device from the
 // expert offsets (no host synchronisation); tokens past the expert's segment
 // are never stored.
+// Large batches run on CTA pairs (cluster of 2, tcgen05.mma.cta_group::2:
+// 256 weight rows x up to 256 tokens, each CTA holding its own weight rows
+// and half of the tokens); few tokens per expert use single CTAs with
+// 64-token tiles (see launch_grouped_gemm).
 // Every pipeline wait is bounded (2 s); on timeout the CTA sets the device
 // error word, lets its in-flight copies and MMAs land, frees its tensor
 // memory and exits.

@@ -100,20 +100,6 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* m, uin
       : "memory");
 }
 
-// The same load, written to the same shared-memory offset of every CTA in
-// `cta_mask` (this GPU's memory only) and completing on the barrier at the
-// same offset in each of them.
-__device__ __forceinline__ void tma_load_2d_mcast(void* dst, const CUtensorMap* m, uint64_t* bar,
-                                                  int x, int y, uint16_t cta_mask,
-                                                  uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster.L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5, %6;" ::"r"(
-          smem_u32(dst)),
-      "l"(m), "r"(smem_u32(bar)), "r"(x), "r"(y), "h"(cta_mask), "l"(policy)
-      : "memory");
-}
-
 // ---- clusters -------------------------------------------------------------------
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
@@ -266,15 +252,6 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
       : "memory");
 }
 
-// Arrive on the barrier at `bar`'s offset in every CTA of `cta_mask` once
-// every tcgen05 operation issued so far by this thread has completed.
-__device__ __forceinline__ void mma_commit_mcast(uint64_t* bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(smem_u32(bar)),
-      "h"(cta_mask)
-      : "memory");
-}
 
 // 32 consecutive fp32 columns of this warp's 32 TMEM lanes (one lane per
 // thread). The registers are valid only after tmem_ld_wait() followed by
