@@ -8,21 +8,28 @@
 // one accumulator across K. A K block is exactly one pipeline stage: the MMA
 // thread writes each block's partial sum afresh into one of up to four TMEM
 // buffers, and the epilogue warps fold it into fp32 registers with its
-// factor sa[token,kb] * sb[kb] (loaded a block ahead) while the MMA fills
-// the next buffers.
+// factor sa[token,kb] * sb[kb] while the MMA fills the next buffers.
 //
 // Orientation and tiles as in moe_grouped_gemm: weights on the MMA's M side
 // (128 rows per tile, which is one weight scale block), tokens on N (at most
-// BNMAX per tile, 16-token granularity). One persistent CTA per SM, 320
-// threads:
+// BNMAX per tile, 16-token granularity). One persistent CTA per SM
+// (tcgen05.mma.cta_group::1), 352 threads:
 //   warp 0      TMA producer (one K block of weights and tokens per stage)
-//   warp 1      MMA issuer (tcgen05.mma.cta_group::1.kind::f8f6f4, K=32 x 4)
-//   warps 2..9  epilogue: warp w reads TMEM lane quadrant w % 4 and one half
-//               of the tile's token columns; per K block it stages its
-//               columns' factors sa*sb in its own shared-memory row (no
-//               barrier across warps), then accumulates.
-// SiLU*mul and the bf16 stores work as in moe_grouped_gemm (gate rows in TMEM
-// lanes 0..63, up rows in 64..127, exchanged through shared memory).
+//   warp 1      MMA issuer (K=32 x 4 per K block)
+//   warps 2..9  epilogue: warp w reads TMEM lane quadrant w % 4 and the
+//               32-column token chunks cg, cg + 2, ... (cg = its column
+//               group, so ragged tiles split evenly) and accumulates with
+//               packed fp32 FMAs; it holds nothing but its accumulators and
+//               the TMEM values in flight
+//   warp 10     scale warp: per K block, the factor rows
+//               sa[token,kb] * sb[kb] of the tile's token columns (SiLU: one
+//               for the gate block, one for the up block) into the slot of
+//               the partial buffer the block goes to, the next block's scales
+//               loaded while the epilogue folds this one
+// SiLU*mul: gate rows sit in TMEM lanes 0..63 and up rows in 64..127; the two
+// warps holding the same j for the same columns trade half of each 32-token
+// chunk through shared memory, and each stages its bf16 results in the slot
+// it has just read before the 16-byte stores.
 // Every wait is bounded; the two warps of a SiLU exchange pair take the abort
 // decision together through bar.red so neither is left at a named barrier.
 #include <cuda.h>
@@ -40,10 +47,11 @@ namespace {
 
 using namespace gemm_common;
 
-constexpr int EPI_WARPS = 8;
-constexpr int BTHREADS = 64 + 32 * EPI_WARPS;
-constexpr int EPI_THREADS = 32 * EPI_WARPS;
-constexpr int BAR_PAIR = 2;  // 2..5: the SiLU exchange pairs
+constexpr int CG = 2;                    // epilogue column groups
+constexpr int EW = 4 * CG;               // epilogue warps
+constexpr int BTHREADS = 96 + 32 * EW;   // producer, MMA issuer, epilogue, scale warp
+constexpr int SCALE_WARP = 2 + EW;
+constexpr int BAR_PAIR = 2;              // named barriers 2..5: the SiLU exchange pairs
 
 // TMEM partial buffers: all 512 columns, at most 4 (the MMA runs up to
 // NPB - 1 K blocks ahead of the epilogue).
@@ -52,17 +60,20 @@ __host__ __device__ constexpr int npb() {
   return 512 / BNMAX > 4 ? 4 : 512 / BNMAX;
 }
 
-template <int BNMAX, int STAGES, bool SILU>
+template <int BNMAX, int STAGES, int NF>
 struct BSmem {
-  uint8_t w[STAGES][W_BYTES];          // weights, one K block per stage
-  uint8_t x[STAGES][BNMAX * BK];       // tokens
-  float fw[EPI_WARPS][BNMAX / 2];      // per epilogue warp: sa*sb of its token columns
-  float xchg[SILU ? 4 : 1][32 * 32];   // SiLU: one slot per exchange pair
-  uint16_t stage_out[EPI_WARPS][32 * 32];
+  uint8_t w[STAGES][W_BYTES];        // weights, one K block per stage
+  uint8_t x[STAGES][BNMAX * BK];     // tokens
+  // per partial buffer: sa[token,kb] * sb[kb] of the tile's token columns, one
+  // row per weight scale block of the tile's rows (SiLU: gate, up)
+  float fs[npb<BNMAX>()][NF][BNMAX];
+  uint32_t scr[EW][16 * 32];         // per epilogue warp: SiLU exchange / bf16 staging
   uint64_t full[STAGES];
   uint64_t empty[STAGES];
   uint64_t pfull[npb<BNMAX>()];   // a K block's partial sum is in TMEM buffer b
-  uint64_t pempty[npb<BNMAX>()];  // the epilogue has read buffer b
+  uint64_t pempty[npb<BNMAX>()];  // every epilogue warp has read it
+  uint64_t sfull[npb<BNMAX>()];   // the factor rows of slot b are written
+  uint64_t sempty[npb<BNMAX>()];  // every epilogue warp has read them
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
@@ -99,12 +110,15 @@ __device__ __forceinline__ void fma2(float& acc0, float& acc1, float v0, float v
 template <int BNMAX, int STAGES, bool SILU>
 __global__ void __launch_bounds__(BTHREADS, 1)
     grouped_gemm_block_kernel(const __grid_constant__ Maps maps, const BParams p) {
-  using S = BSmem<BNMAX, STAGES, SILU>;
+  constexpr int NF = SILU ? 2 : 1;
+  using S = BSmem<BNMAX, STAGES, NF>;
   constexpr int NPB = npb<BNMAX>();
   constexpr uint32_t TCOLS = NPB * BNMAX;  // the partial buffers
-  constexpr int HC = BNMAX / 2;          // token columns per epilogue warp
-  constexpr int NCH = HC / 32;           // 32-column chunks per epilogue warp
-  static_assert(NCH >= 1 && BNMAX <= EPI_THREADS, "tile shape");
+  static_assert(TCOLS >= 32 && TCOLS <= 512 && (TCOLS & (TCOLS - 1)) == 0,
+                "tensor memory is allocated in powers of two from 32 to 512 columns");
+  constexpr int NCH = BNMAX / 32 / CG;  // 32-column chunks per epilogue warp
+  constexpr int HC = NCH * 32;          // its token columns
+  static_assert(NCH >= 1 && NCH * CG * 32 == BNMAX, "tile shape");
   extern __shared__ uint8_t smem_raw[];
   S& sm = *reinterpret_cast<S*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                 ~static_cast<uintptr_t>(1023));
@@ -123,7 +137,9 @@ __global__ void __launch_bounds__(BTHREADS, 1)
     }
     for (int b = 0; b < NPB; ++b) {
       ptx::mbar_init(&sm.pfull[b], 1);
-      ptx::mbar_init(&sm.pempty[b], EPI_WARPS);
+      ptx::mbar_init(&sm.pempty[b], EW);
+      ptx::mbar_init(&sm.sfull[b], 1);
+      ptx::mbar_init(&sm.sempty[b], EW);
     }
     ptx::mbar_init(&sm.drain, 1);
     sm.abort = 0;
@@ -148,8 +164,11 @@ __global__ void __launch_bounds__(BTHREADS, 1)
   if (warp == 0) {
     // ======================= TMA producer ===================================
     if (lane == 0) {
+      // weights evict-first when every block is read once, or when this
+      // expert's tokens fit one chunk; tokens evict-last
       const uint64_t pol_w =
           p.stream_weights ? ptx::policy_evict_first() : ptx::policy_evict_normal();
+      const uint64_t pol_w1 = ptx::policy_evict_first();
       const uint64_t pol_x = ptx::policy_evict_last();
       uint32_t s = 0, ph = 0;
       bool ok = true;
@@ -157,6 +176,7 @@ __global__ void __launch_bounds__(BTHREADS, 1)
         const TileInfo<BNMAX> t = decode_tile<BNMAX>(sm, E, p.NB, g);
         const int rows = (t.ntok + 15) & ~15;
         const uint32_t bytes = W_BYTES + (uint32_t)rows * BK;
+        const uint64_t pw = t.nch == 1 ? pol_w1 : pol_w;
         int y0, y1;  // first rows of the two 64-row weight boxes
         if (SILU) {  // gate rows [j0, j0+64) and up rows [I+j0, I+j0+64)
           y0 = t.e * p.N + t.nb * 64;
@@ -174,8 +194,8 @@ __global__ void __launch_bounds__(BTHREADS, 1)
           armed |= 1u << s;
           armed_par = (armed_par & ~(1u << s)) | (ph << s);
           const int kx = kb * BK;
-          ptx::tma_load_2d(sm.w[s], &maps.w, &sm.full[s], kx, y0, pol_w);
-          ptx::tma_load_2d(sm.w[s] + 64 * BK, &maps.w, &sm.full[s], kx, y1, pol_w);
+          ptx::tma_load_2d(sm.w[s], &maps.w, &sm.full[s], kx, y0, pw);
+          ptx::tma_load_2d(sm.w[s] + 64 * BK, &maps.w, &sm.full[s], kx, y1, pw);
           int r = 0;
 #pragma unroll
           for (int i = 0; i < NXBOX; ++i) {
@@ -238,112 +258,145 @@ __global__ void __launch_bounds__(BTHREADS, 1)
         }
       }
     }
+  } else if (warp == SCALE_WARP) {
+    // ======================= scale warp =====================================
+    constexpr int CPL = BNMAX / 32;  // token columns per lane
+    const int NBk = p.N / 128;       // weight scale blocks along N
+    uint32_t kbg = 0;
+    bool ok = true;
+    for (int g = blockIdx.x; ok && g < total; g += ncta) {
+      const TileInfo<BNMAX> t = decode_tile<BNMAX>(sm, E, p.NB, g);
+      // the scale blocks of the tile's weight rows: its 128-row block (bf16
+      // out), or the block of its 64 gate rows and of its 64 up rows (SiLU)
+      const float* sbe = p.scale_b + (int64_t)t.e * NBk * KB;
+      const float* sb0 = sbe + (SILU ? t.nb / 2 : t.nb) * KB;
+      const float* sb1 = sbe + (SILU ? (p.I + t.nb * 64) / 128 : t.nb) * KB;
+      const float* sa_t = p.scale_a + (int64_t)t.tok0 * KB;
+      float sa[CPL];
+#pragma unroll
+      for (int c = 0; c < CPL; ++c) {
+        const int col = c * 32 + lane;
+        sa[c] = col < t.ntok ? __ldg(sa_t + col * KB) : 0.0f;
+      }
+      float s0 = __ldg(sb0), s1 = SILU ? __ldg(sb1) : 0.0f;
+      for (int kb = 0; kb < KB; ++kb, ++kbg) {
+        const uint32_t b = kbg % NPB;
+        ok = ptx::mbar_wait(&sm.sempty[b], ((kbg / NPB) & 1u) ^ 1u, &sm.abort, WAIT_NS);
+        if (!__all_sync(kFull, ok)) {
+          ok = false;
+          break;
+        }
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) {
+          sm.fs[b][0][c * 32 + lane] = sa[c] * s0;
+          if (SILU) sm.fs[b][NF - 1][c * 32 + lane] = sa[c] * s1;
+        }
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&sm.sfull[b]);
+        if (kb + 1 < KB) {
+#pragma unroll
+          for (int c = 0; c < CPL; ++c) {
+            const int col = c * 32 + lane;
+            sa[c] = col < t.ntok ? __ldg(sa_t + col * KB + kb + 1) : 0.0f;
+          }
+          s0 = __ldg(sb0 + kb + 1);
+          if (SILU) s1 = __ldg(sb1 + kb + 1);
+        }
+      }
+    }
+    if (!ok && lane == 0) {
+      sm.abort = 1;
+      flag_error(p.err, MOE_DEV_PIPE_TIMEOUT);
+    }
   } else {
-    // ======================= epilogue (warps 2..9) ==========================
-    const int q = warp & 3;              // TMEM lane quadrant this warp may access
-    const int hsel = (warp - 2) >> 2;    // which half of the token columns
-    const int col0w = hsel * HC;         // first token column of this warp
-    const int NBk = p.N / 128;           // weight scale blocks along N
-    const bool up_rows = SILU && q >= 2;
-    float* fw = sm.fw[warp - 2];
+    // ======================= epilogue (warps 2 .. 2 + EW - 1) ===============
+    const int ew = warp - 2;
+    const int q = warp & 3;                   // TMEM lane quadrant this warp may access
+    const int cg = ew >> 2;                   // column group: chunks cg, cg + CG, ...
+    const int frow = SILU && q >= 2 ? 1 : 0;  // factor row: up rows (SiLU) or the block
     uint32_t kbg = 0;
     bool stop = false;
     for (int g = blockIdx.x; !stop && g < total; g += ncta) {
       const TileInfo<BNMAX> t = decode_tile<BNMAX>(sm, E, p.NB, g);
       const int n_mma = (t.ntok + 15) & ~15;
-      // the weight scale row of this warp's TMEM lanes: the tile's 128-row
-      // block (bf16 out), or its gate or its up block (SiLU)
-      const int blk = SILU ? ((up_rows ? p.I : 0) + t.nb * 64) / 128 : t.nb;
-      const float* sbw = p.scale_b + ((int64_t)t.e * NBk + blk) * KB;
-      // lane l stages the factors of token columns col0w + l + 32c; this K
-      // block's scales are loaded one block ahead
-      const float* sa_p[NCH];
-      bool tv[NCH];
-      float sa_c[NCH];
-#pragma unroll
-      for (int c = 0; c < NCH; ++c) {
-        const int col = col0w + c * 32 + lane;
-        tv[c] = col < t.ntok;
-        sa_p[c] = p.scale_a + (int64_t)(t.tok0 + (tv[c] ? col : 0)) * KB;
-        sa_c[c] = tv[c] ? __ldg(sa_p[c]) : 0.0f;
-      }
-      float sb_c = __ldg(sbw);
       float acc[HC];
 #pragma unroll
       for (int i = 0; i < HC; ++i) acc[i] = 0.0f;
       for (int kb = 0; kb < KB; ++kb, ++kbg) {
         const uint32_t b = kbg % NPB;
-#pragma unroll
-        for (int c = 0; c < NCH; ++c) fw[c * 32 + lane] = sa_c[c] * sb_c;
-        if (kb + 1 < KB) {
-#pragma unroll
-          for (int c = 0; c < NCH; ++c) sa_c[c] = tv[c] ? __ldg(sa_p[c] + kb + 1) : 0.0f;
-          sb_c = __ldg(sbw + kb + 1);
-        }
-        __syncwarp();
-        bool ok = ptx::mbar_wait(&sm.pfull[b], (kbg / NPB) & 1u, &sm.abort, WAIT_NS);
+        const uint32_t par = (kbg / NPB) & 1u;
+        bool ok = ptx::mbar_wait(&sm.pfull[b], par, &sm.abort, WAIT_NS) &&
+                  ptx::mbar_wait(&sm.sfull[b], par, &sm.abort, WAIT_NS);
         if (!__all_sync(kFull, ok)) {
           stop = true;
           break;
         }
         ptx::tc_fence_after();
-        const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + b * BNMAX + col0w;
+        const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + b * BNMAX;
+        const float* fr = sm.fs[b][frow];
 #pragma unroll
         for (int c = 0; c < NCH; ++c) {
-          if (col0w + c * 32 < n_mma) {  // warp-uniform
+          const int col0 = (cg + c * CG) * 32;
+          if (col0 < n_mma) {  // warp-uniform
             uint32_t v[32];
-            ptx::tmem_ld_32x32b_x32(tb + c * 32, v);
+            ptx::tmem_ld_32x32b_x32(tb + col0, v);
             ptx::tmem_ld_wait();
             ptx::reg_fence(v);
 #pragma unroll
             for (int i = 0; i < 32; i += 4) {
-              const float4 fv = *reinterpret_cast<const float4*>(fw + c * 32 + i);
-              fma2(acc[c * 32 + i + 0], acc[c * 32 + i + 1], __uint_as_float(v[i + 0]),
-                   __uint_as_float(v[i + 1]), fv.x, fv.y);
-              fma2(acc[c * 32 + i + 2], acc[c * 32 + i + 3], __uint_as_float(v[i + 2]),
-                   __uint_as_float(v[i + 3]), fv.z, fv.w);
+              const float4 fv = *reinterpret_cast<const float4*>(fr + col0 + i);
+              float* a = acc + c * 32 + i;
+              fma2(a[0], a[1], __uint_as_float(v[i + 0]), __uint_as_float(v[i + 1]), fv.x, fv.y);
+              fma2(a[2], a[3], __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]), fv.z, fv.w);
             }
           }
         }
         ptx::tc_fence_before();
-        __syncwarp();  // also: the factors are read before the next block's are written
-        if (lane == 0) ptx::mbar_arrive(&sm.pempty[b]);
+        __syncwarp();
+        if (lane == 0) {
+          ptx::mbar_arrive(&sm.pempty[b]);
+          ptx::mbar_arrive(&sm.sempty[b]);
+        }
       }
       // the two warps of a SiLU exchange pair go on to the output together
       // or not at all (a warp that stopped still meets its partner here)
-      if (SILU && bar_red_or(BAR_PAIR + (q & 1) + 2 * hsel, 64, stop)) stop = true;
+      if (SILU && bar_red_or(BAR_PAIR + (q & 1) + 2 * cg, 64, stop)) stop = true;
       if (stop) break;
       // ---- the tile's output: every K block is in acc ----
-      uint16_t* ost = sm.stage_out[warp - 2];
       if (SILU) {
         const int I = p.I;
-        const int pair = (q & 1) + 2 * hsel;
+        const int pair = (q & 1) + 2 * cg;
         const bool holds_gate = q < 2;
         const int mine0 = holds_gate ? 0 : 16;  // gate: tokens 0..15 of a chunk, up: 16..31
-        float* xs = sm.xchg[pair];
+        // this warp gives through its own slot and reads its partner's (the
+        // warp of the other lane half, same column group)
+        float* give = reinterpret_cast<float*>(sm.scr[ew]);
+        float* take = reinterpret_cast<float*>(sm.scr[ew ^ 2]);
+        uint16_t* ost = reinterpret_cast<uint16_t*>(take);
         const int jrow = t.nb * 64 + (q & 1) * 32;  // first j of this warp's 32
         __nv_bfloat16* hbase = reinterpret_cast<__nv_bfloat16*>(p.C);
 #pragma unroll
         for (int c = 0; c < NCH; ++c) {
-          const int col0 = hsel * HC + c * 32;  // first token column of the chunk
+          const int col0 = (cg + c * CG) * 32;  // first token column of the chunk
           if (col0 >= t.ntok) break;            // the same for both warps of the pair
-          // hand the partner the half it computes: the gate holder gives
-          // tokens 16..31 (slots 0..15), the up holder tokens 0..15 (16..31)
+          // the gate holder gives tokens 16..31, the up holder tokens 0..15
 #pragma unroll
           for (int i = 0; i < 16; ++i)
-            xs[(holds_gate ? i : 16 + i) * 32 + lane] =
-                holds_gate ? acc[c * 32 + 16 + i] : acc[c * 32 + i];
+            give[i * 32 + lane] = holds_gate ? acc[c * 32 + 16 + i] : acc[c * 32 + i];
           bar_sync_named(BAR_PAIR + pair, 64);
+          float hv[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const float own = holds_gate ? acc[c * 32 + i] : acc[c * 32 + 16 + i];
-            const float other = xs[(holds_gate ? 16 + i : i) * 32 + lane];
+            const float other = take[i * 32 + lane];
             const float gv = holds_gate ? own : other;
             const float uv = holds_gate ? other : own;
-            const __nv_bfloat16 hb =
-                __float2bfloat16_rn(__fdividef(gv, 1.0f + __expf(-gv)) * uv);
-            ost[i * 32 + lane] = __bfloat16_as_ushort(hb);
+            hv[i] = __fdividef(gv, 1.0f + __expf(-gv)) * uv;
           }
+          __syncwarp();  // the partner's values are read: its slot takes the bf16 rows
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            ost[i * 32 + lane] = __bfloat16_as_ushort(__float2bfloat16_rn(hv[i]));
           __syncwarp();
           // 16 tokens x 32 j: four lanes per token row, 16 bytes each
 #pragma unroll
@@ -356,15 +409,16 @@ __global__ void __launch_bounds__(BTHREADS, 1)
                   *reinterpret_cast<const uint4*>(ost + r * 32 + (lane & 3) * 8);
           }
           __syncwarp();
-          bar_sync_named(BAR_PAIR + pair, 64);  // the slot is free again
+          bar_sync_named(BAR_PAIR + pair, 64);  // both slots are free again
         }
       } else {
         const int N = p.N;
         const int ncol0 = t.nb * BM + q * 32;  // first output column of this warp's 32
+        uint16_t* ost = reinterpret_cast<uint16_t*>(sm.scr[ew]);
         __nv_bfloat16* cbase = reinterpret_cast<__nv_bfloat16*>(p.C);
 #pragma unroll
         for (int c = 0; c < NCH; ++c) {
-          const int col0 = hsel * HC + c * 32;
+          const int col0 = (cg + c * CG) * 32;
           if (col0 >= t.ntok) break;
 #pragma unroll
           for (int i = 0; i < 32; ++i)
@@ -405,19 +459,20 @@ __global__ void __launch_bounds__(BTHREADS, 1)
 }
 
 // The deepest ring that fits next to the rest of the shared memory (at most 8).
-template <int BNMAX, bool SILU>
+template <int BNMAX, int NF>
 constexpr int block_stages() {
-  constexpr size_t fixed = sizeof(BSmem<BNMAX, 1, SILU>) - (W_BYTES + BNMAX * BK) + 1024;
   constexpr size_t per = W_BYTES + BNMAX * BK + 16;
+  constexpr size_t fixed = sizeof(BSmem<BNMAX, 1, NF>) - per + 16 + 1024;
   constexpr size_t n = (227 * 1024 - fixed) / per;
   return n > 8 ? 8 : (int)n;
 }
 
 template <int BNMAX, bool SILU>
 cudaError_t launch_block_cfg(const Maps& maps, const BParams& p, int M, int E, cudaStream_t st) {
-  constexpr int STAGES = block_stages<BNMAX, SILU>();
+  constexpr int NF = SILU ? 2 : 1;
+  constexpr int STAGES = block_stages<BNMAX, NF>();
   static_assert(STAGES >= 3, "pipeline depth");
-  constexpr size_t smem = sizeof(BSmem<BNMAX, STAGES, SILU>) + 1024;
+  constexpr size_t smem = sizeof(BSmem<BNMAX, STAGES, NF>) + 1024;
   static_assert(smem <= 227 * 1024, "shared memory budget");
   auto kern = grouped_gemm_block_kernel<BNMAX, STAGES, SILU>;
   static std::mutex mu;
