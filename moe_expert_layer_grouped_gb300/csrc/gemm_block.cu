@@ -24,8 +24,9 @@
 //   warp 10     scale warp: per K block, the factor rows
 //               sa[token,kb] * sb[kb] of the tile's token columns (SiLU: one
 //               for the gate block, one for the up block) into the slot of
-//               the partial buffer the block goes to, the next block's scales
-//               loaded while the epilogue folds this one
+//               the partial buffer the block goes to; it reads four K blocks
+//               of scales per 16-byte load (each lane's token row is its own
+//               cache line), the next four while these are used
 // SiLU*mul: gate rows sit in TMEM lanes 0..63 and up rows in 64..127; the two
 // warps holding the same j for the same columns trade half of each 32-token
 // chunk through shared memory, and each stages its bf16 results in the slot
@@ -272,6 +273,72 @@ __global__ void __launch_bounds__(BTHREADS, 1)
       const float* sb0 = sbe + (SILU ? t.nb / 2 : t.nb) * KB;
       const float* sb1 = sbe + (SILU ? (p.I + t.nb * 64) / 128 : t.nb) * KB;
       const float* sa_t = p.scale_a + (int64_t)t.tok0 * KB;
+      if ((KB & 3) == 0 && ((reinterpret_cast<uintptr_t>(p.scale_a) |
+                             reinterpret_cast<uintptr_t>(p.scale_b)) & 15) == 0) {
+        // four K blocks of scales per 16-byte load, the next four loaded
+        // while these are used
+        float4 cur[CPL], nxt[CPL];
+        float4 b0c, b1c, b0n, b1n;
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) {
+          const int col = c * 32 + lane;
+          cur[c] = col < t.ntok ? __ldg(reinterpret_cast<const float4*>(sa_t + col * KB))
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        b0c = __ldg(reinterpret_cast<const float4*>(sb0));
+        b1c = SILU ? __ldg(reinterpret_cast<const float4*>(sb1)) : b0c;
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) nxt[c] = cur[c];
+        b0n = b0c;
+        b1n = b1c;
+        if (KB > 4) {
+#pragma unroll
+          for (int c = 0; c < CPL; ++c) {
+            const int col = c * 32 + lane;
+            nxt[c] = col < t.ntok ? __ldg(reinterpret_cast<const float4*>(sa_t + col * KB + 4))
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+          b0n = __ldg(reinterpret_cast<const float4*>(sb0 + 4));
+          b1n = SILU ? __ldg(reinterpret_cast<const float4*>(sb1 + 4)) : b0n;
+        }
+        for (int kb = 0; kb < KB; ++kb, ++kbg) {
+          const int j = kb & 3;
+          if (j == 0 && kb > 0) {
+#pragma unroll
+            for (int c = 0; c < CPL; ++c) cur[c] = nxt[c];
+            b0c = b0n;
+            b1c = b1n;
+            if (kb + 4 < KB) {
+#pragma unroll
+              for (int c = 0; c < CPL; ++c) {
+                const int col = c * 32 + lane;
+                nxt[c] = col < t.ntok
+                             ? __ldg(reinterpret_cast<const float4*>(sa_t + col * KB + kb + 4))
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
+              }
+              b0n = __ldg(reinterpret_cast<const float4*>(sb0 + kb + 4));
+              b1n = SILU ? __ldg(reinterpret_cast<const float4*>(sb1 + kb + 4)) : b0n;
+            }
+          }
+          const uint32_t b = kbg % NPB;
+          ok = ptx::mbar_wait(&sm.sempty[b], ((kbg / NPB) & 1u) ^ 1u, &sm.abort, WAIT_NS);
+          if (!__all_sync(kFull, ok)) {
+            ok = false;
+            break;
+          }
+          const float s0 = j == 0 ? b0c.x : j == 1 ? b0c.y : j == 2 ? b0c.z : b0c.w;
+          const float s1 = j == 0 ? b1c.x : j == 1 ? b1c.y : j == 2 ? b1c.z : b1c.w;
+#pragma unroll
+          for (int c = 0; c < CPL; ++c) {
+            const float a = j == 0 ? cur[c].x : j == 1 ? cur[c].y : j == 2 ? cur[c].z : cur[c].w;
+            sm.fs[b][0][c * 32 + lane] = a * s0;
+            if (SILU) sm.fs[b][NF - 1][c * 32 + lane] = a * s1;
+          }
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(&sm.sfull[b]);
+        }
+        continue;
+      }
       float sa[CPL];
 #pragma unroll
       for (int c = 0; c < CPL; ++c) {
