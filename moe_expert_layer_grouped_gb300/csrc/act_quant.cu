@@ -47,32 +47,42 @@ __global__ void __launch_bounds__(kWarps * 32)
 
 // Block requantisation: one scale per 128 channels of a row (scale
 // [M, I/128]). A warp takes a row two blocks at a time, a half-warp per
-// block (16 lanes x 8 values), the block amax by a 16-lane shuffle.
+// block (16 lanes x 8 values), the block amax by a 16-lane shuffle; the
+// loads of four such steps are issued before the first is used.
 __global__ void __launch_bounds__(kWarps * 32)
     act_quant_block_kernel(const __nv_bfloat16* __restrict__ h, int M, int I,
                            uint8_t* __restrict__ q, float* __restrict__ scale) {
+  constexpr int U = 4;  // steps of two blocks in flight
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t row = (int64_t)blockIdx.x * kWarps + warp;
   if (row >= M) return;  // warp-uniform
   const int nb = I >> 7;
   const uint4* hr = reinterpret_cast<const uint4*>(h + row * I);
   uint2* qr = reinterpret_cast<uint2*>(q + row * I);
-  for (int b0 = 0; b0 < nb; b0 += 2) {
-    const int b = b0 + (lane >> 4);
-    const bool in = b < nb;
-    const int vi = b * 16 + (lane & 15);
-    float f[8];
-    float m = 0.0f;
-    if (in) {
-      bf16x8_to_f32(__ldg(hr + vi), f);
-      m = absmax8(f, 0.0f);
+  for (int b0 = 0; b0 < nb; b0 += 2 * U) {
+    uint4 raw[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int b = b0 + 2 * u + (lane >> 4);
+      if (b < nb) raw[u] = __ldg(hr + b * 16 + (lane & 15));
     }
 #pragma unroll
-    for (int o = 1; o < 16; o <<= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
-    if (in) {
-      const float sc = token_scale(m);
-      qr[vi] = quant8(f, sc);
-      if ((lane & 15) == 0) scale[row * nb + b] = sc;
+    for (int u = 0; u < U; ++u) {
+      const int b = b0 + 2 * u + (lane >> 4);
+      const bool in = b < nb;
+      float f[8];
+      float m = 0.0f;
+      if (in) {
+        bf16x8_to_f32(raw[u], f);
+        m = absmax8(f, 0.0f);
+      }
+#pragma unroll
+      for (int o = 1; o < 16; o <<= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
+      if (in) {
+        const float sc = token_scale(m);
+        qr[b * 16 + (lane & 15)] = quant8(f, sc);
+        if ((lane & 15) == 0) scale[row * nb + b] = sc;
+      }
     }
   }
 }
