@@ -557,7 +557,7 @@ def run_reference(args):
     oracle_build.build()
     wl = synth.WORKLOADS[args.workload]
     steps = args.steps if args.steps is not None else 3
-    warmup = max(0, min(args.warmup, 1))
+    warmup = max(0, args.warmup)
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     d = synth.make_inputs(wl, seed=args.seed, device=dev, weights=True)
     n = synth.to_numpy_inputs(d)
@@ -570,8 +570,10 @@ def run_reference(args):
     fwd = oracle.forward_tokens_block if wl.quant == "block" else oracle.forward_tokens
     fwd(*fargs, tokens=np.arange(min(threads, wl.T), dtype=np.int64), n_shared=S)
     per_tok = (time.time() - t) / min(threads, wl.T)
-    budget = max(5.0, 60.0 / max(1, steps + warmup))
-    ntok = int(max(1, min(wl.T, budget / max(per_tok, 1e-6))))
+    # about 90 s for the whole run (warm-up included), at least one token per
+    # oracle thread per step
+    budget = 90.0 / max(1, steps + warmup)
+    ntok = int(max(min(threads, wl.T), min(wl.T, budget / max(per_tok, 1e-6))))
     toks = np.arange(ntok, dtype=np.int64)
     for _ in range(warmup):
         fwd(*fargs, tokens=toks, n_shared=S)
