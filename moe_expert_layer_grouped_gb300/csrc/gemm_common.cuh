@@ -104,21 +104,37 @@ __device__ __forceinline__ void build_tile_table(S& sm, const int32_t* offsets, 
     if (lo < 0 || hi < lo || hi > M) bad = 1;
     else local += (hi - lo + BNMAX - 1) / BNMAX;
   }
-  sm.thr_sum[tid] = local;
+  // exclusive prefix of the per-thread tile counts: a shuffle scan in each
+  // warp, then one over the warp totals
+  static_assert(THREADS % 32 == 0 && THREADS <= 32 * 32, "block shape");
+  constexpr int NW = THREADS / 32;
+  const int lane = tid & 31, wid = tid >> 5;
+  int incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(kFull, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) sm.thr_sum[wid] = incl;
   bad = __syncthreads_or(bad);
-  if (tid == 0) {
-    int run = 0;
-    for (int i = 0; i < THREADS; ++i) {
-      const int v = sm.thr_sum[i];
-      sm.thr_sum[i] = run;
-      run += v;
+  if (wid == 0) {
+    const int w = lane < NW ? sm.thr_sum[lane] : 0;
+    int wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(kFull, wi, o);
+      if (lane >= o) wi += y;
     }
-    sm.total_tiles = bad ? 0 : run * NBG;
-    sm.tile_start[E] = run * NBG;
-    if (bad) flag_error(err, MOE_DEV_BAD_OFFSETS);
+    __syncwarp();
+    if (lane < NW) sm.thr_sum[lane] = wi - w;  // tiles before warp `lane`
+    if (lane == NW - 1) {
+      sm.total_tiles = bad ? 0 : wi * NBG;
+      sm.tile_start[E] = wi * NBG;
+      if (bad) flag_error(err, MOE_DEV_BAD_OFFSETS);
+    }
   }
   __syncthreads();
-  int run = sm.thr_sum[tid];
+  int run = sm.thr_sum[wid] + incl - local;
   for (int e = e0; e < e1; ++e) {
     sm.tile_start[e] = run * NBG;
     const int lo = sm.offs[e], hi = sm.offs[e + 1];
