@@ -16,6 +16,7 @@ constexpr int kWarps = 8;
 __global__ void __launch_bounds__(kWarps * 32)
     act_quant_kernel(const __nv_bfloat16* __restrict__ h, const float* __restrict__ row_amax,
                      int M, int I, uint8_t* __restrict__ q, float* __restrict__ scale) {
+  chain_entry();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t row = (int64_t)blockIdx.x * kWarps + warp;
   if (row >= M) return;
@@ -52,6 +53,7 @@ __global__ void __launch_bounds__(kWarps * 32)
 __global__ void __launch_bounds__(kWarps * 32)
     act_quant_block_kernel(const __nv_bfloat16* __restrict__ h, int M, int I,
                            uint8_t* __restrict__ q, float* __restrict__ scale) {
+  chain_entry();
   constexpr int U = 4;  // steps of two blocks in flight
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t row = (int64_t)blockIdx.x * kWarps + warp;
@@ -90,22 +92,21 @@ __global__ void __launch_bounds__(kWarps * 32)
 }  // namespace
 
 cudaError_t launch_act_quant_block(const void* h, int M, int I, void* q, float* scale,
-                                   cudaStream_t st) {
+                                   cudaStream_t st, bool pdl) {
   if (M == 0) return cudaSuccess;
   const int blocks = (M + kWarps - 1) / kWarps;
-  act_quant_block_kernel<<<blocks, kWarps * 32, 0, st>>>(
-      reinterpret_cast<const __nv_bfloat16*>(h), M, I, reinterpret_cast<uint8_t*>(q), scale);
-  return cudaGetLastError();
+  return launch_kernel(act_quant_block_kernel, dim3(blocks), dim3(kWarps * 32), 0, st, pdl,
+                       reinterpret_cast<const __nv_bfloat16*>(h), M, I,
+                       reinterpret_cast<uint8_t*>(q), scale);
 }
 
 cudaError_t launch_act_quant(const void* h, const float* row_amax, int M, int I, void* q,
-                             float* scale, cudaStream_t st) {
+                             float* scale, cudaStream_t st, bool pdl) {
   if (M == 0) return cudaSuccess;
   const int blocks = (M + kWarps - 1) / kWarps;
-  act_quant_kernel<<<blocks, kWarps * 32, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(h),
-                                                   row_amax, M, I,
-                                                   reinterpret_cast<uint8_t*>(q), scale);
-  return cudaGetLastError();
+  return launch_kernel(act_quant_kernel, dim3(blocks), dim3(kWarps * 32), 0, st, pdl,
+                       reinterpret_cast<const __nv_bfloat16*>(h), row_amax, M, I,
+                       reinterpret_cast<uint8_t*>(q), scale);
 }
 
 }  // namespace moe

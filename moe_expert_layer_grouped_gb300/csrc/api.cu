@@ -189,32 +189,37 @@ moe_status run_forward(const void* x, const float* logits, const float* bias, co
   void* q2 = at<void>(ws, L.q2);
   void* down = at<void>(ws, L.down);
   cudaError_t e;
+  // The gate is launched plainly (after everything before it on the
+  // stream); every later kernel of the step as a programmatic dependent of
+  // the one before it.
+  constexpr bool kChain = true;
   if ((e = launch_gate(logits, bias, T, E, G, TG, K, scoring, renorm, rsf, ids, w, S, st)))
     return cuda_status(e);
   if (block) {
     if ((e = launch_permute_quant_block(x, ids, T, H, EA, KA, a_q, sa, s2d, offsets,
-                                        at<void>(ws, L.perm), err, st)))
+                                        at<void>(ws, L.perm), err, st, kChain)))
       return cuda_status(e);
     if ((e = launch_grouped_gemm_block(a_q, sa, w13, s13, offsets, M, 2 * I, H, EA,
-                                       MOE_EPI_SILU_MUL, h, err, st)))
+                                       MOE_EPI_SILU_MUL, h, err, st, kChain)))
       return cuda_status(e);
-    if ((e = launch_act_quant_block(h, M, I, q2, sa2, st))) return cuda_status(e);
+    if ((e = launch_act_quant_block(h, M, I, q2, sa2, st, kChain))) return cuda_status(e);
     if ((e = launch_grouped_gemm_block(q2, sa2, w2, s2, offsets, M, H, I, EA, MOE_EPI_BF16,
-                                       down, err, st)))
+                                       down, err, st, kChain, /*early_table=*/true)))
       return cuda_status(e);
   } else {
     if ((e = launch_permute_quant(x, ids, T, H, EA, KA, a_q, sa, s2d, offsets,
-                                  at<void>(ws, L.perm), err, st)))
+                                  at<void>(ws, L.perm), err, st, kChain)))
       return cuda_status(e);
     if ((e = launch_grouped_gemm(a_q, sa, w13, s13, offsets, M, 2 * I, H, EA, MOE_EPI_SILU_MUL,
-                                 h, nullptr, err, st)))
+                                 h, nullptr, err, st, -1, kChain)))
       return cuda_status(e);
-    if ((e = launch_act_quant(h, nullptr, M, I, q2, sa2, st))) return cuda_status(e);
+    if ((e = launch_act_quant(h, nullptr, M, I, q2, sa2, st, kChain))) return cuda_status(e);
     if ((e = launch_grouped_gemm(q2, sa2, w2, s2, offsets, M, H, I, EA, MOE_EPI_BF16, down,
-                                 nullptr, err, st)))
+                                 nullptr, err, st, -1, kChain, /*early_table=*/true)))
       return cuda_status(e);
   }
-  if ((e = launch_unpermute_sum(down, s2d, w, T, KA, H, out, err, st))) return cuda_status(e);
+  if ((e = launch_unpermute_sum(down, s2d, w, T, KA, H, out, err, st, kChain)))
+    return cuda_status(e);
   return MOE_OK;
 }
 

@@ -6,11 +6,44 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "moe_gb300.h"
 
 namespace moe {
 
 constexpr unsigned kFull = 0xffffffffu;
+
+// Every kernel of the forward path starts with this: it waits for the kernel
+// before it on the stream (when launched as its programmatic dependent), then
+// lets the next one start its launch. A kernel therefore never runs ahead of
+// the one before it, and when a kernel starts, every kernel two or more
+// places earlier on the stream has completed.
+__device__ __forceinline__ void chain_entry() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Launches `kern` on `st`. With `pdl` it is launched as a programmatic
+// dependent of the previous kernel on the stream: its CTAs may be scheduled
+// while that kernel still runs, and wait for it in chain_entry().
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t st, bool pdl, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  if (pdl) {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // First fault wins; later ones are dropped.
 __device__ __forceinline__ void flag_error(int* err, int code) {

@@ -102,6 +102,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     gate_kernel(const float* __restrict__ logits, const float* __restrict__ bias, int T, int E,
                 int G, int TG, int K, int scoring, int renorm, float rsf,
                 int32_t* __restrict__ ids_out, float* __restrict__ w_out, int n_shared) {
+  chain_entry();
   extern __shared__ float keys_smem[];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;

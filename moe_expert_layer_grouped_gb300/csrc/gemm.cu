@@ -97,6 +97,7 @@ struct Params {
   int M, N, Kd, E, I, NB, KB;
   int stream_weights;  // 1: each weight block is read by one tile (evict-first)
   int stall_stage;     // failure test: CTA 0 never loads its stage with this index (-1: none)
+  int early_table;     // build the tile table before waiting for the previous kernel
 };
 
 // CS = 1: one CTA per tile of 128 weight rows x N tokens.
@@ -154,7 +155,11 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (PAIR) ptx::cluster_sync();  // the peer's barriers exist before any signal
 
   // ---- tile table from the expert offsets --------------------------------
+  // (inside a chained forward the offsets of the w2 GEMM were written two
+  // kernels earlier, so its table is built before the wait)
+  if (!p.early_table) chain_entry();
   build_tile_table<BNMAX, THREADS>(sm, p.offsets, E, p.M, NBG, p.err, tid);
+  if (p.early_table) chain_entry();
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
@@ -488,7 +493,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 
 // ---- host side ---------------------------------------------------------------
 template <int BNMAX, int STAGES, bool SILU, int CS, int KC>
-cudaError_t launch_cfg(const Maps& maps, const Params& p, int M, int E, cudaStream_t st) {
+cudaError_t launch_cfg(const Maps& maps, const Params& p, int M, int E, cudaStream_t st,
+                       bool pdl) {
   constexpr size_t smem = sizeof(Smem<BNMAX / CS, STAGES, SILU, KC>) + 1024;
   static_assert(smem <= 227 * 1024, "shared memory budget");
   auto kern = grouped_gemm_kernel<BNMAX, STAGES, SILU, CS, KC>;
@@ -513,13 +519,15 @@ cudaError_t launch_cfg(const Maps& maps, const Params& p, int M, int E, cudaStre
   cfg.blockDim = dim3(THREADS);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = CS;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = pdl ? 2 : 1;
   if (CS > 1) {
     // a persistent grid of pairs must be co-resident: no more clusters than
     // the GPU can hold at once
@@ -602,7 +610,7 @@ bool make_tma_map_u8(CUtensorMap* m, const void* base, uint64_t rows, uint64_t c
 cudaError_t launch_grouped_gemm(const void* A, const float* scale_a, const void* B,
                                 const float* scale_b, const int32_t* offsets, int M, int N,
                                 int Kd, int E, int epilogue, void* C, float* row_amax, int* err,
-                                cudaStream_t st, int stall_stage) {
+                                cudaStream_t st, int stall_stage, bool pdl, bool early_table) {
   if (M == 0) return cudaSuccess;
   const bool silu = (epilogue == MOE_EPI_SILU_MUL);
   const bool small = (int64_t)M <= (int64_t)32 * E;  // few rows per expert (decode)
@@ -632,16 +640,17 @@ cudaError_t launch_grouped_gemm(const void* A, const float* scale_a, const void*
   // weight row per stage); many (prefill): tiles of up to 256 tokens
   p.stream_weights = small ? 1 : 0;
   p.stall_stage = stall_stage;
+  p.early_table = early_table ? 1 : 0;
   if (small)
-    return silu ? launch_cfg<64, 4, true, 1, 2>(maps, p, M, E, st)
-                : launch_cfg<64, 4, false, 1, 2>(maps, p, M, E, st);
+    return silu ? launch_cfg<64, 4, true, 1, 2>(maps, p, M, E, st, pdl)
+                : launch_cfg<64, 4, false, 1, 2>(maps, p, M, E, st, pdl);
   // many tokens per expert: CTA pairs on pairs of weight blocks (2-SM MMA),
   // 3 stages of 2 x (16 KB weights + 16 KB tokens) per CTA
   if (p.NB % 2 == 0)
-    return silu ? launch_cfg<256, PAIR_STAGES, true, 2, PAIR_KC>(maps, p, M, E, st)
-                : launch_cfg<256, PAIR_STAGES, false, 2, PAIR_KC>(maps, p, M, E, st);
-  return silu ? launch_cfg<256, 4, true, 1, 1>(maps, p, M, E, st)
-              : launch_cfg<256, 4, false, 1, 1>(maps, p, M, E, st);
+    return silu ? launch_cfg<256, PAIR_STAGES, true, 2, PAIR_KC>(maps, p, M, E, st, pdl)
+                : launch_cfg<256, PAIR_STAGES, false, 2, PAIR_KC>(maps, p, M, E, st, pdl);
+  return silu ? launch_cfg<256, 4, true, 1, 1>(maps, p, M, E, st, pdl)
+              : launch_cfg<256, 4, false, 1, 1>(maps, p, M, E, st, pdl);
 }
 
 }  // namespace moe

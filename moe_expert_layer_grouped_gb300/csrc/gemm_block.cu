@@ -93,6 +93,7 @@ struct BParams {
   int* err;
   int M, N, Kd, E, I, NB, KB;
   int stream_weights;
+  int early_table;  // build the tile table before waiting for the previous kernel
 };
 
 // acc0/1 += v0/1 * f0/1, two lanes of fp32 at once (each rounded as fmaf).
@@ -151,7 +152,11 @@ __global__ void __launch_bounds__(BTHREADS, 1)
     ptx::tmem_alloc(&sm.tmem_base, TCOLS);
     ptx::tmem_relinquish();
   }
+  // (inside a chained forward the offsets of the w2 GEMM were written two
+  // kernels earlier, so its table is built before the wait)
+  if (!p.early_table) chain_entry();
   build_tile_table<BNMAX, BTHREADS>(sm, p.offsets, E, p.M, p.NB, p.err, tid);
+  if (p.early_table) chain_entry();
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
@@ -535,7 +540,8 @@ constexpr int block_stages() {
 }
 
 template <int BNMAX, bool SILU>
-cudaError_t launch_block_cfg(const Maps& maps, const BParams& p, int M, int E, cudaStream_t st) {
+cudaError_t launch_block_cfg(const Maps& maps, const BParams& p, int M, int E, cudaStream_t st,
+                             bool pdl) {
   constexpr int NF = SILU ? 2 : 1;
   constexpr int STAGES = block_stages<BNMAX, NF>();
   static_assert(STAGES >= 3, "pipeline depth");
@@ -557,8 +563,7 @@ cudaError_t launch_block_cfg(const Maps& maps, const BParams& p, int M, int E, c
   }
   const long long upper = ((long long)(M + BNMAX - 1) / BNMAX + E) * p.NB;
   const int grid = (int)std::max<long long>(1, std::min<long long>(sm_count(), upper));
-  kern<<<grid, BTHREADS, smem, st>>>(maps, p);
-  return cudaGetLastError();
+  return launch_kernel(kern, dim3(grid), dim3(BTHREADS), smem, st, pdl, maps, p);
 }
 
 }  // namespace
@@ -566,7 +571,7 @@ cudaError_t launch_block_cfg(const Maps& maps, const BParams& p, int M, int E, c
 cudaError_t launch_grouped_gemm_block(const void* A, const float* scale_a, const void* B,
                                       const float* scale_b, const int32_t* offsets, int M, int N,
                                       int Kd, int E, int epilogue, void* C, int* err,
-                                      cudaStream_t st) {
+                                      cudaStream_t st, bool pdl, bool early_table) {
   if (M == 0) return cudaSuccess;
   const bool silu = (epilogue == MOE_EPI_SILU_MUL);
   const bool small = (int64_t)M <= (int64_t)32 * E;  // few rows per expert (decode)
@@ -590,11 +595,12 @@ cudaError_t launch_grouped_gemm_block(const void* A, const float* scale_a, const
   p.NB = silu ? p.I / 64 : N / BM;
   p.KB = Kd / BK;
   p.stream_weights = small ? 1 : 0;
+  p.early_table = early_table ? 1 : 0;
   if (small)
-    return silu ? launch_block_cfg<64, true>(maps, p, M, E, st)
-                : launch_block_cfg<64, false>(maps, p, M, E, st);
-  return silu ? launch_block_cfg<128, true>(maps, p, M, E, st)
-              : launch_block_cfg<128, false>(maps, p, M, E, st);
+    return silu ? launch_block_cfg<64, true>(maps, p, M, E, st, pdl)
+                : launch_block_cfg<64, false>(maps, p, M, E, st, pdl);
+  return silu ? launch_block_cfg<128, true>(maps, p, M, E, st, pdl)
+              : launch_block_cfg<128, false>(maps, p, M, E, st, pdl);
 }
 
 }  // namespace moe

@@ -21,17 +21,22 @@ cudaError_t launch_gate(const float* logits, const float* bias, int T, int E, in
                         int K, int scoring, int renorm, float rsf, int32_t* ids, float* w,
                         int n_shared, cudaStream_t st);
 
+// The launchers below take `pdl`: launch as a programmatic dependent of the
+// previous kernel on the stream (the forward path chains its kernels this
+// way; the single-step entry points launch plainly).
+
 // permute.cu
 size_t permute_ws_bytes(int T, int E);
 cudaError_t launch_permute_quant(const void* x, const int32_t* ids, int T, int H, int E, int K,
                                  void* a_q, float* scale_a, int32_t* src2dst, int32_t* offsets,
-                                 void* ws, int* err, cudaStream_t st);
+                                 void* ws, int* err, cudaStream_t st, bool pdl = false);
 
 // permute.cu: the same with one scale per 128 channels, scale_a [T*K, H/128]
 // (H % 128 == 0).
 cudaError_t launch_permute_quant_block(const void* x, const int32_t* ids, int T, int H, int E,
                                        int K, void* a_q, float* scale_a, int32_t* src2dst,
-                                       int32_t* offsets, void* ws, int* err, cudaStream_t st);
+                                       int32_t* offsets, void* ws, int* err, cudaStream_t st,
+                                       bool pdl = false);
 
 // permute.cu: device address of the fixed scratch used by
 // moe_permute_quant_noalloc on the current device (nullptr on failure).
@@ -39,28 +44,32 @@ void* permute_static_scratch();
 
 // gemm.cu
 // Returns cudaErrorNotSupported when the TMA descriptors cannot be encoded.
+// `early_table`: the offsets were written two or more kernels earlier on the
+// stream, so the tile table is built before waiting for the previous kernel.
 cudaError_t launch_grouped_gemm(const void* A, const float* scale_a, const void* B,
                                 const float* scale_b, const int32_t* offsets, int M, int N,
                                 int Kd, int E, int epilogue, void* C, float* row_amax, int* err,
-                                cudaStream_t st, int stall_stage = -1);
+                                cudaStream_t st, int stall_stage = -1, bool pdl = false,
+                                bool early_table = false);
 
 // gemm_block.cu: block scales, scale_a [M, Kd/128], scale_b [E, N/128, Kd/128]
 // (N % 128 == 0, Kd % 128 == 0); no row amax.
 cudaError_t launch_grouped_gemm_block(const void* A, const float* scale_a, const void* B,
                                       const float* scale_b, const int32_t* offsets, int M, int N,
                                       int Kd, int E, int epilogue, void* C, int* err,
-                                      cudaStream_t st);
+                                      cudaStream_t st, bool pdl = false, bool early_table = false);
 
 // act_quant.cu
 cudaError_t launch_act_quant(const void* h, const float* row_amax, int M, int I, void* q,
-                             float* scale, cudaStream_t st);
+                             float* scale, cudaStream_t st, bool pdl = false);
 
 // act_quant.cu: one scale per 128 channels, scale [M, I/128] (I % 128 == 0).
 cudaError_t launch_act_quant_block(const void* h, int M, int I, void* q, float* scale,
-                                   cudaStream_t st);
+                                   cudaStream_t st, bool pdl = false);
 
 // unpermute.cu
 cudaError_t launch_unpermute_sum(const void* down, const int32_t* src2dst, const float* w,
-                                 int T, int K, int H, void* out, int* err, cudaStream_t st);
+                                 int T, int K, int H, void* out, int* err, cudaStream_t st,
+                                 bool pdl = false);
 
 }  // namespace moe

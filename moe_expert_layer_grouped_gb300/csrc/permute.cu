@@ -28,6 +28,7 @@ constexpr int kBitsWarps = 8;
 __global__ void __launch_bounds__(kBitsWarps * 32)
     route_bits_kernel(const int32_t* __restrict__ ids, int T, int E, int K,
                       uint32_t* __restrict__ bits, int* err) {
+  chain_entry();
   extern __shared__ uint32_t masks[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int C = (T + 31) >> 5;
@@ -56,6 +57,7 @@ __global__ void __launch_bounds__(kBitsWarps * 32)
 __global__ void __launch_bounds__(1024)
     route_scan_kernel(const uint32_t* __restrict__ bits, int C, int E,
                       int32_t* __restrict__ base, int32_t* __restrict__ offsets) {
+  chain_entry();
   __shared__ int part[1024];
   __shared__ int total[1024];
   __shared__ int excl[1024];
@@ -204,6 +206,7 @@ __global__ void __launch_bounds__(kQuantThreads)
                          const uint32_t* __restrict__ bits, const int32_t* __restrict__ base,
                          int H, int E, int K, uint8_t* __restrict__ a_q,
                          float* __restrict__ scale_a, int32_t* __restrict__ src2dst) {
+  chain_entry();
   __shared__ int dst[32];
   __shared__ float red[kQuantThreads / 32];
   const int t = blockIdx.x;
@@ -244,6 +247,7 @@ __global__ void __launch_bounds__(kSmallThreads)
                                uint8_t* __restrict__ a_q, float* __restrict__ scale_a,
                                int32_t* __restrict__ src2dst, int32_t* __restrict__ offsets,
                                int* err) {
+  chain_entry();
   extern __shared__ int route_smem[];
   __shared__ int dst[32];
   __shared__ float red[kSmallThreads / 32];
@@ -334,22 +338,22 @@ __global__ void __launch_bounds__(kSmallThreads)
 }
 
 template <int VPT, bool BLOCK>
-void launch_small(const void* x, const int32_t* ids, int T, int H, int E, int K, void* a_q,
-                  float* scale_a, int32_t* src2dst, int32_t* offsets, int* err,
-                  cudaStream_t st) {
+cudaError_t launch_small(const void* x, const int32_t* ids, int T, int H, int E, int K,
+                         void* a_q, float* scale_a, int32_t* src2dst, int32_t* offsets, int* err,
+                         cudaStream_t st, bool pdl) {
   const size_t smem = sizeof(int) * (2 * (size_t)T * K + 2 * (size_t)E + 1);
-  permute_quant_small_kernel<VPT, BLOCK><<<T, kSmallThreads, smem, st>>>(
-      reinterpret_cast<const __nv_bfloat16*>(x), ids, T, H, E, K,
-      reinterpret_cast<uint8_t*>(a_q), scale_a, src2dst, offsets, err);
+  return launch_kernel(permute_quant_small_kernel<VPT, BLOCK>, dim3(T), dim3(kSmallThreads),
+                       smem, st, pdl, reinterpret_cast<const __nv_bfloat16*>(x), ids, T, H, E, K,
+                       reinterpret_cast<uint8_t*>(a_q), scale_a, src2dst, offsets, err);
 }
 
 template <int VPT, bool BLOCK>
-void launch_quant(const void* x, const int32_t* ids, const uint32_t* bits, const int32_t* base,
-                  int T, int H, int E, int K, void* a_q, float* scale_a, int32_t* src2dst,
-                  cudaStream_t st) {
-  permute_quant_kernel<VPT, BLOCK><<<T, kQuantThreads, 0, st>>>(
-      reinterpret_cast<const __nv_bfloat16*>(x), ids, bits, base, H, E, K,
-      reinterpret_cast<uint8_t*>(a_q), scale_a, src2dst);
+cudaError_t launch_quant(const void* x, const int32_t* ids, const uint32_t* bits,
+                         const int32_t* base, int T, int H, int E, int K, void* a_q,
+                         float* scale_a, int32_t* src2dst, cudaStream_t st, bool pdl) {
+  return launch_kernel(permute_quant_kernel<VPT, BLOCK>, dim3(T), dim3(kQuantThreads), 0, st,
+                       pdl, reinterpret_cast<const __nv_bfloat16*>(x), ids, bits, base, H, E, K,
+                       reinterpret_cast<uint8_t*>(a_q), scale_a, src2dst);
 }
 
 }  // namespace
@@ -385,49 +389,55 @@ namespace {
 template <bool BLOCK>
 cudaError_t permute_quant(const void* x, const int32_t* ids, int T, int H, int E, int K,
                           void* a_q, float* scale_a, int32_t* src2dst, int32_t* offsets,
-                          void* ws, int* err, cudaStream_t st) {
+                          void* ws, int* err, cudaStream_t st, bool pdl) {
   if (T > 0 && T <= kSmallTokens && T * K <= kSmallRoute) {
     const int vpt = (H / 8 + kSmallThreads - 1) / kSmallThreads;
-    if (vpt <= 1) launch_small<1, BLOCK>(x, ids, T, H, E, K, a_q, scale_a, src2dst, offsets, err, st);
-    else if (vpt <= 2) launch_small<2, BLOCK>(x, ids, T, H, E, K, a_q, scale_a, src2dst, offsets, err, st);
-    else if (vpt <= 4) launch_small<4, BLOCK>(x, ids, T, H, E, K, a_q, scale_a, src2dst, offsets, err, st);
-    else if (vpt <= 8) launch_small<8, BLOCK>(x, ids, T, H, E, K, a_q, scale_a, src2dst, offsets, err, st);
-    else launch_small<16, BLOCK>(x, ids, T, H, E, K, a_q, scale_a, src2dst, offsets, err, st);
-    return cudaGetLastError();
+    if (vpt <= 1) return launch_small<1, BLOCK>(x, ids, T, H, E, K, a_q, scale_a, src2dst, offsets, err, st, pdl);
+    if (vpt <= 2) return launch_small<2, BLOCK>(x, ids, T, H, E, K, a_q, scale_a, src2dst, offsets, err, st, pdl);
+    if (vpt <= 4) return launch_small<4, BLOCK>(x, ids, T, H, E, K, a_q, scale_a, src2dst, offsets, err, st, pdl);
+    if (vpt <= 8) return launch_small<8, BLOCK>(x, ids, T, H, E, K, a_q, scale_a, src2dst, offsets, err, st, pdl);
+    return launch_small<16, BLOCK>(x, ids, T, H, E, K, a_q, scale_a, src2dst, offsets, err, st, pdl);
   }
   const int C = (T + 31) / 32;
   uint32_t* bits = reinterpret_cast<uint32_t*>(ws);
   int32_t* base = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(ws) +
                                              align_up((size_t)C * E * 4));
+  cudaError_t e;
   if (C > 0) {
     const int blocks = (C + kBitsWarps - 1) / kBitsWarps;
-    route_bits_kernel<<<blocks, kBitsWarps * 32, sizeof(uint32_t) * kBitsWarps * E, st>>>(
-        ids, T, E, K, bits, err);
+    if ((e = launch_kernel(route_bits_kernel, dim3(blocks), dim3(kBitsWarps * 32),
+                           sizeof(uint32_t) * kBitsWarps * E, st, pdl, ids, T, E, K, bits, err)))
+      return e;
   }
-  route_scan_kernel<<<1, 1024, 0, st>>>(bits, C, E, base, offsets);
+  if ((e = launch_kernel(route_scan_kernel, dim3(1), dim3(1024), 0, st, pdl, bits, C, E, base,
+                         offsets)))
+    return e;
   if (T > 0) {
     const int vpt = (H / 8 + kQuantThreads - 1) / kQuantThreads;
-    if (vpt <= 1) launch_quant<1, BLOCK>(x, ids, bits, base, T, H, E, K, a_q, scale_a, src2dst, st);
-    else if (vpt <= 2) launch_quant<2, BLOCK>(x, ids, bits, base, T, H, E, K, a_q, scale_a, src2dst, st);
-    else if (vpt <= 4) launch_quant<4, BLOCK>(x, ids, bits, base, T, H, E, K, a_q, scale_a, src2dst, st);
-    else if (vpt <= 8) launch_quant<8, BLOCK>(x, ids, bits, base, T, H, E, K, a_q, scale_a, src2dst, st);
-    else launch_quant<16, BLOCK>(x, ids, bits, base, T, H, E, K, a_q, scale_a, src2dst, st);
+    if (vpt <= 1) return launch_quant<1, BLOCK>(x, ids, bits, base, T, H, E, K, a_q, scale_a, src2dst, st, pdl);
+    if (vpt <= 2) return launch_quant<2, BLOCK>(x, ids, bits, base, T, H, E, K, a_q, scale_a, src2dst, st, pdl);
+    if (vpt <= 4) return launch_quant<4, BLOCK>(x, ids, bits, base, T, H, E, K, a_q, scale_a, src2dst, st, pdl);
+    if (vpt <= 8) return launch_quant<8, BLOCK>(x, ids, bits, base, T, H, E, K, a_q, scale_a, src2dst, st, pdl);
+    return launch_quant<16, BLOCK>(x, ids, bits, base, T, H, E, K, a_q, scale_a, src2dst, st, pdl);
   }
-  return cudaGetLastError();
+  return cudaSuccess;
 }
 
 }  // namespace
 
 cudaError_t launch_permute_quant(const void* x, const int32_t* ids, int T, int H, int E, int K,
                                  void* a_q, float* scale_a, int32_t* src2dst, int32_t* offsets,
-                                 void* ws, int* err, cudaStream_t st) {
-  return permute_quant<false>(x, ids, T, H, E, K, a_q, scale_a, src2dst, offsets, ws, err, st);
+                                 void* ws, int* err, cudaStream_t st, bool pdl) {
+  return permute_quant<false>(x, ids, T, H, E, K, a_q, scale_a, src2dst, offsets, ws, err, st,
+                              pdl);
 }
 
 cudaError_t launch_permute_quant_block(const void* x, const int32_t* ids, int T, int H, int E,
                                        int K, void* a_q, float* scale_a, int32_t* src2dst,
-                                       int32_t* offsets, void* ws, int* err, cudaStream_t st) {
-  return permute_quant<true>(x, ids, T, H, E, K, a_q, scale_a, src2dst, offsets, ws, err, st);
+                                       int32_t* offsets, void* ws, int* err, cudaStream_t st,
+                                       bool pdl) {
+  return permute_quant<true>(x, ids, T, H, E, K, a_q, scale_a, src2dst, offsets, ws, err, st,
+                             pdl);
 }
 
 }  // namespace moe

@@ -18,6 +18,7 @@ __global__ void __launch_bounds__(kThreads)
     unpermute_kernel(const __nv_bfloat16* __restrict__ down, const int32_t* __restrict__ src2dst,
                      const float* __restrict__ topk_w, int K, int H,
                      __nv_bfloat16* __restrict__ out, int* err) {
+  chain_entry();
   __shared__ int64_t src[32];
   __shared__ float w[32];
   const int t = blockIdx.x;
@@ -61,13 +62,13 @@ __global__ void __launch_bounds__(kThreads)
 }  // namespace
 
 cudaError_t launch_unpermute_sum(const void* down, const int32_t* src2dst, const float* w,
-                                 int T, int K, int H, void* out, int* err, cudaStream_t st) {
+                                 int T, int K, int H, void* out, int* err, cudaStream_t st,
+                                 bool pdl) {
   if (T == 0) return cudaSuccess;
   const dim3 grid(T, (H / 8 + kVecPerBlock - 1) / kVecPerBlock);
-  unpermute_kernel<<<grid, kThreads, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(down),
-                                           src2dst, w, K, H,
-                                           reinterpret_cast<__nv_bfloat16*>(out), err);
-  return cudaGetLastError();
+  return launch_kernel(unpermute_kernel, grid, dim3(kThreads), 0, st, pdl,
+                       reinterpret_cast<const __nv_bfloat16*>(down), src2dst, w, K, H,
+                       reinterpret_cast<__nv_bfloat16*>(out), err);
 }
 
 }  // namespace moe
