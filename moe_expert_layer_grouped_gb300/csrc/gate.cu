@@ -8,9 +8,10 @@
 // lanes' top-2 pairs when a group is a power-of-two number of whole lanes
 // (DeepSeek-V3: 4 lanes x 8 experts), else from a per-warp shared-memory copy
 // of the keys. The topk_group groups and then the top_k experts are picked
-// by repeated warp maxima over (order-preserving key, index) packed in 64
-// bits (key descending, index ascending), so the result does not depend on
-// scheduling and matches a sort with ties broken by the lower index.
+// one at a time by two warp reductions (redux.sync): the largest
+// order-preserving key, then the lowest index among the lanes holding it, so
+// the result does not depend on scheduling and matches a sort with ties
+// broken by the lower index.
 //
 // Every floating-point step that decides an id or a weight uses explicit
 // round-to-nearest intrinsics (no contraction), so the fp32 scores are
@@ -73,26 +74,18 @@ __device__ __forceinline__ void warp_argmax(float& v, int& i, float& carry) {
 }
 
 // Total order on fp32 keys as unsigned integers (larger float -> larger
-// integer; -0 and +0 equal, as in IEEE comparison), packed with the index so
-// that one unsigned max picks the larger key and, among equal keys, the lower
-// index. 0 is below every packed key.
-__device__ __forceinline__ uint64_t pack_key(float f, int idx) {
-  uint32_t u = __float_as_uint(f == 0.0f ? 0.0f : f);
-  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-  return ((uint64_t)u << 32) | (uint32_t)(0xFFFFFFFFu - (uint32_t)idx);
+// integer; -0 and +0 equal, as in IEEE comparison). 0 is below every key.
+__device__ __forceinline__ uint32_t order_key(float f) {
+  const uint32_t u = __float_as_uint(f == 0.0f ? 0.0f : f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-__device__ __forceinline__ int packed_index(uint64_t k) {
-  return (int)(0xFFFFFFFFu - (uint32_t)(k & 0xFFFFFFFFull));
-}
-
-__device__ __forceinline__ uint64_t warp_max_u64(uint64_t v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const uint64_t ov = __shfl_xor_sync(kFull, v, o);
-    v = ov > v ? ov : v;
-  }
-  return v;
+// Of the lanes' candidates (key, index), the one with the largest key and,
+// among equal keys, the lowest index (key 0: no candidate). Two warp
+// reductions: the maximum key, then the minimum index among lanes holding it.
+__device__ __forceinline__ int warp_pick(uint32_t key, uint32_t idx) {
+  const uint32_t m = __reduce_max_sync(kFull, key);
+  return (int)__reduce_min_sync(kFull, (key == m && key != 0u) ? idx : 0xFFFFFFFFu);
 }
 
 constexpr int kWarpsPerBlock = 4;
@@ -159,11 +152,10 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     const float gscore = (gsz >= 2) ? __fadd_rn(b1, b2) : b1;
     const int gid = (lane * EPL) / gsz;
     const bool has = lane * EPL < E;
+    const uint32_t gkey = has ? order_key(gscore) : 0u;
     kept = 0ull;
-    for (int it = 0; it < TG; ++it) {
-      const uint64_t c = (has && !((kept >> gid) & 1ull)) ? pack_key(gscore, gid) : 0ull;
-      kept |= 1ull << packed_index(warp_max_u64(c));
-    }
+    for (int it = 0; it < TG; ++it)
+      kept |= 1ull << warp_pick(((kept >> gid) & 1ull) ? 0u : gkey, (uint32_t)gid);
   } else if (TG < G) {
     // padded index e + e/32 keeps the group scans free of bank conflicts
     float* ks = keys_smem + warp * (E + (E >> 5) + 1);
@@ -219,22 +211,37 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     const int e = lane * EPL + j;
     if (e < E && ((kept >> (e / gsz)) & 1ull)) open |= 1u << j;
   }
+  uint32_t ok[EPL];
+#pragma unroll
+  for (int j = 0; j < EPL; ++j) ok[j] = order_key(key[j]);
+  // this lane's best open expert (the first of equal keys: the lower index)
+  uint32_t bk = 0u;
+  int bj = 0;
+#pragma unroll
+  for (int j = 0; j < EPL; ++j)
+    if (((open >> j) & 1u) && ok[j] > bk) {
+      bk = ok[j];
+      bj = j;
+    }
   float my_s = 0.0f, S = 0.0f, m0 = 0.0f;
   int my_id = 0;
   for (int k = 0; k < K; ++k) {
-    uint64_t c = 0ull;
-#pragma unroll
-    for (int j = 0; j < EPL; ++j) {
-      const uint64_t cj = ((open >> j) & 1u) ? pack_key(key[j], lane * EPL + j) : 0ull;
-      c = cj > c ? cj : c;
-    }
-    const int bi = packed_index(warp_max_u64(c));
-    const int slot = bi & (EPL - 1);
-    if (bi / EPL == lane) open &= ~(1u << slot);
+    const int bi = warp_pick(bk, (uint32_t)(lane * EPL + bj));
     float sel = sv[0];
 #pragma unroll
-    for (int j = 1; j < EPL; ++j) sel = (slot == j) ? sv[j] : sel;
+    for (int j = 1; j < EPL; ++j) sel = (bj == j) ? sv[j] : sel;
     const float bs = __shfl_sync(kFull, sel, bi / EPL);
+    if (bi / EPL == lane) {  // the winner's lane takes its next best
+      open &= ~(1u << bj);
+      bk = 0u;
+      bj = 0;
+#pragma unroll
+      for (int j = 0; j < EPL; ++j)
+        if (((open >> j) & 1u) && ok[j] > bk) {
+          bk = ok[j];
+          bj = j;
+        }
+    }
     float term = bs;
     if (!sigmoid) {
       if (k == 0) m0 = bs;

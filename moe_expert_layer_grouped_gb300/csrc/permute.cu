@@ -69,9 +69,19 @@ __global__ void __launch_bounds__(1024)
   const int per = (C + P - 1) / P;
   const int c0 = min(C, p * per), c1 = min(C, c0 + per);
 
+  // eight loads in flight per thread (the words are independent)
   int sum = 0;
-  if (active)
-    for (int c = c0; c < c1; ++c) sum += __popc(__ldg(bits + (int64_t)c * E + e));
+  if (active) {
+    int c = c0;
+    for (; c + 8 <= c1; c += 8) {
+      uint32_t w[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) w[u] = __ldg(bits + (int64_t)(c + u) * E + e);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) sum += __popc(w[u]);
+    }
+    for (; c < c1; ++c) sum += __popc(__ldg(bits + (int64_t)c * E + e));
+  }
   if (active) part[tid] = sum;
   __syncthreads();
   if (tid < E) {
@@ -112,7 +122,18 @@ __global__ void __launch_bounds__(1024)
   __syncthreads();
   if (active) {
     int run = excl[e] + part[tid];
-    for (int c = c0; c < c1; ++c) {
+    int c = c0;
+    for (; c + 8 <= c1; c += 8) {
+      uint32_t w[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) w[u] = __ldg(bits + (int64_t)(c + u) * E + e);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        base[(int64_t)(c + u) * E + e] = run;
+        run += __popc(w[u]);
+      }
+    }
+    for (; c < c1; ++c) {
       const int64_t i = (int64_t)c * E + e;
       base[i] = run;
       run += __popc(__ldg(bits + i));
