@@ -285,3 +285,29 @@ def test_repeated_calls_are_deterministic():
     a = layer(d["x"], d["logits"]).clone()
     for _ in range(3):
         assert torch.equal(layer(d["x"], d["logits"]), a)
+
+
+@pytest.mark.parametrize("name", ["tiny", "dsv3_decode_t128", "dsv3_prefill_t8192",
+                                  "dsv3_decode_t128_block"])
+def test_back_to_back_steps_share_the_workspace(name):
+    """Forwards issued back to back on one stream (no host synchronisation,
+    one workspace; the kernels of a step are chained to each other) give,
+    batch by batch, the output of the same batch run on its own."""
+    wl = synth.WORKLOADS[name]
+    d = synth.make_inputs(wl, seed=0, device=DEV)
+    layer = moe.MoELayer(d["w13"], d["s13"], d["w2"], d["s2"], d["bias"], wl.num_groups,
+                         wl.topk_group, wl.top_k, wl.scoring, wl.renormalize, wl.rsf, wl.T,
+                         n_shared=wl.n_shared, quant=wl.quant)
+    batches = [synth.make_inputs(wl, seed=s, device=DEV, weights=False) for s in (1, 2, 3, 4)]
+    alone = []
+    for b in batches:
+        alone.append(layer(b["x"], b["logits"]).clone())
+        torch.cuda.synchronize()
+    outs = [torch.empty_like(b["x"]) for b in batches]
+    for _ in range(2):
+        for b, o in zip(batches, outs):
+            layer(b["x"], b["logits"], out=o)
+    torch.cuda.synchronize()
+    assert moe.moe_device_status() == 0
+    for a, o in zip(alone, outs):
+        assert torch.equal(o.view(torch.int16), a.view(torch.int16))
