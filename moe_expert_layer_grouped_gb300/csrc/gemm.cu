@@ -12,11 +12,11 @@
 //
 // Design (one persistent CTA per SM, 192 threads, warp-specialised):
 //   warp 0      TMA producer: per stage KC chunks of 128 B of K, each the
-//               128 weight rows (two 64-row boxes: for SiLU the gate and the
-//               up rows) and the tile's tokens (rounded up to 16, covered
-//               exactly by boxes of 64/32/16 rows), into a STAGES-deep ring,
-//               128-byte swizzled; weight blocks read by one tile only are
-//               loaded evict-first, tokens evict-last.
+//               128 weight rows (for SiLU two 64-row boxes, the gate and the
+//               up rows; else one 128-row box) and the tile's tokens (rounded
+//               up to 16, covered exactly by boxes of 64/32/16 rows), into a
+//               STAGES-deep ring, 128-byte swizzled; weight blocks read by one
+//               tile only are loaded evict-first, tokens evict-last.
 //   warp 1      MMA issuer: tcgen05.mma.cta_group::1.kind::f8f6f4,
 //               M=128 x N x K=32, fp32 accumulator in tensor memory; two
 //               accumulators (2 x 256 columns) so the epilogue of tile i
@@ -123,7 +123,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int E = p.E;
 
   if (warp == 0 && lane == 0) {
-    ptx::prefetch_tensormap(&maps.w);
+    ptx::prefetch_tensormap(SILU ? &maps.w : &maps.w128);
     for (int i = 0; i < NXBOX; ++i) ptx::prefetch_tensormap(&maps.x[i]);
     for (int s = 0; s < STAGES; ++s) {
       ptx::mbar_init(&sm.full[s], 1);   // pair: only the even CTA's is used
@@ -220,8 +220,12 @@ __global__ void __launch_bounds__(THREADS, 1)
             uint8_t* xdst = sm.x[s][kc];
             if (PAIR) {
               const uint64_t pw = t.nch == 1 ? pol_w1 : pol_w;
-              ptx::tma_load_2d_pair(wdst, &maps.w, fb, kx, y0, pw);
-              ptx::tma_load_2d_pair(wdst + 64 * BK, &maps.w, fb, kx, y1, pw);
+              if (SILU) {
+                ptx::tma_load_2d_pair(wdst, &maps.w, fb, kx, y0, pw);
+                ptx::tma_load_2d_pair(wdst + 64 * BK, &maps.w, fb, kx, y1, pw);
+              } else {  // the tile's 128 contiguous weight rows in one box
+                ptx::tma_load_2d_pair(wdst, &maps.w128, fb, kx, y0, pw);
+              }
               int r = 0;
 #pragma unroll
               for (int i = 0; i < NXBOX; ++i) {
@@ -234,8 +238,12 @@ __global__ void __launch_bounds__(THREADS, 1)
               }
             } else {
               const uint64_t pw = t.nch == 1 ? pol_w1 : pol_w;
-              ptx::tma_load_2d(wdst, &maps.w, &sm.full[s], kx, y0, pw);
-              ptx::tma_load_2d(wdst + 64 * BK, &maps.w, &sm.full[s], kx, y1, pw);
+              if (SILU) {
+                ptx::tma_load_2d(wdst, &maps.w, &sm.full[s], kx, y0, pw);
+                ptx::tma_load_2d(wdst + 64 * BK, &maps.w, &sm.full[s], kx, y1, pw);
+              } else {
+                ptx::tma_load_2d(wdst, &maps.w128, &sm.full[s], kx, y0, pw);
+              }
               int r = 0;
 #pragma unroll
               for (int i = 0; i < NXBOX; ++i) {
@@ -615,7 +623,8 @@ cudaError_t launch_grouped_gemm(const void* A, const float* scale_a, const void*
   const bool silu = (epilogue == MOE_EPI_SILU_MUL);
   const bool small = (int64_t)M <= (int64_t)32 * E;  // few rows per expert (decode)
   Maps maps;
-  if (!make_tma_map_u8(&maps.w, B, (uint64_t)E * (uint64_t)N, (uint64_t)Kd, 64))
+  if (!make_tma_map_u8(&maps.w, B, (uint64_t)E * (uint64_t)N, (uint64_t)Kd, 64) ||
+      !make_tma_map_u8(&maps.w128, B, (uint64_t)E * (uint64_t)N, (uint64_t)Kd, 128))
     return cudaErrorNotSupported;
   for (int i = 0; i < NXBOX; ++i)
     if (!make_tma_map_u8(&maps.x[i], A, (uint64_t)M, (uint64_t)Kd, 64u >> i))

@@ -28,10 +28,11 @@ constexpr uint64_t DRAIN_NS = 200000000ull;   // bound of the waits after a time
 
 // Token boxes of 64/32/16 rows: a tile's tokens (rounded up to 16) are
 // covered exactly by 64-row boxes plus at most one 32- and one 16-row box
-// (64-row boxes measured fastest; weights also move in 64-row boxes).
+// (64-row boxes measured fastest for tokens).
 constexpr int NXBOX = 3;
 struct Maps {
   CUtensorMap w;           // weights: 64-row boxes
+  CUtensorMap w128;        // weights: 128-row boxes (per-token GEMM, bf16 epilogue)
   CUtensorMap x[NXBOX];    // tokens: box rows 64 >> i
 };
 
