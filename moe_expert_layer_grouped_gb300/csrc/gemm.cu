@@ -123,7 +123,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int E = p.E;
 
   if (warp == 0 && lane == 0) {
-    ptx::prefetch_tensormap(SILU ? &maps.w : &maps.w128);
+    ptx::prefetch_tensormap(SILU ? &maps.wgu : &maps.w128);
     for (int i = 0; i < NXBOX; ++i) ptx::prefetch_tensormap(&maps.x[i]);
     for (int s = 0; s < STAGES; ++s) {
       ptx::mbar_init(&sm.full[s], 1);   // pair: only the even CTA's is used
@@ -190,14 +190,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int rows = PAIR ? (t.ntok + 31) & ~31 : (t.ntok + 15) & ~15;
         const int half = rows / CS;
         const uint32_t bytes = KC * (CS * W_BYTES + (uint32_t)rows * BK);  // all CTAs' loads
-        int y0, y1;  // first rows of the two 64-row weight boxes
-        if (SILU) {  // gate rows [j0, j0+64) and up rows [I+j0, I+j0+64)
-          y0 = t.e * p.N + nb * 64;
-          y1 = y0 + p.I;
-        } else {
-          y0 = t.e * p.N + nb * BM;
-          y1 = y0 + 64;
-        }
+        const int y0 = t.e * p.N + nb * BM;  // bf16 epilogue: the tile's first weight row
         for (int ks = 0; ks < KS; ++ks) {
           if (!ptx::mbar_wait(&sm.empty[s], ph ^ 1u, &sm.abort, WAIT_NS)) {
             ok = false;
@@ -220,12 +213,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             uint8_t* xdst = sm.x[s][kc];
             if (PAIR) {
               const uint64_t pw = t.nch == 1 ? pol_w1 : pol_w;
-              if (SILU) {
-                ptx::tma_load_2d_pair(wdst, &maps.w, fb, kx, y0, pw);
-                ptx::tma_load_2d_pair(wdst + 64 * BK, &maps.w, fb, kx, y1, pw);
-              } else {  // the tile's 128 contiguous weight rows in one box
+              if (SILU)  // 64 gate rows, then the matching 64 up rows
+                ptx::tma_load_4d_pair(wdst, &maps.wgu, fb, kx, nb * 64, 0, t.e, pw);
+              else  // the tile's 128 contiguous weight rows
                 ptx::tma_load_2d_pair(wdst, &maps.w128, fb, kx, y0, pw);
-              }
               int r = 0;
 #pragma unroll
               for (int i = 0; i < NXBOX; ++i) {
@@ -238,12 +229,10 @@ __global__ void __launch_bounds__(THREADS, 1)
               }
             } else {
               const uint64_t pw = t.nch == 1 ? pol_w1 : pol_w;
-              if (SILU) {
-                ptx::tma_load_2d(wdst, &maps.w, &sm.full[s], kx, y0, pw);
-                ptx::tma_load_2d(wdst + 64 * BK, &maps.w, &sm.full[s], kx, y1, pw);
-              } else {
+              if (SILU)
+                ptx::tma_load_4d(wdst, &maps.wgu, &sm.full[s], kx, nb * 64, 0, t.e, pw);
+              else
                 ptx::tma_load_2d(wdst, &maps.w128, &sm.full[s], kx, y0, pw);
-              }
               int r = 0;
 #pragma unroll
               for (int i = 0; i < NXBOX; ++i) {
@@ -572,16 +561,26 @@ EncodeTiledFn encode_fn() {
 
 }  // namespace
 
-// Encoded maps are cached by (address, shape, box) so repeated calls on the
-// same buffers skip the driver-side encoding.
-bool make_tma_map_u8(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
-                     uint32_t box_rows) {
+namespace {
+
+// Encodes a u8 tensor map (128-byte swizzle, L2 256-byte promotion, zero fill
+// outside the tensor). Encoded maps are cached by (address, shape, strides,
+// box, device) so repeated calls on the same buffers skip the driver.
+bool encode_u8(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims,
+               const cuuint64_t* strides, const cuuint32_t* box) {
   struct Entry {
     const void* base;
-    uint64_t rows, cols;
-    uint32_t box;
-    int dev;
+    int rank, dev;
+    cuuint64_t dims[4], strides[3];
+    cuuint32_t box[4];
     CUtensorMap map;
+  };
+  auto same = [&](const Entry& c, int dev) {
+    if (c.base != base || c.rank != rank || c.dev != dev) return false;
+    for (int i = 0; i < rank; ++i)
+      if (c.dims[i] != dims[i] || c.box[i] != box[i] || (i + 1 < rank && c.strides[i] != strides[i]))
+        return false;
+    return true;
   };
   static std::mutex mu;
   static Entry cache[64];
@@ -591,26 +590,50 @@ bool make_tma_map_u8(CUtensorMap* m, const void* base, uint64_t rows, uint64_t c
   {
     std::lock_guard<std::mutex> lk(mu);
     for (const Entry& c : cache)
-      if (c.base == base && c.rows == rows && c.cols == cols && c.box == box_rows &&
-          c.dev == dev) {
+      if (same(c, dev)) {
         *m = c.map;
         return true;
       }
   }
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return false;
+  const cuuint32_t es[4] = {1, 1, 1, 1};
+  if (fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, (cuuint32_t)rank, const_cast<void*>(base), dims,
+         strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  Entry e = {};
+  e.base = base;
+  e.rank = rank;
+  e.dev = dev;
+  for (int i = 0; i < rank; ++i) {
+    e.dims[i] = dims[i];
+    e.box[i] = box[i];
+    if (i + 1 < rank) e.strides[i] = strides[i];
+  }
+  e.map = *m;
+  std::lock_guard<std::mutex> lk(mu);
+  cache[next] = e;
+  next = (next + 1) % 64;
+  return true;
+}
+
+}  // namespace
+
+bool make_tma_map_u8(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
+                     uint32_t box_rows) {
   const cuuint64_t dims[2] = {cols, rows};
   const cuuint64_t strides[1] = {cols};
   const cuuint32_t box[2] = {BK, box_rows};
-  const cuuint32_t es[2] = {1, 1};
-  if (fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
-         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-    return false;
-  std::lock_guard<std::mutex> lk(mu);
-  cache[next] = Entry{base, rows, cols, box_rows, dev, *m};
-  next = (next + 1) % 64;
-  return true;
+  return encode_u8(m, base, 2, dims, strides, box);
+}
+
+bool make_tma_map_gate_up(CUtensorMap* m, const void* base, uint64_t E, uint64_t I,
+                          uint64_t Kd) {
+  const cuuint64_t dims[4] = {Kd, I, 2, E};
+  const cuuint64_t strides[3] = {Kd, I * Kd, 2 * I * Kd};
+  const cuuint32_t box[4] = {BK, 64, 2, 1};
+  return encode_u8(m, base, 4, dims, strides, box);
 }
 
 }  // namespace gemm_common
@@ -623,8 +646,8 @@ cudaError_t launch_grouped_gemm(const void* A, const float* scale_a, const void*
   const bool silu = (epilogue == MOE_EPI_SILU_MUL);
   const bool small = (int64_t)M <= (int64_t)32 * E;  // few rows per expert (decode)
   Maps maps;
-  if (!make_tma_map_u8(&maps.w, B, (uint64_t)E * (uint64_t)N, (uint64_t)Kd, 64) ||
-      !make_tma_map_u8(&maps.w128, B, (uint64_t)E * (uint64_t)N, (uint64_t)Kd, 128))
+  if (silu ? !make_tma_map_gate_up(&maps.wgu, B, (uint64_t)E, (uint64_t)N / 2, (uint64_t)Kd)
+           : !make_tma_map_u8(&maps.w128, B, (uint64_t)E * (uint64_t)N, (uint64_t)Kd, 128))
     return cudaErrorNotSupported;
   for (int i = 0; i < NXBOX; ++i)
     if (!make_tma_map_u8(&maps.x[i], A, (uint64_t)M, (uint64_t)Kd, 64u >> i))

@@ -14,7 +14,8 @@
 // (128 rows per tile, which is one weight scale block), tokens on N (at most
 // BNMAX per tile, 16-token granularity). One persistent CTA per SM
 // (tcgen05.mma.cta_group::1), 352 threads:
-//   warp 0      TMA producer (one K block of weights and tokens per stage)
+//   warp 0      TMA producer (one K block of weights and tokens per stage;
+//               the weights of a K block in one box, as in moe_grouped_gemm)
 //   warp 1      MMA issuer (K=32 x 4 per K block)
 //   warps 2..9  epilogue: warp w reads TMEM lane quadrant w % 4 and the
 //               32-column token chunks cg, cg + 2, ... (cg = its column
@@ -131,7 +132,7 @@ __global__ void __launch_bounds__(BTHREADS, 1)
   const int KB = p.KB;
 
   if (warp == 0 && lane == 0) {
-    ptx::prefetch_tensormap(&maps.w);
+    ptx::prefetch_tensormap(SILU ? &maps.wgu : &maps.w128);
     for (int i = 0; i < NXBOX; ++i) ptx::prefetch_tensormap(&maps.x[i]);
     for (int s = 0; s < STAGES; ++s) {
       ptx::mbar_init(&sm.full[s], 1);
@@ -183,14 +184,7 @@ __global__ void __launch_bounds__(BTHREADS, 1)
         const int rows = (t.ntok + 15) & ~15;
         const uint32_t bytes = W_BYTES + (uint32_t)rows * BK;
         const uint64_t pw = t.nch == 1 ? pol_w1 : pol_w;
-        int y0, y1;  // first rows of the two 64-row weight boxes
-        if (SILU) {  // gate rows [j0, j0+64) and up rows [I+j0, I+j0+64)
-          y0 = t.e * p.N + t.nb * 64;
-          y1 = y0 + p.I;
-        } else {
-          y0 = t.e * p.N + t.nb * BM;
-          y1 = y0 + 64;
-        }
+        const int y0 = t.e * p.N + t.nb * BM;  // bf16 epilogue: the tile's first weight row
         for (int kb = 0; kb < KB; ++kb) {
           if (!ptx::mbar_wait(&sm.empty[s], ph ^ 1u, &sm.abort, WAIT_NS)) {
             ok = false;
@@ -200,8 +194,10 @@ __global__ void __launch_bounds__(BTHREADS, 1)
           armed |= 1u << s;
           armed_par = (armed_par & ~(1u << s)) | (ph << s);
           const int kx = kb * BK;
-          ptx::tma_load_2d(sm.w[s], &maps.w, &sm.full[s], kx, y0, pw);
-          ptx::tma_load_2d(sm.w[s] + 64 * BK, &maps.w, &sm.full[s], kx, y1, pw);
+          if (SILU)  // 64 gate rows, then the matching 64 up rows
+            ptx::tma_load_4d(sm.w[s], &maps.wgu, &sm.full[s], kx, t.nb * 64, 0, t.e, pw);
+          else
+            ptx::tma_load_2d(sm.w[s], &maps.w128, &sm.full[s], kx, y0, pw);
           int r = 0;
 #pragma unroll
           for (int i = 0; i < NXBOX; ++i) {
@@ -576,7 +572,8 @@ cudaError_t launch_grouped_gemm_block(const void* A, const float* scale_a, const
   const bool silu = (epilogue == MOE_EPI_SILU_MUL);
   const bool small = (int64_t)M <= (int64_t)32 * E;  // few rows per expert (decode)
   Maps maps;
-  if (!make_tma_map_u8(&maps.w, B, (uint64_t)E * (uint64_t)N, (uint64_t)Kd, 64))
+  if (silu ? !make_tma_map_gate_up(&maps.wgu, B, (uint64_t)E, (uint64_t)N / 2, (uint64_t)Kd)
+           : !make_tma_map_u8(&maps.w128, B, (uint64_t)E * (uint64_t)N, (uint64_t)Kd, 128))
     return cudaErrorNotSupported;
   for (int i = 0; i < NXBOX; ++i)
     if (!make_tma_map_u8(&maps.x[i], A, (uint64_t)M, (uint64_t)Kd, 64u >> i))

@@ -28,11 +28,16 @@ constexpr uint64_t DRAIN_NS = 200000000ull;   // bound of the waits after a time
 
 // Token boxes of 64/32/16 rows: a tile's tokens (rounded up to 16) are
 // covered exactly by 64-row boxes plus at most one 32- and one 16-row box
-// (64-row boxes measured fastest for tokens).
+// (64-row token boxes measured faster than 128-row ones).
 constexpr int NXBOX = 3;
+// Weights move in one box per 128 B of K: bf16 epilogue, the tile's 128
+// contiguous rows; SiLU, the w13 weights viewed as [E][2][I][Kd] so that one
+// box holds 64 gate rows followed by the matching 64 up rows (rows past I
+// read as 0). One TMA per K chunk measured faster than two 64-row boxes
+// (DeepSeek-V3 prefill w13 -12 %, w2 -5 %).
 struct Maps {
-  CUtensorMap w;           // weights: 64-row boxes
-  CUtensorMap w128;        // weights: 128-row boxes (per-token GEMM, bf16 epilogue)
+  CUtensorMap w128;        // weights [E*N, Kd]: 128-row boxes (bf16 epilogue)
+  CUtensorMap wgu;         // weights [E][2][I][Kd]: gate/up boxes (SiLU)
   CUtensorMap x[NXBOX];    // tokens: box rows 64 >> i
 };
 
@@ -148,6 +153,10 @@ __device__ __forceinline__ void build_tile_table(S& sm, const int32_t* offsets, 
 // driver cannot encode it.
 bool make_tma_map_u8(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
                      uint32_t box_rows);
+
+// Host: the gate/up map of a w13 tensor [E, 2I, Kd] (see Maps::wgu).
+bool make_tma_map_gate_up(CUtensorMap* m, const void* base, uint64_t E, uint64_t I,
+                          uint64_t Kd);
 
 }  // namespace gemm_common
 }  // namespace moe
