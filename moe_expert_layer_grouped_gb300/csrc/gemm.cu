@@ -97,6 +97,7 @@ struct Params {
   int M, N, Kd, E, I, NB, KB;
   int stream_weights;  // 1: each weight block is read by one tile (evict-first)
   int stall_stage;     // failure test: CTA 0 never loads its stage with this index (-1: none)
+  int w_stage_box;     // the weight map holds a stage per box (else a K chunk)
   int early_table;     // build the tile table before waiting for the previous kernel
 };
 
@@ -123,7 +124,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int E = p.E;
 
   if (warp == 0 && lane == 0) {
-    ptx::prefetch_tensormap(SILU ? &maps.wgu : &maps.w128);
+    ptx::prefetch_tensormap(&maps.w);
     for (int i = 0; i < NXBOX; ++i) ptx::prefetch_tensormap(&maps.x[i]);
     for (int s = 0; s < STAGES; ++s) {
       ptx::mbar_init(&sm.full[s], 1);   // pair: only the even CTA's is used
@@ -206,17 +207,39 @@ __global__ void __launch_bounds__(THREADS, 1)
           // failure test: the stage is armed but its bytes never come, so the
           // bounded waits run out
           const bool stall = blockIdx.x == 0 && gstage++ == p.stall_stage;
+          if (!stall && p.w_stage_box) {  // the stage's KC weight chunks in one box
+            const uint64_t pw = t.nch == 1 ? pol_w1 : pol_w;
+            if (PAIR) {
+              if (SILU)  // per chunk 64 gate rows, then the matching 64 up rows
+                ptx::tma_load_5d_pair(sm.w[s][0], &maps.w, fb, 0, nb * 64, 0, ks * KC, t.e, pw);
+              else  // per chunk the tile's 128 contiguous weight rows
+                ptx::tma_load_3d_pair(sm.w[s][0], &maps.w, fb, 0, y0, ks * KC, pw);
+            } else {
+              if (SILU)
+                ptx::tma_load_5d(sm.w[s][0], &maps.w, &sm.full[s], 0, nb * 64, 0, ks * KC, t.e, pw);
+              else
+                ptx::tma_load_3d(sm.w[s][0], &maps.w, &sm.full[s], 0, y0, ks * KC, pw);
+            }
+          }
 #pragma unroll
           for (int kc = 0; kc < (stall ? 0 : KC); ++kc) {
             const int kx = (ks * KC + kc) * BK;  // past Kd: zero-filled, adds nothing
-            uint8_t* wdst = sm.w[s][kc];
             uint8_t* xdst = sm.x[s][kc];
-            if (PAIR) {
+            if (!p.w_stage_box) {  // Kd % 128 != 0: the chunk's weights on their own
               const uint64_t pw = t.nch == 1 ? pol_w1 : pol_w;
-              if (SILU)  // 64 gate rows, then the matching 64 up rows
-                ptx::tma_load_4d_pair(wdst, &maps.wgu, fb, kx, nb * 64, 0, t.e, pw);
-              else  // the tile's 128 contiguous weight rows
-                ptx::tma_load_2d_pair(wdst, &maps.w128, fb, kx, y0, pw);
+              if (PAIR) {
+                if (SILU)
+                  ptx::tma_load_4d_pair(sm.w[s][kc], &maps.w, fb, kx, nb * 64, 0, t.e, pw);
+                else
+                  ptx::tma_load_2d_pair(sm.w[s][kc], &maps.w, fb, kx, y0, pw);
+              } else {
+                if (SILU)
+                  ptx::tma_load_4d(sm.w[s][kc], &maps.w, &sm.full[s], kx, nb * 64, 0, t.e, pw);
+                else
+                  ptx::tma_load_2d(sm.w[s][kc], &maps.w, &sm.full[s], kx, y0, pw);
+              }
+            }
+            if (PAIR) {
               int r = 0;
 #pragma unroll
               for (int i = 0; i < NXBOX; ++i) {
@@ -228,11 +251,6 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
               }
             } else {
-              const uint64_t pw = t.nch == 1 ? pol_w1 : pol_w;
-              if (SILU)
-                ptx::tma_load_4d(wdst, &maps.wgu, &sm.full[s], kx, nb * 64, 0, t.e, pw);
-              else
-                ptx::tma_load_2d(wdst, &maps.w128, &sm.full[s], kx, y0, pw);
               int r = 0;
 #pragma unroll
               for (int i = 0; i < NXBOX; ++i) {
@@ -571,8 +589,8 @@ bool encode_u8(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dim
   struct Entry {
     const void* base;
     int rank, dev;
-    cuuint64_t dims[4], strides[3];
-    cuuint32_t box[4];
+    cuuint64_t dims[5], strides[4];
+    cuuint32_t box[5];
     CUtensorMap map;
   };
   auto same = [&](const Entry& c, int dev) {
@@ -597,7 +615,7 @@ bool encode_u8(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dim
   }
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return false;
-  const cuuint32_t es[4] = {1, 1, 1, 1};
+  const cuuint32_t es[5] = {1, 1, 1, 1, 1};
   if (fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, (cuuint32_t)rank, const_cast<void*>(base), dims,
          strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
@@ -628,12 +646,33 @@ bool make_tma_map_u8(CUtensorMap* m, const void* base, uint64_t rows, uint64_t c
   return encode_u8(m, base, 2, dims, strides, box);
 }
 
-bool make_tma_map_gate_up(CUtensorMap* m, const void* base, uint64_t E, uint64_t I,
-                          uint64_t Kd) {
-  const cuuint64_t dims[4] = {Kd, I, 2, E};
-  const cuuint64_t strides[3] = {Kd, I * Kd, 2 * I * Kd};
-  const cuuint32_t box[4] = {BK, 64, 2, 1};
-  return encode_u8(m, base, 4, dims, strides, box);
+bool make_tma_map_weights(CUtensorMap* m, const void* base, bool silu, uint64_t E, uint64_t N,
+                          uint64_t Kd, uint32_t kc) {
+  if (!weights_stage_box(Kd)) {  // one chunk per box, zero past Kd
+    if (silu) {
+      const uint64_t I = N / 2;
+      const cuuint64_t dims[4] = {Kd, I, 2, E};
+      const cuuint64_t strides[3] = {Kd, I * Kd, 2 * I * Kd};
+      const cuuint32_t box[4] = {BK, 64, 2, 1};
+      return encode_u8(m, base, 4, dims, strides, box);
+    }
+    const cuuint64_t dims[2] = {Kd, E * N};
+    const cuuint64_t strides[1] = {Kd};
+    const cuuint32_t box[2] = {BK, BM};
+    return encode_u8(m, base, 2, dims, strides, box);
+  }
+  const uint64_t KB = Kd / BK;  // 128-byte chunks of K
+  if (silu) {
+    const uint64_t I = N / 2;
+    const cuuint64_t dims[5] = {BK, I, 2, KB, E};
+    const cuuint64_t strides[4] = {Kd, I * Kd, BK, 2 * I * Kd};
+    const cuuint32_t box[5] = {BK, 64, 2, kc, 1};
+    return encode_u8(m, base, 5, dims, strides, box);
+  }
+  const cuuint64_t dims[3] = {BK, E * N, KB};
+  const cuuint64_t strides[2] = {Kd, BK};
+  const cuuint32_t box[3] = {BK, BM, kc};
+  return encode_u8(m, base, 3, dims, strides, box);
 }
 
 }  // namespace gemm_common
@@ -645,9 +684,12 @@ cudaError_t launch_grouped_gemm(const void* A, const float* scale_a, const void*
   if (M == 0) return cudaSuccess;
   const bool silu = (epilogue == MOE_EPI_SILU_MUL);
   const bool small = (int64_t)M <= (int64_t)32 * E;  // few rows per expert (decode)
+  // K chunks per stage of the configuration launched below (the weight box
+  // holds one stage)
+  const int nb_blocks = silu ? (N / 2 + 63) / 64 : (N + BM - 1) / BM;
+  const uint32_t kc = small ? 2u : (nb_blocks % 2 == 0 ? (uint32_t)PAIR_KC : 1u);
   Maps maps;
-  if (silu ? !make_tma_map_gate_up(&maps.wgu, B, (uint64_t)E, (uint64_t)N / 2, (uint64_t)Kd)
-           : !make_tma_map_u8(&maps.w128, B, (uint64_t)E * (uint64_t)N, (uint64_t)Kd, 128))
+  if (!make_tma_map_weights(&maps.w, B, silu, (uint64_t)E, (uint64_t)N, (uint64_t)Kd, kc))
     return cudaErrorNotSupported;
   for (int i = 0; i < NXBOX; ++i)
     if (!make_tma_map_u8(&maps.x[i], A, (uint64_t)M, (uint64_t)Kd, 64u >> i))
@@ -672,6 +714,7 @@ cudaError_t launch_grouped_gemm(const void* A, const float* scale_a, const void*
   // weight row per stage); many (prefill): tiles of up to 256 tokens
   p.stream_weights = small ? 1 : 0;
   p.stall_stage = stall_stage;
+  p.w_stage_box = weights_stage_box((uint64_t)Kd) ? 1 : 0;
   p.early_table = early_table ? 1 : 0;
   if (small)
     return silu ? launch_cfg<64, 4, true, 1, 2>(maps, p, M, E, st, pdl)

@@ -132,7 +132,7 @@ __global__ void __launch_bounds__(BTHREADS, 1)
   const int KB = p.KB;
 
   if (warp == 0 && lane == 0) {
-    ptx::prefetch_tensormap(SILU ? &maps.wgu : &maps.w128);
+    ptx::prefetch_tensormap(&maps.w);
     for (int i = 0; i < NXBOX; ++i) ptx::prefetch_tensormap(&maps.x[i]);
     for (int s = 0; s < STAGES; ++s) {
       ptx::mbar_init(&sm.full[s], 1);
@@ -195,9 +195,9 @@ __global__ void __launch_bounds__(BTHREADS, 1)
           armed_par = (armed_par & ~(1u << s)) | (ph << s);
           const int kx = kb * BK;
           if (SILU)  // 64 gate rows, then the matching 64 up rows
-            ptx::tma_load_4d(sm.w[s], &maps.wgu, &sm.full[s], kx, t.nb * 64, 0, t.e, pw);
+            ptx::tma_load_5d(sm.w[s], &maps.w, &sm.full[s], 0, t.nb * 64, 0, kb, t.e, pw);
           else
-            ptx::tma_load_2d(sm.w[s], &maps.w128, &sm.full[s], kx, y0, pw);
+            ptx::tma_load_3d(sm.w[s], &maps.w, &sm.full[s], 0, y0, kb, pw);
           int r = 0;
 #pragma unroll
           for (int i = 0; i < NXBOX; ++i) {
@@ -571,9 +571,11 @@ cudaError_t launch_grouped_gemm_block(const void* A, const float* scale_a, const
   if (M == 0) return cudaSuccess;
   const bool silu = (epilogue == MOE_EPI_SILU_MUL);
   const bool small = (int64_t)M <= (int64_t)32 * E;  // few rows per expert (decode)
+  // one K block per stage: weight boxes of one chunk (Kd % 128 == 0, checked
+  // at the entry point, keeps the chunked weight view inside the tensor)
   Maps maps;
-  if (silu ? !make_tma_map_gate_up(&maps.wgu, B, (uint64_t)E, (uint64_t)N / 2, (uint64_t)Kd)
-           : !make_tma_map_u8(&maps.w128, B, (uint64_t)E * (uint64_t)N, (uint64_t)Kd, 128))
+  if (!weights_stage_box((uint64_t)Kd) ||
+      !make_tma_map_weights(&maps.w, B, silu, (uint64_t)E, (uint64_t)N, (uint64_t)Kd, 1))
     return cudaErrorNotSupported;
   for (int i = 0; i < NXBOX; ++i)
     if (!make_tma_map_u8(&maps.x[i], A, (uint64_t)M, (uint64_t)Kd, 64u >> i))

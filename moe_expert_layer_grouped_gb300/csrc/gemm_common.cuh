@@ -30,14 +30,17 @@ constexpr uint64_t DRAIN_NS = 200000000ull;   // bound of the waits after a time
 // covered exactly by 64-row boxes plus at most one 32- and one 16-row box
 // (64-row token boxes measured faster than 128-row ones).
 constexpr int NXBOX = 3;
-// Weights move in one box per 128 B of K: bf16 epilogue, the tile's 128
-// contiguous rows; SiLU, the w13 weights viewed as [E][2][I][Kd] so that one
-// box holds 64 gate rows followed by the matching 64 up rows (rows past I
-// read as 0). One TMA per K chunk measured faster than two 64-row boxes
-// (DeepSeek-V3 prefill w13 -12 %, w2 -5 %).
+// Weights. When Kd is a multiple of 128 the weights of a pipeline stage move
+// in one box: K is viewed as (128-byte chunk, chunk index) so that one box
+// holds the stage's KC chunks, each landing as its own [rows][128 B] block.
+// bf16 epilogue: [Kd/128][E*N][128], the tile's 128 rows per chunk. SiLU:
+// [E][Kd/128][2][I][128], 64 gate rows then the matching 64 up rows per chunk
+// (rows past I read as 0). Otherwise (the view would run into the next row)
+// one box per chunk over [E*N][Kd] or [E][2][I][Kd], zero past Kd. Fewer
+// copies per stage measured faster: one box per stage instead of two 64-row
+// boxes per chunk took DeepSeek-V3 prefill w13 from 1.96 to 1.69 ms.
 struct Maps {
-  CUtensorMap w128;        // weights [E*N, Kd]: 128-row boxes (bf16 epilogue)
-  CUtensorMap wgu;         // weights [E][2][I][Kd]: gate/up boxes (SiLU)
+  CUtensorMap w;           // weights (see above; SiLU: 5-D or 4-D, bf16: 3-D or 2-D)
   CUtensorMap x[NXBOX];    // tokens: box rows 64 >> i
 };
 
@@ -154,9 +157,12 @@ __device__ __forceinline__ void build_tile_table(S& sm, const int32_t* offsets, 
 bool make_tma_map_u8(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
                      uint32_t box_rows);
 
-// Host: the gate/up map of a w13 tensor [E, 2I, Kd] (see Maps::wgu).
-bool make_tma_map_gate_up(CUtensorMap* m, const void* base, uint64_t E, uint64_t I,
-                          uint64_t Kd);
+// Host: the weight map of a [E, N, Kd] tensor (see Maps::w): boxes of `kc`
+// K chunks when Kd % 128 == 0 (weights_stage_box), else of one chunk;
+// `silu`: the gate/up view of w13 (N = 2I).
+inline bool weights_stage_box(uint64_t Kd) { return Kd % BK == 0; }
+bool make_tma_map_weights(CUtensorMap* m, const void* base, bool silu, uint64_t E, uint64_t N,
+                          uint64_t Kd, uint32_t kc);
 
 }  // namespace gemm_common
 }  // namespace moe

@@ -236,6 +236,7 @@ GEMM_SHAPES = [
     ([130, 1, 0, 257, 128], 512, 256),
     ([300], 768, 384),
     ([17, 64, 200, 3], 320, 96),
+    ([400, 260], 512, 224),      # CTA pairs with K not a multiple of 128
     ([129, 127], 256, 7168),
     # few rows per expert overall (small token tiles) but one expert with
     # several token chunks
