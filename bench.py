@@ -179,11 +179,37 @@ def rank_seed(seed, rank):
     return seed + rank
 
 
+def _strip_comments(src):
+    """C++ source without comments and blank lines (the hash below follows
+    the code, not its comments)."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        if src.startswith("//", i):
+            i = src.find("\n", i)
+            if i < 0:
+                break
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        elif src[i] == '"':  # string literal (inline PTX): copied as is
+            j = i + 1
+            while j < n and src[j] != '"':
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        else:
+            out.append(src[i])
+            i += 1
+    return "\n".join(l.rstrip() for l in "".join(out).splitlines() if l.strip())
+
+
 def kernel_source_hash():
+    """Identifies the code of the grouped GEMM (comments and blank lines
+    ignored), to tell whether a recorded ncu capture was taken on it."""
     h = hashlib.sha256()
     for f in ("gemm.cu", "gemm_common.cuh", "ptx.cuh", "common.cuh"):
-        with open(os.path.join(ROOT, "moe_expert_layer_grouped_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "moe_expert_layer_grouped_gb300", "csrc", f)) as fh:
+            h.update(_strip_comments(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -11,12 +11,12 @@
 // expert's token count is padded to a multiple of 16 rather than of 128.
 //
 // Design (one persistent CTA per SM, 192 threads, warp-specialised):
-//   warp 0      TMA producer: per stage KC chunks of 128 B of K, each the
-//               128 weight rows (for SiLU two 64-row boxes, the gate and the
-//               up rows; else one 128-row box) and the tile's tokens (rounded
-//               up to 16, covered exactly by boxes of 64/32/16 rows), into a
-//               STAGES-deep ring, 128-byte swizzled; weight blocks read by one
-//               tile only are loaded evict-first, tokens evict-last.
+//   warp 0      TMA producer: per stage KC chunks of 128 B of K: the 128
+//               weight rows of every chunk in one box (for SiLU 64 gate rows
+//               then the matching 64 up rows), and per chunk the tile's tokens
+//               (rounded up to 16, covered exactly by boxes of 64/32/16 rows),
+//               into a STAGES-deep ring, 128-byte swizzled; weight blocks read
+//               by one tile only are loaded evict-first, tokens evict-last.
 //   warp 1      MMA issuer: tcgen05.mma.cta_group::1.kind::f8f6f4,
 //               M=128 x N x K=32, fp32 accumulator in tensor memory; two
 //               accumulators (2 x 256 columns) so the epilogue of tile i
