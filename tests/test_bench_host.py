@@ -1,0 +1,75 @@
+"""Host-side logic of bench.py (CPU): the algorithmic work counted for the
+roofline, the launches per forward, and the kernel-code hash that decides
+whether a recorded ncu traffic figure still describes the GEMM."""
+import os
+import sys
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+from moe_expert_layer_grouped_gb300 import synth  # noqa: E402
+
+
+def test_strip_comments_keeps_code_and_string_literals():
+    src = ('int a; // line comment\n'
+           '/* block\n   comment */ int b = 1;\n'
+           '\n'
+           'asm("tcgen05.ld // not a comment /* either */");\n'
+           'x /* inline */ y;\n')
+    out = bench._strip_comments(src)
+    assert "comment" not in out.replace("not a comment", "")
+    assert 'asm("tcgen05.ld // not a comment /* either */");' in out
+    assert out.splitlines() == ['int a;', ' int b = 1;',
+                                'asm("tcgen05.ld // not a comment /* either */");', 'x  y;']
+
+
+def test_code_hash_ignores_comments_but_not_code():
+    base = "int f(int x) {\n  return x + 1;  // add one\n}\n"
+    same = "// header\nint f(int x) {\n\n  return x + 1;  /* plus one */\n}\n"
+    other = "int f(int x) {\n  return x + 2;\n}\n"
+    s = bench._strip_comments
+    assert s(base) == s(same)
+    assert s(base) != s(other)
+
+
+def test_recorded_traffic_needs_the_current_code(tmp_path, monkeypatch):
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    # the kernel sources the hash reads
+    src = tmp_path / "moe_expert_layer_grouped_gb300" / "csrc"
+    src.mkdir(parents=True)
+    for f in ("gemm.cu", "gemm_common.cuh", "ptx.cuh", "common.cuh"):
+        (src / f).write_text(f"// {f}\nint {f.split('.')[0]};\n")
+    h = bench.kernel_source_hash()
+    (prof / "grouped_gemm_w13_wl.md").write_text(
+        f"- dram_bytes_per_launch: 123456\n- kernel_source_sha256_16: {h}\n")
+    assert bench.recorded_traffic("wl") == 123456.0
+    (src / "gemm.cu").write_text("// gemm.cu, comment edited\nint gemm;\n")
+    assert bench.recorded_traffic("wl") == 123456.0  # comments only
+    (src / "gemm.cu").write_text("int gemm2;\n")
+    assert bench.recorded_traffic("wl") is None      # the code changed
+    assert bench.recorded_traffic("missing") is None
+
+
+def test_step_work_counts_active_experts_only():
+    wl = synth.Workload("w", 4, 128, 64, 4, 1, 1, 2, synth.SOFTMAX, True, 1.0, "none")
+    off = np.array([0, 3, 3, 8, 8], dtype=np.int64)  # experts 0 and 2 active
+    w = bench.step_work(wl, [off])
+    T, H, I, K, E = 4, 128, 64, 2, 4
+    M = T * K
+    w13 = 2 * (2 * I * H + 2 * I * 4)
+    assert w["active"] == 2
+    assert w["gemm13_bytes"] == w13 + M * H + M * 4 + M * I * 2 + (E + 1) * 4
+    assert w["flops13"] == 2.0 * M * 2 * I * H
+    assert w["flops2"] == 2.0 * M * H * I
+
+
+def test_launches_per_forward():
+    dec = synth.WORKLOADS["dsv3_decode_t128"]   # T*K = 1024 slots: one pre-reorder launch
+    pre = synth.WORKLOADS["dsv3_prefill_t8192"]  # three
+    assert bench.launches_per_forward(dec) == 6
+    assert bench.launches_per_forward(pre) == 8
