@@ -17,6 +17,11 @@ DeepSeek-V3-style and a Mixtral-style MoE layer):
   dsv3_skewed_t16384 T=16384 same layer as decode; bias +3.0 on the 26
                      experts with e % 10 == 0, -10 on the 32 with e % 8 == 7,
                      the rest ~N(0, 0.1)
+  dsv3_skewed_half_t16384 the same with +0.225 on the 26 hot experts: the
+                     gate sends them about half of the token-expert
+                     assignments (49.8 % with seed 0, 47-52 % over seeds;
+                     ~185 experts active, up to 3400-5000 rows each) instead
+                     of all of them
   dsv3_decode_t128_e32 / dsv3_prefill_t2048_e32: the DeepSeek-V3 layer with
                      32 experts, small cases for profiling
   *_shared           the same layers plus n_shared shared experts (DeepSeek-V3
@@ -54,6 +59,7 @@ class Workload:
     bias: str  # "none" | "normal" | "zero" | "skewed"
     n_shared: int = 0  # shared experts, stored as experts E .. E+n_shared-1
     quant: str = "token"  # "token": per-channel weight scales; "block": 128 x 128 blocks
+    hot_bias: float = 3.0  # "skewed": the bias of the experts with e % 10 == 0
 
     @property
     def M(self):
@@ -73,6 +79,11 @@ WORKLOADS = {
                               True, 1.0, "none"),
     "dsv3_skewed_t16384": Workload("dsv3_skewed_t16384", 16384, 7168, 2048, 256, 8, 4, 8,
                                    SIGMOID, True, 2.5, "skewed"),
+    # about half of the assignments to the 26 hot experts: with +3.0 every
+    # token takes 8 of them (each group holds at least three, and 4 groups
+    # are kept), so the hot bias is lowered until the gate splits ~50 / 50
+    "dsv3_skewed_half_t16384": Workload("dsv3_skewed_half_t16384", 16384, 7168, 2048, 256, 8,
+                                        4, 8, SIGMOID, True, 2.5, "skewed", hot_bias=0.225),
     # the same layer with 32 experts (1.4 GB of weights): small cases for
     # profiling the decode (weight-streaming) and prefill (tensor) GEMMs
     "dsv3_decode_t128_e32": Workload("dsv3_decode_t128_e32", 128, 7168, 2048, 32, 8, 4, 8,
@@ -146,7 +157,7 @@ def router_bias(wl: Workload, seed, device="cpu") -> Optional[torch.Tensor]:
     b = normal((wl.E,), 0.1, seed, "bias", device)
     if wl.bias == "skewed":
         e = torch.arange(wl.E, device=device)
-        b = torch.where(e % 10 == 0, torch.full_like(b, 3.0), b)
+        b = torch.where(e % 10 == 0, torch.full_like(b, wl.hot_bias), b)
         b = torch.where(e % 8 == 7, torch.full_like(b, -10.0), b)
     return b
 

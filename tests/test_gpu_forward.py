@@ -74,9 +74,24 @@ def test_forward_dsv3_decode_t128(seed):
                     n_sample=None if seed == 0 else 32)
 
 
-@pytest.mark.parametrize("name", ["dsv3_prefill_t8192", "mixtral_t4096", "dsv3_skewed_t16384"])
+@pytest.mark.parametrize("name", ["dsv3_prefill_t8192", "mixtral_t4096", "dsv3_skewed_t16384",
+                                  "dsv3_skewed_half_t16384"])
 def test_forward_large_sampled(name):
     _check_workload(synth.WORKLOADS[name], 0, device_gen=True, n_sample=40)
+
+
+def test_skewed_half_device_inputs_split_about_half():
+    # the benchmark draws its inputs on the device (another generator than
+    # the CPU's): the hot experts still take about half of the assignments
+    wl = synth.WORKLOADS["dsv3_skewed_half_t16384"]
+    for seed in (0, 1):
+        d = synth.make_inputs(wl, seed=seed, device=DEV, weights=False)
+        ids, _ = moe.moe_gate(d["logits"], d["bias"], wl.num_groups, wl.topk_group, wl.top_k,
+                              wl.scoring, wl.renormalize, wl.rsf)
+        ids = ids.cpu().numpy()
+        share = np.mean(ids % 10 == 0)
+        assert 0.40 <= share <= 0.60, (seed, share)
+        assert not np.any(ids % 8 == 7)
 
 
 @pytest.mark.parametrize("T,H,I,E,G,TG,K,scoring,rsf", [
