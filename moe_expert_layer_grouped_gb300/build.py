@@ -19,7 +19,8 @@ LIB = os.path.join(LIB_DIR, "libmoe_gb300.so")
 
 SOURCES = ["api.cu", "gate.cu", "permute.cu", "gemm.cu", "gemm_block.cu", "act_quant.cu",
            "unpermute.cu"]
-HEADERS = ["common.cuh", "ptx.cuh", "internal.h"]
+# every header beside the sources is a rebuild input (a new one cannot be missed)
+HEADERS = sorted(f for f in os.listdir(SRC) if f.endswith((".cuh", ".h")))
 
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",

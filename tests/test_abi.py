@@ -23,6 +23,14 @@ def lib():
     return moe.load()
 
 
+def test_every_source_and_header_is_a_build_input():
+    # a file left out would either not be compiled or, for a header, not
+    # trigger a rebuild when only it changed
+    files = os.listdir(cuda_build.SRC)
+    assert sorted(f for f in files if f.endswith(".cu")) == sorted(cuda_build.SOURCES)
+    assert sorted(f for f in files if f.endswith((".cuh", ".h"))) == sorted(cuda_build.HEADERS)
+
+
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
