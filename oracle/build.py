@@ -20,8 +20,9 @@ def build(force: bool = False) -> str:
     src = os.path.join(HERE, "oracle.c")
     hdr = os.path.join(HERE, "oracle.h")
     os.makedirs(OUT_DIR, exist_ok=True)
+    inputs = (src, hdr, os.path.abspath(__file__))  # the flags live in this file
     if (not force and os.path.exists(LIB)
-            and os.path.getmtime(LIB) >= max(os.path.getmtime(src), os.path.getmtime(hdr))):
+            and os.path.getmtime(LIB) >= max(os.path.getmtime(f) for f in inputs)):
         return LIB
     tmp = LIB + f".tmp{os.getpid()}"
     cmd = ["gcc", *CFLAGS, src, "-o", tmp, "-lm"]
