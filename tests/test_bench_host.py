@@ -1,7 +1,9 @@
 """Host-side logic of bench.py (CPU): the algorithmic work counted for the
 roofline, the launches per forward, and the kernel-code hash that decides
 whether a recorded ncu traffic figure still describes the GEMM."""
+import json
 import os
+import subprocess
 import sys
 
 import numpy as np
@@ -73,3 +75,27 @@ def test_launches_per_forward():
     pre = synth.WORKLOADS["dsv3_prefill_t8192"]  # three
     assert bench.launches_per_forward(dec) == 6
     assert bench.launches_per_forward(pre) == 8
+
+
+def test_reference_arm_prints_the_contract_line():
+    # the reference arm times the oracle on the host cores: no GPU needed
+    env = {k: v for k, v in os.environ.items() if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK")}
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--workload", "tiny", "--steps", "2", "--warmup", "1"],
+                       env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+              "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+              "cpu_baseline", "e2e"):
+        assert k in d, k
+    assert d["impl"] == "reference" and d["steps"] == 2 and d["warmup"] == 1
+    assert d["n_gpus"] == 1 and d["higher_is_better"] is True and d["value"] > 0
+    assert d["config"]["workload"] == "tiny"
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1
+    assert cb["unit"] == d["unit"] and "tiny" in cb["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
