@@ -2,7 +2,7 @@
 
 Each case plants one mistake in a copy of oracle/oracle.c (a dropped
 factor, a flipped tie-break, a wrong rounding, a transposed or shifted
-index, a swapped operand), builds that copy with the oracle's own flags,
+index, a swapped operand, a wrong constant or loop bound), builds that copy with the oracle's own flags,
 points the oracle module at it, and runs the pins that guard that part: at
 least one of them must fail. The real oracle source is never modified; the
 planted copy lives in pytest's temporary directory (CPU only).
@@ -98,6 +98,50 @@ MUTATIONS = [
      "                 (double)sbe[(int64_t)kb * NBk + (n / QB)];",
      [pins.test_grouped_gemm_block_exact_with_power_of_two_scales,
       pins.test_grouped_gemm_block_with_uniform_scales_is_per_token_gemm]),
+    ("per-token scale divided by 488",
+     "    float sc = fmaxf(amax, 1e-10f) / 448.0f;\n    scale[r] = sc;",
+     "    float sc = fmaxf(amax, 1e-10f) / 488.0f;\n    scale[r] = sc;",
+     [pins.test_row_quant_closed_form]),
+    ("requant amax of h before its bf16 rounding",
+     "          hb[j] = oracle_bf16_round(g / (1.0 + exp(-g)) * u);\n"
+     "          float v = fabsf(bf16_to_f32(hb[j]));",
+     "          hb[j] = oracle_bf16_round(g / (1.0 + exp(-g)) * u);\n"
+     "          float v = (float)fabs(g / (1.0 + exp(-g)) * u);",
+     [pins.test_layer_token_path_equals_step_path_and_is_linear_in_rsf,
+      pins.test_layer_single_expert_is_dense_fp8_mlp]),
+    ("sigmoid(g) * u instead of silu(g) * u",
+     "      h[r * I + j] = g / (1.0 + exp(-g)) * u;",
+     "      h[r * I + j] = 1.0 / (1.0 + exp(-g)) * u;",
+     [pins.test_silu_mul_closed_forms]),
+    ("one group more than topk_group kept",
+     "    for (int i = 0; i < TG; ++i) allowed[gkv[i].idx] = 1;",
+     "    for (int i = 0; i <= TG && i < G; ++i) allowed[gkv[i].idx] = 1;",
+     [_gate_handworked, _gate_bruteforce]),
+    ("renormalised over every expert instead of the selected ones",
+     "      for (int k = 0; k < K; ++k) S = S + s[ids[k]];",
+     "      for (int k = 0; k < E; ++k) S = S + s[k];",
+     [_gate_handworked, pins.test_gate_weight_sum_is_rsf_and_linear]),
+    ("FP8 subnormals decoded one binade low",
+     "    v = ldexp((double)m, -9);",
+     "    v = ldexp((double)m, -10);",
+     [pins.test_e4m3_decode_matches_format_and_torch]),
+    ("GEMM without the per-row activation scale",
+     "        c[n] = acc * (double)scale_a[r] * (double)scale_b[(int64_t)e * N + n];",
+     "        c[n] = acc * (double)scale_b[(int64_t)e * N + n];",
+     [pins.test_grouped_gemm_scales_per_row_and_channel]),
+    ("GEMM takes the experts' weights in reverse order",
+     "      const uint8_t* Be = B + (int64_t)e * N * Kd;\n      for (int n = 0; n < N; ++n) {",
+     "      const uint8_t* Be = B + (int64_t)(E - 1 - e) * N * Kd;\n"
+     "      for (int n = 0; n < N; ++n) {",
+     [pins.test_grouped_gemm_exact_integers]),
+    ("sigmoid with the sign of the exponent flipped",
+     "  float e = oracle_exp32(-x);",
+     "  float e = oracle_exp32(x);",
+     [pins.test_sigmoid32_within_three_ulp]),
+    ("pre-reorder scatters the next token's scale",
+     "      scale_a[d] = sc[t];",
+     "      scale_a[d] = sc[(t + 1) % T];",
+     [pins.test_permute_quant_scatter]),
 ]
 
 
