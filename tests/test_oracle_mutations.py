@@ -142,6 +142,22 @@ MUTATIONS = [
      "      scale_a[d] = sc[t];",
      "      scale_a[d] = sc[(t + 1) % T];",
      [pins.test_permute_quant_scatter]),
+    ("softmax renormalised over every expert",
+     "      for (int k = 0; k < K; ++k) S = S + oracle_exp32(l[ids[k]] - m);",
+     "      for (int e = 0; e < E; ++e) S = S + oracle_exp32(l[e] - m);",
+     [_gate_handworked, pins.test_gate_weight_sum_is_rsf_and_linear]),
+    ("softmax normaliser misses the last expert",
+     "      for (int e = 0; e < E; ++e) Z = Z + oracle_exp32(l[e] - m);",
+     "      for (int e = 0; e < E - 1; ++e) Z = Z + oracle_exp32(l[e] - m);",
+     [pins.test_gate_no_renormalise]),
+    ("unrenormalised weights lose routed_scaling_factor",
+     "      for (int k = 0; k < K; ++k) w[k] = s[ids[k]] * rsf;",
+     "      for (int k = 0; k < K; ++k) w[k] = s[ids[k]];",
+     [pins.test_gate_no_renormalise]),
+    ("softmax selects the smallest logits",
+     "      kv[e].key = l[e];",
+     "      kv[e].key = -l[e];",
+     [_gate_handworked, pins.test_gate_weight_sum_is_rsf_and_linear]),
 ]
 
 
