@@ -158,6 +158,24 @@ MUTATIONS = [
      "      kv[e].key = l[e];",
      "      kv[e].key = -l[e];",
      [_gate_handworked, pins.test_gate_weight_sum_is_rsf_and_linear]),
+    ("block GEMM uses the first block's activation scale throughout",
+     "          acc += part * (double)scale_a[(int64_t)r * KB + kb] *",
+     "          acc += part * (double)scale_a[(int64_t)r * KB] *",
+     [pins.test_grouped_gemm_block_exact_with_power_of_two_scales]),
+    ("block pre-reorder copies only the first block scale",
+     "      memcpy(scale_a + d * nb, sc + (int64_t)t * nb, sizeof(float) * (size_t)nb);",
+     "      memcpy(scale_a + d * nb, sc + (int64_t)t * nb, sizeof(float));",
+     [pins.test_layer_block_token_path_equals_step_path_with_shared_expert]),
+    ("block layer picks the w13 weight-scale row modulo instead of by division",
+     "            acc += part * (double)sa[kb] * (double)sbe[(int64_t)(n / QB) * KBH + kb];",
+     "            acc += part * (double)sa[kb] * (double)sbe[(int64_t)(n % (N13 / QB)) * KBH + kb];",
+     [pins.test_layer_block_single_expert_is_dense_block_mlp,
+      pins.test_layer_block_token_path_equals_step_path_with_shared_expert]),
+    ("block layer requant carries the amax across blocks",
+     "        for (int b = 0; b < KBI; ++b) {\n          float amax2 = 0.0f;",
+     "        float amax2 = 0.0f;\n        for (int b = 0; b < KBI; ++b) {",
+     [pins.test_layer_block_single_expert_is_dense_block_mlp,
+      pins.test_layer_block_token_path_equals_step_path_with_shared_expert]),
 ]
 
 

@@ -589,8 +589,10 @@ def _dense_block_mlp(x, w13e, s13e, w2e, s2e):
 
 
 def test_layer_block_single_expert_is_dense_block_mlp():
+    # H and I both span two 128-channel blocks, so a scale carried from one
+    # block to the next (activations, h or weights) changes the result
     rng = np.random.default_rng(53)
-    T, H, I = 6, 256, 128
+    T, H, I = 6, 256, 256
     x, logits, w13, s13, w2, s2 = _random_block_layer(rng, T, H, I, 1)
     out, ids, w = oracle.forward_tokens_block(x, logits, None, w13, s13, w2, s2, 1, 1, 1,
                                               oracle.SOFTMAX, True, 1.0)
@@ -601,7 +603,7 @@ def test_layer_block_single_expert_is_dense_block_mlp():
 
 def test_layer_block_token_path_equals_step_path_with_shared_expert():
     rng = np.random.default_rng(54)
-    T, H, I, E, S = 20, 256, 128, 8, 1
+    T, H, I, E, S = 20, 256, 256, 8, 1
     x, logits, w13, s13, w2, s2 = _random_block_layer(rng, T, H, I, E + S)
     bias = (rng.standard_normal(E) * 0.1).astype(np.float32)
     args = (4, 2, 3, oracle.SIGMOID, True, 2.5)
