@@ -30,6 +30,15 @@ def _gate_bruteforce():
         pins.test_gate_bruteforce_enumeration(*args)
 
 
+# the per-token layer's expert loop: a routed slot's expert, then the shared
+# experts stored after the E routed ones (the next lines make the site unique)
+_SHARED_SITE = ("        const int e = k < K ? ids[k] : E + (k - K);\n"
+                "        const uint8_t* We = w13 + (int64_t)e * N13 * H;\n"
+                "        for (int n = 0; n < N13; ++n) {\n"
+                "          const uint8_t* b = We + (int64_t)n * H;\n"
+                "          double acc = 0.0;\n"
+                "          for (int hh = 0; hh < H; ++hh) acc += a[hh] * g_e4m3_lut[b[hh]];")
+
 # (name, text in oracle.c, planted replacement, pins expected to catch it)
 MUTATIONS = [
     ("renormalised weights lose routed_scaling_factor",
@@ -176,6 +185,18 @@ MUTATIONS = [
      "        float amax2 = 0.0f;\n        for (int b = 0; b < KBI; ++b) {",
      [pins.test_layer_block_single_expert_is_dense_block_mlp,
       pins.test_layer_block_token_path_equals_step_path_with_shared_expert]),
+    ("shared expert taken as the last routed expert",
+     _SHARED_SITE, _SHARED_SITE.replace("E + (k - K);", "E + (k - K) - 1;"),
+     [lambda: pins.test_layer_shared_experts_add_dense_mlps(1)]),
+    ("up rows dequantised with the gate rows' weight scales",
+     "          c[n] = acc * (double)sa * (double)s13[(int64_t)e * N13 + n];",
+     "          c[n] = acc * (double)sa * (double)s13[(int64_t)e * N13 + (n % I)];",
+     [pins.test_layer_single_expert_is_dense_fp8_mlp,
+      pins.test_layer_token_path_equals_step_path_and_is_linear_in_rsf]),
+    ("each expert's output overwrites the token's sum",
+     "          o[cc] += wk * (acc * (double)sa2 * (double)s2[(int64_t)e * H + cc]);",
+     "          o[cc] = wk * (acc * (double)sa2 * (double)s2[(int64_t)e * H + cc]);",
+     [pins.test_layer_token_path_equals_step_path_and_is_linear_in_rsf]),
 ]
 
 
