@@ -197,6 +197,21 @@ MUTATIONS = [
      "          o[cc] += wk * (acc * (double)sa2 * (double)s2[(int64_t)e * H + cc]);",
      "          o[cc] = wk * (acc * (double)sa2 * (double)s2[(int64_t)e * H + cc]);",
      [pins.test_layer_token_path_equals_step_path_and_is_linear_in_rsf]),
+    ("expert histogram counted one slot early",
+     "  for (int64_t i = 0; i < n; ++i) offsets[topk_ids[i] + 1] += 1;",
+     "  for (int64_t i = 0; i < n; ++i) offsets[topk_ids[i]] += 1;",
+     # only the routing pin: its destinations reach past M, so a pin that
+     # scatters rows through them would write outside the buffer
+     [lambda: pins.test_route_invariants(37, 8, 2, False)]),
+    ("an expert's rows all land on its first row",
+     "    src2dst[i] = offsets[e] + fill[e];",
+     "    src2dst[i] = offsets[e];",
+     [lambda: pins.test_route_invariants(37, 8, 2, False),
+      pins.test_permute_then_unpermute_is_identity]),
+    ("post-reorder reads the slot index instead of its permuted row",
+     "      const double* d = down + (int64_t)src2dst[(int64_t)t * K + k] * H;",
+     "      const double* d = down + ((int64_t)t * K + k) * H;",
+     [pins.test_permute_then_unpermute_is_identity]),
 ]
 
 
