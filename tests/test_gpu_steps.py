@@ -78,6 +78,40 @@ def test_gate_sigmoid_sweep_bit_exact():
     assert bad.size == 0, (x[bad[:5], 0], got[bad[:5]], ref[bad[:5]])
 
 
+def _oracle_in_threads(fn, x, pool, parts=16):
+    """fn over slices of x on a thread pool (the oracle's C calls run without
+    the interpreter lock, so the slices run on separate cores)."""
+    out = np.empty_like(x)
+    cut = np.linspace(0, x.size, parts + 1).astype(np.int64)
+
+    def job(i):
+        out[cut[i]:cut[i + 1]] = fn(x[cut[i]:cut[i + 1]])
+
+    list(pool.map(job, range(parts)))
+    return out
+
+
+def test_sigmoid_bit_exact_on_every_fp32_up_to_88():
+    """Every fp32 x with |x| <= 88 (2.24e9 values of both signs, zeros and
+    subnormals included), the range where exp(-x) stays finite: the gate's
+    weight for E=1, K=1, no renormalisation and rsf=1 is the fp32 sigmoid,
+    and it equals the oracle's bit for bit."""
+    from concurrent.futures import ThreadPoolExecutor
+    chunk = 1 << 27
+    top = 0x42B00000  # bit pattern of 88.0f
+    with ThreadPoolExecutor(max_workers=16) as pool:
+        for sign in (0, 0x80000000):
+            for start in range(0, top + 1, chunk):
+                bits = np.arange(start, min(start + chunk, top + 1), dtype=np.uint32)
+                x = (bits | np.uint32(sign)).view(np.float32)
+                _, w = moe.moe_gate(torch.from_numpy(x).view(-1, 1).to(DEV), None, 1, 1, 1,
+                                    synth.SIGMOID, False, 1.0)
+                got = w.view(-1).cpu().numpy().view(np.uint32)
+                ref = _oracle_in_threads(oracle.sigmoid32, x, pool).view(np.uint32)
+                bad = np.nonzero(got != ref)[0]
+                assert bad.size == 0, (x[bad[:5]], got[bad[:5]], ref[bad[:5]])
+
+
 # ---------------------------------------------------------------------------
 # pre-reorder + quantisation
 # ---------------------------------------------------------------------------
