@@ -99,3 +99,16 @@ def test_reference_arm_prints_the_contract_line():
     assert cb["unit"] == d["unit"] and "tiny" in cb["sample"]
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}
+
+
+def test_peaks_come_from_the_measured_file_else_the_fallback(tmp_path, monkeypatch):
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    pk = bench.peaks()                      # no file: the earlier measurements
+    assert pk["source"] == "fallback"
+    assert (pk["hbm"], pk["bf16"], pk["bf16_sustained"]) == (6800.0, 1900.0, 1700.0)
+    (tmp_path / "MEASURED_PEAKS.json").write_text(json.dumps(
+        {"hbm_gbs": 6681.8, "bf16_tflops": 1850.0, "bf16_tflops_sustained": 1765.2,
+         "sm_max_mhz": 2070}))
+    pk = bench.peaks()
+    assert pk["source"] == "measured"
+    assert (pk["hbm"], pk["bf16"], pk["bf16_sustained"]) == (6681.8, 1850.0, 1765.2)
