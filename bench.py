@@ -251,11 +251,20 @@ def make_batches(wl, seed, dev, synth):
     return batches
 
 
-def time_forward(layer, batches, steps, warmup, torch, out):
+def align(torch, barrier):
+    """Every rank's work done and, with several ranks, all ranks at the same
+    point: taken on both sides of a timed region."""
+    torch.cuda.synchronize()
+    if barrier is not None:
+        barrier()
+        torch.cuda.synchronize()
+
+
+def time_forward(layer, batches, steps, warmup, torch, out, barrier=None):
     for i in range(warmup):
         x, l = batches[i % len(batches)]
         layer(x, l, out=out)
-    torch.cuda.synchronize()
+    align(torch, barrier)
     st = torch.cuda.current_stream()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(st)
@@ -263,7 +272,7 @@ def time_forward(layer, batches, steps, warmup, torch, out):
         x, l = batches[i % len(batches)]
         layer(x, l, out=out)
     e1.record(st)
-    torch.cuda.synchronize()
+    align(torch, barrier)
     return e0.elapsed_time(e1)
 
 
@@ -380,7 +389,7 @@ def time_graph(layer, batches, steps, warmup, torch):
     return total / steps
 
 
-def time_e2e(layer, batches, steps, warmup, torch):
+def time_e2e(layer, batches, steps, warmup, torch, barrier=None):
     xs = [b[0].cpu().pin_memory() for b in batches]
     ls = [b[1].cpu().pin_memory() for b in batches]
     T, H = batches[0][0].shape
@@ -388,7 +397,7 @@ def time_e2e(layer, batches, steps, warmup, torch):
     for i in range(warmup):
         j = i % len(batches)
         layer.forward_host(xs[j], ls[j], outs[j])
-    torch.cuda.synchronize()
+    align(torch, barrier)
     st = torch.cuda.current_stream()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(st)
@@ -396,13 +405,14 @@ def time_e2e(layer, batches, steps, warmup, torch):
         j = i % len(batches)
         layer.forward_host(xs[j], ls[j], outs[j])
     e1.record(st)
-    torch.cuda.synchronize()
+    align(torch, barrier)
     h2d = xs[0].numel() * 2 + ls[0].numel() * 4
     d2h = outs[0].numel() * 2
     return e0.elapsed_time(e1) / steps, h2d, d2h
 
 
-def run_workload(moe, synth, torch, wl, seed, steps, warmup, dev, pk, want_clocks):
+def run_workload(moe, synth, torch, wl, seed, steps, warmup, dev, pk, want_clocks,
+                 barrier=None):
     d = synth.make_inputs(wl, seed=seed, device=dev, weights=True)
     layer = moe.MoELayer(d["w13"], d["s13"], d["w2"], d["s2"], d["bias"], wl.num_groups,
                          wl.topk_group, wl.top_k, wl.scoring, wl.renormalize, wl.rsf, wl.T,
@@ -414,7 +424,7 @@ def run_workload(moe, synth, torch, wl, seed, steps, warmup, dev, pk, want_clock
         clocks.start()
         time.sleep(0.3)
     t0 = time.time()
-    ms_total = time_forward(layer, batches, steps, warmup, torch, out)
+    ms_total = time_forward(layer, batches, steps, warmup, torch, out, barrier)
     t1 = time.time()
     if clocks:
         clocks.stop()
@@ -505,12 +515,14 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    r = run_workload(moe, synth, torch, wl, seed, steps, warmup, dev, pk, want_clocks=True)
+    barrier = dist.barrier if world > 1 else None
+    r = run_workload(moe, synth, torch, wl, seed, steps, warmup, dev, pk, want_clocks=True,
+                     barrier=barrier)
     ms_total = max_over_ranks(r["ms_total"], dist if world > 1 else None, dev)
     ms = ms_total / steps
     value = job_tokens_per_s(wl.T, world, ms)
 
-    e2e_ms, h2d, d2h = time_e2e(r["layer"], r["batches"], steps, warmup, torch)
+    e2e_ms, h2d, d2h = time_e2e(r["layer"], r["batches"], steps, warmup, torch, barrier)
     graph_ms = time_graph(r["layer"], r["batches"], steps, warmup, torch)
     e2e_ms = max_over_ranks(e2e_ms, dist if world > 1 else None, dev)
 

@@ -112,3 +112,21 @@ def test_peaks_come_from_the_measured_file_else_the_fallback(tmp_path, monkeypat
     pk = bench.peaks()
     assert pk["source"] == "measured"
     assert (pk["hbm"], pk["bf16"], pk["bf16_sustained"]) == (6681.8, 1850.0, 1765.2)
+
+
+def test_timed_regions_are_bracketed_by_sync_and_barrier():
+    calls = []
+
+    class _Cuda:
+        @staticmethod
+        def synchronize():
+            calls.append("sync")
+
+    class _Torch:
+        cuda = _Cuda
+
+    bench.align(_Torch, None)                     # one rank: the device only
+    assert calls == ["sync"]
+    calls.clear()
+    bench.align(_Torch, lambda: calls.append("barrier"))
+    assert calls == ["sync", "barrier", "sync"]   # own work done, ranks met, then time
