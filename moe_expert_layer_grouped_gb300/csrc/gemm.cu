@@ -11,10 +11,11 @@
 // expert's token count is padded to a multiple of 16 rather than of 128.
 //
 // Design (one persistent CTA per SM, 192 threads, warp-specialised):
-//   warp 0      TMA producer: per stage KC chunks of 128 B of K: the 128
-//               weight rows of every chunk in one box (for SiLU 64 gate rows
-//               then the matching 64 up rows), and per chunk the tile's tokens
-//               (rounded up to 16, covered exactly by boxes of 64/32/16 rows),
+//   warp 0      TMA producer: per stage KC chunks of 128 B of K: the tile's
+//               128 weight rows of all KC chunks in one box (one box per chunk
+//               when Kd % 128 != 0; for SiLU 64 gate rows then the matching
+//               64 up rows), and per chunk the tile's tokens (rounded up to
+//               16, covered exactly by boxes of 64/32/16 rows),
 //               into a STAGES-deep ring, 128-byte swizzled; weight blocks read
 //               by one tile only are loaded evict-first, tokens evict-last.
 //   warp 1      MMA issuer: tcgen05.mma.cta_group::1.kind::f8f6f4,
