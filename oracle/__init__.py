@@ -56,6 +56,10 @@ def lib():
             "oracle_forward_tokens_block": (i32, [P, P, P, P, P, P, P, i32, i32, i32, i32,
                                                   i32, i32, i32, i32, i32, i32, f32, P, i32,
                                                   P, P, P]),
+            "oracle_e2m1_decode": (ctypes.c_double, [ctypes.c_uint8]),
+            "oracle_e2m1_encode_n": (None, [P, P, i64]),
+            "oracle_nvfp4_quant": (None, [P, i64, i32, f32, P, P]),
+            "oracle_grouped_gemm_nvfp4": (None, [P, P, f32, P, P, P, P, i32, i32, i32, i32, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -370,3 +374,58 @@ def forward_steps_block(x_bits, logits, bias, w13, s13, w2, s2, num_groups, topk
     out = unpermute_sum(down, src2dst, w)
     return dict(ids=ids, w=w, a_q=a_q, scale_a=sa, src2dst=src2dst, offsets=offsets,
                 c13=C13, h=h, h_bits=h_bits, q2=q2, scale_a2=sa2, down=down, out=out)
+
+
+# ---------------------------------------------------------------------------
+# NVFP4: E2M1 codes (one per byte, 0..15), one E4M3 block scale per 16
+# elements along K, one fp32 global scale per tensor
+# ---------------------------------------------------------------------------
+FB = 16
+
+
+def e2m1_decode_table():
+    """Value of each of the 16 E2M1 codes (fp64)."""
+    return np.array([lib().oracle_e2m1_decode(q) for q in range(16)], np.float64)
+
+
+def e2m1_decode(q):
+    return e2m1_decode_table()[np.asarray(q, np.uint8) & 0xF]
+
+
+def e2m1_encode(x):
+    x = _c(x, np.float32)
+    q = np.empty(x.shape, np.uint8)
+    lib().oracle_e2m1_encode_n(_p(x), _p(q), x.size)
+    return q
+
+
+def nvfp4_quant(x_bits, g):
+    """bf16 [R,C] (bit patterns), global scale g > 0 -> (E2M1 codes [R,C],
+    E4M3 block-scale codes [R, C/16])."""
+    x = _c(x_bits, np.uint16)
+    R, C = x.shape
+    assert C % FB == 0 and g > 0
+    q = np.empty((R, C), np.uint8)
+    sb = np.empty((R, C // FB), np.uint8)
+    lib().oracle_nvfp4_quant(_p(x), R, C, float(g), _p(q), _p(sb))
+    return q, sb
+
+
+def grouped_gemm_nvfp4(A, sa, ga, B, sb, gb, offsets):
+    """A [M,Kd] and B [E,N,Kd] E2M1 codes; sa [M,Kd/16] and sb [E,N,Kd/16]
+    E4M3 codes; ga the activations' global scale, gb [E] the weights'.
+    Returns the fp64 product [M, N]."""
+    A = _c(A, np.uint8)
+    B = _c(B, np.uint8)
+    sa = _c(sa, np.uint8)
+    sb = _c(sb, np.uint8)
+    gb = _c(gb, np.float32)
+    off = _c(offsets, np.int32)
+    M, Kd = A.shape
+    E, N, Kd2 = B.shape
+    assert Kd == Kd2 and off.size == E + 1 and Kd % FB == 0 and gb.shape == (E,)
+    assert sa.shape == (M, Kd // FB) and sb.shape == (E, N, Kd // FB)
+    C = np.empty((M, N), np.float64)
+    lib().oracle_grouped_gemm_nvfp4(_p(A), _p(sa), float(ga), _p(B), _p(sb), _p(gb), _p(off),
+                                    M, N, Kd, E, _p(C))
+    return C

@@ -17,7 +17,9 @@
  * or property fixed by the pages or by mathematics (hand-worked gate cases,
  * brute-force top-k enumeration, sum-of-weights invariant, permutation
  * bijection and identity, exhaustive FP8 nearest-value search, exact-integer
- * and dense-matmul special cases of the GEMM, a dense MLP for E=1,K=1).
+ * and dense-matmul special cases of the GEMM, a dense MLP for E=1,K=1; for
+ * NVFP4 the format's magnitude list, an exhaustive E2M1 nearest-even search,
+ * the quantiser in closed form and exact power-of-two-scaled GEMMs).
  */
 #include "oracle.h"
 
@@ -811,4 +813,124 @@ int oracle_forward_tokens_block(const uint16_t* x, const float* logits, const fl
     free(sa2);
   }
   return status;
+}
+
+/* ------------------------------------------------------------------------
+ * NVFP4: the FP4 format the pages deploy DeepSeek-R1 in (modelopt_fp4 and
+ * ModelOptNvFp4FusedMoEMethod, "[1/2] sgl-kernel: Fuse routed scaling factor
+ * into select_experts", sglang #8364, Motivation and Highlights). The pages
+ * name the format without writing it out. Reading, from NVIDIA's published
+ * NVFP4 description:
+ *  - elements are E2M1 codes (sign bit, 2 exponent bits with bias 1, one
+ *    mantissa bit): magnitudes 0, 0.5 (the one subnormal), 1, 1.5, 2, 3, 4,
+ *    6; encoding rounds to nearest with ties to the even code and saturates
+ *    to +-6;
+ *  - every 16 consecutive elements along K share one E4M3 block scale;
+ *  - the tensor has one fp32 global scale g (an input: for weights it ships
+ *    with the checkpoint, for activations it is the calibrated input scale);
+ *  - value = e2m1(q) * e4m3(sb) * g.
+ * Quantising a block: sb = e4m3((amax / 6) / g) (fp32 operations), then
+ * q = e2m1(x / (e4m3(sb) * g)); a block whose scale decodes to 0 gets zero
+ * codes. Codes are kept one per byte here (values 0..15).
+ * ---------------------------------------------------------------------- */
+#define FB 16
+
+double oracle_e2m1_decode(uint8_t q) {
+  int s = (q >> 3) & 1;
+  int e = (q >> 1) & 3;
+  int m = q & 1;
+  double v = (e == 0) ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);
+  return s ? -v : v;
+}
+
+uint8_t oracle_e2m1_encode(float x) {
+  uint32_t bits;
+  memcpy(&bits, &x, 4);
+  uint8_t sign = (bits >> 31) ? 0x8 : 0x0;
+  float a = fabsf(x);
+  if (a >= 6.0f) return (uint8_t)(sign | 0x7); /* saturate (also +-inf) */
+  if (a < 1.0f) {
+    /* subnormal range: units of 0.5; m == 2 is the smallest normal, 1.0,
+     * whose code is also 2 */
+    int m = (int)rintf(a * 2.0f); /* exact scaling */
+    return (uint8_t)(sign | m);
+  }
+  int ex;
+  frexpf(a, &ex);
+  int E = ex - 1;                 /* a in [2^E, 2^(E+1)), E in 0..2 */
+  float u = ldexpf(a, 1 - E);     /* units of the ulp 2^(E-1): u in [2, 4) */
+  int m = (int)rintf(u);
+  if (m == 4) {
+    m = 2;
+    E += 1;
+  }
+  int code = ((E + 1) << 1) | (m - 2);
+  if (code > 0x7) code = 0x7;
+  return (uint8_t)(sign | code);
+}
+
+void oracle_e2m1_encode_n(const float* x, uint8_t* q, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) q[i] = oracle_e2m1_encode(x[i]);
+}
+
+void oracle_nvfp4_quant(const uint16_t* x, int64_t R, int C, float g, uint8_t* q,
+                        uint8_t* sb) {
+  const int nb = C / FB;
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < R; ++r) {
+    for (int b = 0; b < nb; ++b) {
+      const uint16_t* blk = x + r * C + (int64_t)b * FB;
+      float amax = 0.0f;
+      for (int c = 0; c < FB; ++c) {
+        float v = fabsf(bf16_to_f32(blk[c]));
+        if (v > amax) amax = v;
+      }
+      uint8_t s = oracle_e4m3_encode((amax / 6.0f) / g);
+      sb[r * nb + b] = s;
+      float step = (float)oracle_e4m3_decode(s) * g;
+      for (int c = 0; c < FB; ++c)
+        q[r * C + (int64_t)b * FB + c] =
+            step > 0.0f ? oracle_e2m1_encode(bf16_to_f32(blk[c]) / step) : 0;
+    }
+  }
+}
+
+void oracle_grouped_gemm_nvfp4(const uint8_t* A, const uint8_t* sa, float ga, const uint8_t* B,
+                               const uint8_t* sb, const float* gb, const int32_t* offsets,
+                               int M, int N, int Kd, int E, double* C) {
+  init_lut();
+  const int KB = Kd / FB;
+  int32_t* row_e = (int32_t*)malloc(sizeof(int32_t) * (size_t)(M > 0 ? M : 1));
+  for (int r = 0; r < M; ++r) row_e[r] = -1;
+  for (int e = 0; e < E; ++e)
+    for (int r = offsets[e]; r < offsets[e + 1] && r < M; ++r) row_e[r] = e;
+#pragma omp parallel
+  {
+    double* a = (double*)malloc(sizeof(double) * (size_t)Kd);
+#pragma omp for schedule(dynamic, 1)
+    for (int r = 0; r < M; ++r) {
+      int e = row_e[r];
+      double* c = C + (int64_t)r * N;
+      if (e < 0) {
+        for (int n = 0; n < N; ++n) c[n] = 0.0;
+        continue;
+      }
+      for (int k = 0; k < Kd; ++k) a[k] = oracle_e2m1_decode(A[(int64_t)r * Kd + k]);
+      const uint8_t* Be = B + (int64_t)e * N * Kd;
+      const uint8_t* sbe = sb + (int64_t)e * N * KB;
+      for (int n = 0; n < N; ++n) {
+        const uint8_t* b = Be + (int64_t)n * Kd;
+        double acc = 0.0;
+        for (int kb = 0; kb < KB; ++kb) {
+          double part = 0.0; /* exact: products are multiples of 1/4 below 37 */
+          for (int k = kb * FB; k < (kb + 1) * FB; ++k) part += a[k] * oracle_e2m1_decode(b[k]);
+          acc += part * g_e4m3_lut[sa[(int64_t)r * KB + kb]] *
+                 g_e4m3_lut[sbe[(int64_t)n * KB + kb]];
+        }
+        c[n] = acc * (double)ga * (double)gb[e];
+      }
+    }
+    free(a);
+  }
+  free(row_e);
 }

@@ -150,6 +150,26 @@ int oracle_forward_tokens_block(const uint16_t* x, const float* logits, const fl
                                 const int64_t* tokens, int n_tok, double* out,
                                 int32_t* ids_out, float* w_out);
 
+/* NVFP4 (E2M1 elements, one E4M3 scale per 16 elements along K, one fp32
+ * global scale per tensor). Codes one per byte (0..15). */
+double oracle_e2m1_decode(uint8_t q);
+/* nearest E2M1 code, ties to the even code, saturating to +-6 */
+uint8_t oracle_e2m1_encode(float x);
+void oracle_e2m1_encode_n(const float* x, uint8_t* q, int64_t n);
+
+/* x bf16 [R,C] (C % 16 == 0), global scale g > 0 -> q [R,C] E2M1 codes,
+ * sb [R, C/16] E4M3 block-scale codes: sb = e4m3((amax/6)/g),
+ * q = e2m1(x / (e4m3(sb) * g)), zero codes where the scale decodes to 0. */
+void oracle_nvfp4_quant(const uint16_t* x, int64_t R, int C, float g, uint8_t* q,
+                        uint8_t* sb);
+
+/* C[r,n] = ga * gb[e] * sum_kb (sum_{k in kb} e2m1(A[r,k]) e2m1(B[e,n,k])) *
+ * e4m3(sa[r,kb]) * e4m3(sb[e,n,kb]) in fp64, kb the 16-element blocks of K.
+ * A [M,Kd], sa [M,Kd/16], B [E,N,Kd], sb [E,N,Kd/16], gb [E]. */
+void oracle_grouped_gemm_nvfp4(const uint8_t* A, const uint8_t* sa, float ga, const uint8_t* B,
+                               const uint8_t* sb, const float* gb, const int32_t* offsets,
+                               int M, int N, int Kd, int E, double* C);
+
 #ifdef __cplusplus
 }
 #endif

@@ -212,6 +212,32 @@ MUTATIONS = [
      "      const double* d = down + (int64_t)src2dst[(int64_t)t * K + k] * H;",
      "      const double* d = down + ((int64_t)t * K + k) * H;",
      [pins.test_permute_then_unpermute_is_identity]),
+    ("E2M1 subnormal ties rounded away from zero",
+     "    int m = (int)rintf(a * 2.0f); /* exact scaling */",
+     "    int m = (int)roundf(a * 2.0f); /* exact scaling */",
+     [pins.test_e2m1_encode_exhaustive_nearest_even]),
+    ("E2M1 normal ties rounded away from zero",
+     "  float u = ldexpf(a, 1 - E);     /* units of the ulp 2^(E-1): u in [2, 4) */\n"
+     "  int m = (int)rintf(u);",
+     "  float u = ldexpf(a, 1 - E);     /* units of the ulp 2^(E-1): u in [2, 4) */\n"
+     "  int m = (int)roundf(u);",
+     [pins.test_e2m1_encode_exhaustive_nearest_even]),
+    ("E2M1 saturating to 4",
+     "  if (a >= 6.0f) return (uint8_t)(sign | 0x7); /* saturate (also +-inf) */",
+     "  if (a >= 6.0f) return (uint8_t)(sign | 0x6); /* saturate (also +-inf) */",
+     [pins.test_e2m1_encode_exhaustive_nearest_even]),
+    ("NVFP4 block scale from amax / 4",
+     "      uint8_t s = oracle_e4m3_encode((amax / 6.0f) / g);",
+     "      uint8_t s = oracle_e4m3_encode((amax / 4.0f) / g);",
+     [pins.test_nvfp4_quant_closed_form]),
+    ("NVFP4 GEMM without the weights' global scale",
+     "        c[n] = acc * (double)ga * (double)gb[e];",
+     "        c[n] = acc * (double)ga;",
+     [pins.test_grouped_gemm_nvfp4_exact_with_power_of_two_scales]),
+    ("NVFP4 GEMM weight block scales in reverse K order",
+     "                 g_e4m3_lut[sbe[(int64_t)n * KB + kb]];",
+     "                 g_e4m3_lut[sbe[(int64_t)n * KB + (KB - 1 - kb)]];",
+     [pins.test_grouped_gemm_nvfp4_exact_with_power_of_two_scales]),
 ]
 
 

@@ -618,3 +618,128 @@ def test_layer_block_token_path_equals_step_path_with_shared_expert():
                                              s2[:E], *args)
     ref = _dense_block_mlp(x, w13[E], s13[E], w2[E], s2[E])
     np.testing.assert_allclose(out - base, ref, rtol=1e-9, atol=1e-12 * np.abs(out).max())
+
+
+# ---------------------------------------------------------------------------
+# NVFP4 (E2M1 elements, an E4M3 scale per 16 elements, an fp32 global scale)
+# ---------------------------------------------------------------------------
+# the eight E2M1 magnitudes of the published format, codes 0..7 in order;
+# codes 8..15 are their negatives
+E2M1_MAGNITUDES = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+
+
+def _e2m1_nearest_even(v):
+    """Brute force: the code of the nearest E2M1 magnitude to |v| (ties to the
+    even code, beyond 6 the largest), with the sign of v in bit 3."""
+    mag = np.asarray(E2M1_MAGNITUDES)
+    a = np.minimum(np.abs(v.astype(np.float64)), 6.0)
+    d = np.abs(a[:, None] - mag[None, :])
+    best = d.min(1, keepdims=True)
+    tied = d == best
+    # among the nearest codes take the even one (there are at most two)
+    code = np.where(tied[:, ::2].any(1), np.argmax(tied & (np.arange(8) % 2 == 0), 1),
+                    np.argmax(tied, 1))
+    return (code | (np.signbit(v) << 3)).astype(np.uint8)
+
+
+def test_e2m1_decode_matches_the_format():
+    t = oracle.e2m1_decode_table()
+    assert t[:8].tolist() == E2M1_MAGNITUDES
+    assert t[8:].tolist() == [-m for m in E2M1_MAGNITUDES]
+    assert np.signbit(t[8])  # code 8 is -0
+
+
+def test_e2m1_encode_exhaustive_nearest_even():
+    # every fp32 in [2^-4, 2^4): all rounding boundaries, the subnormal 0.5
+    # and saturation from 6 up
+    bits = np.arange(np.float32(2.0 ** -4).view(np.uint32), np.float32(16.0).view(np.uint32),
+                     dtype=np.uint32)
+    x = bits.view(np.float32)
+    got = oracle.e2m1_encode(x)
+    for lo in range(0, x.size, 1 << 22):
+        sl = slice(lo, lo + (1 << 22))
+        assert np.array_equal(got[sl], _e2m1_nearest_even(x[sl]))
+    # negatives, zeros, tiny values, infinities
+    rng = np.random.default_rng(11)
+    y = np.concatenate([-x[rng.integers(0, x.size, 1 << 16)],
+                        np.array([0.0, -0.0, 1e-30, -1e-30, 0.25, 0.75, 1.25, 1.75, 2.5, 3.5,
+                                  5.0, -5.0, 6.0, 7.0, 1e30, np.inf, -np.inf], np.float32)])
+    assert np.array_equal(oracle.e2m1_encode(y), _e2m1_nearest_even(y))
+
+
+def test_nvfp4_quant_closed_form():
+    rng = np.random.default_rng(12)
+    R, C = 24, 128
+    x = rng.standard_normal((R, C)) * (10.0 ** rng.uniform(-2, 2, (R, 1)))
+    x[2, 16:32] = 0.0       # an all-zero block
+    xb = _bf16_bits(x)
+    xv = oracle.bf16_to_f64(xb)
+    for g in (np.float32(2.0 ** -3), np.float32(0.0137)):
+        q, sb = oracle.nvfp4_quant(xb, g)
+        blocks = np.abs(xv.reshape(R, C // 16, 16)).max(2).astype(np.float32)
+        # block scale: the E4M3 code of (amax / 6) / g in fp32
+        assert np.array_equal(sb, oracle.e4m3_encode((blocks / np.float32(6.0)) / g))
+        step = (oracle.e4m3_decode(sb).astype(np.float32) * g).astype(np.float32)
+        stepx = np.repeat(step, 16, 1)
+        r = np.where(stepx > 0, xv.astype(np.float32) / np.where(stepx > 0, stepx, 1), 0)
+        exp_q = np.where(stepx > 0, _e2m1_nearest_even(r.ravel().astype(np.float32))
+                         .reshape(R, C), 0)
+        assert np.array_equal(q, exp_q)
+        # the block maximum lands on +-6 (its scale is within 2^-4 of amax/6)
+        am = np.abs(xv.reshape(R, C // 16, 16)).argmax(2)
+        qb = q.reshape(R, C // 16, 16)
+        top = np.take_along_axis(qb, am[..., None], 2)[..., 0] & 0x7
+        assert np.all(top[blocks > 0] == 7)
+        assert np.all(sb[2, 1] == 0) and np.all(q[2, 16:32] == 0)
+
+
+def _nvfp4_problem(rng, counts, N, Kd):
+    E = len(counts)
+    off = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    M = int(off[-1])
+    A = rng.integers(0, 16, (M, Kd)).astype(np.uint8)
+    B = rng.integers(0, 16, (E, N, Kd)).astype(np.uint8)
+    return off, M, A, B
+
+
+def test_grouped_gemm_nvfp4_exact_with_power_of_two_scales():
+    """Power-of-two block and global scales: every term is exact, so the
+    result equals a numpy sum over 16-element blocks of (decoded dot product)
+    x 2^(u+v) x ga x gb[e]. A transposed or shifted block index changes the
+    powers and fails."""
+    rng = np.random.default_rng(13)
+    counts, N, Kd = [9, 0, 20], 48, 96
+    off, M, A, B = _nvfp4_problem(rng, counts, N, Kd)
+    E, KB = len(counts), Kd // 16
+    u = rng.integers(-5, 6, (M, KB))
+    v = rng.integers(-5, 6, (E, N, KB))
+    sa = oracle.e4m3_encode((2.0 ** u).astype(np.float32))
+    sb = oracle.e4m3_encode((2.0 ** v).astype(np.float32))
+    ga = np.float32(0.25)
+    gb = np.array([2.0, 0.5, 8.0], np.float32)
+    C = oracle.grouped_gemm_nvfp4(A, sa, ga, B, sb, gb, off)
+    tab = np.array(E2M1_MAGNITUDES + [-m for m in E2M1_MAGNITUDES])
+    Av, Bv = tab[A], tab[B]
+    ref = np.zeros((M, N))
+    for e in range(E):
+        rows = slice(off[e], off[e + 1])
+        for kb in range(KB):
+            ks = slice(kb * 16, (kb + 1) * 16)
+            part = Av[rows, ks] @ Bv[e, :, ks].T
+            ref[rows] += part * 2.0 ** (u[rows, kb][:, None] + v[e, :, kb][None, :])
+        ref[rows] *= float(ga) * float(gb[e])
+    assert np.array_equal(C, ref)
+
+
+def test_grouped_gemm_nvfp4_uniform_scales_is_a_plain_product():
+    rng = np.random.default_rng(14)
+    counts, N, Kd = [7, 5], 32, 64
+    off, M, A, B = _nvfp4_problem(rng, counts, N, Kd)
+    one = oracle.e4m3_encode(np.float32(1.0))
+    sa = np.full((M, Kd // 16), one, np.uint8)
+    sb = np.full((2, N, Kd // 16), one, np.uint8)
+    C = oracle.grouped_gemm_nvfp4(A, sa, 1.0, B, sb, np.ones(2, np.float32), off)
+    tab = np.array(E2M1_MAGNITUDES + [-m for m in E2M1_MAGNITUDES])
+    for e in range(2):
+        rows = slice(off[e], off[e + 1])
+        assert np.array_equal(C[rows], tab[A[rows]] @ tab[B[e]].T)
