@@ -60,6 +60,9 @@ def lib():
             "oracle_e2m1_encode_n": (None, [P, P, i64]),
             "oracle_nvfp4_quant": (None, [P, i64, i32, f32, P, P]),
             "oracle_grouped_gemm_nvfp4": (None, [P, P, f32, P, P, P, P, i32, i32, i32, i32, P]),
+            "oracle_forward_tokens_nvfp4": (i32, [P, P, P, P, P, P, P, P, P, f32, f32, i32, i32,
+                                                  i32, i32, i32, i32, i32, i32, i32, i32, f32,
+                                                  P, i32, P, P, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -429,3 +432,76 @@ def grouped_gemm_nvfp4(A, sa, ga, B, sb, gb, offsets):
     lib().oracle_grouped_gemm_nvfp4(_p(A), _p(sa), float(ga), _p(B), _p(sb), _p(gb), _p(off),
                                     M, N, Kd, E, _p(C))
     return C
+
+
+def permute_quant_nvfp4(x_bits, topk_ids, E, g):
+    """Pre-reorder with NVFP4 quantisation: each token quantised once (global
+    scale g), its codes and block scales copied to the rows src2dst gives its
+    K slots. Returns (codes [T*K,H], block scales [T*K,H/16], src2dst, offsets)."""
+    ids = _c(topk_ids, np.int32)
+    K = ids.shape[1]
+    offsets, src2dst = route(ids, E)
+    q, sb = nvfp4_quant(x_bits, g)
+    a_q = np.empty((ids.size, q.shape[1]), np.uint8)
+    sa = np.empty((ids.size, sb.shape[1]), np.uint8)
+    a_q[src2dst] = np.repeat(q, K, axis=0)   # slot t*K+k holds token t
+    sa[src2dst] = np.repeat(sb, K, axis=0)
+    return a_q, sa, src2dst, offsets
+
+
+def forward_tokens_nvfp4(x_bits, logits, bias, w13, s13, g13, w2, s2, g2, ga1, ga2, num_groups,
+                         topk_group, top_k, scoring, renormalize, routed_scaling_factor,
+                         tokens=None, n_shared=0):
+    """Whole layer in NVFP4 for the listed tokens: codes w13 [E+S,2I,H] and
+    w2 [E+S,H,I], block scales s13 [E+S,2I,H/16] and s2 [E+S,H,I/16] (E4M3
+    codes), weight global scales g13, g2 [E+S], activation global scales ga1
+    (x) and ga2 (h). Returns (out [n,H] fp64, ids [n,K], w [n,K])."""
+    x = _c(x_bits, np.uint16)
+    logits = _c(logits, np.float32)
+    T, H = x.shape
+    E = logits.shape[1]
+    I = w2.shape[2]
+    n = E + n_shared
+    assert w13.shape == (n, 2 * I, H) and w2.shape == (n, H, I)
+    assert s13.shape == (n, 2 * I, H // FB) and s2.shape == (n, H, I // FB)
+    assert g13.shape == (n,) and g2.shape == (n,)
+    b = None if bias is None else _c(bias, np.float32)
+    tok = np.arange(T, dtype=np.int64) if tokens is None else _c(tokens, np.int64)
+    nt = tok.size
+    out = np.empty((nt, H), np.float64)
+    ids = np.empty((nt, top_k), np.int32)
+    w = np.empty((nt, top_k), np.float32)
+    w13, w2, s13, s2 = (_c(a, np.uint8) for a in (w13, w2, s13, s2))
+    g13, g2 = _c(g13, np.float32), _c(g2, np.float32)
+    rc = lib().oracle_forward_tokens_nvfp4(
+        _p(x), _p(logits), _p(b), _p(w13), _p(s13), _p(g13), _p(w2), _p(s2), _p(g2),
+        float(ga1), float(ga2), T, H, I, E, int(n_shared), num_groups, topk_group, top_k,
+        scoring, int(bool(renormalize)), float(routed_scaling_factor), _p(tok), nt, _p(out),
+        _p(ids), _p(w))
+    if rc != 0:
+        raise ValueError(f"oracle_forward_tokens_nvfp4: status {rc}")
+    return out, ids, w
+
+
+def forward_steps_nvfp4(x_bits, logits, bias, w13, s13, g13, w2, s2, g2, ga1, ga2, num_groups,
+                        topk_group, top_k, scoring, renormalize, routed_scaling_factor,
+                        n_shared=0):
+    """The NVFP4 layer step by step over all tokens (small configurations)."""
+    E = logits.shape[1]
+    ids, w = gate(logits, bias, num_groups, topk_group, top_k, scoring, renormalize,
+                  routed_scaling_factor)
+    if n_shared:
+        T = ids.shape[0]
+        ids = np.concatenate([ids, np.broadcast_to(
+            np.arange(E, E + n_shared, dtype=np.int32), (T, n_shared))], axis=1)
+        w = np.concatenate([w, np.ones((T, n_shared), np.float32)], axis=1)
+        E += n_shared
+    a_q, sa, src2dst, offsets = permute_quant_nvfp4(x_bits, ids, E, ga1)
+    C13 = grouped_gemm_nvfp4(a_q, sa, ga1, w13, s13, g13, offsets)
+    h = silu_mul(C13)
+    h_bits = bf16_round(h)
+    q2, sa2 = nvfp4_quant(h_bits, ga2)
+    down = grouped_gemm_nvfp4(q2, sa2, ga2, w2, s2, g2, offsets)
+    out = unpermute_sum(down, src2dst, w)
+    return dict(ids=ids, w=w, a_q=a_q, scale_a=sa, src2dst=src2dst, offsets=offsets,
+                c13=C13, h=h, h_bits=h_bits, q2=q2, scale_a2=sa2, down=down, out=out)

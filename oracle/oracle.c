@@ -873,26 +873,27 @@ void oracle_e2m1_encode_n(const float* x, uint8_t* q, int64_t n) {
   for (int64_t i = 0; i < n; ++i) q[i] = oracle_e2m1_encode(x[i]);
 }
 
+/* one bf16 row of C values (C % 16 == 0) -> C E2M1 codes, C/16 E4M3 codes */
+static void nvfp4_quant_row(const uint16_t* row, int C, float g, uint8_t* q, uint8_t* sb) {
+  for (int b = 0; b < C / FB; ++b) {
+    const uint16_t* blk = row + (int64_t)b * FB;
+    float amax = 0.0f;
+    for (int c = 0; c < FB; ++c) {
+      float v = fabsf(bf16_to_f32(blk[c]));
+      if (v > amax) amax = v;
+    }
+    uint8_t s = oracle_e4m3_encode((amax / 6.0f) / g);
+    sb[b] = s;
+    float step = (float)oracle_e4m3_decode(s) * g;
+    for (int c = 0; c < FB; ++c)
+      q[(int64_t)b * FB + c] = step > 0.0f ? oracle_e2m1_encode(bf16_to_f32(blk[c]) / step) : 0;
+  }
+}
+
 void oracle_nvfp4_quant(const uint16_t* x, int64_t R, int C, float g, uint8_t* q,
                         uint8_t* sb) {
-  const int nb = C / FB;
 #pragma omp parallel for schedule(static)
-  for (int64_t r = 0; r < R; ++r) {
-    for (int b = 0; b < nb; ++b) {
-      const uint16_t* blk = x + r * C + (int64_t)b * FB;
-      float amax = 0.0f;
-      for (int c = 0; c < FB; ++c) {
-        float v = fabsf(bf16_to_f32(blk[c]));
-        if (v > amax) amax = v;
-      }
-      uint8_t s = oracle_e4m3_encode((amax / 6.0f) / g);
-      sb[r * nb + b] = s;
-      float step = (float)oracle_e4m3_decode(s) * g;
-      for (int c = 0; c < FB; ++c)
-        q[r * C + (int64_t)b * FB + c] =
-            step > 0.0f ? oracle_e2m1_encode(bf16_to_f32(blk[c]) / step) : 0;
-    }
-  }
+  for (int64_t r = 0; r < R; ++r) nvfp4_quant_row(x + r * C, C, g, q + r * C, sb + r * (C / FB));
 }
 
 void oracle_grouped_gemm_nvfp4(const uint8_t* A, const uint8_t* sa, float ga, const uint8_t* B,
@@ -933,4 +934,106 @@ void oracle_grouped_gemm_nvfp4(const uint8_t* A, const uint8_t* sa, float ga, co
     free(a);
   }
   free(row_e);
+}
+
+/* The whole layer in NVFP4 for the listed tokens, with n_shared shared
+ * experts as in oracle_forward_tokens_shared: the hidden state is quantised
+ * with the input global scale ga1, h (rounded to bf16) with ga2, and each
+ * expert's weights carry their own global scales g13[e], g2[e]. Weight
+ * codes w13 [E+S,2I,H], w2 [E+S,H,I]; block scales s13 [E+S,2I,H/16],
+ * s2 [E+S,H,I/16] (E4M3 codes). */
+int oracle_forward_tokens_nvfp4(const uint16_t* x, const float* logits, const float* bias,
+                                const uint8_t* w13, const uint8_t* s13, const float* g13,
+                                const uint8_t* w2, const uint8_t* s2, const float* g2,
+                                float ga1, float ga2, int T, int H, int I, int E,
+                                int n_shared, int num_groups, int topk_group, int top_k,
+                                int scoring, int renormalize, float routed_scaling_factor,
+                                const int64_t* tokens, int n_tok, double* out,
+                                int32_t* ids_out, float* w_out) {
+  int rc = gate_check(T, E, num_groups, topk_group, top_k, scoring, bias);
+  if (rc) return rc;
+  if (n_shared < 0 || H % FB != 0 || I % FB != 0 || !(ga1 > 0.0f) || !(ga2 > 0.0f)) return -1;
+  for (int i = 0; i < n_tok; ++i)
+    if (tokens[i] < 0 || tokens[i] >= T) return -1;
+  init_lut();
+  const int K = top_k;
+  const int N13 = 2 * I;
+  const int KBH = H / FB, KBI = I / FB;
+  int status = 0;
+#pragma omp parallel
+  {
+    kv_t* kv = (kv_t*)malloc(sizeof(kv_t) * (size_t)E);
+    kv_t* gkv = (kv_t*)malloc(sizeof(kv_t) * (size_t)(E + num_groups));
+    float* s = (float*)malloc(sizeof(float) * (size_t)E);
+    uint8_t* qa = (uint8_t*)malloc((size_t)H);
+    uint8_t* sa = (uint8_t*)malloc((size_t)KBH);
+    double* c = (double*)malloc(sizeof(double) * (size_t)N13);
+    uint16_t* hb = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)I);
+    uint8_t* q2 = (uint8_t*)malloc((size_t)I);
+    uint8_t* sa2 = (uint8_t*)malloc((size_t)KBI);
+    int32_t ids[64];
+    float w[64];
+#pragma omp for schedule(dynamic, 1)
+    for (int i = 0; i < n_tok; ++i) {
+      int64_t t = tokens[i];
+      double* o = out + (int64_t)i * H;
+      if (K > 64) {
+        status = -2;
+        continue;
+      }
+      gate_token(logits + t * E, bias, E, num_groups, topk_group, K, scoring, renormalize,
+                 routed_scaling_factor, ids, w, kv, gkv, s);
+      if (ids_out)
+        for (int k = 0; k < K; ++k) ids_out[(int64_t)i * K + k] = ids[k];
+      if (w_out)
+        for (int k = 0; k < K; ++k) w_out[(int64_t)i * K + k] = w[k];
+      nvfp4_quant_row(x + t * H, H, ga1, qa, sa);
+      for (int cc = 0; cc < H; ++cc) o[cc] = 0.0;
+      for (int k = 0; k < K + n_shared; ++k) {
+        const int e = k < K ? ids[k] : E + (k - K);
+        const uint8_t* We = w13 + (int64_t)e * N13 * H;
+        const uint8_t* sbe = s13 + (int64_t)e * N13 * KBH;
+        for (int n = 0; n < N13; ++n) {
+          const uint8_t* b = We + (int64_t)n * H;
+          double acc = 0.0;
+          for (int kb = 0; kb < KBH; ++kb) {
+            double part = 0.0;
+            for (int hh = kb * FB; hh < (kb + 1) * FB; ++hh)
+              part += oracle_e2m1_decode(qa[hh]) * oracle_e2m1_decode(b[hh]);
+            acc += part * g_e4m3_lut[sa[kb]] * g_e4m3_lut[sbe[(int64_t)n * KBH + kb]];
+          }
+          c[n] = acc * (double)ga1 * (double)g13[e];
+        }
+        for (int j = 0; j < I; ++j) {
+          double g = c[j], u = c[I + j];
+          hb[j] = oracle_bf16_round(g / (1.0 + exp(-g)) * u);
+        }
+        nvfp4_quant_row(hb, I, ga2, q2, sa2);
+        const uint8_t* W2e = w2 + (int64_t)e * H * I;
+        const uint8_t* sb2 = s2 + (int64_t)e * H * KBI;
+        double wk = k < K ? (double)w[k] : 1.0;
+        for (int cc = 0; cc < H; ++cc) {
+          const uint8_t* b = W2e + (int64_t)cc * I;
+          double acc = 0.0;
+          for (int kb = 0; kb < KBI; ++kb) {
+            double part = 0.0;
+            for (int j = kb * FB; j < (kb + 1) * FB; ++j)
+              part += oracle_e2m1_decode(q2[j]) * oracle_e2m1_decode(b[j]);
+            acc += part * g_e4m3_lut[sa2[kb]] * g_e4m3_lut[sb2[(int64_t)cc * KBI + kb]];
+          }
+          o[cc] += wk * (acc * (double)ga2 * (double)g2[e]);
+        }
+      }
+    }
+    free(kv);
+    free(gkv);
+    free(s);
+    free(qa);
+    free(sa);
+    free(c);
+    free(hb);
+    free(q2);
+    free(sa2);
+  }
+  return status;
 }

@@ -170,6 +170,20 @@ void oracle_grouped_gemm_nvfp4(const uint8_t* A, const uint8_t* sa, float ga, co
                                const uint8_t* sb, const float* gb, const int32_t* offsets,
                                int M, int N, int Kd, int E, double* C);
 
+/* The whole layer in NVFP4 (with n_shared shared experts as in
+ * oracle_forward_tokens_shared): x quantised with the global scale ga1, the
+ * bf16-rounded h with ga2; w13 [E+S,2I,H] and w2 [E+S,H,I] E2M1 codes,
+ * s13 [E+S,2I,H/16] and s2 [E+S,H,I/16] E4M3 block-scale codes, g13 and g2
+ * [E+S] the weights' global scales. H % 16 == 0, I % 16 == 0. */
+int oracle_forward_tokens_nvfp4(const uint16_t* x, const float* logits, const float* bias,
+                                const uint8_t* w13, const uint8_t* s13, const float* g13,
+                                const uint8_t* w2, const uint8_t* s2, const float* g2,
+                                float ga1, float ga2, int T, int H, int I, int E,
+                                int n_shared, int num_groups, int topk_group, int top_k,
+                                int scoring, int renormalize, float routed_scaling_factor,
+                                const int64_t* tokens, int n_tok, double* out,
+                                int32_t* ids_out, float* w_out);
+
 #ifdef __cplusplus
 }
 #endif

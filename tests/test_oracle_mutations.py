@@ -227,8 +227,8 @@ MUTATIONS = [
      "  if (a >= 6.0f) return (uint8_t)(sign | 0x6); /* saturate (also +-inf) */",
      [pins.test_e2m1_encode_exhaustive_nearest_even]),
     ("NVFP4 block scale from amax / 4",
-     "      uint8_t s = oracle_e4m3_encode((amax / 6.0f) / g);",
-     "      uint8_t s = oracle_e4m3_encode((amax / 4.0f) / g);",
+     "    uint8_t s = oracle_e4m3_encode((amax / 6.0f) / g);",
+     "    uint8_t s = oracle_e4m3_encode((amax / 4.0f) / g);",
      [pins.test_nvfp4_quant_closed_form]),
     ("NVFP4 GEMM without the weights' global scale",
      "        c[n] = acc * (double)ga * (double)gb[e];",
@@ -238,6 +238,15 @@ MUTATIONS = [
      "                 g_e4m3_lut[sbe[(int64_t)n * KB + kb]];",
      "                 g_e4m3_lut[sbe[(int64_t)n * KB + (KB - 1 - kb)]];",
      [pins.test_grouped_gemm_nvfp4_exact_with_power_of_two_scales]),
+    ("NVFP4 layer requantises h with the input's global scale",
+     "        nvfp4_quant_row(hb, I, ga2, q2, sa2);",
+     "        nvfp4_quant_row(hb, I, ga1, q2, sa2);",
+     [pins.test_layer_nvfp4_single_expert_is_dense_nvfp4_mlp]),
+    ("NVFP4 layer without w13's global scale",
+     "          c[n] = acc * (double)ga1 * (double)g13[e];",
+     "          c[n] = acc * (double)ga1;",
+     [pins.test_layer_nvfp4_single_expert_is_dense_nvfp4_mlp,
+      pins.test_layer_nvfp4_token_path_equals_step_path_with_shared_expert]),
 ]
 
 

@@ -743,3 +743,72 @@ def test_grouped_gemm_nvfp4_uniform_scales_is_a_plain_product():
     for e in range(2):
         rows = slice(off[e], off[e + 1])
         assert np.array_equal(C[rows], tab[A[rows]] @ tab[B[e]].T)
+
+
+def _random_nvfp4_layer(rng, T, H, I, E):
+    x = _bf16_bits(rng.standard_normal((T, H)))
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+
+    def weights(rows, cols):
+        codes = rng.integers(0, 16, (E, rows, cols)).astype(np.uint8)
+        scales = oracle.e4m3_encode((2.0 ** rng.uniform(-7, -3, (E, rows, cols // 16)))
+                                    .astype(np.float32))
+        g = rng.uniform(0.5, 2.0, E).astype(np.float32)
+        return codes, scales, g
+
+    w13, s13, g13 = weights(2 * I, H)
+    w2, s2, g2 = weights(H, I)
+    return x, logits, w13, s13, g13, w2, s2, g2
+
+
+def _dense_nvfp4_mlp(x, w13e, s13e, g13e, w2e, s2e, g2e, ga1, ga2):
+    """One expert on every token in NVFP4 with numpy: dequantise codes times
+    block scales times global scales, multiply in fp64."""
+    tab = np.array(E2M1_MAGNITUDES + [-m for m in E2M1_MAGNITUDES])
+    I = w2e.shape[1]
+
+    def deq_act(bits, g):
+        q, sb = oracle.nvfp4_quant(bits, g)
+        return tab[q] * np.repeat(oracle.e4m3_decode(sb), 16, 1) * float(g)
+
+    def deq_w(q, s, g):
+        return tab[q] * np.repeat(oracle.e4m3_decode(s), 16, 1) * float(g)
+
+    C = deq_act(x, ga1) @ deq_w(w13e, s13e, g13e).T
+    g, u = C[:, :I], C[:, I:]
+    hb = oracle.bf16_round(g / (1 + np.exp(-g)) * u)
+    return deq_act(hb, ga2) @ deq_w(w2e, s2e, g2e).T
+
+
+def test_layer_nvfp4_single_expert_is_dense_nvfp4_mlp():
+    # H and I span several 16-element blocks, and the two activation global
+    # scales differ, so a scale taken from the wrong block or tensor shows
+    rng = np.random.default_rng(61)
+    T, H, I = 6, 64, 48
+    x, logits, w13, s13, g13, w2, s2, g2 = _random_nvfp4_layer(rng, T, H, I, 1)
+    ga1, ga2 = np.float32(0.0125), np.float32(0.0031)
+    out, ids, w = oracle.forward_tokens_nvfp4(x, logits, None, w13, s13, g13, w2, s2, g2, ga1,
+                                              ga2, 1, 1, 1, oracle.SOFTMAX, True, 1.0)
+    assert np.all(ids == 0) and np.all(w == 1.0)
+    ref = _dense_nvfp4_mlp(x, w13[0], s13[0], g13[0], w2[0], s2[0], g2[0], ga1, ga2)
+    np.testing.assert_allclose(out, ref, rtol=1e-9, atol=1e-12 * np.abs(ref).max())
+
+
+def test_layer_nvfp4_token_path_equals_step_path_with_shared_expert():
+    rng = np.random.default_rng(62)
+    T, H, I, E, S = 20, 64, 48, 8, 1
+    x, logits, w13, s13, g13, w2, s2, g2 = _random_nvfp4_layer(rng, T, H, I, E + S)
+    bias = (rng.standard_normal(E) * 0.1).astype(np.float32)
+    ga1, ga2 = np.float32(0.0125), np.float32(0.0031)
+    args = (4, 2, 3, oracle.SIGMOID, True, 2.5)
+    steps = oracle.forward_steps_nvfp4(x, logits[:, :E], bias, w13, s13, g13, w2, s2, g2, ga1,
+                                       ga2, *args, n_shared=S)
+    out, ids, w = oracle.forward_tokens_nvfp4(x, logits[:, :E], bias, w13, s13, g13, w2, s2, g2,
+                                              ga1, ga2, *args, n_shared=S)
+    assert np.array_equal(ids, steps["ids"][:, :3]) and np.array_equal(w, steps["w"][:, :3])
+    np.testing.assert_allclose(out, steps["out"], rtol=1e-12, atol=1e-12 * np.abs(out).max())
+    # the shared expert adds its dense NVFP4 MLP with weight 1
+    base, _, _ = oracle.forward_tokens_nvfp4(x, logits[:, :E], bias, w13[:E], s13[:E], g13[:E],
+                                             w2[:E], s2[:E], g2[:E], ga1, ga2, *args)
+    ref = _dense_nvfp4_mlp(x, w13[E], s13[E], g13[E], w2[E], s2[E], g2[E], ga1, ga2)
+    np.testing.assert_allclose(out - base, ref, rtol=1e-9, atol=1e-12 * np.abs(out).max())
