@@ -31,6 +31,36 @@ def test_every_source_and_header_is_a_build_input():
     assert sorted(f for f in files if f.endswith((".cuh", ".h"))) == sorted(cuda_build.HEADERS)
 
 
+def test_header_compiles_as_c_and_links(lib, tmp_path):
+    """The header is plain C (C11, pedantic, warnings as errors) and a C program
+    links against the library and calls it: no device work, the gate call is
+    rejected by host validation."""
+    src = tmp_path / "use_abi.c"
+    src.write_text(r"""
+#include <stdio.h>
+#include "moe_gb300.h"
+int main(void) {
+  int v = moe_abi_version();
+  const char* s = moe_status_string(MOE_ERR_WORKSPACE);
+  /* E % num_groups != 0 */
+  moe_status st = moe_gate((const float*)0x10000, NULL, 4, 10, 3, 1, 2, MOE_SCORE_SIGMOID, 1,
+                           1.0f, (int32_t*)0x10000, (float*)0x10000, NULL);
+  printf("%d %s %d\n", v, s, (int)st);
+  return st == MOE_ERR_INVALID_ARG ? 0 : 1;
+}
+""")
+    so = cuda_build.build()
+    exe = tmp_path / "use_abi"
+    subprocess.run(["gcc", "-std=c11", "-Wall", "-Wextra", "-Werror", "-pedantic",
+                    "-I", os.path.dirname(HEADER), str(src), so,
+                    "-Wl,-rpath," + os.path.dirname(so), "-o", str(exe)], check=True)
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stdout + r.stderr
+    version, name, status = r.stdout.split()
+    assert int(version) == lib.moe_abi_version() and name == "MOE_ERR_WORKSPACE"
+    assert int(status) == INVALID
+
+
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
