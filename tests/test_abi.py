@@ -61,6 +61,26 @@ int main(void) {
     assert int(status) == INVALID
 
 
+def test_product_and_oracle_share_no_code():
+    """The CUDA library and its binding never import, include or load the
+    oracle, and the oracle never touches the library's package or sources
+    (the seeded input generator, synth.py, is the one module both sides use,
+    and it does not import the oracle either)."""
+    pkg = os.path.join(ROOT, "moe_expert_layer_grouped_gb300")
+    to_oracle = re.compile(r"^\s*(import oracle|from oracle)|liboracle|oracle\.h|oracle_build",
+                           re.M)
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".c", ".cpp")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert not to_oracle.search(text), os.path.join(dirpath, f)
+    to_product = re.compile(r"moe_expert_layer_grouped_gb300|moe_gb300\.h|csrc|libmoe_gb300")
+    odir = os.path.join(ROOT, "oracle")
+    for f in os.listdir(odir):
+        if f.endswith((".py", ".c", ".h")):
+            assert not to_product.search(open(os.path.join(odir, f)).read()), f
+
+
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
