@@ -81,6 +81,44 @@ def test_product_and_oracle_share_no_code():
             assert not to_product.search(open(os.path.join(odir, f)).read()), f
 
 
+def _oracle_imports(path):
+    """(enclosing function or None, line) of every import of the oracle package."""
+    import ast
+    tree = ast.parse(open(path).read())
+    found = []
+
+    def visit(node, fn):
+        for child in ast.iter_child_nodes(node):
+            name = child.name if isinstance(child, (ast.FunctionDef, ast.AsyncFunctionDef)) else fn
+            mods = []
+            if isinstance(child, ast.Import):
+                mods = [a.name for a in child.names]
+            elif isinstance(child, ast.ImportFrom):
+                mods = [child.module or ""]
+            if any(m == "oracle" or m.startswith("oracle.") for m in mods):
+                found.append((name, child.lineno))
+            visit(child, name)
+
+    visit(tree, None)
+    return found
+
+
+def test_only_test_smoke_and_baseline_code_use_the_oracle():
+    # outside tests/: smoke() checks against it, build() compiles it, and
+    # the benchmark times it in its CPU-baseline and reference legs
+    allowed = {"__graft_entry__.py": {"smoke", "build"},
+               "bench.py": {"cpu_baseline", "run_reference"}}
+    for dirpath, dirs, files in os.walk(ROOT):
+        rel = os.path.relpath(dirpath, ROOT)
+        dirs[:] = [d for d in dirs if not d.startswith((".", "_")) and d not in ("tests", "oracle")]
+        for f in files:
+            if not f.endswith(".py"):
+                continue
+            key = f if rel == "." else os.path.join(rel, f)
+            for fn, line in _oracle_imports(os.path.join(dirpath, f)):
+                assert fn in allowed.get(key, set()), f"{key}:{line} imports the oracle in {fn}"
+
+
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
