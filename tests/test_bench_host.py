@@ -130,3 +130,28 @@ def test_timed_regions_are_bracketed_by_sync_and_barrier():
     calls.clear()
     bench.align(_Torch, lambda: calls.append("barrier"))
     assert calls == ["sync", "barrier", "sync"]   # own work done, ranks met, then time
+
+
+def test_step_work_block_scales_shared_experts_and_batch_average():
+    # block FP8: one scale per 128 x 128 weight block and per 128 activation channels
+    wl = synth.Workload("b", 2, 256, 128, 4, 1, 1, 2, synth.SOFTMAX, True, 1.0, "none",
+                        quant="block")
+    off = np.array([0, 4, 4, 4, 4], dtype=np.int64)            # one active expert
+    w = bench.step_work(wl, [off])
+    T, H, I, M = 2, 256, 128, 4
+    w13 = 2 * I * H + (2 * I // 128) * (H // 128) * 4
+    assert w["gemm13_bytes"] == w13 + M * H + M * (H // 128) * 4 + M * I * 2 + 5 * 4
+    w2 = H * I + (H // 128) * (I // 128) * 4
+    assert w["gemm2_bytes"] == w2 + M * I + M * (I // 128) * 4 + M * H * 2 + 5 * 4
+    # a shared expert: E + 1 experts, K + 1 slots, always active; logits stay [T, E]
+    wl = synth.Workload("s", 3, 128, 64, 4, 1, 1, 2, synth.SOFTMAX, True, 1.0, "none",
+                        n_shared=1)
+    T, H, I, M = 3, 128, 64, 9
+    a = np.array([0, 3, 3, 6, 6, 9], dtype=np.int64)           # experts 0, 2 and the shared one
+    b = np.array([0, 0, 0, 0, 6, 9], dtype=np.int64)           # expert 3 and the shared one
+    wa, wb, avg = bench.step_work(wl, [a]), bench.step_work(wl, [b]), bench.step_work(wl, [a, b])
+    assert (wa["active"], wb["active"], avg["active"]) == (3, 2, 2.5)
+    assert wa["flops13"] == 2.0 * M * 2 * I * H
+    per_expert = (2 * I * H + 2 * I * 4) + (H * I + H * 4)
+    assert wa["layer_bytes"] == 3 * per_expert + T * H * 2 + T * 4 * 4 + T * H * 2
+    assert avg["layer_bytes"] == (wa["layer_bytes"] + wb["layer_bytes"]) / 2
