@@ -155,3 +155,18 @@ def test_step_work_block_scales_shared_experts_and_batch_average():
     per_expert = (2 * I * H + 2 * I * 4) + (H * I + H * 4)
     assert wa["layer_bytes"] == 3 * per_expert + T * H * 2 + T * 4 * 4 + T * H * 2
     assert avg["layer_bytes"] == (wa["layer_bytes"] + wb["layer_bytes"]) / 2
+
+
+def test_roofline_objects(tmp_path, monkeypatch):
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))      # no recorded traffic here
+    pk = dict(hbm=7000.0, bf16=1900.0, bf16_sustained=850.0, sm_max=2070.0, source="measured")
+    r = {"kern": {"grouped_gemm_w13": 0.5}, "work": {"gemm13_bytes": 3.5e9, "flops13": 0.85e12}}
+    d = bench.roofline_decode(r, pk, "some_workload")
+    assert (d["bound"], d["unit"], d["achieved"], d["peak"], d["frac"]) == \
+        ("hbm", "GB/s", 7000.0, 7000.0, 1.0)
+    assert d["traffic"] is None and d["algorithmic_bytes_per_launch"] == 3500000000
+    p = bench.roofline_prefill(r, pk)
+    # FP8 peak = the sustained bf16 figure x 2: 1700 TFLOP/s; 0.85 TFLOP in 0.5 ms
+    assert (p["bound"], p["unit"], p["achieved"], p["peak"], p["frac"]) == \
+        ("tensor", "TFLOP/s", 1700.0, 1700.0, 1.0)
+    assert "sustained" in p["peak_source"] and p["traffic"] is None
