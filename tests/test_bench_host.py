@@ -170,3 +170,20 @@ def test_roofline_objects(tmp_path, monkeypatch):
     assert (p["bound"], p["unit"], p["achieved"], p["peak"], p["frac"]) == \
         ("tensor", "TFLOP/s", 1700.0, 1700.0, 1.0)
     assert "sustained" in p["peak_source"] and p["traffic"] is None
+
+
+def test_clock_summary_reads_the_timed_window():
+    cs = bench.ClockSampler(0)
+    row = "0, {sm}, 2070, 900.0, 0x0, Not Active, Not Active, Not Active, {cap}"
+    cs.lines = [(0.5, row.format(sm=1000, cap="Active")),          # before the window
+                (1.0, row.format(sm=2070, cap="Not Active")),
+                (1.5, row.format(sm=1900, cap="Active")),
+                (2.0, row.format(sm=2000, cap="Not Active")),
+                (2.2, "garbled line"),
+                (3.5, row.format(sm=1200, cap="Not Active"))]      # after it
+    s = cs.summary(1.0, 2.5)
+    assert s["sm_mhz"] == 2000.0 and s["sm_max_mhz"] == 2070.0     # median of 1900, 2000, 2070
+    assert s["reasons"] == ["sw_power_cap"]
+    # no sample inside the window: the last few samples stand in
+    s = cs.summary(10.0, 11.0)
+    assert s["sm_mhz"] == 2000.0 and s["samples"] == 3
