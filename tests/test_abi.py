@@ -284,3 +284,23 @@ def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(moe, "library_path", lambda: str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="missing"):
         moe.load()
+
+
+def test_binding_rejects_host_tensors_before_calling_the_library():
+    import torch
+    f32 = torch.zeros((4, 8), dtype=torch.float32)
+    bf = torch.zeros((4, 64), dtype=torch.bfloat16)
+    ids = torch.zeros((4, 2), dtype=torch.int32)
+    u8 = torch.zeros((4, 64), dtype=torch.uint8)
+    off = torch.zeros(9, dtype=torch.int32)
+    calls = [
+        lambda: moe.moe_gate(f32, None, 1, 1, 2),
+        lambda: moe.moe_permute_quant(bf, ids, 8),
+        lambda: moe.moe_grouped_gemm(u8, f32[:, 0].contiguous(), u8.view(1, 4, 64),
+                                     torch.ones((1, 4)), off[:2].contiguous()),
+        lambda: moe.moe_act_quant(bf),
+        lambda: moe.moe_unpermute_sum(bf, ids.view(-1), f32[:, :2].contiguous()),
+    ]
+    for call in calls:
+        with pytest.raises(ValueError, match="CUDA tensors"):
+            call()
