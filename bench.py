@@ -448,15 +448,67 @@ def roofline_decode(r, pk, workload):
             "launch_ms": round(k, 4), "peak_source": f"{pk['source']} hbm_gbs"}
 
 
-def roofline_prefill(r, pk):
+def roofline_prefill(r, pk, clocks=None):
+    """Tensor roofline of the w13 GEMM. The GEMM is timed in a loop of a
+    fraction of a second at full clock, a burst, so the denominator is the
+    burst bf16 figure x the FP8:bf16 ratio; the sustained-derived fraction
+    and a clock-normalised figure (the launch time scaled by the median SM
+    clock over the maximum, i.e. the rate at the maximum clock) stand beside
+    it."""
     k = r["kern"]["grouped_gemm_w13"]
     fl = r["work"]["flops13"]
     achieved = fl / (k * 1e-3) / 1e12
-    peak = pk["bf16_sustained"] * FP8_PER_BF16
-    return {"kernel": "grouped_gemm_w13", "bound": "tensor", "achieved": round(achieved, 1),
-            "peak": round(peak, 1), "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
-            "traffic": None, "algorithmic_flops_per_launch": fl, "launch_ms": round(k, 4),
-            "peak_source": f"{pk['source']} bf16_tflops_sustained x {FP8_PER_BF16} (fp8/bf16)"}
+    peak = pk["bf16"] * FP8_PER_BF16
+    peak_sus = pk["bf16_sustained"] * FP8_PER_BF16
+    out = {"kernel": "grouped_gemm_w13", "bound": "tensor", "achieved": round(achieved, 1),
+           "peak": round(peak, 1), "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+           "traffic": None, "algorithmic_flops_per_launch": fl, "launch_ms": round(k, 4),
+           "peak_source": f"{pk['source']} bf16_tflops (burst) x {FP8_PER_BF16} (fp8/bf16)",
+           "frac_of_sustained_peak": round(achieved / peak_sus, 4),
+           "sustained_peak": round(peak_sus, 1)}
+    norm = clock_normalised(achieved, clocks, pk)
+    if norm is not None:
+        out["clock_normalised"] = {"achieved": round(norm[0], 1), "frac": round(norm[0] / peak, 4),
+                                   "sm_mhz": norm[1], "to_mhz": norm[2]}
+    return out
+
+
+def clock_normalised(rate, clocks, pk):
+    """The rate the same work would reach at the maximum SM clock: time x
+    median SM MHz / max MHz. None without a clock record."""
+    if not clocks or not clocks.get("sm_mhz"):
+        return None
+    mx = clocks.get("sm_max_mhz") or pk.get("sm_max") or 2070.0
+    med = float(clocks["sm_mhz"])
+    if med <= 0 or mx <= 0:
+        return None
+    return rate * mx / med, med, mx
+
+
+def layer_fracs(r, pk, clocks=None):
+    """The layer's FP8 tensor fraction (whole step): burst denominator, the
+    sustained one, and clock-normalised."""
+    tf = r["work"]["layer_flops"] / (r["ms"] * 1e-3) / 1e12
+    out = {"layer_fp8_tensor_frac": round(tf / (pk["bf16"] * FP8_PER_BF16), 4),
+           "layer_fp8_tensor_frac_of_sustained": round(
+               tf / (pk["bf16_sustained"] * FP8_PER_BF16), 4)}
+    norm = clock_normalised(tf, clocks, pk)
+    if norm is not None:
+        out["layer_fp8_tensor_frac_clock_normalised"] = round(
+            norm[0] / (pk["bf16"] * FP8_PER_BF16), 4)
+    return out
+
+
+def workload_config(wl, world):
+    """The `config` object of both arms' JSON lines: the workload and its
+    shapes, nothing measured."""
+    return {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E,
+            "num_groups": wl.num_groups, "topk_group": wl.topk_group, "top_k": wl.top_k,
+            "scoring": "sigmoid" if wl.scoring == 0 else "softmax", "rsf": wl.rsf,
+            "n_shared": wl.n_shared, "quant": wl.quant, "batches_cycled": N_BATCHES,
+            "l2": "no flush: each step streams the active experts' weights (GBs, see "
+                  "layer_bytes_gb) through the 129 MB L2",
+            "parallelism": f"replicas x{world} (no collective on the data path)"}
 
 
 def cpu_baseline(synth, torch, wl, seed, r, budget_s=15.0):
@@ -532,18 +584,15 @@ def run_ours(args):
         "warmup": warmup, "ms_per_step": round(ms, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "fp8_e4m3 x fp8_e4m3 -> fp32 (bf16 io)",
         "data": "synthetic (seeded; weights ~N(0,0.02) quantised to e4m3 per channel)",
-        "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E,
-                   "num_groups": wl.num_groups, "topk_group": wl.topk_group, "top_k": wl.top_k,
-                   "scoring": "sigmoid" if wl.scoring == 0 else "softmax", "rsf": wl.rsf,
-                   "n_shared": wl.n_shared, "quant": wl.quant, "batches_cycled": N_BATCHES,
-                   "l2": "no flush: each step streams the active experts' weights "
-                         f"(~{r['work']['layer_bytes'] / 1e9:.2f} GB) through the 129 MB L2",
-                   "parallelism": f"replicas x{world} (no collective on the data path)"},
+        "config": workload_config(wl, world),
+        "layer_bytes_gb": round(r["work"]["layer_bytes"] / 1e9, 3),
         "tflops": round(r["work"]["layer_flops"] / (r["ms"] * 1e-3) / 1e12, 2),
         "layer_hbm_gbs": round(r["work"]["layer_bytes"] / (r["ms"] * 1e-3) / 1e9, 1),
+        **(layer_fracs(r, pk, r["clocks"]) if wl.T > 512 else {}),
         "active_experts": r["work"]["active"],
         "kernels_ms": {k: round(v, 4) for k, v in r["kern"].items()},
-        "roofline": roofline_decode(r, pk, wl.name) if wl.T <= 512 else roofline_prefill(r, pk),
+        "roofline": (roofline_decode(r, pk, wl.name) if wl.T <= 512
+                     else roofline_prefill(r, pk, r["clocks"])),
         "e2e": {"value": round(job_tokens_per_s(wl.T, world, e2e_ms), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "graph": {"ms_per_step": round(graph_ms, 5),
@@ -563,11 +612,9 @@ def run_ours(args):
             "workload": wl2.name, "T": wl2.T, "value": round(wl2.T / (r2["ms"] * 1e-3), 1),
             "unit": "tokens/s", "ms_per_step": round(r2["ms"], 4), "steps": s_steps,
             "tflops": round(r2["work"]["layer_flops"] / (r2["ms"] * 1e-3) / 1e12, 2),
-            "layer_fp8_tensor_frac": round(
-                r2["work"]["layer_flops"] / (r2["ms"] * 1e-3) / 1e12
-                / (pk["bf16_sustained"] * FP8_PER_BF16), 4),
+            **layer_fracs(r2, pk, r2["clocks"]),
             "kernels_ms": {k: round(v, 4) for k, v in r2["kern"].items()},
-            "roofline": roofline_prefill(r2, pk), "clocks": r2["clocks"]}
+            "roofline": roofline_prefill(r2, pk, r2["clocks"]), "clocks": r2["clocks"]}
         r = None
         del r2
         torch.cuda.empty_cache()
@@ -635,8 +682,7 @@ def run_reference(args):
         "warmup": warmup, "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64 (FP8 codes decoded exactly)",
         "data": "synthetic (seeded)",
-        "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E,
-                   "top_k": wl.top_k, "n_shared": wl.n_shared, "quant": wl.quant},
+        "config": workload_config(wl, args.gpus),
         "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": threads,
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,

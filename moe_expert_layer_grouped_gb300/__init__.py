@@ -131,6 +131,27 @@ def _need_cuda(*ts):
                 raise ValueError("moe_gb300: tensors must be contiguous")
 
 
+def _need_buf(fn, name, t, numel, dtypes):
+    """A caller-supplied output buffer must hold `numel` elements of one of
+    `dtypes`: a smaller one would be written past its end by the kernels."""
+    if t.numel() != numel or t.dtype not in dtypes:
+        raise ValueError(f"{fn}: {name} must hold {numel} elements of "
+                         f"{' or '.join(str(d) for d in dtypes)}, got {t.numel()} of {t.dtype}")
+
+
+def _permute_bufs(fn, T, H, K, E, a_q, scale_a, src2dst, offsets, scales_per_row=1):
+    import torch
+    M = T * K
+    if a_q is not None:
+        _need_buf(fn, "a_q", a_q, M * H, (torch.uint8, torch.float8_e4m3fn))
+    if scale_a is not None:
+        _need_buf(fn, "scale_a", scale_a, M * scales_per_row, (torch.float32,))
+    if src2dst is not None:
+        _need_buf(fn, "src2dst", src2dst, M, (torch.int32,))
+    if offsets is not None:
+        _need_buf(fn, "offsets", offsets, E + 1, (torch.int32,))
+
+
 def _u8(t):
     import torch
     return t.view(torch.uint8) if t.dtype != torch.uint8 else t
@@ -159,9 +180,10 @@ def moe_permute_workspace_size(T, E, K):
 def moe_permute_quant(x, topk_ids, E, a_q=None, scale_a=None, src2dst=None, offsets=None,
                       workspace=None, stream=None):
     import torch
-    _need_cuda(x, topk_ids)
+    _need_cuda(x, topk_ids, a_q, scale_a, src2dst, offsets)
     T, H = x.shape
     K = topk_ids.shape[1]
+    _permute_bufs("moe_permute_quant", T, H, K, E, a_q, scale_a, src2dst, offsets)
     dev = x.device
     M = T * K
     a_q = torch.empty((M, H), dtype=torch.uint8, device=dev) if a_q is None else a_q
@@ -186,6 +208,7 @@ def moe_permute_quant_noalloc(x, topk_ids, E, a_q, scale_a, src2dst, offsets, st
     _need_cuda(x, topk_ids, a_q, scale_a, src2dst, offsets)
     T, H = x.shape
     K = topk_ids.shape[1]
+    _permute_bufs("moe_permute_quant_noalloc", T, H, K, E, a_q, scale_a, src2dst, offsets)
     _check("moe_permute_quant_noalloc", load().moe_permute_quant_noalloc(
         _ptr(x), _ptr(topk_ids), T, H, E, K, _ptr(_u8(a_q)), _ptr(scale_a), _ptr(src2dst),
         _ptr(offsets), _stream(stream)))
@@ -324,9 +347,11 @@ def moe_permute_quant_block(x, topk_ids, E, a_q=None, scale_a=None, src2dst=None
                             workspace=None, stream=None):
     """moe_permute_quant with one scale per token per 128 channels: scale_a [T*K, H/128]."""
     import torch
-    _need_cuda(x, topk_ids)
+    _need_cuda(x, topk_ids, a_q, scale_a, src2dst, offsets)
     T, H = x.shape
     K = topk_ids.shape[1]
+    _permute_bufs("moe_permute_quant_block", T, H, K, E, a_q, scale_a, src2dst, offsets,
+                  scales_per_row=H // 128)
     dev = x.device
     M = T * K
     a_q = torch.empty((M, H), dtype=torch.uint8, device=dev) if a_q is None else a_q

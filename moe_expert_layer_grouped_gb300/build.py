@@ -45,8 +45,15 @@ def _newest_input():
     return max(os.path.getmtime(f) for f in files)
 
 
+# "compiled" or "reused": what the last build() call did (so a log can tell a
+# fresh compile of the sources from a library left by an earlier build)
+last_action = None
+
+
 def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
+    global last_action
     if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= _newest_input():
+        last_action = "reused"
         return LIB
     os.makedirs(OBJ, exist_ok=True)
     os.makedirs(LIB_DIR, exist_ok=True)
@@ -75,6 +82,7 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, LIB)
+    last_action = "compiled"
     return LIB
 
 

@@ -67,9 +67,11 @@ moe_status check_gate(const float* logits, const float* bias, int T, int E, int 
   return MOE_OK;
 }
 
-moe_status check_permute(const void* x, const int32_t* ids, int T, int H, int E, int K,
-                         const void* a_q, const float* sa, const int32_t* s2d,
-                         const int32_t* offsets, const void* ws, size_t ws_bytes) {
+// Every check of a pre-reorder call except its workspace (shared by the
+// workspace and the allocation-free entry points).
+moe_status check_permute_args(const void* x, const int32_t* ids, int T, int H, int E, int K,
+                              const void* a_q, const float* sa, const int32_t* s2d,
+                              const int32_t* offsets) {
   if (T < 0 || H < 1 || E < 1 || K < 1) return MOE_ERR_INVALID_ARG;
   if (H % 32 != 0) return MOE_ERR_INVALID_ARG;
   if (E > kMaxE || K > kMaxK || H > kMaxH) return MOE_ERR_UNSUPPORTED;
@@ -77,6 +79,14 @@ moe_status check_permute(const void* x, const int32_t* ids, int T, int H, int E,
   if (!ok_ptr(offsets)) return MOE_ERR_INVALID_ARG;
   if (T > 0 && (!ok_ptr(x) || !ok_ptr(ids) || !ok_ptr(a_q) || !ok_ptr(sa) || !ok_ptr(s2d)))
     return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+moe_status check_permute(const void* x, const int32_t* ids, int T, int H, int E, int K,
+                         const void* a_q, const float* sa, const int32_t* s2d,
+                         const int32_t* offsets, const void* ws, size_t ws_bytes) {
+  const moe_status s = check_permute_args(x, ids, T, H, E, K, a_q, sa, s2d, offsets);
+  if (s != MOE_OK) return s;
   const size_t need = permute_ws_bytes(T, E);
   if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0 || ws_bytes < need)
     return MOE_ERR_WORKSPACE;
@@ -279,13 +289,9 @@ moe_status moe_permute_quant_noalloc(const void* x, const int32_t* topk_ids, int
                                      int32_t* offsets, void* stream) {
   // the same checks as moe_permute_quant, with the fixed scratch as workspace;
   // all of them come before any CUDA call
-  if (T < 0 || H < 1 || E < 1 || K < 1 || H % 32 != 0) return MOE_ERR_INVALID_ARG;
-  if (E > kMaxE || K > kMaxK || H > kMaxH) return MOE_ERR_UNSUPPORTED;
-  if ((int64_t)T * K >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
-  if (!ok_ptr(offsets)) return MOE_ERR_INVALID_ARG;
-  if (T > 0 && (!ok_ptr(x) || !ok_ptr(topk_ids) || !ok_ptr(a_q) || !ok_ptr(scale_a) ||
-                !ok_ptr(src2dst)))
-    return MOE_ERR_INVALID_ARG;
+  const moe_status s = check_permute_args(x, topk_ids, T, H, E, K, a_q, scale_a, src2dst,
+                                          offsets);
+  if (s != MOE_OK) return s;
   if (permute_ws_bytes(T, E) > MOE_PERMUTE_NOALLOC_SCRATCH_BYTES) return MOE_ERR_WORKSPACE;
   void* ws = permute_static_scratch();
   int* err = device_error_word();

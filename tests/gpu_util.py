@@ -47,3 +47,65 @@ def random_e4m3(rng, shape):
     q = rng.integers(0, 256, shape).astype(np.uint8)
     q[(q & 0x7F) == 0x7F] &= 0xFE
     return q
+
+
+def gemm_token_tile(M, E, quant="token"):
+    """Token tile of the grouped GEMM launch the library picks for M permuted
+    rows over E experts: (most tokens per tile, CTA pair). Few rows per
+    expert (M <= 32*E) take 64-token tiles on single CTAs; otherwise the
+    per-token GEMM takes 256-token tiles on CTA pairs (every workload here has
+    an even number of weight blocks) and the block-scaled GEMM 128-token
+    tiles on single CTAs."""
+    if M <= 32 * E:
+        return 64, False
+    return (256, True) if quant == "token" else (128, False)
+
+
+def tile_cover_rows(offsets, bn, pair):
+    """Permuted rows that put at least one compared row in every (expert,
+    token chunk) tile: each chunk's first and last row and, for a CTA pair,
+    the last row of the even CTA's half and the first of the odd one's.
+    Chunks follow the kernel's tile table: an expert's cnt rows split into
+    ceil(cnt/bn) equal chunks, rounded up to 16 rows."""
+    rows = set()
+    off = np.asarray(offsets, np.int64)
+    for e in range(off.size - 1):
+        lo_e, cnt = int(off[e]), int(off[e + 1] - off[e])
+        if cnt <= 0:
+            continue
+        nch = -(-cnt // bn)
+        csz = ((-(-cnt // nch)) + 15) // 16 * 16
+        for tc in range(nch):
+            lo = tc * csz
+            hi = min(cnt, lo + csz)
+            if lo >= hi:
+                continue
+            rows.update((lo_e + lo, lo_e + hi - 1))
+            if pair:
+                half = ((hi - lo + 31) // 32 * 32) // 2
+                for r in (lo + half - 1, lo + half):
+                    if lo <= r < hi:
+                        rows.add(lo_e + r)
+    return np.array(sorted(rows), np.int64)
+
+
+def tile_cover_tokens(topk_ids, E, quant="token", n_random=40, seed=0):
+    """Tokens whose outputs, compared with the oracle, exercise every tile of
+    both grouped GEMMs (all weight blocks of a tile see each of its tokens):
+    the tokens at tile_cover_rows, the first and last token and n_random
+    more. The permutation is the oracle's (stable by expert, ascending
+    token). Returns (tokens, number of tiles)."""
+    import oracle
+    ids = np.ascontiguousarray(topk_ids, np.int32)
+    T, K = ids.shape
+    offsets, src2dst = oracle.route(ids, E)
+    bn, pair = gemm_token_tile(T * K, E, quant)
+    rows = tile_cover_rows(offsets, bn, pair)
+    row_token = np.empty(T * K, np.int64)
+    row_token[src2dst] = np.arange(T * K, dtype=np.int64) // K
+    rng = np.random.default_rng(seed)
+    extra = rng.choice(T, min(n_random, T), replace=False)
+    tokens = np.unique(np.concatenate([row_token[rows], [0, T - 1], extra]))
+    cnt = np.diff(offsets.astype(np.int64))
+    ntiles = int(sum(-(-c // bn) for c in cnt if c > 0))
+    return tokens, ntiles

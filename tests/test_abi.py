@@ -304,3 +304,29 @@ def test_binding_rejects_host_tensors_before_calling_the_library():
     for call in calls:
         with pytest.raises(ValueError, match="CUDA tensors"):
             call()
+
+
+def test_binding_rejects_undersized_prereorder_buffers():
+    """Caller-supplied pre-reorder outputs must match T*K rows (a smaller
+    buffer would be written past its end); checked before any library call."""
+    import torch
+    T, H, K, E = 4, 64, 2, 8
+    ok = dict(a_q=torch.zeros((T * K, H), dtype=torch.uint8),
+              scale_a=torch.zeros(T * K, dtype=torch.float32),
+              src2dst=torch.zeros(T * K, dtype=torch.int32),
+              offsets=torch.zeros(E + 1, dtype=torch.int32))
+    moe._permute_bufs("f", T, H, K, E, **ok)                     # right sizes: accepted
+    moe._permute_bufs("f", T, H, K, E, None, None, None, None)   # the binding allocates
+    bad = [("a_q", torch.zeros((T * K - 1, H), dtype=torch.uint8)),
+           ("a_q", torch.zeros((T * K, H), dtype=torch.int8)),
+           ("scale_a", torch.zeros(T * K - 1, dtype=torch.float32)),
+           ("src2dst", torch.zeros(T * K, dtype=torch.int64)),
+           ("offsets", torch.zeros(E, dtype=torch.int32))]
+    for name, t in bad:
+        kw = dict(ok, **{name: t})
+        with pytest.raises(ValueError, match=name):
+            moe._permute_bufs("f", T, H, K, E, **kw)
+    # block scales: one per 128 channels
+    kw = dict(ok, scale_a=torch.zeros(T * K * 2, dtype=torch.float32))
+    moe._permute_bufs("f", T, 256, K, E, **dict(kw, a_q=torch.zeros((T * K, 256), dtype=torch.uint8)),
+                      scales_per_row=2)

@@ -93,7 +93,7 @@ def test_reference_arm_prints_the_contract_line():
         assert k in d, k
     assert d["impl"] == "reference" and d["steps"] == 2 and d["warmup"] == 1
     assert d["n_gpus"] == 1 and d["higher_is_better"] is True and d["value"] > 0
-    assert d["config"]["workload"] == "tiny"
+    assert d["config"] == bench.workload_config(synth.WORKLOADS["tiny"], 1)
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1
     assert cb["unit"] == d["unit"] and "tiny" in cb["sample"]
@@ -165,11 +165,37 @@ def test_roofline_objects(tmp_path, monkeypatch):
     assert (d["bound"], d["unit"], d["achieved"], d["peak"], d["frac"]) == \
         ("hbm", "GB/s", 7000.0, 7000.0, 1.0)
     assert d["traffic"] is None and d["algorithmic_bytes_per_launch"] == 3500000000
+    pk = dict(hbm=7000.0, bf16=850.0, bf16_sustained=425.0, sm_max=2070.0, source="measured")
     p = bench.roofline_prefill(r, pk)
-    # FP8 peak = the sustained bf16 figure x 2: 1700 TFLOP/s; 0.85 TFLOP in 0.5 ms
+    # the GEMM is timed in a short loop at full clock (a burst): FP8 peak =
+    # the burst bf16 figure x 2 = 1700 TFLOP/s; 0.85 TFLOP in 0.5 ms
     assert (p["bound"], p["unit"], p["achieved"], p["peak"], p["frac"]) == \
         ("tensor", "TFLOP/s", 1700.0, 1700.0, 1.0)
-    assert "sustained" in p["peak_source"] and p["traffic"] is None
+    assert "burst" in p["peak_source"] and p["traffic"] is None
+    # the sustained-derived fraction stands beside it
+    assert (p["sustained_peak"], p["frac_of_sustained_peak"]) == (850.0, 2.0)
+    assert "clock_normalised" not in p                       # no clock record given
+    # at a median 1035 MHz of 2070 the same launch would run twice as fast
+    p = bench.roofline_prefill(r, pk, {"sm_mhz": 1035.0, "sm_max_mhz": 2070.0})
+    assert p["clock_normalised"] == {"achieved": 3400.0, "frac": 2.0, "sm_mhz": 1035.0,
+                                     "to_mhz": 2070.0}
+    # the layer's fractions: 1.7 TFLOP per 1 ms step
+    lf = bench.layer_fracs({"work": {"layer_flops": 1.7e12}, "ms": 1.0}, pk,
+                           {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0})
+    assert lf == {"layer_fp8_tensor_frac": 1.0, "layer_fp8_tensor_frac_of_sustained": 2.0,
+                  "layer_fp8_tensor_frac_clock_normalised": 1.0}
+
+
+def test_both_arms_print_the_same_config():
+    """The reference arm's config is the same object as ours (nothing
+    measured in it), so the driver can match the two lines."""
+    wl = synth.WORKLOADS["dsv3_prefill_t8192"]
+    a, b = bench.workload_config(wl, 1), bench.workload_config(wl, 1)
+    assert a == b and a["workload"] == wl.name
+    for k in ("T", "H", "I", "E", "num_groups", "topk_group", "top_k", "scoring", "rsf",
+              "n_shared", "quant", "batches_cycled", "l2", "parallelism"):
+        assert k in a, k
+    assert a["num_groups"] == 8 and a["topk_group"] == 4 and a["scoring"] == "sigmoid"
 
 
 def test_clock_summary_reads_the_timed_window():

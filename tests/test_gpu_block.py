@@ -2,6 +2,8 @@
 scales) on the GPU, through the C ABI, against the CPU oracle: the block
 permute-quant and requant bit-exact; the block GEMMs and the whole layer
 within the layer tolerance."""
+import time
+
 import numpy as np
 import pytest
 import torch
@@ -10,7 +12,8 @@ import moe_expert_layer_grouped_gb300 as moe
 import oracle
 from moe_expert_layer_grouped_gb300 import synth
 
-from gpu_util import assert_parity, bf16_bits, bf16_np, np_bf16_to_torch, ragged_offsets, random_e4m3
+from gpu_util import (assert_parity, bf16_bits, bf16_np, np_bf16_to_torch, ragged_offsets,
+                      random_e4m3, tile_cover_tokens)
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
@@ -141,17 +144,24 @@ def _check_block_layer(wl, seed, n_sample=None):
     out = layer(d["x"], d["logits"])
     torch.cuda.synchronize()
     assert moe.moe_device_status() == 0
+    n = synth.to_numpy_inputs(d)
     if n_sample is None:
         tokens = np.arange(wl.T, dtype=np.int64)
-    else:
-        rng = np.random.default_rng(seed)
-        tokens = np.unique(np.concatenate([[0, wl.T - 1],
-                                           rng.choice(wl.T, n_sample, replace=False)]))
-    n = synth.to_numpy_inputs(d)
+    else:  # a token of every tile of both block GEMMs, the tile edges, 40 random ones
+        ids, _ = oracle.gate(n["logits"], n["bias"], wl.num_groups, wl.topk_group, wl.top_k,
+                             wl.scoring, wl.renormalize, wl.rsf)
+        if wl.n_shared:
+            shared = np.arange(wl.E, wl.E + wl.n_shared, dtype=np.int32)
+            ids = np.concatenate([ids, np.broadcast_to(shared, (wl.T, wl.n_shared))], axis=1)
+        tokens, ntiles = tile_cover_tokens(ids, wl.E + wl.n_shared, quant="block", seed=seed)
+    t0 = time.time()
     ref, _, _ = oracle.forward_tokens_block(n["x"], n["logits"], n["bias"], n["w13"], n["s13"],
                                             n["w2"], n["s2"], wl.num_groups, wl.topk_group,
                                             wl.top_k, wl.scoring, wl.renormalize, wl.rsf,
                                             tokens=tokens, n_shared=wl.n_shared)
+    if n_sample is not None:
+        print(f"{wl.name}: {tokens.size} tokens cover {ntiles} tiles; "
+              f"oracle {time.time() - t0:.1f} s")
     got = bf16_np(out[torch.from_numpy(tokens).to(DEV)])
     assert_parity(got, ref, wl.name)
     return layer, d, out
@@ -167,8 +177,8 @@ def test_forward_block_dsv3_decode_t128():
 
 
 @pytest.mark.parametrize("name", ["dsv3_prefill_t8192_block", "mixtral_t4096_block"])
-def test_forward_block_large_sampled(name):
-    _check_block_layer(synth.WORKLOADS[name], 0, n_sample=40)
+def test_forward_block_large_every_tile(name):
+    _check_block_layer(synth.WORKLOADS[name], 0, n_sample="tiles")
 
 
 def test_forward_block_shared_expert_ragged_and_host_buffers():

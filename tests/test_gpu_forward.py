@@ -5,6 +5,8 @@ through the same MoELayer call the benchmark times. Plus edge cases: the
 per-row scale regression, guard bands around every output, empty and one-token
 batches, the host-buffer entry point. Shared experts (moe_forward_shared)
 are checked the same way on layers that add one or two of them."""
+import time
+
 import numpy as np
 import pytest
 import torch
@@ -13,7 +15,7 @@ import moe_expert_layer_grouped_gb300 as moe
 import oracle
 from moe_expert_layer_grouped_gb300 import synth
 
-from gpu_util import assert_parity, bf16_bits, bf16_np
+from gpu_util import assert_parity, bf16_bits, bf16_np, tile_cover_tokens
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
@@ -40,7 +42,22 @@ def _oracle_tokens(wl, d, tokens):
                                  wl.renormalize, wl.rsf, tokens=tokens, n_shared=wl.n_shared)
 
 
+def _cover_tokens(wl, d, seed, quant="token"):
+    """Tokens that reach every tile of both GEMMs at the launch the forward
+    uses (from the oracle's routing), plus 40 random ones and the ends."""
+    n = synth.to_numpy_inputs({"logits": d["logits"], "bias": d["bias"]})
+    ids, _ = oracle.gate(n["logits"], n["bias"], wl.num_groups, wl.topk_group, wl.top_k,
+                         wl.scoring, wl.renormalize, wl.rsf)
+    S = wl.n_shared
+    if S:
+        shared = np.broadcast_to(np.arange(wl.E, wl.E + S, dtype=np.int32), (wl.T, S))
+        ids = np.concatenate([ids, shared], axis=1)
+    return tile_cover_tokens(ids, wl.E + S, quant=quant, seed=seed)
+
+
 def _check_workload(wl, seed, device_gen, n_sample=None):
+    """n_sample None: every token; "tiles": a token of every GEMM tile (and
+    the tile edges) plus 40 random ones; an int: that many random ones."""
     d = synth.make_inputs(wl, seed=seed, device=DEV if device_gen else "cpu")
     d = {k: (None if v is None else v.to(DEV)) for k, v in d.items()}
     layer = _layer(wl, d)
@@ -49,13 +66,20 @@ def _check_workload(wl, seed, device_gen, n_sample=None):
                           wl.scoring, wl.renormalize, wl.rsf)
     torch.cuda.synchronize()
     assert moe.moe_device_status() == 0
+    ntiles = None
     if n_sample is None:
         tokens = np.arange(wl.T, dtype=np.int64)
+    elif n_sample == "tiles":
+        tokens, ntiles = _cover_tokens(wl, d, seed)
     else:
         rng = np.random.default_rng(seed)
         tokens = np.unique(np.concatenate([[0, wl.T - 1],
                                            rng.choice(wl.T, n_sample, replace=False)]))
+    t0 = time.time()
     ref, rids, rw = _oracle_tokens(wl, d, tokens)
+    dt = time.time() - t0
+    if ntiles is not None:
+        print(f"{wl.name}: {tokens.size} tokens cover {ntiles} tiles; oracle {dt:.1f} s")
     sel = torch.from_numpy(tokens).to(DEV)
     assert np.array_equal(ids[sel].cpu().numpy(), rids)
     assert np.array_equal(w[sel].cpu().numpy(), rw)
@@ -76,8 +100,8 @@ def test_forward_dsv3_decode_t128(seed):
 
 @pytest.mark.parametrize("name", ["dsv3_prefill_t8192", "mixtral_t4096", "dsv3_skewed_t16384",
                                   "dsv3_skewed_half_t16384"])
-def test_forward_large_sampled(name):
-    _check_workload(synth.WORKLOADS[name], 0, device_gen=True, n_sample=40)
+def test_forward_large_every_tile(name):
+    _check_workload(synth.WORKLOADS[name], 0, device_gen=True, n_sample="tiles")
 
 
 def test_skewed_half_device_inputs_split_about_half():
@@ -108,7 +132,7 @@ def test_forward_shapes(T, H, I, E, G, TG, K, scoring, rsf):
 
 @pytest.mark.parametrize("name,seed,n_sample", [
     ("tiny_shared", 0, None), ("tiny_shared", 1, None), ("tiny_shared", 2, None),
-    ("dsv3_decode_t128_shared", 0, None), ("dsv3_prefill_t8192_shared", 0, 40),
+    ("dsv3_decode_t128_shared", 0, None), ("dsv3_prefill_t8192_shared", 0, "tiles"),
 ])
 def test_forward_shared_expert(name, seed, n_sample):
     wl = synth.WORKLOADS[name]

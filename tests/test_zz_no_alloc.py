@@ -5,10 +5,12 @@ a plug-in running inside another runtime that owns all device memory and
 gives it only its input and output buffers, or a latency-critical loop that
 must not allocate. For them the library offers moe_permute_quant_noalloc,
 which uses a fixed scratch array in the library's own device memory instead
-of a caller workspace. These tests call it through the C ABI and check that
-it returns exactly what moe_permute_quant (which takes the caller's
-workspace) returns, on two calls in a row, so the second call must not be
-disturbed by what the first left in the shared scratch.
+of a caller workspace. These tests call it through the C ABI, twice in a
+row, and check every output bit for bit against moe_permute_quant (which
+takes the caller's workspace) and against the CPU oracle. Both calls are
+large enough to take the three-kernel path, the one that uses the scratch,
+and the first uses more of it than the second, so the second call would
+read the first call's leftovers if any of them were read at all.
 
 This file is collected after every other test file.
 """
@@ -36,17 +38,25 @@ def _p(t):
 
 
 @pytest.mark.gpu
-def test_noalloc_matches_workspace_entry_point_on_two_calls():
+def test_noalloc_matches_workspace_entry_point_and_oracle_on_two_calls():
+    import oracle
     lib = _lib()
     dev = torch.device("cuda:0")
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
-    # the first call uses more scratch (more 32-token blocks x experts) than
-    # the second, so stale entries would be visible if any were read
-    for call, (T, H, E, K) in enumerate([(4099, 256, 64, 6), (300, 7168, 256, 8)]):
+    # both calls have more than 512 tokens, so both take the three-kernel path
+    # (per-block expert bitmasks and bases in the scratch); the first covers
+    # 256 blocks of 32 tokens x 256 experts, the second 32 x 256
+    cases = [(8192, 256, 256, 8), (1024, 7168, 256, 8)]
+    for T, H, E, K in cases:
+        assert T > 512 and lib.moe_permute_workspace_size(T, E, K) <= SCRATCH_BYTES
+    need = [lib.moe_permute_workspace_size(T, E, K) for T, _, E, K in cases]
+    assert need[0] > need[1]
+    for call, (T, H, E, K) in enumerate(cases):
         rng = np.random.default_rng(100 + call)
-        ids = torch.from_numpy(
-            np.stack([rng.choice(E, K, replace=False) for _ in range(T)]).astype(np.int32)).to(dev)
+        ids_np = np.stack([rng.choice(E, K, replace=False) for _ in range(T)]).astype(np.int32)
+        ids = torch.from_numpy(ids_np).to(dev)
         x = torch.from_numpy(rng.standard_normal((T, H)).astype(np.float32)).to(torch.bfloat16)
+        x_bits = x.view(torch.int16).numpy().view(np.uint16).copy()
         x = x.to(dev)
         ref_aq, ref_sa, ref_s2d, ref_off = moe.moe_permute_quant(x, ids, E)
         M = T * K
@@ -58,10 +68,18 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls():
                                            _p(s2d), _p(off), stream)
         assert st == MOE_OK
         torch.cuda.synchronize()
+        # the same bits as the workspace entry point
         assert torch.equal(off, ref_off), f"call {call}: offsets"
         assert torch.equal(s2d, ref_s2d), f"call {call}: src2dst"
         assert torch.equal(sa.view(torch.int32), ref_sa.view(torch.int32)), f"call {call}: scales"
         assert torch.equal(a_q, ref_aq), f"call {call}: codes"
+        # and the oracle's
+        o_aq, o_sa, o_s2d, o_off = oracle.permute_quant(x_bits, ids_np, E)
+        assert np.array_equal(off.cpu().numpy(), o_off), f"call {call}: offsets vs oracle"
+        assert np.array_equal(s2d.cpu().numpy(), o_s2d), f"call {call}: src2dst vs oracle"
+        assert np.array_equal(sa.cpu().numpy().view(np.uint32), o_sa.view(np.uint32)), \
+            f"call {call}: scales vs oracle"
+        assert np.array_equal(a_q.cpu().numpy(), o_aq), f"call {call}: codes vs oracle"
     assert moe.moe_device_status() == 0
 
 
