@@ -190,6 +190,39 @@ MOE_API moe_status moe_grouped_gemm(const void* A, const float* scale_a,
                             void* stream);
 
 /*
+ * moe_permute_quant_rows — moe_permute_quant with each token's codes stored
+ * ONCE, in token order: a_tok [T,H] e4m3 (row t = token t's codes), and
+ * row_token [T*K] i32 (out) = the token of each permuted row
+ * (row_token[src2dst[t*K+k]] = t). scale_a [T*K] (permuted order), src2dst
+ * and offsets as moe_permute_quant; same workspace and limits. A token's
+ * K copies are not written (the K-fold row write of the pre-reorder becomes
+ * one), and moe_grouped_gemm_rows reads the rows through row_token.
+ * Bit-exact.
+ */
+MOE_API moe_status moe_permute_quant_rows(const void* x, const int32_t* topk_ids, int T,
+                                          int H, int E, int K, void* a_tok, float* scale_a,
+                                          int32_t* src2dst, int32_t* row_token,
+                                          int32_t* offsets, void* ws, size_t ws_bytes,
+                                          void* stream);
+
+/*
+ * moe_grouped_gemm_rows — moe_grouped_gemm whose permuted row r of A is row
+ * row_token[r] of the token-order A_tok [T,Kd] e4m3 (each tile's token rows
+ * are gathered four at a time by TMA). Everything else, results included,
+ * as moe_grouped_gemm on A[r] = A_tok[row_token[r]]: scale_a [M] stays in
+ * permuted order. row_token values outside [0,T) read as zero rows.
+ * Speed: on the DeepSeek-V3 prefill w13 shape (M = 65536 rows, 256 experts)
+ * this measured 4.31 ms against 1.72 ms for moe_grouped_gemm on the K-fold
+ * copies (the four-row gathers bound it), so moe_forward does not use it;
+ * it serves callers short of memory for the K copies.
+ */
+MOE_API moe_status moe_grouped_gemm_rows(const void* A_tok, int T, const int32_t* row_token,
+                                         const float* scale_a, const void* B,
+                                         const float* scale_b, const int32_t* offsets, int M,
+                                         int N, int Kd, int E, int epilogue, void* C,
+                                         float* row_amax, void* stream);
+
+/*
  * moe_act_quant — per-token requantisation of the activation output.
  * [P2] Changelog/Code Review: down_input is quantised per token to FP8 with
  * the per-token quantiser, giving w2_input_scale.
@@ -353,6 +386,93 @@ MOE_API moe_status moe_forward_block_host(const void* x_host,
                               int top_k, int scoring, int renormalize,
                               float routed_scaling_factor, void* out_host,
                               void* ws, size_t ws_bytes, void* stream);
+
+/* ==========================================================================
+ * Expert parallelism over R ranks: rank r holds experts [r*E/R, (r+1)*E/R)
+ * (EPR = E/R of them) and its own tokens. [P3] Results deploys the layer
+ * with --enable-ep-moe --ep-size 8 over 8 GPUs without describing the
+ * exchange; it is read here as one all-to-all of token rows each way, done
+ * by the caller (NCCL or any transport) between these calls:
+ *   1. moe_gate, then moe_ep_dispatch on the rank's tokens: rows sorted by
+ *      global expert, so rank r's rows are the block
+ *      [offsets[r*EPR], offsets[(r+1)*EPR]) of a_q / scale_a;
+ *      expert_counts[e] = offsets[e+1] - offsets[e].
+ *   2. exchange: counts first (rank s sends expert_counts[r*EPR .. +EPR) to
+ *      rank r, giving recv_counts [R][EPR]), then the rows and their scales
+ *      (source blocks concatenated in source-rank order, Mr rows in all).
+ *   3. moe_ep_expert_forward on the received rows with the local experts'
+ *      weights: merge into expert-contiguous order (expert e: the rows of
+ *      source 0, then source 1, ...), w13 GEMM + SiLU*mul, requant, w2 GEMM,
+ *      then the output rows gathered back into arrival order (`back`).
+ *   4. exchange back: each block of `back` returns to its source rank, in
+ *      the order it came, so the rank's returned rows line up with its a_q.
+ *   5. moe_ep_combine: the weighted top-k sum through src2dst (as
+ *      moe_unpermute_sum).
+ * With R = 1 and the exchanges as copies, the result is moe_forward's, bit
+ * for bit. Every row's values are those of the one-GPU layer (the GEMMs and
+ * the requant work per row).
+ * ======================================================================== */
+
+/* Scratch bytes of the merge table for R sources and EPR local experts. */
+MOE_API size_t moe_ep_table_size(int R, int EPR);
+
+/* moe_ep_dispatch — moe_permute_quant (same arguments, workspace and
+ * outputs) plus expert_counts [E] i32 (out, device). E % R == 0 and
+ * E <= 1024. */
+MOE_API moe_status moe_ep_dispatch(const void* x, const int32_t* topk_ids, int T,
+                              int H, int E, int K, int R, void* a_q,
+                              float* scale_a, int32_t* src2dst, int32_t* offsets,
+                              int32_t* expert_counts, void* ws, size_t ws_bytes,
+                              void* stream);
+
+/*
+ * moe_ep_recv_reorder — merge of the received rows into expert-contiguous
+ * order. recv_rows [Mr,H] e4m3 and recv_scales [Mr] f32 in arrival order
+ * (source blocks in source-rank order, each sorted by local expert);
+ * recv_counts [R][EPR] i32 on the device (rows from source s for local
+ * expert e; they must be >= 0 and sum to Mr, else MOE_DEV_BAD_OFFSETS is
+ * raised, nothing is copied and the offsets are zero).
+ * Out: a_q [Mr,H] e4m3 and scale_a [Mr] f32 in expert order, offsets
+ * [EPR+1] i32, arrival2row [Mr] i32 (the expert-order row of each arrival
+ * row). ws: moe_ep_table_size(R,EPR) bytes, 256-byte aligned.
+ * Limits: H % 32 == 0, R*EPR <= 1024. Bit-exact (a permutation).
+ */
+MOE_API moe_status moe_ep_recv_reorder(const void* recv_rows, const float* recv_scales,
+                              const int32_t* recv_counts, int R, int EPR, int Mr,
+                              int H, void* a_q, float* scale_a, int32_t* offsets,
+                              int32_t* arrival2row, void* ws, size_t ws_bytes,
+                              void* stream);
+
+/* moe_ep_return_gather — back[j,:] = down[arrival2row[j],:] for j < Mr
+ * (bf16 rows of H values); an index outside [0,Mr) raises
+ * MOE_DEV_BAD_OFFSETS and leaves that row unwritten. H % 8 == 0. */
+MOE_API moe_status moe_ep_return_gather(const void* down, const int32_t* arrival2row,
+                              int Mr, int H, void* back, void* stream);
+
+/* Workspace bytes of moe_ep_expert_forward. */
+MOE_API size_t moe_ep_expert_workspace_size(int Mr, int H, int I, int R, int EPR);
+
+/*
+ * moe_ep_expert_forward — the expert side of one step on this rank:
+ * moe_ep_recv_reorder, moe_grouped_gemm (SILU_MUL) with w13 [EPR,2I,H] /
+ * s13 [EPR,2I], moe_act_quant, moe_grouped_gemm (BF16) with w2 [EPR,H,I] /
+ * s2 [EPR,H], moe_ep_return_gather into back [Mr,H] bf16, chained on one
+ * stream. Arguments as those calls; ws: moe_ep_expert_workspace_size bytes,
+ * 256-byte aligned. Limits: H % 32 == 0, I % 32 == 0, R*EPR <= 1024.
+ */
+MOE_API moe_status moe_ep_expert_forward(const void* recv_rows, const float* recv_scales,
+                              const int32_t* recv_counts, int R, int EPR, int Mr,
+                              int H, int I, const void* w13, const float* s13,
+                              const void* w2, const float* s2, void* back,
+                              void* ws, size_t ws_bytes, void* stream);
+
+/* moe_ep_combine — the weighted top-k sum of the rows returned to this rank
+ * (back_rows [T*K,H] bf16, in the order moe_ep_dispatch sorted them):
+ * out[t,:] = bf16(sum_k topk_w[t,k] * back_rows[src2dst[t*K+k],:]), fp32 in
+ * slot order, as moe_unpermute_sum. */
+MOE_API moe_status moe_ep_combine(const void* back_rows, const int32_t* src2dst,
+                              const float* topk_w, int T, int K, int H, void* out,
+                              void* stream);
 
 /*
  * moe_test_gemm_timeout — failure-detection test of the GEMM pipeline (the

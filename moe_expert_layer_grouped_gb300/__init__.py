@@ -20,8 +20,12 @@ __all__ = [
     "moe_forward_shared", "moe_forward_shared_host", "moe_permute_quant_block",
     "moe_grouped_gemm_block", "moe_act_quant_block", "moe_block_workspace_size",
     "moe_forward_block", "moe_forward_block_host", "moe_test_gemm_timeout",
-    "moe_permute_quant_noalloc", "moe_act_quant", "moe_unpermute_sum", "moe_workspace_size", "moe_forward",
+    "moe_permute_quant_noalloc", "moe_permute_quant_rows", "moe_grouped_gemm_rows",
+    "moe_act_quant", "moe_unpermute_sum", "moe_workspace_size", "moe_forward",
     "moe_forward_host", "moe_device_status", "MoELayer",
+    # expert parallelism (moe_expert_layer_grouped_gb300.ep)
+    "moe_ep_dispatch", "moe_ep_recv_reorder", "moe_ep_return_gather", "moe_ep_expert_forward",
+    "moe_ep_combine", "EPMoELayer",
 ]
 
 SIGMOID = 0
@@ -85,6 +89,16 @@ _SIGNATURES = {
     "moe_forward_block_host": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I,
                                     _I, _I, _F, _P, _P, _SZ, _P]),
     "moe_device_status": (_I, [ctypes.POINTER(_I)]),
+    "moe_permute_quant_rows": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_grouped_gemm_rows": (_I, [_P, _I, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P]),
+    "moe_ep_table_size": (_SZ, [_I, _I]),
+    "moe_ep_dispatch": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_ep_recv_reorder": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_ep_return_gather": (_I, [_P, _P, _I, _I, _P, _P]),
+    "moe_ep_expert_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
+    "moe_ep_expert_forward": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _SZ,
+                                   _P]),
+    "moe_ep_combine": (_I, [_P, _P, _P, _I, _I, _I, _P, _P]),
 }
 
 
@@ -213,6 +227,49 @@ def moe_permute_quant_noalloc(x, topk_ids, E, a_q, scale_a, src2dst, offsets, st
         _ptr(x), _ptr(topk_ids), T, H, E, K, _ptr(_u8(a_q)), _ptr(scale_a), _ptr(src2dst),
         _ptr(offsets), _stream(stream)))
     return a_q, scale_a, src2dst, offsets
+
+
+def moe_permute_quant_rows(x, topk_ids, E, workspace=None, stream=None):
+    """Pre-reorder storing each token's codes once, in token order. Returns
+    (a_tok [T,H], scale_a [T*K], src2dst [T*K], row_token [T*K], offsets)."""
+    import torch
+    _need_cuda(x, topk_ids, workspace)
+    T, H = x.shape
+    K = topk_ids.shape[1]
+    dev = x.device
+    M = T * K
+    a_tok = torch.empty((T, H), dtype=torch.uint8, device=dev)
+    scale_a = torch.empty(M, dtype=torch.float32, device=dev)
+    src2dst = torch.empty(M, dtype=torch.int32, device=dev)
+    row_token = torch.empty(M, dtype=torch.int32, device=dev)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    if workspace is None:
+        workspace = torch.empty(max(moe_permute_workspace_size(T, E, K), 256), dtype=torch.uint8,
+                                device=dev)
+    _check("moe_permute_quant_rows", load().moe_permute_quant_rows(
+        _ptr(x), _ptr(topk_ids), T, H, E, K, _ptr(a_tok), _ptr(scale_a), _ptr(src2dst),
+        _ptr(row_token), _ptr(offsets), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+    return a_tok, scale_a, src2dst, row_token, offsets
+
+
+def moe_grouped_gemm_rows(A_tok, row_token, scale_a, B, scale_b, offsets, epilogue=EPI_BF16,
+                          C=None, row_amax=None, stream=None):
+    """moe_grouped_gemm with permuted row r of A = A_tok[row_token[r]]."""
+    import torch
+    _need_cuda(A_tok, row_token, scale_a, B, scale_b, offsets, C, row_amax)
+    T, Kd = A_tok.shape
+    M = row_token.numel()
+    E, N, Kd2 = B.shape
+    if Kd != Kd2:
+        raise ValueError("moe_grouped_gemm_rows: K mismatch")
+    if C is None:
+        cols = N // 2 if epilogue == EPI_SILU_MUL else N
+        C = torch.empty((M, cols), dtype=torch.bfloat16, device=A_tok.device)
+    _check("moe_grouped_gemm_rows", load().moe_grouped_gemm_rows(
+        _ptr(_u8(A_tok)), T, _ptr(row_token), _ptr(scale_a), _ptr(_u8(B)), _ptr(scale_b),
+        _ptr(offsets), M, N, Kd, E, epilogue, _ptr(C), _ptr(row_amax), _stream(stream)))
+    return C
 
 
 def moe_grouped_gemm(A, scale_a, B, scale_b, offsets, epilogue=EPI_BF16, C=None, row_amax=None,
@@ -542,3 +599,7 @@ class MoELayer:
                                 self.s2, self.num_groups, self.topk_group, self.top_k,
                                 self.scoring, self.renormalize, self.rsf, out_host,
                                 self.workspace, stream=stream)
+
+
+from .ep import (EPMoELayer, moe_ep_combine, moe_ep_dispatch, moe_ep_expert_forward,  # noqa: E402
+                 moe_ep_recv_reorder, moe_ep_return_gather)

@@ -217,6 +217,9 @@ moe_status run_forward(const void* x, const float* logits, const float* bias, co
                                        down, err, st, kChain, /*early_table=*/true)))
       return cuda_status(e);
   } else {
+    // (the token-order rows of moe_permute_quant_rows with four-row TMA
+    // gathers in the GEMM measured 2.5x slower for w13 than these K-fold
+    // copies loaded as 64-row boxes, so the forward keeps the copies)
     if ((e = launch_permute_quant(x, ids, T, H, EA, KA, a_q, sa, s2d, offsets,
                                   at<void>(ws, L.perm), err, st, kChain)))
       return cuda_status(e);
@@ -309,6 +312,38 @@ moe_status moe_grouped_gemm(const void* A, const float* scale_a, const void* B,
   if (err == nullptr) return MOE_ERR_CUDA;
   return cuda_status(launch_grouped_gemm(A, scale_a, B, scale_b, offsets, M, N, Kd, E, epilogue,
                                          C, row_amax, err, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_permute_quant_rows(const void* x, const int32_t* topk_ids, int T, int H, int E,
+                                  int K, void* a_tok, float* scale_a, int32_t* src2dst,
+                                  int32_t* row_token, int32_t* offsets, void* ws,
+                                  size_t ws_bytes, void* stream) {
+  moe_status s = check_permute(x, topk_ids, T, H, E, K, a_tok, scale_a, src2dst, offsets, ws,
+                               ws_bytes);
+  if (s != MOE_OK) return s;
+  if (T > 0 && !ok_ptr(row_token)) return MOE_ERR_INVALID_ARG;
+  int* err = device_error_word();
+  if (err == nullptr) return MOE_ERR_CUDA;
+  return cuda_status(launch_permute_quant(x, topk_ids, T, H, E, K, a_tok, scale_a, src2dst,
+                                          offsets, ws, err, static_cast<cudaStream_t>(stream),
+                                          false, T > 0 ? row_token : nullptr));
+}
+
+moe_status moe_grouped_gemm_rows(const void* A_tok, int T, const int32_t* row_token,
+                                 const float* scale_a, const void* B, const float* scale_b,
+                                 const int32_t* offsets, int M, int N, int Kd, int E,
+                                 int epilogue, void* C, float* row_amax, void* stream) {
+  if (T < 0) return MOE_ERR_INVALID_ARG;
+  moe_status s = check_gemm(A_tok, scale_a, B, scale_b, offsets, M, N, Kd, E, epilogue, C,
+                            row_amax);
+  if (s != MOE_OK) return s;
+  if (M > 0 && (T < 1 || !ok_ptr(row_token))) return MOE_ERR_INVALID_ARG;
+  int* err = device_error_word();
+  if (err == nullptr) return MOE_ERR_CUDA;
+  return cuda_status(launch_grouped_gemm(A_tok, scale_a, B, scale_b, offsets, M, N, Kd, E,
+                                         epilogue, C, row_amax, err,
+                                         static_cast<cudaStream_t>(stream), -1, false, false,
+                                         row_token, T));
 }
 
 moe_status moe_test_gemm_timeout(const void* A, const float* scale_a, const void* B,
@@ -534,6 +569,154 @@ moe_status moe_forward_block_host(const void* x_host, const float* logits_host,
   return forward_host(x_host, logits_host, bias, w13, s13, w2, s2, T, H, I, E, n_shared,
                       num_groups, topk_group, top_k, scoring, renormalize,
                       routed_scaling_factor, out_host, ws, ws_bytes, stream, true);
+}
+
+// ---- expert-parallel dispatch / combine ---------------------------------------
+size_t moe_ep_table_size(int R, int EPR) {
+  if (R < 1 || EPR < 1) return 0;
+  return ep_table_bytes(R, EPR);
+}
+
+moe_status moe_ep_dispatch(const void* x, const int32_t* topk_ids, int T, int H, int E, int K,
+                           int R, void* a_q, float* scale_a, int32_t* src2dst, int32_t* offsets,
+                           int32_t* expert_counts, void* ws, size_t ws_bytes, void* stream) {
+  if (R < 1 || E < 1 || E % R != 0) return MOE_ERR_INVALID_ARG;
+  if (R * (E / R) > ep_max_table() || E > kMaxE) return MOE_ERR_UNSUPPORTED;
+  if (!ok_ptr(expert_counts)) return MOE_ERR_INVALID_ARG;
+  moe_status s = check_permute(x, topk_ids, T, H, E, K, a_q, scale_a, src2dst, offsets, ws,
+                               ws_bytes);
+  if (s != MOE_OK) return s;
+  int* err = device_error_word();
+  if (err == nullptr) return MOE_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_permute_quant(x, topk_ids, T, H, E, K, a_q, scale_a, src2dst, offsets,
+                                       ws, err, st);
+  if (e != cudaSuccess) return cuda_status(e);
+  return cuda_status(launch_ep_counts(offsets, E, expert_counts, st, true));
+}
+
+namespace {
+moe_status check_ep_recv(const void* rows, const float* scales, const int32_t* cnt, int R,
+                         int EPR, int Mr, int H) {
+  if (R < 1 || EPR < 1 || Mr < 0 || H < 1 || H % 32 != 0) return MOE_ERR_INVALID_ARG;
+  if ((int64_t)R * EPR > ep_max_table() || H > kMaxH) return MOE_ERR_UNSUPPORTED;
+  if (!ok_ptr(cnt)) return MOE_ERR_INVALID_ARG;
+  if (Mr > 0 && (!ok_ptr(rows) || !ok_ptr(scales))) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+// Workspace of moe_ep_expert_forward: the merge table, then the local
+// layer's intermediates, 256-byte aligned pieces.
+struct EpLayout {
+  size_t table, offsets, a_q, sa, a2r, h, q2, sa2, down, total;
+};
+
+EpLayout ep_layout(int Mr, int H, int I, int R, int EPR) {
+  EpLayout L;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o += align_up(bytes > 0 ? bytes : 1);
+    return at;
+  };
+  const size_t M = (size_t)(Mr > 0 ? Mr : 0);
+  L.table = take(ep_table_bytes(R, EPR));
+  L.offsets = take((size_t)(EPR + 1) * 4);
+  L.a_q = take(M * H);
+  L.sa = take(M * 4);
+  L.a2r = take(M * 4);
+  L.h = take(M * I * 2);
+  L.q2 = take(M * I);
+  L.sa2 = take(M * 4);
+  L.down = take(M * H * 2);
+  L.total = o;
+  return L;
+}
+}  // namespace
+
+moe_status moe_ep_recv_reorder(const void* recv_rows, const float* recv_scales,
+                               const int32_t* recv_counts, int R, int EPR, int Mr, int H,
+                               void* a_q, float* scale_a, int32_t* offsets,
+                               int32_t* arrival2row, void* ws, size_t ws_bytes, void* stream) {
+  moe_status s = check_ep_recv(recv_rows, recv_scales, recv_counts, R, EPR, Mr, H);
+  if (s != MOE_OK) return s;
+  if (!ok_ptr(offsets)) return MOE_ERR_INVALID_ARG;
+  if (Mr > 0 && (!ok_ptr(a_q) || !ok_ptr(scale_a) || !ok_ptr(arrival2row)))
+    return MOE_ERR_INVALID_ARG;
+  if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0 ||
+      ws_bytes < ep_table_bytes(R, EPR))
+    return MOE_ERR_WORKSPACE;
+  int* err = device_error_word();
+  if (err == nullptr) return MOE_ERR_CUDA;
+  return cuda_status(launch_ep_recv_reorder(recv_rows, recv_scales, recv_counts, R, EPR, Mr, H,
+                                            a_q, scale_a, offsets, arrival2row, ws, err,
+                                            static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_ep_return_gather(const void* down, const int32_t* arrival2row, int Mr, int H,
+                                void* back, void* stream) {
+  if (Mr < 0 || H < 1 || H % 8 != 0) return MOE_ERR_INVALID_ARG;
+  if (Mr > 0 && (!ok_ptr(down) || !ok_ptr(arrival2row) || !ok_ptr(back)))
+    return MOE_ERR_INVALID_ARG;
+  int* err = device_error_word();
+  if (err == nullptr) return MOE_ERR_CUDA;
+  return cuda_status(launch_ep_return_gather(down, arrival2row, Mr, H, back, err,
+                                             static_cast<cudaStream_t>(stream)));
+}
+
+size_t moe_ep_expert_workspace_size(int Mr, int H, int I, int R, int EPR) {
+  if (Mr < 0 || H < 1 || I < 1 || R < 1 || EPR < 1) return 0;
+  return ep_layout(Mr, H, I, R, EPR).total;
+}
+
+moe_status moe_ep_expert_forward(const void* recv_rows, const float* recv_scales,
+                                 const int32_t* recv_counts, int R, int EPR, int Mr, int H,
+                                 int I, const void* w13, const float* s13, const void* w2,
+                                 const float* s2, void* back, void* ws, size_t ws_bytes,
+                                 void* stream) {
+  moe_status s = check_ep_recv(recv_rows, recv_scales, recv_counts, R, EPR, Mr, H);
+  if (s != MOE_OK) return s;
+  if (I < 1 || I % 32 != 0) return MOE_ERR_INVALID_ARG;
+  if ((int64_t)EPR * 2 * I >= ((int64_t)1 << 31) || (int64_t)EPR * H >= ((int64_t)1 << 31))
+    return MOE_ERR_UNSUPPORTED;
+  if (!ok_ptr(w13) || !ok_ptr(s13) || !ok_ptr(w2) || !ok_ptr(s2)) return MOE_ERR_INVALID_ARG;
+  if (Mr > 0 && !ok_ptr(back)) return MOE_ERR_INVALID_ARG;
+  const EpLayout L = ep_layout(Mr, H, I, R, EPR);
+  if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0 ||
+      ws_bytes < L.total)
+    return MOE_ERR_WORKSPACE;
+  int* err = device_error_word();
+  if (err == nullptr) return MOE_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int32_t* offsets = at<int32_t>(ws, L.offsets);
+  void* a_q = at<void>(ws, L.a_q);
+  float* sa = at<float>(ws, L.sa);
+  int32_t* a2r = at<int32_t>(ws, L.a2r);
+  void* h = at<void>(ws, L.h);
+  void* q2 = at<void>(ws, L.q2);
+  float* sa2 = at<float>(ws, L.sa2);
+  void* down = at<void>(ws, L.down);
+  // merge -> w13 GEMM + SiLU*mul -> requant -> w2 GEMM -> back to arrival
+  // order, each a programmatic dependent of the one before (the merge table
+  // first, launched plainly)
+  cudaError_t e;
+  if ((e = launch_ep_recv_reorder(recv_rows, recv_scales, recv_counts, R, EPR, Mr, H, a_q, sa,
+                                  offsets, a2r, at<void>(ws, L.table), err, st, false)))
+    return cuda_status(e);
+  if (Mr == 0) return MOE_OK;
+  if ((e = launch_grouped_gemm(a_q, sa, w13, s13, offsets, Mr, 2 * I, H, EPR, MOE_EPI_SILU_MUL,
+                               h, nullptr, err, st, -1, true)))
+    return cuda_status(e);
+  if ((e = launch_act_quant(h, nullptr, Mr, I, q2, sa2, st, true))) return cuda_status(e);
+  if ((e = launch_grouped_gemm(q2, sa2, w2, s2, offsets, Mr, H, I, EPR, MOE_EPI_BF16, down,
+                               nullptr, err, st, -1, true, /*early_table=*/true)))
+    return cuda_status(e);
+  return cuda_status(launch_ep_return_gather(down, a2r, Mr, H, back, err, st, true));
+}
+
+moe_status moe_ep_combine(const void* back_rows, const int32_t* src2dst, const float* topk_w,
+                          int T, int K, int H, void* out, void* stream) {
+  return moe_unpermute_sum(back_rows, src2dst, topk_w, T, K, H, out, stream);
 }
 
 moe_status moe_device_status(int* code) {

@@ -100,6 +100,10 @@ struct Params {
   int stall_stage;     // failure test: CTA 0 never loads its stage with this index (-1: none)
   int w_stage_box;     // the weight map holds a stage per box (else a K chunk)
   int early_table;     // build the tile table before waiting for the previous kernel
+  // token rows gathered from a token-order A ([T, Kd], maps.xg): permuted row
+  // r is row row_token[r] of it (null: A is in permuted order, maps.x)
+  const int32_t* row_token;
+  int T;
 };
 
 // CS = 1: one CTA per tile of 128 weight rows x N tokens.
@@ -124,9 +128,13 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int lane = tid & 31;
   const int E = p.E;
 
+  const bool gather = p.row_token != nullptr;
   if (warp == 0 && lane == 0) {
     ptx::prefetch_tensormap(&maps.w);
-    for (int i = 0; i < NXBOX; ++i) ptx::prefetch_tensormap(&maps.x[i]);
+    if (gather)
+      ptx::prefetch_tensormap(&maps.xg);
+    else
+      for (int i = 0; i < NXBOX; ++i) ptx::prefetch_tensormap(&maps.x[i]);
     for (int s = 0; s < STAGES; ++s) {
       ptx::mbar_init(&sm.full[s], 1);   // pair: only the even CTA's is used
       ptx::mbar_init(&sm.empty[s], 1);  // one (multicast) MMA commit
@@ -173,41 +181,60 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint32_t armed = 0, armed_par = 0;
   if (warp == 0) {
     // ======================= TMA producer ===================================
-    if (lane == 0) {
-      // weights: evict-first when a block is read once (every block when
-      // streaming; otherwise the blocks of experts whose tokens fit one
-      // chunk), so they do not push the token tiles, read once per weight
-      // block group, out of L2
-      const uint64_t pol_w = p.stream_weights ? ptx::policy_evict_first() : ptx::policy_evict_normal();
-      const uint64_t pol_w1 = ptx::policy_evict_first();
-      const uint64_t pol_x = ptx::policy_evict_last();
-      uint32_t s = 0, ph = 0;
-      int gstage = 0;  // stages issued by this CTA
-      bool ok = true;
-      for (int g = cluster; ok && g < total; g += nclusters) {
-        const TileInfo<BNMAX> t = decode_tile<BNMAX>(sm, E, NBG, g);
-        const int nb = t.nb * CS + rank;
-        // token rows of the MMA (N): a multiple of 16, of 32 for a pair so
-        // each CTA holds N/2 rows; this CTA loads rows [rank*half, +half)
-        const int rows = PAIR ? (t.ntok + 31) & ~31 : (t.ntok + 15) & ~15;
-        const int half = rows / CS;
-        const uint32_t bytes = KC * (CS * W_BYTES + (uint32_t)rows * BK);  // all CTAs' loads
-        const int y0 = t.e * p.N + nb * BM;  // bf16 epilogue: the tile's first weight row
-        for (int ks = 0; ks < KS; ++ks) {
-          if (!ptx::mbar_wait(&sm.empty[s], ph ^ 1u, &sm.abort, WAIT_NS)) {
-            ok = false;
-            break;
+    // lane 0 waits for free stages, arms them and loads the weights (and the
+    // token boxes); with a token-order A every lane gathers four token rows
+    // of the stage per instruction (G4 groups of four rows per lane)
+    constexpr int G4 = (BNMAX / CS + 127) / 128;
+    // weights: evict-first when a block is read once (every block when
+    // streaming; otherwise the blocks of experts whose tokens fit one
+    // chunk), so they do not push the token tiles, read once per weight
+    // block group, out of L2
+    const uint64_t pol_w = p.stream_weights ? ptx::policy_evict_first() : ptx::policy_evict_normal();
+    const uint64_t pol_w1 = ptx::policy_evict_first();
+    const uint64_t pol_x = ptx::policy_evict_last();
+    uint32_t s = 0, ph = 0;
+    int gstage = 0;  // stages issued by this CTA
+    bool ok = true;
+    for (int g = cluster; ok && g < total; g += nclusters) {
+      const TileInfo<BNMAX> t = decode_tile<BNMAX>(sm, E, NBG, g);
+      const int nb = t.nb * CS + rank;
+      // token rows of the MMA (N): a multiple of 16, of 32 for a pair so
+      // each CTA holds N/2 rows; this CTA loads rows [rank*half, +half)
+      const int rows = PAIR ? (t.ntok + 31) & ~31 : (t.ntok + 15) & ~15;
+      const int half = rows / CS;
+      const uint32_t bytes = KC * (CS * W_BYTES + (uint32_t)rows * BK);  // all CTAs' loads
+      const int y0 = t.e * p.N + nb * BM;  // bf16 epilogue: the tile's first weight row
+      // gather: this lane's token rows (rows past the tile: row T, outside
+      // the tensor, read as zeros)
+      int tr[G4][4];
+      if (gather) {
+#pragma unroll
+        for (int q = 0; q < G4; ++q)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int rr = (q * 32 + lane) * 4 + i;  // row within this CTA's half
+            const int rt = rank * half + rr;         // row within the tile
+            tr[q][i] = (rr < half && rt < t.ntok) ? __ldg(p.row_token + t.tok0 + rt) : p.T;
           }
+      }
+      for (int ks = 0; ks < KS; ++ks) {
+        // every lane waits (each then sees the stage free before it issues)
+        const bool got = ptx::mbar_wait(&sm.empty[s], ph ^ 1u, &sm.abort, WAIT_NS);
+        if (!__all_sync(kFull, got)) {
+          ok = false;
+          break;
+        }
+        // pair: completions count on the even CTA's barrier
+        const uint32_t fb = PAIR ? ptx::map_to_rank(ptx::smem_u32(&sm.full[s]), 0) : 0u;
+        // failure test: the stage is armed but its bytes never come, so the
+        // bounded waits run out
+        const bool stall = blockIdx.x == 0 && gstage++ == p.stall_stage;
+        if (lane == 0) {
           if (rank == 0) {
             ptx::mbar_arrive_expect_tx(&sm.full[s], bytes);
             armed |= 1u << s;
             armed_par = (armed_par & ~(1u << s)) | (ph << s);
           }
-          // pair: completions count on the even CTA's barrier
-          const uint32_t fb = PAIR ? ptx::map_to_rank(ptx::smem_u32(&sm.full[s]), 0) : 0u;
-          // failure test: the stage is armed but its bytes never come, so the
-          // bounded waits run out
-          const bool stall = blockIdx.x == 0 && gstage++ == p.stall_stage;
           if (!stall && p.w_stage_box) {  // the stage's KC weight chunks in one box
             const uint64_t pw = t.nch == 1 ? pol_w1 : pol_w;
             if (PAIR) {
@@ -240,6 +267,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                   ptx::tma_load_2d(sm.w[s][kc], &maps.w, &sm.full[s], kx, y0, pw);
               }
             }
+            if (gather) continue;
             if (PAIR) {
               int r = 0;
 #pragma unroll
@@ -263,16 +291,35 @@ __global__ void __launch_bounds__(THREADS, 1)
               }
             }
           }
-          if (++s == STAGES) {
-            s = 0;
-            ph ^= 1u;
+        }
+        if (gather && !stall) {
+#pragma unroll
+          for (int kc = 0; kc < KC; ++kc) {
+            const int kx = (ks * KC + kc) * BK;
+#pragma unroll
+            for (int q = 0; q < G4; ++q) {
+              const int rr = (q * 32 + lane) * 4;
+              if (rr < half) {
+                uint8_t* xdst = sm.x[s][kc] + rr * BK;
+                if (PAIR)
+                  ptx::tma_gather4_pair(xdst, &maps.xg, fb, kx, tr[q][0], tr[q][1], tr[q][2],
+                                        tr[q][3], pol_x);
+                else
+                  ptx::tma_gather4(xdst, &maps.xg, &sm.full[s], kx, tr[q][0], tr[q][1],
+                                   tr[q][2], tr[q][3], pol_x);
+              }
+            }
           }
         }
+        if (++s == STAGES) {
+          s = 0;
+          ph ^= 1u;
+        }
       }
-      if (!ok) {
-        sm.abort = 1;
-        flag_error(p.err, MOE_DEV_PIPE_TIMEOUT);
-      }
+    }
+    if (!ok && lane == 0) {
+      sm.abort = 1;
+      flag_error(p.err, MOE_DEV_PIPE_TIMEOUT);
     }
   } else if (warp == 1) {
     // ======================= MMA issuer =====================================
@@ -647,6 +694,13 @@ bool make_tma_map_u8(CUtensorMap* m, const void* base, uint64_t rows, uint64_t c
   return encode_u8(m, base, 2, dims, strides, box);
 }
 
+bool make_tma_map_rows(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols) {
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols};
+  const cuuint32_t box[2] = {BK, 1};
+  return encode_u8(m, base, 2, dims, strides, box);
+}
+
 bool make_tma_map_weights(CUtensorMap* m, const void* base, bool silu, uint64_t E, uint64_t N,
                           uint64_t Kd, uint32_t kc) {
   if (!weights_stage_box(Kd)) {  // one chunk per box, zero past Kd
@@ -678,13 +732,16 @@ bool make_tma_map_weights(CUtensorMap* m, const void* base, bool silu, uint64_t 
 
 }  // namespace gemm_common
 
+bool gemm_many_rows(int M, int E) { return (int64_t)M > (int64_t)32 * E; }
+
 cudaError_t launch_grouped_gemm(const void* A, const float* scale_a, const void* B,
                                 const float* scale_b, const int32_t* offsets, int M, int N,
                                 int Kd, int E, int epilogue, void* C, float* row_amax, int* err,
-                                cudaStream_t st, int stall_stage, bool pdl, bool early_table) {
+                                cudaStream_t st, int stall_stage, bool pdl, bool early_table,
+                                const int32_t* row_token, int T) {
   if (M == 0) return cudaSuccess;
   const bool silu = (epilogue == MOE_EPI_SILU_MUL);
-  const bool small = (int64_t)M <= (int64_t)32 * E;  // few rows per expert (decode)
+  const bool small = !gemm_many_rows(M, E);  // few rows per expert (decode)
   // K chunks per stage of the configuration launched below (the weight box
   // holds one stage)
   const int nb_blocks = silu ? (N / 2 + 63) / 64 : (N + BM - 1) / BM;
@@ -692,10 +749,16 @@ cudaError_t launch_grouped_gemm(const void* A, const float* scale_a, const void*
   Maps maps;
   if (!make_tma_map_weights(&maps.w, B, silu, (uint64_t)E, (uint64_t)N, (uint64_t)Kd, kc))
     return cudaErrorNotSupported;
-  for (int i = 0; i < NXBOX; ++i)
-    if (!make_tma_map_u8(&maps.x[i], A, (uint64_t)M, (uint64_t)Kd, 64u >> i))
-      return cudaErrorNotSupported;
+  if (row_token != nullptr) {  // A is [T, Kd] in token order
+    if (!make_tma_map_rows(&maps.xg, A, (uint64_t)T, (uint64_t)Kd)) return cudaErrorNotSupported;
+  } else {
+    for (int i = 0; i < NXBOX; ++i)
+      if (!make_tma_map_u8(&maps.x[i], A, (uint64_t)M, (uint64_t)Kd, 64u >> i))
+        return cudaErrorNotSupported;
+  }
   Params p;
+  p.row_token = row_token;
+  p.T = T;
   p.scale_a = scale_a;
   p.scale_b = scale_b;
   p.offsets = offsets;

@@ -42,6 +42,7 @@ constexpr int NXBOX = 3;
 struct Maps {
   CUtensorMap w;           // weights (see above; SiLU: 5-D or 4-D, bf16: 3-D or 2-D)
   CUtensorMap x[NXBOX];    // tokens: box rows 64 >> i
+  CUtensorMap xg;          // token-order rows [T, Kd], box one row high (gather4)
 };
 
 template <int BNMAX>
@@ -156,6 +157,10 @@ __device__ __forceinline__ void build_tile_table(S& sm, const int32_t* offsets, 
 // driver cannot encode it.
 bool make_tma_map_u8(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
                      uint32_t box_rows);
+
+// Host: 2-D u8 tensor [rows, cols] with a box of 128 B x 1 row (128-byte
+// swizzle, zero fill) for four-row gathers.
+bool make_tma_map_rows(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols);
 
 // Host: the weight map of a [E, N, Kd] tensor (see Maps::w): boxes of `kc`
 // K chunks when Kd % 128 == 0 (weights_stage_box), else of one chunk;

@@ -27,9 +27,13 @@ cudaError_t launch_gate(const float* logits, const float* bias, int T, int E, in
 
 // permute.cu
 size_t permute_ws_bytes(int T, int E);
+// row_token non-null: a_q is [T, H], each token's codes stored once in token
+// order, and row_token [T*K] receives the token of every permuted row (the
+// grouped GEMM then gathers the rows, see launch_grouped_gemm).
 cudaError_t launch_permute_quant(const void* x, const int32_t* ids, int T, int H, int E, int K,
                                  void* a_q, float* scale_a, int32_t* src2dst, int32_t* offsets,
-                                 void* ws, int* err, cudaStream_t st, bool pdl = false);
+                                 void* ws, int* err, cudaStream_t st, bool pdl = false,
+                                 int32_t* row_token = nullptr);
 
 // permute.cu: the same with one scale per 128 channels, scale_a [T*K, H/128]
 // (H % 128 == 0).
@@ -46,11 +50,16 @@ void* permute_static_scratch();
 // Returns cudaErrorNotSupported when the TMA descriptors cannot be encoded.
 // `early_table`: the offsets were written two or more kernels earlier on the
 // stream, so the tile table is built before waiting for the previous kernel.
+// row_token non-null: A is [T, Kd] in token order and permuted row r's
+// tokens are row row_token[r] of it (loaded by four-row TMA gathers).
 cudaError_t launch_grouped_gemm(const void* A, const float* scale_a, const void* B,
                                 const float* scale_b, const int32_t* offsets, int M, int N,
                                 int Kd, int E, int epilogue, void* C, float* row_amax, int* err,
                                 cudaStream_t st, int stall_stage = -1, bool pdl = false,
-                                bool early_table = false);
+                                bool early_table = false, const int32_t* row_token = nullptr,
+                                int T = 0);
+// Whether the grouped GEMM takes its many-rows-per-expert configuration.
+bool gemm_many_rows(int M, int E);
 
 // gemm_block.cu: block scales, scale_a [M, Kd/128], scale_b [E, N/128, Kd/128]
 // (N % 128 == 0, Kd % 128 == 0); no row amax.
@@ -71,5 +80,18 @@ cudaError_t launch_act_quant_block(const void* h, int M, int I, void* q, float* 
 cudaError_t launch_unpermute_sum(const void* down, const int32_t* src2dst, const float* w,
                                  int T, int K, int H, void* out, int* err, cudaStream_t st,
                                  bool pdl = false);
+
+// ep.cu: expert-parallel merge of received rows and gather back.
+// table: ep_table_bytes(R, EPR) bytes of scratch (256-byte aligned).
+size_t ep_table_bytes(int R, int EPR);
+int ep_max_table();  // largest R * EPR
+cudaError_t launch_ep_counts(const int32_t* offsets, int E, int32_t* counts, cudaStream_t st,
+                             bool pdl = false);
+cudaError_t launch_ep_recv_reorder(const void* rows, const float* scales, const int32_t* cnt,
+                                   int R, int EPR, int Mr, int H, void* a_q, float* scale_a,
+                                   int32_t* offsets, int32_t* arrival2row, void* table,
+                                   int* err, cudaStream_t st, bool pdl = false);
+cudaError_t launch_ep_return_gather(const void* down, const int32_t* arrival2row, int Mr, int H,
+                                    void* back, int* err, cudaStream_t st, bool pdl = false);
 
 }  // namespace moe

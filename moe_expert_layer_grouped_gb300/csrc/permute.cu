@@ -147,11 +147,15 @@ constexpr int kQuantThreads = 128;
 // amax (per row, or per 128 channels when BLOCK), quantises it and stores the
 // codes and scale to every destination row dst[0..K) >= 0. dst[] is written
 // by threads 0..K-1 before the call; it is read only after a block barrier.
+// With row_token (per-token scales only), the codes are stored once, in
+// token order (row t of a_q, [T, H]), and row_token[d] = t is written for
+// every destination row d instead; the scales still go to every d.
 template <int VPT, bool BLOCK, int NT = kQuantThreads>
 __device__ __forceinline__ void quant_scatter(const __nv_bfloat16* __restrict__ x, int t, int H,
                                               int K, const int* dst, float* red,
                                               uint8_t* __restrict__ a_q,
-                                              float* __restrict__ scale_a) {
+                                              float* __restrict__ scale_a,
+                                              int32_t* __restrict__ row_token = nullptr) {
   const int tid = threadIdx.x;
   const int nvec = H >> 3;
   const uint4* xr = reinterpret_cast<const uint4*>(x + (int64_t)t * H);
@@ -201,7 +205,10 @@ __device__ __forceinline__ void quant_scatter(const __nv_bfloat16* __restrict__ 
 #pragma unroll
   for (int w = 1; w < NT / 32; ++w) amax = fmaxf(amax, red[w]);
   const float sc = token_scale(amax);
-  if (tid < K && dst[tid] >= 0) scale_a[dst[tid]] = sc;
+  if (tid < K && dst[tid] >= 0) {
+    scale_a[dst[tid]] = sc;
+    if (row_token != nullptr) row_token[dst[tid]] = t;
+  }
 #pragma unroll
   for (int i = 0; i < VPT; ++i) {
     const int idx = tid + i * NT;
@@ -209,6 +216,10 @@ __device__ __forceinline__ void quant_scatter(const __nv_bfloat16* __restrict__ 
       float f[8];
       bf16x8_to_f32(v[i], f);
       const uint2 q = quant8(f, sc);
+      if (row_token != nullptr) {
+        *reinterpret_cast<uint2*>(a_q + (int64_t)t * H + (int64_t)idx * 8) = q;
+        continue;
+      }
       for (int k = 0; k < K; ++k) {
         const int d = dst[k];
         if (d >= 0) *reinterpret_cast<uint2*>(a_q + (int64_t)d * H + (int64_t)idx * 8) = q;
@@ -226,7 +237,8 @@ __global__ void __launch_bounds__(kQuantThreads)
     permute_quant_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ ids,
                          const uint32_t* __restrict__ bits, const int32_t* __restrict__ base,
                          int H, int E, int K, uint8_t* __restrict__ a_q,
-                         float* __restrict__ scale_a, int32_t* __restrict__ src2dst) {
+                         float* __restrict__ scale_a, int32_t* __restrict__ src2dst,
+                         int32_t* __restrict__ row_token) {
   chain_entry();
   __shared__ int dst[32];
   __shared__ float red[kQuantThreads / 32];
@@ -243,7 +255,7 @@ __global__ void __launch_bounds__(kQuantThreads)
     dst[tid] = d;
     src2dst[(int64_t)t * K + tid] = d;
   }
-  quant_scatter<VPT, BLOCK>(x, t, H, K, dst, red, a_q, scale_a);
+  quant_scatter<VPT, BLOCK>(x, t, H, K, dst, red, a_q, scale_a, row_token);
 }
 
 // Small batches (T <= 512, T*K <= 4096): one launch does the routing and the
@@ -267,7 +279,7 @@ __global__ void __launch_bounds__(kSmallThreads)
                                const int32_t* __restrict__ ids, int T, int H, int E, int K,
                                uint8_t* __restrict__ a_q, float* __restrict__ scale_a,
                                int32_t* __restrict__ src2dst, int32_t* __restrict__ offsets,
-                               int* err) {
+                               int* err, int32_t* __restrict__ row_token) {
   chain_entry();
   extern __shared__ int route_smem[];
   __shared__ int dst[32];
@@ -355,26 +367,28 @@ __global__ void __launch_bounds__(kSmallThreads)
     dst[tid] = d;
     src2dst[(int64_t)t * K + tid] = d;
   }
-  quant_scatter<VPT, BLOCK, kSmallThreads>(x, t, H, K, dst, red, a_q, scale_a);
+  quant_scatter<VPT, BLOCK, kSmallThreads>(x, t, H, K, dst, red, a_q, scale_a, row_token);
 }
 
 template <int VPT, bool BLOCK>
 cudaError_t launch_small(const void* x, const int32_t* ids, int T, int H, int E, int K,
                          void* a_q, float* scale_a, int32_t* src2dst, int32_t* offsets, int* err,
-                         cudaStream_t st, bool pdl) {
+                         cudaStream_t st, bool pdl, int32_t* row_token) {
   const size_t smem = sizeof(int) * (2 * (size_t)T * K + 2 * (size_t)E + 1);
   return launch_kernel(permute_quant_small_kernel<VPT, BLOCK>, dim3(T), dim3(kSmallThreads),
                        smem, st, pdl, reinterpret_cast<const __nv_bfloat16*>(x), ids, T, H, E, K,
-                       reinterpret_cast<uint8_t*>(a_q), scale_a, src2dst, offsets, err);
+                       reinterpret_cast<uint8_t*>(a_q), scale_a, src2dst, offsets, err,
+                       row_token);
 }
 
 template <int VPT, bool BLOCK>
 cudaError_t launch_quant(const void* x, const int32_t* ids, const uint32_t* bits,
                          const int32_t* base, int T, int H, int E, int K, void* a_q,
-                         float* scale_a, int32_t* src2dst, cudaStream_t st, bool pdl) {
+                         float* scale_a, int32_t* src2dst, cudaStream_t st, bool pdl,
+                         int32_t* row_token) {
   return launch_kernel(permute_quant_kernel<VPT, BLOCK>, dim3(T), dim3(kQuantThreads), 0, st,
                        pdl, reinterpret_cast<const __nv_bfloat16*>(x), ids, bits, base, H, E, K,
-                       reinterpret_cast<uint8_t*>(a_q), scale_a, src2dst);
+                       reinterpret_cast<uint8_t*>(a_q), scale_a, src2dst, row_token);
 }
 
 }  // namespace
@@ -410,14 +424,15 @@ namespace {
 template <bool BLOCK>
 cudaError_t permute_quant(const void* x, const int32_t* ids, int T, int H, int E, int K,
                           void* a_q, float* scale_a, int32_t* src2dst, int32_t* offsets,
-                          void* ws, int* err, cudaStream_t st, bool pdl) {
+                          void* ws, int* err, cudaStream_t st, bool pdl,
+                          int32_t* row_token = nullptr) {
   if (T > 0 && T <= kSmallTokens && T * K <= kSmallRoute) {
     const int vpt = (H / 8 + kSmallThreads - 1) / kSmallThreads;
-    if (vpt <= 1) return launch_small<1, BLOCK>(x, ids, T, H, E, K, a_q, scale_a, src2dst, offsets, err, st, pdl);
-    if (vpt <= 2) return launch_small<2, BLOCK>(x, ids, T, H, E, K, a_q, scale_a, src2dst, offsets, err, st, pdl);
-    if (vpt <= 4) return launch_small<4, BLOCK>(x, ids, T, H, E, K, a_q, scale_a, src2dst, offsets, err, st, pdl);
-    if (vpt <= 8) return launch_small<8, BLOCK>(x, ids, T, H, E, K, a_q, scale_a, src2dst, offsets, err, st, pdl);
-    return launch_small<16, BLOCK>(x, ids, T, H, E, K, a_q, scale_a, src2dst, offsets, err, st, pdl);
+    if (vpt <= 1) return launch_small<1, BLOCK>(x, ids, T, H, E, K, a_q, scale_a, src2dst, offsets, err, st, pdl, row_token);
+    if (vpt <= 2) return launch_small<2, BLOCK>(x, ids, T, H, E, K, a_q, scale_a, src2dst, offsets, err, st, pdl, row_token);
+    if (vpt <= 4) return launch_small<4, BLOCK>(x, ids, T, H, E, K, a_q, scale_a, src2dst, offsets, err, st, pdl, row_token);
+    if (vpt <= 8) return launch_small<8, BLOCK>(x, ids, T, H, E, K, a_q, scale_a, src2dst, offsets, err, st, pdl, row_token);
+    return launch_small<16, BLOCK>(x, ids, T, H, E, K, a_q, scale_a, src2dst, offsets, err, st, pdl, row_token);
   }
   const int C = (T + 31) / 32;
   uint32_t* bits = reinterpret_cast<uint32_t*>(ws);
@@ -435,11 +450,11 @@ cudaError_t permute_quant(const void* x, const int32_t* ids, int T, int H, int E
     return e;
   if (T > 0) {
     const int vpt = (H / 8 + kQuantThreads - 1) / kQuantThreads;
-    if (vpt <= 1) return launch_quant<1, BLOCK>(x, ids, bits, base, T, H, E, K, a_q, scale_a, src2dst, st, pdl);
-    if (vpt <= 2) return launch_quant<2, BLOCK>(x, ids, bits, base, T, H, E, K, a_q, scale_a, src2dst, st, pdl);
-    if (vpt <= 4) return launch_quant<4, BLOCK>(x, ids, bits, base, T, H, E, K, a_q, scale_a, src2dst, st, pdl);
-    if (vpt <= 8) return launch_quant<8, BLOCK>(x, ids, bits, base, T, H, E, K, a_q, scale_a, src2dst, st, pdl);
-    return launch_quant<16, BLOCK>(x, ids, bits, base, T, H, E, K, a_q, scale_a, src2dst, st, pdl);
+    if (vpt <= 1) return launch_quant<1, BLOCK>(x, ids, bits, base, T, H, E, K, a_q, scale_a, src2dst, st, pdl, row_token);
+    if (vpt <= 2) return launch_quant<2, BLOCK>(x, ids, bits, base, T, H, E, K, a_q, scale_a, src2dst, st, pdl, row_token);
+    if (vpt <= 4) return launch_quant<4, BLOCK>(x, ids, bits, base, T, H, E, K, a_q, scale_a, src2dst, st, pdl, row_token);
+    if (vpt <= 8) return launch_quant<8, BLOCK>(x, ids, bits, base, T, H, E, K, a_q, scale_a, src2dst, st, pdl, row_token);
+    return launch_quant<16, BLOCK>(x, ids, bits, base, T, H, E, K, a_q, scale_a, src2dst, st, pdl, row_token);
   }
   return cudaSuccess;
 }
@@ -448,9 +463,10 @@ cudaError_t permute_quant(const void* x, const int32_t* ids, int T, int H, int E
 
 cudaError_t launch_permute_quant(const void* x, const int32_t* ids, int T, int H, int E, int K,
                                  void* a_q, float* scale_a, int32_t* src2dst, int32_t* offsets,
-                                 void* ws, int* err, cudaStream_t st, bool pdl) {
+                                 void* ws, int* err, cudaStream_t st, bool pdl,
+                                 int32_t* row_token) {
   return permute_quant<false>(x, ids, T, H, E, K, a_q, scale_a, src2dst, offsets, ws, err, st,
-                              pdl);
+                              pdl, row_token);
 }
 
 cudaError_t launch_permute_quant_block(const void* x, const int32_t* ids, int T, int H, int E,

@@ -128,6 +128,19 @@ __device__ __forceinline__ void tma_load_5d(void* dst, const CUtensorMap* m, uin
       : "memory");
 }
 
+// Four rows of a 2-D tensor (row coordinates r0..r3, any order, out-of-range
+// rows read as the fill value) from column x, each row one box of the map
+// (box one row high), landing as four consecutive box rows at dst;
+// completing on `bar` with 4 x the box's bytes.
+__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* m, uint64_t* bar, int x,
+                                            int r0, int r1, int r2, int r3, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%3, %4, %5, %6, %7}], [%2], %8;" ::"r"(smem_u32(dst)),
+      "l"(m), "r"(smem_u32(bar)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "l"(policy)
+      : "memory");
+}
+
 // ---- clusters -------------------------------------------------------------------
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
@@ -198,6 +211,19 @@ __device__ __forceinline__ void tma_load_5d_pair(void* dst, const CUtensorMap* m
       "cp.async.bulk.tensor.5d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx"
       "::bytes.L2::cache_hint [%0], [%1, {%3, %4, %5, %6, %7}], [%2], %8;" ::"r"(smem_u32(dst)),
       "l"(m), "r"(bar_cluster), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "l"(policy)
+      : "memory");
+}
+
+// tma_gather4 for a CTA-pair MMA (completion counted on `bar_cluster`, a
+// shared::cluster address, possibly in the peer CTA).
+__device__ __forceinline__ void tma_gather4_pair(void* dst, const CUtensorMap* m,
+                                                 uint32_t bar_cluster, int x, int r0, int r1,
+                                                 int r2, int r3, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile::gather4.mbarrier"
+      "::complete_tx::bytes.L2::cache_hint [%0], [%1, {%3, %4, %5, %6, %7}], [%2], %8;" ::"r"(
+          smem_u32(dst)),
+      "l"(m), "r"(bar_cluster), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "l"(policy)
       : "memory");
 }
 
