@@ -35,6 +35,7 @@ FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 FALLBACK_BF16_TFLOPS_SUSTAINED = 1700.0
 FP8_PER_BF16 = 2.0  # nominal dense FP8 : bf16 tensor throughput
+FP4_PER_BF16 = 6.0  # nominal dense FP4 : bf16 on GB300 (13.5 : 2.25 PFLOP/s)
 
 
 def launches_per_forward(wl):
@@ -44,6 +45,14 @@ def launches_per_forward(wl):
     pre = 1 if (wl.T <= 512 and wl.T * k <= 4096) else 3
     return 5 + pre
 N_BATCHES = 4  # distinct token batches cycled through the timed steps
+
+
+DTYPES = {"token": "fp8_e4m3 x fp8_e4m3 -> fp32 (bf16 io)",
+          "block": "fp8_e4m3 x fp8_e4m3, 128-blocks -> fp32 (bf16 io)",
+          "nvfp4": "e2m1 x e2m1, e4m3 scale per 16 -> fp32 (bf16 io)"}
+DATA = {"token": "synthetic (seeded; weights ~N(0,0.02) quantised to e4m3 per channel)",
+        "block": "synthetic (seeded; weights ~N(0,0.02) quantised to e4m3 per 128x128 block)",
+        "nvfp4": "synthetic (seeded; NVFP4 weights drawn in the format, std ~0.02)"}
 
 
 def parse():
@@ -145,6 +154,19 @@ def step_work(wl, offsets_list):
     for off in offsets_list:
         cnt = off[1:] - off[:-1]
         active = int((cnt > 0).sum())
+        if wl.quant == "nvfp4":  # half-byte codes, a scale byte per 16, a global scale
+            w13 = active * (2 * I * H // 2 + 2 * I * H // 16 + 4)
+            w2 = active * (H * I // 2 + H * I // 16 + 4)
+            sa, sa2 = M * H // 16, M * I // 16
+            gemm13_bytes = w13 + M * H // 2 + sa + M * I * 2 + (E + 1) * 4
+            gemm2_bytes = w2 + M * I // 2 + sa2 + M * H * 2 + (E + 1) * 4
+            flops13 = 2.0 * M * 2 * I * H
+            flops2 = 2.0 * M * H * I
+            layer_bytes = w13 + w2 + T * H * 2 + T * wl.E * 4 + T * H * 2
+            res.append(dict(active=active, gemm13_bytes=gemm13_bytes, gemm2_bytes=gemm2_bytes,
+                            flops13=flops13, flops2=flops2, layer_bytes=layer_bytes,
+                            layer_flops=flops13 + flops2))
+            continue
         if wl.quant == "block":  # scales per 128 x 128 weight block / 128 channels
             w13 = active * (2 * I * H + (2 * I // 128) * (H // 128) * 4)
             w2 = active * (H * I + (H // 128) * (I // 128) * 4)
@@ -294,6 +316,7 @@ def time_breakdown(moe, layer, wl, batches, steps, torch):
         ids[:, wl.top_k:] = torch.arange(wl.E, E, dtype=torch.int32, device=dev)
         w[:, wl.top_k:] = 1.0
     block = wl.quant == "block"
+    fp4 = wl.quant == "nvfp4"
     a_q = torch.empty((M, H), dtype=torch.uint8, device=dev)
     sa = torch.empty((M, H // 128) if block else M, dtype=torch.float32, device=dev)
     s2d = torch.empty(M, dtype=torch.int32, device=dev)
@@ -320,6 +343,21 @@ def time_breakdown(moe, layer, wl, batches, steps, torch):
             ids[:, :wl.top_k] = ids_r
             w[:, :wl.top_k] = w_r
         if ev: ev[7].record(st)
+        if fp4:
+            fa, fsa, fs2d, foff = moe.moe_permute_quant_nvfp4(x, ids, E, layer.ga1, workspace=pws)
+            if ev: ev[2].record(st)
+            fh = moe.moe_grouped_gemm_nvfp4(fa, fsa, layer.ga1, layer.w13, layer.s13, layer.g13,
+                                            foff, moe.EPI_SILU_MUL, C=h)
+            if ev: ev[3].record(st)
+            fq, fsf = moe.moe_act_quant_nvfp4(fh, layer.ga2)
+            if ev: ev[4].record(st)
+            fd = moe.moe_grouped_gemm_nvfp4(fq, fsf, layer.ga2, layer.w2, layer.s2, layer.g2,
+                                            foff, moe.EPI_BF16, C=down)
+            if ev: ev[5].record(st)
+            moe.moe_unpermute_sum(fd, fs2d, w, out=out)
+            if ev: ev[6].record(st)
+            off.copy_(foff)
+            return
         if block:
             moe.moe_permute_quant_block(x, ids, E, a_q=a_q, scale_a=sa, src2dst=s2d,
                                         offsets=off, workspace=pws)
@@ -411,12 +449,17 @@ def time_e2e(layer, batches, steps, warmup, torch, barrier=None):
     return e0.elapsed_time(e1) / steps, h2d, d2h
 
 
+def make_layer(moe, wl, d):
+    fp4 = dict(g13=d["g13"], g2=d["g2"], ga1=wl.ga1, ga2=wl.ga2) if wl.quant == "nvfp4" else None
+    return moe.MoELayer(d["w13"], d["s13"], d["w2"], d["s2"], d["bias"], wl.num_groups,
+                        wl.topk_group, wl.top_k, wl.scoring, wl.renormalize, wl.rsf, wl.T,
+                        n_shared=wl.n_shared, quant=wl.quant, nvfp4=fp4)
+
+
 def run_workload(moe, synth, torch, wl, seed, steps, warmup, dev, pk, want_clocks,
                  barrier=None):
     d = synth.make_inputs(wl, seed=seed, device=dev, weights=True)
-    layer = moe.MoELayer(d["w13"], d["s13"], d["w2"], d["s2"], d["bias"], wl.num_groups,
-                         wl.topk_group, wl.top_k, wl.scoring, wl.renormalize, wl.rsf, wl.T,
-                         n_shared=wl.n_shared, quant=wl.quant)
+    layer = make_layer(moe, wl, d)
     batches = make_batches(wl, seed, dev, synth)
     out = torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device=dev)
     clocks = ClockSampler(dev.index) if want_clocks else None
@@ -448,7 +491,12 @@ def roofline_decode(r, pk, workload):
             "launch_ms": round(k, 4), "peak_source": f"{pk['source']} hbm_gbs"}
 
 
-def roofline_prefill(r, pk, clocks=None):
+def tensor_ratio(wl):
+    """Nominal dense tensor throughput of the workload's operand type over bf16."""
+    return FP4_PER_BF16 if wl.quant == "nvfp4" else FP8_PER_BF16
+
+
+def roofline_prefill(r, pk, clocks=None, ratio=FP8_PER_BF16):
     """Tensor roofline of the w13 GEMM. The GEMM is timed in a loop of a
     fraction of a second at full clock, a burst, so the denominator is the
     burst bf16 figure x the FP8:bf16 ratio; the sustained-derived fraction
@@ -458,12 +506,13 @@ def roofline_prefill(r, pk, clocks=None):
     k = r["kern"]["grouped_gemm_w13"]
     fl = r["work"]["flops13"]
     achieved = fl / (k * 1e-3) / 1e12
-    peak = pk["bf16"] * FP8_PER_BF16
-    peak_sus = pk["bf16_sustained"] * FP8_PER_BF16
+    peak = pk["bf16"] * ratio
+    peak_sus = pk["bf16_sustained"] * ratio
+    kind = "fp4" if ratio == FP4_PER_BF16 else "fp8"
     out = {"kernel": "grouped_gemm_w13", "bound": "tensor", "achieved": round(achieved, 1),
            "peak": round(peak, 1), "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
            "traffic": None, "algorithmic_flops_per_launch": fl, "launch_ms": round(k, 4),
-           "peak_source": f"{pk['source']} bf16_tflops (burst) x {FP8_PER_BF16} (fp8/bf16)",
+           "peak_source": f"{pk['source']} bf16_tflops (burst) x {ratio} ({kind}/bf16)",
            "frac_of_sustained_peak": round(achieved / peak_sus, 4),
            "sustained_peak": round(peak_sus, 1)}
     norm = clock_normalised(achieved, clocks, pk)
@@ -485,17 +534,19 @@ def clock_normalised(rate, clocks, pk):
     return rate * mx / med, med, mx
 
 
-def layer_fracs(r, pk, clocks=None):
-    """The layer's FP8 tensor fraction (whole step): burst denominator, the
-    sustained one, and clock-normalised."""
+def layer_fracs(r, pk, clocks=None, ratio=FP8_PER_BF16):
+    """The layer's tensor fraction (whole step) for its operand type (FP8, or
+    FP4 with ratio FP4_PER_BF16): burst denominator, the sustained one, and
+    clock-normalised."""
+    kind = "fp4" if ratio == FP4_PER_BF16 else "fp8"
     tf = r["work"]["layer_flops"] / (r["ms"] * 1e-3) / 1e12
-    out = {"layer_fp8_tensor_frac": round(tf / (pk["bf16"] * FP8_PER_BF16), 4),
-           "layer_fp8_tensor_frac_of_sustained": round(
-               tf / (pk["bf16_sustained"] * FP8_PER_BF16), 4)}
+    out = {f"layer_{kind}_tensor_frac": round(tf / (pk["bf16"] * ratio), 4),
+           f"layer_{kind}_tensor_frac_of_sustained": round(tf / (pk["bf16_sustained"] * ratio),
+                                                           4)}
     norm = clock_normalised(tf, clocks, pk)
     if norm is not None:
-        out["layer_fp8_tensor_frac_clock_normalised"] = round(
-            norm[0] / (pk["bf16"] * FP8_PER_BF16), 4)
+        out[f"layer_{kind}_tensor_frac_clock_normalised"] = round(norm[0] / (pk["bf16"] * ratio),
+                                                                  4)
     return out
 
 
@@ -511,27 +562,43 @@ def workload_config(wl, world):
             "parallelism": f"replicas x{world} (no collective on the data path)"}
 
 
+def oracle_forward(oracle, synth, wl, n):
+    """The oracle's whole-layer function for the workload's format, as
+    f(tokens) -> (out, ids, w); n: the inputs as numpy arrays."""
+    if wl.quant == "nvfp4":
+        import torch
+        w13 = synth.unpack_e2m1(torch.from_numpy(n["w13"])).numpy()
+        w2 = synth.unpack_e2m1(torch.from_numpy(n["w2"])).numpy()
+        return lambda tokens: oracle.forward_tokens_nvfp4(
+            n["x"], n["logits"], n["bias"], w13, n["s13"], n["g13"], w2, n["s2"], n["g2"],
+            wl.ga1, wl.ga2, wl.num_groups, wl.topk_group, wl.top_k, wl.scoring, wl.renormalize,
+            wl.rsf, tokens=tokens, n_shared=wl.n_shared)
+    fwd = oracle.forward_tokens_block if wl.quant == "block" else oracle.forward_tokens
+    return lambda tokens: fwd(n["x"], n["logits"], n["bias"], n["w13"], n["s13"], n["w2"],
+                              n["s2"], wl.num_groups, wl.topk_group, wl.top_k, wl.scoring,
+                              wl.renormalize, wl.rsf, tokens=tokens, n_shared=wl.n_shared)
+
+
 def cpu_baseline(synth, torch, wl, seed, r, budget_s=15.0):
     """The oracle, as it stands, on a bounded sample of tokens of the first
     timed batch; weights copied from the device."""
     import numpy as np
     import oracle
-    n = synth.to_numpy_inputs({"w13": r["layer"].w13, "s13": r["layer"].s13,
-                               "w2": r["layer"].w2, "s2": r["layer"].s2,
-                               "bias": r["layer"].bias, "x": r["batches"][0][0],
-                               "logits": r["batches"][0][1]})
-    args = (n["x"], n["logits"], n["bias"], n["w13"], n["s13"], n["w2"], n["s2"],
-            wl.num_groups, wl.topk_group, wl.top_k, wl.scoring, wl.renormalize, wl.rsf)
+    L = r["layer"]
+    d = {"w13": L.w13, "s13": L.s13, "w2": L.w2, "s2": L.s2, "bias": L.bias,
+         "x": r["batches"][0][0], "logits": r["batches"][0][1]}
+    if wl.quant == "nvfp4":
+        d.update(g13=L.g13, g2=L.g2)
+    fwd = oracle_forward(oracle, synth, wl, synth.to_numpy_inputs(d))
     threads = oracle.get_threads()
-    fwd = oracle.forward_tokens_block if wl.quant == "block" else oracle.forward_tokens
     t = time.time()
-    fwd(*args, tokens=np.arange(min(threads, wl.T), dtype=np.int64), n_shared=wl.n_shared)
+    fwd(np.arange(min(threads, wl.T), dtype=np.int64))
     per_tok = (time.time() - t) / min(threads, wl.T)
     ntok = int(max(1, min(wl.T, budget_s / max(per_tok, 1e-6))))
     reps = max(1, int(budget_s / max(per_tok * ntok, 1e-6)))
     toks = np.tile(np.arange(ntok, dtype=np.int64), reps)
     t = time.time()
-    fwd(*args, tokens=toks, n_shared=wl.n_shared)
+    fwd(toks)
     dt = time.time() - t
     return {"value": round(toks.size / dt, 3), "unit": "tokens/s", "cores": threads,
             "kind": "oracle",
@@ -582,17 +649,17 @@ def run_ours(args):
         "metric": "MoE-layer tokens/s + % of FP8/HBM roofline, DeepSeek-V3 shape T=128/8192",
         "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": steps,
         "warmup": warmup, "ms_per_step": round(ms, 5), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "fp8_e4m3 x fp8_e4m3 -> fp32 (bf16 io)",
-        "data": "synthetic (seeded; weights ~N(0,0.02) quantised to e4m3 per channel)",
+        "scaling": "weak", "vs_baseline": None, "dtype": DTYPES[wl.quant],
+        "data": DATA[wl.quant],
         "config": workload_config(wl, world),
         "layer_bytes_gb": round(r["work"]["layer_bytes"] / 1e9, 3),
         "tflops": round(r["work"]["layer_flops"] / (r["ms"] * 1e-3) / 1e12, 2),
         "layer_hbm_gbs": round(r["work"]["layer_bytes"] / (r["ms"] * 1e-3) / 1e9, 1),
-        **(layer_fracs(r, pk, r["clocks"]) if wl.T > 512 else {}),
+        **(layer_fracs(r, pk, r["clocks"], tensor_ratio(wl)) if wl.T > 512 else {}),
         "active_experts": r["work"]["active"],
         "kernels_ms": {k: round(v, 4) for k, v in r["kern"].items()},
         "roofline": (roofline_decode(r, pk, wl.name) if wl.T <= 512
-                     else roofline_prefill(r, pk, r["clocks"])),
+                     else roofline_prefill(r, pk, r["clocks"], tensor_ratio(wl))),
         "e2e": {"value": round(job_tokens_per_s(wl.T, world, e2e_ms), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "graph": {"ms_per_step": round(graph_ms, 5),
@@ -620,9 +687,7 @@ def run_ours(args):
         torch.cuda.empty_cache()
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         d = synth.make_inputs(wl, seed=seed, device=dev, weights=True)
-        layer = moe.MoELayer(d["w13"], d["s13"], d["w2"], d["s2"], d["bias"], wl.num_groups,
-                             wl.topk_group, wl.top_k, wl.scoring, wl.renormalize, wl.rsf, wl.T,
-                             n_shared=wl.n_shared, quant=wl.quant)
+        layer = make_layer(moe, wl, d)
         line["cpu_baseline"] = cpu_baseline(synth, torch, wl, seed,
                                             {"layer": layer, "batches": make_batches(
                                                 wl, seed, dev, synth)})
@@ -653,13 +718,10 @@ def run_reference(args):
     d = synth.make_inputs(wl, seed=args.seed, device=dev, weights=True)
     n = synth.to_numpy_inputs(d)
     del d
-    fargs = (n["x"], n["logits"], n["bias"], n["w13"], n["s13"], n["w2"], n["s2"],
-             wl.num_groups, wl.topk_group, wl.top_k, wl.scoring, wl.renormalize, wl.rsf)
+    fwd = oracle_forward(oracle, synth, wl, n)
     threads = oracle.get_threads()
     t = time.time()
-    S = wl.n_shared
-    fwd = oracle.forward_tokens_block if wl.quant == "block" else oracle.forward_tokens
-    fwd(*fargs, tokens=np.arange(min(threads, wl.T), dtype=np.int64), n_shared=S)
+    fwd(np.arange(min(threads, wl.T), dtype=np.int64))
     per_tok = (time.time() - t) / min(threads, wl.T)
     # about 90 s for the whole run (warm-up included), at least one token per
     # oracle thread per step
@@ -667,10 +729,10 @@ def run_reference(args):
     ntok = int(max(min(threads, wl.T), min(wl.T, budget / max(per_tok, 1e-6))))
     toks = np.arange(ntok, dtype=np.int64)
     for _ in range(warmup):
-        fwd(*fargs, tokens=toks, n_shared=S)
+        fwd(toks)
     t = time.time()
     for _ in range(steps):
-        fwd(*fargs, tokens=toks, n_shared=S)
+        fwd(toks)
     dt = (time.time() - t) / steps
     value = ntok / dt
     sample = (f"{ntok} of the {wl.T} tokens of one {wl.name} batch per step, whole layer "
@@ -680,7 +742,7 @@ def run_reference(args):
         "metric": "MoE-layer tokens/s + % of FP8/HBM roofline, DeepSeek-V3 shape T=128/8192",
         "value": round(value, 3), "unit": "tokens/s", "n_gpus": args.gpus, "steps": steps,
         "warmup": warmup, "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f64 (FP8 codes decoded exactly)",
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64 (codes decoded exactly)",
         "data": "synthetic (seeded)",
         "config": workload_config(wl, args.gpus),
         "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": threads,

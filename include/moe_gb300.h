@@ -388,6 +388,77 @@ MOE_API moe_status moe_forward_block_host(const void* x_host,
                               void* ws, size_t ws_bytes, void* stream);
 
 /* ==========================================================================
+ * NVFP4: the FP4 format [P3] deploys DeepSeek-R1 in (modelopt_fp4; the
+ * pages name it without writing it out). Reading, from NVIDIA's published
+ * NVFP4 description: E2M1 elements (magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6),
+ * one E4M3 scale per 16 consecutive elements along K, one fp32 global scale
+ * per tensor; value = e2m1(q) * e4m3(s) * g. A 16-element block of x is
+ * quantised with s = e4m3((amax / 6) / g) and q = e2m1(x / (e4m3(s) * g))
+ * (IEEE fp32 divisions; nearest even, saturating; a block whose scale
+ * decodes to 0 gets zero codes). The activations' global scales (ga1 for x,
+ * ga2 for h) are inputs (calibrated input scales), as are the weights' g13[e]
+ * and g2[e].
+ * Packed layouts: codes two per byte along K, element 2j in the low nibble
+ * of byte j; scales one byte per 16 elements:
+ *   w13 [E,2I,H/2], s13 [E,2I,H/16], w2 [E,H,I/2], s2 [E,H,I/16] (bytes);
+ *   g13, g2 [E] f32. H % 256 == 0 and I % 256 == 0.
+ * The GEMMs run on the block-scaled tensor-core MMA
+ * (tcgen05.mma.kind::mxf4nvf4.block_scale, block 16, UE4M3 scales).
+ * ======================================================================== */
+
+/* moe_permute_quant in NVFP4 with global scale g > 0: a_q [T*K, H/2] packed
+ * E2M1, sf [T*K, H/16] E4M3 block scales; src2dst, offsets and the workspace
+ * as moe_permute_quant. Bit-exact. H % 16 == 0. */
+MOE_API moe_status moe_permute_quant_nvfp4(const void* x, const int32_t* topk_ids, int T,
+                                           int H, int E, int K, float g, void* a_q,
+                                           uint8_t* sf, int32_t* src2dst, int32_t* offsets,
+                                           void* ws, size_t ws_bytes, void* stream);
+
+/* NVFP4 requantisation of h [M,I] bf16 with global scale g > 0:
+ * q [M, I/2] packed E2M1, sf [M, I/16] E4M3. Bit-exact. I % 32 == 0. */
+MOE_API moe_status moe_act_quant_nvfp4(const void* h, int M, int I, float g, void* q,
+                                       uint8_t* sf, void* stream);
+
+/* moe_grouped_gemm in NVFP4: A [M, Kd/2] packed, sfa [M, Kd/16], ga (the
+ * activations' global scale); B [E, N, Kd/2] packed, sfb [E, N, Kd/16], gb
+ * [E] f32; acc[r,n] = sum_k a b sa sb (fp32), dequantised by ga * gb[e],
+ * then the epilogue (no row amax). Kd % 256 == 0, N % 128 == 0. */
+MOE_API moe_status moe_grouped_gemm_nvfp4(const void* A, const uint8_t* sfa, float ga,
+                                          const void* B, const uint8_t* sfb, const float* gb,
+                                          const int32_t* offsets, int M, int N, int Kd, int E,
+                                          int epilogue, void* C, void* stream);
+
+/* Workspace bytes of moe_forward_nvfp4 (with shared experts pass E+n_shared
+ * and top_k+n_shared). */
+MOE_API size_t moe_nvfp4_workspace_size(int T, int H, int I, int E, int K);
+
+/* The whole layer in NVFP4: gate, pre-reorder + NVFP4 quant (ga1), w13 GEMM
+ * + SiLU*mul, NVFP4 requant (ga2), w2 GEMM, weighted post-reorder; n_shared
+ * shared experts as in moe_forward_shared (0 for none). Weights and scales
+ * as above; otherwise as moe_forward_shared. */
+MOE_API moe_status moe_forward_nvfp4(const void* x, const float* logits, const float* bias,
+                                     const void* w13, const uint8_t* s13, const float* g13,
+                                     const void* w2, const uint8_t* s2, const float* g2,
+                                     float ga1, float ga2, int T, int H, int I, int E,
+                                     int n_shared, int num_groups, int topk_group, int top_k,
+                                     int scoring, int renormalize,
+                                     float routed_scaling_factor, void* out, void* ws,
+                                     size_t ws_bytes, void* stream);
+
+/* moe_forward_nvfp4 with x_host [T,H] bf16, logits_host [T,E] f32 and
+ * out_host [T,H] bf16 in host memory, copied through the workspace on
+ * `stream` (pinned memory keeps the copies asynchronous). */
+MOE_API moe_status moe_forward_nvfp4_host(const void* x_host, const float* logits_host,
+                                          const float* bias, const void* w13,
+                                          const uint8_t* s13, const float* g13,
+                                          const void* w2, const uint8_t* s2, const float* g2,
+                                          float ga1, float ga2, int T, int H, int I, int E,
+                                          int n_shared, int num_groups, int topk_group,
+                                          int top_k, int scoring, int renormalize,
+                                          float routed_scaling_factor, void* out_host,
+                                          void* ws, size_t ws_bytes, void* stream);
+
+/* ==========================================================================
  * Expert parallelism over R ranks: rank r holds experts [r*E/R, (r+1)*E/R)
  * (EPR = E/R of them) and its own tokens. [P3] Results deploys the layer
  * with --enable-ep-moe --ep-size 8 over 8 GPUs without describing the

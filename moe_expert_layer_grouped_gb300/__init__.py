@@ -21,6 +21,8 @@ __all__ = [
     "moe_grouped_gemm_block", "moe_act_quant_block", "moe_block_workspace_size",
     "moe_forward_block", "moe_forward_block_host", "moe_test_gemm_timeout",
     "moe_permute_quant_noalloc", "moe_permute_quant_rows", "moe_grouped_gemm_rows",
+    "moe_permute_quant_nvfp4", "moe_act_quant_nvfp4", "moe_grouped_gemm_nvfp4",
+    "moe_nvfp4_workspace_size", "moe_forward_nvfp4", "moe_forward_nvfp4_host",
     "moe_act_quant", "moe_unpermute_sum", "moe_workspace_size", "moe_forward",
     "moe_forward_host", "moe_device_status", "MoELayer",
     # expert parallelism (moe_expert_layer_grouped_gb300.ep)
@@ -91,6 +93,14 @@ _SIGNATURES = {
     "moe_device_status": (_I, [ctypes.POINTER(_I)]),
     "moe_permute_quant_rows": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_grouped_gemm_rows": (_I, [_P, _I, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P]),
+    "moe_permute_quant_nvfp4": (_I, [_P, _P, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_act_quant_nvfp4": (_I, [_P, _I, _I, _F, _P, _P, _P]),
+    "moe_grouped_gemm_nvfp4": (_I, [_P, _P, _F, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P]),
+    "moe_nvfp4_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
+    "moe_forward_nvfp4": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _F, _F, _I, _I, _I, _I, _I,
+                               _I, _I, _I, _I, _I, _F, _P, _P, _SZ, _P]),
+    "moe_forward_nvfp4_host": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _F, _F, _I, _I, _I, _I,
+                                    _I, _I, _I, _I, _I, _I, _F, _P, _P, _SZ, _P]),
     "moe_ep_table_size": (_SZ, [_I, _I]),
     "moe_ep_dispatch": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_ep_recv_reorder": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P]),
@@ -498,6 +508,107 @@ def moe_forward_block_host(x_host, logits_host, bias, w13, s13, w2, s2, n_shared
     return out_host
 
 
+# ---- NVFP4 (E2M1 codes two per byte, E4M3 scale per 16 along K, fp32 global)
+def moe_permute_quant_nvfp4(x, topk_ids, E, g, workspace=None, stream=None):
+    """Pre-reorder with NVFP4 quantisation (global scale g). Returns (a_q
+    [T*K, H/2] packed, sf [T*K, H/16], src2dst, offsets)."""
+    import torch
+    _need_cuda(x, topk_ids, workspace)
+    T, H = x.shape
+    K = topk_ids.shape[1]
+    dev = x.device
+    M = T * K
+    a_q = torch.empty((M, H // 2), dtype=torch.uint8, device=dev)
+    sf = torch.empty((M, H // 16), dtype=torch.uint8, device=dev)
+    src2dst = torch.empty(M, dtype=torch.int32, device=dev)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    if workspace is None:
+        workspace = torch.empty(max(moe_permute_workspace_size(T, E, K), 256), dtype=torch.uint8,
+                                device=dev)
+    _check("moe_permute_quant_nvfp4", load().moe_permute_quant_nvfp4(
+        _ptr(x), _ptr(topk_ids), T, H, E, K, float(g), _ptr(a_q), _ptr(sf), _ptr(src2dst),
+        _ptr(offsets), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream)))
+    return a_q, sf, src2dst, offsets
+
+
+def moe_act_quant_nvfp4(h, g, stream=None):
+    """NVFP4 requantisation of h [M, I] bf16: (q [M, I/2] packed, sf [M, I/16])."""
+    import torch
+    _need_cuda(h)
+    M, I = h.shape
+    q = torch.empty((M, I // 2), dtype=torch.uint8, device=h.device)
+    sf = torch.empty((M, I // 16), dtype=torch.uint8, device=h.device)
+    _check("moe_act_quant_nvfp4", load().moe_act_quant_nvfp4(
+        _ptr(h), M, I, float(g), _ptr(q), _ptr(sf), _stream(stream)))
+    return q, sf
+
+
+def moe_grouped_gemm_nvfp4(A, sfa, ga, B, sfb, gb, offsets, epilogue=EPI_BF16, C=None,
+                           stream=None):
+    """A [M, Kd/2] packed, sfa [M, Kd/16]; B [E, N, Kd/2] packed, sfb [E, N, Kd/16],
+    gb [E]; ga a float."""
+    import torch
+    _need_cuda(A, sfa, B, sfb, gb, offsets, C)
+    M = A.shape[0]
+    E, N, kb = B.shape
+    Kd = 2 * kb
+    if C is None:
+        cols = N // 2 if epilogue == EPI_SILU_MUL else N
+        C = torch.empty((M, cols), dtype=torch.bfloat16, device=A.device)
+    _check("moe_grouped_gemm_nvfp4", load().moe_grouped_gemm_nvfp4(
+        _ptr(A), _ptr(sfa), float(ga), _ptr(B), _ptr(sfb), _ptr(gb), _ptr(offsets), M, N, Kd, E,
+        epilogue, _ptr(C), _stream(stream)))
+    return C
+
+
+def moe_nvfp4_workspace_size(T, H, I, E, K):
+    return load().moe_nvfp4_workspace_size(T, H, I, E, K)
+
+
+def moe_forward_nvfp4(x, logits, bias, w13, s13, g13, w2, s2, g2, ga1, ga2, n_shared,
+                      num_groups, topk_group, top_k, scoring=SIGMOID, renormalize=True,
+                      routed_scaling_factor=1.0, out=None, workspace=None, stream=None):
+    """The layer in NVFP4: w13 [E+S, 2I, H/2], s13 [E+S, 2I, H/16], g13 [E+S];
+    w2 [E+S, H, I/2], s2 [E+S, H, I/16], g2 [E+S]; ga1, ga2 floats."""
+    import torch
+    _need_cuda(x, logits, bias, w13, s13, g13, w2, s2, g2, out, workspace)
+    T, H = x.shape
+    E = logits.shape[1]
+    I = w2.shape[2] * 2
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=x.device) if out is None else out
+    if workspace is None:
+        nws = moe_nvfp4_workspace_size(T, H, I, E + n_shared, top_k + n_shared)
+        workspace = torch.empty(nws, dtype=torch.uint8, device=x.device)
+    _check("moe_forward_nvfp4", load().moe_forward_nvfp4(
+        _ptr(x), _ptr(logits), _ptr(bias), _ptr(w13), _ptr(s13), _ptr(g13), _ptr(w2), _ptr(s2),
+        _ptr(g2), float(ga1), float(ga2), T, H, I, E, int(n_shared), num_groups, topk_group,
+        top_k, scoring, int(bool(renormalize)), float(routed_scaling_factor), _ptr(out),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out
+
+
+def moe_forward_nvfp4_host(x_host, logits_host, bias, w13, s13, g13, w2, s2, g2, ga1, ga2,
+                           n_shared, num_groups, topk_group, top_k, scoring, renormalize,
+                           routed_scaling_factor, out_host, workspace, stream=None):
+    """moe_forward_nvfp4 with x, logits and out in host memory."""
+    _need_cuda(bias, w13, s13, g13, w2, s2, g2, workspace)
+    for t in (x_host, logits_host, out_host):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError("moe_forward_nvfp4_host: x, logits and out must be contiguous "
+                             "host tensors")
+    T, H = x_host.shape
+    E = logits_host.shape[1]
+    I = w2.shape[2] * 2
+    _check("moe_forward_nvfp4_host", load().moe_forward_nvfp4_host(
+        _ptr(x_host), _ptr(logits_host), _ptr(bias), _ptr(w13), _ptr(s13), _ptr(g13), _ptr(w2),
+        _ptr(s2), _ptr(g2), float(ga1), float(ga2), T, H, I, E, int(n_shared), num_groups,
+        topk_group, top_k, scoring, int(bool(renormalize)), float(routed_scaling_factor),
+        _ptr(out_host), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream)))
+    return out_host
+
+
 def moe_test_gemm_timeout(A, scale_a, B, scale_b, offsets, epilogue, C, stall_stage,
                           stream=None):
     """Failure-detection test: one pipeline stage of CTA 0 never receives its
@@ -528,26 +639,41 @@ class MoELayer:
     quant="block")."""
 
     def __init__(self, w13, s13, w2, s2, bias, num_groups, topk_group, top_k, scoring,
-                 renormalize, routed_scaling_factor, max_tokens, n_shared=0, quant="token"):
+                 renormalize, routed_scaling_factor, max_tokens, n_shared=0, quant="token",
+                 nvfp4=None):
+        """quant="nvfp4": w13/w2 hold packed E2M1 codes and s13/s2 E4M3 block
+        scales; nvfp4 = dict(g13=..., g2=..., ga1=..., ga2=...) the global
+        scales."""
         import torch
-        if quant not in ("token", "block"):
-            raise ValueError("MoELayer: quant is 'token' or 'block'")
+        if quant not in ("token", "block", "nvfp4"):
+            raise ValueError("MoELayer: quant is 'token', 'block' or 'nvfp4'")
         self.quant = quant
         self.w13, self.s13, self.w2, self.s2, self.bias = w13, s13, w2, s2, bias
         EA, I2, self.H = w13.shape
+        if quant == "nvfp4":
+            self.H *= 2  # two codes per byte
+            self.g13, self.g2 = nvfp4["g13"], nvfp4["g2"]
+            self.ga1, self.ga2 = float(nvfp4["ga1"]), float(nvfp4["ga2"])
         self.n_shared = n_shared
         self.E = EA - n_shared  # routed experts
         self.I = I2 // 2
         self.num_groups, self.topk_group, self.top_k = num_groups, topk_group, top_k
         self.scoring, self.renormalize, self.rsf = scoring, renormalize, routed_scaling_factor
         self.max_tokens = max_tokens
-        size = moe_block_workspace_size if quant == "block" else moe_workspace_size
+        size = {"block": moe_block_workspace_size, "nvfp4": moe_nvfp4_workspace_size}.get(
+            quant, moe_workspace_size)
         self.workspace = torch.empty(size(max_tokens, self.H, self.I, EA, top_k + n_shared),
                                      dtype=torch.uint8, device=w13.device)
 
     def __call__(self, x, logits, out=None, stream=None):
         if x.shape[0] > self.max_tokens:
             raise ValueError("MoELayer: more tokens than the workspace was sized for")
+        if self.quant == "nvfp4":
+            return moe_forward_nvfp4(x, logits, self.bias, self.w13, self.s13, self.g13, self.w2,
+                                     self.s2, self.g2, self.ga1, self.ga2, self.n_shared,
+                                     self.num_groups, self.topk_group, self.top_k, self.scoring,
+                                     self.renormalize, self.rsf, out=out,
+                                     workspace=self.workspace, stream=stream)
         if self.quant == "block":
             return moe_forward_block(x, logits, self.bias, self.w13, self.s13, self.w2, self.s2,
                                      self.n_shared, self.num_groups, self.topk_group,
@@ -583,6 +709,13 @@ class MoELayer:
         return g
 
     def forward_host(self, x_host, logits_host, out_host, stream=None):
+        if self.quant == "nvfp4":
+            return moe_forward_nvfp4_host(x_host, logits_host, self.bias, self.w13, self.s13,
+                                          self.g13, self.w2, self.s2, self.g2, self.ga1,
+                                          self.ga2, self.n_shared, self.num_groups,
+                                          self.topk_group, self.top_k, self.scoring,
+                                          self.renormalize, self.rsf, out_host,
+                                          self.workspace, stream=stream)
         if self.quant == "block":
             return moe_forward_block_host(x_host, logits_host, self.bias, self.w13, self.s13,
                                           self.w2, self.s2, self.n_shared, self.num_groups,

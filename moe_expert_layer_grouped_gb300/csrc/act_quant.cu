@@ -89,7 +89,57 @@ __global__ void __launch_bounds__(kWarps * 32)
   }
 }
 
+// NVFP4 requantisation of h with the global scale g: q [M, I/2] (two E2M1
+// codes per byte), sf [M, I/16] E4M3 block scales. One warp per row; a
+// 16-channel block is the 8-value vectors of lanes 2i and 2i+1.
+__global__ void __launch_bounds__(kWarps * 32)
+    act_quant_nvfp4_kernel(const __nv_bfloat16* __restrict__ h, int M, int I, float g,
+                           uint8_t* __restrict__ q, uint8_t* __restrict__ sf) {
+  chain_entry();
+  constexpr int U = 4;  // vectors per lane in flight
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t row = (int64_t)blockIdx.x * kWarps + warp;
+  if (row >= M) return;  // warp-uniform
+  const int nvec = I >> 3;
+  const uint4* hr = reinterpret_cast<const uint4*>(h + row * I);
+  uint32_t* qr = reinterpret_cast<uint32_t*>(q + row * (I >> 1));
+  uint8_t* sr = sf + row * (I >> 4);
+  for (int v0 = 0; v0 < nvec; v0 += 32 * U) {
+    uint4 raw[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int i = v0 + u * 32 + lane;
+      if (i < nvec) raw[u] = __ldg(hr + i);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int i = v0 + u * 32 + lane;
+      float f[8];
+      float m = 0.0f;
+      if (i < nvec) {
+        bf16x8_to_f32(raw[u], f);
+        m = absmax8(f, 0.0f);
+      }
+      m = fmaxf(m, __shfl_xor_sync(kFull, m, 1));
+      if (i < nvec) {
+        const uint32_t code = nvfp4_scale_code(m, g);
+        qr[i] = nvfp4_codes8(f, __fmul_rn(e4m3_value(code), g));
+        if ((i & 1) == 0) sr[i >> 1] = (uint8_t)code;
+      }
+    }
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_act_quant_nvfp4(const void* h, int M, int I, float g, void* q, uint8_t* sf,
+                                   cudaStream_t st, bool pdl) {
+  if (M == 0) return cudaSuccess;
+  const int blocks = (M + kWarps - 1) / kWarps;
+  return launch_kernel(act_quant_nvfp4_kernel, dim3(blocks), dim3(kWarps * 32), 0, st, pdl,
+                       reinterpret_cast<const __nv_bfloat16*>(h), M, I, g,
+                       reinterpret_cast<uint8_t*>(q), sf);
+}
 
 cudaError_t launch_act_quant_block(const void* h, int M, int I, void* q, float* scale,
                                    cudaStream_t st, bool pdl) {

@@ -571,6 +571,202 @@ moe_status moe_forward_block_host(const void* x_host, const float* logits_host,
                       routed_scaling_factor, out_host, ws, ws_bytes, stream, true);
 }
 
+// ---- NVFP4 -----------------------------------------------------------------------
+namespace {
+
+bool nvfp4_dims_ok(int K) { return K >= 256 && K % 256 == 0; }
+
+// moe_forward_nvfp4's workspace, 256-byte aligned pieces.
+struct Fp4Layout {
+  size_t ids, w, perm, offsets, s2d, a_q, sfa, h, q2, sfa2, down, x_in, logits_in, out, total;
+};
+
+Fp4Layout fp4_layout(int T, int H, int I, int E, int K) {
+  Fp4Layout L;
+  const size_t M = (size_t)T * K;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o += align_up(bytes > 0 ? bytes : 1);
+    return at;
+  };
+  L.ids = take(M * 4);
+  L.w = take(M * 4);
+  L.perm = take(permute_ws_bytes(T, E));
+  L.offsets = take((size_t)(E + 1) * 4);
+  L.s2d = take(M * 4);
+  L.a_q = take(M * (size_t)H / 2);
+  L.sfa = take(M * (size_t)H / 16);
+  L.h = take(M * (size_t)I * 2);
+  L.q2 = take(M * (size_t)I / 2);
+  L.sfa2 = take(M * (size_t)I / 16);
+  L.down = take(M * (size_t)H * 2);
+  L.x_in = take((size_t)T * H * 2);
+  L.logits_in = take((size_t)T * E * 4);
+  L.out = take((size_t)T * H * 2);
+  L.total = o;
+  return L;
+}
+
+moe_status check_gemm_nvfp4(const void* A, const void* sfa, float ga, const void* B,
+                            const void* sfb, const float* gb, const int32_t* offsets, int M,
+                            int N, int Kd, int E, int epi, const void* C) {
+  if (M < 0 || N < 1 || Kd < 1 || E < 1) return MOE_ERR_INVALID_ARG;
+  if (epi != MOE_EPI_BF16 && epi != MOE_EPI_SILU_MUL) return MOE_ERR_INVALID_ARG;
+  if (!nvfp4_dims_ok(Kd) || N % 128 != 0) return MOE_ERR_INVALID_ARG;
+  if (!(ga > 0.0f)) return MOE_ERR_INVALID_ARG;
+  if (E > kMaxE) return MOE_ERR_UNSUPPORTED;
+  if ((int64_t)E * N >= ((int64_t)1 << 31) || (int64_t)M >= ((int64_t)1 << 31))
+    return MOE_ERR_UNSUPPORTED;
+  if (!ok_ptr(offsets) || !ok_ptr(B) || !ok_ptr(sfb) || !ok_ptr(gb)) return MOE_ERR_INVALID_ARG;
+  if (M > 0 && (!ok_ptr(A) || !ok_ptr(sfa) || !ok_ptr(C))) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+moe_status run_forward_nvfp4(const void* x, const float* logits, const float* bias,
+                             const void* w13, const uint8_t* s13, const float* g13,
+                             const void* w2, const uint8_t* s2, const float* g2, float ga1,
+                             float ga2, int T, int H, int I, int E, int S, int G, int TG, int K,
+                             int scoring, int renorm, float rsf, void* out, void* ws,
+                             cudaStream_t st) {
+  const int EA = E + S, KA = K + S;
+  const Fp4Layout L = fp4_layout(T, H, I, EA, KA);
+  int* err = device_error_word();
+  if (err == nullptr) return MOE_ERR_CUDA;
+  const int M = T * KA;
+  int32_t* ids = at<int32_t>(ws, L.ids);
+  float* w = at<float>(ws, L.w);
+  int32_t* offsets = at<int32_t>(ws, L.offsets);
+  int32_t* s2d = at<int32_t>(ws, L.s2d);
+  void* a_q = at<void>(ws, L.a_q);
+  uint8_t* sfa = at<uint8_t>(ws, L.sfa);
+  void* h = at<void>(ws, L.h);
+  void* q2 = at<void>(ws, L.q2);
+  uint8_t* sfa2 = at<uint8_t>(ws, L.sfa2);
+  void* down = at<void>(ws, L.down);
+  cudaError_t e;
+  constexpr bool kChain = true;
+  if ((e = launch_gate(logits, bias, T, E, G, TG, K, scoring, renorm, rsf, ids, w, S, st)))
+    return cuda_status(e);
+  if ((e = launch_permute_quant_nvfp4(x, ids, T, H, EA, KA, ga1, a_q, sfa, s2d, offsets,
+                                      at<void>(ws, L.perm), err, st, kChain)))
+    return cuda_status(e);
+  if ((e = launch_grouped_gemm_nvfp4(a_q, sfa, ga1, w13, s13, g13, offsets, M, 2 * I, H, EA,
+                                     MOE_EPI_SILU_MUL, h, err, st, kChain)))
+    return cuda_status(e);
+  if ((e = launch_act_quant_nvfp4(h, M, I, ga2, q2, sfa2, st, kChain))) return cuda_status(e);
+  if ((e = launch_grouped_gemm_nvfp4(q2, sfa2, ga2, w2, s2, g2, offsets, M, H, I, EA,
+                                     MOE_EPI_BF16, down, err, st, kChain, /*early_table=*/true)))
+    return cuda_status(e);
+  if ((e = launch_unpermute_sum(down, s2d, w, T, KA, H, out, err, st, kChain)))
+    return cuda_status(e);
+  return MOE_OK;
+}
+
+}  // namespace
+
+moe_status moe_permute_quant_nvfp4(const void* x, const int32_t* topk_ids, int T, int H, int E,
+                                   int K, float g, void* a_q, uint8_t* sf, int32_t* src2dst,
+                                   int32_t* offsets, void* ws, size_t ws_bytes, void* stream) {
+  moe_status s = check_permute(x, topk_ids, T, H, E, K, a_q, reinterpret_cast<const float*>(sf),
+                               src2dst, offsets, ws, ws_bytes);
+  if (s != MOE_OK) return s;
+  if (H % 16 != 0 || !(g > 0.0f)) return MOE_ERR_INVALID_ARG;
+  int* err = device_error_word();
+  if (err == nullptr) return MOE_ERR_CUDA;
+  return cuda_status(launch_permute_quant_nvfp4(x, topk_ids, T, H, E, K, g, a_q, sf, src2dst,
+                                                offsets, ws, err,
+                                                static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_act_quant_nvfp4(const void* h, int M, int I, float g, void* q, uint8_t* sf,
+                               void* stream) {
+  if (M < 0 || I < 1 || I % 32 != 0 || !(g > 0.0f)) return MOE_ERR_INVALID_ARG;
+  if (M > 0 && (!ok_ptr(h) || !ok_ptr(q) || !ok_ptr(sf))) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_act_quant_nvfp4(h, M, I, g, q, sf, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_grouped_gemm_nvfp4(const void* A, const uint8_t* sfa, float ga, const void* B,
+                                  const uint8_t* sfb, const float* gb, const int32_t* offsets,
+                                  int M, int N, int Kd, int E, int epilogue, void* C,
+                                  void* stream) {
+  moe_status s = check_gemm_nvfp4(A, sfa, ga, B, sfb, gb, offsets, M, N, Kd, E, epilogue, C);
+  if (s != MOE_OK) return s;
+  int* err = device_error_word();
+  if (err == nullptr) return MOE_ERR_CUDA;
+  return cuda_status(launch_grouped_gemm_nvfp4(A, sfa, ga, B, sfb, gb, offsets, M, N, Kd, E,
+                                               epilogue, C, err,
+                                               static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_forward_nvfp4_host(const void* x_host, const float* logits_host,
+                                  const float* bias, const void* w13, const uint8_t* s13,
+                                  const float* g13, const void* w2, const uint8_t* s2,
+                                  const float* g2, float ga1, float ga2, int T, int H, int I,
+                                  int E, int n_shared, int num_groups, int topk_group,
+                                  int top_k, int scoring, int renormalize,
+                                  float routed_scaling_factor, void* out_host, void* ws,
+                                  size_t ws_bytes, void* stream) {
+  if (T > 0 && (x_host == nullptr || logits_host == nullptr || out_host == nullptr))
+    return MOE_ERR_INVALID_ARG;
+  if (ws == nullptr) return MOE_ERR_WORKSPACE;
+  if (T < 0 || H < 1 || I < 1 || E < 1 || top_k < 1 || n_shared < 0) return MOE_ERR_INVALID_ARG;
+  const Fp4Layout L = fp4_layout(T, H, I, E + n_shared, top_k + n_shared);
+  void* x_d = at<void>(ws, L.x_in);
+  float* l_d = at<float>(ws, L.logits_in);
+  void* o_d = at<void>(ws, L.out);
+  // the device entry point's checks, on the staging buffers
+  moe_status s = moe_forward_nvfp4(x_d, l_d, bias, w13, s13, g13, w2, s2, g2, ga1, ga2, 0, H, I,
+                                   E, n_shared, num_groups, topk_group, top_k, scoring,
+                                   renormalize, routed_scaling_factor, o_d, ws, ws_bytes,
+                                   stream);
+  if (s != MOE_OK || T == 0) return s;
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t xb = (size_t)T * H * 2, lb = (size_t)T * E * 4;
+  if (cudaMemcpyAsync(x_d, x_host, xb, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+      cudaMemcpyAsync(l_d, logits_host, lb, cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  s = run_forward_nvfp4(x_d, l_d, bias, w13, s13, g13, w2, s2, g2, ga1, ga2, T, H, I, E,
+                        n_shared, num_groups, topk_group, top_k, scoring, renormalize,
+                        routed_scaling_factor, o_d, ws, st);
+  if (s != MOE_OK) return s;
+  if (cudaMemcpyAsync(out_host, o_d, xb, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+size_t moe_nvfp4_workspace_size(int T, int H, int I, int E, int K) {
+  if (T < 0 || H < 1 || I < 1 || E < 1 || K < 1) return 0;
+  return fp4_layout(T, H, I, E, K).total;
+}
+
+moe_status moe_forward_nvfp4(const void* x, const float* logits, const float* bias,
+                             const void* w13, const uint8_t* s13, const float* g13,
+                             const void* w2, const uint8_t* s2, const float* g2, float ga1,
+                             float ga2, int T, int H, int I, int E, int n_shared,
+                             int num_groups, int topk_group, int top_k, int scoring,
+                             int renormalize, float routed_scaling_factor, void* out, void* ws,
+                             size_t ws_bytes, void* stream) {
+  if (!nvfp4_dims_ok(H) || !nvfp4_dims_ok(I)) return MOE_ERR_INVALID_ARG;
+  if (!(ga1 > 0.0f) || !(ga2 > 0.0f)) return MOE_ERR_INVALID_ARG;
+  if (!ok_ptr(g13) || !ok_ptr(g2)) return MOE_ERR_INVALID_ARG;
+  // the per-token layer's checks (shapes, gate, pointers), then this layer's
+  // workspace
+  moe_status s = check_forward(x, logits, bias, w13, reinterpret_cast<const float*>(s13), w2,
+                               reinterpret_cast<const float*>(s2), T, H, I, E, n_shared,
+                               num_groups, topk_group, top_k, scoring, out, ws, (size_t)-1,
+                               false);
+  if (s != MOE_OK) return s;
+  if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0 ||
+      ws_bytes < fp4_layout(T, H, I, E + n_shared, top_k + n_shared).total)
+    return MOE_ERR_WORKSPACE;
+  if (T == 0) return MOE_OK;
+  return run_forward_nvfp4(x, logits, bias, w13, s13, g13, w2, s2, g2, ga1, ga2, T, H, I, E,
+                           n_shared, num_groups, topk_group, top_k, scoring, renormalize,
+                           routed_scaling_factor, out, ws, static_cast<cudaStream_t>(stream));
+}
+
 // ---- expert-parallel dispatch / combine ---------------------------------------
 size_t moe_ep_table_size(int R, int EPR) {
   if (R < 1 || EPR < 1) return 0;

@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp4.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -95,6 +96,38 @@ __device__ __forceinline__ float absmax8(const float (&f)[8], float m) {
 #pragma unroll
   for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(f[i]));
   return m;
+}
+
+// ---- NVFP4 (E2M1 elements, one E4M3 scale per 16 along K, fp32 global
+// scale g) ------------------------------------------------------------------
+
+// Exact value of an e4m3 code (every e4m3 value is an fp16 value).
+__device__ __forceinline__ float e4m3_value(uint32_t code) {
+  const __half_raw h = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)code, __NV_E4M3);
+  return __half2float(__half(h));
+}
+
+// Block scale of 16 values with largest magnitude amax: the e4m3 code of
+// (amax / 6) / g (IEEE divisions, round to nearest even, saturating).
+__device__ __forceinline__ uint32_t nvfp4_scale_code(float amax, float g) {
+  const float s = __fdiv_rn(__fdiv_rn(amax, 6.0f), g);
+  return e4m3x2(s, 0.0f) & 0xFFu;
+}
+
+// 8 values -> 8 E2M1 codes x / step (IEEE division, nearest even,
+// saturating to +-6), element 2j in the low nibble of byte j; all zero when
+// step is 0.
+__device__ __forceinline__ uint32_t nvfp4_codes8(const float (&f)[8], float step) {
+  if (!(step > 0.0f)) return 0u;
+  uint32_t r = 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const __nv_fp4x2_storage_t b = __nv_cvt_float2_to_fp4x2(
+        make_float2(__fdiv_rn(f[2 * j], step), __fdiv_rn(f[2 * j + 1], step)), __NV_E2M1,
+        cudaRoundNearest);
+    r |= (uint32_t)b << (8 * j);
+  }
+  return r;
 }
 
 }  // namespace moe

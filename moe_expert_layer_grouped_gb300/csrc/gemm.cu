@@ -633,16 +633,18 @@ namespace {
 // outside the tensor). Encoded maps are cached by (address, shape, strides,
 // box, device) so repeated calls on the same buffers skip the driver.
 bool encode_u8(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims,
-               const cuuint64_t* strides, const cuuint32_t* box) {
+               const cuuint64_t* strides, const cuuint32_t* box,
+               CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   struct Entry {
     const void* base;
-    int rank, dev;
+    int rank, dev, swizzle;
     cuuint64_t dims[5], strides[4];
     cuuint32_t box[5];
     CUtensorMap map;
   };
   auto same = [&](const Entry& c, int dev) {
-    if (c.base != base || c.rank != rank || c.dev != dev) return false;
+    if (c.base != base || c.rank != rank || c.dev != dev || c.swizzle != (int)swizzle)
+      return false;
     for (int i = 0; i < rank; ++i)
       if (c.dims[i] != dims[i] || c.box[i] != box[i] || (i + 1 < rank && c.strides[i] != strides[i]))
         return false;
@@ -665,13 +667,14 @@ bool encode_u8(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dim
   if (fn == nullptr) return false;
   const cuuint32_t es[5] = {1, 1, 1, 1, 1};
   if (fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, (cuuint32_t)rank, const_cast<void*>(base), dims,
-         strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+         strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return false;
   Entry e = {};
   e.base = base;
   e.rank = rank;
   e.dev = dev;
+  e.swizzle = (int)swizzle;
   for (int i = 0; i < rank; ++i) {
     e.dims[i] = dims[i];
     e.box[i] = box[i];
@@ -692,6 +695,29 @@ bool make_tma_map_u8(CUtensorMap* m, const void* base, uint64_t rows, uint64_t c
   const cuuint64_t strides[1] = {cols};
   const cuuint32_t box[2] = {BK, box_rows};
   return encode_u8(m, base, 2, dims, strides, box);
+}
+
+bool make_tma_map_scales(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
+                         uint32_t box_rows) {
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols};
+  const cuuint32_t box[2] = {16, box_rows};
+  return encode_u8(m, base, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+bool make_tma_map_weight_scales(CUtensorMap* m, const void* base, bool silu, uint64_t E,
+                                uint64_t N, uint64_t cols) {
+  if (silu) {  // [E][2][I][cols]: 64 gate rows, then the matching 64 up rows
+    const uint64_t I = N / 2;
+    const cuuint64_t dims[4] = {cols, I, 2, E};
+    const cuuint64_t strides[3] = {cols, I * cols, 2 * I * cols};
+    const cuuint32_t box[4] = {16, 64, 2, 1};
+    return encode_u8(m, base, 4, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+  }
+  const cuuint64_t dims[2] = {cols, E * N};
+  const cuuint64_t strides[1] = {cols};
+  const cuuint32_t box[2] = {16, BM};
+  return encode_u8(m, base, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 bool make_tma_map_rows(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols) {

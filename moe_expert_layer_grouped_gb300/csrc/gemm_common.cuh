@@ -162,6 +162,15 @@ bool make_tma_map_u8(CUtensorMap* m, const void* base, uint64_t rows, uint64_t c
 // swizzle, zero fill) for four-row gathers.
 bool make_tma_map_rows(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols);
 
+// Host: block-scale maps (no swizzle, boxes 16 bytes wide): a [rows, cols]
+// byte tensor with box_rows rows per box, and the weights' [E, N, cols]
+// scales with 128-row boxes (silu: 64 gate rows then the matching 64 up
+// rows, as the weight tile).
+bool make_tma_map_scales(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
+                         uint32_t box_rows);
+bool make_tma_map_weight_scales(CUtensorMap* m, const void* base, bool silu, uint64_t E,
+                                uint64_t N, uint64_t cols);
+
 // Host: the weight map of a [E, N, Kd] tensor (see Maps::w): boxes of `kc`
 // K chunks when Kd % 128 == 0 (weights_stage_box), else of one chunk;
 // `silu`: the gate/up view of w13 (N = 2I).

@@ -1,0 +1,459 @@
+// The grouped GEMM in NVFP4, the FP4 format the pages deploy DeepSeek-R1 in
+// ("[1/2] sgl-kernel: Fuse routed scaling factor into select_experts",
+// sglang #8364, Motivation and Highlights: modelopt_fp4,
+// ModelOptNvFp4FusedMoEMethod): E2M1 elements, one E4M3 scale per 16
+// elements along K for every row of both operands, one fp32 global scale per
+// tensor (ga for the activations, gb[e] per expert for the weights).
+//   C[r,n] = ga * gb[e] * sum_k a[r,k] sa[r,k/16] * b[e,n,k] sb[e,n,k/16]
+// with the block-scaled 5th-generation tensor-core MMA
+// (tcgen05.mma.kind::mxf4nvf4.block_scale.scale_vec::4X, K = 64 per
+// instruction) and the same epilogues as the FP8 kernel (bf16 out, or
+// SiLU(gate)*up with gate rows [j0, j0+64) and up rows [I+j0, I+j0+64) in one
+// 128-row tile).
+//
+// Layouts: A [M, Kd/2] and B [E, N, Kd/2] bytes, two E2M1 codes per byte
+// (element 2j in the low nibble), K-major; sa [M, Kd/16], sb [E, N, Kd/16]
+// E4M3 codes. Kd % 256 == 0, so a 128-byte K chunk (256 elements) is whole.
+//
+// Design (one persistent CTA per SM, 192 threads, single-CTA MMAs):
+//   warp 0      TMA producer, one K chunk per stage: the tile's 128 weight
+//               rows (one box), their 128 x 16 scale bytes, the token rows
+//               (64/32/16-row boxes) and their scale bytes.
+//   warp 1      scales + MMA: the whole warp rearranges the stage's scale
+//               bytes (row-major as loaded) into the 32-row x 16-byte blocks
+//               tcgen05.cp copies to tensor memory (block j: bytes of row
+//               m0 + 32*m1 at offset 16*m0 + 4*m1, the four scales of MMA
+//               step j), fences them for the async proxy, and lane 0 copies
+//               them (tcgen05.cp.32x128b.warpx4) and issues the four MMAs of
+//               the chunk, each reading its scales from four columns.
+//   warps 2..5  epilogue as in the FP8 kernel, dequantising by ga * gb[e].
+// Tensor memory: two accumulators of 128 columns (token tiles <= 128), then
+// per pipeline stage 16 columns of weight scales and 16 of token scales,
+// released with the stage.
+// Every pipeline wait is bounded (2 s); on timeout the CTA sets the device
+// error word, lets its in-flight copies and MMAs land, frees its tensor
+// memory and exits.
+#include <cuda.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+#include "gemm_common.cuh"
+#include "ptx.cuh"
+
+namespace moe {
+namespace {
+
+using namespace gemm_common;
+
+constexpr int FT = 192;
+constexpr int FBN = 128;       // tokens per tile (MMA N)
+constexpr int FSTAGES = 4;
+constexpr int SFROW = 16;      // scale bytes per row per 128-byte K chunk
+constexpr uint32_t F_ACC = 128;                     // TMEM columns per accumulator
+constexpr uint32_t F_SF0 = 2 * F_ACC;               // first scale column
+constexpr uint32_t F_SFSTAGE = 32;                  // scale columns per stage
+constexpr uint32_t F_TMEM = 512;
+static_assert(F_SF0 + FSTAGES * F_SFSTAGE <= F_TMEM, "tensor memory budget");
+
+struct FMaps {
+  CUtensorMap w;          // weights, one 128-byte chunk of 128 rows per box
+  CUtensorMap x[NXBOX];   // token rows, boxes of 64 >> i rows
+  CUtensorMap sw;         // weight scales, 16 bytes x 128 rows per box
+  CUtensorMap sx[NXBOX];  // token scales, 16 bytes x (64 >> i) rows
+};
+
+template <bool SILU>
+struct FSmem {
+  uint8_t w[FSTAGES][W_BYTES];
+  uint8_t x[FSTAGES][FBN * BK];
+  uint8_t sw[FSTAGES][BM * SFROW];    // row-major, as loaded
+  uint8_t sx[FSTAGES][FBN * SFROW];
+  uint32_t atom_a[FSTAGES][4][128];   // tcgen05.cp sources, one per MMA K step
+  uint32_t atom_b[FSTAGES][4][128];
+  float xchg[SILU ? 2 : 1][2][32 * 32];
+  uint16_t stage_out[4][32 * 32];
+  uint64_t full[FSTAGES];
+  uint64_t empty[FSTAGES];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+  int total_tiles;
+  int never;
+  int thr_sum[FT];
+  int tile_start[MAX_E + 1];
+  int offs[MAX_E + 1];
+};
+
+struct FParams {
+  float ga;
+  const float* gb;
+  const int32_t* offsets;
+  void* C;
+  int* err;
+  int M, N, Kd, E, I, NB, KB;
+  int stream_weights;
+  int early_table;
+};
+
+// Scale bytes of 128 rows x 16 (row-major, 4 words a row) -> four blocks of
+// 32 rows x 16 bytes: block j, word 4*m0 + m1 = word j of row m0 + 32*m1.
+__device__ __forceinline__ void arrange_scales(const uint32_t* raw, uint32_t (*atom)[128],
+                                               int lane) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int w = lane + 32 * i;            // word 4*m0 + m1 of each block
+    const int row = (w & 3) * 32 + (w >> 2);
+    const uint4 r = *reinterpret_cast<const uint4*>(raw + row * 4);
+    atom[0][w] = r.x;
+    atom[1][w] = r.y;
+    atom[2][w] = r.z;
+    atom[3][w] = r.w;
+  }
+}
+
+template <bool SILU>
+__global__ void __launch_bounds__(FT, 1)
+    grouped_gemm_nvfp4_kernel(const __grid_constant__ FMaps maps, const FParams p) {
+  using S = FSmem<SILU>;
+  extern __shared__ uint8_t smem_raw[];
+  S& sm = *reinterpret_cast<S*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                ~static_cast<uintptr_t>(1023));
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int E = p.E;
+  const int KS = p.KB;  // one K chunk per stage
+
+  if (warp == 0 && lane == 0) {
+    ptx::prefetch_tensormap(&maps.w);
+    ptx::prefetch_tensormap(&maps.sw);
+    for (int i = 0; i < NXBOX; ++i) {
+      ptx::prefetch_tensormap(&maps.x[i]);
+      ptx::prefetch_tensormap(&maps.sx[i]);
+    }
+    for (int s = 0; s < FSTAGES; ++s) {
+      ptx::mbar_init(&sm.full[s], 1);
+      ptx::mbar_init(&sm.empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(&sm.tfull[b], 1);
+      ptx::mbar_init(&sm.tempty[b], 128);
+    }
+    ptx::mbar_init(&sm.drain, 1);
+    sm.abort = 0;
+    sm.never = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(&sm.tmem_base, F_TMEM);
+    ptx::tmem_relinquish();
+  }
+  if (!p.early_table) chain_entry();
+  build_tile_table<FBN, FT>(sm, p.offsets, E, p.M, p.NB, p.err, tid);
+  if (p.early_table) chain_entry();
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+  const int total = sm.total_tiles;
+
+  uint32_t armed = 0, armed_par = 0;
+  if (warp == 0) {
+    // ======================= TMA producer ===================================
+    if (lane == 0) {
+      const uint64_t pol_w = p.stream_weights ? ptx::policy_evict_first() : ptx::policy_evict_normal();
+      const uint64_t pol_w1 = ptx::policy_evict_first();
+      const uint64_t pol_x = ptx::policy_evict_last();
+      uint32_t s = 0, ph = 0;
+      bool ok = true;
+      for (int g = blockIdx.x; ok && g < total; g += gridDim.x) {
+        const TileInfo<FBN> t = decode_tile<FBN>(sm, E, p.NB, g);
+        const int rows = (t.ntok + 15) & ~15;
+        const uint32_t bytes = W_BYTES + BM * SFROW + (uint32_t)rows * (BK + SFROW);
+        const int y0 = t.e * p.N + t.nb * BM;  // bf16 epilogue: first weight row
+        const uint64_t pw = t.nch == 1 ? pol_w1 : pol_w;
+        for (int ks = 0; ks < KS; ++ks) {
+          if (!ptx::mbar_wait(&sm.empty[s], ph ^ 1u, &sm.abort, WAIT_NS)) {
+            ok = false;
+            break;
+          }
+          ptx::mbar_arrive_expect_tx(&sm.full[s], bytes);
+          armed |= 1u << s;
+          armed_par = (armed_par & ~(1u << s)) | (ph << s);
+          if (SILU) {
+            ptx::tma_load_5d(sm.w[s], &maps.w, &sm.full[s], 0, t.nb * 64, 0, ks, t.e, pw);
+            ptx::tma_load_4d(sm.sw[s], &maps.sw, &sm.full[s], ks * SFROW, t.nb * 64, 0, t.e, pw);
+          } else {
+            ptx::tma_load_3d(sm.w[s], &maps.w, &sm.full[s], 0, y0, ks, pw);
+            ptx::tma_load_2d(sm.sw[s], &maps.sw, &sm.full[s], ks * SFROW, y0, pw);
+          }
+          int r = 0;
+#pragma unroll
+          for (int i = 0; i < NXBOX; ++i) {
+            const int box = 64 >> i;
+            while (rows - r >= box) {
+              ptx::tma_load_2d(sm.x[s] + r * BK, &maps.x[i], &sm.full[s], ks * BK, t.tok0 + r,
+                               pol_x);
+              ptx::tma_load_2d(sm.sx[s] + r * SFROW, &maps.sx[i], &sm.full[s], ks * SFROW,
+                               t.tok0 + r, pol_x);
+              r += box;
+            }
+          }
+          if (++s == FSTAGES) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        sm.abort = 1;
+        flag_error(p.err, MOE_DEV_PIPE_TIMEOUT);
+      }
+    }
+  } else if (warp == 1) {
+    // ======================= scales + MMA ===================================
+    uint32_t s = 0, ph = 0;
+    bool ok = true, issued = false;
+    int iter = 0;
+    for (int g = blockIdx.x; ok && g < total; g += gridDim.x, ++iter) {
+      const TileInfo<FBN> t = decode_tile<FBN>(sm, E, p.NB, g);
+      const int n_mma = (t.ntok + 15) & ~15;
+      const uint32_t idesc = ptx::idesc_nvfp4(BM, n_mma);
+      const int b = iter & 1;
+      const uint32_t tph = (iter >> 1) & 1;
+      if (!__all_sync(kFull, ptx::mbar_wait(&sm.tempty[b], tph ^ 1u, &sm.abort, WAIT_NS))) {
+        ok = false;
+        break;
+      }
+      ptx::tc_fence_after();
+      const uint32_t d = tmem + (uint32_t)b * F_ACC;
+      for (int ks = 0; ks < KS; ++ks) {
+        if (!__all_sync(kFull, ptx::mbar_wait(&sm.full[s], ph, &sm.abort, WAIT_NS))) {
+          ok = false;
+          break;
+        }
+        arrange_scales(reinterpret_cast<const uint32_t*>(sm.sw[s]), sm.atom_a[s], lane);
+        arrange_scales(reinterpret_cast<const uint32_t*>(sm.sx[s]), sm.atom_b[s], lane);
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          ptx::tc_fence_after();
+          const uint32_t sfa = tmem + F_SF0 + (uint32_t)s * F_SFSTAGE;
+          const uint32_t sfb = sfa + 16;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            ptx::tmem_cp_32x128b_x4(sfa + 4 * j, ptx::sdesc_rows16(ptx::smem_u32(sm.atom_a[s][j])));
+            ptx::tmem_cp_32x128b_x4(sfb + 4 * j, ptx::sdesc_rows16(ptx::smem_u32(sm.atom_b[s][j])));
+          }
+          const uint32_t a0 = ptx::smem_u32(sm.w[s]);
+          const uint32_t b0 = ptx::smem_u32(sm.x[s]);
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            ptx::mma_nvfp4(d, ptx::sdesc_sw128(a0 + j * 32), ptx::sdesc_sw128(b0 + j * 32), idesc,
+                           sfa + 4 * j, sfb + 4 * j, (ks | j) != 0 ? 1u : 0u);
+          ptx::mma_commit(&sm.empty[s]);
+        }
+        __syncwarp();
+        issued = true;
+        if (++s == FSTAGES) {
+          s = 0;
+          ph ^= 1u;
+        }
+      }
+      if (!ok) break;
+      if (lane == 0) ptx::mma_commit(&sm.tfull[b]);
+    }
+    if (!ok && lane == 0) {
+      sm.abort = 1;
+      flag_error(p.err, MOE_DEV_PIPE_TIMEOUT);
+      if (issued) {
+        ptx::mma_commit(&sm.drain);
+        ptx::mbar_wait(&sm.drain, 0, &sm.never, DRAIN_NS);
+      }
+    }
+  } else {
+    // ======================= epilogue (warps 2..5) ==========================
+    const int q = warp & 3;
+    int iter = 0;
+    for (int g = blockIdx.x; g < total; g += gridDim.x, ++iter) {
+      const TileInfo<FBN> t = decode_tile<FBN>(sm, E, p.NB, g);
+      const int b = iter & 1;
+      const uint32_t tph = (iter >> 1) & 1;
+      bool ok = ptx::mbar_wait(&sm.tfull[b], tph, &sm.abort, WAIT_NS);
+      ok = __all_sync(kFull, ok);
+      if (SILU) ok = !bar_red_or(1 + (q & 1), 64, !ok);
+      if (!ok) {
+        sm.abort = 1;
+        flag_error(p.err, MOE_DEV_PIPE_TIMEOUT);
+        break;
+      }
+      ptx::tc_fence_after();
+      const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)b * F_ACC;
+      const int nchunk = (t.ntok + 31) >> 5;
+      const float scale = p.ga * __ldg(p.gb + t.e);  // both global scales
+      uint16_t* ost = sm.stage_out[q];
+      if (SILU) {
+        const int I = p.I;
+        const int pair = q & 1;
+        const bool holds_gate = q < 2;
+        __nv_bfloat16* hbase = reinterpret_cast<__nv_bfloat16*>(p.C);
+        const int mine0 = holds_gate ? 0 : 16;
+        const int jrow = t.nb * 64 + pair * 32;
+        uint32_t v[32];
+        ptx::tmem_ld_32x32b_x32(tbase, v);
+#pragma unroll 1
+        for (int c = 0; c < nchunk; ++c) {
+          ptx::tmem_ld_wait();
+          ptx::reg_fence(v);
+          float* give = sm.xchg[pair][c & 1] + (holds_gate ? 16 * 32 : 0);
+          const float* take = sm.xchg[pair][c & 1] + (holds_gate ? 0 : 16 * 32);
+          float own_v[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float lo = __uint_as_float(v[i]), hi = __uint_as_float(v[16 + i]);
+            own_v[i] = holds_gate ? lo : hi;
+            give[i * 32 + lane] = holds_gate ? hi : lo;
+          }
+          if (c + 1 < nchunk) ptx::tmem_ld_32x32b_x32(tbase + (c + 1) * 32, v);
+          bar_sync_named(1 + pair, 64);
+          const int tk0 = c * 32 + mine0;
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float other = take[i * 32 + lane];
+            const float gv = (holds_gate ? own_v[i] : other) * scale;
+            const float uv = (holds_gate ? other : own_v[i]) * scale;
+            // the result is rounded to bf16, so a fast divide is well inside it
+            ost[i * 32 + lane] = __bfloat16_as_ushort(
+                __float2bfloat16_rn(__fdividef(gv, 1.0f + __expf(-gv)) * uv));
+          }
+          __syncwarp();
+          if (jrow < I) {
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+              const int r = k * 8 + (lane >> 2);
+              if (tk0 + r < t.ntok)
+                *reinterpret_cast<uint4*>(hbase + (int64_t)(t.tok0 + tk0 + r) * I + jrow +
+                                          (lane & 3) * 8) =
+                    *reinterpret_cast<const uint4*>(ost + r * 32 + (lane & 3) * 8);
+            }
+          }
+          __syncwarp();
+        }
+        bar_sync_named(1 + pair, 64);
+      } else {
+        const int N = p.N;
+        const int ncol0 = t.nb * BM + q * 32;
+        __nv_bfloat16* cbase = reinterpret_cast<__nv_bfloat16*>(p.C);
+        uint32_t v[32];
+        ptx::tmem_ld_32x32b_x32(tbase, v);
+#pragma unroll 1
+        for (int c = 0; c < nchunk; ++c) {
+          ptx::tmem_ld_wait();
+          ptx::reg_fence(v);
+          float f[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]);
+          if (c + 1 < nchunk) ptx::tmem_ld_32x32b_x32(tbase + (c + 1) * 32, v);
+          const int tk0 = c * 32;
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            ost[i * 32 + lane] = __bfloat16_as_ushort(__float2bfloat16_rn(f[i] * scale));
+          __syncwarp();
+          if (ncol0 < N) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const int r = k * 8 + (lane >> 2);
+              if (tk0 + r < t.ntok)
+                *reinterpret_cast<uint4*>(cbase + (int64_t)(t.tok0 + tk0 + r) * N + ncol0 +
+                                          (lane & 3) * 8) =
+                    *reinterpret_cast<const uint4*>(ost + r * 32 + (lane & 3) * 8);
+            }
+          }
+          __syncwarp();
+        }
+      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(&sm.tempty[b]);
+    }
+  }
+
+  // ---- teardown -------------------------------------------------------------
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 0 && lane == 0 && *reinterpret_cast<volatile int*>(&sm.abort))
+    for (int i = 0; i < FSTAGES; ++i)
+      if ((armed >> i) & 1u)
+        ptx::mbar_wait(&sm.full[i], (armed_par >> i) & 1u, &sm.never, DRAIN_NS);
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, F_TMEM);
+  }
+}
+
+template <bool SILU>
+cudaError_t launch_f(const FMaps& maps, const FParams& p, int M, int E, cudaStream_t st,
+                     bool pdl) {
+  constexpr size_t smem = sizeof(FSmem<SILU>) + 1024;
+  static_assert(smem <= 227 * 1024, "shared memory budget");
+  auto kern = grouped_gemm_nvfp4_kernel<SILU>;
+  static std::mutex mu;
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    if (dev >= 64 || !attr_set[dev]) {
+      cudaError_t e =
+          cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+      if (dev < 64) attr_set[dev] = true;
+    }
+  }
+  const long long upper = ((long long)(M + FBN - 1) / FBN + E) * p.NB;
+  const int grid = (int)std::max<long long>(1, std::min<long long>(sm_count(), upper));
+  return launch_kernel(kern, dim3(grid), dim3(FT), smem, st, pdl, maps, p);
+}
+
+}  // namespace
+
+cudaError_t launch_grouped_gemm_nvfp4(const void* A, const uint8_t* sfa, float ga, const void* B,
+                                      const uint8_t* sfb, const float* gb,
+                                      const int32_t* offsets, int M, int N, int Kd, int E,
+                                      int epilogue, void* C, int* err, cudaStream_t st, bool pdl,
+                                      bool early_table) {
+  if (M == 0) return cudaSuccess;
+  const bool silu = (epilogue == MOE_EPI_SILU_MUL);
+  const uint64_t kb = (uint64_t)Kd / 2;   // bytes of a row
+  const uint64_t sc = (uint64_t)Kd / 16;  // scale bytes of a row
+  FMaps maps;
+  if (!make_tma_map_weights(&maps.w, B, silu, (uint64_t)E, (uint64_t)N, kb, 1) ||
+      !make_tma_map_weight_scales(&maps.sw, sfb, silu, (uint64_t)E, (uint64_t)N, sc))
+    return cudaErrorNotSupported;
+  for (int i = 0; i < NXBOX; ++i)
+    if (!make_tma_map_u8(&maps.x[i], A, (uint64_t)M, kb, 64u >> i) ||
+        !make_tma_map_scales(&maps.sx[i], sfa, (uint64_t)M, sc, 64u >> i))
+      return cudaErrorNotSupported;
+  FParams p;
+  p.ga = ga;
+  p.gb = gb;
+  p.offsets = offsets;
+  p.C = C;
+  p.err = err;
+  p.M = M;
+  p.N = N;
+  p.Kd = Kd;
+  p.E = E;
+  p.I = N / 2;
+  p.NB = silu ? p.I / 64 : N / BM;
+  p.KB = Kd / 256;
+  p.stream_weights = gemm_many_rows(M, E) ? 0 : 1;
+  p.early_table = early_table ? 1 : 0;
+  return silu ? launch_f<true>(maps, p, M, E, st, pdl) : launch_f<false>(maps, p, M, E, st, pdl);
+}
+
+}  // namespace moe

@@ -42,6 +42,13 @@ cudaError_t launch_permute_quant_block(const void* x, const int32_t* ids, int T,
                                        int32_t* offsets, void* ws, int* err, cudaStream_t st,
                                        bool pdl = false);
 
+// permute.cu: the same routing with NVFP4 quantisation (global scale g):
+// a_q [T*K, H/2] (two E2M1 codes per byte), sf [T*K, H/16] E4M3 block scales.
+cudaError_t launch_permute_quant_nvfp4(const void* x, const int32_t* ids, int T, int H, int E,
+                                       int K, float g, void* a_q, uint8_t* sf, int32_t* src2dst,
+                                       int32_t* offsets, void* ws, int* err, cudaStream_t st,
+                                       bool pdl = false);
+
 // permute.cu: device address of the fixed scratch used by
 // moe_permute_quant_noalloc on the current device (nullptr on failure).
 void* permute_static_scratch();
@@ -75,6 +82,21 @@ cudaError_t launch_act_quant(const void* h, const float* row_amax, int M, int I,
 // act_quant.cu: one scale per 128 channels, scale [M, I/128] (I % 128 == 0).
 cudaError_t launch_act_quant_block(const void* h, int M, int I, void* q, float* scale,
                                    cudaStream_t st, bool pdl = false);
+
+// act_quant.cu: NVFP4 requantisation with global scale g: q [M, I/2],
+// sf [M, I/16].
+cudaError_t launch_act_quant_nvfp4(const void* h, int M, int I, float g, void* q, uint8_t* sf,
+                                   cudaStream_t st, bool pdl = false);
+
+// gemm_nvfp4.cu: NVFP4 grouped GEMM. A [M, Kd/2] and B [E, N, Kd/2] packed
+// E2M1 (Kd % 256 == 0), sfa [M, Kd/16] and sfb [E, N, Kd/16] E4M3 block
+// scales, ga and gb [E] fp32 global scales; acc * ga * gb[e] then the
+// epilogue of launch_grouped_gemm (no row amax).
+cudaError_t launch_grouped_gemm_nvfp4(const void* A, const uint8_t* sfa, float ga, const void* B,
+                                      const uint8_t* sfb, const float* gb,
+                                      const int32_t* offsets, int M, int N, int Kd, int E,
+                                      int epilogue, void* C, int* err, cudaStream_t st,
+                                      bool pdl = false, bool early_table = false);
 
 // unpermute.cu
 cudaError_t launch_unpermute_sum(const void* down, const int32_t* src2dst, const float* w,

@@ -228,17 +228,56 @@ __device__ __forceinline__ void quant_scatter(const __nv_bfloat16* __restrict__ 
   }
 }
 
+// NVFP4: codes [T*K, H/2] (two E2M1 codes per byte, element 2j in the low
+// nibble), one E4M3 scale per 16 channels sf [T*K, H/16], with the global
+// scale g: scale code = e4m3((amax16 / 6) / g), codes = e2m1(x / (e4m3(code)
+// * g)). A 16-channel block is two 8-value vectors, held by two adjacent
+// threads (vector tid + i*NT, NT even), so its amax takes one shuffle.
+template <int VPT, int NT = kQuantThreads>
+__device__ __forceinline__ void quant_scatter_nvfp4(const __nv_bfloat16* __restrict__ x, int t,
+                                                    int H, int K, const int* dst, float g,
+                                                    uint8_t* __restrict__ a_q,
+                                                    uint8_t* __restrict__ sf) {
+  static_assert(NT % 2 == 0, "vector pairs");
+  const int tid = threadIdx.x;
+  const int nvec = H >> 3;
+  const uint4* xr = reinterpret_cast<const uint4*>(x + (int64_t)t * H);
+  __syncthreads();  // dst[] is complete
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    const int idx = tid + i * NT;
+    float f[8];
+    float m = 0.0f;
+    if (idx < nvec) {
+      bf16x8_to_f32(__ldg(xr + idx), f);
+      m = absmax8(f, 0.0f);
+    }
+    m = fmaxf(m, __shfl_xor_sync(kFull, m, 1));
+    if (idx < nvec) {
+      const uint32_t code = nvfp4_scale_code(m, g);
+      const uint32_t q = nvfp4_codes8(f, __fmul_rn(e4m3_value(code), g));
+      for (int k = 0; k < K; ++k) {
+        const int d = dst[k];
+        if (d < 0) continue;
+        *reinterpret_cast<uint32_t*>(a_q + (int64_t)d * (H >> 1) + (int64_t)idx * 4) = q;
+        if ((idx & 1) == 0) sf[(int64_t)d * (H >> 4) + (idx >> 1)] = (uint8_t)code;
+      }
+    }
+  }
+}
+
 // BLOCK: one scale per 128 channels (scale_a [M, H/128]) instead of one per
 // token. A 128-channel block is 16 vectors, held by the 16 lanes of a
 // half-warp (vector tid + i*128 lies in block tid/16 + 8i), so its amax is a
 // 16-lane shuffle reduction.
-template <int VPT, bool BLOCK>  // VPT: 16-byte vectors (8 bf16) per thread
+// QM: 0 per-token FP8, 1 block FP8, 2 NVFP4 (scale_a unused, sf / g used)
+template <int VPT, int QM>  // VPT: 16-byte vectors (8 bf16) per thread
 __global__ void __launch_bounds__(kQuantThreads)
     permute_quant_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ ids,
                          const uint32_t* __restrict__ bits, const int32_t* __restrict__ base,
                          int H, int E, int K, uint8_t* __restrict__ a_q,
                          float* __restrict__ scale_a, int32_t* __restrict__ src2dst,
-                         int32_t* __restrict__ row_token) {
+                         int32_t* __restrict__ row_token, float g, uint8_t* __restrict__ sf) {
   chain_entry();
   __shared__ int dst[32];
   __shared__ float red[kQuantThreads / 32];
@@ -255,7 +294,10 @@ __global__ void __launch_bounds__(kQuantThreads)
     dst[tid] = d;
     src2dst[(int64_t)t * K + tid] = d;
   }
-  quant_scatter<VPT, BLOCK>(x, t, H, K, dst, red, a_q, scale_a, row_token);
+  if constexpr (QM == 2)
+    quant_scatter_nvfp4<VPT>(x, t, H, K, dst, g, a_q, sf);
+  else
+    quant_scatter<VPT, QM == 1>(x, t, H, K, dst, red, a_q, scale_a, row_token);
 }
 
 // Small batches (T <= 512, T*K <= 4096): one launch does the routing and the
@@ -273,13 +315,14 @@ constexpr int kSmallTokens = 512;  // every CTA re-reads all T*K ids: keep T sma
 #endif
 constexpr int kSmallThreads = SMALL_THREADS;  // more warps per token than the large path
 
-template <int VPT, bool BLOCK>
+template <int VPT, int QM>
 __global__ void __launch_bounds__(kSmallThreads)
     permute_quant_small_kernel(const __nv_bfloat16* __restrict__ x,
                                const int32_t* __restrict__ ids, int T, int H, int E, int K,
                                uint8_t* __restrict__ a_q, float* __restrict__ scale_a,
                                int32_t* __restrict__ src2dst, int32_t* __restrict__ offsets,
-                               int* err, int32_t* __restrict__ row_token) {
+                               int* err, int32_t* __restrict__ row_token, float g,
+                               uint8_t* __restrict__ sf) {
   chain_entry();
   extern __shared__ int route_smem[];
   __shared__ int dst[32];
@@ -367,28 +410,31 @@ __global__ void __launch_bounds__(kSmallThreads)
     dst[tid] = d;
     src2dst[(int64_t)t * K + tid] = d;
   }
-  quant_scatter<VPT, BLOCK, kSmallThreads>(x, t, H, K, dst, red, a_q, scale_a, row_token);
+  if constexpr (QM == 2)
+    quant_scatter_nvfp4<VPT, kSmallThreads>(x, t, H, K, dst, g, a_q, sf);
+  else
+    quant_scatter<VPT, QM == 1, kSmallThreads>(x, t, H, K, dst, red, a_q, scale_a, row_token);
 }
 
-template <int VPT, bool BLOCK>
+template <int VPT, int QM>
 cudaError_t launch_small(const void* x, const int32_t* ids, int T, int H, int E, int K,
                          void* a_q, float* scale_a, int32_t* src2dst, int32_t* offsets, int* err,
-                         cudaStream_t st, bool pdl, int32_t* row_token) {
+                         cudaStream_t st, bool pdl, int32_t* row_token, float g, uint8_t* sf) {
   const size_t smem = sizeof(int) * (2 * (size_t)T * K + 2 * (size_t)E + 1);
-  return launch_kernel(permute_quant_small_kernel<VPT, BLOCK>, dim3(T), dim3(kSmallThreads),
+  return launch_kernel(permute_quant_small_kernel<VPT, QM>, dim3(T), dim3(kSmallThreads),
                        smem, st, pdl, reinterpret_cast<const __nv_bfloat16*>(x), ids, T, H, E, K,
                        reinterpret_cast<uint8_t*>(a_q), scale_a, src2dst, offsets, err,
-                       row_token);
+                       row_token, g, sf);
 }
 
-template <int VPT, bool BLOCK>
+template <int VPT, int QM>
 cudaError_t launch_quant(const void* x, const int32_t* ids, const uint32_t* bits,
                          const int32_t* base, int T, int H, int E, int K, void* a_q,
                          float* scale_a, int32_t* src2dst, cudaStream_t st, bool pdl,
-                         int32_t* row_token) {
-  return launch_kernel(permute_quant_kernel<VPT, BLOCK>, dim3(T), dim3(kQuantThreads), 0, st,
+                         int32_t* row_token, float g, uint8_t* sf) {
+  return launch_kernel(permute_quant_kernel<VPT, QM>, dim3(T), dim3(kQuantThreads), 0, st,
                        pdl, reinterpret_cast<const __nv_bfloat16*>(x), ids, bits, base, H, E, K,
-                       reinterpret_cast<uint8_t*>(a_q), scale_a, src2dst, row_token);
+                       reinterpret_cast<uint8_t*>(a_q), scale_a, src2dst, row_token, g, sf);
 }
 
 }  // namespace
@@ -421,18 +467,20 @@ size_t permute_ws_bytes(int T, int E) {
 
 namespace {
 
-template <bool BLOCK>
+template <int QM>
 cudaError_t permute_quant(const void* x, const int32_t* ids, int T, int H, int E, int K,
                           void* a_q, float* scale_a, int32_t* src2dst, int32_t* offsets,
                           void* ws, int* err, cudaStream_t st, bool pdl,
-                          int32_t* row_token = nullptr) {
+                          int32_t* row_token = nullptr, float g = 0.0f, uint8_t* sf = nullptr) {
   if (T > 0 && T <= kSmallTokens && T * K <= kSmallRoute) {
     const int vpt = (H / 8 + kSmallThreads - 1) / kSmallThreads;
-    if (vpt <= 1) return launch_small<1, BLOCK>(x, ids, T, H, E, K, a_q, scale_a, src2dst, offsets, err, st, pdl, row_token);
-    if (vpt <= 2) return launch_small<2, BLOCK>(x, ids, T, H, E, K, a_q, scale_a, src2dst, offsets, err, st, pdl, row_token);
-    if (vpt <= 4) return launch_small<4, BLOCK>(x, ids, T, H, E, K, a_q, scale_a, src2dst, offsets, err, st, pdl, row_token);
-    if (vpt <= 8) return launch_small<8, BLOCK>(x, ids, T, H, E, K, a_q, scale_a, src2dst, offsets, err, st, pdl, row_token);
-    return launch_small<16, BLOCK>(x, ids, T, H, E, K, a_q, scale_a, src2dst, offsets, err, st, pdl, row_token);
+#define MOE_SMALL(V) launch_small<V, QM>(x, ids, T, H, E, K, a_q, scale_a, src2dst, offsets, err, st, pdl, row_token, g, sf)
+    if (vpt <= 1) return MOE_SMALL(1);
+    if (vpt <= 2) return MOE_SMALL(2);
+    if (vpt <= 4) return MOE_SMALL(4);
+    if (vpt <= 8) return MOE_SMALL(8);
+    return MOE_SMALL(16);
+#undef MOE_SMALL
   }
   const int C = (T + 31) / 32;
   uint32_t* bits = reinterpret_cast<uint32_t*>(ws);
@@ -450,11 +498,13 @@ cudaError_t permute_quant(const void* x, const int32_t* ids, int T, int H, int E
     return e;
   if (T > 0) {
     const int vpt = (H / 8 + kQuantThreads - 1) / kQuantThreads;
-    if (vpt <= 1) return launch_quant<1, BLOCK>(x, ids, bits, base, T, H, E, K, a_q, scale_a, src2dst, st, pdl, row_token);
-    if (vpt <= 2) return launch_quant<2, BLOCK>(x, ids, bits, base, T, H, E, K, a_q, scale_a, src2dst, st, pdl, row_token);
-    if (vpt <= 4) return launch_quant<4, BLOCK>(x, ids, bits, base, T, H, E, K, a_q, scale_a, src2dst, st, pdl, row_token);
-    if (vpt <= 8) return launch_quant<8, BLOCK>(x, ids, bits, base, T, H, E, K, a_q, scale_a, src2dst, st, pdl, row_token);
-    return launch_quant<16, BLOCK>(x, ids, bits, base, T, H, E, K, a_q, scale_a, src2dst, st, pdl, row_token);
+#define MOE_QUANT(V) launch_quant<V, QM>(x, ids, bits, base, T, H, E, K, a_q, scale_a, src2dst, st, pdl, row_token, g, sf)
+    if (vpt <= 1) return MOE_QUANT(1);
+    if (vpt <= 2) return MOE_QUANT(2);
+    if (vpt <= 4) return MOE_QUANT(4);
+    if (vpt <= 8) return MOE_QUANT(8);
+    return MOE_QUANT(16);
+#undef MOE_QUANT
   }
   return cudaSuccess;
 }
@@ -465,16 +515,23 @@ cudaError_t launch_permute_quant(const void* x, const int32_t* ids, int T, int H
                                  void* a_q, float* scale_a, int32_t* src2dst, int32_t* offsets,
                                  void* ws, int* err, cudaStream_t st, bool pdl,
                                  int32_t* row_token) {
-  return permute_quant<false>(x, ids, T, H, E, K, a_q, scale_a, src2dst, offsets, ws, err, st,
-                              pdl, row_token);
+  return permute_quant<0>(x, ids, T, H, E, K, a_q, scale_a, src2dst, offsets, ws, err, st, pdl,
+                          row_token);
 }
 
 cudaError_t launch_permute_quant_block(const void* x, const int32_t* ids, int T, int H, int E,
                                        int K, void* a_q, float* scale_a, int32_t* src2dst,
                                        int32_t* offsets, void* ws, int* err, cudaStream_t st,
                                        bool pdl) {
-  return permute_quant<true>(x, ids, T, H, E, K, a_q, scale_a, src2dst, offsets, ws, err, st,
-                             pdl);
+  return permute_quant<1>(x, ids, T, H, E, K, a_q, scale_a, src2dst, offsets, ws, err, st, pdl);
+}
+
+cudaError_t launch_permute_quant_nvfp4(const void* x, const int32_t* ids, int T, int H, int E,
+                                       int K, float g, void* a_q, uint8_t* sf, int32_t* src2dst,
+                                       int32_t* offsets, void* ws, int* err, cudaStream_t st,
+                                       bool pdl) {
+  return permute_quant<2>(x, ids, T, H, E, K, a_q, nullptr, src2dst, offsets, ws, err, st, pdl,
+                          nullptr, g, sf);
 }
 
 }  // namespace moe

@@ -305,6 +305,59 @@ __device__ __forceinline__ void mma_e4m3(uint32_t d_tmem, uint64_t adesc, uint64
       : "memory");
 }
 
+// Instruction descriptor of tcgen05.mma.kind::mxf4nvf4.block_scale (PTX ISA,
+// tcgen05 "Instruction descriptor" table for the block-scaled kinds): bits
+// 4-5 B scale-factor id (0), 7-9 A type and 10-12 B type (E2M1 = 1), 15/16
+// A/B K-major (0), 17-22 N >> 3, 23 scale type (0: UE4M3), 24-28 M >> 4,
+// 29-30 A scale-factor id (0); D is fp32 for these kinds.
+__host__ __device__ constexpr uint32_t idesc_nvfp4(int M, int N) {
+  return (1u << 7) | (1u << 10)                // A, B: E2M1
+         | ((uint32_t)(N >> 3) << 17)          // N / 8
+         | ((uint32_t)(M >> 4) << 24);         // M / 16
+}
+
+// D[tmem] (+)= (A * SFA) (B * SFB)^T with E2M1 A/B in shared memory (two
+// codes per byte, K-major, K = 64 per instruction) and one UE4M3 scale per
+// 16 elements along K for every row of A and of B, read from tensor memory
+// at sfa / sfb (.scale_vec::4X: four scales per row per instruction).
+__device__ __forceinline__ void mma_nvfp4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t sfa, uint32_t sfb,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, "
+      "[%4], [%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+      : "memory");
+}
+
+// Shared-memory descriptor of an unswizzled K-major block of 16-byte rows
+// (8-row core matrices of 128 contiguous bytes, consecutive core matrices
+// 128 bytes apart), the source of a tcgen05.cp of 32 rows x 128 bits.
+__device__ __forceinline__ uint64_t sdesc_rows16(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)(128 >> 4) << 16;   // leading-dimension byte offset
+  d |= (uint64_t)(128 >> 4) << 32;   // stride-dimension byte offset
+  d |= (uint64_t)1 << 46;            // descriptor version
+  return d;                           // layout bits 61-63: 0, no swizzle
+}
+
+// Copies 32 rows x 16 bytes from shared memory (descriptor sdesc) into
+// tensor memory columns taddr .. taddr+3 of lanes 0..31, replicated into
+// each of the four 32-lane quadrants.
+__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+               : "memory");
+}
+
+// Orders this thread's earlier generic-proxy shared-memory writes before
+// later async-proxy reads of them (tcgen05.cp, tcgen05.mma, TMA).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // CTA-pair MMA, issued by one thread of the even CTA: D (256 x N, rows
 // 0..127 in this CTA's tensor memory, 128..255 in the peer's) (+)= A * B^T,
 // A's rows 0..127 / 128..255 and B's rows 0..N/2-1 / N/2..N-1 read from this

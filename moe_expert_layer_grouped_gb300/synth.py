@@ -58,8 +58,14 @@ class Workload:
     rsf: float
     bias: str  # "none" | "normal" | "zero" | "skewed"
     n_shared: int = 0  # shared experts, stored as experts E .. E+n_shared-1
-    quant: str = "token"  # "token": per-channel weight scales; "block": 128 x 128 blocks
+    # "token": per-channel weight scales; "block": 128 x 128 blocks; "nvfp4":
+    # E2M1 weights with an E4M3 scale per 16 along K and a global scale
+    quant: str = "token"
     hot_bias: float = 3.0  # "skewed": the bias of the experts with e % 10 == 0
+    # NVFP4 activations' global scales (calibrated input scales: about the
+    # largest |x| and |h| over 6 x 448, so block scales use the E4M3 range)
+    ga1: float = 5.0 / (6 * 448)
+    ga2: float = 2.0 / (6 * 448)
 
     @property
     def M(self):
@@ -99,6 +105,13 @@ for _name in ["dsv3_decode_t128", "dsv3_prefill_t8192", "mixtral_t4096", "dsv3_d
               "dsv3_prefill_t2048_e32"]:
     WORKLOADS[f"{_name}_block"] = replace(WORKLOADS[_name], name=f"{_name}_block",
                                           quant="block")
+
+WORKLOADS["tiny_nvfp4"] = replace(WORKLOADS["tiny"], name="tiny_nvfp4", H=256, I=256,
+                                  quant="nvfp4")
+for _name in ["dsv3_decode_t128", "dsv3_prefill_t8192", "mixtral_t4096", "dsv3_decode_t128_e32",
+              "dsv3_prefill_t2048_e32"]:
+    WORKLOADS[f"{_name}_nvfp4"] = replace(WORKLOADS[_name], name=f"{_name}_nvfp4",
+                                          quant="nvfp4")
 
 # tensor ids: each tensor draws from its own generator stream
 _TID = {"x": 0, "logits": 1, "bias": 2, "w13": 3, "w2": 4}
@@ -149,6 +162,46 @@ def expert_weights(E, rows, cols, seed, tensor, device="cpu", std=0.02, quant="t
     return q, s
 
 
+# NVFP4 weights are drawn directly in their format (no quantiser): E2M1
+# magnitude codes 0..7 with these probabilities (a half-normal folded onto
+# 0, 0.5, 1, 1.5, 2, 3, 4, 6), a random sign, E4M3 block-scale codes uniform
+# in [0x28, 0x38] (0.25 .. 1.0), and a global scale so that values have a
+# standard deviation near 0.02.
+E2M1_MAG_PROBS = [0.10, 0.19, 0.19, 0.16, 0.13, 0.12, 0.07, 0.04]
+NVFP4_WEIGHT_G = 0.02 / 1.6
+
+
+def pack_e2m1(codes: torch.Tensor) -> torch.Tensor:
+    """E2M1 codes [..., 2n] (uint8, 0..15) -> bytes [..., n], element 2j in
+    the low nibble of byte j."""
+    c = codes.to(torch.uint8)
+    return c[..., 0::2] | (c[..., 1::2] << 4)
+
+
+def unpack_e2m1(packed: torch.Tensor) -> torch.Tensor:
+    """bytes [..., n] -> E2M1 codes [..., 2n] (the inverse of pack_e2m1)."""
+    p = packed.to(torch.uint8)
+    return torch.stack([p & 0xF, p >> 4], dim=-1).reshape(*p.shape[:-1], 2 * p.shape[-1])
+
+
+def expert_weights_nvfp4(E, rows, cols, seed, tensor, device="cpu"):
+    """[E, rows, cols] NVFP4 weights: packed codes [E, rows, cols/2], E4M3
+    block scales [E, rows, cols/16] (uint8), global scales [E] f32."""
+    q = torch.empty((E, rows, cols // 2), dtype=torch.uint8, device=device)
+    sb = torch.empty((E, rows, cols // 16), dtype=torch.uint8, device=device)
+    g = _gen(seed, tensor, device)
+    cdf = torch.cumsum(torch.tensor(E2M1_MAG_PROBS, dtype=torch.float32, device=device), 0)
+    for e in range(E):
+        u = torch.rand((rows, cols), generator=g, device=device)
+        mag = torch.bucketize(u, cdf[:-1], right=True).to(torch.uint8)
+        sign = (torch.rand((rows, cols), generator=g, device=device) < 0.5).to(torch.uint8) << 3
+        q[e] = pack_e2m1(mag | sign)
+        sb[e] = torch.randint(0x28, 0x39, (rows, cols // 16), generator=g, device=device,
+                              dtype=torch.int32).to(torch.uint8)
+    gs = torch.full((E,), NVFP4_WEIGHT_G, dtype=torch.float32, device=device)
+    return q, sb, gs
+
+
 def router_bias(wl: Workload, seed, device="cpu") -> Optional[torch.Tensor]:
     if wl.bias == "none":
         return None
@@ -169,7 +222,9 @@ def make_inputs(wl: Workload, seed=0, device="cpu", weights=True):
     w13: u8 [E,2I,H] (rows 0..I-1 gate, I..2I-1 up) with s13 f32 [E,2I];
     w2: u8 [E,H,I] with s2 f32 [E,H]; with n_shared shared experts the
     leading dimension is E + n_shared. Block workloads: s13 [E, 2I/128, H/128],
-    s2 [E, H/128, I/128].
+    s2 [E, H/128, I/128]. NVFP4 workloads: w13 [E,2I,H/2] and w2 [E,H,I/2]
+    packed E2M1 codes, s13 [E,2I,H/16] and s2 [E,H,I/16] E4M3 block scales
+    (uint8), g13 and g2 [E] f32 global scales.
     """
     d = dict(
         x=normal((wl.T, wl.H), 1.0, seed, "x", device, torch.bfloat16),
@@ -178,6 +233,11 @@ def make_inputs(wl: Workload, seed=0, device="cpu", weights=True):
     )
     if weights:
         n = wl.E + wl.n_shared
+        if wl.quant == "nvfp4":
+            d["w13"], d["s13"], d["g13"] = expert_weights_nvfp4(n, 2 * wl.I, wl.H, seed, "w13",
+                                                                device)
+            d["w2"], d["s2"], d["g2"] = expert_weights_nvfp4(n, wl.H, wl.I, seed, "w2", device)
+            return d
         d["w13"], d["s13"] = expert_weights(n, 2 * wl.I, wl.H, seed, "w13", device,
                                             quant=wl.quant)
         d["w2"], d["s2"] = expert_weights(n, wl.H, wl.I, seed, "w2", device, quant=wl.quant)

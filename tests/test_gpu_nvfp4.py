@@ -1,0 +1,205 @@
+"""NVFP4 path on the GPU through the C ABI, against the oracle's NVFP4
+functions: the E2M1 conversion on every bf16 value in [-6, 6] (the
+quantiser with a unit step), the requant and the pre-reorder bit for bit,
+the block-scaled grouped GEMM on one tile first and then on ragged shapes
+of both epilogues, and the whole layer (every token of the small and decode
+layers, a token of every GEMM tile of the prefill layer)."""
+import numpy as np
+import pytest
+import torch
+
+import moe_expert_layer_grouped_gb300 as moe
+import oracle
+from moe_expert_layer_grouped_gb300 import synth
+
+from gpu_util import assert_parity, bf16_np, ragged_offsets, tile_cover_tokens
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import __graft_entry__
+    __graft_entry__.build()
+    yield
+    assert moe.moe_device_status() == 0
+
+
+def _t(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+
+
+def _unpack(t):
+    return synth.unpack_e2m1(t.cpu()).numpy()
+
+
+def _bf16_bits(a32):
+    return torch.from_numpy(np.ascontiguousarray(a32, np.float32)).to(torch.bfloat16) \
+        .view(torch.int16).numpy().view(np.uint16)
+
+
+def test_e2m1_conversion_of_every_bf16_in_range():
+    """Blocks of one 6.0 and 15 test values with g = 1: the block scale is
+    e4m3(6/6/1) = 1.0 exactly, so the codes are e2m1(v) of each bf16 v."""
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    vals = (bits.astype(np.uint32) << 16).view(np.float32)
+    keep = np.isfinite(vals) & (np.abs(vals) <= 6.0)
+    v = vals[keep]
+    n = -(-v.size // 15) * 15
+    v = np.concatenate([v, np.zeros(n - v.size, np.float32)]).reshape(-1, 15)
+    blocks = np.concatenate([np.full((v.shape[0], 1), 6.0, np.float32), v], axis=1)
+    rows = blocks.reshape(-1, 256) if blocks.size % 256 == 0 else \
+        np.concatenate([blocks.ravel(), np.zeros(256 - blocks.size % 256, np.float32)]).reshape(-1, 256)
+    h = _bf16_bits(rows)
+    q, sf = moe.moe_act_quant_nvfp4(_t(h).view(torch.bfloat16), 1.0)
+    torch.cuda.synchronize()
+    oq, osf = oracle.nvfp4_quant(h, 1.0)
+    assert np.array_equal(sf.cpu().numpy(), osf)
+    got = _unpack(q)
+    exp = oracle.e2m1_encode(rows.astype(np.float32))
+    assert np.array_equal(oq, exp)                   # the oracle's quantiser agrees
+    bad = np.argwhere(got != exp)
+    assert bad.shape[0] == 0, (bad.shape[0], bad[:5].tolist())
+
+
+@pytest.mark.parametrize("g", [1.0, 0.37, 5.0 / (6 * 448)])
+def test_act_quant_nvfp4_matches_oracle(g):
+    rng = np.random.default_rng(7)
+    M, I = 257, 512
+    x = rng.standard_normal((M, I)).astype(np.float32)
+    x *= (10.0 ** rng.uniform(-4, 3, (M, 1))).astype(np.float32)   # rows of every size
+    x[3] = 0.0                                                       # all-zero row
+    x[5, 16:32] = 0.0                                                # an all-zero block
+    x[9, :16] = 1e-30                                                # scale below e4m3
+    h = _bf16_bits(x)
+    q, sf = moe.moe_act_quant_nvfp4(_t(h).view(torch.bfloat16), g)
+    torch.cuda.synchronize()
+    oq, osf = oracle.nvfp4_quant(h, g)
+    assert np.array_equal(sf.cpu().numpy(), osf)
+    assert np.array_equal(_unpack(q), oq)
+
+
+@pytest.mark.parametrize("T,H,E,K", [(8, 256, 8, 2), (300, 512, 24, 6), (4099, 256, 64, 6)])
+def test_permute_quant_nvfp4_matches_oracle(T, H, E, K):
+    rng = np.random.default_rng(T + H)
+    ids = np.stack([rng.choice(E, K, replace=False) for _ in range(T)]).astype(np.int32)
+    x = torch.from_numpy(rng.standard_normal((T, H)).astype(np.float32)).to(torch.bfloat16)
+    x_bits = x.view(torch.int16).numpy().view(np.uint16).copy()
+    g = 5.0 / (6 * 448)
+    a_q, sf, s2d, off = moe.moe_permute_quant_nvfp4(x.to(DEV), _t(ids), E, g)
+    torch.cuda.synchronize()
+    o_aq, o_sf, o_s2d, o_off = oracle.permute_quant_nvfp4(x_bits, ids, E, g)
+    assert np.array_equal(off.cpu().numpy(), o_off)
+    assert np.array_equal(s2d.cpu().numpy(), o_s2d)
+    assert np.array_equal(sf.cpu().numpy(), o_sf)
+    assert np.array_equal(_unpack(a_q), o_aq)
+
+
+def _fp4_problem(rng, counts, N, Kd):
+    E = len(counts)
+    off = ragged_offsets(counts)
+    M = int(off[-1])
+    A = rng.integers(0, 16, (M, Kd)).astype(np.uint8)
+    B = rng.integers(0, 16, (E, N, Kd)).astype(np.uint8)
+    sa = rng.integers(0x20, 0x40, (M, Kd // 16)).astype(np.uint8)    # 2^-3 .. 2^0 area
+    sb = rng.integers(0x20, 0x40, (E, N, Kd // 16)).astype(np.uint8)
+    gb = (10.0 ** rng.uniform(-3, -1, E)).astype(np.float32)
+    return A, sa, B, sb, gb, off
+
+
+def _run_fp4(A, sa, ga, B, sb, gb, off, epi):
+    pa = synth.pack_e2m1(torch.from_numpy(A))
+    pb = synth.pack_e2m1(torch.from_numpy(B))
+    return moe.moe_grouped_gemm_nvfp4(pa.to(DEV), _t(sa), ga, pb.to(DEV), _t(sb), _t(gb),
+                                      _t(off), epi)
+
+
+def test_nvfp4_gemm_one_tile():
+    """One expert, 64 tokens, one 128-row weight block, one K chunk."""
+    rng = np.random.default_rng(1)
+    A, sa, B, sb, gb, off = _fp4_problem(rng, [64], 128, 256)
+    C = _run_fp4(A, sa, 0.5, B, sb, gb, off, moe.EPI_BF16)
+    torch.cuda.synchronize()
+    assert moe.moe_device_status() == 0
+    ref = oracle.grouped_gemm_nvfp4(A, sa, 0.5, B, sb, gb, off)
+    got = bf16_np(C)
+    assert np.all(np.abs(got - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-5 * np.abs(ref).max())
+    assert_parity(got, ref, "nvfp4 gemm, one tile")
+
+
+FP4_SHAPES = [
+    # counts per expert, N, Kd
+    ([5, 0, 9], 256, 256),
+    ([130, 1, 0, 257, 128], 256, 512),
+    ([300], 384, 768),
+    ([17, 64, 200, 3], 128, 256),
+    ([129, 127], 256, 7168),
+    ([150, 0, 3, 40, 0, 0, 7, 0, 0, 0, 0, 0, 0, 0, 0, 1], 256, 512),
+]
+
+
+@pytest.mark.parametrize("counts,N,Kd", FP4_SHAPES)
+def test_nvfp4_gemm_bf16_epilogue(counts, N, Kd):
+    rng = np.random.default_rng(sum(counts) + N + Kd)
+    A, sa, B, sb, gb, off = _fp4_problem(rng, counts, N, Kd)
+    C = _run_fp4(A, sa, 0.25, B, sb, gb, off, moe.EPI_BF16)
+    torch.cuda.synchronize()
+    ref = oracle.grouped_gemm_nvfp4(A, sa, 0.25, B, sb, gb, off)
+    got = bf16_np(C)
+    assert np.all(np.abs(got - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-4 * np.abs(ref).max())
+    assert_parity(got, ref, "nvfp4 gemm bf16")
+
+
+@pytest.mark.parametrize("counts,N,Kd", FP4_SHAPES)
+def test_nvfp4_gemm_silu_epilogue(counts, N, Kd):
+    rng = np.random.default_rng(3 * sum(counts) + N + Kd)
+    A, sa, B, sb, gb, off = _fp4_problem(rng, counts, N, Kd)
+    C = _run_fp4(A, sa, 0.25, B, sb, gb, off, moe.EPI_SILU_MUL)
+    torch.cuda.synchronize()
+    ref = oracle.silu_mul(oracle.grouped_gemm_nvfp4(A, sa, 0.25, B, sb, gb, off))
+    got = bf16_np(C)
+    assert np.all(np.abs(got - ref) <= 2.0 ** -7 * np.abs(ref) + 1e-4 * np.abs(ref).max())
+    assert_parity(got, ref, "nvfp4 gemm silu")
+
+
+def _layer_nvfp4(wl, d):
+    return moe.MoELayer(d["w13"], d["s13"], d["w2"], d["s2"], d["bias"], wl.num_groups,
+                        wl.topk_group, wl.top_k, wl.scoring, wl.renormalize, wl.rsf, wl.T,
+                        n_shared=wl.n_shared, quant="nvfp4",
+                        nvfp4=dict(g13=d["g13"], g2=d["g2"], ga1=wl.ga1, ga2=wl.ga2))
+
+
+def _check_nvfp4_layer(wl, seed, sample=False):
+    d = synth.make_inputs(wl, seed=seed, device=DEV)
+    out = _layer_nvfp4(wl, d)(d["x"], d["logits"])
+    torch.cuda.synchronize()
+    assert moe.moe_device_status() == 0
+    n = synth.to_numpy_inputs({k: d[k] for k in ("x", "logits", "bias", "s13", "g13", "s2",
+                                                  "g2")})
+    w13, w2 = _unpack(d["w13"]), _unpack(d["w2"])
+    if sample:
+        ids, _ = oracle.gate(n["logits"], n["bias"], wl.num_groups, wl.topk_group, wl.top_k,
+                             wl.scoring, wl.renormalize, wl.rsf)
+        tokens, _ = tile_cover_tokens(ids, wl.E, quant="nvfp4", seed=seed)
+    else:
+        tokens = np.arange(wl.T, dtype=np.int64)
+    ref, _, _ = oracle.forward_tokens_nvfp4(n["x"], n["logits"], n["bias"], w13, n["s13"],
+                                            n["g13"], w2, n["s2"], n["g2"], wl.ga1, wl.ga2,
+                                            wl.num_groups, wl.topk_group, wl.top_k, wl.scoring,
+                                            wl.renormalize, wl.rsf, tokens=tokens,
+                                            n_shared=wl.n_shared)
+    assert_parity(bf16_np(out[torch.from_numpy(tokens).to(DEV)]), ref, wl.name)
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_forward_nvfp4_tiny(seed):
+    _check_nvfp4_layer(synth.WORKLOADS["tiny_nvfp4"], seed)
+
+
+def test_forward_nvfp4_dsv3_decode_t128():
+    _check_nvfp4_layer(synth.WORKLOADS["dsv3_decode_t128_nvfp4"], 0)
+
+
+def test_forward_nvfp4_dsv3_prefill_every_tile():
+    _check_nvfp4_layer(synth.WORKLOADS["dsv3_prefill_t8192_nvfp4"], 0, sample=True)
