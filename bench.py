@@ -343,7 +343,7 @@ def time_breakdown(moe, layer, wl, batches, steps, torch):
             ids[:, :wl.top_k] = ids_r
             w[:, :wl.top_k] = w_r
         if ev: ev[7].record(st)
-        if fp4:
+        if fp4:  # (the layer holds the arranged weight scales)
             fa, fsa, fs2d, foff = moe.moe_permute_quant_nvfp4(x, ids, E, layer.ga1, workspace=pws)
             if ev: ev[2].record(st)
             fh = moe.moe_grouped_gemm_nvfp4(fa, fsa, layer.ga1, layer.w13, layer.s13, layer.g13,
@@ -587,8 +587,8 @@ def cpu_baseline(synth, torch, wl, seed, r, budget_s=15.0):
     L = r["layer"]
     d = {"w13": L.w13, "s13": L.s13, "w2": L.w2, "s2": L.s2, "bias": L.bias,
          "x": r["batches"][0][0], "logits": r["batches"][0][1]}
-    if wl.quant == "nvfp4":
-        d.update(g13=L.g13, g2=L.g2)
+    if wl.quant == "nvfp4":  # the row-major block scales (the layer's are arranged)
+        d.update(s13=L.s13_rows, s2=L.s2_rows, g13=L.g13, g2=L.g2)
     fwd = oracle_forward(oracle, synth, wl, synth.to_numpy_inputs(d))
     threads = oracle.get_threads()
     t = time.time()

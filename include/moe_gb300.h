@@ -402,6 +402,9 @@ MOE_API moe_status moe_forward_block_host(const void* x_host,
  * of byte j; scales one byte per 16 elements:
  *   w13 [E,2I,H/2], s13 [E,2I,H/16], w2 [E,H,I/2], s2 [E,H,I/16] (bytes);
  *   g13, g2 [E] f32. H % 256 == 0 and I % 256 == 0.
+ * The GEMMs take the weights' scales ARRANGED by moe_nvfp4_arrange_scales
+ * (once, when the layer is set up): same bytes, in the order the kernel
+ * copies them to tensor memory.
  * The GEMMs run on the block-scaled tensor-core MMA
  * (tcgen05.mma.kind::mxf4nvf4.block_scale, block 16, UE4M3 scales).
  * ======================================================================== */
@@ -419,10 +422,24 @@ MOE_API moe_status moe_permute_quant_nvfp4(const void* x, const int32_t* topk_id
 MOE_API moe_status moe_act_quant_nvfp4(const void* h, int M, int I, float g, void* q,
                                        uint8_t* sf, void* stream);
 
+/*
+ * moe_nvfp4_arrange_scales — the weights' block scales sb [E,N,Kd/16] (one
+ * byte per 16 elements along K) rewritten into out (same size, a distinct
+ * buffer) in the order moe_grouped_gemm_nvfp4 copies them to tensor memory:
+ * for expert e, weight tile nb, K chunk c (256 elements) and MMA step j
+ * (64 elements), 512 bytes holding at 16*(m%32) + 4*(m/32) + b scale 4j+b
+ * of chunk c of the tile's row m. Tile rows: epilogue MOE_EPI_BF16, rows
+ * 128*nb + m; MOE_EPI_SILU_MUL (w13, N = 2I), rows 64*nb + m for m < 64
+ * (gate) and I + 64*nb + m - 64 (up). Kd % 256 == 0, N % 128 == 0.
+ */
+MOE_API moe_status moe_nvfp4_arrange_scales(const uint8_t* sb, int E, int N, int Kd,
+                                            int epilogue, uint8_t* out, void* stream);
+
 /* moe_grouped_gemm in NVFP4: A [M, Kd/2] packed, sfa [M, Kd/16], ga (the
- * activations' global scale); B [E, N, Kd/2] packed, sfb [E, N, Kd/16], gb
- * [E] f32; acc[r,n] = sum_k a b sa sb (fp32), dequantised by ga * gb[e],
- * then the epilogue (no row amax). Kd % 256 == 0, N % 128 == 0. */
+ * activations' global scale); B [E, N, Kd/2] packed, sfb the weight scales
+ * arranged by moe_nvfp4_arrange_scales for this epilogue, gb [E] f32;
+ * acc[r,n] = sum_k a b sa sb (fp32), dequantised by ga * gb[e], then the
+ * epilogue (no row amax). Kd % 256 == 0, N % 128 == 0. */
 MOE_API moe_status moe_grouped_gemm_nvfp4(const void* A, const uint8_t* sfa, float ga,
                                           const void* B, const uint8_t* sfb, const float* gb,
                                           const int32_t* offsets, int M, int N, int Kd, int E,
@@ -434,8 +451,9 @@ MOE_API size_t moe_nvfp4_workspace_size(int T, int H, int I, int E, int K);
 
 /* The whole layer in NVFP4: gate, pre-reorder + NVFP4 quant (ga1), w13 GEMM
  * + SiLU*mul, NVFP4 requant (ga2), w2 GEMM, weighted post-reorder; n_shared
- * shared experts as in moe_forward_shared (0 for none). Weights and scales
- * as above; otherwise as moe_forward_shared. */
+ * shared experts as in moe_forward_shared (0 for none). Weights as above;
+ * s13 and s2 arranged by moe_nvfp4_arrange_scales (s13 with
+ * MOE_EPI_SILU_MUL, s2 with MOE_EPI_BF16); otherwise as moe_forward_shared. */
 MOE_API moe_status moe_forward_nvfp4(const void* x, const float* logits, const float* bias,
                                      const void* w13, const uint8_t* s13, const float* g13,
                                      const void* w2, const uint8_t* s2, const float* g2,

@@ -23,6 +23,7 @@ __all__ = [
     "moe_permute_quant_noalloc", "moe_permute_quant_rows", "moe_grouped_gemm_rows",
     "moe_permute_quant_nvfp4", "moe_act_quant_nvfp4", "moe_grouped_gemm_nvfp4",
     "moe_nvfp4_workspace_size", "moe_forward_nvfp4", "moe_forward_nvfp4_host",
+    "moe_nvfp4_arrange_scales",
     "moe_act_quant", "moe_unpermute_sum", "moe_workspace_size", "moe_forward",
     "moe_forward_host", "moe_device_status", "MoELayer",
     # expert parallelism (moe_expert_layer_grouped_gb300.ep)
@@ -97,6 +98,7 @@ _SIGNATURES = {
     "moe_act_quant_nvfp4": (_I, [_P, _I, _I, _F, _P, _P, _P]),
     "moe_grouped_gemm_nvfp4": (_I, [_P, _P, _F, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P]),
     "moe_nvfp4_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
+    "moe_nvfp4_arrange_scales": (_I, [_P, _I, _I, _I, _I, _P, _P]),
     "moe_forward_nvfp4": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _F, _F, _I, _I, _I, _I, _I,
                                _I, _I, _I, _I, _I, _F, _P, _P, _SZ, _P]),
     "moe_forward_nvfp4_host": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _F, _F, _I, _I, _I, _I,
@@ -544,10 +546,21 @@ def moe_act_quant_nvfp4(h, g, stream=None):
     return q, sf
 
 
+def moe_nvfp4_arrange_scales(sb, epilogue, stream=None):
+    """Weight block scales [E, N, Kd/16] -> the GEMM's copy order (same shape)."""
+    import torch
+    _need_cuda(sb)
+    E, N, ks = sb.shape
+    out = torch.empty_like(sb)
+    _check("moe_nvfp4_arrange_scales", load().moe_nvfp4_arrange_scales(
+        _ptr(sb), E, N, ks * 16, epilogue, _ptr(out), _stream(stream)))
+    return out
+
+
 def moe_grouped_gemm_nvfp4(A, sfa, ga, B, sfb, gb, offsets, epilogue=EPI_BF16, C=None,
                            stream=None):
-    """A [M, Kd/2] packed, sfa [M, Kd/16]; B [E, N, Kd/2] packed, sfb [E, N, Kd/16],
-    gb [E]; ga a float."""
+    """A [M, Kd/2] packed, sfa [M, Kd/16]; B [E, N, Kd/2] packed, sfb [E, N, Kd/16]
+    arranged by moe_nvfp4_arrange_scales (same epilogue), gb [E]; ga a float."""
     import torch
     _need_cuda(A, sfa, B, sfb, gb, offsets, C)
     M = A.shape[0]
@@ -654,6 +667,11 @@ class MoELayer:
             self.H *= 2  # two codes per byte
             self.g13, self.g2 = nvfp4["g13"], nvfp4["g2"]
             self.ga1, self.ga2 = float(nvfp4["ga1"]), float(nvfp4["ga2"])
+            # the weights' block scales in the order the GEMMs copy them (the
+            # row-major ones stay in s13_rows / s2_rows)
+            self.s13_rows, self.s2_rows = s13, s2
+            self.s13 = moe_nvfp4_arrange_scales(s13, EPI_SILU_MUL)
+            self.s2 = moe_nvfp4_arrange_scales(s2, EPI_BF16)
         self.n_shared = n_shared
         self.E = EA - n_shared  # routed experts
         self.I = I2 // 2

@@ -736,6 +736,15 @@ moe_status moe_forward_nvfp4_host(const void* x_host, const float* logits_host,
   return MOE_OK;
 }
 
+moe_status moe_nvfp4_arrange_scales(const uint8_t* sb, int E, int N, int Kd, int epilogue,
+                                    uint8_t* out, void* stream) {
+  if (E < 1 || N < 1 || !nvfp4_dims_ok(Kd) || N % 128 != 0) return MOE_ERR_INVALID_ARG;
+  if (epilogue != MOE_EPI_BF16 && epilogue != MOE_EPI_SILU_MUL) return MOE_ERR_INVALID_ARG;
+  if (!ok_ptr(sb) || !ok_ptr(out) || sb == out) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_nvfp4_arrange_scales(sb, E, N, Kd, epilogue, out,
+                                                 static_cast<cudaStream_t>(stream)));
+}
+
 size_t moe_nvfp4_workspace_size(int T, int H, int I, int E, int K) {
   if (T < 0 || H < 1 || I < 1 || E < 1 || K < 1) return 0;
   return fp4_layout(T, H, I, E, K).total;

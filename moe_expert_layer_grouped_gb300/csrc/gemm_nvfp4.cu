@@ -15,18 +15,31 @@
 // (element 2j in the low nibble), K-major; sa [M, Kd/16], sb [E, N, Kd/16]
 // E4M3 codes. Kd % 256 == 0, so a 128-byte K chunk (256 elements) is whole.
 //
-// Design (one persistent CTA per SM, 192 threads, single-CTA MMAs):
+// Design (one persistent CTA per SM, 320 threads, single-CTA MMAs):
 //   warp 0      TMA producer, one K chunk per stage: the tile's 128 weight
-//               rows (one box), their 128 x 16 scale bytes, the token rows
-//               (64/32/16-row boxes) and their scale bytes.
-//   warp 1      scales + MMA: the whole warp rearranges the stage's scale
-//               bytes (row-major as loaded) into the 32-row x 16-byte blocks
-//               tcgen05.cp copies to tensor memory (block j: bytes of row
-//               m0 + 32*m1 at offset 16*m0 + 4*m1, the four scales of MMA
-//               step j), fences them for the async proxy, and lane 0 copies
-//               them (tcgen05.cp.32x128b.warpx4) and issues the four MMAs of
-//               the chunk, each reading its scales from four columns.
+//               rows (one box), their scales (2 KB, already in copy order,
+//               see below), the token rows (64/32/16-row boxes) and their
+//               scale bytes (row-major).
+//   warps 6..9  token scales, one warp per 32-lane quadrant of tensor
+//               memory: each writes the stage's token scales from registers
+//               (tcgen05.st) into its quadrant in the layout the MMA reads
+//               (lane i, column 4j + c: the four scales of MMA step j of token
+//               row i + 32c, the same in every quadrant) and signals the MMA
+//               thread.
+//   warp 1      MMA: lane 0 copies the stage's four weight-scale blocks
+//               (tcgen05.cp.32x128b.warpx4; block j: bytes of row m0 + 32*m1
+//               at offset 16*m0 + 4*m1, replicated into the four quadrants)
+//               and issues the four MMAs of the chunk, each reading its scales
+//               from four tensor-memory columns.
+// Token scales go from registers to tensor memory rather than through a
+// rearranged shared-memory block copied by tcgen05.cp: generic-proxy stores
+// followed by a tcgen05.cp of the same bytes cost about 40 % of the decode
+// w13 time in an earlier version.
 //   warps 2..5  epilogue as in the FP8 kernel, dequantising by ga * gb[e].
+// The weights' scales are arranged once, when the layer is set up
+// (moe_nvfp4_arrange_scales): for expert e, weight tile nb (its 128 rows in
+// the kernel's row order) and K chunk c, 2 KB holding the four blocks of the
+// chunk's MMA steps, so a stage loads them with one bulk copy.
 // Tensor memory: two accumulators of 128 columns (token tiles <= 128), then
 // per pipeline stage 16 columns of weight scales and 16 of token scales,
 // released with the stage.
@@ -48,34 +61,32 @@ namespace {
 
 using namespace gemm_common;
 
-constexpr int FT = 192;
-constexpr int FBN = 128;       // tokens per tile (MMA N)
-constexpr int FSTAGES = 4;
+constexpr int FT = 320;  // 10 warps: producer, MMA, 4 epilogue, 4 token scales
+constexpr int SCALE_WARP0 = 6;
 constexpr int SFROW = 16;      // scale bytes per row per 128-byte K chunk
-constexpr uint32_t F_ACC = 128;                     // TMEM columns per accumulator
-constexpr uint32_t F_SF0 = 2 * F_ACC;               // first scale column
 constexpr uint32_t F_SFSTAGE = 32;                  // scale columns per stage
 constexpr uint32_t F_TMEM = 512;
-static_assert(F_SF0 + FSTAGES * F_SFSTAGE <= F_TMEM, "tensor memory budget");
+// Tile width FBN (tokens, MMA N) and pipeline depth FSTAGES per launch:
+// few tokens per expert (decode) 64 x 6 stages, the weight stream's bytes in
+// flight being what bounds it; otherwise 128 x 5. Tensor memory: two FBN-
+// column accumulators, then FSTAGES x 32 scale columns.
 
 struct FMaps {
   CUtensorMap w;          // weights, one 128-byte chunk of 128 rows per box
   CUtensorMap x[NXBOX];   // token rows, boxes of 64 >> i rows
-  CUtensorMap sw;         // weight scales, 16 bytes x 128 rows per box
   CUtensorMap sx[NXBOX];  // token scales, 16 bytes x (64 >> i) rows
 };
 
-template <bool SILU>
+template <bool SILU, int FBN, int FSTAGES>
 struct FSmem {
   uint8_t w[FSTAGES][W_BYTES];
   uint8_t x[FSTAGES][FBN * BK];
-  uint8_t sw[FSTAGES][BM * SFROW];    // row-major, as loaded
-  uint8_t sx[FSTAGES][FBN * SFROW];
-  uint32_t atom_a[FSTAGES][4][128];   // tcgen05.cp sources, one per MMA K step
-  uint32_t atom_b[FSTAGES][4][128];
+  uint8_t sx[FSTAGES][FBN * SFROW];   // token scales, row-major as loaded
+  uint32_t atom_a[FSTAGES][4][128];   // weight scales: tcgen05.cp sources, one per MMA step
   float xchg[SILU ? 2 : 1][2][32 * 32];
   uint16_t stage_out[4][32 * 32];
   uint64_t full[FSTAGES];
+  uint64_t sready[FSTAGES];  // the stage's token scales are in tensor memory
   uint64_t empty[FSTAGES];
   uint64_t tfull[2];
   uint64_t tempty[2];
@@ -92,6 +103,7 @@ struct FSmem {
 struct FParams {
   float ga;
   const float* gb;
+  const uint8_t* sba;  // arranged weight scales [E][NB][KB][2048]
   const int32_t* offsets;
   void* C;
   int* err;
@@ -100,26 +112,13 @@ struct FParams {
   int early_table;
 };
 
-// Scale bytes of 128 rows x 16 (row-major, 4 words a row) -> four blocks of
-// 32 rows x 16 bytes: block j, word 4*m0 + m1 = word j of row m0 + 32*m1.
-__device__ __forceinline__ void arrange_scales(const uint32_t* raw, uint32_t (*atom)[128],
-                                               int lane) {
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int w = lane + 32 * i;            // word 4*m0 + m1 of each block
-    const int row = (w & 3) * 32 + (w >> 2);
-    const uint4 r = *reinterpret_cast<const uint4*>(raw + row * 4);
-    atom[0][w] = r.x;
-    atom[1][w] = r.y;
-    atom[2][w] = r.z;
-    atom[3][w] = r.w;
-  }
-}
-
-template <bool SILU>
+template <bool SILU, int FBN, int FSTAGES>
 __global__ void __launch_bounds__(FT, 1)
     grouped_gemm_nvfp4_kernel(const __grid_constant__ FMaps maps, const FParams p) {
-  using S = FSmem<SILU>;
+  constexpr uint32_t F_ACC = FBN;              // TMEM columns per accumulator
+  constexpr uint32_t F_SF0 = 2 * F_ACC;        // first scale column
+  static_assert(F_SF0 + FSTAGES * F_SFSTAGE <= F_TMEM, "tensor memory budget");
+  using S = FSmem<SILU, FBN, FSTAGES>;
   extern __shared__ uint8_t smem_raw[];
   S& sm = *reinterpret_cast<S*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                 ~static_cast<uintptr_t>(1023));
@@ -131,13 +130,13 @@ __global__ void __launch_bounds__(FT, 1)
 
   if (warp == 0 && lane == 0) {
     ptx::prefetch_tensormap(&maps.w);
-    ptx::prefetch_tensormap(&maps.sw);
     for (int i = 0; i < NXBOX; ++i) {
       ptx::prefetch_tensormap(&maps.x[i]);
       ptx::prefetch_tensormap(&maps.sx[i]);
     }
     for (int s = 0; s < FSTAGES; ++s) {
       ptx::mbar_init(&sm.full[s], 1);
+      ptx::mbar_init(&sm.sready[s], 4);  // one arrival per scale warp
       ptx::mbar_init(&sm.empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -174,7 +173,8 @@ __global__ void __launch_bounds__(FT, 1)
       for (int g = blockIdx.x; ok && g < total; g += gridDim.x) {
         const TileInfo<FBN> t = decode_tile<FBN>(sm, E, p.NB, g);
         const int rows = (t.ntok + 15) & ~15;
-        const uint32_t bytes = W_BYTES + BM * SFROW + (uint32_t)rows * (BK + SFROW);
+        const uint32_t bytes = W_BYTES + 4 * 512 + (uint32_t)rows * (BK + SFROW);
+        const uint8_t* sba = p.sba + (((int64_t)t.e * p.NB + t.nb) * p.KB) * 2048;
         const int y0 = t.e * p.N + t.nb * BM;  // bf16 epilogue: first weight row
         const uint64_t pw = t.nch == 1 ? pol_w1 : pol_w;
         for (int ks = 0; ks < KS; ++ks) {
@@ -185,13 +185,11 @@ __global__ void __launch_bounds__(FT, 1)
           ptx::mbar_arrive_expect_tx(&sm.full[s], bytes);
           armed |= 1u << s;
           armed_par = (armed_par & ~(1u << s)) | (ph << s);
-          if (SILU) {
+          if (SILU)
             ptx::tma_load_5d(sm.w[s], &maps.w, &sm.full[s], 0, t.nb * 64, 0, ks, t.e, pw);
-            ptx::tma_load_4d(sm.sw[s], &maps.sw, &sm.full[s], ks * SFROW, t.nb * 64, 0, t.e, pw);
-          } else {
+          else
             ptx::tma_load_3d(sm.w[s], &maps.w, &sm.full[s], 0, y0, ks, pw);
-            ptx::tma_load_2d(sm.sw[s], &maps.sw, &sm.full[s], ks * SFROW, y0, pw);
-          }
+          ptx::bulk_load(sm.atom_a[s], sba + (int64_t)ks * 2048, 4 * 512, &sm.full[s], pw);
           int r = 0;
 #pragma unroll
           for (int i = 0; i < NXBOX; ++i) {
@@ -216,40 +214,35 @@ __global__ void __launch_bounds__(FT, 1)
       }
     }
   } else if (warp == 1) {
-    // ======================= scales + MMA ===================================
-    uint32_t s = 0, ph = 0;
-    bool ok = true, issued = false;
-    int iter = 0;
-    for (int g = blockIdx.x; ok && g < total; g += gridDim.x, ++iter) {
-      const TileInfo<FBN> t = decode_tile<FBN>(sm, E, p.NB, g);
-      const int n_mma = (t.ntok + 15) & ~15;
-      const uint32_t idesc = ptx::idesc_nvfp4(BM, n_mma);
-      const int b = iter & 1;
-      const uint32_t tph = (iter >> 1) & 1;
-      if (!__all_sync(kFull, ptx::mbar_wait(&sm.tempty[b], tph ^ 1u, &sm.abort, WAIT_NS))) {
-        ok = false;
-        break;
-      }
-      ptx::tc_fence_after();
-      const uint32_t d = tmem + (uint32_t)b * F_ACC;
-      for (int ks = 0; ks < KS; ++ks) {
-        if (!__all_sync(kFull, ptx::mbar_wait(&sm.full[s], ph, &sm.abort, WAIT_NS))) {
+    // ======================= MMA issuer =====================================
+    if (lane == 0) {
+      uint32_t s = 0, ph = 0;
+      bool ok = true, issued = false;
+      int iter = 0;
+      for (int g = blockIdx.x; ok && g < total; g += gridDim.x, ++iter) {
+        const TileInfo<FBN> t = decode_tile<FBN>(sm, E, p.NB, g);
+        const int n_mma = (t.ntok + 15) & ~15;
+        const uint32_t idesc = ptx::idesc_nvfp4(BM, n_mma);
+        const int b = iter & 1;
+        const uint32_t tph = (iter >> 1) & 1;
+        if (!ptx::mbar_wait(&sm.tempty[b], tph ^ 1u, &sm.abort, WAIT_NS)) {
           ok = false;
           break;
         }
-        arrange_scales(reinterpret_cast<const uint32_t*>(sm.sw[s]), sm.atom_a[s], lane);
-        arrange_scales(reinterpret_cast<const uint32_t*>(sm.sx[s]), sm.atom_b[s], lane);
-        ptx::fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
+        ptx::tc_fence_after();
+        const uint32_t d = tmem + (uint32_t)b * F_ACC;
+        for (int ks = 0; ks < KS; ++ks) {
+          if (!ptx::mbar_wait(&sm.full[s], ph, &sm.abort, WAIT_NS) ||
+              !ptx::mbar_wait(&sm.sready[s], ph, &sm.abort, WAIT_NS)) {
+            ok = false;
+            break;
+          }
           ptx::tc_fence_after();
           const uint32_t sfa = tmem + F_SF0 + (uint32_t)s * F_SFSTAGE;
           const uint32_t sfb = sfa + 16;
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
+          for (int j = 0; j < 4; ++j)
             ptx::tmem_cp_32x128b_x4(sfa + 4 * j, ptx::sdesc_rows16(ptx::smem_u32(sm.atom_a[s][j])));
-            ptx::tmem_cp_32x128b_x4(sfb + 4 * j, ptx::sdesc_rows16(ptx::smem_u32(sm.atom_b[s][j])));
-          }
           const uint32_t a0 = ptx::smem_u32(sm.w[s]);
           const uint32_t b0 = ptx::smem_u32(sm.x[s]);
 #pragma unroll
@@ -257,26 +250,64 @@ __global__ void __launch_bounds__(FT, 1)
             ptx::mma_nvfp4(d, ptx::sdesc_sw128(a0 + j * 32), ptx::sdesc_sw128(b0 + j * 32), idesc,
                            sfa + 4 * j, sfb + 4 * j, (ks | j) != 0 ? 1u : 0u);
           ptx::mma_commit(&sm.empty[s]);
+          issued = true;
+          if (++s == FSTAGES) {
+            s = 0;
+            ph ^= 1u;
+          }
         }
+        if (!ok) break;
+        ptx::mma_commit(&sm.tfull[b]);
+      }
+      if (!ok) {
+        sm.abort = 1;
+        flag_error(p.err, MOE_DEV_PIPE_TIMEOUT);
+        if (issued) {
+          ptx::mma_commit(&sm.drain);
+          ptx::mbar_wait(&sm.drain, 0, &sm.never, DRAIN_NS);
+        }
+      }
+    }
+  } else if (warp >= SCALE_WARP0) {
+    // ======================= token scales (warps 6..9) ======================
+    // lane i of this warp's quadrant, register 4j + c: the four scales of MMA
+    // step j of token row i + 32c (rows past the tile: zero)
+    const uint32_t tq = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    uint32_t s = 0, ph = 0;
+    bool ok = true;
+    for (int g = blockIdx.x; ok && g < total; g += gridDim.x) {
+      for (int ks = 0; ks < KS; ++ks) {
+        if (!__all_sync(kFull, ptx::mbar_wait(&sm.full[s], ph, &sm.abort, WAIT_NS))) {
+          ok = false;
+          break;
+        }
+        uint32_t r[16];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int row = lane + 32 * c;
+          uint4 v = make_uint4(0u, 0u, 0u, 0u);
+          if (row < FBN) v = *reinterpret_cast<const uint4*>(sm.sx[s] + row * SFROW);
+          r[c] = v.x;
+          r[4 + c] = v.y;
+          r[8 + c] = v.z;
+          r[12 + c] = v.w;
+        }
+        ptx::tmem_st_32x32b_x16(tq + F_SF0 + (uint32_t)s * F_SFSTAGE + 16, r);
+        ptx::tmem_st_wait();
+        ptx::tc_fence_before();
         __syncwarp();
-        issued = true;
+        if (lane == 0) ptx::mbar_arrive(&sm.sready[s]);
         if (++s == FSTAGES) {
           s = 0;
           ph ^= 1u;
         }
       }
-      if (!ok) break;
-      if (lane == 0) ptx::mma_commit(&sm.tfull[b]);
     }
     if (!ok && lane == 0) {
       sm.abort = 1;
       flag_error(p.err, MOE_DEV_PIPE_TIMEOUT);
-      if (issued) {
-        ptx::mma_commit(&sm.drain);
-        ptx::mbar_wait(&sm.drain, 0, &sm.never, DRAIN_NS);
-      }
     }
-  } else {
+  } else if (warp >= 2 && warp <= 5) {
     // ======================= epilogue (warps 2..5) ==========================
     const int q = warp & 3;
     int iter = 0;
@@ -395,12 +426,12 @@ __global__ void __launch_bounds__(FT, 1)
   }
 }
 
-template <bool SILU>
+template <bool SILU, int FBN, int FSTAGES>
 cudaError_t launch_f(const FMaps& maps, const FParams& p, int M, int E, cudaStream_t st,
                      bool pdl) {
-  constexpr size_t smem = sizeof(FSmem<SILU>) + 1024;
+  constexpr size_t smem = sizeof(FSmem<SILU, FBN, FSTAGES>) + 1024;
   static_assert(smem <= 227 * 1024, "shared memory budget");
-  auto kern = grouped_gemm_nvfp4_kernel<SILU>;
+  auto kern = grouped_gemm_nvfp4_kernel<SILU, FBN, FSTAGES>;
   static std::mutex mu;
   static bool attr_set[64] = {};
   int dev = 0;
@@ -419,7 +450,46 @@ cudaError_t launch_f(const FMaps& maps, const FParams& p, int M, int E, cudaStre
   return launch_kernel(kern, dim3(grid), dim3(FT), smem, st, pdl, maps, p);
 }
 
+// Weight scales sb [E][N][Kd/16] -> the kernel's copy order: for expert e,
+// weight tile nb, K chunk c, MMA step j: 512 bytes, byte 16*(m%32) +
+// 4*(m/32) + b = scale 4j+b of chunk c of the tile's row m (SiLU tiles: rows
+// m < 64 are gate rows 64nb+m, the rest up rows I+64nb+m-64). One thread
+// per (e, nb, c, m).
+__global__ void arrange_scales_kernel(const uint8_t* __restrict__ sb, int E, int N, int KB,
+                                      int silu, uint8_t* __restrict__ out) {
+  const int NB = silu ? N / 2 / 64 : N / BM;
+  const int64_t n = (int64_t)E * NB * KB * BM;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int m = (int)(i % BM);
+    const int64_t tc = i / BM;  // (e, nb, c)
+    const int c = (int)(tc % KB);
+    const int64_t enb = tc / KB;
+    const int nb = (int)(enb % NB);
+    const int e = (int)(enb / NB);
+    const int I = N / 2;
+    const int row = silu ? (m < 64 ? nb * 64 + m : I + nb * 64 + (m - 64)) : nb * BM + m;
+    const uint32_t* src = reinterpret_cast<const uint32_t*>(
+        sb + ((int64_t)e * N + row) * (KB * 16) + (int64_t)c * 16);
+    uint32_t* dst = reinterpret_cast<uint32_t*>(out + tc * 2048);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) dst[j * 128 + (m % 32) * 4 + (m / 32)] = __ldg(src + j);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_nvfp4_arrange_scales(const uint8_t* sb, int E, int N, int Kd, int epilogue,
+                                        uint8_t* out, cudaStream_t st) {
+  const bool silu = epilogue == MOE_EPI_SILU_MUL;
+  const int KB = Kd / 256;
+  const int NB = silu ? N / 2 / 64 : N / BM;
+  const int64_t n = (int64_t)E * NB * KB * BM;
+  if (n == 0) return cudaSuccess;
+  const int blocks = (int)std::min<int64_t>((n + 255) / 256, (int64_t)sm_count() * 32);
+  arrange_scales_kernel<<<blocks, 256, 0, st>>>(sb, E, N, KB, silu ? 1 : 0, out);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_grouped_gemm_nvfp4(const void* A, const uint8_t* sfa, float ga, const void* B,
                                       const uint8_t* sfb, const float* gb,
@@ -431,8 +501,7 @@ cudaError_t launch_grouped_gemm_nvfp4(const void* A, const uint8_t* sfa, float g
   const uint64_t kb = (uint64_t)Kd / 2;   // bytes of a row
   const uint64_t sc = (uint64_t)Kd / 16;  // scale bytes of a row
   FMaps maps;
-  if (!make_tma_map_weights(&maps.w, B, silu, (uint64_t)E, (uint64_t)N, kb, 1) ||
-      !make_tma_map_weight_scales(&maps.sw, sfb, silu, (uint64_t)E, (uint64_t)N, sc))
+  if (!make_tma_map_weights(&maps.w, B, silu, (uint64_t)E, (uint64_t)N, kb, 1))
     return cudaErrorNotSupported;
   for (int i = 0; i < NXBOX; ++i)
     if (!make_tma_map_u8(&maps.x[i], A, (uint64_t)M, kb, 64u >> i) ||
@@ -441,6 +510,7 @@ cudaError_t launch_grouped_gemm_nvfp4(const void* A, const uint8_t* sfa, float g
   FParams p;
   p.ga = ga;
   p.gb = gb;
+  p.sba = sfb;
   p.offsets = offsets;
   p.C = C;
   p.err = err;
@@ -451,9 +521,14 @@ cudaError_t launch_grouped_gemm_nvfp4(const void* A, const uint8_t* sfa, float g
   p.I = N / 2;
   p.NB = silu ? p.I / 64 : N / BM;
   p.KB = Kd / 256;
-  p.stream_weights = gemm_many_rows(M, E) ? 0 : 1;
+  const bool many = gemm_many_rows(M, E);
+  p.stream_weights = many ? 0 : 1;
   p.early_table = early_table ? 1 : 0;
-  return silu ? launch_f<true>(maps, p, M, E, st, pdl) : launch_f<false>(maps, p, M, E, st, pdl);
+  if (!many)
+    return silu ? launch_f<true, 64, 6>(maps, p, M, E, st, pdl)
+                : launch_f<false, 64, 6>(maps, p, M, E, st, pdl);
+  return silu ? launch_f<true, 128, 5>(maps, p, M, E, st, pdl)
+              : launch_f<false, 128, 5>(maps, p, M, E, st, pdl);
 }
 
 }  // namespace moe

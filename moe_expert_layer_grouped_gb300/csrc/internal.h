@@ -89,9 +89,12 @@ cudaError_t launch_act_quant_nvfp4(const void* h, int M, int I, float g, void* q
                                    cudaStream_t st, bool pdl = false);
 
 // gemm_nvfp4.cu: NVFP4 grouped GEMM. A [M, Kd/2] and B [E, N, Kd/2] packed
-// E2M1 (Kd % 256 == 0), sfa [M, Kd/16] and sfb [E, N, Kd/16] E4M3 block
-// scales, ga and gb [E] fp32 global scales; acc * ga * gb[e] then the
-// epilogue of launch_grouped_gemm (no row amax).
+// E2M1 (Kd % 256 == 0), sfa [M, Kd/16] E4M3 block scales, sfb the weights'
+// scales arranged by launch_nvfp4_arrange_scales, ga and gb [E] fp32 global
+// scales; acc * ga * gb[e] then the epilogue of launch_grouped_gemm (no row
+// amax).
+cudaError_t launch_nvfp4_arrange_scales(const uint8_t* sb, int E, int N, int Kd, int epilogue,
+                                        uint8_t* out, cudaStream_t st);
 cudaError_t launch_grouped_gemm_nvfp4(const void* A, const uint8_t* sfa, float ga, const void* B,
                                       const uint8_t* sfb, const float* gb,
                                       const int32_t* offsets, int M, int N, int Kd, int E,

@@ -55,10 +55,10 @@ def gemm_token_tile(M, E, quant="token"):
     expert (M <= 32*E) take 64-token tiles on single CTAs; otherwise the
     per-token GEMM takes 256-token tiles on CTA pairs (every workload here has
     an even number of weight blocks) and the block-scaled GEMM 128-token
-    tiles on single CTAs. The NVFP4 GEMM takes 128-token tiles on single
-    CTAs at every size."""
+    tiles on single CTAs. The NVFP4 GEMM takes 64- or 128-token tiles on
+    single CTAs."""
     if quant == "nvfp4":
-        return 128, False
+        return (64 if M <= 32 * E else 128), False
     if M <= 32 * E:
         return 64, False
     return (256, True) if quant == "token" else (128, False)

@@ -111,8 +111,34 @@ def _fp4_problem(rng, counts, N, Kd):
 def _run_fp4(A, sa, ga, B, sb, gb, off, epi):
     pa = synth.pack_e2m1(torch.from_numpy(A))
     pb = synth.pack_e2m1(torch.from_numpy(B))
-    return moe.moe_grouped_gemm_nvfp4(pa.to(DEV), _t(sa), ga, pb.to(DEV), _t(sb), _t(gb),
+    sba = moe.moe_nvfp4_arrange_scales(_t(sb), epi)
+    return moe.moe_grouped_gemm_nvfp4(pa.to(DEV), _t(sa), ga, pb.to(DEV), sba, _t(gb),
                                       _t(off), epi)
+
+
+@pytest.mark.parametrize("silu", [False, True])
+def test_arranged_scales_follow_their_definition(silu):
+    """Every scale byte lands where the header says (the copy order of the
+    GEMM): block (e, nb, c, j), byte 16*(m%32) + 4*(m/32) + b."""
+    rng = np.random.default_rng(2)
+    E, N, Kd = 3, 256, 512
+    sb = rng.integers(0, 256, (E, N, Kd // 16)).astype(np.uint8)
+    epi = moe.EPI_SILU_MUL if silu else moe.EPI_BF16
+    got = moe.moe_nvfp4_arrange_scales(_t(sb), epi).cpu().numpy().reshape(-1)
+    I, KB = N // 2, Kd // 256
+    NB = I // 64 if silu else N // 128
+    exp = np.empty_like(got)
+    for e in range(E):
+        for nb in range(NB):
+            for m in range(128):
+                row = (64 * nb + m if m < 64 else I + 64 * nb + m - 64) if silu else 128 * nb + m
+                for c in range(KB):
+                    base = ((e * NB + nb) * KB + c) * 2048
+                    for j in range(4):
+                        for b in range(4):
+                            exp[base + 512 * j + 16 * (m % 32) + 4 * (m // 32) + b] = \
+                                sb[e, row, 16 * c + 4 * j + b]
+    assert np.array_equal(got, exp)
 
 
 def test_nvfp4_gemm_one_tile():
