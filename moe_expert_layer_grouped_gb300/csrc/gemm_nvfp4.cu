@@ -26,11 +26,13 @@
 //               (lane i, column 4j + c: the four scales of MMA step j of token
 //               row i + 32c, the same in every quadrant) and signals the MMA
 //               thread.
-//   warp 1      MMA: lane 0 copies the stage's four weight-scale blocks
-//               (tcgen05.cp.32x128b.warpx4; block j: bytes of row m0 + 32*m1
-//               at offset 16*m0 + 4*m1, replicated into the four quadrants)
-//               and issues the four MMAs of the chunk, each reading its scales
-//               from four tensor-memory columns.
+//               Lane 0 of warp 6 also copies the stage's four weight-scale
+//               blocks (tcgen05.cp.32x128b.warpx4; block j: bytes of row
+//               m0 + 32*m1 at offset 16*m0 + 4*m1, replicated into the four
+//               quadrants), its commit being the last arrival the MMA thread
+//               waits for.
+//   warp 1      MMA: lane 0 issues the four MMAs of the chunk, each reading
+//               its scales from four tensor-memory columns.
 // Token scales go from registers to tensor memory rather than through a
 // rearranged shared-memory block copied by tcgen05.cp: generic-proxy stores
 // followed by a tcgen05.cp of the same bytes cost about 40 % of the decode
@@ -91,6 +93,7 @@ struct FSmem {
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t drain;
+  uint64_t sdrain;  // the weight-scale copies, before the teardown
   uint32_t tmem_base;
   int abort;
   int total_tiles;
@@ -136,7 +139,8 @@ __global__ void __launch_bounds__(FT, 1)
     }
     for (int s = 0; s < FSTAGES; ++s) {
       ptx::mbar_init(&sm.full[s], 1);
-      ptx::mbar_init(&sm.sready[s], 4);  // one arrival per scale warp
+      // one arrival per scale warp and the commit of the weight-scale copies
+      ptx::mbar_init(&sm.sready[s], 5);
       ptx::mbar_init(&sm.empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -144,6 +148,7 @@ __global__ void __launch_bounds__(FT, 1)
       ptx::mbar_init(&sm.tempty[b], 128);
     }
     ptx::mbar_init(&sm.drain, 1);
+    ptx::mbar_init(&sm.sdrain, 1);
     sm.abort = 0;
     sm.never = 0;
     ptx::fence_mbar_init();
@@ -240,9 +245,6 @@ __global__ void __launch_bounds__(FT, 1)
           ptx::tc_fence_after();
           const uint32_t sfa = tmem + F_SF0 + (uint32_t)s * F_SFSTAGE;
           const uint32_t sfb = sfa + 16;
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            ptx::tmem_cp_32x128b_x4(sfa + 4 * j, ptx::sdesc_rows16(ptx::smem_u32(sm.atom_a[s][j])));
           const uint32_t a0 = ptx::smem_u32(sm.w[s]);
           const uint32_t b0 = ptx::smem_u32(sm.x[s]);
 #pragma unroll
@@ -281,6 +283,16 @@ __global__ void __launch_bounds__(FT, 1)
           ok = false;
           break;
         }
+        if (warp == SCALE_WARP0 && lane == 0) {
+          // the weights' scale blocks into the stage's columns, ahead of the
+          // MMAs; the commit is the fifth arrival on sready
+          ptx::tc_fence_after();
+          const uint32_t sfa = tmem + F_SF0 + (uint32_t)s * F_SFSTAGE;
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            ptx::tmem_cp_32x128b_x4(sfa + 4 * j, ptx::sdesc_rows16(ptx::smem_u32(sm.atom_a[s][j])));
+          ptx::mma_commit(&sm.sready[s]);
+        }
         uint32_t r[16];
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
@@ -303,9 +315,17 @@ __global__ void __launch_bounds__(FT, 1)
         }
       }
     }
-    if (!ok && lane == 0) {
-      sm.abort = 1;
-      flag_error(p.err, MOE_DEV_PIPE_TIMEOUT);
+    if (lane == 0) {
+      if (!ok) {
+        sm.abort = 1;
+        flag_error(p.err, MOE_DEV_PIPE_TIMEOUT);
+      }
+      // the copies this thread issued land before the tensor memory is freed
+      // (at once when the MMA thread has waited for them all)
+      if (warp == SCALE_WARP0) {
+        ptx::mma_commit(&sm.sdrain);
+        ptx::mbar_wait(&sm.sdrain, 0, &sm.never, DRAIN_NS);
+      }
     }
   } else if (warp >= 2 && warp <= 5) {
     // ======================= epilogue (warps 2..5) ==========================
