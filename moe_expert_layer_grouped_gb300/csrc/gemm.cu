@@ -720,6 +720,17 @@ bool make_tma_map_weight_scales(CUtensorMap* m, const void* base, bool silu, uin
   return encode_u8(m, base, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
+bool make_tma_map_weights_pairs32(CUtensorMap* m, const void* base, uint64_t E, uint64_t N,
+                                  uint64_t Kd) {
+  // [E][Kd/128][2][I][128] (as the SiLU stage view), boxes of 32 gate rows
+  // then the matching 32 up rows of one 128-byte chunk
+  const uint64_t I = N / 2, KB = Kd / BK;
+  const cuuint64_t dims[5] = {BK, I, 2, KB, E};
+  const cuuint64_t strides[4] = {Kd, I * Kd, BK, 2 * I * Kd};
+  const cuuint32_t box[5] = {BK, 32, 2, 1, 1};
+  return encode_u8(m, base, 5, dims, strides, box);
+}
+
 bool make_tma_map_rows(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols) {
   const cuuint64_t dims[2] = {cols, rows};
   const cuuint64_t strides[1] = {cols};

@@ -162,6 +162,11 @@ bool make_tma_map_u8(CUtensorMap* m, const void* base, uint64_t rows, uint64_t c
 // swizzle, zero fill) for four-row gathers.
 bool make_tma_map_rows(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols);
 
+// Host: w13 [E, 2I, Kd] (Kd % 128 == 0) viewed per 128-byte K chunk, boxes of
+// 32 gate rows followed by the matching 32 up rows.
+bool make_tma_map_weights_pairs32(CUtensorMap* m, const void* base, uint64_t E, uint64_t N,
+                                  uint64_t Kd);
+
 // Host: block-scale maps (no swizzle, boxes 16 bytes wide): a [rows, cols]
 // byte tensor with box_rows rows per box, and the weights' [E, N, cols]
 // scales with 128-row boxes (silu: 64 gate rows then the matching 64 up
