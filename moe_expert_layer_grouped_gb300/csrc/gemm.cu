@@ -720,6 +720,16 @@ bool make_tma_map_weight_scales(CUtensorMap* m, const void* base, bool silu, uin
   return encode_u8(m, base, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
+bool make_tma_map_weights_rows(CUtensorMap* m, const void* base, uint64_t E, uint64_t N,
+                               uint64_t Kd, uint32_t rows) {
+  // [Kd/128][E*N][128]: one 128-byte K chunk of `rows` consecutive rows per box
+  const uint64_t KB = Kd / BK;
+  const cuuint64_t dims[3] = {BK, E * N, KB};
+  const cuuint64_t strides[2] = {Kd, BK};
+  const cuuint32_t box[3] = {BK, rows, 1};
+  return encode_u8(m, base, 3, dims, strides, box);
+}
+
 bool make_tma_map_weights_pairs32(CUtensorMap* m, const void* base, uint64_t E, uint64_t N,
                                   uint64_t Kd) {
   // [E][Kd/128][2][I][128] (as the SiLU stage view), boxes of 32 gate rows

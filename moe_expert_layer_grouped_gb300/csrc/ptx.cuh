@@ -250,6 +250,21 @@ __device__ __forceinline__ void tmem_relinquish() {
   asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
 }
 
+// Warpgroup register reallocation: every warp of the warpgroup executes it.
+// The increases of a CTA must be covered by its decreases and the registers
+// it was launched with, else the increase waits.
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  static_assert(N % 8 == 0 && N >= 24 && N <= 256, "setmaxnreg range");
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  static_assert(N % 8 == 0 && N >= 24 && N <= 256, "setmaxnreg range");
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
   asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
                : "memory");
@@ -420,6 +435,18 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)
       : "memory");
 }
 
+// 16 consecutive fp32 columns of this warp's 32 TMEM lanes (as the x32 form).
+__device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+
 // Writes r[0..15] of each lane into 16 consecutive TMEM columns from taddr,
 // lane quadrant of the calling warp (lanes 32*(warp%4) ..); visible to later
 // tcgen05 operations after tmem_st_wait() and a thread-sync fence.
@@ -452,6 +479,150 @@ __device__ __forceinline__ void reg_fence(uint32_t (&r)[32]) {
                  "+r"(r[30]), "+r"(r[31])
                :
                : "memory");
+}
+
+__device__ __forceinline__ void reg_fence(uint32_t (&r)[16]) {
+  asm volatile(""
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                 "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                 "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
+               :
+               : "memory");
+}
+
+// Loads 16 TMEM columns (32x32b.x16) into nxt, folds cur into acc
+// (acc[i] += cur[i] * f, fp32 FMAs in pairs) while the load is in flight,
+// then waits for the load. One asm statement, so nothing can read nxt
+// before the wait; nxt is read-write so that it never shares a register
+// with cur or acc.
+__device__ __forceinline__ void tmem_ld_fold_x16(uint32_t taddr, uint32_t (&nxt)[16],
+                                                const uint32_t (&cur)[16], float (&acc)[16],
+                                                float f) {
+  asm volatile(
+      "{\n\t.reg .b64 fp, x, y;\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%49];\n\t"
+      "mov.b64 fp, {%48, %48};\n\t"
+      "mov.b64 x, {%32, %33};\n\tmov.b64 y, {%16, %17};\n\t"
+      "fma.rn.f32x2 y, x, fp, y;\n\tmov.b64 {%16, %17}, y;\n\t"
+      "mov.b64 x, {%34, %35};\n\tmov.b64 y, {%18, %19};\n\t"
+      "fma.rn.f32x2 y, x, fp, y;\n\tmov.b64 {%18, %19}, y;\n\t"
+      "mov.b64 x, {%36, %37};\n\tmov.b64 y, {%20, %21};\n\t"
+      "fma.rn.f32x2 y, x, fp, y;\n\tmov.b64 {%20, %21}, y;\n\t"
+      "mov.b64 x, {%38, %39};\n\tmov.b64 y, {%22, %23};\n\t"
+      "fma.rn.f32x2 y, x, fp, y;\n\tmov.b64 {%22, %23}, y;\n\t"
+      "mov.b64 x, {%40, %41};\n\tmov.b64 y, {%24, %25};\n\t"
+      "fma.rn.f32x2 y, x, fp, y;\n\tmov.b64 {%24, %25}, y;\n\t"
+      "mov.b64 x, {%42, %43};\n\tmov.b64 y, {%26, %27};\n\t"
+      "fma.rn.f32x2 y, x, fp, y;\n\tmov.b64 {%26, %27}, y;\n\t"
+      "mov.b64 x, {%44, %45};\n\tmov.b64 y, {%28, %29};\n\t"
+      "fma.rn.f32x2 y, x, fp, y;\n\tmov.b64 {%28, %29}, y;\n\t"
+      "mov.b64 x, {%46, %47};\n\tmov.b64 y, {%30, %31};\n\t"
+      "fma.rn.f32x2 y, x, fp, y;\n\tmov.b64 {%30, %31}, y;\n\t"
+      "tcgen05.wait::ld.sync.aligned;\n\t}"
+      : "+r"(nxt[0]), "+r"(nxt[1]), "+r"(nxt[2]), "+r"(nxt[3]), "+r"(nxt[4]), "+r"(nxt[5]), "+r"(nxt[6]), "+r"(nxt[7]), "+r"(nxt[8]), "+r"(nxt[9]), "+r"(nxt[10]), "+r"(nxt[11]), "+r"(nxt[12]), "+r"(nxt[13]), "+r"(nxt[14]), "+r"(nxt[15]), "+f"(acc[0]), "+f"(acc[1]), "+f"(acc[2]), "+f"(acc[3]), "+f"(acc[4]), "+f"(acc[5]), "+f"(acc[6]), "+f"(acc[7]), "+f"(acc[8]), "+f"(acc[9]), "+f"(acc[10]), "+f"(acc[11]), "+f"(acc[12]), "+f"(acc[13]), "+f"(acc[14]), "+f"(acc[15])
+      : "r"(cur[0]), "r"(cur[1]), "r"(cur[2]), "r"(cur[3]), "r"(cur[4]), "r"(cur[5]), "r"(cur[6]), "r"(cur[7]), "r"(cur[8]), "r"(cur[9]), "r"(cur[10]), "r"(cur[11]), "r"(cur[12]), "r"(cur[13]), "r"(cur[14]), "r"(cur[15]), "f"(f), "r"(taddr)
+      : "memory");
+}
+
+
+__device__ __forceinline__ void tmem_ld_fold_x32(uint32_t taddr, uint32_t (&nxt)[32],
+                                                const uint32_t (&cur)[32], float (&acc)[32],
+                                                float f) {
+  asm volatile(
+      "{\n\t.reg .b64 fp, x, y;\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%97];\n\t"
+      "mov.b64 fp, {%96, %96};\n\t"
+      "mov.b64 x, {%64, %65};\n\tmov.b64 y, {%32, %33};\n\t"
+      "fma.rn.f32x2 y, x, fp, y;\n\tmov.b64 {%32, %33}, y;\n\t"
+      "mov.b64 x, {%66, %67};\n\tmov.b64 y, {%34, %35};\n\t"
+      "fma.rn.f32x2 y, x, fp, y;\n\tmov.b64 {%34, %35}, y;\n\t"
+      "mov.b64 x, {%68, %69};\n\tmov.b64 y, {%36, %37};\n\t"
+      "fma.rn.f32x2 y, x, fp, y;\n\tmov.b64 {%36, %37}, y;\n\t"
+      "mov.b64 x, {%70, %71};\n\tmov.b64 y, {%38, %39};\n\t"
+      "fma.rn.f32x2 y, x, fp, y;\n\tmov.b64 {%38, %39}, y;\n\t"
+      "mov.b64 x, {%72, %73};\n\tmov.b64 y, {%40, %41};\n\t"
+      "fma.rn.f32x2 y, x, fp, y;\n\tmov.b64 {%40, %41}, y;\n\t"
+      "mov.b64 x, {%74, %75};\n\tmov.b64 y, {%42, %43};\n\t"
+      "fma.rn.f32x2 y, x, fp, y;\n\tmov.b64 {%42, %43}, y;\n\t"
+      "mov.b64 x, {%76, %77};\n\tmov.b64 y, {%44, %45};\n\t"
+      "fma.rn.f32x2 y, x, fp, y;\n\tmov.b64 {%44, %45}, y;\n\t"
+      "mov.b64 x, {%78, %79};\n\tmov.b64 y, {%46, %47};\n\t"
+      "fma.rn.f32x2 y, x, fp, y;\n\tmov.b64 {%46, %47}, y;\n\t"
+      "mov.b64 x, {%80, %81};\n\tmov.b64 y, {%48, %49};\n\t"
+      "fma.rn.f32x2 y, x, fp, y;\n\tmov.b64 {%48, %49}, y;\n\t"
+      "mov.b64 x, {%82, %83};\n\tmov.b64 y, {%50, %51};\n\t"
+      "fma.rn.f32x2 y, x, fp, y;\n\tmov.b64 {%50, %51}, y;\n\t"
+      "mov.b64 x, {%84, %85};\n\tmov.b64 y, {%52, %53};\n\t"
+      "fma.rn.f32x2 y, x, fp, y;\n\tmov.b64 {%52, %53}, y;\n\t"
+      "mov.b64 x, {%86, %87};\n\tmov.b64 y, {%54, %55};\n\t"
+      "fma.rn.f32x2 y, x, fp, y;\n\tmov.b64 {%54, %55}, y;\n\t"
+      "mov.b64 x, {%88, %89};\n\tmov.b64 y, {%56, %57};\n\t"
+      "fma.rn.f32x2 y, x, fp, y;\n\tmov.b64 {%56, %57}, y;\n\t"
+      "mov.b64 x, {%90, %91};\n\tmov.b64 y, {%58, %59};\n\t"
+      "fma.rn.f32x2 y, x, fp, y;\n\tmov.b64 {%58, %59}, y;\n\t"
+      "mov.b64 x, {%92, %93};\n\tmov.b64 y, {%60, %61};\n\t"
+      "fma.rn.f32x2 y, x, fp, y;\n\tmov.b64 {%60, %61}, y;\n\t"
+      "mov.b64 x, {%94, %95};\n\tmov.b64 y, {%62, %63};\n\t"
+      "fma.rn.f32x2 y, x, fp, y;\n\tmov.b64 {%62, %63}, y;\n\t"
+      "tcgen05.wait::ld.sync.aligned;\n\t}"
+      : "+r"(nxt[0]), "+r"(nxt[1]), "+r"(nxt[2]), "+r"(nxt[3]), "+r"(nxt[4]), "+r"(nxt[5]), "+r"(nxt[6]), "+r"(nxt[7]), "+r"(nxt[8]), "+r"(nxt[9]), "+r"(nxt[10]), "+r"(nxt[11]), "+r"(nxt[12]), "+r"(nxt[13]), "+r"(nxt[14]), "+r"(nxt[15]), "+r"(nxt[16]), "+r"(nxt[17]), "+r"(nxt[18]), "+r"(nxt[19]), "+r"(nxt[20]), "+r"(nxt[21]), "+r"(nxt[22]), "+r"(nxt[23]), "+r"(nxt[24]), "+r"(nxt[25]), "+r"(nxt[26]), "+r"(nxt[27]), "+r"(nxt[28]), "+r"(nxt[29]), "+r"(nxt[30]), "+r"(nxt[31]), "+f"(acc[0]), "+f"(acc[1]), "+f"(acc[2]), "+f"(acc[3]), "+f"(acc[4]), "+f"(acc[5]), "+f"(acc[6]), "+f"(acc[7]), "+f"(acc[8]), "+f"(acc[9]), "+f"(acc[10]), "+f"(acc[11]), "+f"(acc[12]), "+f"(acc[13]), "+f"(acc[14]), "+f"(acc[15]), "+f"(acc[16]), "+f"(acc[17]), "+f"(acc[18]), "+f"(acc[19]), "+f"(acc[20]), "+f"(acc[21]), "+f"(acc[22]), "+f"(acc[23]), "+f"(acc[24]), "+f"(acc[25]), "+f"(acc[26]), "+f"(acc[27]), "+f"(acc[28]), "+f"(acc[29]), "+f"(acc[30]), "+f"(acc[31])
+      : "r"(cur[0]), "r"(cur[1]), "r"(cur[2]), "r"(cur[3]), "r"(cur[4]), "r"(cur[5]), "r"(cur[6]), "r"(cur[7]), "r"(cur[8]), "r"(cur[9]), "r"(cur[10]), "r"(cur[11]), "r"(cur[12]), "r"(cur[13]), "r"(cur[14]), "r"(cur[15]), "r"(cur[16]), "r"(cur[17]), "r"(cur[18]), "r"(cur[19]), "r"(cur[20]), "r"(cur[21]), "r"(cur[22]), "r"(cur[23]), "r"(cur[24]), "r"(cur[25]), "r"(cur[26]), "r"(cur[27]), "r"(cur[28]), "r"(cur[29]), "r"(cur[30]), "r"(cur[31]), "f"(f), "r"(taddr)
+      : "memory");
+}
+
+
+// The x16 load and its wait in one statement: r is complete on return.
+__device__ __forceinline__ void tmem_ld_sync_x16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+
+// The x32 load and its wait in one statement: r is complete on return.
+__device__ __forceinline__ void tmem_ld_sync_x32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld_sync(uint32_t taddr, uint32_t (&r)[16]) {
+  tmem_ld_sync_x16(taddr, r);
+}
+__device__ __forceinline__ void tmem_ld_sync(uint32_t taddr, uint32_t (&r)[32]) {
+  tmem_ld_sync_x32(taddr, r);
+}
+__device__ __forceinline__ void tmem_ld_fold(uint32_t taddr, uint32_t (&nxt)[16],
+                                             const uint32_t (&cur)[16], float (&acc)[16],
+                                             float f) {
+  tmem_ld_fold_x16(taddr, nxt, cur, acc, f);
+}
+__device__ __forceinline__ void tmem_ld_fold(uint32_t taddr, uint32_t (&nxt)[32],
+                                             const uint32_t (&cur)[32], float (&acc)[32],
+                                             float f) {
+  tmem_ld_fold_x32(taddr, nxt, cur, acc, f);
+}
+
+// tmem_ld_32x32b_x16 / _x32 by the register count of the destination.
+__device__ __forceinline__ void tmem_ld_32x32b(uint32_t taddr, uint32_t (&r)[16]) {
+  tmem_ld_32x32b_x16(taddr, r);
+}
+__device__ __forceinline__ void tmem_ld_32x32b(uint32_t taddr, uint32_t (&r)[32]) {
+  tmem_ld_32x32b_x32(taddr, r);
 }
 
 }  // namespace ptx
