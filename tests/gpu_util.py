@@ -52,13 +52,15 @@ def random_e4m3(rng, shape):
 def gemm_token_tile(M, E, quant="token"):
     """Token tile of the grouped GEMM launch the library picks for M permuted
     rows over E experts: (most tokens per tile, CTA pair). Few rows per
-    expert (M <= 32*E) take 64-token tiles on single CTAs; otherwise the
-    per-token GEMM takes 256-token tiles on CTA pairs (every workload here has
-    an even number of weight blocks) and the block-scaled GEMM 128-token
-    tiles on single CTAs. The NVFP4 GEMM takes 64- or 128-token tiles on
-    single CTAs."""
+    expert (M <= 32*E) take 64-token tiles on single CTAs in the per-token
+    GEMM; otherwise it takes 256-token tiles on CTA pairs (every workload here
+    has an even number of weight blocks). The block-scaled GEMM always takes
+    128-token tiles (tokens are its MMA's M side) on single CTAs; the NVFP4
+    GEMM 64- or 128-token tiles on single CTAs."""
     if quant == "nvfp4":
         return (64 if M <= 32 * E else 128), False
+    if quant == "block":
+        return 128, False
     if M <= 32 * E:
         return 64, False
     return (256, True) if quant == "token" else (128, False)

@@ -38,6 +38,9 @@ def test_launch_shapes_follow_the_library():
     assert gemm_token_tile(128 * 8, 256) == (64, False)         # decode: M <= 32 E
     assert gemm_token_tile(8192 * 8, 256) == (256, True)        # prefill: CTA pairs
     assert gemm_token_tile(8192 * 8, 256, "block") == (128, False)
+    assert gemm_token_tile(128 * 8, 256, "block") == (128, False)   # tokens on M at any size
+    assert gemm_token_tile(128 * 8, 256, "nvfp4") == (64, False)
+    assert gemm_token_tile(8192 * 8, 256, "nvfp4") == (128, False)
 
 
 def test_prefill_sample_touches_every_expert_chunk():
