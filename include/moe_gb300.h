@@ -563,6 +563,77 @@ MOE_API moe_status moe_ep_combine(const void* back_rows, const int32_t* src2dst,
                               const float* topk_w, int T, int K, int H, void* out,
                               void* stream);
 
+/* ---- pipelined host batches --------------------------------------------------
+ * A serving loop feeds the layer batch after batch from host memory. Run one
+ * call at a time, batch i+1's inputs cross the host link only after batch i's
+ * output has come back, so the copies add to the compute. The pipelined entry
+ * point below runs n batches through the same forward as moe_forward /
+ * moe_forward_shared / moe_forward_block / moe_forward_nvfp4. Batch i+1's
+ * inputs are copied in, and batch i-1's output copied out, while batch i
+ * computes. Each batch's result is bit-identical to that batch run through
+ * the matching device entry point alone.
+ */
+typedef enum {
+  MOE_QUANT_TOKEN = 0, /* per-token FP8: moe_forward / moe_forward_shared */
+  MOE_QUANT_BLOCK = 1, /* block-quantised FP8: moe_forward_block */
+  MOE_QUANT_NVFP4 = 2  /* NVFP4: moe_forward_nvfp4 */
+} moe_quant;
+
+/* The layer a pipelined call runs: the arguments of the matching device
+ * entry point, by name. s13 / s2 are f32 (token, block) or the arranged
+ * E4M3 bytes of moe_nvfp4_arrange_scales (NVFP4); g13, g2, ga1 and ga2 are
+ * read for NVFP4 only. Every pointer is a device pointer; the caller keeps
+ * them valid while the call's work runs. */
+typedef struct moe_layer {
+  int quant; /* moe_quant */
+  int T, H, I, E, n_shared, num_groups, topk_group, top_k, scoring, renormalize;
+  float routed_scaling_factor;
+  const float* bias;
+  const void* w13;
+  const void* s13;
+  const void* w2;
+  const void* s2;
+  const float* g13;
+  const float* g2;
+  float ga1, ga2;
+} moe_layer;
+
+/* Workspace bytes moe_forward_host_pipelined needs for layer *L: the
+ * matching forward's workspace plus two device slots for a batch's x,
+ * logits and out. 0 if *L is invalid (NULL, an unknown quant or a size the
+ * forward's workspace function rejects). */
+MOE_API size_t moe_pipeline_workspace_size(const moe_layer* L);
+
+/*
+ * moe_forward_host_pipelined — n_batches forwards of layer *L over host
+ * buffers: x_host[i] [T,H] bf16 and logits_host[i] [T,E] f32 in,
+ * out_host[i] [T,H] bf16 out, for i = 0 .. n_batches-1.
+ *
+ * Streams. The forwards run on `stream`, in order. The copies into device
+ * slot i % 2 and back out run on two internal copy streams of the current
+ * device (created on first use and kept). Events order them:
+ * - slot i % 2 is refilled only after batch i-2's forward has read it;
+ * - batch i's forward waits for its inputs, and for batch i-2's output to
+ *   have left the slot.
+ * All of the call's work starts after the work already on `stream`, and
+ * `stream` reaches the end of the call only once every output has landed.
+ *
+ * Host buffers. They must be pinned for the copies to overlap the compute
+ * (pageable memory works, serialised) and stay valid until `stream` passes
+ * the call. The same buffer may appear in several batches.
+ *
+ * Errors. MOE_ERR_INVALID_ARG for a NULL array or entry, n_batches < 1 or a
+ * layer the forward rejects; MOE_ERR_WORKSPACE for a workspace below
+ * moe_pipeline_workspace_size(L) or not 256-byte aligned. These are
+ * returned before any work is queued. MOE_ERR_CUDA if a copy, event or
+ * launch fails part way; earlier batches' work may then already be queued.
+ */
+MOE_API moe_status moe_forward_host_pipelined(const moe_layer* L, int n_batches,
+                                              const void* const* x_host,
+                                              const float* const* logits_host,
+                                              void* const* out_host, void* ws,
+                                              size_t ws_bytes, void* stream);
+
 /*
  * moe_test_gemm_timeout — failure-detection test of the GEMM pipeline (the
  * pages have no counterpart). Runs moe_grouped_gemm, except that CTA 0 arms

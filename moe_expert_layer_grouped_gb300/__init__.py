@@ -25,7 +25,8 @@ __all__ = [
     "moe_nvfp4_workspace_size", "moe_forward_nvfp4", "moe_forward_nvfp4_host",
     "moe_nvfp4_arrange_scales",
     "moe_act_quant", "moe_unpermute_sum", "moe_workspace_size", "moe_forward",
-    "moe_forward_host", "moe_device_status", "MoELayer",
+    "moe_forward_host", "moe_device_status", "MoELayer", "QUANT_TOKEN", "QUANT_BLOCK",
+    "QUANT_NVFP4", "MoELayerDesc", "moe_pipeline_workspace_size", "moe_forward_host_pipelined",
     # expert parallelism (moe_expert_layer_grouped_gb300.ep)
     "moe_ep_dispatch", "moe_ep_recv_reorder", "moe_ep_return_gather", "moe_ep_expert_forward",
     "moe_ep_combine", "EPMoELayer",
@@ -35,6 +36,9 @@ SIGMOID = 0
 SOFTMAX = 1
 EPI_BF16 = 0
 EPI_SILU_MUL = 1
+QUANT_TOKEN = 0
+QUANT_BLOCK = 1
+QUANT_NVFP4 = 2
 # device error codes read by moe_device_status()
 DEV_OK = 0
 DEV_BAD_EXPERT_ID = 1
@@ -63,7 +67,21 @@ _P = ctypes.c_void_p
 _I = ctypes.c_int
 _F = ctypes.c_float
 _SZ = ctypes.c_size_t
+
+
+class MoELayerDesc(ctypes.Structure):
+    """struct moe_layer of the C header: the layer a pipelined call runs."""
+    _fields_ = [("quant", _I), ("T", _I), ("H", _I), ("I", _I), ("E", _I), ("n_shared", _I),
+                ("num_groups", _I), ("topk_group", _I), ("top_k", _I), ("scoring", _I),
+                ("renormalize", _I), ("routed_scaling_factor", _F), ("bias", _P),
+                ("w13", _P), ("s13", _P), ("w2", _P), ("s2", _P), ("g13", _P), ("g2", _P),
+                ("ga1", _F), ("ga2", _F)]
+
+
 _SIGNATURES = {
+    "moe_pipeline_workspace_size": (_SZ, [ctypes.POINTER(MoELayerDesc)]),
+    "moe_forward_host_pipelined": (_I, [ctypes.POINTER(MoELayerDesc), _I, _P, _P, _P, _P, _SZ,
+                                        _P]),
     "moe_status_string": (ctypes.c_char_p, [_I]),
     "moe_abi_version": (_I, []),
     "moe_gate": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P]),
@@ -645,6 +663,29 @@ def moe_device_status():
     return code.value
 
 
+def moe_pipeline_workspace_size(desc):
+    return load().moe_pipeline_workspace_size(ctypes.byref(desc))
+
+
+def moe_forward_host_pipelined(desc, x_hosts, logits_hosts, out_hosts, workspace, stream=None):
+    """n batches of host tensors (x [T,H] bf16, logits [T,E] f32 in, out
+    [T,H] bf16 out; pinned for the copies to overlap the compute) through the
+    layer `desc`, with batch i+1's inputs and batch i-1's output crossing the
+    host link while batch i computes."""
+    n = len(x_hosts)
+    if not (len(logits_hosts) == n == len(out_hosts)) or n < 1:
+        raise ValueError("moe_forward_host_pipelined: one x, logits and out per batch")
+    for t in list(x_hosts) + list(logits_hosts) + list(out_hosts):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError("moe_forward_host_pipelined: host tensors, contiguous")
+    arr = lambda ts: (ctypes.c_void_p * n)(*[t.data_ptr() for t in ts])  # noqa: E731
+    xs, ls, os_ = arr(x_hosts), arr(logits_hosts), arr(out_hosts)
+    _check("moe_forward_host_pipelined", load().moe_forward_host_pipelined(
+        ctypes.byref(desc), n, ctypes.cast(xs, _P), ctypes.cast(ls, _P), ctypes.cast(os_, _P),
+        _ptr(workspace), workspace.numel(), _stream(stream)))
+    return out_hosts
+
+
 class MoELayer:
     """A layer's resident weights plus a reusable workspace; calls moe_forward
     (moe_forward_shared when the layer has shared experts, stored as the last
@@ -725,6 +766,32 @@ class MoELayer:
         with torch.cuda.graph(g):
             self(x, logits, out=out)
         return g
+
+    def desc(self, T):
+        """The struct moe_layer of this layer for batches of T tokens."""
+        q = {"token": QUANT_TOKEN, "block": QUANT_BLOCK, "nvfp4": QUANT_NVFP4}[self.quant]
+        fp4 = self.quant == "nvfp4"
+        v = lambda t: None if t is None else t.data_ptr()  # noqa: E731
+        return MoELayerDesc(q, T, self.H, self.I, self.E, self.n_shared, self.num_groups,
+                            self.topk_group, self.top_k, self.scoring, int(self.renormalize),
+                            self.rsf, v(self.bias), v(self.w13), v(self.s13), v(self.w2),
+                            v(self.s2), v(self.g13) if fp4 else None,
+                            v(self.g2) if fp4 else None, self.ga1 if fp4 else 0.0,
+                            self.ga2 if fp4 else 0.0)
+
+    def forward_host_pipelined(self, x_hosts, logits_hosts, out_hosts, stream=None):
+        """Batches from host memory through moe_forward_host_pipelined (copies
+        overlapped with the compute); the pipeline workspace is kept per T."""
+        import torch
+        T = x_hosts[0].shape[0]
+        d = self.desc(T)
+        ws = getattr(self, "_pipe_ws", None)
+        need = moe_pipeline_workspace_size(d)
+        if need == 0:
+            raise MoEError("moe_pipeline_workspace_size", -1)
+        if ws is None or ws.numel() < need:
+            ws = self._pipe_ws = torch.empty(need, dtype=torch.uint8, device=self.w13.device)
+        return moe_forward_host_pipelined(d, x_hosts, logits_hosts, out_hosts, ws, stream)
 
     def forward_host(self, x_host, logits_host, out_host, stream=None):
         if self.quant == "nvfp4":

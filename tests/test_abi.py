@@ -330,3 +330,50 @@ def test_binding_rejects_undersized_prereorder_buffers():
     kw = dict(ok, scale_a=torch.zeros(T * K * 2, dtype=torch.float32))
     moe._permute_bufs("f", T, 256, K, E, **dict(kw, a_q=torch.zeros((T * K, 256), dtype=torch.uint8)),
                       scales_per_row=2)
+
+
+def _desc(**kw):
+    d = dict(quant=moe.QUANT_TOKEN, T=16, H=128, I=64, E=8, n_shared=0, num_groups=1,
+             topk_group=1, top_k=2, scoring=0, renormalize=1, routed_scaling_factor=1.0,
+             bias=None, w13=0x10000, s13=0x10000, w2=0x10000, s2=0x10000, g13=None, g2=None,
+             ga1=0.0, ga2=0.0)
+    d.update(kw)
+    return moe.MoELayerDesc(**d)
+
+
+def test_pipeline_workspace_size(lib):
+    import ctypes
+    assert lib.moe_pipeline_workspace_size(None) == 0
+    assert lib.moe_pipeline_workspace_size(ctypes.byref(_desc(quant=7))) == 0
+    assert lib.moe_pipeline_workspace_size(ctypes.byref(_desc(E=0))) == 0
+    assert lib.moe_pipeline_workspace_size(ctypes.byref(_desc(T=0))) == 0
+    d = _desc()
+    fw = lib.moe_workspace_size(16, 128, 64, 8, 2)
+    slots = 2 * (16 * 128 * 2) + 2 * 512 + 2 * (16 * 128 * 2)   # x, logits (256-aligned), out
+    assert lib.moe_pipeline_workspace_size(ctypes.byref(d)) >= fw + slots
+    blk = _desc(quant=moe.QUANT_BLOCK, I=128)
+    assert lib.moe_pipeline_workspace_size(ctypes.byref(blk)) >= lib.moe_block_workspace_size(
+        16, 128, 128, 8, 2)
+    assert lib.moe_pipeline_workspace_size(ctypes.byref(_desc(quant=moe.QUANT_BLOCK))) == 0
+
+
+def test_pipelined_call_rejects_bad_arguments_before_any_device_work(lib):
+    import ctypes
+    d = _desc()
+    need = lib.moe_pipeline_workspace_size(ctypes.byref(d))
+    one = (ctypes.c_void_p * 1)(0x20000)
+    null1 = (ctypes.c_void_p * 1)(None)
+    ws = ctypes.c_void_p(0x100000)
+    call = lambda n, x, l, o, w, nb: lib.moe_forward_host_pipelined(  # noqa: E731
+        ctypes.byref(d), n, x, l, o, w, nb, None)
+    cp = lambda a: ctypes.cast(a, ctypes.c_void_p)  # noqa: E731
+    assert lib.moe_forward_host_pipelined(None, 1, cp(one), cp(one), cp(one), ws, need, None) == -1
+    assert call(0, cp(one), cp(one), cp(one), ws, need) == -1
+    assert call(1, None, cp(one), cp(one), ws, need) == -1
+    assert call(1, cp(one), cp(null1), cp(one), ws, need) == -1
+    assert call(1, cp(one), cp(one), cp(one), ws, need - 1) == -3
+    assert call(1, cp(one), cp(one), cp(one), ctypes.c_void_p(0x100008), need) == -3
+    assert call(1, cp(one), cp(one), cp(one), None, need) == -3
+    bad = _desc(num_groups=3)   # E % num_groups != 0: the forward's own check
+    assert lib.moe_forward_host_pipelined(ctypes.byref(bad), 1, cp(one), cp(one), cp(one), ws,
+                                          need, None) == -1
