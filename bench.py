@@ -328,6 +328,11 @@ def time_breakdown(moe, layer, wl, batches, steps, torch):
     sa2 = torch.empty((M, I // 128) if block else M, dtype=torch.float32, device=dev)
     down = torch.empty((M, H), dtype=torch.bfloat16, device=dev)
     out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    if fp4:  # NVFP4 codes and E4M3 block scales, preallocated like the FP8 buffers
+        fa = torch.empty((M, H // 2), dtype=torch.uint8, device=dev)
+        fsa = torch.empty((M, H // 16), dtype=torch.uint8, device=dev)
+        fq = torch.empty((M, I // 2), dtype=torch.uint8, device=dev)
+        fsf = torch.empty((M, I // 16), dtype=torch.uint8, device=dev)
     names = ["gate", "permute_quant", "grouped_gemm_w13", "act_quant", "grouped_gemm_w2",
              "unpermute_sum"]
     st = torch.cuda.current_stream()
@@ -344,19 +349,19 @@ def time_breakdown(moe, layer, wl, batches, steps, torch):
             w[:, :wl.top_k] = w_r
         if ev: ev[7].record(st)
         if fp4:  # (the layer holds the arranged weight scales)
-            fa, fsa, fs2d, foff = moe.moe_permute_quant_nvfp4(x, ids, E, layer.ga1, workspace=pws)
+            moe.moe_permute_quant_nvfp4(x, ids, E, layer.ga1, workspace=pws, a_q=fa, sf=fsa,
+                                        src2dst=s2d, offsets=off)
             if ev: ev[2].record(st)
-            fh = moe.moe_grouped_gemm_nvfp4(fa, fsa, layer.ga1, layer.w13, layer.s13, layer.g13,
-                                            foff, moe.EPI_SILU_MUL, C=h)
+            moe.moe_grouped_gemm_nvfp4(fa, fsa, layer.ga1, layer.w13, layer.s13, layer.g13,
+                                       off, moe.EPI_SILU_MUL, C=h)
             if ev: ev[3].record(st)
-            fq, fsf = moe.moe_act_quant_nvfp4(fh, layer.ga2)
+            moe.moe_act_quant_nvfp4(h, layer.ga2, q=fq, sf=fsf)
             if ev: ev[4].record(st)
-            fd = moe.moe_grouped_gemm_nvfp4(fq, fsf, layer.ga2, layer.w2, layer.s2, layer.g2,
-                                            foff, moe.EPI_BF16, C=down)
+            moe.moe_grouped_gemm_nvfp4(fq, fsf, layer.ga2, layer.w2, layer.s2, layer.g2,
+                                       off, moe.EPI_BF16, C=down)
             if ev: ev[5].record(st)
-            moe.moe_unpermute_sum(fd, fs2d, w, out=out)
+            moe.moe_unpermute_sum(down, s2d, w, out=out)
             if ev: ev[6].record(st)
-            off.copy_(foff)
             return
         if block:
             moe.moe_permute_quant_block(x, ids, E, a_q=a_q, scale_a=sa, src2dst=s2d,

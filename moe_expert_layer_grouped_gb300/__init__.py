@@ -529,19 +529,26 @@ def moe_forward_block_host(x_host, logits_host, bias, w13, s13, w2, s2, n_shared
 
 
 # ---- NVFP4 (E2M1 codes two per byte, E4M3 scale per 16 along K, fp32 global)
-def moe_permute_quant_nvfp4(x, topk_ids, E, g, workspace=None, stream=None):
+def moe_permute_quant_nvfp4(x, topk_ids, E, g, workspace=None, stream=None, a_q=None, sf=None,
+                            src2dst=None, offsets=None):
     """Pre-reorder with NVFP4 quantisation (global scale g). Returns (a_q
-    [T*K, H/2] packed, sf [T*K, H/16], src2dst, offsets)."""
+    [T*K, H/2] packed, sf [T*K, H/16], src2dst, offsets); given buffers are
+    filled in place."""
     import torch
-    _need_cuda(x, topk_ids, workspace)
+    _need_cuda(x, topk_ids, workspace, a_q, sf, src2dst, offsets)
     T, H = x.shape
     K = topk_ids.shape[1]
     dev = x.device
     M = T * K
-    a_q = torch.empty((M, H // 2), dtype=torch.uint8, device=dev)
-    sf = torch.empty((M, H // 16), dtype=torch.uint8, device=dev)
-    src2dst = torch.empty(M, dtype=torch.int32, device=dev)
-    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    a_q = torch.empty((M, H // 2), dtype=torch.uint8, device=dev) if a_q is None else a_q
+    sf = torch.empty((M, H // 16), dtype=torch.uint8, device=dev) if sf is None else sf
+    src2dst = torch.empty(M, dtype=torch.int32, device=dev) if src2dst is None else src2dst
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev) if offsets is None else offsets
+    fn = "moe_permute_quant_nvfp4"
+    _need_buf(fn, "a_q", a_q, M * (H // 2), (torch.uint8,))
+    _need_buf(fn, "sf", sf, M * (H // 16), (torch.uint8,))
+    _need_buf(fn, "src2dst", src2dst, M, (torch.int32,))
+    _need_buf(fn, "offsets", offsets, E + 1, (torch.int32,))
     if workspace is None:
         workspace = torch.empty(max(moe_permute_workspace_size(T, E, K), 256), dtype=torch.uint8,
                                 device=dev)
@@ -552,13 +559,16 @@ def moe_permute_quant_nvfp4(x, topk_ids, E, g, workspace=None, stream=None):
     return a_q, sf, src2dst, offsets
 
 
-def moe_act_quant_nvfp4(h, g, stream=None):
-    """NVFP4 requantisation of h [M, I] bf16: (q [M, I/2] packed, sf [M, I/16])."""
+def moe_act_quant_nvfp4(h, g, stream=None, q=None, sf=None):
+    """NVFP4 requantisation of h [M, I] bf16: (q [M, I/2] packed, sf [M, I/16]);
+    given buffers are filled in place."""
     import torch
-    _need_cuda(h)
+    _need_cuda(h, q, sf)
     M, I = h.shape
-    q = torch.empty((M, I // 2), dtype=torch.uint8, device=h.device)
-    sf = torch.empty((M, I // 16), dtype=torch.uint8, device=h.device)
+    q = torch.empty((M, I // 2), dtype=torch.uint8, device=h.device) if q is None else q
+    sf = torch.empty((M, I // 16), dtype=torch.uint8, device=h.device) if sf is None else sf
+    _need_buf("moe_act_quant_nvfp4", "q", q, M * (I // 2), (torch.uint8,))
+    _need_buf("moe_act_quant_nvfp4", "sf", sf, M * (I // 16), (torch.uint8,))
     _check("moe_act_quant_nvfp4", load().moe_act_quant_nvfp4(
         _ptr(h), M, I, float(g), _ptr(q), _ptr(sf), _stream(stream)))
     return q, sf
