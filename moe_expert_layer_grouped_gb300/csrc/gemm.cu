@@ -730,15 +730,20 @@ bool make_tma_map_weights_rows(CUtensorMap* m, const void* base, uint64_t E, uin
   return encode_u8(m, base, 3, dims, strides, box);
 }
 
-bool make_tma_map_weights_pairs32(CUtensorMap* m, const void* base, uint64_t E, uint64_t N,
-                                  uint64_t Kd) {
-  // [E][Kd/128][2][I][128] (as the SiLU stage view), boxes of 32 gate rows
-  // then the matching 32 up rows of one 128-byte chunk
+bool make_tma_map_weights_gateup(CUtensorMap* m, const void* base, uint64_t E, uint64_t N,
+                                 uint64_t Kd, uint32_t jrows) {
+  // [E][Kd/128][2][I][128] (as the SiLU stage view), boxes of jrows gate rows
+  // then the matching jrows up rows of one 128-byte chunk
   const uint64_t I = N / 2, KB = Kd / BK;
   const cuuint64_t dims[5] = {BK, I, 2, KB, E};
   const cuuint64_t strides[4] = {Kd, I * Kd, BK, 2 * I * Kd};
-  const cuuint32_t box[5] = {BK, 32, 2, 1, 1};
+  const cuuint32_t box[5] = {BK, jrows, 2, 1, 1};
   return encode_u8(m, base, 5, dims, strides, box);
+}
+
+bool make_tma_map_weights_pairs32(CUtensorMap* m, const void* base, uint64_t E, uint64_t N,
+                                  uint64_t Kd) {
+  return make_tma_map_weights_gateup(m, base, E, N, Kd, 32);
 }
 
 bool make_tma_map_rows(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols) {
@@ -787,6 +792,12 @@ cudaError_t launch_grouped_gemm(const void* A, const float* scale_a, const void*
                                 cudaStream_t st, int stall_stage, bool pdl, bool early_table,
                                 const int32_t* row_token, int T) {
   if (M == 0) return cudaSuccess;
+  // long K with many rows per expert: pairs with two accumulators per CTA
+  // (gemm_wide.cu), which stage each token row half as often
+  if (row_token == nullptr && row_amax == nullptr && stall_stage < 0 &&
+      gemm_wide_applies(M, N, Kd, E, epilogue))
+    return launch_grouped_gemm_wide(A, scale_a, B, scale_b, offsets, M, N, Kd, E, epilogue, C,
+                                    err, st, pdl, early_table);
   const bool silu = (epilogue == MOE_EPI_SILU_MUL);
   const bool small = !gemm_many_rows(M, E);  // few rows per expert (decode)
   // K chunks per stage of the configuration launched below (the weight box

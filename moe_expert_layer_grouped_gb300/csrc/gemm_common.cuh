@@ -168,6 +168,11 @@ bool make_tma_map_weights_rows(CUtensorMap* m, const void* base, uint64_t E, uin
                                uint64_t Kd, uint32_t rows);
 
 // Host: w13 [E, 2I, Kd] (Kd % 128 == 0) viewed per 128-byte K chunk, boxes of
+// jrows (<= 256) gate rows followed by the matching jrows up rows.
+bool make_tma_map_weights_gateup(CUtensorMap* m, const void* base, uint64_t E, uint64_t N,
+                                 uint64_t Kd, uint32_t jrows);
+
+// Host: w13 [E, 2I, Kd] (Kd % 128 == 0) viewed per 128-byte K chunk, boxes of
 // 32 gate rows followed by the matching 32 up rows.
 bool make_tma_map_weights_pairs32(CUtensorMap* m, const void* base, uint64_t E, uint64_t N,
                                   uint64_t Kd);

@@ -68,6 +68,16 @@ cudaError_t launch_grouped_gemm(const void* A, const float* scale_a, const void*
 // Whether the grouped GEMM takes its many-rows-per-expert configuration.
 bool gemm_many_rows(int M, int E);
 
+// gemm_wide.cu: the per-token GEMM on CTA pairs with 256 weight rows per CTA
+// (two accumulators), for many rows per expert and K of at least 32 blocks of
+// 128 (SiLU: I % 256 == 0; bf16: N % 512 == 0). launch_grouped_gemm takes it
+// by itself when it applies and no row amax, gather or stall test is asked.
+bool gemm_wide_applies(int M, int N, int Kd, int E, int epilogue);
+cudaError_t launch_grouped_gemm_wide(const void* A, const float* scale_a, const void* B,
+                                     const float* scale_b, const int32_t* offsets, int M, int N,
+                                     int Kd, int E, int epilogue, void* C, int* err,
+                                     cudaStream_t st, bool pdl = false, bool early_table = false);
+
 // gemm_block.cu: block scales, scale_a [M, Kd/128], scale_b [E, N/128, Kd/128]
 // (N % 128 == 0, Kd % 128 == 0); no row amax.
 cudaError_t launch_grouped_gemm_block(const void* A, const float* scale_a, const void* B,
