@@ -20,8 +20,9 @@
 // used only where K is long (at least 32 blocks of 128), which keeps the
 // drain a small share of a tile.
 //
-// Roles (192 threads): warp 0 TMA producer, warp 1 the MMA issuer (the even
-// CTA's lane 0 issues for both), warps 2-5 the epilogue (lane quadrant w % 4).
+// Roles (320 threads): warp 0 TMA producer, warp 1 the MMA issuer (the even
+// CTA's lane 0 issues for both), warps 2-9 the epilogue (lane quadrant w % 4,
+// two warps per quadrant on alternate token chunks, so a tile drains faster).
 // Every wait is bounded: on timeout the CTA sets the device error word, lets
 // its copies and MMAs land, frees its tensor memory and leaves.
 #include <cuda.h>
@@ -39,7 +40,8 @@ namespace {
 
 using namespace gemm_common;
 
-constexpr int WT = 192;
+constexpr int WEW = 8;               // epilogue warps: two per TMEM lane quadrant
+constexpr int WT = 64 + 32 * WEW;
 constexpr int WSTAGES = 4;
 constexpr int WROWS = 256;          // weight rows per CTA (two accumulators)
 constexpr int WBN = 256;            // tokens per pair tile (MMA N), half per CTA
@@ -49,7 +51,7 @@ constexpr uint32_t WTMEM = 2 * WACC;
 struct WSmem {
   uint8_t w[WSTAGES][WROWS * BK];      // this CTA's 256 weight rows, one K block
   uint8_t x[WSTAGES][(WBN / 2) * BK];  // this CTA's half of the tile's tokens
-  uint16_t stage_out[4][32 * 32];      // per epilogue warp: bf16 [token][32 columns]
+  uint16_t stage_out[WEW][32 * 32];    // per epilogue warp: bf16 [token][32 columns]
   uint64_t full[WSTAGES];              // only the even CTA's are armed and waited
   uint64_t empty[WSTAGES];
   uint64_t tfull;                      // the tile's accumulators are complete
@@ -95,7 +97,7 @@ __global__ void __launch_bounds__(WT, 1)
       ptx::mbar_init(&sm.empty[s], 1);
     }
     ptx::mbar_init(&sm.tfull, 1);
-    ptx::mbar_init(&sm.tempty, 2 * 128);  // every epilogue thread of both CTAs
+    ptx::mbar_init(&sm.tempty, 2 * 32 * WEW);  // every epilogue thread of both CTAs
     ptx::mbar_init(&sm.drain, 1);
     sm.abort = 0;
     sm.never = 0;
@@ -228,8 +230,11 @@ __global__ void __launch_bounds__(WT, 1)
       }
     }
   } else {
-    // ======================= epilogue (warps 2..5) ==========================
+    // ======================= epilogue (warps 2..) ===========================
+    // warp w reads lane quadrant w % 4; the two warps of a quadrant take the
+    // even and the odd 32-token chunks
     const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    const int par = (warp - 2) / 4;
     int iter = 0;
     for (int g = cluster; g < total; g += nclusters, ++iter) {
       const TileInfo<WBN> t = decode_tile<WBN>(sm, E, p.NBG, g);
@@ -244,7 +249,7 @@ __global__ void __launch_bounds__(WT, 1)
       const int nchunk = (t.ntok + 31) >> 5;
       const int64_t e = t.e;
       const int blk = t.nb * 2 + rank;
-      uint16_t* ost = sm.stage_out[q];
+      uint16_t* ost = sm.stage_out[warp - 2];
       if (SILU) {
         const int I = p.I;
         const int jrow = blk * 128 + q * 32;  // first j of this warp's 32
@@ -253,10 +258,13 @@ __global__ void __launch_bounds__(WT, 1)
         const float su = __ldg(p.scale_b + e * p.N + I + j);
         __nv_bfloat16* hbase = reinterpret_cast<__nv_bfloat16*>(p.C);
 #pragma unroll 1
-        for (int c = 0; c < nchunk; ++c) {
+        for (int c = par; c < nchunk; c += WEW / 4) {
           uint32_t gv[32], uv[32];
-          ptx::tmem_ld_sync_x32(tq + c * 32, gv);
-          ptx::tmem_ld_sync_x32(tq + WACC + c * 32, uv);
+          ptx::tmem_ld_32x32b_x32(tq + c * 32, gv);
+          ptx::tmem_ld_32x32b_x32(tq + WACC + c * 32, uv);
+          ptx::tmem_ld_wait();
+          ptx::reg_fence(gv);
+          ptx::reg_fence(uv);
           const int tk0 = c * 32;
           const float sa_l = (tk0 + lane < t.ntok) ? __ldg(p.scale_a + t.tok0 + tk0 + lane) : 0.0f;
 #pragma unroll
@@ -289,7 +297,7 @@ __global__ void __launch_bounds__(WT, 1)
           const int ncol0 = blk * WROWS + acc * 128 + q * 32;  // first column of this warp's 32
           const float sb = __ldg(p.scale_b + e * N + ncol0 + lane);
 #pragma unroll 1
-          for (int c = 0; c < nchunk; ++c) {
+          for (int c = par; c < nchunk; c += WEW / 4) {
             uint32_t v[32];
             ptx::tmem_ld_sync_x32(tq + (uint32_t)acc * WACC + c * 32, v);
             const int tk0 = c * 32;
