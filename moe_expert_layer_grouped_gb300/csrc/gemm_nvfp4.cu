@@ -66,7 +66,7 @@ using namespace gemm_common;
 constexpr int FT = 320;  // 10 warps: producer, MMA, 4 epilogue, 4 token scales
 constexpr int SCALE_WARP0 = 6;
 constexpr int SFROW = 16;      // scale bytes per row per 128-byte K chunk
-constexpr uint32_t F_SFSTAGE = 32;                  // scale columns per stage
+constexpr uint32_t F_SFCHUNK = 32;  // scale columns per K chunk: 16 for the weights, 16 tokens
 constexpr uint32_t F_TMEM = 512;
 // Tile width FBN (tokens, MMA N) and pipeline depth FSTAGES per launch:
 // few tokens per expert (decode) 64 x 6 stages, the weight stream's bytes in
@@ -79,12 +79,12 @@ struct FMaps {
   CUtensorMap sx[NXBOX];  // token scales, 16 bytes x (64 >> i) rows
 };
 
-template <bool SILU, int FBN, int FSTAGES>
+template <bool SILU, int FBN, int FSTAGES, int FKC>
 struct FSmem {
-  uint8_t w[FSTAGES][W_BYTES];
-  uint8_t x[FSTAGES][FBN * BK];
-  uint8_t sx[FSTAGES][FBN * SFROW];   // token scales, row-major as loaded
-  uint32_t atom_a[FSTAGES][4][128];   // weight scales: tcgen05.cp sources, one per MMA step
+  uint8_t w[FSTAGES][FKC * W_BYTES];       // FKC K chunks of the tile's weight rows (one box)
+  uint8_t x[FSTAGES][FKC][FBN * BK];
+  uint8_t sx[FSTAGES][FKC][FBN * SFROW];   // token scales, row-major as loaded
+  uint32_t atom_a[FSTAGES][FKC * 4][128];  // weight scales: tcgen05.cp sources, one per MMA step
   float xchg[SILU ? 2 : 1][2][32 * 32];
   uint16_t stage_out[4][32 * 32];
   uint64_t full[FSTAGES];
@@ -115,13 +115,14 @@ struct FParams {
   int early_table;
 };
 
-template <bool SILU, int FBN, int FSTAGES>
+template <bool SILU, int FBN, int FSTAGES, int FKC>
 __global__ void __launch_bounds__(FT, 1)
     grouped_gemm_nvfp4_kernel(const __grid_constant__ FMaps maps, const FParams p) {
   constexpr uint32_t F_ACC = FBN;              // TMEM columns per accumulator
   constexpr uint32_t F_SF0 = 2 * F_ACC;        // first scale column
+  constexpr uint32_t F_SFSTAGE = FKC * F_SFCHUNK;  // scale columns per stage
   static_assert(F_SF0 + FSTAGES * F_SFSTAGE <= F_TMEM, "tensor memory budget");
-  using S = FSmem<SILU, FBN, FSTAGES>;
+  using S = FSmem<SILU, FBN, FSTAGES, FKC>;
   extern __shared__ uint8_t smem_raw[];
   S& sm = *reinterpret_cast<S*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                 ~static_cast<uintptr_t>(1023));
@@ -129,7 +130,7 @@ __global__ void __launch_bounds__(FT, 1)
   const int warp = tid >> 5;
   const int lane = tid & 31;
   const int E = p.E;
-  const int KS = p.KB;  // one K chunk per stage
+  const int KS = p.KB / FKC;  // FKC K chunks per stage (KB % FKC == 0)
 
   if (warp == 0 && lane == 0) {
     ptx::prefetch_tensormap(&maps.w);
@@ -178,7 +179,7 @@ __global__ void __launch_bounds__(FT, 1)
       for (int g = blockIdx.x; ok && g < total; g += gridDim.x) {
         const TileInfo<FBN> t = decode_tile<FBN>(sm, E, p.NB, g);
         const int rows = (t.ntok + 15) & ~15;
-        const uint32_t bytes = W_BYTES + 4 * 512 + (uint32_t)rows * (BK + SFROW);
+        const uint32_t bytes = FKC * (W_BYTES + 4 * 512 + (uint32_t)rows * (BK + SFROW));
         const uint8_t* sba = p.sba + (((int64_t)t.e * p.NB + t.nb) * p.KB) * 2048;
         const int y0 = t.e * p.N + t.nb * BM;  // bf16 epilogue: first weight row
         const uint64_t pw = t.nch == 1 ? pol_w1 : pol_w;
@@ -190,21 +191,25 @@ __global__ void __launch_bounds__(FT, 1)
           ptx::mbar_arrive_expect_tx(&sm.full[s], bytes);
           armed |= 1u << s;
           armed_par = (armed_par & ~(1u << s)) | (ph << s);
+          const int c0 = ks * FKC;  // the stage's first K chunk
           if (SILU)
-            ptx::tma_load_5d(sm.w[s], &maps.w, &sm.full[s], 0, t.nb * 64, 0, ks, t.e, pw);
+            ptx::tma_load_5d(sm.w[s], &maps.w, &sm.full[s], 0, t.nb * 64, 0, c0, t.e, pw);
           else
-            ptx::tma_load_3d(sm.w[s], &maps.w, &sm.full[s], 0, y0, ks, pw);
-          ptx::bulk_load(sm.atom_a[s], sba + (int64_t)ks * 2048, 4 * 512, &sm.full[s], pw);
-          int r = 0;
+            ptx::tma_load_3d(sm.w[s], &maps.w, &sm.full[s], 0, y0, c0, pw);
+          ptx::bulk_load(sm.atom_a[s], sba + (int64_t)c0 * 2048, FKC * 4 * 512, &sm.full[s], pw);
 #pragma unroll
-          for (int i = 0; i < NXBOX; ++i) {
-            const int box = 64 >> i;
-            while (rows - r >= box) {
-              ptx::tma_load_2d(sm.x[s] + r * BK, &maps.x[i], &sm.full[s], ks * BK, t.tok0 + r,
-                               pol_x);
-              ptx::tma_load_2d(sm.sx[s] + r * SFROW, &maps.sx[i], &sm.full[s], ks * SFROW,
-                               t.tok0 + r, pol_x);
-              r += box;
+          for (int kc = 0; kc < FKC; ++kc) {
+            int r = 0;
+#pragma unroll
+            for (int i = 0; i < NXBOX; ++i) {
+              const int box = 64 >> i;
+              while (rows - r >= box) {
+                ptx::tma_load_2d(sm.x[s][kc] + r * BK, &maps.x[i], &sm.full[s], (c0 + kc) * BK,
+                                 t.tok0 + r, pol_x);
+                ptx::tma_load_2d(sm.sx[s][kc] + r * SFROW, &maps.sx[i], &sm.full[s],
+                                 (c0 + kc) * SFROW, t.tok0 + r, pol_x);
+                r += box;
+              }
             }
           }
           if (++s == FSTAGES) {
@@ -243,14 +248,17 @@ __global__ void __launch_bounds__(FT, 1)
             break;
           }
           ptx::tc_fence_after();
-          const uint32_t sfa = tmem + F_SF0 + (uint32_t)s * F_SFSTAGE;
-          const uint32_t sfb = sfa + 16;
-          const uint32_t a0 = ptx::smem_u32(sm.w[s]);
-          const uint32_t b0 = ptx::smem_u32(sm.x[s]);
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            ptx::mma_nvfp4(d, ptx::sdesc_sw128(a0 + j * 32), ptx::sdesc_sw128(b0 + j * 32), idesc,
-                           sfa + 4 * j, sfb + 4 * j, (ks | j) != 0 ? 1u : 0u);
+          for (int kc = 0; kc < FKC; ++kc) {
+            const uint32_t sfa = tmem + F_SF0 + (uint32_t)s * F_SFSTAGE + kc * F_SFCHUNK;
+            const uint32_t sfb = sfa + 16;
+            const uint32_t a0 = ptx::smem_u32(sm.w[s]) + kc * W_BYTES;
+            const uint32_t b0 = ptx::smem_u32(sm.x[s][kc]);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              ptx::mma_nvfp4(d, ptx::sdesc_sw128(a0 + j * 32), ptx::sdesc_sw128(b0 + j * 32),
+                             idesc, sfa + 4 * j, sfb + 4 * j, (ks | kc | j) != 0 ? 1u : 0u);
+          }
           ptx::mma_commit(&sm.empty[s]);
           issued = true;
           if (++s == FSTAGES) {
@@ -287,24 +295,31 @@ __global__ void __launch_bounds__(FT, 1)
           // the weights' scale blocks into the stage's columns, ahead of the
           // MMAs; the commit is the fifth arrival on sready
           ptx::tc_fence_after();
-          const uint32_t sfa = tmem + F_SF0 + (uint32_t)s * F_SFSTAGE;
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            ptx::tmem_cp_32x128b_x4(sfa + 4 * j, ptx::sdesc_rows16(ptx::smem_u32(sm.atom_a[s][j])));
+          for (int kc = 0; kc < FKC; ++kc) {
+            const uint32_t sfa = tmem + F_SF0 + (uint32_t)s * F_SFSTAGE + kc * F_SFCHUNK;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              ptx::tmem_cp_32x128b_x4(sfa + 4 * j,
+                                      ptx::sdesc_rows16(ptx::smem_u32(sm.atom_a[s][kc * 4 + j])));
+          }
           ptx::mma_commit(&sm.sready[s]);
         }
-        uint32_t r[16];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const int row = lane + 32 * c;
-          uint4 v = make_uint4(0u, 0u, 0u, 0u);
-          if (row < FBN) v = *reinterpret_cast<const uint4*>(sm.sx[s] + row * SFROW);
-          r[c] = v.x;
-          r[4 + c] = v.y;
-          r[8 + c] = v.z;
-          r[12 + c] = v.w;
+        for (int kc = 0; kc < FKC; ++kc) {
+          uint32_t r[16];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int row = lane + 32 * c;
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (row < FBN) v = *reinterpret_cast<const uint4*>(sm.sx[s][kc] + row * SFROW);
+            r[c] = v.x;
+            r[4 + c] = v.y;
+            r[8 + c] = v.z;
+            r[12 + c] = v.w;
+          }
+          ptx::tmem_st_32x32b_x16(tq + F_SF0 + (uint32_t)s * F_SFSTAGE + kc * F_SFCHUNK + 16, r);
         }
-        ptx::tmem_st_32x32b_x16(tq + F_SF0 + (uint32_t)s * F_SFSTAGE + 16, r);
         ptx::tmem_st_wait();
         ptx::tc_fence_before();
         __syncwarp();
@@ -446,12 +461,12 @@ __global__ void __launch_bounds__(FT, 1)
   }
 }
 
-template <bool SILU, int FBN, int FSTAGES>
+template <bool SILU, int FBN, int FSTAGES, int FKC>
 cudaError_t launch_f(const FMaps& maps, const FParams& p, int M, int E, cudaStream_t st,
                      bool pdl) {
-  constexpr size_t smem = sizeof(FSmem<SILU, FBN, FSTAGES>) + 1024;
+  constexpr size_t smem = sizeof(FSmem<SILU, FBN, FSTAGES, FKC>) + 1024;
   static_assert(smem <= 227 * 1024, "shared memory budget");
-  auto kern = grouped_gemm_nvfp4_kernel<SILU, FBN, FSTAGES>;
+  auto kern = grouped_gemm_nvfp4_kernel<SILU, FBN, FSTAGES, FKC>;
   static std::mutex mu;
   static bool attr_set[64] = {};
   int dev = 0;
@@ -520,8 +535,12 @@ cudaError_t launch_grouped_gemm_nvfp4(const void* A, const uint8_t* sfa, float g
   const bool silu = (epilogue == MOE_EPI_SILU_MUL);
   const uint64_t kb = (uint64_t)Kd / 2;   // bytes of a row
   const uint64_t sc = (uint64_t)Kd / 16;  // scale bytes of a row
+  // few tokens per expert: two K chunks per stage (256 contiguous bytes of
+  // every weight row) when the chunk count is even
+  const bool many = gemm_many_rows(M, E);
+  const int fkc = (!many && (Kd / 256) % 2 == 0) ? 2 : 1;
   FMaps maps;
-  if (!make_tma_map_weights(&maps.w, B, silu, (uint64_t)E, (uint64_t)N, kb, 1))
+  if (!make_tma_map_weights(&maps.w, B, silu, (uint64_t)E, (uint64_t)N, kb, (uint32_t)fkc))
     return cudaErrorNotSupported;
   for (int i = 0; i < NXBOX; ++i)
     if (!make_tma_map_u8(&maps.x[i], A, (uint64_t)M, kb, 64u >> i) ||
@@ -541,14 +560,16 @@ cudaError_t launch_grouped_gemm_nvfp4(const void* A, const uint8_t* sfa, float g
   p.I = N / 2;
   p.NB = silu ? p.I / 64 : N / BM;
   p.KB = Kd / 256;
-  const bool many = gemm_many_rows(M, E);
   p.stream_weights = many ? 0 : 1;
   p.early_table = early_table ? 1 : 0;
+  if (!many && fkc == 2)
+    return silu ? launch_f<true, 64, 3, 2>(maps, p, M, E, st, pdl)
+                : launch_f<false, 64, 3, 2>(maps, p, M, E, st, pdl);
   if (!many)
-    return silu ? launch_f<true, 64, 6>(maps, p, M, E, st, pdl)
-                : launch_f<false, 64, 6>(maps, p, M, E, st, pdl);
-  return silu ? launch_f<true, 128, 5>(maps, p, M, E, st, pdl)
-              : launch_f<false, 128, 5>(maps, p, M, E, st, pdl);
+    return silu ? launch_f<true, 64, 6, 1>(maps, p, M, E, st, pdl)
+                : launch_f<false, 64, 6, 1>(maps, p, M, E, st, pdl);
+  return silu ? launch_f<true, 128, 5, 1>(maps, p, M, E, st, pdl)
+              : launch_f<false, 128, 5, 1>(maps, p, M, E, st, pdl);
 }
 
 }  // namespace moe

@@ -162,6 +162,10 @@ FP4_SHAPES = [
     ([17, 64, 200, 3], 128, 256),
     ([129, 127], 256, 7168),
     ([150, 0, 3, 40, 0, 0, 7, 0, 0, 0, 0, 0, 0, 0, 0, 1], 256, 512),
+    # few rows per expert: two K chunks per stage (even chunk count, the ring
+    # wrapping within a tile), and one per stage (odd chunk count)
+    ([3, 0, 9, 1, 5, 2, 0, 7], 256, 2048),
+    ([3, 9, 1, 5], 256, 768),
 ]
 
 
