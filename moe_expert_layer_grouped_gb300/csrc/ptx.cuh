@@ -295,7 +295,8 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// Shared-memory matrix descriptor for a K-major operand tile written by TMA
+// Shared-memory matrix descriptor (PTX ISA, tcgen05 "Shared Memory
+// Descriptor") for a K-major operand tile written by TMA
 // with 128-byte swizzling: rows of 128 bytes, 8-row (1024-byte) swizzle
 // atoms stacked along M/N (stride byte offset 1024). The leading byte offset
 // is unused for swizzled K-major layouts. Bits 46-47 hold the descriptor
@@ -310,7 +311,8 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
   return d;
 }
 
-// Instruction descriptor of tcgen05.mma.kind::f8f6f4: A and B e4m3, D fp32,
+// Instruction descriptor of tcgen05.mma.kind::f8f6f4 (PTX ISA, tcgen05
+// "Instruction descriptor" table for kind::f16 / f8f6f4): A and B e4m3, D fp32,
 // both operands K-major, tile M x N.
 __host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
   return (1u << 4)                          // D format: f32
@@ -345,7 +347,9 @@ __host__ __device__ constexpr uint32_t idesc_nvfp4(int M, int N) {
 // D[tmem] (+)= (A * SFA) (B * SFB)^T with E2M1 A/B in shared memory (two
 // codes per byte, K-major, K = 64 per instruction) and one UE4M3 scale per
 // 16 elements along K for every row of A and of B, read from tensor memory
-// at sfa / sfb (.scale_vec::4X: four scales per row per instruction).
+// at sfa / sfb (.scale_vec::4X: four scales per row per instruction; PTX
+// ISA, tcgen05 "Block Scaling" and its scale-factor layout in tensor
+// memory: row m in lane m % 32, column m / 32 of the instruction's group).
 __device__ __forceinline__ void mma_nvfp4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
                                           uint32_t idesc, uint32_t sfa, uint32_t sfb,
                                           uint32_t accumulate) {
@@ -358,7 +362,8 @@ __device__ __forceinline__ void mma_nvfp4(uint32_t d_tmem, uint64_t adesc, uint6
       : "memory");
 }
 
-// Shared-memory descriptor of an unswizzled K-major block of 16-byte rows
+// Shared-memory descriptor (PTX ISA, tcgen05 "Shared Memory Descriptor",
+// no-swizzle layout) of an unswizzled K-major block of 16-byte rows
 // (8-row core matrices of 128 contiguous bytes, consecutive core matrices
 // 128 bytes apart), the source of a tcgen05.cp of 32 rows x 128 bits.
 __device__ __forceinline__ uint64_t sdesc_rows16(uint32_t saddr) {
@@ -372,7 +377,8 @@ __device__ __forceinline__ uint64_t sdesc_rows16(uint32_t saddr) {
 
 // Copies 32 rows x 16 bytes from shared memory (descriptor sdesc) into
 // tensor memory columns taddr .. taddr+3 of lanes 0..31, replicated into
-// each of the four 32-lane quadrants.
+// each of the four 32-lane quadrants (PTX ISA, tcgen05.cp: shape 32x128b
+// with the .warpx4 multicast).
 __device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
   asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
                : "memory");
