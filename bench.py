@@ -577,6 +577,20 @@ def layer_fracs(r, pk, clocks=None, ratio=FP8_PER_BF16):
     return out
 
 
+def layer_bound(r, pk, ratio=FP8_PER_BF16):
+    """The layer's own roofline: the larger of its tensor time (all GEMM
+    FLOPs at the burst peak of its operand type) and its HBM time (the bytes
+    no implementation can avoid: the active experts' weights and scales, x,
+    logits and out, at the measured copy rate), and the step time's
+    fraction of it. Intermediates (permuted rows, h, down) are not counted:
+    they are this implementation's choice."""
+    t_ms = r["work"]["layer_flops"] / (pk["bf16"] * ratio * 1e12) * 1e3
+    h_ms = r["work"]["layer_bytes"] / (pk["hbm"] * 1e9) * 1e3
+    bound = max(t_ms, h_ms)
+    return {"bound": "tensor" if t_ms >= h_ms else "hbm", "tensor_ms": round(t_ms, 4),
+            "hbm_ms": round(h_ms, 4), "frac": round(bound / r["ms"], 4)}
+
+
 def workload_config(wl, world):
     """The `config` object of both arms' JSON lines: the workload and its
     shapes, nothing measured."""
@@ -685,6 +699,7 @@ def run_ours(args):
         "tflops": round(r["work"]["layer_flops"] / (r["ms"] * 1e-3) / 1e12, 2),
         "layer_hbm_gbs": round(r["work"]["layer_bytes"] / (r["ms"] * 1e-3) / 1e9, 1),
         **(layer_fracs(r, pk, r["clocks"], tensor_ratio(wl)) if wl.T > 512 else {}),
+        "layer_bound": layer_bound(r, pk, tensor_ratio(wl)),
         "active_experts": r["work"]["active"],
         "kernels_ms": {k: round(v, 4) for k, v in r["kern"].items()},
         "roofline": (roofline_decode(r, pk, wl.name) if wl.T <= 512

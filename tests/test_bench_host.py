@@ -213,3 +213,20 @@ def test_clock_summary_reads_the_timed_window():
     # no sample inside the window: the last few samples stand in
     s = cs.summary(10.0, 11.0)
     assert s["sm_mhz"] == 2000.0 and s["samples"] == 3
+
+
+def test_layer_bound_takes_the_larger_of_tensor_and_hbm_time():
+    pk = {"bf16": 2000.0, "hbm": 8000.0}
+    # 4 TFLOP at 4000 TFLOP/s (FP8 = 2 x bf16) = 1 ms; 16 GB at 8 TB/s = 2 ms
+    r = {"work": {"layer_flops": 4e12, "layer_bytes": 16e9}, "ms": 4.0}
+    b = bench.layer_bound(r, pk)
+    assert b["bound"] == "hbm" and b["tensor_ms"] == 1.0 and b["hbm_ms"] == 2.0
+    assert b["frac"] == 0.5
+    r = {"work": {"layer_flops": 12e12, "layer_bytes": 8e9}, "ms": 6.0}
+    b = bench.layer_bound(r, pk)
+    assert b["bound"] == "tensor" and b["tensor_ms"] == 3.0 and b["frac"] == 0.5
+    # FP4 operands: the tensor time at 6 x bf16
+    r = {"work": {"layer_flops": 12e12, "layer_bytes": 10e9}, "ms": 2.5}
+    b = bench.layer_bound(r, pk, bench.FP4_PER_BF16)
+    assert b["tensor_ms"] == 1.0 and b["hbm_ms"] == 1.25 and b["bound"] == "hbm"
+    assert b["frac"] == 0.5
