@@ -183,6 +183,21 @@ def _need_buf(fn, name, t, numel, dtypes):
                          f"{' or '.join(str(d) for d in dtypes)}, got {t.numel()} of {t.dtype}")
 
 
+def _gemm_bufs(fn, M, N, E, cols, scale_a, n_sa, scale_b, n_sb, offsets, C, row_amax,
+               scale_dtypes=None):
+    """The grouped GEMM's scale, offset and output tensors must hold what the
+    kernels read and write (an undersized one would be read or written past
+    its end on the device)."""
+    import torch
+    sd = scale_dtypes or (torch.float32,)
+    _need_buf(fn, "scale_a", scale_a, n_sa, sd)
+    _need_buf(fn, "scale_b", scale_b, n_sb, sd)
+    _need_buf(fn, "offsets", offsets, E + 1, (torch.int32,))
+    _need_buf(fn, "C", C, M * cols, (torch.bfloat16,))
+    if row_amax is not None:
+        _need_buf(fn, "row_amax", row_amax, M, (torch.float32,))
+
+
 def _permute_bufs(fn, T, H, K, E, a_q, scale_a, src2dst, offsets, scales_per_row=1):
     import torch
     M = T * K
@@ -293,9 +308,11 @@ def moe_grouped_gemm_rows(A_tok, row_token, scale_a, B, scale_b, offsets, epilog
     E, N, Kd2 = B.shape
     if Kd != Kd2:
         raise ValueError("moe_grouped_gemm_rows: K mismatch")
+    cols = N // 2 if epilogue == EPI_SILU_MUL else N
     if C is None:
-        cols = N // 2 if epilogue == EPI_SILU_MUL else N
         C = torch.empty((M, cols), dtype=torch.bfloat16, device=A_tok.device)
+    _gemm_bufs("moe_grouped_gemm_rows", M, N, E, cols, scale_a, M, scale_b, E * N, offsets, C,
+               row_amax)
     _check("moe_grouped_gemm_rows", load().moe_grouped_gemm_rows(
         _ptr(_u8(A_tok)), T, _ptr(row_token), _ptr(scale_a), _ptr(_u8(B)), _ptr(scale_b),
         _ptr(offsets), M, N, Kd, E, epilogue, _ptr(C), _ptr(row_amax), _stream(stream)))
@@ -310,9 +327,11 @@ def moe_grouped_gemm(A, scale_a, B, scale_b, offsets, epilogue=EPI_BF16, C=None,
     E, N, Kd2 = B.shape
     if Kd2 != Kd:
         raise ValueError("moe_grouped_gemm: K mismatch")
+    cols = N // 2 if epilogue == EPI_SILU_MUL else N
     if C is None:
-        cols = N // 2 if epilogue == EPI_SILU_MUL else N
         C = torch.empty((M, cols), dtype=torch.bfloat16, device=A.device)
+    _gemm_bufs("moe_grouped_gemm", M, N, E, cols, scale_a, M, scale_b, E * N, offsets, C,
+               row_amax)
     _check("moe_grouped_gemm", load().moe_grouped_gemm(
         _ptr(_u8(A)), _ptr(scale_a), _ptr(_u8(B)), _ptr(scale_b), _ptr(offsets), M, N, Kd, E,
         epilogue, _ptr(C), _ptr(row_amax), _stream(stream)))
@@ -325,6 +344,11 @@ def moe_act_quant(h, row_amax=None, q=None, scale=None, stream=None):
     M, I = h.shape
     q = torch.empty((M, I), dtype=torch.uint8, device=h.device) if q is None else q
     scale = torch.empty(M, dtype=torch.float32, device=h.device) if scale is None else scale
+    _need_cuda(q, scale)
+    _need_buf("moe_act_quant", "q", q, M * I, (torch.uint8, torch.float8_e4m3fn))
+    _need_buf("moe_act_quant", "scale", scale, M, (torch.float32,))
+    if row_amax is not None:
+        _need_buf("moe_act_quant", "row_amax", row_amax, M, (torch.float32,))
     _check("moe_act_quant", load().moe_act_quant(
         _ptr(h), _ptr(row_amax), M, I, _ptr(_u8(q)), _ptr(scale), _stream(stream)))
     return q, scale
@@ -336,6 +360,11 @@ def moe_unpermute_sum(down, src2dst, topk_w, out=None, stream=None):
     T, K = topk_w.shape
     H = down.shape[1]
     out = torch.empty((T, H), dtype=torch.bfloat16, device=down.device) if out is None else out
+    _need_cuda(out)
+    _need_buf("moe_unpermute_sum", "down", down, T * K * H, (torch.bfloat16,))
+    _need_buf("moe_unpermute_sum", "src2dst", src2dst, T * K, (torch.int32,))
+    _need_buf("moe_unpermute_sum", "topk_w", topk_w, T * K, (torch.float32,))
+    _need_buf("moe_unpermute_sum", "out", out, T * H, (torch.bfloat16,))
     _check("moe_unpermute_sum", load().moe_unpermute_sum(
         _ptr(down), _ptr(src2dst), _ptr(topk_w), T, K, H, _ptr(out), _stream(stream)))
     return out
@@ -363,6 +392,7 @@ def moe_forward(x, logits, bias, w13, s13, w2, s2, num_groups, topk_group, top_k
     _need_cuda(x, logits, bias, w13, s13, w2, s2, out, workspace)
     T, H, I, E = _dims(x, logits, w13, w2)
     out = torch.empty((T, H), dtype=torch.bfloat16, device=x.device) if out is None else out
+    _need_buf("moe_forward", "out", out, T * H, (torch.bfloat16,))
     nws = moe_workspace_size(T, H, I, E, top_k)
     if workspace is None:
         workspace = torch.empty(nws, dtype=torch.uint8, device=x.device)
@@ -400,6 +430,7 @@ def moe_forward_shared(x, logits, bias, w13, s13, w2, s2, n_shared, num_groups, 
     _need_cuda(x, logits, bias, w13, s13, w2, s2, out, workspace)
     T, H, I, E = _dims(x, logits, w13, w2, n_shared)
     out = torch.empty((T, H), dtype=torch.bfloat16, device=x.device) if out is None else out
+    _need_buf("moe_forward_shared", "out", out, T * H, (torch.bfloat16,))
     if workspace is None:
         nws = moe_workspace_size(T, H, I, E + n_shared, top_k + n_shared)
         workspace = torch.empty(nws, dtype=torch.uint8, device=x.device)
@@ -465,9 +496,11 @@ def moe_grouped_gemm_block(A, scale_a, B, scale_b, offsets, epilogue=EPI_BF16, C
     E, N, Kd2 = B.shape
     if Kd2 != Kd:
         raise ValueError("moe_grouped_gemm_block: K mismatch")
+    cols = N // 2 if epilogue == EPI_SILU_MUL else N
     if C is None:
-        cols = N // 2 if epilogue == EPI_SILU_MUL else N
         C = torch.empty((M, cols), dtype=torch.bfloat16, device=A.device)
+    _gemm_bufs("moe_grouped_gemm_block", M, N, E, cols, scale_a, M * (Kd // 128), scale_b,
+               E * (N // 128) * (Kd // 128), offsets, C, None)
     _check("moe_grouped_gemm_block", load().moe_grouped_gemm_block(
         _ptr(_u8(A)), _ptr(scale_a), _ptr(_u8(B)), _ptr(scale_b), _ptr(offsets), M, N, Kd, E,
         epilogue, _ptr(C), _stream(stream)))
@@ -482,6 +515,9 @@ def moe_act_quant_block(h, q=None, scale=None, stream=None):
     q = torch.empty((M, I), dtype=torch.uint8, device=h.device) if q is None else q
     if scale is None:
         scale = torch.empty((M, I // 128), dtype=torch.float32, device=h.device)
+    _need_cuda(q, scale)
+    _need_buf("moe_act_quant_block", "q", q, M * I, (torch.uint8, torch.float8_e4m3fn))
+    _need_buf("moe_act_quant_block", "scale", scale, M * (I // 128), (torch.float32,))
     _check("moe_act_quant_block", load().moe_act_quant_block(
         _ptr(h), M, I, _ptr(_u8(q)), _ptr(scale), _stream(stream)))
     return q, scale
@@ -499,6 +535,7 @@ def moe_forward_block(x, logits, bias, w13, s13, w2, s2, n_shared, num_groups, t
     _need_cuda(x, logits, bias, w13, s13, w2, s2, out, workspace)
     T, H, I, E = _dims(x, logits, w13, w2, n_shared)
     out = torch.empty((T, H), dtype=torch.bfloat16, device=x.device) if out is None else out
+    _need_buf("moe_forward_block", "out", out, T * H, (torch.bfloat16,))
     if workspace is None:
         nws = moe_block_workspace_size(T, H, I, E + n_shared, top_k + n_shared)
         workspace = torch.empty(nws, dtype=torch.uint8, device=x.device)
@@ -594,9 +631,12 @@ def moe_grouped_gemm_nvfp4(A, sfa, ga, B, sfb, gb, offsets, epilogue=EPI_BF16, C
     M = A.shape[0]
     E, N, kb = B.shape
     Kd = 2 * kb
+    cols = N // 2 if epilogue == EPI_SILU_MUL else N
     if C is None:
-        cols = N // 2 if epilogue == EPI_SILU_MUL else N
         C = torch.empty((M, cols), dtype=torch.bfloat16, device=A.device)
+    _gemm_bufs("moe_grouped_gemm_nvfp4", M, N, E, cols, sfa, M * (Kd // 16), sfb,
+               E * N * (Kd // 16), offsets, C, None, scale_dtypes=(torch.uint8,))
+    _need_buf("moe_grouped_gemm_nvfp4", "gb", gb, E, (torch.float32,))
     _check("moe_grouped_gemm_nvfp4", load().moe_grouped_gemm_nvfp4(
         _ptr(A), _ptr(sfa), float(ga), _ptr(B), _ptr(sfb), _ptr(gb), _ptr(offsets), M, N, Kd, E,
         epilogue, _ptr(C), _stream(stream)))
@@ -618,6 +658,7 @@ def moe_forward_nvfp4(x, logits, bias, w13, s13, g13, w2, s2, g2, ga1, ga2, n_sh
     E = logits.shape[1]
     I = w2.shape[2] * 2
     out = torch.empty((T, H), dtype=torch.bfloat16, device=x.device) if out is None else out
+    _need_buf("moe_forward_nvfp4", "out", out, T * H, (torch.bfloat16,))
     if workspace is None:
         nws = moe_nvfp4_workspace_size(T, H, I, E + n_shared, top_k + n_shared)
         workspace = torch.empty(nws, dtype=torch.uint8, device=x.device)

@@ -332,6 +332,34 @@ def test_binding_rejects_undersized_prereorder_buffers():
                       scales_per_row=2)
 
 
+def test_binding_rejects_undersized_gemm_buffers():
+    """The grouped GEMM wrappers check every scale, offset and output tensor
+    against what the kernels read and write, before any library call."""
+    import torch
+    M, N, E, cols = 10, 256, 4, 128
+    ok = dict(scale_a=torch.zeros(M, dtype=torch.float32),
+              scale_b=torch.zeros(E * N, dtype=torch.float32),
+              offsets=torch.zeros(E + 1, dtype=torch.int32),
+              C=torch.zeros((M, cols), dtype=torch.bfloat16), row_amax=None)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        moe._gemm_bufs("f", M, N, E, cols, a["scale_a"], M, a["scale_b"], E * N, a["offsets"],
+                       a["C"], a["row_amax"])
+
+    call()
+    call(row_amax=torch.zeros(M, dtype=torch.float32))
+    bad = [("scale_a", torch.zeros(M - 1, dtype=torch.float32)),
+           ("scale_b", torch.zeros(E * N, dtype=torch.float16)),
+           ("offsets", torch.zeros(E, dtype=torch.int32)),
+           ("C", torch.zeros((M, cols - 1), dtype=torch.bfloat16)),
+           ("C", torch.zeros((M, cols), dtype=torch.float32)),
+           ("row_amax", torch.zeros(M - 1, dtype=torch.float32))]
+    for name, t in bad:
+        with pytest.raises(ValueError, match=name):
+            call(**{name: t})
+
+
 def _desc(**kw):
     d = dict(quant=moe.QUANT_TOKEN, T=16, H=128, I=64, E=8, n_shared=0, num_groups=1,
              topk_group=1, top_k=2, scoring=0, renormalize=1, routed_scaling_factor=1.0,
