@@ -6,9 +6,9 @@
 //
 // The scales change every 128 channels of K, so the tensor cores cannot keep
 // one accumulator across K. A K block is exactly one pipeline stage: the MMA
-// thread writes each block's partial sum afresh into one of four TMEM
-// buffers, and the epilogue warps fold it into fp32 registers while the MMA
-// fills the next buffers.
+// thread writes each block's partial sum afresh into one of the TMEM partial
+// buffers (2 of 256 columns, or 4 of 128), and the epilogue warps fold it
+// into fp32 registers while the MMA fills the next one.
 //
 // Orientation: tokens are the MMA's M side (128 rows per tile) and weights
 // its N side: 256 rows (two weight scale blocks; SiLU: four groups of 32 gate
@@ -23,15 +23,16 @@
 // One persistent CTA per SM (tcgen05.mma.cta_group::1), 384 threads:
 //   warp 0      TMA producer (one K block of tokens and weights per stage)
 //   warp 1      MMA issuer (K = 32 x 4 per K block) into TMEM partial buffer
-//               kb % (512 / N)
+//               kb % (512 / weight rows per tile)
 //   warps 2, 3  idle (they complete warpgroup 0, which hands its registers
 //               to the epilogue)
 //   warps 4..11 epilogue: warp w reads TMEM lane quadrant w % 4 (32 token
 //               rows) and the columns of its half (w - 4) / 4 (one scale
 //               block), folds each K block's partial with its row's factor
-//               (holding the half's 128 fp32 sums in registers), and at the
-//               tile's end writes its row segment (SiLU*mul of its gate/up
-//               pairs, or bf16 outputs) with 16-byte stores.
+//               (holding the half's fp32 sums in registers: 128 with
+//               256-row tiles), and at the tile's end writes its row segment
+//               (SiLU*mul of its gate/up pairs, or bf16 outputs) through a
+//               2 KB shared-memory slot, 8 rows x 64 bytes per store.
 // Every wait is bounded.
 #include <cuda.h>
 
@@ -60,9 +61,7 @@ constexpr int WG0_REGS = 88;
 constexpr int EPI_REGS = 208;
 static_assert(128 * WG0_REGS + 32 * EW * EPI_REGS == BTHREADS * LAUNCH_REGS,
               "register split must add up to the launch's registers");
-#ifndef BLK_CW
-#define BLK_CW 16  // TMEM columns per epilogue load
-#endif
+constexpr int BLK_CW = 16;  // TMEM columns per epilogue load (32 measured slower)
 
 // NW weight rows per tile (MMA N): 256 when N allows (two scale blocks, a
 // quarter fewer bytes staged per MMA), else 128. TMEM holds 512 / NW partial
