@@ -16,7 +16,7 @@
 // E4M3 codes. Kd % 256 == 0, so a 128-byte K chunk (256 elements) is whole.
 //
 // Design (one persistent CTA per SM, 320 threads, single-CTA MMAs):
-//   warp 0      TMA producer, one K chunk per stage: the tile's 128 weight
+//   warp 0      TMA producer, one or two K chunks per stage: the tile's 128 weight
 //               rows (one box), their scales (2 KB, already in copy order,
 //               see below), the token rows (64/32/16-row boxes) and their
 //               scale bytes (row-major).
@@ -68,10 +68,12 @@ constexpr int SCALE_WARP0 = 6;
 constexpr int SFROW = 16;      // scale bytes per row per 128-byte K chunk
 constexpr uint32_t F_SFCHUNK = 32;  // scale columns per K chunk: 16 for the weights, 16 tokens
 constexpr uint32_t F_TMEM = 512;
-// Tile width FBN (tokens, MMA N) and pipeline depth FSTAGES per launch:
-// few tokens per expert (decode) 64 x 6 stages, the weight stream's bytes in
-// flight being what bounds it; otherwise 128 x 5. Tensor memory: two FBN-
-// column accumulators, then FSTAGES x 32 scale columns.
+// Tile width FBN (tokens, MMA N), pipeline depth FSTAGES and K chunks per
+// stage FKC per launch: few tokens per expert (decode) 64 tokens x 3 stages
+// of 2 chunks, the weight stream's bytes in flight being what bounds it;
+// otherwise 128 x 2 stages of 2 chunks; one chunk per stage (6 / 5 stages)
+// when the chunk count is odd. Tensor memory: two FBN-column accumulators,
+// then FSTAGES x FKC x 32 scale columns.
 
 struct FMaps {
   CUtensorMap w;          // weights, one 128-byte chunk of 128 rows per box
@@ -535,10 +537,10 @@ cudaError_t launch_grouped_gemm_nvfp4(const void* A, const uint8_t* sfa, float g
   const bool silu = (epilogue == MOE_EPI_SILU_MUL);
   const uint64_t kb = (uint64_t)Kd / 2;   // bytes of a row
   const uint64_t sc = (uint64_t)Kd / 16;  // scale bytes of a row
-  // few tokens per expert: two K chunks per stage (256 contiguous bytes of
-  // every weight row) when the chunk count is even
+  // two K chunks per stage (256 contiguous bytes of every weight row, half the
+  // barrier round trips per byte) when the chunk count is even
   const bool many = gemm_many_rows(M, E);
-  const int fkc = (!many && (Kd / 256) % 2 == 0) ? 2 : 1;
+  const int fkc = ((Kd / 256) % 2 == 0) ? 2 : 1;
   FMaps maps;
   if (!make_tma_map_weights(&maps.w, B, silu, (uint64_t)E, (uint64_t)N, kb, (uint32_t)fkc))
     return cudaErrorNotSupported;
@@ -568,6 +570,9 @@ cudaError_t launch_grouped_gemm_nvfp4(const void* A, const uint8_t* sfa, float g
   if (!many)
     return silu ? launch_f<true, 64, 6, 1>(maps, p, M, E, st, pdl)
                 : launch_f<false, 64, 6, 1>(maps, p, M, E, st, pdl);
+  if (fkc == 2)
+    return silu ? launch_f<true, 128, 2, 2>(maps, p, M, E, st, pdl)
+                : launch_f<false, 128, 2, 2>(maps, p, M, E, st, pdl);
   return silu ? launch_f<true, 128, 5, 1>(maps, p, M, E, st, pdl)
               : launch_f<false, 128, 5, 1>(maps, p, M, E, st, pdl);
 }
