@@ -16,10 +16,10 @@
 // E4M3 codes. Kd % 256 == 0, so a 128-byte K chunk (256 elements) is whole.
 //
 // Design (one persistent CTA per SM, 320 threads, single-CTA MMAs):
-//   warp 0      TMA producer, one or two K chunks per stage: the tile's 128 weight
-//               rows (one box), their scales (2 KB, already in copy order,
-//               see below), the token rows (64/32/16-row boxes) and their
-//               scale bytes (row-major).
+//   warp 0      TMA producer, one or two K chunks per stage: the tile's 128
+//               weight rows (one box), their scales (2 KB per chunk, already
+//               in copy order, see below), the token rows (64/32/16-row
+//               boxes) and their scale bytes (row-major).
 //   warps 6..9  token scales, one warp per 32-lane quadrant of tensor
 //               memory: each writes the stage's token scales from registers
 //               (tcgen05.st) into its quadrant in the layout the MMA reads
