@@ -721,23 +721,23 @@ bool make_tma_map_weight_scales(CUtensorMap* m, const void* base, bool silu, uin
 }
 
 bool make_tma_map_weights_rows(CUtensorMap* m, const void* base, uint64_t E, uint64_t N,
-                               uint64_t Kd, uint32_t rows) {
-  // [Kd/128][E*N][128]: one 128-byte K chunk of `rows` consecutive rows per box
+                               uint64_t Kd, uint32_t rows, uint32_t kc) {
+  // [Kd/128][E*N][128]: kc 128-byte K chunks of `rows` consecutive rows per box
   const uint64_t KB = Kd / BK;
   const cuuint64_t dims[3] = {BK, E * N, KB};
   const cuuint64_t strides[2] = {Kd, BK};
-  const cuuint32_t box[3] = {BK, rows, 1};
+  const cuuint32_t box[3] = {BK, rows, kc};
   return encode_u8(m, base, 3, dims, strides, box);
 }
 
 bool make_tma_map_weights_gateup(CUtensorMap* m, const void* base, uint64_t E, uint64_t N,
-                                 uint64_t Kd, uint32_t jrows) {
+                                 uint64_t Kd, uint32_t jrows, uint32_t kc) {
   // [E][Kd/128][2][I][128] (as the SiLU stage view), boxes of jrows gate rows
-  // then the matching jrows up rows of one 128-byte chunk
+  // then the matching jrows up rows, for kc 128-byte chunks
   const uint64_t I = N / 2, KB = Kd / BK;
   const cuuint64_t dims[5] = {BK, I, 2, KB, E};
   const cuuint64_t strides[4] = {Kd, I * Kd, BK, 2 * I * Kd};
-  const cuuint32_t box[5] = {BK, jrows, 2, 1, 1};
+  const cuuint32_t box[5] = {BK, jrows, 2, kc, 1};
   return encode_u8(m, base, 5, dims, strides, box);
 }
 

@@ -162,15 +162,16 @@ bool make_tma_map_u8(CUtensorMap* m, const void* base, uint64_t rows, uint64_t c
 // swizzle, zero fill) for four-row gathers.
 bool make_tma_map_rows(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols);
 
-// Host: weights [E, N, Kd] (Kd % 128 == 0), one 128-byte K chunk of `rows`
+// Host: weights [E, N, Kd] (Kd % 128 == 0), kc 128-byte K chunks of `rows`
 // (<= 256) consecutive rows per box.
 bool make_tma_map_weights_rows(CUtensorMap* m, const void* base, uint64_t E, uint64_t N,
-                               uint64_t Kd, uint32_t rows);
+                               uint64_t Kd, uint32_t rows, uint32_t kc = 1);
 
 // Host: w13 [E, 2I, Kd] (Kd % 128 == 0) viewed per 128-byte K chunk, boxes of
-// jrows (<= 256) gate rows followed by the matching jrows up rows.
+// jrows (<= 256) gate rows followed by the matching jrows up rows, for kc
+// consecutive chunks.
 bool make_tma_map_weights_gateup(CUtensorMap* m, const void* base, uint64_t E, uint64_t N,
-                                 uint64_t Kd, uint32_t jrows);
+                                 uint64_t Kd, uint32_t jrows, uint32_t kc = 1);
 
 // Host: w13 [E, 2I, Kd] (Kd % 128 == 0) viewed per 128-byte K chunk, boxes of
 // 32 gate rows followed by the matching 32 up rows.

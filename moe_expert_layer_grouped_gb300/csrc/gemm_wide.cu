@@ -42,15 +42,18 @@ using namespace gemm_common;
 
 constexpr int WEW = 8;               // epilogue warps: two per TMEM lane quadrant
 constexpr int WT = 64 + 32 * WEW;
-constexpr int WSTAGES = 4;
+// K blocks per pipeline stage: 2 (two stages of 96 KB) measured slower than
+// 1 (four of 48 KB): DeepSeek-V3 prefill w13 1.56 against 1.48 ms
+constexpr int WKC = 1;
+constexpr int WSTAGES = 4 / WKC;    // 192 KB of stages
 constexpr int WROWS = 256;          // weight rows per CTA (two accumulators)
 constexpr int WBN = 256;            // tokens per pair tile (MMA N), half per CTA
 constexpr uint32_t WACC = 256;      // TMEM columns per accumulator
 constexpr uint32_t WTMEM = 2 * WACC;
 
 struct WSmem {
-  uint8_t w[WSTAGES][WROWS * BK];      // this CTA's 256 weight rows, one K block
-  uint8_t x[WSTAGES][(WBN / 2) * BK];  // this CTA's half of the tile's tokens
+  uint8_t w[WSTAGES][WKC][WROWS * BK];      // this CTA's 256 weight rows, WKC K blocks
+  uint8_t x[WSTAGES][WKC][(WBN / 2) * BK];  // this CTA's half of the tile's tokens
   uint16_t stage_out[WEW][32 * 32];    // per epilogue warp: bf16 [token][32 columns]
   uint64_t full[WSTAGES];              // only the even CTA's are armed and waited
   uint64_t empty[WSTAGES];
@@ -87,7 +90,7 @@ __global__ void __launch_bounds__(WT, 1)
   const int warp = tid >> 5;
   const int lane = tid & 31;
   const int E = p.E;
-  const int KB = p.KB;
+  const int KS = (p.KB + WKC - 1) / WKC;  // pipeline stages per tile
 
   if (warp == 0 && lane == 0) {
     ptx::prefetch_tensormap(&maps.w);
@@ -135,12 +138,12 @@ __global__ void __launch_bounds__(WT, 1)
       // token rows of the MMA: a multiple of 32, half in each CTA
       const int rows = (t.ntok + 31) & ~31;
       const int half = rows / 2;
-      const uint32_t bytes = (uint32_t)(2 * WROWS + rows) * BK;  // both CTAs' loads
+      const uint32_t bytes = WKC * (uint32_t)(2 * WROWS + rows) * BK;  // both CTAs' loads
       const uint64_t pw = t.nch == 1 ? pol_w1 : pol_w;
       const int blk = t.nb * 2 + rank;       // this CTA's 256-row weight block
       const int jq = blk * 128;              // SiLU: its first j
       const int y0 = t.e * p.N + blk * WROWS;  // bf16: its first weight row
-      for (int kb = 0; kb < KB; ++kb) {
+      for (int ks = 0; ks < KS; ++ks) {
         const bool got = ptx::mbar_wait(&sm.empty[s], ph ^ 1u, &sm.abort, WAIT_NS);
         if (!__all_sync(kFull, got)) {
           ok = false;
@@ -153,18 +156,22 @@ __global__ void __launch_bounds__(WT, 1)
             armed |= 1u << s;
             armed_par = (armed_par & ~(1u << s)) | (ph << s);
           }
-          if (SILU)  // 128 gate rows, then the matching 128 up rows
-            ptx::tma_load_5d_pair(sm.w[s], &maps.w, fb, 0, jq, 0, kb, t.e, pw);
+          // the stage's WKC K blocks (past Kd: zero-filled, adding nothing)
+          if (SILU)  // per K block 128 gate rows, then the matching 128 up rows
+            ptx::tma_load_5d_pair(sm.w[s][0], &maps.w, fb, 0, jq, 0, ks * WKC, t.e, pw);
           else
-            ptx::tma_load_3d_pair(sm.w[s], &maps.w, fb, 0, y0, kb, pw);
-          int r = 0;
+            ptx::tma_load_3d_pair(sm.w[s][0], &maps.w, fb, 0, y0, ks * WKC, pw);
 #pragma unroll
-          for (int i = 0; i < NXBOX; ++i) {
-            const int box = 64 >> i;
-            while (half - r >= box) {
-              ptx::tma_load_2d_pair(sm.x[s] + r * BK, &maps.x[i], fb, kb * BK,
-                                    t.tok0 + rank * half + r, pol_x);
-              r += box;
+          for (int kc = 0; kc < WKC; ++kc) {
+            int r = 0;
+#pragma unroll
+            for (int i = 0; i < NXBOX; ++i) {
+              const int box = 64 >> i;
+              while (half - r >= box) {
+                ptx::tma_load_2d_pair(sm.x[s][kc] + r * BK, &maps.x[i], fb, (ks * WKC + kc) * BK,
+                                      t.tok0 + rank * half + r, pol_x);
+                r += box;
+              }
             }
           }
         }
@@ -194,21 +201,24 @@ __global__ void __launch_bounds__(WT, 1)
           break;
         }
         ptx::tc_fence_after();
-        for (int kb = 0; kb < KB; ++kb) {
+        for (int ks = 0; ks < KS; ++ks) {
           if (!ptx::mbar_wait(&sm.full[s], ph, &sm.abort, WAIT_NS)) {
             ok = false;
             break;
           }
           ptx::tc_fence_after();
-          const uint32_t b0 = ptx::smem_u32(sm.x[s]);
 #pragma unroll
-          for (int acc = 0; acc < 2; ++acc) {
-            const uint32_t a0 = ptx::smem_u32(sm.w[s]) + (uint32_t)acc * 128 * BK;
+          for (int kc = 0; kc < WKC; ++kc) {
+            const uint32_t b0 = ptx::smem_u32(sm.x[s][kc]);
 #pragma unroll
-            for (int kk = 0; kk < BK / 32; ++kk)
-              ptx::mma_e4m3_pair(tmem + (uint32_t)acc * WACC, ptx::sdesc_sw128(a0 + kk * 32),
-                                 ptx::sdesc_sw128(b0 + kk * 32), idesc,
-                                 (kb | kk) != 0 ? 1u : 0u);
+            for (int acc = 0; acc < 2; ++acc) {
+              const uint32_t a0 = ptx::smem_u32(sm.w[s][kc]) + (uint32_t)acc * 128 * BK;
+#pragma unroll
+              for (int kk = 0; kk < BK / 32; ++kk)
+                ptx::mma_e4m3_pair(tmem + (uint32_t)acc * WACC, ptx::sdesc_sw128(a0 + kk * 32),
+                                   ptx::sdesc_sw128(b0 + kk * 32), idesc,
+                                   (ks | kc | kk) != 0 ? 1u : 0u);
+            }
           }
           issued = true;
           ptx::mma_commit_pair_mcast(&sm.empty[s], kPair);  // frees the stage in both CTAs
@@ -405,9 +415,10 @@ cudaError_t launch_grouped_gemm_wide(const void* A, const float* scale_a, const 
   const bool silu = (epilogue == MOE_EPI_SILU_MUL);
   Maps maps;
   const bool wok =
-      silu ? make_tma_map_weights_gateup(&maps.w, B, (uint64_t)E, (uint64_t)N, (uint64_t)Kd, 128)
+      silu ? make_tma_map_weights_gateup(&maps.w, B, (uint64_t)E, (uint64_t)N, (uint64_t)Kd, 128,
+                                         WKC)
            : make_tma_map_weights_rows(&maps.w, B, (uint64_t)E, (uint64_t)N, (uint64_t)Kd,
-                                       (uint32_t)WROWS);
+                                       (uint32_t)WROWS, WKC);
   if (!wok) return cudaErrorNotSupported;
   for (int i = 0; i < NXBOX; ++i)
     if (!make_tma_map_u8(&maps.x[i], A, (uint64_t)M, (uint64_t)Kd, 64u >> i))
