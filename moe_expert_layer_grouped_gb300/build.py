@@ -18,7 +18,8 @@ LIB_DIR = os.path.join(HERE, "_lib")
 LIB = os.path.join(LIB_DIR, "libmoe_gb300.so")
 
 SOURCES = ["api.cu", "gate.cu", "permute.cu", "gemm.cu", "gemm_block.cu", "act_quant.cu",
-           "unpermute.cu", "ep.cu", "gemm_nvfp4.cu", "pipeline.cu", "gemm_wide.cu"]
+           "unpermute.cu", "ep.cu", "gemm_nvfp4.cu", "pipeline.cu", "gemm_wide.cu",
+           "gemm_nvfp4_wide.cu"]
 # every header beside the sources is a rebuild input (a new one cannot be missed)
 HEADERS = sorted(f for f in os.listdir(SRC) if f.endswith((".cuh", ".h")))
 

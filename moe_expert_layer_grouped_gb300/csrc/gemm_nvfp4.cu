@@ -534,6 +534,11 @@ cudaError_t launch_grouped_gemm_nvfp4(const void* A, const uint8_t* sfa, float g
                                       int epilogue, void* C, int* err, cudaStream_t st, bool pdl,
                                       bool early_table) {
   if (M == 0) return cudaSuccess;
+  // many rows per expert: 256 weight rows per CTA (gemm_nvfp4_wide.cu), which
+  // stages each token row half as often
+  if (gemm_nvfp4_wide_applies(M, N, Kd, E, epilogue))
+    return launch_grouped_gemm_nvfp4_wide(A, sfa, ga, B, sfb, gb, offsets, M, N, Kd, E, epilogue,
+                                          C, err, st, pdl, early_table);
   const bool silu = (epilogue == MOE_EPI_SILU_MUL);
   const uint64_t kb = (uint64_t)Kd / 2;   // bytes of a row
   const uint64_t sc = (uint64_t)Kd / 16;  // scale bytes of a row

@@ -111,6 +111,17 @@ cudaError_t launch_grouped_gemm_nvfp4(const void* A, const uint8_t* sfa, float g
                                       int epilogue, void* C, int* err, cudaStream_t st,
                                       bool pdl = false, bool early_table = false);
 
+// gemm_nvfp4_wide.cu: the same GEMM with 256 weight rows per CTA, for many
+// rows per expert (gemm_many_rows) when the weight rows split into 256-row
+// tiles (SiLU: I % 128 == 0, bf16: N % 256 == 0); launch_grouped_gemm_nvfp4
+// dispatches to it.
+bool gemm_nvfp4_wide_applies(int M, int N, int Kd, int E, int epilogue);
+cudaError_t launch_grouped_gemm_nvfp4_wide(const void* A, const uint8_t* sfa, float ga,
+                                           const void* B, const uint8_t* sfb, const float* gb,
+                                           const int32_t* offsets, int M, int N, int Kd, int E,
+                                           int epilogue, void* C, int* err, cudaStream_t st,
+                                           bool pdl, bool early_table);
+
 // unpermute.cu
 cudaError_t launch_unpermute_sum(const void* down, const int32_t* src2dst, const float* w,
                                  int T, int K, int H, void* out, int* err, cudaStream_t st,

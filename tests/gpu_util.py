@@ -56,7 +56,8 @@ def gemm_token_tile(M, E, quant="token"):
     GEMM; otherwise it takes 256-token tiles on CTA pairs (every workload here
     has an even number of weight blocks). The block-scaled GEMM always takes
     128-token tiles (tokens are its MMA's M side) on single CTAs; the NVFP4
-    GEMM 64- or 128-token tiles on single CTAs."""
+    GEMM 64- or 128-token tiles on single CTAs (128- or 256-row weight
+    tiles: the token chunks are the same)."""
     if quant == "nvfp4":
         return (64 if M <= 32 * E else 128), False
     if quant == "block":

@@ -166,6 +166,12 @@ FP4_SHAPES = [
     # wrapping within a tile), and one per stage (odd chunk count)
     ([3, 0, 9, 1, 5, 2, 0, 7], 256, 2048),
     ([3, 9, 1, 5], 256, 768),
+    # many rows per expert with 256-row weight tiles (SiLU: I % 128 == 0,
+    # bf16: N % 256 == 0): the two-accumulator kernel. Three 256-row tiles,
+    # five K chunks on a three-stage ring (it wraps inside a tile), experts of
+    # 0, 1 and 511 tokens (four 128-token chunks); one K chunk per tile.
+    ([260, 0, 129, 511, 1, 40], 768, 1280),
+    ([1000, 300], 512, 256),
 ]
 
 
