@@ -209,13 +209,14 @@ __device__ __forceinline__ void quant_scatter(const __nv_bfloat16* __restrict__ 
     scale_a[dst[tid]] = sc;
     if (row_token != nullptr) row_token[dst[tid]] = t;
   }
+  const Recip rb = recip_bracket(sc);
 #pragma unroll
   for (int i = 0; i < VPT; ++i) {
     const int idx = tid + i * NT;
     if (idx < nvec) {
       float f[8];
       bf16x8_to_f32(v[i], f);
-      const uint2 q = quant8(f, sc);
+      const uint2 q = quant8(f, rb);
       if (row_token != nullptr) {
         *reinterpret_cast<uint2*>(a_q + (int64_t)t * H + (int64_t)idx * 8) = q;
         continue;
@@ -242,6 +243,7 @@ __device__ __forceinline__ void quant_scatter_nvfp4(const __nv_bfloat16* __restr
   const int tid = threadIdx.x;
   const int nvec = H >> 3;
   const uint4* xr = reinterpret_cast<const uint4*>(x + (int64_t)t * H);
+  const Recip rg = recip_bracket(g);
   __syncthreads();  // dst[] is complete
 #pragma unroll
   for (int i = 0; i < VPT; ++i) {
@@ -254,7 +256,7 @@ __device__ __forceinline__ void quant_scatter_nvfp4(const __nv_bfloat16* __restr
     }
     m = fmaxf(m, __shfl_xor_sync(kFull, m, 1));
     if (idx < nvec) {
-      const uint32_t code = nvfp4_scale_code(m, g);
+      const uint32_t code = nvfp4_scale_code(m, g, rg);
       const uint32_t q = nvfp4_codes8(f, __fmul_rn(e4m3_value(code), g));
       for (int k = 0; k < K; ++k) {
         const int d = dst[k];

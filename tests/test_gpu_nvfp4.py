@@ -39,9 +39,13 @@ def _bf16_bits(a32):
         .view(torch.int16).numpy().view(np.uint16)
 
 
-def test_e2m1_conversion_of_every_bf16_in_range():
-    """Blocks of one 6.0 and 15 test values with g = 1: the block scale is
-    e4m3(6/6/1) = 1.0 exactly, so the codes are e2m1(v) of each bf16 v."""
+@pytest.mark.parametrize("g", [1.0, 1 + 2.0 ** -22, 1 - 2.0 ** -23, 1 + 2.0 ** -19])
+def test_e2m1_conversion_of_every_bf16_in_range(g):
+    """Blocks of one 6.0 and 15 test values: with g = 1 the block scale is
+    e4m3(6/6/1) = 1.0 exactly, so the codes are e2m1(v) of each bf16 v. A g
+    a few fp32 ulps from 1 keeps the scale code at 1.0 and moves the
+    quotients v / g of the bf16 values at e2m1 midpoints just to one side of
+    the boundary (within 2^-20 of it, or just outside for 2^-19)."""
     bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
     vals = (bits.astype(np.uint32) << 16).view(np.float32)
     keep = np.isfinite(vals) & (np.abs(vals) <= 6.0)
@@ -52,12 +56,14 @@ def test_e2m1_conversion_of_every_bf16_in_range():
     rows = blocks.reshape(-1, 256) if blocks.size % 256 == 0 else \
         np.concatenate([blocks.ravel(), np.zeros(256 - blocks.size % 256, np.float32)]).reshape(-1, 256)
     h = _bf16_bits(rows)
-    q, sf = moe.moe_act_quant_nvfp4(_t(h).view(torch.bfloat16), 1.0)
+    g32 = float(np.float32(g))
+    q, sf = moe.moe_act_quant_nvfp4(_t(h).view(torch.bfloat16), g32)
     torch.cuda.synchronize()
-    oq, osf = oracle.nvfp4_quant(h, 1.0)
+    oq, osf = oracle.nvfp4_quant(h, g32)
     assert np.array_equal(sf.cpu().numpy(), osf)
+    assert np.all(osf[:, 0] == 0x38)                 # e4m3 1.0 in every block
     got = _unpack(q)
-    exp = oracle.e2m1_encode(rows.astype(np.float32))
+    exp = oracle.e2m1_encode((rows.astype(np.float32) / np.float32(g32)).astype(np.float32))
     assert np.array_equal(oq, exp)                   # the oracle's quantiser agrees
     bad = np.argwhere(got != exp)
     assert bad.shape[0] == 0, (bad.shape[0], bad[:5].tolist())

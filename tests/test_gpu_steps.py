@@ -218,8 +218,37 @@ def test_fp8_encoder_matches_oracle_on_every_bf16():
     assert bad[0].size == 0, (h_bits[bad][:5], got[bad][:5], ref[bad][:5])
 
 
-@pytest.mark.parametrize("M,I", [(1, 32), (513, 2048), (4099, 14336), (64, 96)])
+@pytest.mark.parametrize("amax", [448.0 * (1 + 2.0 ** -21), 448.0 * (1 - 2.0 ** -22),
+                                  448.0 * (1 + 2.0 ** -19), 336.0 * (1 + 2.0 ** -21)])
+def test_fp8_encoder_near_rounding_boundaries(amax):
+    """Scales a few fp32 ulps from 1 (or 0.75) put the quotients of the bf16
+    values that are e4m3 midpoints within 2^-20 of a rounding boundary, on
+    either side of it: the codes are the encoder applied to the IEEE fp32
+    quotient x / scale, scale = amax / 448 as the kernel forms it."""
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    v = (bits.astype(np.uint32) << 16).view(np.float32)
+    bits = bits[np.isfinite(v) & (np.abs(v) <= 448.0)]
+    cols = 256
+    rows = -(-bits.size // cols)
+    h_bits = np.concatenate([bits, np.zeros(rows * cols - bits.size, np.uint16)]).reshape(rows, cols)
+    a32 = np.float32(amax)
+    q, s = moe.moe_act_quant(np_bf16_to_torch(h_bits, DEV),
+                             row_amax=torch.full((rows,), float(a32), device=DEV))
+    sc = a32 / np.float32(448.0)
+    assert np.all(s.cpu().numpy() == sc)
+    x = oracle.bf16_to_f64(h_bits).astype(np.float32)
+    ref = oracle.e4m3_encode((x / sc).astype(np.float32))
+    got = q.cpu().numpy()
+    bad = np.nonzero(got != ref)
+    assert bad[0].size == 0, (h_bits[bad][:5], got[bad][:5], ref[bad][:5])
+
+
+@pytest.mark.parametrize("M,I", [(1, 32), (513, 2048), (4099, 14336), (64, 96), (37, 512),
+                                 (300, 1024), (70, 4096), (33, 7168), (17, 12288), (5, 20480)])
 def test_act_quant_bit_exact(M, I):
+    """Every launch shape of the requant: a warp per row (up to 512
+    channels), a CTA of 64 threads holding 2 or 4 vectors each (up to 2048),
+    of 256 threads holding 2 to 8 (up to 16384), two passes beyond."""
     rng = np.random.default_rng(M)
     h = torch.from_numpy(rng.standard_normal((M, I)).astype(np.float32)
                          * 10.0 ** rng.uniform(-4, 2, (M, 1)).astype(np.float32)).to(torch.bfloat16)
