@@ -682,8 +682,16 @@ def run_ours(args):
     ms = ms_total / steps
     value = job_tokens_per_s(wl.T, world, ms)
 
+    # the clocks of the host-buffer runs too: they run right after the device-timed
+    # region, and a power cap reached there shows up only in them
+    e2e_clocks = ClockSampler(dev.index)
+    e2e_clocks.start()
+    time.sleep(0.3)
+    te0 = time.time()
     e2e_ms, e2e1_ms, h2d, d2h = time_e2e(r["layer"], r["batches"], steps, warmup, torch,
                                          barrier)
+    te1 = time.time()
+    e2e_clocks.stop()
     graph_ms = time_graph(r["layer"], r["batches"], steps, warmup, torch)
     e2e_ms = max_over_ranks(e2e_ms, dist if world > 1 else None, dev)
     e2e1_ms = max_over_ranks(e2e1_ms, dist if world > 1 else None, dev)
@@ -707,6 +715,7 @@ def run_ours(args):
         "e2e": {"value": round(job_tokens_per_s(wl.T, world, e2e_ms), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_ms, 5),
+                "clocks": e2e_clocks.summary(te0, te1),
                 "api": "MoELayer.forward_host_pipelined -> moe_forward_host_pipelined: every "
                        "step's x and logits copied in from pinned host memory and its output "
                        "copied back, batch i+1's inputs and batch i-1's output in flight "

@@ -197,11 +197,69 @@ __global__ void __launch_bounds__(kWarps * 32)
   }
 }
 
+// The same with a row per CTA, read once (as the FP8 requant): vector
+// u * NT + tid in registers, every load of the row issued before the first
+// is used; each eighth thread stores the scale bytes of four blocks (its own
+// and those of the threads 2, 4 and 6 above it) as one word.
+template <int V, int NT>
+__global__ void __launch_bounds__(NT)
+    act_quant_nvfp4_cta_kernel(const __nv_bfloat16* __restrict__ h, int I, float g,
+                               uint8_t* __restrict__ q, uint8_t* __restrict__ sf) {
+  chain_entry();
+  const int tid = threadIdx.x;
+  const int64_t row = blockIdx.x;
+  const int nvec = I >> 3;  // I % 256 == 0: a multiple of 32, validity is warp-uniform
+  const uint4* hr = reinterpret_cast<const uint4*>(h + row * I);
+  uint32_t* qr = reinterpret_cast<uint32_t*>(q + row * (I >> 1));
+  uint8_t* sr = sf + row * (I >> 4);
+  const Recip rg = recip_bracket(g);
+  uint4 raw[V];
+#pragma unroll
+  for (int u = 0; u < V; ++u) {
+    const int i = u * NT + tid;
+    if (i < nvec) raw[u] = __ldg(hr + i);
+  }
+#pragma unroll
+  for (int u = 0; u < V; ++u) {
+    const int i = u * NT + tid;
+    if (i >= nvec) break;  // warp-uniform
+    float f[8];
+    bf16x8_to_f32(raw[u], f);
+    float m = absmax8(f, 0.0f);
+    m = fmaxf(m, __shfl_xor_sync(kFull, m, 1));
+    const uint32_t code = nvfp4_scale_code(m, g, rg);
+    qr[i] = nvfp4_codes8(f, __fmul_rn(e4m3_value(code), g));
+    const uint32_t c2 = __shfl_down_sync(kFull, code, 2);
+    const uint32_t c4 = __shfl_down_sync(kFull, code, 4);
+    const uint32_t c6 = __shfl_down_sync(kFull, code, 6);
+    if ((tid & 7) == 0)
+      *reinterpret_cast<uint32_t*>(sr + (i >> 1)) = code | (c2 << 8) | (c4 << 16) | (c6 << 24);
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_act_quant_nvfp4(const void* h, int M, int I, float g, void* q, uint8_t* sf,
                                    cudaStream_t st, bool pdl) {
   if (M == 0) return cudaSuccess;
+  // a row per CTA held in registers up to 16384 channels (65536 x 2048:
+  // 64 threads of 4 vectors) when I % 256 == 0 (whole warps of vectors, and
+  // 4-byte-aligned words of scale bytes); a warp per row in steps of 4
+  // vectors a lane otherwise
+  const int nvec = I >> 3;
+  const __nv_bfloat16* hb = reinterpret_cast<const __nv_bfloat16*>(h);
+  uint8_t* qb = reinterpret_cast<uint8_t*>(q);
+#define MOE_AQF(V, NT) launch_kernel(act_quant_nvfp4_cta_kernel<V, NT>, dim3(M), dim3(NT), 0, \
+                                     st, pdl, hb, I, g, qb, sf)
+  if (I % 256 == 0) {
+    if (nvec <= 64 * 2) return MOE_AQF(2, 64);
+    if (nvec <= 64 * 4) return MOE_AQF(4, 64);
+    if (nvec <= 256 * 2) return MOE_AQF(2, 256);
+    if (nvec <= 256 * 4) return MOE_AQF(4, 256);
+    if (nvec <= 256 * 6) return MOE_AQF(6, 256);
+    if (nvec <= 256 * 8) return MOE_AQF(8, 256);
+  }
+#undef MOE_AQF
   const int blocks = (M + kWarps - 1) / kWarps;
   return launch_kernel(act_quant_nvfp4_kernel, dim3(blocks), dim3(kWarps * 32), 0, st, pdl,
                        reinterpret_cast<const __nv_bfloat16*>(h), M, I, g,

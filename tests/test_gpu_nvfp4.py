@@ -86,6 +86,25 @@ def test_act_quant_nvfp4_matches_oracle(g):
     assert np.array_equal(_unpack(q), oq)
 
 
+@pytest.mark.parametrize("M,I", [(70, 256), (33, 2048), (20, 4096), (9, 8192), (7, 12288),
+                                 (5, 14336), (3, 20480), (41, 96), (6, 2080)])
+def test_act_quant_nvfp4_every_launch_shape(M, I):
+    """A CTA per row of 64 threads holding 2 or 4 vectors each, of 256 threads
+    holding 2 to 8 (I % 256 == 0), and a warp per row beyond 16384 channels
+    or when I is not a multiple of 256."""
+    rng = np.random.default_rng(M + I)
+    x = rng.standard_normal((M, I)).astype(np.float32)
+    x *= (10.0 ** rng.uniform(-3, 2, (M, 1))).astype(np.float32)
+    x[0, 32:48] = 0.0
+    h = _bf16_bits(x)
+    g = 5.0 / (6 * 448)
+    q, sf = moe.moe_act_quant_nvfp4(_t(h).view(torch.bfloat16), g)
+    torch.cuda.synchronize()
+    oq, osf = oracle.nvfp4_quant(h, g)
+    assert np.array_equal(sf.cpu().numpy(), osf)
+    assert np.array_equal(_unpack(q), oq)
+
+
 @pytest.mark.parametrize("T,H,E,K", [(8, 256, 8, 2), (300, 512, 24, 6), (4099, 256, 64, 6)])
 def test_permute_quant_nvfp4_matches_oracle(T, H, E, K):
     rng = np.random.default_rng(T + H)
