@@ -445,6 +445,24 @@ MOE_API moe_status moe_grouped_gemm_nvfp4(const void* A, const uint8_t* sfa, flo
                                           const int32_t* offsets, int M, int N, int Kd, int E,
                                           int epilogue, void* C, void* stream);
 
+/*
+ * moe_test_gemm_nvfp4_timeout — failure-detection test of the NVFP4 GEMM
+ * pipelines (the pages have no counterpart), as moe_test_gemm_timeout:
+ * runs moe_grouped_gemm_nvfp4 (whichever kernel its shapes select), except
+ * that CTA 0 arms its pipeline stage number stall_stage (>= 0, counted over
+ * its tiles) but never issues that stage's loads. Its bounded waits run out
+ * (about 2 s), it sets MOE_DEV_PIPE_TIMEOUT, lets its issued copies and MMAs
+ * land, frees its tensor memory and exits; the other CTAs finish. Returns
+ * MOE_OK; moe_device_status then reports the timeout and the context stays
+ * usable. C is left partly written. The same argument checks as
+ * moe_grouped_gemm_nvfp4.
+ */
+MOE_API moe_status moe_test_gemm_nvfp4_timeout(const void* A, const uint8_t* sfa, float ga,
+                                               const void* B, const uint8_t* sfb,
+                                               const float* gb, const int32_t* offsets,
+                                               int M, int N, int Kd, int E, int epilogue,
+                                               void* C, int stall_stage, void* stream);
+
 /* Workspace bytes of moe_forward_nvfp4 (with shared experts pass E+n_shared
  * and top_k+n_shared). */
 MOE_API size_t moe_nvfp4_workspace_size(int T, int H, int I, int E, int K);

@@ -23,7 +23,7 @@ __all__ = [
     "moe_permute_quant_noalloc", "moe_permute_quant_rows", "moe_grouped_gemm_rows",
     "moe_permute_quant_nvfp4", "moe_act_quant_nvfp4", "moe_grouped_gemm_nvfp4",
     "moe_nvfp4_workspace_size", "moe_forward_nvfp4", "moe_forward_nvfp4_host",
-    "moe_nvfp4_arrange_scales",
+    "moe_nvfp4_arrange_scales", "moe_test_gemm_nvfp4_timeout",
     "moe_act_quant", "moe_unpermute_sum", "moe_workspace_size", "moe_forward",
     "moe_forward_host", "moe_device_status", "MoELayer", "QUANT_TOKEN", "QUANT_BLOCK",
     "QUANT_NVFP4", "MoELayerDesc", "moe_pipeline_workspace_size", "moe_forward_host_pipelined",
@@ -115,6 +115,8 @@ _SIGNATURES = {
     "moe_permute_quant_nvfp4": (_I, [_P, _P, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_act_quant_nvfp4": (_I, [_P, _I, _I, _F, _P, _P, _P]),
     "moe_grouped_gemm_nvfp4": (_I, [_P, _P, _F, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P]),
+    "moe_test_gemm_nvfp4_timeout": (_I, [_P, _P, _F, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _I,
+                                         _P]),
     "moe_nvfp4_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
     "moe_nvfp4_arrange_scales": (_I, [_P, _I, _I, _I, _I, _P, _P]),
     "moe_forward_nvfp4": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _F, _F, _I, _I, _I, _I, _I,
@@ -701,6 +703,21 @@ def moe_test_gemm_timeout(A, scale_a, B, scale_b, offsets, epilogue, C, stall_st
     E, N, _ = B.shape
     _check("moe_test_gemm_timeout", load().moe_test_gemm_timeout(
         _ptr(_u8(A)), _ptr(scale_a), _ptr(_u8(B)), _ptr(scale_b), _ptr(offsets), M, N, Kd, E,
+        epilogue, _ptr(C), int(stall_stage), _stream(stream)))
+    return C
+
+
+def moe_test_gemm_nvfp4_timeout(A, sfa, ga, B, sfb, gb, offsets, epilogue, C, stall_stage,
+                                stream=None):
+    """moe_test_gemm_timeout for the NVFP4 GEMM (A [M, Kd/2] and B [E, N, Kd/2]
+    packed, sfb arranged): one pipeline stage of CTA 0 never receives its
+    bytes, the waits run out (~2 s), moe_device_status() then returns
+    DEV_PIPE_TIMEOUT and the context stays usable."""
+    _need_cuda(A, sfa, B, sfb, gb, offsets, C)
+    M, Kd = A.shape[0], A.shape[1] * 2
+    E, N = B.shape[0], B.shape[1]
+    _check("moe_test_gemm_nvfp4_timeout", load().moe_test_gemm_nvfp4_timeout(
+        _ptr(A), _ptr(sfa), float(ga), _ptr(B), _ptr(sfb), _ptr(gb), _ptr(offsets), M, N, Kd, E,
         epilogue, _ptr(C), int(stall_stage), _stream(stream)))
     return C
 

@@ -699,6 +699,21 @@ moe_status moe_grouped_gemm_nvfp4(const void* A, const uint8_t* sfa, float ga, c
                                                static_cast<cudaStream_t>(stream)));
 }
 
+moe_status moe_test_gemm_nvfp4_timeout(const void* A, const uint8_t* sfa, float ga,
+                                       const void* B, const uint8_t* sfb, const float* gb,
+                                       const int32_t* offsets, int M, int N, int Kd, int E,
+                                       int epilogue, void* C, int stall_stage, void* stream) {
+  moe_status s = check_gemm_nvfp4(A, sfa, ga, B, sfb, gb, offsets, M, N, Kd, E, epilogue, C);
+  if (s != MOE_OK) return s;
+  if (stall_stage < 0) return MOE_ERR_INVALID_ARG;
+  int* err = device_error_word();
+  if (err == nullptr) return MOE_ERR_CUDA;
+  return cuda_status(launch_grouped_gemm_nvfp4(A, sfa, ga, B, sfb, gb, offsets, M, N, Kd, E,
+                                               epilogue, C, err,
+                                               static_cast<cudaStream_t>(stream), false, false,
+                                               stall_stage));
+}
+
 moe_status moe_forward_nvfp4_host(const void* x_host, const float* logits_host,
                                   const float* bias, const void* w13, const uint8_t* s13,
                                   const float* g13, const void* w2, const uint8_t* s2,

@@ -115,6 +115,7 @@ struct FParams {
   int M, N, Kd, E, I, NB, KB;
   int stream_weights;
   int early_table;
+  int stall_stage;  // failure test: CTA 0 never loads its stage with this index (-1: none)
 };
 
 template <bool SILU, int FBN, int FSTAGES, int FKC>
@@ -177,6 +178,7 @@ __global__ void __launch_bounds__(FT, 1)
       const uint64_t pol_w1 = ptx::policy_evict_first();
       const uint64_t pol_x = ptx::policy_evict_last();
       uint32_t s = 0, ph = 0;
+      int gstage = 0;  // stages issued by this CTA
       bool ok = true;
       for (int g = blockIdx.x; ok && g < total; g += gridDim.x) {
         const TileInfo<FBN> t = decode_tile<FBN>(sm, E, p.NB, g);
@@ -193,6 +195,15 @@ __global__ void __launch_bounds__(FT, 1)
           ptx::mbar_arrive_expect_tx(&sm.full[s], bytes);
           armed |= 1u << s;
           armed_par = (armed_par & ~(1u << s)) | (ph << s);
+          // failure test: the stage is armed but its bytes never come, so the
+          // bounded waits run out
+          if (blockIdx.x == 0 && gstage++ == p.stall_stage) {
+            if (++s == FSTAGES) {
+              s = 0;
+              ph ^= 1u;
+            }
+            continue;
+          }
           const int c0 = ks * FKC;  // the stage's first K chunk
           if (SILU)
             ptx::tma_load_5d(sm.w[s], &maps.w, &sm.full[s], 0, t.nb * 64, 0, c0, t.e, pw);
@@ -532,13 +543,13 @@ cudaError_t launch_grouped_gemm_nvfp4(const void* A, const uint8_t* sfa, float g
                                       const uint8_t* sfb, const float* gb,
                                       const int32_t* offsets, int M, int N, int Kd, int E,
                                       int epilogue, void* C, int* err, cudaStream_t st, bool pdl,
-                                      bool early_table) {
+                                      bool early_table, int stall_stage) {
   if (M == 0) return cudaSuccess;
   // many rows per expert: 256 weight rows per CTA (gemm_nvfp4_wide.cu), which
   // stages each token row half as often
   if (gemm_nvfp4_wide_applies(M, N, Kd, E, epilogue))
     return launch_grouped_gemm_nvfp4_wide(A, sfa, ga, B, sfb, gb, offsets, M, N, Kd, E, epilogue,
-                                          C, err, st, pdl, early_table);
+                                          C, err, st, pdl, early_table, stall_stage);
   const bool silu = (epilogue == MOE_EPI_SILU_MUL);
   const uint64_t kb = (uint64_t)Kd / 2;   // bytes of a row
   const uint64_t sc = (uint64_t)Kd / 16;  // scale bytes of a row
@@ -569,6 +580,7 @@ cudaError_t launch_grouped_gemm_nvfp4(const void* A, const uint8_t* sfa, float g
   p.KB = Kd / 256;
   p.stream_weights = many ? 0 : 1;
   p.early_table = early_table ? 1 : 0;
+  p.stall_stage = stall_stage;
   if (!many && fkc == 2)
     return silu ? launch_f<true, 64, 3, 2>(maps, p, M, E, st, pdl)
                 : launch_f<false, 64, 3, 2>(maps, p, M, E, st, pdl);

@@ -105,6 +105,7 @@ struct QParams {
   int* err;
   int M, N, Kd, E, I, NB, NBG, KB;
   int early_table;
+  int stall_stage;  // failure test: CTA 0 never loads its stage with this index (-1: none)
 };
 
 template <bool SILU>
@@ -158,6 +159,7 @@ __global__ void __launch_bounds__(QT, 1)
       const uint64_t pol_w1 = ptx::policy_evict_first();
       const uint64_t pol_x = ptx::policy_evict_last();
       uint32_t s = 0, ph = 0;
+      int gstage = 0;  // stages issued by this CTA
       bool ok = true;
       for (int g = blockIdx.x; ok && g < total; g += gridDim.x) {
         const TileInfo<QBN> t = decode_tile<QBN>(sm, E, p.NBG, g);
@@ -175,6 +177,15 @@ __global__ void __launch_bounds__(QT, 1)
           ptx::mbar_arrive_expect_tx(&sm.full[s], bytes);
           armed |= 1u << s;
           armed_par = (armed_par & ~(1u << s)) | (ph << s);
+          // failure test: the stage is armed but its bytes never come, so the
+          // bounded waits run out
+          if (blockIdx.x == 0 && gstage++ == p.stall_stage) {
+            if (++s == QSTAGES) {
+              s = 0;
+              ph ^= 1u;
+            }
+            continue;
+          }
           if (SILU)  // 128 gate rows from j = 128 nb, then the matching 128 up rows
             ptx::tma_load_5d(sm.w[s], &maps.w, &sm.full[s], 0, t.nb * 128, 0, ks, t.e, pw);
           else
@@ -460,7 +471,7 @@ cudaError_t launch_grouped_gemm_nvfp4_wide(const void* A, const uint8_t* sfa, fl
                                            const void* B, const uint8_t* sfb, const float* gb,
                                            const int32_t* offsets, int M, int N, int Kd, int E,
                                            int epilogue, void* C, int* err, cudaStream_t st,
-                                           bool pdl, bool early_table) {
+                                           bool pdl, bool early_table, int stall_stage) {
   if (M == 0) return cudaSuccess;
   const bool silu = (epilogue == MOE_EPI_SILU_MUL);
   const uint64_t kb = (uint64_t)Kd / 2;   // bytes of a row
@@ -491,6 +502,7 @@ cudaError_t launch_grouped_gemm_nvfp4_wide(const void* A, const uint8_t* sfa, fl
   p.NBG = p.NB / 2;                 // 256-row tiles of this kernel
   p.KB = Kd / 256;
   p.early_table = early_table ? 1 : 0;
+  p.stall_stage = stall_stage;
   return silu ? launch_q<true>(maps, p, M, E, st, pdl) : launch_q<false>(maps, p, M, E, st, pdl);
 }
 

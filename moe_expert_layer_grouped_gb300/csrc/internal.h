@@ -109,7 +109,8 @@ cudaError_t launch_grouped_gemm_nvfp4(const void* A, const uint8_t* sfa, float g
                                       const uint8_t* sfb, const float* gb,
                                       const int32_t* offsets, int M, int N, int Kd, int E,
                                       int epilogue, void* C, int* err, cudaStream_t st,
-                                      bool pdl = false, bool early_table = false);
+                                      bool pdl = false, bool early_table = false,
+                                      int stall_stage = -1);
 
 // gemm_nvfp4_wide.cu: the same GEMM with 256 weight rows per CTA, for many
 // rows per expert (gemm_many_rows) when the weight rows split into 256-row
@@ -120,7 +121,7 @@ cudaError_t launch_grouped_gemm_nvfp4_wide(const void* A, const uint8_t* sfa, fl
                                            const void* B, const uint8_t* sfb, const float* gb,
                                            const int32_t* offsets, int M, int N, int Kd, int E,
                                            int epilogue, void* C, int* err, cudaStream_t st,
-                                           bool pdl, bool early_table);
+                                           bool pdl, bool early_table, int stall_stage);
 
 // unpermute.cu
 cudaError_t launch_unpermute_sum(const void* down, const int32_t* src2dst, const float* w,
