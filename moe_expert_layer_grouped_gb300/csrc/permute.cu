@@ -233,36 +233,63 @@ __device__ __forceinline__ void quant_scatter(const __nv_bfloat16* __restrict__ 
 // nibble), one E4M3 scale per 16 channels sf [T*K, H/16], with the global
 // scale g: scale code = e4m3((amax16 / 6) / g), codes = e2m1(x / (e4m3(code)
 // * g)). A 16-channel block is two 8-value vectors, held by two adjacent
-// threads (vector tid + i*NT, NT even), so its amax takes one shuffle.
+// threads (vector tid + i*NT, NT even), so its amax takes one shuffle. The
+// token's vectors are all loaded before the first is used. When H % 256 == 0
+// (whole warps of vectors: validity is warp-uniform) every eighth thread
+// stores the scale bytes of four blocks as one word.
 template <int VPT, int NT = kQuantThreads>
 __device__ __forceinline__ void quant_scatter_nvfp4(const __nv_bfloat16* __restrict__ x, int t,
                                                     int H, int K, const int* dst, float g,
                                                     uint8_t* __restrict__ a_q,
                                                     uint8_t* __restrict__ sf) {
-  static_assert(NT % 2 == 0, "vector pairs");
+  static_assert(NT % 32 == 0, "whole warps");
   const int tid = threadIdx.x;
   const int nvec = H >> 3;
+  const bool words = (H & 255) == 0;
   const uint4* xr = reinterpret_cast<const uint4*>(x + (int64_t)t * H);
   const Recip rg = recip_bracket(g);
-  __syncthreads();  // dst[] is complete
+  constexpr int G = VPT < 8 ? VPT : 8;  // vectors loaded ahead (16 spilled in the small kernel)
 #pragma unroll
-  for (int i = 0; i < VPT; ++i) {
-    const int idx = tid + i * NT;
-    float f[8];
-    float m = 0.0f;
-    if (idx < nvec) {
-      bf16x8_to_f32(__ldg(xr + idx), f);
-      m = absmax8(f, 0.0f);
+  for (int i0 = 0; i0 < VPT; i0 += G) {
+    uint4 v[G];
+#pragma unroll
+    for (int j = 0; j < G; ++j) {
+      const int idx = tid + (i0 + j) * NT;
+      if (idx < nvec) v[j] = __ldg(xr + idx);
     }
-    m = fmaxf(m, __shfl_xor_sync(kFull, m, 1));
-    if (idx < nvec) {
-      const uint32_t code = nvfp4_scale_code(m, g, rg);
-      const uint32_t q = nvfp4_codes8(f, __fmul_rn(e4m3_value(code), g));
-      for (int k = 0; k < K; ++k) {
-        const int d = dst[k];
-        if (d < 0) continue;
-        *reinterpret_cast<uint32_t*>(a_q + (int64_t)d * (H >> 1) + (int64_t)idx * 4) = q;
-        if ((idx & 1) == 0) sf[(int64_t)d * (H >> 4) + (idx >> 1)] = (uint8_t)code;
+    if (i0 == 0) __syncthreads();  // dst[] is complete
+#pragma unroll
+    for (int j = 0; j < G; ++j) {
+      const int i = i0 + j;
+      const int idx = tid + i * NT;
+      float f[8];
+      float m = 0.0f;
+      if (idx < nvec) {
+        bf16x8_to_f32(v[j], f);
+        m = absmax8(f, 0.0f);
+      }
+      m = fmaxf(m, __shfl_xor_sync(kFull, m, 1));
+      uint32_t code = 0, q = 0;
+      if (idx < nvec) {
+        code = nvfp4_scale_code(m, g, rg);
+        q = nvfp4_codes8(f, __fmul_rn(e4m3_value(code), g));
+      }
+      const uint32_t c2 = __shfl_down_sync(kFull, code, 2);
+      const uint32_t c4 = __shfl_down_sync(kFull, code, 4);
+      const uint32_t c6 = __shfl_down_sync(kFull, code, 6);
+      if (idx < nvec) {
+        const uint32_t word = code | (c2 << 8) | (c4 << 16) | (c6 << 24);
+        for (int k = 0; k < K; ++k) {
+          const int d = dst[k];
+          if (d < 0) continue;
+          *reinterpret_cast<uint32_t*>(a_q + (int64_t)d * (H >> 1) + (int64_t)idx * 4) = q;
+          uint8_t* srow = sf + (int64_t)d * (H >> 4);
+          if (words) {
+            if ((idx & 7) == 0) *reinterpret_cast<uint32_t*>(srow + (idx >> 1)) = word;
+          } else if ((idx & 1) == 0) {
+            srow[idx >> 1] = (uint8_t)code;
+          }
+        }
       }
     }
   }

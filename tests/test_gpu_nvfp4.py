@@ -105,7 +105,11 @@ def test_act_quant_nvfp4_every_launch_shape(M, I):
     assert np.array_equal(_unpack(q), oq)
 
 
-@pytest.mark.parametrize("T,H,E,K", [(8, 256, 8, 2), (300, 512, 24, 6), (4099, 256, 64, 6)])
+@pytest.mark.parametrize("T,H,E,K", [(8, 256, 8, 2), (300, 512, 24, 6), (4099, 256, 64, 6),
+                                     # scale bytes one by one (H % 256 != 0), both routings
+                                     (37, 224, 16, 4), (600, 224, 16, 4),
+                                     # DeepSeek-V3's H on both routings
+                                     (40, 7168, 32, 8), (1030, 7168, 64, 8)])
 def test_permute_quant_nvfp4_matches_oracle(T, H, E, K):
     rng = np.random.default_rng(T + H)
     ids = np.stack([rng.choice(E, K, replace=False) for _ in range(T)]).astype(np.int32)
