@@ -71,9 +71,11 @@ constexpr uint32_t F_TMEM = 512;
 // Tile width FBN (tokens, MMA N), pipeline depth FSTAGES and K chunks per
 // stage FKC per launch: few tokens per expert (decode) 64 tokens x 3 stages
 // of 2 chunks, the weight stream's bytes in flight being what bounds it;
-// otherwise 128 x 2 stages of 2 chunks; one chunk per stage (6 / 5 stages)
-// when the chunk count is odd. Tensor memory: two FBN-column accumulators,
-// then FSTAGES x FKC x 32 scale columns.
+// otherwise 128 x 2 stages of 2 chunks (many tokens per expert go to the
+// 256-row kernel of gemm_nvfp4_wide.cu whenever the weight rows split into
+// 256-row tiles); one chunk per stage (6 / 5 stages) when the chunk count is
+// odd. Tensor memory: two FBN-column accumulators, then FSTAGES x FKC x 32
+// scale columns.
 
 struct FMaps {
   CUtensorMap w;          // weights, one 128-byte chunk of 128 rows per box
