@@ -32,11 +32,18 @@
 //               two tiles' arranged scale blocks (two bulk copies), the token
 //               rows (64/32/16-row boxes) and their scale bytes.
 //   warp 1      MMA: lane 0 issues 2 x 4 MMAs per K chunk (K = 64 each).
-//   warps 2..9  epilogue, lane quadrant warp % 4, two warps per quadrant on
-//               alternate 32-token chunks.
+//   warps 2..9  epilogue, lane quadrant warp % 4.
 //   warps 10..13 scales: one warp per lane quadrant writes the stage's three
 //               16-column scale groups (two weight halves, tokens) into its
-//               quadrant and arrives on the stage's scale barrier.
+//               quadrant and arrives on the stage's scale barrier. After a
+//               tile's last stage it joins the tile's drain.
+// A tile drains through three warps per lane quadrant (two epilogue warps and
+// the scale warp), each taking every third 32-token item: the MMA thread
+// cannot start the next tile before the drain ends, so the scale warps are
+// not needed elsewhere meanwhile. The epilogue costs DeepSeek-V3's w2 about a
+// quarter of its time (0.862 ms, 0.625 with the accumulators released
+// unread, 0.752 without the output stores); the third warp per quadrant took
+// it to 0.852 ms.
 // Tensor memory: the two 128-column accumulators (one tile: its drain is not
 // overlapped with the next tile's MMAs), then 48 scale columns per stage.
 // Every wait is bounded (2 s); on timeout the CTA sets the device error word,
@@ -59,6 +66,7 @@ using namespace gemm_common;
 constexpr int QEW = 8;                     // epilogue warps: two per lane quadrant
 constexpr int QSW0 = 2 + QEW;              // first scale warp
 constexpr int QT = 32 * (QSW0 + 4);        // 448 threads
+constexpr int QDRAIN = QEW / 4 + 1;        // warps per lane quadrant that drain a tile
 constexpr int QBN = 128;                   // tokens per tile (MMA N)
 constexpr int QROWS = 256;                 // weight rows per tile (two accumulators)
 constexpr int QSTAGES = 3;                 // 54 KB per stage
@@ -80,7 +88,7 @@ struct QSmem {
   uint8_t x[QSTAGES][QBN * BK];
   uint8_t sx[QSTAGES][QBN * QSFROW];   // token scales, row-major as loaded
   uint4 sa[QSTAGES][2][4][32];         // the two tiles' arranged weight-scale blocks
-  uint16_t stage_out[QEW][32 * 32];    // per epilogue warp: bf16 [token][32 columns]
+  uint16_t stage_out[QEW + 4][32 * 32];  // per draining warp: bf16 [token][32 columns]
   uint64_t full[QSTAGES];
   uint64_t sready[QSTAGES];  // the stage's scales are in tensor memory
   uint64_t empty[QSTAGES];
@@ -108,6 +116,66 @@ struct QParams {
   int stall_stage;  // failure test: CTA 0 never loads its stage with this index (-1: none)
 };
 
+// One warp's share of a tile's drain, in its lane quadrant q (TMEM lanes
+// tq ..): the 32-token x 32-row items slot, slot + QDRAIN, ... of the tile.
+// SiLU: item c = token chunk c of both accumulators (gate j and up j in the
+// same lane), written as h columns; bf16: item it = accumulator it / nchunk,
+// token chunk it % nchunk. Each item goes through the warp's shared-memory
+// tile ost so that four lanes write a token's 64 bytes in 16-byte stores.
+template <bool SILU>
+__device__ __forceinline__ void drain_items(const QParams& p, const TileInfo<QBN>& t,
+                                            uint32_t tq, int q, int slot, uint16_t* ost,
+                                            int lane) {
+  const int nchunk = (t.ntok + 31) >> 5;
+  const int items = SILU ? nchunk : 2 * nchunk;
+  const float scale = p.ga * __ldg(p.gb + t.e);  // both global scales
+#pragma unroll 1
+  for (int it = slot; it < items; it += QDRAIN) {
+    const int acc = SILU ? 0 : it / nchunk;
+    const int c = it - acc * nchunk;
+    const int tk0 = c * 32;
+    __nv_bfloat16* dst;
+    int ld;
+    if (SILU) {
+      uint32_t gv[32], uv[32];
+      ptx::tmem_ld_32x32b_x32(tq + c * 32, gv);
+      ptx::tmem_ld_32x32b_x32(tq + QACC + c * 32, uv);
+      ptx::tmem_ld_wait();
+      ptx::reg_fence(gv);
+      ptx::reg_fence(uv);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const float gg = __uint_as_float(gv[i]) * scale;
+        const float uu = __uint_as_float(uv[i]) * scale;
+        // silu(g) * u, rounded to bf16: a fast divide is well inside it
+        ost[i * 32 + lane] =
+            __bfloat16_as_ushort(__float2bfloat16_rn(__fdividef(gg, 1.0f + __expf(-gg)) * uu));
+      }
+      ld = p.I;
+      dst = reinterpret_cast<__nv_bfloat16*>(p.C) + t.nb * 128 + q * 32;  // this warp's 32 j
+    } else {
+      uint32_t v[32];
+      ptx::tmem_ld_sync_x32(tq + (uint32_t)acc * QACC + c * 32, v);
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        ost[i * 32 + lane] =
+            __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[i]) * scale));
+      ld = p.N;
+      dst = reinterpret_cast<__nv_bfloat16*>(p.C) + t.nb * QROWS + acc * 128 + q * 32;
+    }
+    __syncwarp();
+    // 32 tokens x 32 columns: four lanes per token row, 16 bytes each
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int r = k * 8 + (lane >> 2);
+      if (tk0 + r < t.ntok)
+        *reinterpret_cast<uint4*>(dst + (int64_t)(t.tok0 + tk0 + r) * ld + (lane & 3) * 8) =
+            *reinterpret_cast<const uint4*>(ost + r * 32 + (lane & 3) * 8);
+    }
+    __syncwarp();
+  }
+}
+
 template <bool SILU>
 __global__ void __launch_bounds__(QT, 1)
     grouped_gemm_nvfp4_wide_kernel(const __grid_constant__ QMaps maps, const QParams p) {
@@ -132,7 +200,7 @@ __global__ void __launch_bounds__(QT, 1)
       ptx::mbar_init(&sm.empty[s], 1);
     }
     ptx::mbar_init(&sm.tfull, 1);
-    ptx::mbar_init(&sm.tempty, 32 * QEW);
+    ptx::mbar_init(&sm.tempty, 32 * (QEW + 4));  // every draining thread
     ptx::mbar_init(&sm.drain, 1);
     sm.abort = 0;
     sm.never = 0;
@@ -269,6 +337,7 @@ __global__ void __launch_bounds__(QT, 1)
     }
   } else if (warp >= QSW0) {
     // ======================= scales (warps 10..13) ==========================
+    // (and, after each tile's stages, a third of its drain)
     // Register 4j + c of lane i: the four scales of MMA step j of the
     // operand's row i + 32c. Weights, from the arranged blocks (lane i's
     // 16 bytes of block j: words c = 0..3 for tile rows i + 32c): bf16 tiles
@@ -277,7 +346,8 @@ __global__ void __launch_bounds__(QT, 1)
     const uint32_t tq = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     uint32_t s = 0, ph = 0;
     bool ok = true;
-    for (int g = blockIdx.x; ok && g < total; g += gridDim.x) {
+    int iter = 0;
+    for (int g = blockIdx.x; ok && g < total; g += gridDim.x, ++iter) {
       for (int ks = 0; ks < KS; ++ks) {
         if (!__all_sync(kFull, ptx::mbar_wait(&sm.full[s], ph, &sm.abort, WAIT_NS))) {
           ok = false;
@@ -334,6 +404,19 @@ __global__ void __launch_bounds__(QT, 1)
           ph ^= 1u;
         }
       }
+      if (!ok) break;
+      // then a third of the tile's drain: the MMA cannot start the next tile
+      // before it ends, so the next stages' scales lose nothing by waiting
+      const bool got = ptx::mbar_wait(&sm.tfull, (uint32_t)(iter & 1), &sm.abort, WAIT_NS);
+      if (!__all_sync(kFull, got)) {
+        ok = false;
+        break;
+      }
+      ptx::tc_fence_after();
+      drain_items<SILU>(p, decode_tile<QBN>(sm, E, p.NBG, g), tq, warp & 3, QDRAIN - 1,
+                        sm.stage_out[warp - 2], lane);
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(&sm.tempty);
     }
     if (!ok && lane == 0) {
       sm.abort = 1;
@@ -353,71 +436,8 @@ __global__ void __launch_bounds__(QT, 1)
         break;
       }
       ptx::tc_fence_after();
-      const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16);
-      const int nchunk = (t.ntok + 31) >> 5;
-      const float scale = p.ga * __ldg(p.gb + t.e);  // both global scales
-      uint16_t* ost = sm.stage_out[warp - 2];
-      if (SILU) {
-        const int I = p.I;
-        const int jrow = t.nb * 128 + q * 32;  // first j of this warp's 32
-        __nv_bfloat16* hbase = reinterpret_cast<__nv_bfloat16*>(p.C);
-#pragma unroll 1
-        for (int c = par; c < nchunk; c += QEW / 4) {
-          uint32_t gv[32], uv[32];
-          ptx::tmem_ld_32x32b_x32(tq + c * 32, gv);
-          ptx::tmem_ld_32x32b_x32(tq + QACC + c * 32, uv);
-          ptx::tmem_ld_wait();
-          ptx::reg_fence(gv);
-          ptx::reg_fence(uv);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float gg = __uint_as_float(gv[i]) * scale;
-            const float uu = __uint_as_float(uv[i]) * scale;
-            // silu(g) * u, rounded to bf16: a fast divide is well inside it
-            ost[i * 32 + lane] =
-                __bfloat16_as_ushort(__float2bfloat16_rn(__fdividef(gg, 1.0f + __expf(-gg)) * uu));
-          }
-          __syncwarp();
-          // 32 tokens x 32 j: four lanes per token row, 16 bytes each
-          const int tk0 = c * 32;
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const int r = k * 8 + (lane >> 2);
-            if (tk0 + r < t.ntok)
-              *reinterpret_cast<uint4*>(hbase + (int64_t)(t.tok0 + tk0 + r) * I + jrow +
-                                        (lane & 3) * 8) =
-                  *reinterpret_cast<const uint4*>(ost + r * 32 + (lane & 3) * 8);
-          }
-          __syncwarp();
-        }
-      } else {
-        const int N = p.N;
-        __nv_bfloat16* cbase = reinterpret_cast<__nv_bfloat16*>(p.C);
-#pragma unroll 1
-        for (int acc = 0; acc < 2; ++acc) {
-          const int ncol0 = t.nb * QROWS + acc * 128 + q * 32;  // this warp's first column
-#pragma unroll 1
-          for (int c = par; c < nchunk; c += QEW / 4) {
-            uint32_t v[32];
-            ptx::tmem_ld_sync_x32(tq + (uint32_t)acc * QACC + c * 32, v);
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              ost[i * 32 + lane] =
-                  __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[i]) * scale));
-            __syncwarp();
-            const int tk0 = c * 32;
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const int r = k * 8 + (lane >> 2);
-              if (tk0 + r < t.ntok)
-                *reinterpret_cast<uint4*>(cbase + (int64_t)(t.tok0 + tk0 + r) * N + ncol0 +
-                                          (lane & 3) * 8) =
-                    *reinterpret_cast<const uint4*>(ost + r * 32 + (lane & 3) * 8);
-            }
-            __syncwarp();
-          }
-        }
-      }
+      drain_items<SILU>(p, t, tmem + ((uint32_t)(q * 32) << 16), q, par, sm.stage_out[warp - 2],
+                        lane);
       ptx::tc_fence_before();
       ptx::mbar_arrive(&sm.tempty);
     }
