@@ -23,12 +23,12 @@ def built():
     yield
 
 
-def _problem(epi):
-    rng = np.random.default_rng(77 + epi)
-    # few rows per expert: one CTA per tile; K = 1024 gives every tile several
-    # pipeline stages whatever their depth in K
-    counts, N, Kd = [20, 3, 0, 17, 9, 30, 1, 12], 256, 1024
-    off = ragged_offsets(counts)
+def _problem(epi, counts=(20, 3, 0, 17, 9, 30, 1, 12)):
+    rng = np.random.default_rng(77 + epi + len(counts))
+    # K = 1024 gives every tile several pipeline stages whatever their depth
+    # in K
+    N, Kd = 256, 1024
+    off = ragged_offsets(list(counts))
     M = int(off[-1])
     A = random_e4m3(rng, (M, Kd))
     B = random_e4m3(rng, (len(counts), N, Kd))
@@ -38,8 +38,13 @@ def _problem(epi):
 
 
 @pytest.mark.parametrize("epi", [moe.EPI_BF16, moe.EPI_SILU_MUL])
-def test_gemm_wait_timeout_is_reported_and_context_survives(epi):
-    A, sa, B, sb, off = _problem(epi)
+@pytest.mark.parametrize("counts", [(20, 3, 0, 17, 9, 30, 1, 12),   # few rows: single CTAs
+                                    (300, 0, 129, 211)])            # many: CTA pairs
+def test_gemm_wait_timeout_is_reported_and_context_survives(epi, counts):
+    """The decode-shaped problem runs single CTAs; the other (more than 32
+    rows per expert) CTA pairs, where the stalled CTA's peer gives up on its
+    own bounded waits and both meet at the teardown's cluster barrier."""
+    A, sa, B, sb, off = _problem(epi, counts)
     t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
     N = B.shape[1]
     cols = N // 2 if epi == moe.EPI_SILU_MUL else N
