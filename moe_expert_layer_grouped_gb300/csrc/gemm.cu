@@ -794,10 +794,9 @@ cudaError_t launch_grouped_gemm(const void* A, const float* scale_a, const void*
   if (M == 0) return cudaSuccess;
   // long K with many rows per expert: pairs with two accumulators per CTA
   // (gemm_wide.cu), which stage each token row half as often
-  if (row_token == nullptr && row_amax == nullptr && stall_stage < 0 &&
-      gemm_wide_applies(M, N, Kd, E, epilogue))
+  if (row_token == nullptr && row_amax == nullptr && gemm_wide_applies(M, N, Kd, E, epilogue))
     return launch_grouped_gemm_wide(A, scale_a, B, scale_b, offsets, M, N, Kd, E, epilogue, C,
-                                    err, st, pdl, early_table);
+                                    err, st, pdl, early_table, stall_stage);
   const bool silu = (epilogue == MOE_EPI_SILU_MUL);
   const bool small = !gemm_many_rows(M, E);  // few rows per expert (decode)
   // K chunks per stage of the configuration launched below (the weight box

@@ -78,6 +78,7 @@ struct WParams {
   int M, N, Kd, E, I, NBG, KB;
   int stream_weights;
   int early_table;
+  int stall_stage;  // failure test: CTA 0 never loads its stage with this index (-1: none)
 };
 
 template <bool SILU>
@@ -132,6 +133,7 @@ __global__ void __launch_bounds__(WT, 1)
     const uint64_t pol_w1 = ptx::policy_evict_first();
     const uint64_t pol_x = ptx::policy_evict_last();
     uint32_t s = 0, ph = 0;
+    int gstage = 0;  // stages issued by this CTA
     bool ok = true;
     for (int g = cluster; ok && g < total; g += nclusters) {
       const TileInfo<WBN> t = decode_tile<WBN>(sm, E, p.NBG, g);
@@ -150,12 +152,17 @@ __global__ void __launch_bounds__(WT, 1)
           break;
         }
         const uint32_t fb = ptx::map_to_rank(ptx::smem_u32(&sm.full[s]), 0);
+        // failure test: the stage is armed but this CTA's bytes never come,
+        // so the bounded waits run out
+        const bool stall = blockIdx.x == 0 && gstage++ == p.stall_stage;
         if (lane == 0) {
           if (rank == 0) {
             ptx::mbar_arrive_expect_tx(&sm.full[s], bytes);
             armed |= 1u << s;
             armed_par = (armed_par & ~(1u << s)) | (ph << s);
           }
+        }
+        if (lane == 0 && !stall) {
           // the stage's WKC K blocks (past Kd: zero-filled, adding nothing)
           if (SILU)  // per K block 128 gate rows, then the matching 128 up rows
             ptx::tma_load_5d_pair(sm.w[s][0], &maps.w, fb, 0, jq, 0, ks * WKC, t.e, pw);
@@ -410,7 +417,8 @@ bool gemm_wide_applies(int M, int N, int Kd, int E, int epilogue) {
 cudaError_t launch_grouped_gemm_wide(const void* A, const float* scale_a, const void* B,
                                      const float* scale_b, const int32_t* offsets, int M, int N,
                                      int Kd, int E, int epilogue, void* C, int* err,
-                                     cudaStream_t st, bool pdl, bool early_table) {
+                                     cudaStream_t st, bool pdl, bool early_table,
+                                     int stall_stage) {
   if (M == 0) return cudaSuccess;
   const bool silu = (epilogue == MOE_EPI_SILU_MUL);
   Maps maps;
@@ -438,6 +446,7 @@ cudaError_t launch_grouped_gemm_wide(const void* A, const float* scale_a, const 
   p.KB = Kd / BK;
   p.stream_weights = 0;
   p.early_table = early_table ? 1 : 0;
+  p.stall_stage = stall_stage;
   return silu ? launch_wide_cfg<true>(maps, p, M, E, st, pdl)
               : launch_wide_cfg<false>(maps, p, M, E, st, pdl);
 }

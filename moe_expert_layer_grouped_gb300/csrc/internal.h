@@ -76,7 +76,8 @@ bool gemm_wide_applies(int M, int N, int Kd, int E, int epilogue);
 cudaError_t launch_grouped_gemm_wide(const void* A, const float* scale_a, const void* B,
                                      const float* scale_b, const int32_t* offsets, int M, int N,
                                      int Kd, int E, int epilogue, void* C, int* err,
-                                     cudaStream_t st, bool pdl = false, bool early_table = false);
+                                     cudaStream_t st, bool pdl = false, bool early_table = false,
+                                     int stall_stage = -1);
 
 // gemm_block.cu: block scales, scale_a [M, Kd/128], scale_b [E, N/128, Kd/128]
 // (N % 128 == 0, Kd % 128 == 0); no row amax.

@@ -23,11 +23,10 @@ def built():
     yield
 
 
-def _problem(epi, counts=(20, 3, 0, 17, 9, 30, 1, 12)):
-    rng = np.random.default_rng(77 + epi + len(counts))
+def _problem(epi, counts=(20, 3, 0, 17, 9, 30, 1, 12), N=256, Kd=1024):
+    rng = np.random.default_rng(77 + epi + len(counts) + Kd)
     # K = 1024 gives every tile several pipeline stages whatever their depth
     # in K
-    N, Kd = 256, 1024
     off = ragged_offsets(list(counts))
     M = int(off[-1])
     A = random_e4m3(rng, (M, Kd))
@@ -38,13 +37,16 @@ def _problem(epi, counts=(20, 3, 0, 17, 9, 30, 1, 12)):
 
 
 @pytest.mark.parametrize("epi", [moe.EPI_BF16, moe.EPI_SILU_MUL])
-@pytest.mark.parametrize("counts", [(20, 3, 0, 17, 9, 30, 1, 12),   # few rows: single CTAs
-                                    (300, 0, 129, 211)])            # many: CTA pairs
-def test_gemm_wait_timeout_is_reported_and_context_survives(epi, counts):
-    """The decode-shaped problem runs single CTAs; the other (more than 32
-    rows per expert) CTA pairs, where the stalled CTA's peer gives up on its
-    own bounded waits and both meet at the teardown's cluster barrier."""
-    A, sa, B, sb, off = _problem(epi, counts)
+@pytest.mark.parametrize("counts,N,Kd", [
+    ((20, 3, 0, 17, 9, 30, 1, 12), 256, 1024),  # few rows: single CTAs
+    ((300, 0, 129, 211), 256, 1024),            # many: CTA pairs
+    ((300, 0, 129, 211), 512, 4096)])           # many, 32 K blocks: the two-accumulator pairs
+def test_gemm_wait_timeout_is_reported_and_context_survives(epi, counts, N, Kd):
+    """The decode-shaped problem runs single CTAs; the others (more than 32
+    rows per expert) CTA pairs with one or two accumulators per CTA, where the
+    stalled CTA's peer gives up on its own bounded waits and both meet at the
+    teardown's cluster barrier."""
+    A, sa, B, sb, off = _problem(epi, counts, N, Kd)
     t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
     N = B.shape[1]
     cols = N // 2 if epi == moe.EPI_SILU_MUL else N
