@@ -46,6 +46,10 @@
 // it to 0.852 ms.
 // Tensor memory: the two 128-column accumulators (one tile: its drain is not
 // overlapped with the next tile's MMAs), then 48 scale columns per stage.
+// Shared memory: four stages of 54 KB when the tile table (E + 1 entries
+// twice, sized at launch) leaves room, i.e. up to ~470 experts, else three:
+// DeepSeek-V3 prefill w13 1.283 -> 1.210 ms with the fourth stage, the drain
+// then staged 8 tokens at a time to make room.
 // Every wait is bounded (2 s); on timeout the CTA sets the device error word,
 // lets its copies and MMAs land, frees its tensor memory and leaves.
 #include <cuda.h>
@@ -69,13 +73,13 @@ constexpr int QT = 32 * (QSW0 + 4);        // 448 threads
 constexpr int QDRAIN = QEW / 4 + 1;        // warps per lane quadrant that drain a tile
 constexpr int QBN = 128;                   // tokens per tile (MMA N)
 constexpr int QROWS = 256;                 // weight rows per tile (two accumulators)
-constexpr int QSTAGES = 3;                 // 54 KB per stage
 constexpr int QSFROW = 16;                 // scale bytes per row per 128-byte K chunk
+constexpr int QSUB = 8;                    // tokens per drain round (shared-memory tile)
 constexpr uint32_t QACC = 128;             // tensor-memory columns per accumulator
 constexpr uint32_t QSF0 = 2 * QACC;        // first scale column
 constexpr uint32_t QSFSTAGE = 48;          // scale columns per stage: 16 + 16 weights, 16 tokens
 constexpr uint32_t QTMEM = 512;
-static_assert(QSF0 + QSTAGES * QSFSTAGE <= QTMEM, "tensor memory budget");
+constexpr size_t QSMEM_MAX = 227 * 1024;
 
 struct QMaps {
   CUtensorMap w;          // 256 weight rows of one 128-byte K chunk per box
@@ -83,15 +87,20 @@ struct QMaps {
   CUtensorMap sx[NXBOX];  // token scales, 16 bytes x (64 >> i) rows
 };
 
+// The stage ring, 54 KB a stage, then the tile table (tile_start and offs,
+// E + 1 entries each) after the struct, sized by the launch: four stages
+// when they fit in the 227 KB with the table, else three.
+template <int STG>
 struct QSmem {
-  uint8_t w[QSTAGES][QROWS * BK];      // accumulator 0's rows, then accumulator 1's
-  uint8_t x[QSTAGES][QBN * BK];
-  uint8_t sx[QSTAGES][QBN * QSFROW];   // token scales, row-major as loaded
-  uint4 sa[QSTAGES][2][4][32];         // the two tiles' arranged weight-scale blocks
-  uint16_t stage_out[QEW + 4][32 * 32];  // per draining warp: bf16 [token][32 columns]
-  uint64_t full[QSTAGES];
-  uint64_t sready[QSTAGES];  // the stage's scales are in tensor memory
-  uint64_t empty[QSTAGES];
+  static_assert(QSF0 + STG * QSFSTAGE <= QTMEM, "tensor memory budget");
+  uint8_t w[STG][QROWS * BK];          // accumulator 0's rows, then accumulator 1's
+  uint8_t x[STG][QBN * BK];
+  uint8_t sx[STG][QBN * QSFROW];       // token scales, row-major as loaded
+  uint4 sa[STG][2][4][32];             // the two tiles' arranged weight-scale blocks
+  uint16_t stage_out[QEW + 4][QSUB * 32];  // per draining warp: bf16 [token][32 columns]
+  uint64_t full[STG];
+  uint64_t sready[STG];  // the stage's scales are in tensor memory
+  uint64_t empty[STG];
   uint64_t tfull;
   uint64_t tempty;
   uint64_t drain;
@@ -100,8 +109,15 @@ struct QSmem {
   int total_tiles;
   int never;
   int thr_sum[32];
-  int tile_start[MAX_E + 1];
-  int offs[MAX_E + 1];
+};
+
+// The tile table's view for build_tile_table / decode_tile: the arrays live
+// in the dynamic shared memory after the struct.
+struct QTab {
+  int* tile_start;
+  int* offs;
+  int* thr_sum;
+  int& total_tiles;
 };
 
 struct QParams {
@@ -116,12 +132,26 @@ struct QParams {
   int stall_stage;  // failure test: CTA 0 never loads its stage with this index (-1: none)
 };
 
+// QSUB tokens x 32 columns from the warp's shared-memory tile to dst (row
+// stride ld), tokens tk.. of tile t: four lanes per token row, 16 bytes each.
+__device__ __forceinline__ void store_rows(uint16_t* ost, __nv_bfloat16* dst, int ld,
+                                           const TileInfo<QBN>& t, int tk, int lane) {
+  static_assert(QSUB * 4 == 32, "one 16-byte store per lane");
+  __syncwarp();
+  const int r = lane >> 2;
+  if (tk + r < t.ntok)
+    *reinterpret_cast<uint4*>(dst + (int64_t)(t.tok0 + tk + r) * ld + (lane & 3) * 8) =
+        *reinterpret_cast<const uint4*>(ost + r * 32 + (lane & 3) * 8);
+  __syncwarp();
+}
+
 // One warp's share of a tile's drain, in its lane quadrant q (TMEM lanes
 // tq ..): the 32-token x 32-row items slot, slot + QDRAIN, ... of the tile.
 // SiLU: item c = token chunk c of both accumulators (gate j and up j in the
 // same lane), written as h columns; bf16: item it = accumulator it / nchunk,
 // token chunk it % nchunk. Each item goes through the warp's shared-memory
-// tile ost so that four lanes write a token's 64 bytes in 16-byte stores.
+// tile ost, QSUB tokens at a time, so that four lanes write a token's 64
+// bytes in 16-byte stores.
 template <bool SILU>
 __device__ __forceinline__ void drain_items(const QParams& p, const TileInfo<QBN>& t,
                                             uint32_t tq, int q, int slot, uint16_t* ost,
@@ -143,45 +173,48 @@ __device__ __forceinline__ void drain_items(const QParams& p, const TileInfo<QBN
       ptx::tmem_ld_wait();
       ptx::reg_fence(gv);
       ptx::reg_fence(uv);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const float gg = __uint_as_float(gv[i]) * scale;
-        const float uu = __uint_as_float(uv[i]) * scale;
-        // silu(g) * u, rounded to bf16: a fast divide is well inside it
-        ost[i * 32 + lane] =
-            __bfloat16_as_ushort(__float2bfloat16_rn(__fdividef(gg, 1.0f + __expf(-gg)) * uu));
-      }
       ld = p.I;
       dst = reinterpret_cast<__nv_bfloat16*>(p.C) + t.nb * 128 + q * 32;  // this warp's 32 j
+      // QSUB tokens at a time through the shared-memory tile
+#pragma unroll
+      for (int i0 = 0; i0 < 32; i0 += QSUB) {
+#pragma unroll
+        for (int i = i0; i < i0 + QSUB; ++i) {
+          const float gg = __uint_as_float(gv[i]) * scale;
+          const float uu = __uint_as_float(uv[i]) * scale;
+          // silu(g) * u, rounded to bf16: a fast divide is well inside it
+          ost[(i - i0) * 32 + lane] =
+              __bfloat16_as_ushort(__float2bfloat16_rn(__fdividef(gg, 1.0f + __expf(-gg)) * uu));
+        }
+        store_rows(ost, dst, ld, t, tk0 + i0, lane);
+      }
     } else {
       uint32_t v[32];
       ptx::tmem_ld_sync_x32(tq + (uint32_t)acc * QACC + c * 32, v);
-#pragma unroll
-      for (int i = 0; i < 32; ++i)
-        ost[i * 32 + lane] =
-            __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[i]) * scale));
       ld = p.N;
       dst = reinterpret_cast<__nv_bfloat16*>(p.C) + t.nb * QROWS + acc * 128 + q * 32;
-    }
-    __syncwarp();
-    // 32 tokens x 32 columns: four lanes per token row, 16 bytes each
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int r = k * 8 + (lane >> 2);
-      if (tk0 + r < t.ntok)
-        *reinterpret_cast<uint4*>(dst + (int64_t)(t.tok0 + tk0 + r) * ld + (lane & 3) * 8) =
-            *reinterpret_cast<const uint4*>(ost + r * 32 + (lane & 3) * 8);
+      for (int i0 = 0; i0 < 32; i0 += QSUB) {
+#pragma unroll
+        for (int i = i0; i < i0 + QSUB; ++i)
+          ost[(i - i0) * 32 + lane] =
+              __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[i]) * scale));
+        store_rows(ost, dst, ld, t, tk0 + i0, lane);
+      }
     }
-    __syncwarp();
   }
 }
 
-template <bool SILU>
+template <bool SILU, int STG>
 __global__ void __launch_bounds__(QT, 1)
     grouped_gemm_nvfp4_wide_kernel(const __grid_constant__ QMaps maps, const QParams p) {
+  constexpr int QSTAGES = STG;
   extern __shared__ uint8_t smem_raw[];
-  QSmem& sm = *reinterpret_cast<QSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                        ~static_cast<uintptr_t>(1023));
+  using S = QSmem<STG>;
+  S& sm = *reinterpret_cast<S*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                ~static_cast<uintptr_t>(1023));
+  int* const tab_mem = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(&sm) + sizeof(S));
+  QTab tab{tab_mem, tab_mem + p.E + 1, sm.thr_sum, sm.total_tiles};
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
@@ -211,7 +244,7 @@ __global__ void __launch_bounds__(QT, 1)
     ptx::tmem_relinquish();
   }
   if (!p.early_table) chain_entry();
-  build_tile_table<QBN, QT>(sm, p.offsets, E, p.M, p.NBG, p.err, tid);
+  build_tile_table<QBN, QT>(tab, p.offsets, E, p.M, p.NBG, p.err, tid);
   if (p.early_table) chain_entry();
   ptx::tc_fence_before();
   __syncthreads();
@@ -230,7 +263,7 @@ __global__ void __launch_bounds__(QT, 1)
       int gstage = 0;  // stages issued by this CTA
       bool ok = true;
       for (int g = blockIdx.x; ok && g < total; g += gridDim.x) {
-        const TileInfo<QBN> t = decode_tile<QBN>(sm, E, p.NBG, g);
+        const TileInfo<QBN> t = decode_tile<QBN>(tab, E, p.NBG, g);
         const int rows = (t.ntok + 15) & ~15;
         const uint32_t bytes = QROWS * BK + 2 * 2048 + (uint32_t)rows * (BK + QSFROW);
         // the two 128-row tiles' arranged scales, chunk 0
@@ -290,7 +323,7 @@ __global__ void __launch_bounds__(QT, 1)
       bool ok = true, issued = false;
       int iter = 0;
       for (int g = blockIdx.x; ok && g < total; g += gridDim.x, ++iter) {
-        const TileInfo<QBN> t = decode_tile<QBN>(sm, E, p.NBG, g);
+        const TileInfo<QBN> t = decode_tile<QBN>(tab, E, p.NBG, g);
         const int n_mma = (t.ntok + 15) & ~15;
         const uint32_t idesc = ptx::idesc_nvfp4(BM, n_mma);
         if (!ptx::mbar_wait(&sm.tempty, (uint32_t)(iter & 1) ^ 1u, &sm.abort, WAIT_NS)) {
@@ -413,7 +446,7 @@ __global__ void __launch_bounds__(QT, 1)
         break;
       }
       ptx::tc_fence_after();
-      drain_items<SILU>(p, decode_tile<QBN>(sm, E, p.NBG, g), tq, warp & 3, QDRAIN - 1,
+      drain_items<SILU>(p, decode_tile<QBN>(tab, E, p.NBG, g), tq, warp & 3, QDRAIN - 1,
                         sm.stage_out[warp - 2], lane);
       ptx::tc_fence_before();
       ptx::mbar_arrive(&sm.tempty);
@@ -428,7 +461,7 @@ __global__ void __launch_bounds__(QT, 1)
     const int par = (warp - 2) / 4;
     int iter = 0;
     for (int g = blockIdx.x; g < total; g += gridDim.x, ++iter) {
-      const TileInfo<QBN> t = decode_tile<QBN>(sm, E, p.NBG, g);
+      const TileInfo<QBN> t = decode_tile<QBN>(tab, E, p.NBG, g);
       const bool ok = ptx::mbar_wait(&sm.tfull, (uint32_t)(iter & 1), &sm.abort, WAIT_NS);
       if (!__all_sync(kFull, ok)) {
         sm.abort = 1;
@@ -456,12 +489,17 @@ __global__ void __launch_bounds__(QT, 1)
   }
 }
 
-template <bool SILU>
+template <int STG>
+size_t q_smem_bytes(int E) {
+  return sizeof(QSmem<STG>) + 2 * (size_t)(E + 1) * sizeof(int) + 1024;
+}
+
+template <bool SILU, int STG>
 cudaError_t launch_q(const QMaps& maps, const QParams& p, int M, int E, cudaStream_t st,
                      bool pdl) {
-  constexpr size_t smem = sizeof(QSmem) + 1024;
-  static_assert(smem <= 227 * 1024, "shared memory budget");
-  auto kern = grouped_gemm_nvfp4_wide_kernel<SILU>;
+  const size_t smem = q_smem_bytes<STG>(E);
+  if (smem > QSMEM_MAX) return cudaErrorInvalidValue;
+  auto kern = grouped_gemm_nvfp4_wide_kernel<SILU, STG>;
   static std::mutex mu;
   static bool attr_set[64] = {};
   int dev = 0;
@@ -470,7 +508,7 @@ cudaError_t launch_q(const QMaps& maps, const QParams& p, int M, int E, cudaStre
     std::lock_guard<std::mutex> lk(mu);
     if (dev >= 64 || !attr_set[dev]) {
       cudaError_t e =
-          cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+          cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)QSMEM_MAX);
       if (e != cudaSuccess) return e;
       if (dev < 64) attr_set[dev] = true;
     }
@@ -523,7 +561,11 @@ cudaError_t launch_grouped_gemm_nvfp4_wide(const void* A, const uint8_t* sfa, fl
   p.KB = Kd / 256;
   p.early_table = early_table ? 1 : 0;
   p.stall_stage = stall_stage;
-  return silu ? launch_q<true>(maps, p, M, E, st, pdl) : launch_q<false>(maps, p, M, E, st, pdl);
+  // four stages when they fit with the tile table (E up to ~470), else three
+  if (q_smem_bytes<4>(E) <= QSMEM_MAX)
+    return silu ? launch_q<true, 4>(maps, p, M, E, st, pdl)
+                : launch_q<false, 4>(maps, p, M, E, st, pdl);
+  return silu ? launch_q<true, 3>(maps, p, M, E, st, pdl) : launch_q<false, 3>(maps, p, M, E, st, pdl);
 }
 
 }  // namespace moe

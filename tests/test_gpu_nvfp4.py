@@ -201,6 +201,8 @@ FP4_SHAPES = [
     # 0, 1 and 511 tokens (four 128-token chunks); one K chunk per tile.
     ([260, 0, 129, 511, 1, 40], 768, 1280),
     ([1000, 300], 512, 256),
+    # 480 experts: the tile table leaves room for three stages only
+    ([33 + (7 * e) % 29 for e in range(480)], 256, 512),
 ]
 
 
