@@ -53,8 +53,10 @@ __device__ __forceinline__ float exp32(float x) {
   return __fmul_rn(y, __int_as_float((n2 + 127) << 23));
 }
 
+// 1 / (1 + exp(-x)); the correctly rounded reciprocal is the correctly
+// rounded quotient 1 / y, so this is the IEEE division's result
 __device__ __forceinline__ float sigmoid32(float x) {
-  return __fdiv_rn(1.0f, __fadd_rn(1.0f, exp32(-x)));
+  return __frcp_rn(__fadd_rn(1.0f, exp32(-x)));
 }
 
 // Arg-max over the warp: larger value wins, equal values go to the lower
