@@ -279,6 +279,39 @@ def test_block_validation(lib):
     assert lib.moe_forward_block_host(*bad, P(0x100000), 1 << 40, None) == INVALID
 
 
+def test_nvfp4_validation(lib):
+    """NVFP4 needs K in whole 256-element chunks, N in 128-row tiles, positive
+    global scales and a stall stage >= 0 for the timeout test; refused before
+    any device work."""
+    g = lib.moe_grouped_gemm_nvfp4
+    args = lambda **kw: [kw.get("A", GOOD), GOOD, kw.get("ga", 0.5), GOOD, GOOD, GOOD, GOOD,
+                         64, kw.get("N", 256), kw.get("Kd", 512), kw.get("E", 4),
+                         kw.get("epi", 0), GOOD]
+    assert g(*args(Kd=128), None) == INVALID                 # K chunks of 256
+    assert g(*args(Kd=384), None) == INVALID
+    assert g(*args(N=192), None) == INVALID                  # 128-row tiles
+    assert g(*args(ga=0.0), None) == INVALID
+    assert g(*args(epi=2), None) == INVALID
+    assert g(*args(E=2048), None) == UNSUPPORTED
+    assert g(*args(A=ODD), None) == INVALID                  # 16-byte alignment
+    t = lib.moe_test_gemm_nvfp4_timeout
+    assert t(*args(), -1, None) == INVALID
+    assert t(*args(Kd=128), 1, None) == INVALID
+    a = lib.moe_act_quant_nvfp4
+    assert a(GOOD, 10, 48, 0.5, GOOD, GOOD, None) == INVALID   # I % 32
+    assert a(GOOD, 10, 64, 0.0, GOOD, GOOD, None) == INVALID   # g
+    assert a(None, 10, 64, 0.5, GOOD, GOOD, None) == INVALID
+    p = lib.moe_permute_quant_nvfp4
+    need = lib.moe_permute_workspace_size(16, 8, 2)
+    perm = lambda H, gs: p(GOOD, GOOD, 16, H, 8, 2, gs, GOOD, GOOD, GOOD, GOOD, P(0x100000),
+                           need, None)
+    assert perm(48, 0.5) == INVALID                           # H % 32
+    assert perm(256, 0.0) == INVALID                          # g
+    r = lib.moe_nvfp4_arrange_scales
+    assert r(GOOD, 4, 256, 128, 0, GOOD, None) == INVALID      # K chunks of 256
+    assert r(GOOD, 4, 192, 256, 0, GOOD, None) == INVALID      # 128-row tiles
+
+
 def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(moe, "_lib", None)
     monkeypatch.setattr(moe, "library_path", lambda: str(tmp_path / "missing.so"))
