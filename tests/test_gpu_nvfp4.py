@@ -239,7 +239,8 @@ def _layer_nvfp4(wl, d):
 
 def _check_nvfp4_layer(wl, seed, sample=False):
     d = synth.make_inputs(wl, seed=seed, device=DEV)
-    out = _layer_nvfp4(wl, d)(d["x"], d["logits"])
+    layer = _layer_nvfp4(wl, d)
+    out = layer(d["x"], d["logits"])
     torch.cuda.synchronize()
     assert moe.moe_device_status() == 0
     n = synth.to_numpy_inputs({k: d[k] for k in ("x", "logits", "bias", "s13", "g13", "s2",
@@ -257,6 +258,7 @@ def _check_nvfp4_layer(wl, seed, sample=False):
                                             wl.renormalize, wl.rsf, tokens=tokens,
                                             n_shared=wl.n_shared)
     assert_parity(bf16_np(out[torch.from_numpy(tokens).to(DEV)]), ref, wl.name)
+    return layer, d, out
 
 
 @pytest.mark.parametrize("seed", [0, 1, 2])
@@ -270,3 +272,19 @@ def test_forward_nvfp4_dsv3_decode_t128():
 
 def test_forward_nvfp4_dsv3_prefill_every_tile():
     _check_nvfp4_layer(synth.WORKLOADS["dsv3_prefill_t8192_nvfp4"], 0, sample=True)
+
+
+def test_forward_nvfp4_shared_expert_ragged_and_host_buffers():
+    """A shared expert (every token's weight-1 slot) on the NVFP4 path, every
+    token against the oracle; ~84 rows per expert, so both GEMMs take the
+    two-accumulator kernel, the shared expert's 300 rows in three token
+    chunks. The host-buffer entry point gives the same bytes."""
+    wl = synth.Workload("nvfp4_shared", 300, 512, 256, 24, 4, 2, 6, synth.SIGMOID, True, 2.5,
+                        "normal", n_shared=1, quant="nvfp4")
+    layer, d, out = _check_nvfp4_layer(wl, 3)
+    xh, lh = d["x"].cpu().pin_memory(), d["logits"].cpu().pin_memory()
+    oh = torch.empty_like(xh).pin_memory()
+    layer.forward_host(xh, lh, oh)
+    torch.cuda.synchronize()
+    assert moe.moe_device_status() == 0
+    assert torch.equal(oh.view(torch.int16), out.cpu().view(torch.int16))
